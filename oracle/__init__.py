@@ -1,0 +1,184 @@
+"""Python access to the CPU oracle — TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  It wraps ``blk_oracle.cpp`` (plain,
+single-threaded f64 C++; contract and readings in ``blk_oracle.h``) through
+ctypes, and shares no code with the GPU library.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = [os.path.join(_HERE, "blk_oracle.cpp"), os.path.join(_HERE, "blk_oracle.h")]
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+WEIGHT_FIELDS = ("ln1_g", "wq", "wk", "wv", "bq", "bk", "bv", "wo", "ln2_g",
+                 "w_gate", "w_up", "w_down")
+
+
+class OrcConfig(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int64), ("n_heads", ctypes.c_int64),
+                ("n_kv_heads", ctypes.c_int64), ("head_dim", ctypes.c_int64),
+                ("intermediate", ctypes.c_int64), ("rms_eps", ctypes.c_double),
+                ("rope_theta", ctypes.c_double), ("max_ctx", ctypes.c_int64),
+                ("has_qkv_bias", ctypes.c_int64)]
+
+
+class OrcWeights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in WEIGHT_FIELDS]
+
+
+def build(force: bool = False) -> str:
+    """Compile liboracle.so with g++: -O2, no FP contraction, no fast-math."""
+    newest = max(os.path.getmtime(s) for s in _SRC)
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= newest:
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    subprocess.check_call(["g++", "-O2", "-std=c++17", "-ffp-contract=off", "-fno-fast-math",
+                           "-fPIC", "-shared", _SRC[0], "-o", tmp])
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            vp, i64, dbl = ctypes.c_void_p, ctypes.c_int64, ctypes.c_double
+            lib.orc_half_to_double.argtypes = [ctypes.c_uint16]
+            lib.orc_half_to_double.restype = dbl
+            lib.orc_double_to_half.argtypes = [dbl]
+            lib.orc_double_to_half.restype = ctypes.c_uint16
+            lib.orc_rmsnorm.argtypes = [vp, vp, i64, dbl, vp]
+            lib.orc_rmsnorm.restype = None
+            lib.orc_rope.argtypes = [vp, i64, dbl, dbl]
+            lib.orc_rope.restype = None
+            lib.orc_linear.argtypes = [vp, vp, vp, i64, i64, vp]
+            lib.orc_linear.restype = None
+            lib.orc_silu.argtypes = [dbl]
+            lib.orc_silu.restype = dbl
+            lib.orc_attend.argtypes = [vp, vp, vp, i64, i64, i64, dbl, vp]
+            lib.orc_attend.restype = None
+            lib.orc_block_forward.argtypes = [ctypes.POINTER(OrcConfig), ctypes.POINTER(OrcWeights),
+                                              vp, vp, i64, i64, vp, vp, vp, vp, vp, i64, vp]
+            lib.orc_block_forward.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _f64(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _u16(a) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.float16:
+        return a.view(np.uint16)
+    if a.dtype != np.uint16:
+        raise TypeError(f"expected fp16 bits, got {a.dtype}")
+    return a
+
+
+# ---- component functions (for the pin tests) ------------------------------
+
+def half_to_double(bits: int) -> float:
+    return _load().orc_half_to_double(int(bits))
+
+
+def double_to_half(v: float) -> int:
+    return int(_load().orc_double_to_half(float(v)))
+
+
+def rmsnorm(x, g=None, eps: float = 1e-6) -> np.ndarray:
+    x = _f64(x)
+    g = None if g is None else _f64(g)
+    y = np.empty_like(x)
+    _load().orc_rmsnorm(x.ctypes.data, None if g is None else g.ctypes.data, x.size, eps, y.ctypes.data)
+    return y
+
+
+def rope(v, pos: float, theta: float = 10000.0) -> np.ndarray:
+    v = _f64(v).copy()
+    _load().orc_rope(v.ctypes.data, v.size, float(pos), float(theta))
+    return v
+
+
+def linear(W, x, b=None) -> np.ndarray:
+    W = _u16(W)
+    x = _f64(x)
+    n_out, n_in = W.shape
+    bb = None if b is None else _u16(b)
+    y = np.empty(n_out, dtype=np.float64)
+    _load().orc_linear(W.ctypes.data, None if bb is None else bb.ctypes.data, x.ctypes.data,
+                       n_out, n_in, y.ctypes.data)
+    return y
+
+
+def silu(z: float) -> float:
+    return _load().orc_silu(float(z))
+
+
+def attend(q, K, V, scale: float) -> np.ndarray:
+    """One query head against rows of K/V (fp16 [n_keys, D])."""
+    q = _f64(q)
+    K, V = _u16(K), _u16(V)
+    n, D = K.shape
+    o = np.empty(D, dtype=np.float64)
+    _load().orc_attend(q.ctypes.data, K.ctypes.data, V.ctypes.data, n, D, D, float(scale), o.ctypes.data)
+    return o
+
+
+# ---- the whole block --------------------------------------------------------
+
+def block_forward(shape, weights: dict, x, pos, L: int, k_cache, v_cache, max_ctx: int | None = None,
+                  rows=None):
+    """Run the block for T = len(x) new tokens on top of L history slots.
+
+    ``shape`` is a ``synth.BlockShape``.  ``k_cache``/``v_cache`` (fp16
+    [Hkv, max_ctx, D]) are updated in place.  Returns (out, k_new, v_new);
+    ``out`` covers ``rows`` (all rows when None)."""
+    lib = _load()
+    x = _u16(x)
+    T = x.shape[0]
+    pos = np.ascontiguousarray(pos, dtype=np.int64)
+    kc, vc = k_cache.view(np.uint16), v_cache.view(np.uint16)
+    if not (kc.flags.c_contiguous and vc.flags.c_contiguous):
+        raise ValueError("caches must be C-contiguous")
+    C = kc.shape[1] if max_ctx is None else max_ctx
+    cfg = OrcConfig(shape.hidden, shape.n_heads, shape.n_kv_heads, shape.head_dim, shape.intermediate,
+                    shape.rms_eps, shape.rope_theta, C, 1 if shape.has_qkv_bias else 0)
+    keep = {}
+    wts = OrcWeights()
+    for name in WEIGHT_FIELDS:
+        arr = weights.get(name)
+        if arr is None:
+            setattr(wts, name, None)
+            continue
+        arr = _u16(arr)
+        keep[name] = arr
+        setattr(wts, name, arr.ctypes.data)
+    Hkv, D, H = shape.n_kv_heads, shape.head_dim, shape.hidden
+    k_new = np.empty((T, Hkv, D), dtype=np.uint16)
+    v_new = np.empty((T, Hkv, D), dtype=np.uint16)
+    if rows is None:
+        rows_arr, n_rows = None, T
+    else:
+        rows_arr = np.ascontiguousarray(rows, dtype=np.int64)
+        n_rows = rows_arr.size
+    out = np.empty((n_rows, H), dtype=np.uint16)
+    rc = lib.orc_block_forward(ctypes.byref(cfg), ctypes.byref(wts), x.ctypes.data, pos.ctypes.data,
+                               T, L, kc.ctypes.data, vc.ctypes.data, k_new.ctypes.data,
+                               v_new.ctypes.data, None if rows_arr is None else rows_arr.ctypes.data,
+                               n_rows, out.ctypes.data)
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (rc={rc})")
+    return out.view(np.float16), k_new.view(np.float16), v_new.view(np.float16)

@@ -1,0 +1,106 @@
+/*
+ * CPU oracle for one Qwen2-style decoder block — TEST INFRASTRUCTURE ONLY.
+ *
+ * Only the tests, the smoke check and the benchmark's CPU-baseline leg use
+ * this library.  The GPU library never links, includes or calls it, and it
+ * never calls the GPU library: the two share no code.
+ *
+ * Everything is plain, single-threaded C++ with f64 arithmetic.  fp16 values
+ * (IEEE binary16, passed as raw uint16_t bit patterns) are decoded exactly to
+ * f64; the only roundings to fp16 are the K/V written to the cache and the
+ * block output, both round-to-nearest-even.
+ *
+ * Block definition followed (web page "An MLIR-based LLM compilation method",
+ * TopOp/TpuOp paper translation, §3.1 Listings 1 and 2; §4.1 for the three
+ * phases): RMSNorm -> q/k/v MatMul -> Gather cos/sin by position_ids -> Rope
+ * on q and k -> (Concat with history K/V) -> FAttention -> o MatMul + input ->
+ * RMSNorm -> MLP + residual -> return (o, k, v).
+ *
+ * Readings where the page is silent (each also listed in the design notes):
+ *   RMSNorm   y_i = x_i / sqrt(mean(x^2) + eps) * g_i
+ *   Rope      rotate_half pairs (i, i + D/2), angle = pos * theta^(-2i/D)
+ *   FAttention softmax(q.k / sqrt(D)) over slots 0 .. L+t (causal, slot order),
+ *             q head h reads kv head h / (Hq/Hkv)
+ *   MLP       SwiGLU: down(silu(gate(x)) * up(x)), silu(z) = z / (1 + e^-z)
+ *   biases    q/k/v only, and only when has_qkv_bias
+ *   returned K is after Rope, V as projected; both also land in cache slots
+ *   [L, L+T).
+ *
+ * Parity status of each function (what pins it without trusting itself) is
+ * given beside it; the full-size block output is pinned only through the
+ * component pins and the small-case brute-force checks ("parity unpinned by
+ * the pages": they print no worked numeric example).
+ */
+#ifndef BLK_ORACLE_H
+#define BLK_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct {
+  int64_t hidden, n_heads, n_kv_heads, head_dim, intermediate;
+  double rms_eps, rope_theta;
+  int64_t max_ctx;
+  int64_t has_qkv_bias;
+} orc_config;
+
+/* Host pointers to fp16 bit patterns, weights [out, in] row-major. */
+typedef struct {
+  const uint16_t *ln1_g, *wq, *wk, *wv, *bq, *bk, *bv, *wo, *ln2_g, *w_gate,
+      *w_up, *w_down;
+} orc_weights;
+
+/* binary16 <-> f64.  Pinned against numpy's float16 on every bit pattern. */
+double orc_half_to_double(uint16_t h);
+uint16_t orc_double_to_half(double v);
+
+/* y = x / sqrt(mean(x^2) + eps) * g over n elements (g may be NULL = ones).
+ * Pinned: constant vector closed form, scale invariance, output RMS. */
+void orc_rmsnorm(const double* x, const double* g, int64_t n, double eps,
+                 double* y);
+
+/* In-place rotate_half RoPE of one head of width D at position pos.
+ * Pinned: one-hot closed forms (pairing, sign, frequency), pos 0 identity,
+ * pair-norm preservation, rot(a) then rot(b) == rot(a+b). */
+void orc_rope(double* v, int64_t D, double pos, double theta);
+
+/* y[o] = sum_i W[o][i] * x[i] (+ b[o] when b != NULL); W fp16 [n_out, n_in].
+ * Pinned: one-hot input selects a weight column; zero weights give the bias. */
+void orc_linear(const uint16_t* W, const uint16_t* b, const double* x,
+                int64_t n_out, int64_t n_in, double* y);
+
+/* silu(z) = z / (1 + exp(-z)).  Pinned: silu(0)=0, limits, odd-part identity. */
+double orc_silu(double z);
+
+/* One query head against n_keys cache rows (row stride `stride` elements):
+ * o = sum_j softmax_j(q . K_j * scale) V_j, with the maximum subtracted.
+ * Pinned: one key -> V, identical keys -> mean of V, two-key closed form,
+ * brute-force dense masked softmax on small cases. */
+void orc_attend(const double* q, const uint16_t* K, const uint16_t* V,
+                int64_t n_keys, int64_t D, int64_t stride, double scale,
+                double* o);
+
+/* The whole block for T new tokens on top of L history slots.
+ *   x        fp16 [T, hidden]
+ *   pos      int64 [T] position_ids (drive RoPE only)
+ *   k_cache, v_cache  fp16 [n_kv_heads, max_ctx, head_dim], slots [0, L)
+ *            read, slots [L, L+T) written, others untouched
+ *   k_new, v_new      fp16 [T, n_kv_heads, head_dim] (may be NULL)
+ *   rows     NULL: every row, out is [T, hidden]; else n_rows row indices,
+ *            out is [n_rows, hidden] (K/V are still produced for all rows)
+ * Returns 0, or -1 on a bad argument (T <= 0, L < 0, L + T > max_ctx,
+ * n_heads % n_kv_heads != 0, odd head_dim, row index out of range).
+ * prefill is L = 0, prefill_kv is L > 0, decode is T = 1. */
+int orc_block_forward(const orc_config* cfg, const orc_weights* w,
+                      const uint16_t* x, const int64_t* pos, int64_t T,
+                      int64_t L, uint16_t* k_cache, uint16_t* v_cache,
+                      uint16_t* k_new, uint16_t* v_new, const int64_t* rows,
+                      int64_t n_rows, uint16_t* out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

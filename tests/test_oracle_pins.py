@@ -1,0 +1,380 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+Each test names the property it checks.  None of them re-types an oracle
+formula and compares it with itself: they use closed forms, invariants,
+special cases, the page's printed constants, an independent fp16 conversion
+(numpy) and a brute-force matrix restatement on small cases.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from brute_block import block as brute_block
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------- fp16 codec
+
+def test_half_decode_every_pattern_matches_numpy():
+    bits = np.arange(65536, dtype=np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    ours = np.array([oracle.half_to_double(b) for b in bits])
+    finite = np.isfinite(ref)
+    assert np.array_equal(ours[finite], ref[finite])
+    assert np.array_equal(np.isnan(ours), np.isnan(ref))
+    assert np.array_equal(ours[np.isinf(ref)], ref[np.isinf(ref)])
+
+
+def test_half_encode_matches_numpy_rne():
+    rng = np.random.default_rng(1)
+    vals = np.concatenate([
+        rng.standard_normal(20000), rng.standard_normal(5000) * 1e-5, rng.standard_normal(5000) * 2e4,
+        (np.arange(1, 2049) + 0.5) * 2.0 ** -10, (np.arange(1, 1024) + 0.5) * 2.0 ** -24,
+        [0.0, -0.0, 65504.0, 65519.999, 65520.0, 7e4, 2.0 ** -25, 1.5 * 2.0 ** -25, 2.0 ** -14 * (1 - 2.0 ** -12)],
+    ])
+    with np.errstate(over="ignore"):
+        ref = vals.astype(np.float16).view(np.uint16)
+    ours = np.array([oracle.double_to_half(v) for v in vals], dtype=np.uint16)
+    assert np.array_equal(ours, ref)
+
+
+# ----------------------------------------------------------------- RMSNorm
+
+def test_rmsnorm_constant_vector_closed_form():
+    c, n, eps = 3.0, 64, 1e-6
+    y = oracle.rmsnorm(np.full(n, c), eps=eps)
+    assert np.allclose(y, c / math.sqrt(c * c + eps), rtol=0, atol=1e-15)
+
+
+def test_rmsnorm_scale_invariance_and_unit_rms():
+    x = synth.normal_f64(0, 100, 0, 1536)
+    y1 = oracle.rmsnorm(x, eps=1e-6)
+    y2 = oracle.rmsnorm(1000.0 * x, eps=1e-6)
+    assert np.allclose(y1, y2, rtol=1e-6, atol=0)
+    ms = np.mean(x * x)
+    assert math.isclose(math.sqrt(np.mean(y1 * y1)), math.sqrt(ms / (ms + 1e-6)), rel_tol=1e-12)
+
+
+def test_rmsnorm_gain_is_elementwise():
+    x = synth.normal_f64(0, 101, 0, 32)
+    g = np.arange(1, 33, dtype=np.float64)
+    assert np.allclose(oracle.rmsnorm(x, g), oracle.rmsnorm(x) * g, rtol=1e-15, atol=0)
+
+
+# -------------------------------------------------------------------- RoPE
+
+def test_rope_position_zero_is_identity():
+    # ds4.c study notes, part 4 'RoPE rotation': pos = 0 gives angle 0, no rotation
+    v = synth.normal_f64(0, 102, 0, 128)
+    assert np.array_equal(oracle.rope(v, 0.0), v)
+
+
+def test_rope_one_hot_pins_pairing_sign_and_frequency():
+    D, theta, p = 8, 10000.0, 3.0
+    for i in range(D // 2):
+        w = theta ** (-2.0 * i / D)
+        e = np.zeros(D)
+        e[i] = 1.0
+        out = oracle.rope(e, p, theta)
+        want = np.zeros(D)
+        want[i] = math.cos(p * w)            # first half keeps cos
+        want[i + D // 2] = math.sin(p * w)   # partner at i + D/2 gets +sin
+        assert np.allclose(out, want, atol=1e-15), i
+        e = np.zeros(D)
+        e[i + D // 2] = 1.0
+        out = oracle.rope(e, p, theta)
+        want = np.zeros(D)
+        want[i] = -math.sin(p * w)
+        want[i + D // 2] = math.cos(p * w)
+        assert np.allclose(out, want, atol=1e-15), i
+
+
+def test_rope_preserves_pair_norms_and_composes():
+    D = 128
+    v = synth.normal_f64(0, 103, 0, D)
+    a, b = 123.0, 4567.0
+    r = oracle.rope(v, a)
+    n0 = v[: D // 2] ** 2 + v[D // 2:] ** 2
+    n1 = r[: D // 2] ** 2 + r[D // 2:] ** 2
+    assert np.allclose(n0, n1, rtol=1e-12)
+    assert np.allclose(oracle.rope(r, b), oracle.rope(v, a + b), atol=1e-9)
+
+
+def test_rope_scores_depend_on_relative_position_only():
+    D = 64
+    q = synth.normal_f64(0, 104, 0, D)
+    k = synth.normal_f64(0, 105, 0, D)
+    s1 = oracle.rope(q, 50.0) @ oracle.rope(k, 20.0)
+    s2 = oracle.rope(q, 1030.0) @ oracle.rope(k, 1000.0)
+    assert math.isclose(s1, s2, rel_tol=1e-9, abs_tol=1e-9)
+
+
+# ------------------------------------------------------------ linear / silu
+
+def test_linear_one_hot_selects_a_column_and_bias_adds():
+    W = synth.normal_f16(0, 106, (24, 40))
+    for j in (0, 7, 39):
+        e = np.zeros(40)
+        e[j] = 1.0
+        assert np.array_equal(oracle.linear(W, e), W[:, j].astype(np.float64))
+    b = synth.normal_f16(0, 107, (24,))
+    y = oracle.linear(np.zeros((24, 40), np.float16), np.ones(40), b)
+    assert np.array_equal(y, b.astype(np.float64))
+
+
+def test_silu_special_values():
+    assert oracle.silu(0.0) == 0.0
+    assert math.isclose(oracle.silu(40.0), 40.0, rel_tol=1e-15)
+    assert abs(oracle.silu(-40.0)) < 1e-15
+    for z in (0.3, 1.7, 5.0):
+        # silu(z) - silu(-z) = z for every z
+        assert math.isclose(oracle.silu(z) - oracle.silu(-z), z, rel_tol=1e-14)
+        assert math.isclose(oracle.silu(z), z * (0.5 + 0.5 * math.tanh(z / 2)), rel_tol=1e-14)
+
+
+# --------------------------------------------------------------- attention
+
+def test_attend_single_key_returns_v():
+    # ds4.c study notes, part 4 'first token': attention over itself only
+    D = 64
+    q = synth.normal_f64(0, 108, 0, D)
+    K = synth.normal_f16(0, 109, (1, D))
+    V = synth.normal_f16(0, 110, (1, D))
+    assert np.array_equal(oracle.attend(q, K, V, 1 / 8), V[0].astype(np.float64))
+
+
+def test_attend_identical_keys_gives_mean_of_v():
+    D, n = 128, 37
+    q = synth.normal_f64(0, 111, 0, D)
+    K = np.tile(synth.normal_f16(0, 112, (1, D)), (n, 1))
+    V = synth.normal_f16(0, 113, (n, D))
+    o = oracle.attend(q, K, V, 1 / math.sqrt(D))
+    assert np.allclose(o, V.astype(np.float64).mean(axis=0), rtol=1e-13, atol=1e-15)
+
+
+def test_attend_two_key_closed_form_pins_scale():
+    D, c = 64, 5.0
+    q = np.zeros(D)
+    q[0] = c
+    K = np.zeros((2, D), np.float16)
+    K[0, 0] = 1.0
+    V = np.zeros((2, D), np.float16)
+    V[0, :] = 2.0
+    V[1, :] = -1.0
+    o = oracle.attend(q, K, V, 1 / math.sqrt(D))
+    e = math.exp(c / math.sqrt(D))
+    assert np.allclose(o, (2.0 * e - 1.0) / (e + 1.0), rtol=1e-14)
+
+
+def test_attend_split_merge_equals_one_pass():
+    # log-sum-exp merge of two halves equals attention over the whole range
+    D, n, a = 64, 50, 19
+    q = synth.normal_f64(0, 114, 0, D)
+    K = synth.normal_f16(0, 115, (n, D))
+    V = synth.normal_f16(0, 116, (n, D))
+    s = 1 / 8
+
+    def stats(Kp):
+        sc = (Kp.astype(np.float64) @ q) * s
+        m = sc.max()
+        return m, np.exp(sc - m).sum()
+
+    o1, o2 = oracle.attend(q, K[:a], V[:a], s), oracle.attend(q, K[a:], V[a:], s)
+    (m1, l1), (m2, l2) = stats(K[:a]), stats(K[a:])
+    m = max(m1, m2)
+    w1, w2 = l1 * math.exp(m1 - m), l2 * math.exp(m2 - m)
+    merged = (w1 * o1 + w2 * o2) / (w1 + w2)
+    assert np.allclose(merged, oracle.attend(q, K, V, s), rtol=1e-12, atol=1e-14)
+
+
+# ------------------------------------------------------------ whole block
+
+def _tiny_case(T, L, max_ctx=64, seed=0, sentinel=-7.0):
+    s = synth.TINY
+    w = synth.block_weights(s, seed=seed)
+    x = synth.hidden_input(s, T, seed=seed)
+    kc, vc = synth.kv_history(s, max_ctx, L, seed=seed, sentinel=sentinel)
+    return s, w, x, synth.positions(L, T), kc, vc
+
+
+@pytest.mark.parametrize("T,L", [(16, 0), (4, 16), (1, 20), (7, 9)])
+def test_block_matches_bruteforce_restatement(T, L):
+    s, w, x, pos, kc, vc = _tiny_case(T, L)
+    bo, bk, bv = brute_block(s, w, x, pos, L, kc.copy(), vc.copy())
+    out, kn, vn = oracle.block_forward(s, w, x, pos, L, kc, vc)
+    # K/V are rounded from f64 in both; allow a one-ulp difference where the
+    # two summation orders straddle a rounding boundary
+    assert np.max(np.abs(kn.astype(np.float64) - bk.astype(np.float64))) <= 2.0 ** -10
+    assert np.max(np.abs(vn.astype(np.float64) - bv.astype(np.float64))) <= 2.0 ** -10
+    d = np.abs(out.astype(np.float64) - bo.astype(np.float64))
+    assert d.max() <= 2.0 ** -8          # at most one fp16 ulp at |out| < 8
+    assert np.mean(out.view(np.uint16) == bo.view(np.uint16)) > 0.99
+
+
+def test_block_cache_placement_and_untouched_slots():
+    T, L, C = 5, 11, 40
+    s, w, x, pos, kc, vc = _tiny_case(T, L, max_ctx=C)
+    k0, v0 = kc.copy(), vc.copy()
+    out, kn, vn = oracle.block_forward(s, w, x, pos, L, kc, vc)
+    assert np.array_equal(kc[:, L:L + T, :].view(np.uint16), kn.transpose(1, 0, 2).view(np.uint16))
+    assert np.array_equal(vc[:, L:L + T, :].view(np.uint16), vn.transpose(1, 0, 2).view(np.uint16))
+    for arr, ref in ((kc, k0), (vc, v0)):
+        assert np.array_equal(arr[:, :L].view(np.uint16), ref[:, :L].view(np.uint16))
+        assert np.array_equal(arr[:, L + T:].view(np.uint16), ref[:, L + T:].view(np.uint16))
+
+
+def test_block_residual_passthrough_with_zero_output_weights():
+    s, w, x, pos, kc, vc = _tiny_case(6, 3)
+    w = dict(w, wo=np.zeros_like(w["wo"]), w_down=np.zeros_like(w["w_down"]))
+    out, _, _ = oracle.block_forward(s, w, x, pos, 3, kc, vc)
+    assert np.array_equal(out.view(np.uint16), x.view(np.uint16))
+
+
+def test_block_kv_from_bias_only():
+    # zero K/V weights: k = RoPE(bk) at each position, v = bv
+    s = synth.BlockShape(64, 2, 1, 32, 48, True)
+    w = synth.block_weights(s, seed=3)
+    w["wk"] = np.zeros_like(w["wk"])
+    w["wv"] = np.zeros_like(w["wv"])
+    T = 3
+    x = synth.hidden_input(s, T, seed=3)
+    kc, vc = synth.kv_history(s, 8, 0)
+    pos = np.array([0, 5, 9], np.int64)
+    _, kn, vn = oracle.block_forward(s, w, x, pos, 0, kc, vc)
+    bk = w["bk"].astype(np.float64)
+    D = 32
+    for t, p in enumerate(pos):
+        c = np.cos(p * 10000.0 ** (-np.arange(0, D, 2) / D))
+        sn = np.sin(p * 10000.0 ** (-np.arange(0, D, 2) / D))
+        want = np.concatenate([bk[:16] * c - bk[16:] * sn, bk[16:] * c + bk[:16] * sn])
+        assert np.array_equal(kn[t, 0].view(np.uint16), want.astype(np.float16).view(np.uint16)) or \
+            np.max(np.abs(kn[t, 0].astype(np.float64) - want)) <= 2.0 ** -11
+        assert np.array_equal(vn[t, 0].view(np.uint16), w["bv"].view(np.uint16))
+
+
+def test_block_gqa_mapping_and_output_orientation():
+    # V of kv head g is the constant g + 1, so every query head's attention
+    # output is the constant of its kv head; Wo is a permutation matrix, Wd = 0.
+    s = synth.BlockShape(256, 4, 2, 64, 32, False)
+    w = synth.block_weights(s, seed=5)
+    w["wv"] = np.zeros_like(w["wv"])
+    T, L, C = 2, 6, 16
+    x = synth.hidden_input(s, T, seed=5)
+    kc, vc = synth.kv_history(s, C, L, seed=5)
+    vc[0, :L] = 1.0
+    vc[1, :L] = 2.0
+    w["w_down"] = np.zeros_like(w["w_down"])
+    perm = (np.arange(256) * 5 + 3) % 256          # not an involution
+    Wo = np.zeros((256, 256), np.float16)
+    Wo[np.arange(256), perm] = 1.0                 # out[o] = attn[perm[o]]
+    w["wo"] = Wo
+    # new rows contribute v = 0, so restrict to keys where that is harmless:
+    # expected attn = (sum over history of const * p) = const * (mass on history)
+    out, _, _ = oracle.block_forward(s, w, x, synth.positions(L, T), L, kc, vc)
+    # recompute history mass with the component functions is circular; instead
+    # check the structure: within each kv group the output of Wo is constant per
+    # group and group 1 is exactly twice group 0 (same softmax mass per head is
+    # not implied, so compare ratios per query head)
+    attn_est = out.astype(np.float64) - x.astype(np.float64)   # [T, 256] = attn[perm]
+    attn = np.empty_like(attn_est)
+    attn[:, perm] = attn_est
+    heads = attn.reshape(T, 4, 64)
+    # inside one head all 64 dims equal (V is constant across d)
+    assert np.allclose(heads, heads[..., :1], atol=2.0 ** -9)
+    # heads 0,1 (kv 0) see constant 1, heads 2,3 (kv 1) see 2; the new rows
+    # add a little mass on v = 0, so values are in (0, c]
+    assert np.all(heads[:, 0:2] <= 1.0 + 2 ** -9) and np.all(heads[:, 0:2] > 0.5)
+    assert np.all(heads[:, 2:4] <= 2.0 + 2 ** -8) and np.all(heads[:, 2:4] > 1.0)
+
+
+def test_block_causality():
+    T, L = 8, 4
+    s, w, x, pos, kc, vc = _tiny_case(T, L)
+    out1, _, _ = oracle.block_forward(s, w, x, pos, L, kc.copy(), vc.copy())
+    x2 = x.copy()
+    x2[5:] = synth.hidden_input(s, 3, seed=9)
+    out2, _, _ = oracle.block_forward(s, w, x2, pos, L, kc.copy(), vc.copy())
+    assert np.array_equal(out1[:5].view(np.uint16), out2[:5].view(np.uint16))
+    assert not np.array_equal(out1[5:].view(np.uint16), out2[5:].view(np.uint16))
+
+
+def test_block_position_shift_invariance():
+    T = 12
+    s, w, x, pos, kc, vc = _tiny_case(T, 0)
+    out1, k1, _ = oracle.block_forward(s, w, x, pos, 0, kc.copy(), vc.copy())
+    out2, k2, _ = oracle.block_forward(s, w, x, pos + 1000, 0, kc.copy(), vc.copy())
+    assert not np.array_equal(k1.view(np.uint16), k2.view(np.uint16))
+    # only relative positions reach the scores; K is rounded after rotation,
+    # so allow the resulting tiny difference
+    assert np.max(np.abs(out1.astype(np.float64) - out2.astype(np.float64))) <= 2.0 ** -7
+
+
+def test_block_rows_subset_equals_full():
+    s, w, x, pos, kc, vc = _tiny_case(9, 5)
+    full, kf, vf = oracle.block_forward(s, w, x, pos, 5, kc.copy(), vc.copy())
+    rows = [8, 0, 4]
+    sub, ks, vs = oracle.block_forward(s, w, x, pos, 5, kc.copy(), vc.copy(), rows=rows)
+    assert np.array_equal(sub.view(np.uint16), full[rows].view(np.uint16))
+    assert np.array_equal(ks.view(np.uint16), kf.view(np.uint16))
+
+
+def test_phase_chain_identities_bit_exact():
+    """prefill(T) == prefill(T-k) -> prefill_kv(k) == prefill(T-1) -> decode
+    (the three-phase split of the TopOp/TpuOp paper, section 4.1)."""
+    T, C = 16, 32
+    s, w, x, pos, _, _ = _tiny_case(T, 0, max_ctx=C)
+    kc0, vc0 = synth.kv_history(s, C, 0)
+    full, kf, vf = oracle.block_forward(s, w, x, pos, 0, kc0, vc0)
+
+    for k in (1, 4, 7):
+        kc, vc = synth.kv_history(s, C, 0)
+        o1, _, _ = oracle.block_forward(s, w, x[:T - k], pos[:T - k], 0, kc, vc)
+        o2, _, _ = oracle.block_forward(s, w, x[T - k:], pos[T - k:], T - k, kc, vc)
+        assert np.array_equal(np.concatenate([o1, o2]).view(np.uint16), full.view(np.uint16))
+        assert np.array_equal(kc.view(np.uint16), kc0.view(np.uint16))
+        assert np.array_equal(vc.view(np.uint16), vc0.view(np.uint16))
+
+    kc, vc = synth.kv_history(s, C, 0)
+    outs = [oracle.block_forward(s, w, x[:T - 4], pos[:T - 4], 0, kc, vc)[0]]
+    for t in range(T - 4, T):    # four decode steps
+        outs.append(oracle.block_forward(s, w, x[t:t + 1], pos[t:t + 1], t, kc, vc)[0])
+    assert np.array_equal(np.concatenate(outs).view(np.uint16), full.view(np.uint16))
+
+
+def test_oracle_rejects_bad_arguments():
+    s, w, x, pos, kc, vc = _tiny_case(4, 0, max_ctx=8)
+    with pytest.raises(ValueError):
+        oracle.block_forward(s, w, x, pos, 6, kc, vc)          # 6 + 4 > max_ctx
+    with pytest.raises(ValueError):
+        oracle.block_forward(s, w, x, pos, 0, kc, vc, rows=[4])
+
+
+# ------------------------------------------------------ page constants
+
+def test_page_param_count_pins_the_1p5b_shape():
+    """The packed-parameter count printed by the buddy-mlir runtime equals the
+    element count of 28 blocks of the 1.5B shape (with q/k/v bias), the
+    embedding, final norm, an untied LM head and a head_dim/2 RoPE buffer."""
+    c = json.load(open(os.path.join(GOLDEN, "page_constants.json")))
+    s = synth.QWEN2_1P5B
+    assert s.head_dim == c["head_dim_named_HiddenSize"]
+    assert s.n_kv_heads == c["kv_heads_named_HeadNum"]
+    per_layer = sum(int(np.prod(v)) for v in synth.weight_shapes(s).values())
+    total = s.n_layers * per_layer + 2 * c["MaxVocabSize"] * s.hidden + s.hidden + s.head_dim // 2
+    assert total == c["ParamsSize"]
+    # K and V per layer make the 56 cache fields of the prefill return struct
+    assert 2 * s.n_layers == c["kv_fields_in_prefill_returns"]
+    assert c["kv_cache_shape"][1:] == [s.n_kv_heads, c["MaxTokenLength"], s.head_dim]
+
+
+def test_page_gqa_example_shape():
+    c = json.load(open(os.path.join(GOLDEN, "gqa_example_shape.json")))
+    s = synth.GQA_4096
+    assert (s.n_layers, s.hidden, s.n_kv_heads, s.head_dim) == (
+        c["num_layers"], c["hidden_size"], c["kv_head"], c["head_dim"])
