@@ -1,0 +1,461 @@
+#!/usr/bin/env python
+"""Throughput of the GB300 decoder-block library on synthetic seeded inputs.
+
+Headline (one JSON line on rank 0): prefill tokens/s of one 1.5B-shaped layer
+(hidden 1536, 12 q / 2 kv heads, head_dim 128, intermediate 8960, QKV bias)
+at the static prefill shape [1, 1024], position_ids 0..1023.  A step is one
+blk_prefill call (the whole block: RMSNorm, QKV + bias, RoPE + KV append,
+causal GQA attention, o_proj + residual, RMSNorm, SwiGLU MLP + residual).
+The L2 is flushed (a 256 MB write) before every timed step, because one
+layer's weights (94 MB) fit in the 129 MB L2.
+
+Also reported: decode of the 28-layer 1.5B stack at cache lengths 1024,
+4096, 16384 and 32768 (one CUDA graph per step, KV appended in place;
+2.6 GB of weights per step, so no flush is needed), µs/step and the
+fraction of the HBM roofline (weight + KV bytes over measured copy
+bandwidth).
+
+--impl reference times the CPU oracle (single-threaded f64) on a bounded
+sample of the same prefill workload.  Under torchrun (N > 1) each rank runs
+an independent replica (no collective on the data path); rank 0 prints the
+whole-job numbers.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "prefill tok/s (1.5B-shaped layer, [1,1024]) + decode us/step vs ctx (28 layers)"
+UNIT = "tok/s"
+DECODE_CTX = (1024, 4096, 16384, 32768)
+PREFILL_T = 1024
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-decode", action="store_true", help="skip the decode table")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--decode-ctx", type=str, default=",".join(map(str, DECODE_CTX)))
+    return ap.parse_args()
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.3)
+        self.proc.terminate()
+        self.proc.wait()
+        self.file.flush()
+        rows = [r.split(",") for r in open(self.file.name).read().strip().splitlines() if r.strip()]
+        os.unlink(self.file.name)
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in rows:
+            r = [c.strip() for c in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ helpers
+
+def dist_init(args):
+    import torch
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if (args.impl == "ours" and torch.cuda.is_available()) else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available() and args.impl == "ours":
+        torch.cuda.set_device(local)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_max(v, ws):
+    if ws == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(v)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def prefill_flops(s, T, L=0):
+    H, Hq, Hkv, D, I = s.hidden, s.n_heads, s.n_kv_heads, s.head_dim, s.intermediate
+    gemm = {
+        "gemm_qkv": 2.0 * T * (Hq + 2 * Hkv) * D * H,
+        "gemm_o": 2.0 * T * H * Hq * D,
+        "gemm_gateup": 2.0 * T * 2 * I * H,
+        "gemm_down": 2.0 * T * H * I,
+    }
+    pairs = sum(L + t + 1 for t in range(T))          # (query, key) pairs per head
+    attn = 4.0 * D * Hq * pairs                       # QK^T and PV, 2 flops per MAC
+    return gemm, attn
+
+
+def decode_bytes(s, L, n_layers):
+    H, Hq, Hkv, D, I = s.hidden, s.n_heads, s.n_kv_heads, s.head_dim, s.intermediate
+    w = 2 * ((Hq + 2 * Hkv) * D * H + H * Hq * D + 3 * I * H + 2 * H)
+    if s.has_qkv_bias:
+        w += 2 * (Hq + 2 * Hkv) * D
+    kv = 2 * Hkv * D * 2 * (L + 1)
+    return n_layers * (w + kv), n_layers * w
+
+
+# ------------------------------------------------------------- CPU oracle
+
+_ORACLE_INPUTS = {}
+
+
+def oracle_prefill_sample(n_rows: int, rotate: int = 0):
+    """Times the oracle on the prefill workload: K/V of all 1024 rows plus the
+    full block output of n_rows evenly spaced rows; returns (tok/s
+    extrapolated to all rows, seconds spent, sample description)."""
+    import oracle
+    import synth
+    s = synth.QWEN2_1P5B
+    if not _ORACLE_INPUTS:
+        oracle.build()
+        _ORACLE_INPUTS.update(w=synth.block_weights(s, seed=0),
+                              x=synth.hidden_input(s, PREFILL_T, seed=0),
+                              pos=synth.positions(0, PREFILL_T))
+    w, x, pos = _ORACLE_INPUTS["w"], _ORACLE_INPUTS["x"], _ORACLE_INPUTS["pos"]
+    kc, vc = synth.kv_history(s, PREFILL_T, 0)
+    t0 = time.perf_counter()
+    oracle.block_forward(s, w, x, pos, 0, kc, vc, rows=[0])
+    t_kv = time.perf_counter() - t0               # all K/V rows + one output row
+    spent = t_kv
+    step = PREFILL_T // n_rows
+    rows = [(i * step + rotate) % PREFILL_T for i in range(n_rows)]
+    kc2, vc2 = synth.kv_history(s, PREFILL_T, 0)
+    t0 = time.perf_counter()
+    oracle.block_forward(s, w, x, pos, 0, kc2, vc2, rows=rows)
+    t2 = time.perf_counter() - t0
+    spent += t2
+    t_rows = max(t2 - t_kv, 1e-9)                 # cost of the sampled output rows
+    t_full = t_kv + t_rows * PREFILL_T / n_rows
+    desc = (f"oracle on the 1.5B-shaped layer, prefill [1,1024]: K/V for all 1024 rows + full "
+            f"output of {n_rows} evenly spaced rows, scaled to 1024 rows; single-threaded")
+    return PREFILL_T / t_full, spent, desc
+
+
+# ------------------------------------------------------------------ ours
+
+def bench_ours(args, ws, rank, local):
+    import torch
+    import decode_qwen2_block_gb300 as blk
+    from decode_qwen2_block_gb300 import build as gpu_build
+    from decode_qwen2_block_gb300.stack import LayerStack
+    import synth
+
+    gpu_build.build()
+    peaks = load_peaks()
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    s = synth.QWEN2_1P5B
+    K, W = args.steps, args.warmup
+
+    # ---------------- prefill, one layer, [1, 1024] ----------------
+    T = PREFILL_T
+    w_np = synth.block_weights(s, layer=0, seed=0)
+    w_dev = {k: torch.from_numpy(v).to(dev) for k, v in w_np.items()}
+    x_np = synth.hidden_input(s, T, seed=0)
+    x = torch.from_numpy(x_np).to(dev)
+    pos = torch.from_numpy(synth.positions(0, T)).to(dev)
+    block = blk.Block(s, T)
+    wts = blk.Block.weights(w_dev)
+    kc = torch.zeros((s.n_kv_heads, T, s.head_dim), dtype=torch.float16, device=dev)
+    vc = torch.zeros_like(kc)
+    out = torch.empty((T, s.hidden), dtype=torch.float16, device=dev)
+    kn = torch.empty((T, s.n_kv_heads, s.head_dim), dtype=torch.float16, device=dev)
+    vn = torch.empty_like(kn)
+    wsb = torch.empty(block.workspace_bytes(T), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def prefill_step():
+        block.prefill(wts, x, pos, kc, vc, out, wsb, kn, vn, stream=stream)
+
+    for _ in range(W):
+        flush.zero_()
+        prefill_step()
+    torch.cuda.synchronize()
+    block.check()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    barrier(ws)
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.zero_()
+        evs[i][0].record(stream)
+        prefill_step()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    total_ms = reduce_max(sum(step_ms), ws)
+
+    # e2e: host (pinned) inputs -> device -> block -> host outputs, every step
+    x_h = torch.from_numpy(x_np).pin_memory()
+    pos_h = torch.from_numpy(synth.positions(0, T)).pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    kn_h = torch.empty(kn.shape, dtype=kn.dtype).pin_memory()
+    vn_h = torch.empty(vn.shape, dtype=vn.dtype).pin_memory()
+    x_e, pos_e = torch.empty_like(x), torch.empty_like(pos)
+
+    def e2e_step():
+        x_e.copy_(x_h, non_blocking=True)
+        pos_e.copy_(pos_h, non_blocking=True)
+        block.prefill(wts, x_e, pos_e, kc, vc, out, wsb, kn, vn, stream=stream)
+        out_h.copy_(out, non_blocking=True)
+        kn_h.copy_(kn, non_blocking=True)
+        vn_h.copy_(vn, non_blocking=True)
+
+    for _ in range(W):
+        flush.zero_()
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)]
+    barrier(ws)
+    for i in range(K):
+        flush.zero_()
+        e2e_evs[i][0].record(stream)
+        e2e_step()
+        e2e_evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    e2e_ms = reduce_max(sum(a.elapsed_time(b) for a, b in e2e_evs), ws)
+    h2d = x_h.numel() * 2 + pos_h.numel() * 8
+    d2h = (out_h.numel() + kn_h.numel() + vn_h.numel()) * 2
+
+    # per-kernel durations (events around each kernel; separate pass)
+    block.timing(True)
+    for i in range(K):
+        flush.zero_()
+        prefill_step()
+        block.timing_collect(stream)
+    block.timing(False)
+    table = block.timing_table()
+    launches_per_step = sum(n for _, n in table.values()) // K
+    gemm_flops, attn_flops = prefill_flops(s, T)
+    kernels = {}
+    for name, (ms, n) in table.items():
+        kernels[name] = {"avg_us": 1e3 * ms / n, "launches_per_step": n // K,
+                         "share": ms / sum(v[0] for v in table.values())}
+    dom = max(table, key=lambda k: table[k][0])
+    if dom in gemm_flops or dom == "attn_prefill":
+        work = gemm_flops[dom] if dom in gemm_flops else attn_flops
+        per_launch = table[dom][0] / table[dom][1] * (table[dom][1] // K)   # ms per step
+        achieved = work / (per_launch * 1e-3) / 1e12
+        roof = {"kernel": dom, "bound": "tensor", "achieved": achieved,
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"], "traffic": None,
+                "peak_source": peaks["source"] + " bf16 dense burst (fp16 runs at the bf16 rate)"}
+    else:
+        roof = {"kernel": dom, "bound": "hbm", "achieved": None, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": None, "traffic": None}
+    gemm_ms = sum(table[k][0] for k in gemm_flops if k in table) / K
+    gemm_frac = sum(gemm_flops.values()) / (gemm_ms * 1e-3) / 1e12 / peaks["bf16_tflops"]
+
+    result = {
+        "metric": METRIC, "value": ws * T * K / (total_ms * 1e-3), "unit": UNIT,
+        "n_gpus": ws, "steps": K, "warmup": W, "ms_per_step": total_ms / K,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic (seeded N(0,0.02) weights, N(0,1) activations)",
+        "config": {"workload": "qwen2-1.5B-shaped decoder layer, prefill [1,1024], pos 0..1023",
+                   "hidden": 1536, "heads": 12, "kv_heads": 2, "head_dim": 128,
+                   "intermediate": 8960, "qkv_bias": True, "layers": 1, "seq_len": T,
+                   "l2": "flushed (256 MB write) before every timed step",
+                   "parallelism": f"replicas x{ws}"},
+        "e2e": {"value": ws * T * K / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * K,
+        "roofline": roof,
+        "prefill_gemm_frac_of_tensor_peak": gemm_frac,
+        "kernels": kernels,
+    }
+
+    # ---------------- decode, 28 layers ----------------
+    if not args.no_decode:
+        result["decode"] = bench_decode(args, s, dev, stream, peaks, ws)
+    result["clocks"] = clocks.stop()
+    return result
+
+
+def bench_decode(args, s, dev, stream, peaks, ws):
+    import torch
+    import synth
+    from decode_qwen2_block_gb300.stack import LayerStack
+    K, W = args.steps, args.warmup
+    ctxs = [int(c) for c in args.decode_ctx.split(",") if c]
+    n = s.n_layers
+    C = max(ctxs) + W + K + 8
+    Lmax = max(ctxs)
+    wl = []
+    for l in range(n):
+        wnp = synth.block_weights(s, layer=l, seed=0)
+        wl.append({k: torch.from_numpy(v).to(dev) for k, v in wnp.items()})
+    caches = []
+    for l in range(n):
+        k, v = synth.kv_history(s, C, Lmax, layer=l, seed=0)
+        caches.append((torch.from_numpy(k).to(dev), torch.from_numpy(v).to(dev)))
+    st = LayerStack(s, wl, C, 1, caches=caches, chain=True)
+    xs = [torch.from_numpy(synth.hidden_input(s, 1, seed=0, stream_offset=i + 1)).to(dev)
+          for i in range(W + K)]
+    out = {}
+    for L in ctxs:
+        poss = [torch.tensor([L + i], dtype=torch.int64, device=dev) for i in range(W + K)]
+        graphs = [st.capture("decode", xs[i], poss[i], L + i, key=("decode", L, i))[0]
+                  for i in range(W + K)]
+        for i in range(W):
+            graphs[i].replay()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)]
+        barrier(ws)
+        torch.cuda.synchronize()
+        for i in range(K):
+            evs[i][0].record(stream)
+            graphs[W + i].replay()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        barrier(ws)
+        st.block.check()
+        ms = reduce_max(sum(a.elapsed_time(b) for a, b in evs), ws) / K
+        nbytes, wbytes = decode_bytes(s, L + W + K // 2, n)
+        achieved = nbytes / (ms * 1e-3) / 1e9
+        out[str(L)] = {"us_per_step": ms * 1e3, "tok_s": ws * 1e3 / ms,
+                       "bytes_per_step": nbytes, "achieved_gbs": achieved,
+                       "frac_of_hbm_peak": achieved / peaks["hbm_gbs"],
+                       "roofline_us": nbytes / (peaks["hbm_gbs"] * 1e9) * 1e6}
+        del graphs
+        st.graphs.clear()
+    # per-kernel durations at the largest context (eager, events per kernel)
+    L = ctxs[-1]
+    st.block.timing(True)
+    pos = torch.tensor([L], dtype=torch.int64, device=dev)
+    for i in range(2):
+        st.run("decode", xs[0], pos, L)
+        st.block.timing_collect(stream)
+    st.block.timing(False)
+    table = st.block.timing_table()
+    tot = sum(v[0] for v in table.values())
+    out["kernels_at_ctx"] = L
+    out["kernels"] = {k: {"avg_us": 1e3 * ms / cnt, "share": ms / tot} for k, (ms, cnt) in table.items()}
+    out["launches_per_step"] = sum(c for _, c in table.values()) // 2
+    out["workload"] = "qwen2-1.5B-shaped 28-layer stack, batch-1 decode, one CUDA graph per step"
+    return out
+
+
+# ------------------------------------------------------------------ main
+
+def main():
+    args = parse()
+    ws, rank, local = dist_init(args)
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        per_step, times = [], []
+        sample_rows = 8
+        for i in range(args.warmup + args.steps):
+            tok_s, secs, desc = oracle_prefill_sample(sample_rows, rotate=i)
+            if i >= args.warmup:
+                per_step.append(tok_s)
+                times.append(secs)
+        v = statistics.mean(per_step)
+        line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": ws,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * PREFILL_T / v,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic (seeded)",
+                "config": {"workload": "qwen2-1.5B-shaped decoder layer, prefill [1,1024], pos 0..1023"},
+                "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                 "sample": desc, "host_cores": os.cpu_count()},
+                "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+    result = bench_ours(args, ws, rank, local)
+    if rank == 0 and not args.no_cpu:
+        tok_s, secs, desc = oracle_prefill_sample(128)
+        result["cpu_baseline"] = {"value": tok_s, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                  "sample": desc, "host_cores": os.cpu_count(),
+                                  "seconds": secs}
+    if rank == 0:
+        print(json.dumps(result))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

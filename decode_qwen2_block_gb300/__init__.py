@@ -1,0 +1,267 @@
+"""GB300 decoder-block library: Python binding of libblk.so.
+
+The binding only marshals arguments: every step of the block runs in the
+library's CUDA kernels (see include/blk.h for the contract).  It loads the
+in-tree ``libblk.so`` and raises if it has not been built; there is no CPU or
+PyTorch fallback.
+
+Low-level functions carry the C names (``blk_create``, ``blk_prefill``,
+``blk_prefill_kv``, ``blk_decode``, ...) and take plain integers for device
+pointers.  ``Block`` is a convenience wrapper taking torch CUDA tensors.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libblk.so")
+
+BLK_OK = 0
+BLK_ERR_NULL = -1
+BLK_ERR_ALIGN = -2
+BLK_ERR_SHAPE = -3
+BLK_ERR_CACHE_OVERFLOW = -4
+BLK_ERR_WORKSPACE = -5
+BLK_ERR_CUDA = -6
+BLK_ERR_DEVICE_TIMEOUT = -7
+BLK_ERR_POSITION = -8
+BLK_ERR_DEVICE = -9
+BLK_FLAG_CHAIN = 1
+
+EXPORTED = ("blk_create", "blk_destroy", "blk_set_flags", "blk_workspace_bytes", "blk_prefill",
+            "blk_prefill_kv", "blk_decode", "blk_check", "blk_status_str", "blk_timing",
+            "blk_timing_collect", "blk_timing_read")
+BLK_N_KERNELS = 16
+
+WEIGHT_FIELDS = ("ln1_g", "wq", "wk", "wv", "bq", "bk", "bv", "wo", "ln2_g", "w_gate", "w_up",
+                 "w_down")
+
+
+class BlkConfig(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int32), ("n_heads", ctypes.c_int32),
+                ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("intermediate", ctypes.c_int32), ("rms_eps", ctypes.c_float),
+                ("rope_theta", ctypes.c_float), ("max_ctx", ctypes.c_int64),
+                ("has_qkv_bias", ctypes.c_int32)]
+
+
+class BlkWeights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in WEIGHT_FIELDS]
+
+
+class BlkError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {blk_status_str(status)} ({status})" if what else
+                         f"{blk_status_str(status)} ({status})")
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Loads libblk.so (once).  Raises if it is missing: build it first with
+    ``python -c 'import __graft_entry__ as g; g.build()'``."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"libblk.so not found at {path}; the CUDA library must be built "
+                           "(decode_qwen2_block_gb300/build.py) — there is no fallback")
+    lib = ctypes.CDLL(path)
+    vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    lib.blk_create.argtypes = [ctypes.POINTER(BlkConfig), ctypes.POINTER(vp)]
+    lib.blk_create.restype = i32
+    lib.blk_destroy.argtypes = [vp]
+    lib.blk_destroy.restype = None
+    lib.blk_set_flags.argtypes = [vp, ctypes.c_uint32]
+    lib.blk_set_flags.restype = i32
+    lib.blk_workspace_bytes.argtypes = [vp, i64]
+    lib.blk_workspace_bytes.restype = ctypes.c_size_t
+    lib.blk_prefill.argtypes = [vp, ctypes.POINTER(BlkWeights), vp, vp, i64, vp, vp, vp, vp, vp,
+                                vp, ctypes.c_size_t, vp]
+    lib.blk_prefill.restype = i32
+    lib.blk_prefill_kv.argtypes = [vp, ctypes.POINTER(BlkWeights), vp, vp, i64, i64, vp, vp, vp,
+                                   vp, vp, vp, ctypes.c_size_t, vp]
+    lib.blk_prefill_kv.restype = i32
+    lib.blk_decode.argtypes = [vp, ctypes.POINTER(BlkWeights), vp, vp, i64, vp, vp, vp, vp, vp,
+                               vp, ctypes.c_size_t, vp]
+    lib.blk_decode.restype = i32
+    lib.blk_check.argtypes = [vp, vp]
+    lib.blk_check.restype = i32
+    lib.blk_status_str.argtypes = [i32]
+    lib.blk_status_str.restype = ctypes.c_char_p
+    lib.blk_timing.argtypes = [vp, i32]
+    lib.blk_timing.restype = i32
+    lib.blk_timing_collect.argtypes = [vp, vp]
+    lib.blk_timing_collect.restype = i32
+    lib.blk_timing_read.argtypes = [vp, i32, ctypes.POINTER(ctypes.c_double),
+                                    ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_char_p)]
+    lib.blk_timing_read.restype = i32
+    _lib = lib
+    return lib
+
+
+# ---- C-named entry points (plain integer pointers) ---------------------------
+
+def blk_status_str(status: int) -> str:
+    return load().blk_status_str(int(status)).decode()
+
+
+def blk_create(cfg: BlkConfig) -> int:
+    h = ctypes.c_void_p()
+    rc = load().blk_create(ctypes.byref(cfg), ctypes.byref(h))
+    if rc != BLK_OK:
+        raise BlkError(rc, "blk_create")
+    return h.value
+
+
+def blk_destroy(handle: int) -> None:
+    load().blk_destroy(handle)
+
+
+def blk_set_flags(handle: int, flags: int) -> int:
+    return load().blk_set_flags(handle, flags)
+
+
+def blk_workspace_bytes(handle: int, max_T: int) -> int:
+    return load().blk_workspace_bytes(handle, max_T)
+
+
+def blk_prefill(handle, w: BlkWeights, x, pos, T, k_cache, v_cache, out, k_new, v_new, ws,
+                ws_bytes, stream) -> int:
+    return load().blk_prefill(handle, ctypes.byref(w), x, pos, T, k_cache, v_cache, out, k_new,
+                              v_new, ws, ws_bytes, stream)
+
+
+def blk_prefill_kv(handle, w: BlkWeights, x, pos, T, cache_len, k_cache, v_cache, out, k_new,
+                   v_new, ws, ws_bytes, stream) -> int:
+    return load().blk_prefill_kv(handle, ctypes.byref(w), x, pos, T, cache_len, k_cache, v_cache,
+                                 out, k_new, v_new, ws, ws_bytes, stream)
+
+
+def blk_decode(handle, w: BlkWeights, x, pos, cache_len, k_cache, v_cache, out, k_new, v_new, ws,
+               ws_bytes, stream) -> int:
+    return load().blk_decode(handle, ctypes.byref(w), x, pos, cache_len, k_cache, v_cache, out,
+                             k_new, v_new, ws, ws_bytes, stream)
+
+
+def blk_check(handle, stream) -> int:
+    return load().blk_check(handle, stream)
+
+
+def blk_timing(handle, on: bool) -> int:
+    return load().blk_timing(handle, 1 if on else 0)
+
+
+def blk_timing_collect(handle, stream) -> int:
+    return load().blk_timing_collect(handle, stream)
+
+
+def blk_timing_read(handle, kernel: int):
+    """Returns (name, total_ms, launches) or None for an unknown id."""
+    ms, n, name = ctypes.c_double(), ctypes.c_int64(), ctypes.c_char_p()
+    rc = load().blk_timing_read(handle, kernel, ctypes.byref(ms), ctypes.byref(n), ctypes.byref(name))
+    if rc != BLK_OK:
+        return None
+    return name.value.decode(), ms.value, n.value
+
+
+# ---- torch convenience wrapper ------------------------------------------------
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+class Block:
+    """One block shape on the current CUDA device.
+
+    ``shape`` needs the attributes hidden, n_heads, n_kv_heads, head_dim,
+    intermediate, has_qkv_bias, rms_eps, rope_theta."""
+
+    def __init__(self, shape, max_ctx: int, chain: bool = False):
+        self.shape = shape
+        self.max_ctx = int(max_ctx)
+        self.cfg = BlkConfig(shape.hidden, shape.n_heads, shape.n_kv_heads, shape.head_dim,
+                             shape.intermediate, shape.rms_eps, shape.rope_theta, self.max_ctx,
+                             1 if shape.has_qkv_bias else 0)
+        self.handle = blk_create(self.cfg)
+        if chain:
+            blk_set_flags(self.handle, BLK_FLAG_CHAIN)
+
+    def close(self):
+        if getattr(self, "handle", None):
+            blk_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def set_chain(self, on: bool):
+        blk_set_flags(self.handle, BLK_FLAG_CHAIN if on else 0)
+
+    def workspace_bytes(self, max_T: int) -> int:
+        return blk_workspace_bytes(self.handle, max_T)
+
+    @staticmethod
+    def weights(wdict) -> BlkWeights:
+        w = BlkWeights()
+        for n in WEIGHT_FIELDS:
+            setattr(w, n, _ptr(wdict.get(n)))
+        return w
+
+    @staticmethod
+    def _stream(stream):
+        import torch
+        s = torch.cuda.current_stream() if stream is None else stream
+        return s.cuda_stream
+
+    def prefill(self, w: BlkWeights, x, pos, k_cache, v_cache, out, ws, k_new=None, v_new=None,
+                stream=None):
+        rc = blk_prefill(self.handle, w, _ptr(x), _ptr(pos), x.shape[0], _ptr(k_cache),
+                         _ptr(v_cache), _ptr(out), _ptr(k_new), _ptr(v_new), _ptr(ws),
+                         ws.numel() * ws.element_size(), self._stream(stream))
+        if rc != BLK_OK:
+            raise BlkError(rc, "blk_prefill")
+
+    def prefill_kv(self, w: BlkWeights, x, pos, cache_len: int, k_cache, v_cache, out, ws,
+                   k_new=None, v_new=None, stream=None):
+        rc = blk_prefill_kv(self.handle, w, _ptr(x), _ptr(pos), x.shape[0], cache_len,
+                            _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(k_new), _ptr(v_new),
+                            _ptr(ws), ws.numel() * ws.element_size(), self._stream(stream))
+        if rc != BLK_OK:
+            raise BlkError(rc, "blk_prefill_kv")
+
+    def decode(self, w: BlkWeights, x, pos, cache_len: int, k_cache, v_cache, out, ws,
+               k_new=None, v_new=None, stream=None):
+        rc = blk_decode(self.handle, w, _ptr(x), _ptr(pos), cache_len, _ptr(k_cache),
+                        _ptr(v_cache), _ptr(out), _ptr(k_new), _ptr(v_new), _ptr(ws),
+                        ws.numel() * ws.element_size(), self._stream(stream))
+        if rc != BLK_OK:
+            raise BlkError(rc, "blk_decode")
+
+    def timing(self, on: bool):
+        rc = blk_timing(self.handle, on)
+        if rc != BLK_OK:
+            raise BlkError(rc, "blk_timing")
+
+    def timing_collect(self, stream=None):
+        return blk_timing_collect(self.handle, self._stream(stream))
+
+    def timing_table(self) -> dict:
+        """{kernel name: (total_ms, launches)} for kernels launched at least once."""
+        out = {}
+        for k in range(BLK_N_KERNELS):
+            r = blk_timing_read(self.handle, k)
+            if r and r[0] and r[2] > 0:
+                out[r[0]] = (r[1], r[2])
+        return out
+
+    def check(self, stream=None):
+        rc = blk_check(self.handle, self._stream(stream))
+        if rc != BLK_OK:
+            raise BlkError(rc, "device status")

@@ -1,0 +1,548 @@
+// C ABI of the decoder-block library: argument validation, workspace layout
+// and the kernel sequence of each phase.  See include/blk.h for the contract.
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <new>
+#include <vector>
+
+#include "../../include/blk.h"
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace blk;
+
+namespace {
+constexpr int kMaxPending = 1024;
+// Kernel ids for per-kernel timing (blk_timing_read).
+enum KernelId {
+  kKRmsNorm = 0, kKGemmQKV, kKRopeAppend, kKAttnPrefill, kKGemmO, kKGemmGateUp,
+  kKGemmDown, kKGemvQKV, kKAttnDecode, kKGemvO, kKGemvGateUp, kKGemvDown,
+  kKCount
+};
+const char* const kKernelNames[BLK_N_KERNELS] = {
+    "rmsnorm_rows", "gemm_qkv", "rope_append", "attn_prefill", "gemm_o",
+    "gemm_gateup", "gemm_down", "gemv_qkv_rope_append", "attn_decode_splitk",
+    "gemv_o", "gemv_gateup", "gemv_down", "", "", "", ""};
+}  // namespace
+
+struct blk_handle_s {
+  blk_config cfg;
+  int device;
+  int num_sms;
+  float2* rope;   // [max_ctx][head_dim / 2] (cos, sin)
+  int* status;    // device status word
+  uint32_t flags;
+  int max_splits; // decode attention splits at max_ctx
+  // per-kernel timing
+  bool timing;
+  bool overflow;
+  cudaEvent_t* ev;  // 2 * kMaxPending, created on first blk_timing(h, 1)
+  int pending;
+  int pending_kernel[kMaxPending];
+  double total_ms[BLK_N_KERNELS];
+  int64_t launches[BLK_N_KERNELS];
+};
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
+
+bool aligned(const void* p, size_t a) {
+  return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
+
+bool group_supported(int g) {
+  return g == 1 || g == 2 || g == 4 || g == 6 || g == 8 || g == 16;
+}
+
+int shape_ok(const blk_config* c) {
+  if (c->hidden <= 0 || c->n_heads <= 0 || c->n_kv_heads <= 0 ||
+      c->intermediate <= 0 || c->max_ctx < 1)
+    return BLK_ERR_SHAPE;
+  if (c->head_dim != 64 && c->head_dim != 128) return BLK_ERR_SHAPE;
+  if (c->n_heads % c->n_kv_heads != 0) return BLK_ERR_SHAPE;
+  if (!group_supported(c->n_heads / c->n_kv_heads)) return BLK_ERR_SHAPE;
+  if (c->hidden % 64 || c->intermediate % 64) return BLK_ERR_SHAPE;
+  if ((c->n_heads * c->head_dim) % 64) return BLK_ERR_SHAPE;
+  if (c->hidden > 16384 || c->intermediate > 16384) return BLK_ERR_SHAPE;
+  if (c->n_heads * c->head_dim > 16384) return BLK_ERR_SHAPE;
+  if (!(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f)) return BLK_ERR_SHAPE;
+  if (c->max_ctx > (int64_t)1 << 31) return BLK_ERR_SHAPE;
+  return BLK_OK;
+}
+
+// Workspace layout.  Prefill and decode buffers start at offset 0 (a call
+// uses one of the two layouts).
+struct PrefillWs {
+  size_t xn16, qkv32, q16, attn16, h32, hn16, act16, total;
+};
+struct DecodeWs {
+  size_t q32, attn16, h32, act16, part_ml, part_acc, counters, total;
+};
+
+PrefillWs prefill_ws(const blk_config& c, int64_t T) {
+  const size_t H = c.hidden, D = c.head_dim, Hq = c.n_heads, Hkv = c.n_kv_heads,
+               I = c.intermediate, N = (Hq + 2 * Hkv) * D;
+  PrefillWs w;
+  size_t o = 0;
+  w.xn16 = o; o = align_up(o + T * H * 2);
+  w.qkv32 = o; o = align_up(o + T * N * 4);
+  w.q16 = o; o = align_up(o + T * Hq * D * 2);
+  w.attn16 = o; o = align_up(o + T * Hq * D * 2);
+  w.h32 = o; o = align_up(o + T * H * 4);
+  w.hn16 = o; o = align_up(o + T * H * 2);
+  w.act16 = o; o = align_up(o + T * I * 2);
+  w.total = o;
+  return w;
+}
+
+DecodeWs decode_ws(const blk_config& c, int max_splits) {
+  const size_t H = c.hidden, D = c.head_dim, Hq = c.n_heads, Hkv = c.n_kv_heads,
+               I = c.intermediate, S = max_splits;
+  DecodeWs w;
+  size_t o = 0;
+  w.q32 = o; o = align_up(o + Hq * D * 4);
+  w.attn16 = o; o = align_up(o + Hq * D * 2);
+  w.h32 = o; o = align_up(o + H * 4);
+  w.act16 = o; o = align_up(o + I * 2);
+  w.part_ml = o; o = align_up(o + Hq * S * 8);
+  w.part_acc = o; o = align_up(o + Hq * S * D * 4);
+  w.counters = o; o = align_up(o + Hkv * 4);
+  w.total = o;
+  return w;
+}
+
+int check_weights(const blk_config& c, const blk_weights* w) {
+  if (!w) return BLK_ERR_NULL;
+  const void* mats[] = {w->wq, w->wk, w->wv, w->wo, w->w_gate, w->w_up, w->w_down};
+  for (const void* m : mats) {
+    if (!m) return BLK_ERR_NULL;
+    if (!aligned(m, 16)) return BLK_ERR_ALIGN;
+  }
+  if (!w->ln1_g || !w->ln2_g) return BLK_ERR_NULL;
+  if (!aligned(w->ln1_g, 2) || !aligned(w->ln2_g, 2)) return BLK_ERR_ALIGN;
+  if (c.has_qkv_bias) {
+    if (!w->bq || !w->bk || !w->bv) return BLK_ERR_NULL;
+    if (!aligned(w->bq, 2) || !aligned(w->bk, 2) || !aligned(w->bv, 2))
+      return BLK_ERR_ALIGN;
+  }
+  return BLK_OK;
+}
+
+int check_call(blk_handle h, const blk_weights* w, const void* x,
+               const int64_t* pos, int64_t T, int64_t L, const void* kc,
+               const void* vc, const void* out, const void* kn, const void* vn,
+               const void* ws) {
+  if (!h) return BLK_ERR_NULL;
+  int rc = check_weights(h->cfg, w);
+  if (rc) return rc;
+  if (!x || !pos || !kc || !vc || !out || !ws) return BLK_ERR_NULL;
+  const void* a16[] = {x, kc, vc, out, ws};
+  for (const void* p : a16)
+    if (!aligned(p, 16)) return BLK_ERR_ALIGN;
+  if ((kn && !aligned(kn, 16)) || (vn && !aligned(vn, 16))) return BLK_ERR_ALIGN;
+  if (!aligned(pos, 8)) return BLK_ERR_ALIGN;
+  if (T < 1 || T > ((int64_t)1 << 31)) return BLK_ERR_SHAPE;
+  if (L < 0 || L + T > h->cfg.max_ctx) return BLK_ERR_CACHE_OVERFLOW;
+  return BLK_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? BLK_OK : BLK_ERR_CUDA; }
+
+// Brackets one launch with events when the handle's timing is on.
+struct Timer {
+  blk_handle h;
+  cudaStream_t s;
+  int slot = -1;
+  void begin(int kid) {
+    slot = -1;
+    if (!h->timing) return;
+    if (h->pending >= kMaxPending) {
+      h->overflow = true;
+      return;
+    }
+    slot = h->pending++;
+    h->pending_kernel[slot] = kid;
+    cudaEventRecord(h->ev[2 * slot], s);
+  }
+  void end() {
+    if (slot >= 0) cudaEventRecord(h->ev[2 * slot + 1], s);
+    slot = -1;
+  }
+};
+
+#define BLK_LAUNCH(TIMER, KID, EXPR)   \
+  do {                                 \
+    (TIMER).begin(KID);                \
+    const cudaError_t e_ = (EXPR);     \
+    (TIMER).end();                     \
+    if (e_ != cudaSuccess) return BLK_ERR_CUDA; \
+  } while (0)
+
+// prefill and prefill_kv: T new rows after L history slots.
+int run_prefill(blk_handle h, const blk_weights* w, const void* x,
+                const int64_t* pos, int64_t T, int64_t L, void* k_cache,
+                void* v_cache, void* out, void* k_new, void* v_new, void* ws,
+                size_t ws_bytes, void* stream) {
+  int rc = check_call(h, w, x, pos, T, L, k_cache, v_cache, out, k_new, v_new, ws);
+  if (rc) return rc;
+  const blk_config& c = h->cfg;
+  const PrefillWs lay = prefill_ws(c, T);
+  if (ws_bytes < lay.total) return BLK_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned char* base = static_cast<unsigned char*>(ws);
+  __half* xn16 = reinterpret_cast<__half*>(base + lay.xn16);
+  float* qkv32 = reinterpret_cast<float*>(base + lay.qkv32);
+  __half* q16 = reinterpret_cast<__half*>(base + lay.q16);
+  __half* attn16 = reinterpret_cast<__half*>(base + lay.attn16);
+  float* h32 = reinterpret_cast<float*>(base + lay.h32);
+  __half* hn16 = reinterpret_cast<__half*>(base + lay.hn16);
+  __half* act16 = reinterpret_cast<__half*>(base + lay.act16);
+  const int H = c.hidden, D = c.head_dim, Hq = c.n_heads, Hkv = c.n_kv_heads,
+            I = c.intermediate, NQKV = (Hq + 2 * Hkv) * D, M = (int)T;
+  const bool first_pdl = (h->flags & BLK_FLAG_CHAIN) != 0;
+  Timer tm{h, s};
+
+  BLK_LAUNCH(tm, kKRmsNorm,
+             launch_rmsnorm_rows(x, false, static_cast<const __half*>(w->ln1_g), M, H,
+                                 c.rms_eps, xn16, s, first_pdl));
+  const void* wqkv[3] = {w->wq, w->wk, w->wv};
+  const int ncols[3] = {Hq * D, Hkv * D, Hkv * D};
+  int col = 0;
+  for (int k = 0; k < 3; ++k) {
+    GemmParams g = {};
+    g.A = xn16;
+    g.B = static_cast<const __half*>(wqkv[k]);
+    g.M = M; g.N = ncols[k]; g.K = H;
+    g.outF32 = qkv32 + col;
+    g.ldo = NQKV;
+    BLK_LAUNCH(tm, kKGemmQKV, launch_gemm(g, kEpiStoreF32, s, true));
+    col += ncols[k];
+  }
+  RopeAppendParams ra = {};
+  ra.qkv32 = qkv32;
+  ra.bq = static_cast<const __half*>(c.has_qkv_bias ? w->bq : nullptr);
+  ra.bk = static_cast<const __half*>(c.has_qkv_bias ? w->bk : nullptr);
+  ra.bv = static_cast<const __half*>(c.has_qkv_bias ? w->bv : nullptr);
+  ra.pos = pos;
+  ra.rope = h->rope;
+  ra.rope_len = c.max_ctx;
+  ra.T = M; ra.Hq = Hq; ra.Hkv = Hkv; ra.D = D;
+  ra.cache_len = L; ra.max_ctx = c.max_ctx;
+  ra.q16 = q16;
+  ra.kc = static_cast<__half*>(k_cache);
+  ra.vc = static_cast<__half*>(v_cache);
+  ra.k_new = static_cast<__half*>(k_new);
+  ra.v_new = static_cast<__half*>(v_new);
+  ra.err = h->status;
+  BLK_LAUNCH(tm, kKRopeAppend, launch_rope_append(ra, s, true));
+
+  PrefillAttnParams pa = {};
+  pa.q16 = q16;
+  pa.kc = static_cast<const __half*>(k_cache);
+  pa.vc = static_cast<const __half*>(v_cache);
+  pa.max_ctx = c.max_ctx; pa.cache_len = L;
+  pa.T = M; pa.Hq = Hq; pa.Hkv = Hkv; pa.D = D;
+  pa.scale_log2 = (float)(1.4426950408889634 / sqrt((double)D));
+  pa.attn16 = attn16;
+  BLK_LAUNCH(tm, kKAttnPrefill, launch_prefill_attn(pa, s, true));
+
+  GemmParams go = {};
+  go.A = attn16; go.B = static_cast<const __half*>(w->wo);
+  go.M = M; go.N = H; go.K = Hq * D;
+  go.outF32 = h32; go.resF16 = static_cast<const __half*>(x); go.ldo = H;
+  BLK_LAUNCH(tm, kKGemmO, launch_gemm(go, kEpiResidF32, s, true));
+
+  BLK_LAUNCH(tm, kKRmsNorm,
+             launch_rmsnorm_rows(h32, true, static_cast<const __half*>(w->ln2_g), M, H,
+                                 c.rms_eps, hn16, s, true));
+
+  GemmParams gu = {};
+  gu.A = hn16; gu.B = static_cast<const __half*>(w->w_gate);
+  gu.B2 = static_cast<const __half*>(w->w_up);
+  gu.M = M; gu.N = I; gu.K = H;
+  gu.outF16 = act16; gu.ldo = I;
+  BLK_LAUNCH(tm, kKGemmGateUp, launch_gemm(gu, kEpiSwiGLU, s, true));
+
+  GemmParams gd = {};
+  gd.A = act16; gd.B = static_cast<const __half*>(w->w_down);
+  gd.M = M; gd.N = H; gd.K = I;
+  gd.outF16 = static_cast<__half*>(out); gd.resF32 = h32; gd.ldo = H;
+  BLK_LAUNCH(tm, kKGemmDown, launch_gemm(gd, kEpiResidOutF16, s, true));
+  return BLK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int blk_create(const blk_config* cfg, blk_handle* out) {
+  if (!cfg || !out) return BLK_ERR_NULL;
+  *out = nullptr;
+  int rc = shape_ok(cfg);
+  if (rc) return rc;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return BLK_ERR_CUDA;
+  int major = 0, minor = 0, sms = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev))
+    return BLK_ERR_CUDA;
+  if (major != 10 || minor != 3) return BLK_ERR_DEVICE;
+  if (configure_kernels() != cudaSuccess) return BLK_ERR_CUDA;
+
+  blk_handle h = new (std::nothrow) blk_handle_s();
+  if (!h) return BLK_ERR_CUDA;
+  h->cfg = *cfg;
+  h->device = dev;
+  h->num_sms = sms;
+  h->max_splits = decode_attn_max_splits(cfg->max_ctx, cfg->n_kv_heads, sms);
+
+  const int half = cfg->head_dim / 2;
+  std::vector<float2> table((size_t)cfg->max_ctx * half);
+  for (int i = 0; i < half; ++i) {
+    const double inv = pow((double)cfg->rope_theta, -2.0 * i / (double)cfg->head_dim);
+    for (int64_t p = 0; p < cfg->max_ctx; ++p) {
+      const double a = (double)p * inv;
+      table[(size_t)p * half + i] = make_float2((float)cos(a), (float)sin(a));
+    }
+  }
+  if (cudaMalloc(&h->rope, table.size() * sizeof(float2)) != cudaSuccess ||
+      cudaMalloc(&h->status, sizeof(int)) != cudaSuccess ||
+      cudaMemcpy(h->rope, table.data(), table.size() * sizeof(float2),
+                 cudaMemcpyHostToDevice) != cudaSuccess ||
+      cudaMemset(h->status, 0, sizeof(int)) != cudaSuccess) {
+    blk_destroy(h);
+    return BLK_ERR_CUDA;
+  }
+  *out = h;
+  return BLK_OK;
+}
+
+void blk_destroy(blk_handle h) {
+  if (!h) return;
+  if (h->rope) cudaFree(h->rope);
+  if (h->status) cudaFree(h->status);
+  if (h->ev) {
+    for (int i = 0; i < 2 * kMaxPending; ++i) cudaEventDestroy(h->ev[i]);
+    delete[] h->ev;
+  }
+  delete h;
+}
+
+int blk_set_flags(blk_handle h, uint32_t flags) {
+  if (!h) return BLK_ERR_NULL;
+  h->flags = flags;
+  return BLK_OK;
+}
+
+size_t blk_workspace_bytes(blk_handle h, int64_t max_T) {
+  if (!h || max_T < 1) return 0;
+  const size_t a = prefill_ws(h->cfg, max_T).total;
+  const size_t b = decode_ws(h->cfg, h->max_splits).total;
+  return a > b ? a : b;
+}
+
+int blk_prefill(blk_handle h, const blk_weights* w, const void* x,
+                const int64_t* pos, int64_t T, void* k_cache, void* v_cache,
+                void* out, void* k_new, void* v_new, void* ws, size_t ws_bytes,
+                void* stream) {
+  return run_prefill(h, w, x, pos, T, 0, k_cache, v_cache, out, k_new, v_new, ws,
+                     ws_bytes, stream);
+}
+
+int blk_prefill_kv(blk_handle h, const blk_weights* w, const void* x,
+                   const int64_t* pos, int64_t T, int64_t cache_len,
+                   void* k_cache, void* v_cache, void* out, void* k_new,
+                   void* v_new, void* ws, size_t ws_bytes, void* stream) {
+  return run_prefill(h, w, x, pos, T, cache_len, k_cache, v_cache, out, k_new,
+                     v_new, ws, ws_bytes, stream);
+}
+
+int blk_decode(blk_handle h, const blk_weights* w, const void* x,
+               const int64_t* pos, int64_t cache_len, void* k_cache,
+               void* v_cache, void* out, void* k_new, void* v_new, void* ws,
+               size_t ws_bytes, void* stream) {
+  int rc = check_call(h, w, x, pos, 1, cache_len, k_cache, v_cache, out, k_new,
+                      v_new, ws);
+  if (rc) return rc;
+  const blk_config& c = h->cfg;
+  const DecodeWs lay = decode_ws(c, h->max_splits);
+  if (ws_bytes < lay.total) return BLK_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned char* base = static_cast<unsigned char*>(ws);
+  float* q32 = reinterpret_cast<float*>(base + lay.q32);
+  __half* attn16 = reinterpret_cast<__half*>(base + lay.attn16);
+  float* h32 = reinterpret_cast<float*>(base + lay.h32);
+  __half* act16 = reinterpret_cast<__half*>(base + lay.act16);
+  float2* part_ml = reinterpret_cast<float2*>(base + lay.part_ml);
+  float* part_acc = reinterpret_cast<float*>(base + lay.part_acc);
+  unsigned* counters = reinterpret_cast<unsigned*>(base + lay.counters);
+  const int H = c.hidden, D = c.head_dim, Hq = c.n_heads, Hkv = c.n_kv_heads,
+            I = c.intermediate;
+  const bool first_pdl = (h->flags & BLK_FLAG_CHAIN) != 0;
+  Timer tm{h, s};
+
+  GemvParams g = {};
+  g.W[0] = static_cast<const __half*>(w->wq);
+  g.W[1] = static_cast<const __half*>(w->wk);
+  g.W[2] = static_cast<const __half*>(w->wv);
+  if (c.has_qkv_bias) {
+    g.bias[0] = static_cast<const __half*>(w->bq);
+    g.bias[1] = static_cast<const __half*>(w->bk);
+    g.bias[2] = static_cast<const __half*>(w->bv);
+  }
+  g.K = H;
+  g.x16 = static_cast<const __half*>(x);
+  g.gain = static_cast<const __half*>(w->ln1_g);
+  g.eps = c.rms_eps;
+  g.Hq = Hq; g.Hkv = Hkv; g.D = D;
+  const int heads = Hq + 2 * Hkv;
+  int parts = h->num_sms / heads;
+  if (parts < 1) parts = 1;
+  if (parts > D / 2) parts = D / 2;
+  g.parts = parts;
+  g.pos = pos;
+  g.rope = h->rope;
+  g.rope_len = c.max_ctx;
+  g.kc = static_cast<__half*>(k_cache);
+  g.vc = static_cast<__half*>(v_cache);
+  g.max_ctx = c.max_ctx;
+  g.slot = cache_len;
+  g.k_new = static_cast<__half*>(k_new);
+  g.v_new = static_cast<__half*>(v_new);
+  g.q32 = q32;
+  g.counters = counters;
+  g.n_counters = Hkv;
+  g.err = h->status;
+  BLK_LAUNCH(tm, kKGemvQKV,
+             launch_gemv(g, kGemvQKV, gemv_grid(g, kGemvQKV, h->num_sms), s, first_pdl));
+
+  DecodeAttnParams da = {};
+  da.q32 = q32;
+  da.kc = static_cast<const __half*>(k_cache);
+  da.vc = static_cast<const __half*>(v_cache);
+  da.max_ctx = c.max_ctx;
+  da.n_keys = cache_len + 1;
+  da.Hq = Hq; da.Hkv = Hkv; da.D = D;
+  decode_attn_splits(da.n_keys, Hkv, h->num_sms, &da.splits, &da.slots_per_split);
+  if (da.splits > h->max_splits) return BLK_ERR_WORKSPACE;
+  da.part_ml = part_ml;
+  da.part_acc = part_acc;
+  da.counters = counters;
+  da.attn16 = attn16;
+  da.scale_log2 = (float)(1.4426950408889634 / sqrt((double)D));
+  da.err = h->status;
+  BLK_LAUNCH(tm, kKAttnDecode, launch_decode_attn(da, s, true));
+
+  GemvParams go = {};
+  go.W[0] = static_cast<const __half*>(w->wo);
+  go.K = Hq * D; go.N = H;
+  go.x16 = attn16;
+  go.res16 = static_cast<const __half*>(x);
+  go.out32 = h32;
+  go.err = h->status;
+  BLK_LAUNCH(tm, kKGemvO, launch_gemv(go, kGemvO, gemv_grid(go, kGemvO, h->num_sms), s, true));
+
+  GemvParams gu = {};
+  gu.W[0] = static_cast<const __half*>(w->w_gate);
+  gu.W[1] = static_cast<const __half*>(w->w_up);
+  gu.K = H; gu.N = I;
+  gu.x32 = h32;
+  gu.gain = static_cast<const __half*>(w->ln2_g);
+  gu.eps = c.rms_eps;
+  gu.out16 = act16;
+  gu.err = h->status;
+  BLK_LAUNCH(tm, kKGemvGateUp,
+             launch_gemv(gu, kGemvGateUp, gemv_grid(gu, kGemvGateUp, h->num_sms), s, true));
+
+  GemvParams gd = {};
+  gd.W[0] = static_cast<const __half*>(w->w_down);
+  gd.K = I; gd.N = H;
+  gd.x16 = act16;
+  gd.res32 = h32;
+  gd.out16 = static_cast<__half*>(out);
+  gd.err = h->status;
+  BLK_LAUNCH(tm, kKGemvDown,
+             launch_gemv(gd, kGemvDown, gemv_grid(gd, kGemvDown, h->num_sms), s, true));
+  return BLK_OK;
+}
+
+int blk_check(blk_handle h, void* stream) {
+  if (!h) return BLK_ERR_NULL;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return BLK_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, h->status, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return BLK_ERR_CUDA;
+  if (v != 0 && cudaMemset(h->status, 0, sizeof v) != cudaSuccess) return BLK_ERR_CUDA;
+  if (v == kDevTimeout) return BLK_ERR_DEVICE_TIMEOUT;
+  if (v == kDevPosition) return BLK_ERR_POSITION;
+  return BLK_OK;
+}
+
+int blk_timing(blk_handle h, int on) {
+  if (!h) return BLK_ERR_NULL;
+  if (on && !h->ev) {
+    h->ev = new (std::nothrow) cudaEvent_t[2 * kMaxPending]();
+    if (!h->ev) return BLK_ERR_CUDA;
+    for (int i = 0; i < 2 * kMaxPending; ++i)
+      if (cudaEventCreate(&h->ev[i]) != cudaSuccess) return BLK_ERR_CUDA;
+  }
+  h->timing = on != 0;
+  return BLK_OK;
+}
+
+int blk_timing_collect(blk_handle h, void* stream) {
+  if (!h) return BLK_ERR_NULL;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return BLK_ERR_CUDA;
+  for (int i = 0; i < h->pending; ++i) {
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, h->ev[2 * i], h->ev[2 * i + 1]) != cudaSuccess)
+      return BLK_ERR_CUDA;
+    h->total_ms[h->pending_kernel[i]] += ms;
+    h->launches[h->pending_kernel[i]] += 1;
+  }
+  h->pending = 0;
+  const bool over = h->overflow;
+  h->overflow = false;
+  return over ? BLK_ERR_WORKSPACE : BLK_OK;
+}
+
+int blk_timing_read(blk_handle h, int kernel, double* total_ms, int64_t* launches,
+                    const char** name) {
+  if (!h) return BLK_ERR_NULL;
+  if (kernel < 0 || kernel >= kKCount) return BLK_ERR_SHAPE;
+  if (total_ms) *total_ms = h->total_ms[kernel];
+  if (launches) *launches = h->launches[kernel];
+  if (name) *name = kKernelNames[kernel];
+  return BLK_OK;
+}
+
+const char* blk_status_str(int status) {
+  switch (status) {
+    case BLK_OK: return "ok";
+    case BLK_ERR_NULL: return "a required pointer is NULL";
+    case BLK_ERR_ALIGN: return "a pointer is not aligned (16 bytes for tensors, 8 for position ids)";
+    case BLK_ERR_SHAPE: return "unsupported or inconsistent shape";
+    case BLK_ERR_CACHE_OVERFLOW: return "cache_len + T exceeds max_ctx (or cache_len < 0)";
+    case BLK_ERR_WORKSPACE: return "workspace smaller than blk_workspace_bytes()";
+    case BLK_ERR_CUDA: return "a CUDA runtime call or kernel launch failed";
+    case BLK_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait timed out";
+    case BLK_ERR_POSITION: return "a position id was outside [0, max_ctx) and was clamped";
+    case BLK_ERR_DEVICE: return "the current GPU is not sm_103 (GB300)";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"
+
+namespace blk {
+cudaError_t configure_gemv_kernels();
+cudaError_t configure_kernels() { return configure_gemv_kernels(); }
+}  // namespace blk

@@ -1,0 +1,73 @@
+"""A stack of decoder blocks driven through the C ABI.
+
+Runs one phase over every layer in order (layer l's output is layer l+1's
+input), with the BLK_FLAG_CHAIN promise set so that each layer's first
+kernel overlaps the previous layer's last kernel, and can capture a decode
+step into a CUDA graph (one graph per cache length, since cache_len is a
+by-value argument).  All work is the library's kernels; torch only supplies
+device memory, streams and graphs.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import Block
+
+
+class LayerStack:
+    def __init__(self, shape, layer_weights, max_ctx: int, max_T: int, caches=None,
+                 chain: bool = True, device="cuda"):
+        """layer_weights: list of dicts of fp16 CUDA tensors (one per layer).
+        caches: optional list of (k_cache, v_cache) per layer; allocated
+        (zero-filled) when None."""
+        self.shape = shape
+        self.n_layers = len(layer_weights)
+        self.block = Block(shape, max_ctx, chain=chain)
+        self.wdev = layer_weights
+        self.w = [Block.weights(wd) for wd in layer_weights]
+        H, Hkv, D = shape.hidden, shape.n_kv_heads, shape.head_dim
+        if caches is None:
+            caches = [(torch.zeros((Hkv, max_ctx, D), dtype=torch.float16, device=device),
+                       torch.zeros((Hkv, max_ctx, D), dtype=torch.float16, device=device))
+                      for _ in range(self.n_layers)]
+        self.caches = caches
+        self.ws = torch.empty(self.block.workspace_bytes(max_T), dtype=torch.uint8, device=device)
+        self.max_T = max_T
+        # ping-pong activations between layers
+        self.bufs = [torch.empty((max_T, H), dtype=torch.float16, device=device) for _ in range(2)]
+        self.graphs = {}
+
+    def run(self, phase: str, x, pos, cache_len: int, layer_outputs=None, stream=None):
+        """Runs `phase` over all layers; returns the last layer's output (a
+        view of an internal buffer).  layer_outputs, if given, is a list that
+        receives a copy of each layer's input (for layer-local checks)."""
+        T = x.shape[0]
+        cur = x
+        for l in range(self.n_layers):
+            out = self.bufs[l % 2][:T]
+            if layer_outputs is not None:
+                layer_outputs.append(cur.clone())
+            kc, vc = self.caches[l]
+            if phase == "decode":
+                self.block.decode(self.w[l], cur, pos, cache_len, kc, vc, out, self.ws,
+                                  stream=stream)
+            elif phase == "prefill":
+                self.block.prefill(self.w[l], cur, pos, kc, vc, out, self.ws, stream=stream)
+            else:
+                self.block.prefill_kv(self.w[l], cur, pos, cache_len, kc, vc, out, self.ws,
+                                      stream=stream)
+            cur = out
+        return cur
+
+    def capture(self, phase: str, x, pos, cache_len: int, key=None):
+        """Captures one pass over all layers into a CUDA graph.  x and pos must
+        stay alive and at the same address for every replay."""
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                out = self.run(phase, x, pos, cache_len, stream=s)
+        torch.cuda.current_stream().wait_stream(s)
+        self.graphs[key if key is not None else (phase, cache_len)] = (g, out)
+        return g, out

@@ -1,0 +1,172 @@
+/*
+ * blk.h — C ABI of the GB300 decoder-block library (libblk.so).
+ *
+ * One call runs one Qwen2-style decoder block forward for one sequence
+ * (batch 1) on one GPU.  The block is the one printed as TopOp pseudo-code in
+ * "An MLIR-based LLM compilation method" (TopOp/TpuOp paper translation),
+ * §3.1 Listing 1 (no history) and Listing 2 (with history K/V):
+ *
+ *   xn   = RMSNorm(x) * ln1_g                  y = x / sqrt(mean(x^2) + eps)
+ *   q,k,v= xn Wq^T (+bq), xn Wk^T (+bk), xn Wv^T (+bv)
+ *   cos,sin gathered by position_ids from a precomputed table
+ *   q,k  = RoPE(q), RoPE(k)                    rotate_half pairs (i, i + D/2),
+ *                                              angle = pos * theta^(-2i/D)
+ *   attn = FAttention(q, [history K; k], [history V; v])
+ *          softmax(q.k / sqrt(D)), causal in cache-slot order, q head h reads
+ *          kv head h / (n_heads / n_kv_heads)
+ *   h    = x + attn Wo^T
+ *   out  = h + W_down (silu(RMSNorm(h) W_gate^T) * (RMSNorm(h) W_up^T))
+ *   returns (out, k, v)                        k after RoPE, v as projected
+ *
+ * and its three statically shaped phases of that paper's §4.1: prefill
+ * (T new tokens, no history), prefill_kv (T new tokens after cache_len
+ * history slots), decode (one token after cache_len slots).
+ *
+ * Data types: every activation, weight and cache element is IEEE binary16
+ * (fp16), passed as `void*` / `const void*`; position_ids are int64.
+ * Arithmetic is fp32 on the GPU (fp16 tensor-core inputs, fp32 accumulate).
+ *
+ * Ownership: the caller owns every buffer passed in (weights, inputs, outputs,
+ * KV cache, workspace) and every pointer named "device" must be device memory
+ * on the handle's GPU, 16-byte aligned.  The library allocates device memory
+ * only in blk_create (a RoPE table and a status word), never on the hot path.
+ * Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ * stream) and never synchronize, trap or abort.
+ *
+ * KV cache: one K and one V buffer per layer, each [n_kv_heads][max_ctx][head_dim]
+ * (the buddy-mlir runtime's per-layer [1, kv_heads, max_len, head_dim] cache of
+ * its §6.4.3).  A call reads slots [0, cache_len), writes slots
+ * [cache_len, cache_len + T) in place, and leaves every other slot untouched.
+ * Slots are the cache's order; position_ids drive RoPE only.
+ */
+#ifndef BLK_H
+#define BLK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes (0 = success, negative = failure). */
+#define BLK_OK 0
+#define BLK_ERR_NULL (-1)            /* a required pointer is NULL              */
+#define BLK_ERR_ALIGN (-2)           /* a device pointer is not 16-byte aligned */
+#define BLK_ERR_SHAPE (-3)           /* unsupported or inconsistent shape       */
+#define BLK_ERR_CACHE_OVERFLOW (-4)  /* cache_len + T > max_ctx, or cache_len<0 */
+#define BLK_ERR_WORKSPACE (-5)       /* ws_bytes below blk_workspace_bytes()    */
+#define BLK_ERR_CUDA (-6)            /* a CUDA runtime call or launch failed    */
+#define BLK_ERR_DEVICE_TIMEOUT (-7)  /* a bounded device-side wait gave up      */
+#define BLK_ERR_POSITION (-8)        /* a position id outside [0, max_ctx)      */
+#define BLK_ERR_DEVICE (-9)          /* the current GPU is not sm_103 (GB300)   */
+
+/* Block shape.  Supported: head_dim 64 or 128; n_heads % n_kv_heads == 0 with
+ * group size n_heads / n_kv_heads in {1, 2, 4, 6, 8, 16}; hidden and
+ * intermediate multiples of 64 and at most 16384; n_heads*head_dim multiple
+ * of 64; max_ctx >= 1. */
+typedef struct {
+  int32_t hidden;
+  int32_t n_heads;
+  int32_t n_kv_heads;
+  int32_t head_dim;
+  int32_t intermediate;
+  float rms_eps;      /* 1e-6 for every shape here                          */
+  float rope_theta;   /* 10000                                              */
+  int64_t max_ctx;    /* cache slots per head; also bounds position_ids     */
+  int32_t has_qkv_bias;
+} blk_config;
+
+/* Device pointers to one layer's fp16 weights.  Matrices are [out, in]
+ * row-major (PyTorch nn.Linear layout): wq [n_heads*D, hidden],
+ * wk/wv [n_kv_heads*D, hidden], wo [hidden, n_heads*D],
+ * w_gate/w_up [intermediate, hidden], w_down [hidden, intermediate];
+ * ln1_g/ln2_g [hidden]; bq/bk/bv [out] or NULL when !has_qkv_bias. */
+typedef struct {
+  const void *ln1_g, *wq, *wk, *wv, *bq, *bk, *bv, *wo, *ln2_g, *w_gate,
+      *w_up, *w_down;
+} blk_weights;
+
+typedef struct blk_handle_s* blk_handle;
+
+/* Option bits for blk_set_flags. */
+#define BLK_FLAG_CHAIN 1u
+/* BLK_FLAG_CHAIN: the caller promises that the stream work enqueued just
+ * before each call never writes that call's weights or KV-cache history
+ * (true for a layer stack run back to back).  The first kernel of each call
+ * then starts streaming weights while the previous kernel is still running
+ * (programmatic dependent launch).  Off by default: the first kernel then
+ * waits for all earlier stream work. */
+
+/* Creates a handle for `cfg` on the current CUDA device: validates the shape,
+ * builds the fp32 cos/sin table [max_ctx][head_dim/2] (angles in f64) and a
+ * status word.  Returns BLK_OK, BLK_ERR_NULL, BLK_ERR_SHAPE, BLK_ERR_DEVICE or
+ * BLK_ERR_CUDA. */
+int blk_create(const blk_config* cfg, blk_handle* out);
+
+/* Frees the handle's device memory.  NULL is ignored. */
+void blk_destroy(blk_handle h);
+
+int blk_set_flags(blk_handle h, uint32_t flags);
+
+/* Workspace bytes needed by a call with up to max_T new tokens (decode needs
+ * max_T = 1).  0 on a bad handle or max_T < 1. */
+size_t blk_workspace_bytes(blk_handle h, int64_t max_T);
+
+/* prefill (Listing 1): T new tokens, no history (cache_len = 0).
+ *   x      device fp16 [T, hidden]
+ *   pos    device int64 [T]
+ *   k_cache, v_cache  device fp16 [n_kv_heads, max_ctx, head_dim]; slots
+ *          [0, T) written
+ *   out    device fp16 [T, hidden]
+ *   k_new, v_new  device fp16 [T, n_kv_heads, head_dim], or NULL
+ *   ws     device workspace of ws_bytes >= blk_workspace_bytes(h, T); its
+ *          contents need no initialisation and are garbage afterwards
+ * x, pos, out and ws must not overlap the caches or each other. */
+int blk_prefill(blk_handle h, const blk_weights* w, const void* x,
+                const int64_t* pos, int64_t T, void* k_cache, void* v_cache,
+                void* out, void* k_new, void* v_new, void* ws,
+                size_t ws_bytes, void* stream);
+
+/* prefill_kv (Listing 2): T new tokens after cache_len history slots; new
+ * row t attends slots [0, cache_len + t].  Arguments as blk_prefill. */
+int blk_prefill_kv(blk_handle h, const blk_weights* w, const void* x,
+                   const int64_t* pos, int64_t T, int64_t cache_len,
+                   void* k_cache, void* v_cache, void* out, void* k_new,
+                   void* v_new, void* ws, size_t ws_bytes, void* stream);
+
+/* decode (§4.1): one token after cache_len slots; attends [0, cache_len].
+ *   x [1, hidden], pos [1], out [1, hidden], k_new/v_new [1, n_kv_heads, D].
+ * Uses the weight-streaming kernels (HBM-bound path). */
+int blk_decode(blk_handle h, const blk_weights* w, const void* x,
+               const int64_t* pos, int64_t cache_len, void* k_cache,
+               void* v_cache, void* out, void* k_new, void* v_new, void* ws,
+               size_t ws_bytes, void* stream);
+
+/* Synchronizes `stream`, then reports and clears the handle's device status
+ * word: BLK_OK, BLK_ERR_DEVICE_TIMEOUT or BLK_ERR_POSITION (a kernel clamped
+ * an out-of-range position id), or BLK_ERR_CUDA if the stream failed. */
+int blk_check(blk_handle h, void* stream);
+
+/* Per-kernel timing, for benchmarks.  While on, every kernel a call enqueues
+ * is bracketed by CUDA events recorded on the call's stream (this keeps
+ * consecutive kernels from overlapping, so time the whole step with timing
+ * off).  blk_timing_collect synchronizes `stream` and adds the elapsed time
+ * of every bracketed launch since the previous collect to a per-kernel total;
+ * at most 1024 launches are held between two collects (later ones are not
+ * timed and blk_timing_collect returns BLK_ERR_WORKSPACE).  blk_timing_read
+ * returns the totals of kernel id `kernel` (0 <= kernel < BLK_N_KERNELS) and
+ * its name; BLK_ERR_SHAPE for an unknown id. */
+#define BLK_N_KERNELS 16
+int blk_timing(blk_handle h, int on);
+int blk_timing_collect(blk_handle h, void* stream);
+int blk_timing_read(blk_handle h, int kernel, double* total_ms,
+                    int64_t* launches, const char** name);
+
+/* Static description of a status code. */
+const char* blk_status_str(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* BLK_H */
