@@ -9,6 +9,7 @@
 
 #include "../../include/blk.h"
 #include "common.cuh"
+#include "gemm_tc.h"
 #include "kernels.h"
 
 using namespace blk;
@@ -66,7 +67,7 @@ int shape_ok(const blk_config* c) {
   if (c->head_dim != 64 && c->head_dim != 128) return BLK_ERR_SHAPE;
   if (c->n_heads % c->n_kv_heads != 0) return BLK_ERR_SHAPE;
   if (!group_supported(c->n_heads / c->n_kv_heads)) return BLK_ERR_SHAPE;
-  if (c->hidden % 64 || c->intermediate % 64) return BLK_ERR_SHAPE;
+  if (c->hidden % 64 || c->intermediate % 8) return BLK_ERR_SHAPE;
   if ((c->n_heads * c->head_dim) % 64) return BLK_ERR_SHAPE;
   if (c->hidden > 16384 || c->intermediate > 16384) return BLK_ERR_SHAPE;
   if (c->n_heads * c->head_dim > 16384) return BLK_ERR_SHAPE;
@@ -78,7 +79,7 @@ int shape_ok(const blk_config* c) {
 // Workspace layout.  Prefill and decode buffers start at offset 0 (a call
 // uses one of the two layouts).
 struct PrefillWs {
-  size_t xn16, qkv32, q16, attn16, h32, hn16, act16, total;
+  size_t xn16, q16, attn16, h32, hn16, act16, total;
 };
 struct DecodeWs {
   size_t q32, attn16, h32, act16, part_ml, part_acc, counters, total;
@@ -86,11 +87,11 @@ struct DecodeWs {
 
 PrefillWs prefill_ws(const blk_config& c, int64_t T) {
   const size_t H = c.hidden, D = c.head_dim, Hq = c.n_heads, Hkv = c.n_kv_heads,
-               I = c.intermediate, N = (Hq + 2 * Hkv) * D;
+               I = c.intermediate;
+  (void)Hkv;
   PrefillWs w;
   size_t o = 0;
   w.xn16 = o; o = align_up(o + T * H * 2);
-  w.qkv32 = o; o = align_up(o + T * N * 4);
   w.q16 = o; o = align_up(o + T * Hq * D * 2);
   w.attn16 = o; o = align_up(o + T * Hq * D * 2);
   w.h32 = o; o = align_up(o + T * H * 4);
@@ -196,51 +197,47 @@ int run_prefill(blk_handle h, const blk_weights* w, const void* x,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   unsigned char* base = static_cast<unsigned char*>(ws);
   __half* xn16 = reinterpret_cast<__half*>(base + lay.xn16);
-  float* qkv32 = reinterpret_cast<float*>(base + lay.qkv32);
   __half* q16 = reinterpret_cast<__half*>(base + lay.q16);
   __half* attn16 = reinterpret_cast<__half*>(base + lay.attn16);
   float* h32 = reinterpret_cast<float*>(base + lay.h32);
   __half* hn16 = reinterpret_cast<__half*>(base + lay.hn16);
   __half* act16 = reinterpret_cast<__half*>(base + lay.act16);
   const int H = c.hidden, D = c.head_dim, Hq = c.n_heads, Hkv = c.n_kv_heads,
-            I = c.intermediate, NQKV = (Hq + 2 * Hkv) * D, M = (int)T;
+            I = c.intermediate, M = (int)T;
   const bool first_pdl = (h->flags & BLK_FLAG_CHAIN) != 0;
   Timer tm{h, s};
 
+  // RMSNorm 1
   BLK_LAUNCH(tm, kKRmsNorm,
              launch_rmsnorm_rows(x, false, static_cast<const __half*>(w->ln1_g), M, H,
                                  c.rms_eps, xn16, s, first_pdl));
-  const void* wqkv[3] = {w->wq, w->wk, w->wv};
-  const int ncols[3] = {Hq * D, Hkv * D, Hkv * D};
-  int col = 0;
-  for (int k = 0; k < 3; ++k) {
-    GemmParams g = {};
-    g.A = xn16;
-    g.B = static_cast<const __half*>(wqkv[k]);
-    g.M = M; g.N = ncols[k]; g.K = H;
-    g.outF32 = qkv32 + col;
-    g.ldo = NQKV;
-    BLK_LAUNCH(tm, kKGemmQKV, launch_gemm(g, kEpiStoreF32, s, true));
-    col += ncols[k];
-  }
-  RopeAppendParams ra = {};
-  ra.qkv32 = qkv32;
-  ra.bq = static_cast<const __half*>(c.has_qkv_bias ? w->bq : nullptr);
-  ra.bk = static_cast<const __half*>(c.has_qkv_bias ? w->bk : nullptr);
-  ra.bv = static_cast<const __half*>(c.has_qkv_bias ? w->bv : nullptr);
-  ra.pos = pos;
-  ra.rope = h->rope;
-  ra.rope_len = c.max_ctx;
-  ra.T = M; ra.Hq = Hq; ra.Hkv = Hkv; ra.D = D;
-  ra.cache_len = L; ra.max_ctx = c.max_ctx;
-  ra.q16 = q16;
-  ra.kc = static_cast<__half*>(k_cache);
-  ra.vc = static_cast<__half*>(v_cache);
-  ra.k_new = static_cast<__half*>(k_new);
-  ra.v_new = static_cast<__half*>(v_new);
-  ra.err = h->status;
-  BLK_LAUNCH(tm, kKRopeAppend, launch_rope_append(ra, s, true));
 
+  // QKV projection + bias + RoPE + KV append
+  TcGemmParams g = {};
+  if (make_tmap_2d(&g.tmA, xn16, M, H, 128) ||
+      make_tmap_2d(&g.tmB[0], w->wq, (int64_t)Hq * D, H, 128) ||
+      make_tmap_2d(&g.tmB[1], w->wk, (int64_t)Hkv * D, H, 128) ||
+      make_tmap_2d(&g.tmB[2], w->wv, (int64_t)Hkv * D, H, 128))
+    return BLK_ERR_CUDA;
+  g.M = M; g.N = (Hq + 2 * Hkv) * D; g.K = H;
+  g.seg_rows[0] = Hq * D; g.seg_rows[1] = Hkv * D; g.seg_rows[2] = Hkv * D;
+  if (c.has_qkv_bias) {
+    g.bias[0] = static_cast<const __half*>(w->bq);
+    g.bias[1] = static_cast<const __half*>(w->bk);
+    g.bias[2] = static_cast<const __half*>(w->bv);
+  }
+  g.pos = pos; g.rope = h->rope; g.rope_len = c.max_ctx;
+  g.Hq = Hq; g.Hkv = Hkv; g.D = D;
+  g.q16 = q16;
+  g.kc = static_cast<__half*>(k_cache);
+  g.vc = static_cast<__half*>(v_cache);
+  g.k_new = static_cast<__half*>(k_new);
+  g.v_new = static_cast<__half*>(v_new);
+  g.max_ctx = c.max_ctx; g.cache_len = L;
+  g.err = h->status;
+  BLK_LAUNCH(tm, kKGemmQKV, launch_tc_gemm(g, kTcQKV, h->num_sms, s, true));
+
+  // causal GQA attention over [history; new rows]
   PrefillAttnParams pa = {};
   pa.q16 = q16;
   pa.kc = static_cast<const __half*>(k_cache);
@@ -251,28 +248,41 @@ int run_prefill(blk_handle h, const blk_weights* w, const void* x,
   pa.attn16 = attn16;
   BLK_LAUNCH(tm, kKAttnPrefill, launch_prefill_attn(pa, s, true));
 
-  GemmParams go = {};
-  go.A = attn16; go.B = static_cast<const __half*>(w->wo);
+  // o_proj + residual -> h (fp32)
+  TcGemmParams go = {};
+  if (make_tmap_2d(&go.tmA, attn16, M, (int64_t)Hq * D, 128) ||
+      make_tmap_2d(&go.tmB[0], w->wo, H, (int64_t)Hq * D, 128))
+    return BLK_ERR_CUDA;
   go.M = M; go.N = H; go.K = Hq * D;
-  go.outF32 = h32; go.resF16 = static_cast<const __half*>(x); go.ldo = H;
-  BLK_LAUNCH(tm, kKGemmO, launch_gemm(go, kEpiResidF32, s, true));
+  go.res16 = static_cast<const __half*>(x); go.out32 = h32; go.ldo = H;
+  go.err = h->status;
+  BLK_LAUNCH(tm, kKGemmO, launch_tc_gemm(go, kTcResidF32, h->num_sms, s, true));
 
+  // RMSNorm 2
   BLK_LAUNCH(tm, kKRmsNorm,
              launch_rmsnorm_rows(h32, true, static_cast<const __half*>(w->ln2_g), M, H,
                                  c.rms_eps, hn16, s, true));
 
-  GemmParams gu = {};
-  gu.A = hn16; gu.B = static_cast<const __half*>(w->w_gate);
-  gu.B2 = static_cast<const __half*>(w->w_up);
+  // gate | up + SwiGLU
+  TcGemmParams gu = {};
+  if (make_tmap_2d(&gu.tmA, hn16, M, H, 128) ||
+      make_tmap_2d(&gu.tmB[0], w->w_gate, I, H, 128) ||
+      make_tmap_2d(&gu.tmB[1], w->w_up, I, H, 128))
+    return BLK_ERR_CUDA;
   gu.M = M; gu.N = I; gu.K = H;
-  gu.outF16 = act16; gu.ldo = I;
-  BLK_LAUNCH(tm, kKGemmGateUp, launch_gemm(gu, kEpiSwiGLU, s, true));
+  gu.out16 = act16; gu.ldo = I;
+  gu.err = h->status;
+  BLK_LAUNCH(tm, kKGemmGateUp, launch_tc_gemm(gu, kTcGateUp, h->num_sms, s, true));
 
-  GemmParams gd = {};
-  gd.A = act16; gd.B = static_cast<const __half*>(w->w_down);
+  // down + residual -> out
+  TcGemmParams gd = {};
+  if (make_tmap_2d(&gd.tmA, act16, M, I, 128) ||
+      make_tmap_2d(&gd.tmB[0], w->w_down, H, I, 128))
+    return BLK_ERR_CUDA;
   gd.M = M; gd.N = H; gd.K = I;
-  gd.outF16 = static_cast<__half*>(out); gd.resF32 = h32; gd.ldo = H;
-  BLK_LAUNCH(tm, kKGemmDown, launch_gemm(gd, kEpiResidOutF16, s, true));
+  gd.res32 = h32; gd.out16 = static_cast<__half*>(out); gd.ldo = H;
+  gd.err = h->status;
+  BLK_LAUNCH(tm, kKGemmDown, launch_tc_gemm(gd, kTcResidOutF16, h->num_sms, s, true));
   return BLK_OK;
 }
 
@@ -544,5 +554,8 @@ const char* blk_status_str(int status) {
 
 namespace blk {
 cudaError_t configure_gemv_kernels();
-cudaError_t configure_kernels() { return configure_gemv_kernels(); }
+cudaError_t configure_kernels() {
+  const cudaError_t e = configure_gemv_kernels();
+  return e != cudaSuccess ? e : configure_tc_gemm_kernels();
+}
 }  // namespace blk

@@ -1,0 +1,459 @@
+// Prefill projections on the 5th-generation tensor cores (tcgen05 + TMEM).
+//
+// D[m, n] = sum_k A[m, k] * B[n, k]: A = activations [M, K] fp16, B = weights
+// [N, K] fp16 (nn.Linear layout), both K-major; fp32 accumulation in TMEM.
+//
+// One persistent CTA per SM, 6 warps:
+//   warp 0   TMA producer: 128x64 A tiles and BNx64 B tiles, 128-byte
+//            swizzle, into a ring of shared-memory stages (mbarrier full /
+//            empty pairs).  Weight tiles of the first stages are issued before
+//            griddepcontrol.wait (they never depend on the previous kernel).
+//   warp 1   allocates TMEM (two accumulators of BN fp32 columns) and its lane
+//            0 issues tcgen05.mma.cta_group::1.kind::f16 (M=128, N=BN, K=16)
+//            four times per stage; tcgen05.commit frees the stage and, after
+//            the last stage of a tile, hands the accumulator to the epilogue.
+//   warps 2-5 epilogue: tcgen05.ld 32 columns at a time (thread = tile row),
+//            fused per projection:
+//              QKV    + bias, RoPE on q/k pairs (i, i+D/2), q -> fp16 buffer,
+//                     k/v -> cache slots cache_len + m and k_new / v_new
+//              O      + residual (block input, fp16) -> h (fp32)
+//              GATEUP B tile = 128 rows of W_gate over 128 rows of W_up,
+//                     silu(gate) * up -> activation (fp16)
+//              DOWN   + residual h (fp32) -> block output (fp16)
+//            and then release the accumulator, so the MMA of the next tile
+//            overlaps this epilogue.
+// Every mbarrier wait is bounded; on a timeout the CTA records an error,
+// stops issuing work, waits (bounded) for what it already issued and frees
+// its TMEM before returning.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "gemm_tc.h"
+
+namespace blk {
+
+namespace {
+
+constexpr int BM = 128, BK = 64;
+constexpr int kThreads = 192;
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map,
+                                            int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row atoms of
+// 1024 bytes (SBO), start address in 16-byte units, descriptor version 1.
+__device__ __forceinline__ uint64_t smem_desc_sw128(const void* p) {
+  const uint64_t addr = (smem_u32(p) & 0x3FFFFu) >> 4;
+  uint64_t d = addr;
+  d |= (uint64_t)1 << 16;            // leading byte offset (unused for SW128 K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;  // stride byte offset: 8 rows x 128 B
+  d |= (uint64_t)1 << 46;            // version
+  d |= (uint64_t)2 << 61;            // swizzle mode: 128B
+  return d;
+}
+
+// Instruction descriptor, kind::f16: D f32, A/B f16, both K-major, M x N.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b,
+                                        uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, "
+      "%9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, "
+      "%24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+        "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+        "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+        "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]),
+        "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void store_h32(__half* dst, const float* v) {
+  // 32 fp16 values, dst 16-byte aligned
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint4 u;
+    __half2* h = reinterpret_cast<__half2*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __floats2half2_rn(v[8 * j + 2 * i], v[8 * j + 2 * i + 1]);
+    d[j] = u;
+  }
+}
+
+template <int BN>
+struct Cfg {
+  static constexpr int kStages = BN == 256 ? 4 : 6;
+  static constexpr int kABytes = BM * BK * 2;
+  static constexpr int kBBytes = BN * BK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kTmemCols = 2 * BN;  // two accumulators
+  static constexpr size_t kSmem = (size_t)kStages * kStageBytes + 1024 + 256;
+};
+
+template <int EPI, int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ TcGemmParams p) {
+  using C = Cfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
+  uint64_t* empty = full + C::kStages;
+  uint64_t* tfull = empty + C::kStages;   // [2]
+  uint64_t* tempty = tfull + 2;           // [2]
+  uint64_t* drain = tempty + 2;           // [1], used only on the abort path
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int KB = (p.K + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    asm volatile(
+        "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+            smem_u32(tmem_slot)),
+        "r"((uint32_t)C::kTmemCols)
+        : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int it = 0;
+      bool waited = false;
+      for (int tile = blockIdx.x; tile < p.num_tiles && !*abort_flag; tile += gridDim.x) {
+        const int mt = tile % p.tiles_m, nt = tile / p.tiles_m;
+        const int m0 = mt * BM, n0 = nt * (EPI == kTcGateUp ? BN / 2 : BN);
+        int seg = 0, row0 = n0;
+        if (EPI == kTcQKV) {
+          while (seg < 2 && row0 >= p.seg_rows[seg]) row0 -= p.seg_rows[seg++];
+        }
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const int s = it % C::kStages;
+          if (!mbar_wait(&empty[s], ((it / C::kStages) & 1) ^ 1, p.err)) {
+            *abort_flag = 1;
+            break;
+          }
+          uint8_t* sa = smem + (size_t)s * C::kStageBytes;
+          uint8_t* sb = sa + C::kABytes;
+          mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+          if (EPI == kTcGateUp) {
+            tma_load_2d(sb, &p.tmB[0], kb * BK, row0, &full[s]);
+            tma_load_2d(sb + C::kBBytes / 2, &p.tmB[1], kb * BK, row0, &full[s]);
+          } else {
+            tma_load_2d(sb, &p.tmB[seg], kb * BK, row0, &full[s]);
+          }
+          if (!waited) {  // activations come from the previous kernel
+            griddep_wait();
+            griddep_launch();
+            waited = true;
+          }
+          tma_load_2d(sa, &p.tmA, kb * BK, m0, &full[s]);
+        }
+      }
+      if (!waited) {
+        griddep_wait();
+        griddep_launch();
+      }
+      if (*abort_flag) {
+        for (int k = max(0, it - C::kStages); k < it; ++k)
+          mbar_wait(&full[k % C::kStages], (k / C::kStages) & 1, nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_f16(BM, BN);
+      int it = 0, tcount = 0;
+      bool issued = false;
+      for (int tile = blockIdx.x; tile < p.num_tiles && !*abort_flag;
+           tile += gridDim.x, ++tcount) {
+        const int acc = tcount & 1;
+        if (!mbar_wait(&tempty[acc], ((tcount >> 1) & 1) ^ 1, p.err)) {
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const int s = it % C::kStages;
+          if (!mbar_wait(&full[s], (it / C::kStages) & 1, p.err)) {
+            *abort_flag = 1;
+            break;
+          }
+          tc_fence_after();
+          const uint8_t* sa = smem + (size_t)s * C::kStageBytes;
+          const uint64_t da = smem_desc_sw128(sa);
+          const uint64_t db = smem_desc_sw128(sa + C::kABytes);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)  // +32 bytes per K step inside the swizzle atom
+            mma_f16(d_tmem, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0);
+          issued = true;
+          mma_commit(&empty[s]);
+        }
+        if (*abort_flag) break;
+        mma_commit(&tfull[acc]);
+      }
+      if (*abort_flag && issued) {  // let issued MMAs finish before TMEM is freed
+        mma_commit(drain);
+        mbar_wait(drain, 0, nullptr);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    griddep_wait();
+    griddep_launch();
+    const int q = warp & 3;              // TMEM lane quarter this warp may access
+    const int row_in_tile = q * 32 + lane;
+    int tcount = 0;
+    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++tcount) {
+      const int acc = tcount & 1;
+      if (!mbar_wait(&tfull[acc], (tcount >> 1) & 1, p.err)) {
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const int mt = tile % p.tiles_m, nt = tile / p.tiles_m;
+      const int m = mt * BM + row_in_tile;
+      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
+      const bool row_ok = m < p.M;
+      float v0[32], v1[32];
+
+      if constexpr (EPI == kTcQKV) {
+        const int D = p.D, half = D / 2;
+        const int n0 = nt * BN;
+        const int64_t pos = row_ok ? p.pos[m] : 0;
+        for (int hh = 0; hh < BN / D; ++hh) {
+          const int hd = n0 / D + hh;  // head index over q | k | v
+          for (int c0 = 0; c0 < half; c0 += 32) {
+            tmem_ld32(tbase + hh * D + c0, v0);
+            tmem_ld32(tbase + hh * D + half + c0, v1);
+            if (!row_ok) continue;
+            const __half* bias;
+            int local;
+            if (hd < p.Hq) { bias = p.bias[0]; local = hd; }
+            else if (hd < p.Hq + p.Hkv) { bias = p.bias[1]; local = hd - p.Hq; }
+            else { bias = p.bias[2]; local = hd - p.Hq - p.Hkv; }
+            if (bias) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                v0[i] += __half2float(bias[local * D + c0 + i]);
+                v1[i] += __half2float(bias[local * D + half + c0 + i]);
+              }
+            }
+            if (hd < p.Hq + p.Hkv) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                const float2 cs = rope_cs(p.rope, p.rope_len, half, pos, c0 + i, p.err);
+                const float a = v0[i], b = v1[i];
+                v0[i] = a * cs.x - b * cs.y;
+                v1[i] = b * cs.x + a * cs.y;
+              }
+            }
+            if (hd < p.Hq) {
+              __half* dst = p.q16 + ((size_t)m * p.Hq + hd) * D;
+              store_h32(dst + c0, v0);
+              store_h32(dst + half + c0, v1);
+            } else {
+              const bool is_k = hd < p.Hq + p.Hkv;
+              __half* cache = is_k ? p.kc : p.vc;
+              __half* nw = is_k ? p.k_new : p.v_new;
+              __half* dst = cache + ((size_t)local * p.max_ctx + p.cache_len + m) * D;
+              store_h32(dst + c0, v0);
+              store_h32(dst + half + c0, v1);
+              if (nw) {
+                __half* d2 = nw + ((size_t)m * p.Hkv + local) * D;
+                store_h32(d2 + c0, v0);
+                store_h32(d2 + half + c0, v1);
+              }
+            }
+          }
+        }
+      } else if constexpr (EPI == kTcGateUp) {
+        const int j0 = nt * (BN / 2);
+        for (int c0 = 0; c0 < BN / 2; c0 += 32) {
+          tmem_ld32(tbase + c0, v0);
+          tmem_ld32(tbase + BN / 2 + c0, v1);
+          if (!row_ok) continue;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v0[i] = silu(v0[i]) * v1[i];
+          __half* dst = p.out16 + (size_t)m * p.ldo + j0 + c0;
+          if (j0 + c0 + 32 <= p.N) {
+            store_h32(dst, v0);
+          } else {
+            for (int i = 0; i < 32 && j0 + c0 + i < p.N; ++i) dst[i] = __float2half_rn(v0[i]);
+          }
+        }
+      } else {
+        const int n0 = nt * BN;
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          tmem_ld32(tbase + c0, v0);
+          if (!row_ok || n0 + c0 >= p.N) continue;
+          const size_t o = (size_t)m * p.ldo + n0 + c0;
+          if constexpr (EPI == kTcResidF32) {
+            const uint4* r = reinterpret_cast<const uint4*>(p.res16 + o);
+            float4* dst = reinterpret_cast<float4*>(p.out32 + o);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              float f[8];
+              h8_to_f32(r[j], f);
+              dst[2 * j] = make_float4(v0[8 * j] + f[0], v0[8 * j + 1] + f[1],
+                                       v0[8 * j + 2] + f[2], v0[8 * j + 3] + f[3]);
+              dst[2 * j + 1] = make_float4(v0[8 * j + 4] + f[4], v0[8 * j + 5] + f[5],
+                                           v0[8 * j + 6] + f[6], v0[8 * j + 7] + f[7]);
+            }
+          } else {
+            const float4* r = reinterpret_cast<const float4*>(p.res32 + o);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const float4 f = r[j];
+              v0[4 * j] += f.x;
+              v0[4 * j + 1] += f.y;
+              v0[4 * j + 2] += f.z;
+              v0[4 * j + 3] += f.w;
+            }
+            store_h32(p.out16 + o, v0);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"((uint32_t)C::kTmemCols)
+                 : "memory");
+  }
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------- host side
+
+int make_tmap_2d(CUtensorMap* map, const void* base, int64_t rows, int64_t K,
+                 int box_rows) {
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = cuTensorMapEncodeTiled(
+      map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+      estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : -1;
+}
+
+template <int EPI, int BN>
+static cudaError_t launch_tc(TcGemmParams& p, int num_sms, cudaStream_t s, bool pdl) {
+  using C = Cfg<BN>;
+  p.tiles_m = (p.M + BM - 1) / BM;
+  const int bn_out = EPI == kTcGateUp ? BN / 2 : BN;
+  p.tiles_n = (p.N + bn_out - 1) / bn_out;
+  p.num_tiles = p.tiles_m * p.tiles_n;
+  const int grid = p.num_tiles < num_sms ? p.num_tiles : num_sms;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<EPI, BN>, p);
+}
+
+cudaError_t launch_tc_gemm(TcGemmParams& p, int epi, int num_sms, cudaStream_t s,
+                           bool pdl) {
+  switch (epi) {
+    case kTcQKV: return launch_tc<kTcQKV, 128>(p, num_sms, s, pdl);
+    case kTcResidF32: return launch_tc<kTcResidF32, 128>(p, num_sms, s, pdl);
+    case kTcGateUp: return launch_tc<kTcGateUp, 256>(p, num_sms, s, pdl);
+    default: return launch_tc<kTcResidOutF16, 128>(p, num_sms, s, pdl);
+  }
+}
+
+cudaError_t configure_tc_gemm_kernels() {
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(tc_gemm_kernel<kTcQKV, 128>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)Cfg<128>::kSmem)))
+    return e;
+  if ((e = cudaFuncSetAttribute(tc_gemm_kernel<kTcResidF32, 128>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)Cfg<128>::kSmem)))
+    return e;
+  if ((e = cudaFuncSetAttribute(tc_gemm_kernel<kTcGateUp, 256>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)Cfg<256>::kSmem)))
+    return e;
+  return cudaFuncSetAttribute(tc_gemm_kernel<kTcResidOutF16, 128>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)Cfg<128>::kSmem);
+}
+
+}  // namespace blk

@@ -1,0 +1,54 @@
+// tcgen05 GEMM for the prefill projections (see gemm_tc.cu).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace blk {
+
+enum TcEpi {
+  kTcQKV = 0,          // + bias, RoPE, q -> q16, k/v -> cache + k_new/v_new
+  kTcResidF32 = 1,     // out32 = acc + res16         (o_proj)
+  kTcGateUp = 2,       // out16 = silu(gate) * up     (B = W_gate | W_up)
+  kTcResidOutF16 = 3   // out16 = acc + res32         (down)
+};
+
+struct TcGemmParams {
+  CUtensorMap tmA;      // activations [M, K]
+  CUtensorMap tmB[3];   // weights: QKV q/k/v; GATEUP gate/up; else [0]
+  int M, N, K;          // N: output columns (QKV: (Hq+2Hkv)*D; GATEUP: I)
+  int seg_rows[3];      // QKV: rows of wq, wk, wv
+  int tiles_m, tiles_n, num_tiles;  // set by the launcher
+  // QKV epilogue
+  const __half* bias[3];
+  const int64_t* pos;
+  const float2* rope;
+  int64_t rope_len;
+  int Hq, Hkv, D;
+  __half* q16;          // [M, Hq, D]
+  __half* kc;
+  __half* vc;
+  __half* k_new;
+  __half* v_new;
+  int64_t max_ctx, cache_len;
+  // other epilogues
+  const __half* res16;
+  const float* res32;
+  float* out32;
+  __half* out16;
+  int ldo;
+  int* err;
+};
+
+// 2-D tensor map over a row-major [rows, K] fp16 matrix, box 64 x box_rows,
+// 128-byte swizzle, zero fill out of bounds.  Returns 0 on success.
+int make_tmap_2d(CUtensorMap* map, const void* base, int64_t rows, int64_t K,
+                 int box_rows);
+
+cudaError_t launch_tc_gemm(TcGemmParams& p, int epi, int num_sms, cudaStream_t s,
+                           bool pdl);
+cudaError_t configure_tc_gemm_kernels();
+
+}  // namespace blk

@@ -85,46 +85,6 @@ cudaError_t launch_rmsnorm_rows(const void* x, bool x_is_f32, const __half* g,
                                 int rows, int H, float eps, __half* y,
                                 cudaStream_t s, bool pdl);
 
-// C[m, n] = sum_k A[m, k] * B[n, k] with an epilogue:
-enum GemmEpi {
-  kEpiStoreF32 = 0,    // outF32[m * ldo + n] = acc
-  kEpiResidF32 = 1,    // outF32[m * ldo + n] = acc + resF16[m * ldo + n]
-  kEpiSwiGLU = 2,      // outF16[m * ldo + n] = silu(acc) * acc(B2)
-  kEpiResidOutF16 = 3  // outF16[m * ldo + n] = acc + resF32[m * ldo + n]
-};
-struct GemmParams {
-  const __half* A;
-  const __half* B;
-  const __half* B2;
-  int M, N, K;
-  float* outF32;
-  __half* outF16;
-  const __half* resF16;
-  const float* resF32;
-  int ldo;
-};
-cudaError_t launch_gemm(const GemmParams& p, int epi, cudaStream_t s, bool pdl);
-
-struct RopeAppendParams {
-  const float* qkv32;  // [T, (Hq + 2 Hkv) * D]
-  const __half* bq;
-  const __half* bk;
-  const __half* bv;
-  const int64_t* pos;
-  const float2* rope;
-  int64_t rope_len;
-  int T, Hq, Hkv, D;
-  int64_t cache_len, max_ctx;
-  __half* q16;   // [T, Hq, D]
-  __half* kc;
-  __half* vc;
-  __half* k_new;
-  __half* v_new;
-  int* err;
-};
-cudaError_t launch_rope_append(const RopeAppendParams& p, cudaStream_t s,
-                               bool pdl);
-
 struct PrefillAttnParams {
   const __half* q16;  // [T, Hq, D]
   const __half* kc;

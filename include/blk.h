@@ -62,9 +62,9 @@ extern "C" {
 #define BLK_ERR_DEVICE (-9)          /* the current GPU is not sm_103 (GB300)   */
 
 /* Block shape.  Supported: head_dim 64 or 128; n_heads % n_kv_heads == 0 with
- * group size n_heads / n_kv_heads in {1, 2, 4, 6, 8, 16}; hidden and
- * intermediate multiples of 64 and at most 16384; n_heads*head_dim multiple
- * of 64; max_ctx >= 1. */
+ * group size n_heads / n_kv_heads in {1, 2, 4, 6, 8, 16}; hidden a multiple
+ * of 64, intermediate a multiple of 8, both at most 16384; n_heads*head_dim
+ * a multiple of 64; max_ctx >= 1. */
 typedef struct {
   int32_t hidden;
   int32_t n_heads;

@@ -59,11 +59,11 @@ def test_null_handle_and_arguments_are_rejected(lib):
 
 
 @pytest.mark.parametrize("bad", [
-    dict(head_dim=96), dict(n_heads=5), dict(hidden=200), dict(intermediate=100),
+    dict(head_dim=96), dict(n_heads=5), dict(hidden=200), dict(intermediate=100), dict(intermediate=684),
     dict(max_ctx=0), dict(n_heads=12, n_kv_heads=1), dict(hidden=32768), dict(rope_theta=0.0),
 ])
 def test_bad_shapes_rejected_before_any_device_call(lib, bad):
-    base = dict(hidden=256, n_heads=4, n_kv_heads=2, head_dim=64, intermediate=704,
+    base = dict(hidden=256, n_heads=4, n_kv_heads=2, head_dim=64, intermediate=688,
                 rms_eps=1e-6, rope_theta=1e4, max_ctx=64, has_qkv_bias=0)
     base.update(bad)
     cfg = blk.BlkConfig(**base)
