@@ -27,11 +27,13 @@ BLK_ERR_CUDA = -6
 BLK_ERR_DEVICE_TIMEOUT = -7
 BLK_ERR_POSITION = -8
 BLK_ERR_DEVICE = -9
+BLK_ERR_SCRATCH_LIMIT = -10
+BLK_STATIC_SCRATCH_BYTES = 1 << 20
 BLK_FLAG_CHAIN = 1
 
 EXPORTED = ("blk_create", "blk_destroy", "blk_set_flags", "blk_workspace_bytes", "blk_prefill",
             "blk_prefill_kv", "blk_decode", "blk_check", "blk_status_str", "blk_timing",
-            "blk_timing_collect", "blk_timing_read")
+            "blk_timing_collect", "blk_timing_read", "blk_decode_static")
 BLK_N_KERNELS = 16
 
 WEIGHT_FIELDS = ("ln1_g", "wq", "wk", "wv", "bq", "bk", "bv", "wo", "ln2_g", "w_gate", "w_up",
@@ -88,6 +90,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.blk_decode.argtypes = [vp, ctypes.POINTER(BlkWeights), vp, vp, i64, vp, vp, vp, vp, vp,
                                vp, ctypes.c_size_t, vp]
     lib.blk_decode.restype = i32
+    lib.blk_decode_static.argtypes = [vp, ctypes.POINTER(BlkWeights), vp, vp, i64, vp, vp, vp, vp,
+                                      vp, vp]
+    lib.blk_decode_static.restype = i32
     lib.blk_check.argtypes = [vp, vp]
     lib.blk_check.restype = i32
     lib.blk_status_str.argtypes = [i32]
@@ -145,6 +150,14 @@ def blk_decode(handle, w: BlkWeights, x, pos, cache_len, k_cache, v_cache, out, 
                ws_bytes, stream) -> int:
     return load().blk_decode(handle, ctypes.byref(w), x, pos, cache_len, k_cache, v_cache, out,
                              k_new, v_new, ws, ws_bytes, stream)
+
+
+def blk_decode_static(handle, w: BlkWeights, x, pos, cache_len, k_cache, v_cache, out, k_new,
+                      v_new, stream) -> int:
+    """Decode with the library's fixed device scratch instead of a workspace
+    (for callers that cannot allocate device memory; see include/blk.h)."""
+    return load().blk_decode_static(handle, ctypes.byref(w), x, pos, cache_len, k_cache, v_cache,
+                                    out, k_new, v_new, stream)
 
 
 def blk_check(handle, stream) -> int:

@@ -9,6 +9,7 @@
 
 #include "../../include/blk.h"
 #include "common.cuh"
+#include "blk_internal.h"
 #include "gemm_tc.h"
 #include "kernels.h"
 
@@ -495,6 +496,16 @@ int blk_check(blk_handle h, void* stream) {
   return BLK_OK;
 }
 
+}  // extern "C"
+
+size_t blk_internal_decode_ws_bytes(blk_handle h) {
+  return decode_ws(h->cfg, h->max_splits).total;
+}
+
+int blk_internal_device(blk_handle h) { return h->device; }
+
+extern "C" {
+
 int blk_timing(blk_handle h, int on) {
   if (!h) return BLK_ERR_NULL;
   if (on && !h->ev) {
@@ -546,6 +557,8 @@ const char* blk_status_str(int status) {
     case BLK_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait timed out";
     case BLK_ERR_POSITION: return "a position id was outside [0, max_ctx) and was clamped";
     case BLK_ERR_DEVICE: return "the current GPU is not sm_103 (GB300)";
+    case BLK_ERR_SCRATCH_LIMIT:
+      return "the shape needs more decode scratch than blk_decode_static's fixed 1 MiB array";
     default: return "unknown status";
   }
 }

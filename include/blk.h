@@ -60,6 +60,8 @@ extern "C" {
 #define BLK_ERR_DEVICE_TIMEOUT (-7)  /* a bounded device-side wait gave up      */
 #define BLK_ERR_POSITION (-8)        /* a position id outside [0, max_ctx)      */
 #define BLK_ERR_DEVICE (-9)          /* the current GPU is not sm_103 (GB300)   */
+#define BLK_ERR_SCRATCH_LIMIT (-10)  /* shape needs more scratch than
+                                        blk_decode_static's fixed array holds   */
 
 /* Block shape.  Supported: head_dim 64 or 128; n_heads % n_kv_heads == 0 with
  * group size n_heads / n_kv_heads in {1, 2, 4, 6, 8, 16}; hidden a multiple
@@ -142,6 +144,41 @@ int blk_decode(blk_handle h, const blk_weights* w, const void* x,
                const int64_t* pos, int64_t cache_len, void* k_cache,
                void* v_cache, void* out, void* k_new, void* v_new, void* ws,
                size_t ws_bytes, void* stream);
+
+/* blk_decode_static — decode without a workspace argument, for callers that
+ * cannot allocate device memory.  (The paper has no counterpart: this entry
+ * point exists only for such callers.)
+ *
+ * Some callers may not call cudaMalloc or any allocating routine: a plugin
+ * running inside a host framework whose memory manager owns all device memory
+ * and rejects outside allocations, or a latency-critical serving loop, where
+ * cudaMalloc / cudaFree can synchronize the whole device.  This entry point
+ * takes the same inputs and outputs as blk_decode but uses, as its scratch, a
+ * fixed array of BLK_STATIC_SCRATCH_BYTES (1 MiB) compiled into the library
+ * as a __device__ variable.  Every GPU that loads the library holds that
+ * array until the process exits.  It allocates nothing: no cudaMalloc, no
+ * cudaFree, no allocating library routine.
+ *
+ * Limit: a shape whose decode scratch (the same bytes blk_decode would need
+ * from its workspace) exceeds BLK_STATIC_SCRATCH_BYTES is rejected with
+ * BLK_ERR_SCRATCH_LIMIT before anything is enqueued.  The 1.5B shape needs
+ * about 0.5 MiB; the hidden-4096 / 32-head shape needs about 1.3 MiB and is
+ * rejected.
+ *
+ * Set-up: the first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and caches it; make that
+ * first call before any stream capture begins.
+ *
+ * Sharing: all calls on a device share the one array and it keeps the last
+ * call's contents (the kernels clear what must start at zero).  Calls whose
+ * work overlaps on the GPU — on different streams, or from different
+ * handles — race on the array; serialize them (one stream, or events).
+ * Return codes are those of blk_decode plus BLK_ERR_SCRATCH_LIMIT. */
+#define BLK_STATIC_SCRATCH_BYTES ((size_t)1 << 20)
+int blk_decode_static(blk_handle h, const blk_weights* w, const void* x,
+                      const int64_t* pos, int64_t cache_len, void* k_cache,
+                      void* v_cache, void* out, void* k_new, void* v_new,
+                      void* stream);
 
 /* Synchronizes `stream`, then reports and clears the handle's device status
  * word: BLK_OK, BLK_ERR_DEVICE_TIMEOUT or BLK_ERR_POSITION (a kernel clamped
