@@ -33,7 +33,8 @@ BLK_FLAG_CHAIN = 1
 
 EXPORTED = ("blk_create", "blk_destroy", "blk_set_flags", "blk_workspace_bytes", "blk_prefill",
             "blk_prefill_kv", "blk_decode", "blk_check", "blk_status_str", "blk_timing",
-            "blk_timing_collect", "blk_timing_read", "blk_decode_static")
+            "blk_timing_collect", "blk_timing_read", "blk_decode_static", "blk_decode_stack",
+            "blk_set_trace")
 BLK_N_KERNELS = 16
 
 WEIGHT_FIELDS = ("ln1_g", "wq", "wk", "wv", "bq", "bk", "bv", "wo", "ln2_g", "w_gate", "w_up",
@@ -90,6 +91,12 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.blk_decode.argtypes = [vp, ctypes.POINTER(BlkWeights), vp, vp, i64, vp, vp, vp, vp, vp,
                                vp, ctypes.c_size_t, vp]
     lib.blk_decode.restype = i32
+    lib.blk_set_trace.argtypes = [vp, vp, ctypes.c_size_t]
+    lib.blk_set_trace.restype = i32
+    lib.blk_decode_stack.argtypes = [vp, ctypes.POINTER(BlkWeights), i32, ctypes.POINTER(vp),
+                                     ctypes.POINTER(vp), vp, vp, i64, vp, ctypes.POINTER(vp),
+                                     ctypes.POINTER(vp), vp, ctypes.c_size_t, vp]
+    lib.blk_decode_stack.restype = i32
     lib.blk_decode_static.argtypes = [vp, ctypes.POINTER(BlkWeights), vp, vp, i64, vp, vp, vp, vp,
                                       vp, vp]
     lib.blk_decode_static.restype = i32
@@ -150,6 +157,17 @@ def blk_decode(handle, w: BlkWeights, x, pos, cache_len, k_cache, v_cache, out, 
                ws_bytes, stream) -> int:
     return load().blk_decode(handle, ctypes.byref(w), x, pos, cache_len, k_cache, v_cache, out,
                              k_new, v_new, ws, ws_bytes, stream)
+
+
+def blk_set_trace(handle, buf_ptr, nbytes) -> int:
+    return load().blk_set_trace(handle, buf_ptr, nbytes)
+
+
+def blk_decode_stack(handle, w_array, n_layers, k_caches, v_caches, x, pos, cache_len, out,
+                     k_new, v_new, ws, ws_bytes, stream) -> int:
+    """w_array: (BlkWeights * n); k_caches/v_caches/k_new/v_new: (c_void_p * n) or None."""
+    return load().blk_decode_stack(handle, w_array, n_layers, k_caches, v_caches, x, pos,
+                                   cache_len, out, k_new, v_new, ws, ws_bytes, stream)
 
 
 def blk_decode_static(handle, w: BlkWeights, x, pos, cache_len, k_cache, v_cache, out, k_new,

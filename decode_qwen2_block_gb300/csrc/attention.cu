@@ -1,17 +1,9 @@
-// Causal GQA attention over the fp16 KV cache.
-//
-// Decode (one query token): split-K "flash-decode".  CTA (g, s) takes kv
-// head g and slot range s of [0, n_keys); its 4 warps each stream part of the
-// range and keep, for all G = Hq/Hkv query heads of the group, the running
-// max m, sum l and unnormalised output (online softmax, base-2 exponent with
-// log2(e)/sqrt(D) folded into q).  The CTA merges its warps and writes one
-// partial per query head; the last CTA of kv head g to finish (atomic
-// counter, zeroed by the preceding QKV kernel) merges all partials into the
-// normalised output.  Scores use one lane per slot (a full K row per lane, q
+// Causal GQA attention over the fp16 KV cache for prefill / prefill_kv: one
+// warp per (new row t, kv head g) over slots [0, cache_len + t], keeping for
+// all G = Hq/Hkv query heads of the group the running max, sum and
+// unnormalised output (online softmax, base-2 exponent with log2(e)/sqrt(D)
+// folded into q).  Scores use one lane per slot (a full K row per lane, q
 // broadcast from shared memory); the V accumulation uses lanes along D.
-//
-// Prefill / prefill_kv: one warp per (new row t, kv head g) over slots
-// [0, cache_len + t], same per-warp routine.
 #include <math.h>
 
 #include "common.cuh"
@@ -100,99 +92,6 @@ __device__ __forceinline__ void init_state(WarpState<G, D>& st) {
   }
 }
 
-constexpr int kDecWarps = 4;
-
-template <int G, int D>
-__global__ void __launch_bounds__(kDecWarps * 32)
-    decode_attn_kernel(const __grid_constant__ DecodeAttnParams p) {
-  __shared__ __align__(16) float q_s[G * D];
-  __shared__ float sm_m[kDecWarps][G], sm_l[kDecWarps][G];
-  __shared__ __align__(16) float sm_acc[kDecWarps][G][D];
-  __shared__ int is_last;
-  const int g = blockIdx.x / p.splits, s = blockIdx.x % p.splits;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr int DPL = D / 32;
-
-  griddep_wait();
-  griddep_launch();
-
-  for (int i = threadIdx.x; i < G * D; i += blockDim.x)
-    q_s[i] = p.q32[g * G * D + i] * p.scale_log2;
-  __syncthreads();
-
-  const int64_t j0 = (int64_t)s * p.slots_per_split;
-  const int64_t j1 = min(p.n_keys, j0 + p.slots_per_split);
-  const int64_t len = j1 - j0;
-  const int64_t w0 = j0 + len * warp / kDecWarps, w1 = j0 + len * (warp + 1) / kDecWarps;
-  WarpState<G, D> st;
-  init_state(st);
-  const size_t head_off = (size_t)g * p.max_ctx * D;
-  warp_attend<G, D>(q_s, p.kc + head_off, p.vc + head_off, w0, w1, st);
-
-  if (lane == 0) {
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      sm_m[warp][h] = st.m[h];
-      sm_l[warp][h] = st.l[h];
-    }
-  }
-#pragma unroll
-  for (int h = 0; h < G; ++h)
-#pragma unroll
-    for (int e = 0; e < DPL; ++e) sm_acc[warp][h][lane * DPL + e] = st.acc[h][e];
-  __syncthreads();
-
-  // Merge the CTA's warps: one thread per (h, d).
-  for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
-    const int h = i / D, d = i % D;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, sm_m[w][h]);
-    float Lsum = 0.f, O = 0.f;
-#pragma unroll
-    for (int w = 0; w < kDecWarps; ++w) {
-      const float c = exp2f(sm_m[w][h] - M);
-      Lsum += sm_l[w][h] * c;
-      O += sm_acc[w][h][d] * c;
-    }
-    const int hq = g * G + h;
-    if (p.splits == 1) {
-      p.attn16[hq * D + d] = __float2half_rn(O / Lsum);
-    } else {
-      p.part_acc[((size_t)hq * p.splits + s) * D + d] = O;
-      if (d == 0) p.part_ml[(size_t)hq * p.splits + s] = make_float2(M, Lsum);
-    }
-  }
-  if (p.splits == 1) return;
-
-  // Last CTA of this kv head merges every split.
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const unsigned prev = atomicAdd(&p.counters[g], 1u);
-    is_last = (prev == (unsigned)p.splits - 1u);
-  }
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
-  for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
-    const int h = i / D, d = i % D;
-    const int hq = g * G + h;
-    const float2* ml = p.part_ml + (size_t)hq * p.splits;
-    const float* acc = p.part_acc + (size_t)hq * p.splits * D + d;
-    float M = -INFINITY;
-    for (int k = 0; k < p.splits; ++k) M = fmaxf(M, __ldcg(&ml[k].x));
-    float Lsum = 0.f, O = 0.f;
-    for (int k = 0; k < p.splits; ++k) {
-      const float2 v = __ldcg(&ml[k]);
-      const float c = exp2f(v.x - M);
-      Lsum += v.y * c;
-      O += __ldcg(acc + (size_t)k * D) * c;
-    }
-    p.attn16[hq * D + d] = __float2half_rn(O / Lsum);
-  }
-}
-
 template <int G, int D>
 __global__ void __launch_bounds__(32)
     prefill_attn_simple_kernel(const __grid_constant__ PrefillAttnParams p) {
@@ -219,38 +118,6 @@ __global__ void __launch_bounds__(32)
 }
 
 // ---------------------------------------------------------------- host side
-
-void decode_attn_splits(int64_t n_keys, int Hkv, int num_sms, int* splits,
-                        int* slots_per_split) {
-  const int64_t max_splits = decode_attn_max_splits(n_keys, Hkv, num_sms);
-  int64_t want = (n_keys + 63) / 64;  // at least 64 slots per CTA
-  if (want > max_splits) want = max_splits;
-  if (want < 1) want = 1;
-  const int64_t sps = (n_keys + want - 1) / want;
-  *slots_per_split = (int)sps;
-  *splits = (int)((n_keys + sps - 1) / sps);
-}
-
-int decode_attn_max_splits(int64_t max_ctx, int Hkv, int num_sms) {
-  int64_t m = (num_sms + Hkv - 1) / Hkv;
-  const int64_t by_len = (max_ctx + 63) / 64;
-  if (m > by_len) m = by_len;
-  return (int)(m < 1 ? 1 : m);
-}
-
-template <int G, int D>
-static cudaError_t launch_dec(const DecodeAttnParams& p, cudaStream_t s, bool pdl) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.Hkv * p.splits);
-  cfg.blockDim = dim3(kDecWarps * 32);
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, decode_attn_kernel<G, D>, p);
-}
 
 template <int G, int D>
 static cudaError_t launch_pre(const PrefillAttnParams& p, cudaStream_t s, bool pdl) {
@@ -290,10 +157,6 @@ static cudaError_t launch_pre(const PrefillAttnParams& p, cudaStream_t s, bool p
     }                                                          \
     return cudaErrorInvalidValue;                              \
   } while (0)
-
-cudaError_t launch_decode_attn(const DecodeAttnParams& p, cudaStream_t s, bool pdl) {
-  BLK_GD_DISPATCH(launch_dec, p, s, pdl);
-}
 
 cudaError_t launch_prefill_attn(const PrefillAttnParams& p, cudaStream_t s, bool pdl) {
   BLK_GD_DISPATCH(launch_pre, p, s, pdl);

@@ -10,6 +10,7 @@
 #include "../../include/blk.h"
 #include "common.cuh"
 #include "blk_internal.h"
+#include "decode_persistent.h"
 #include "gemm_tc.h"
 #include "kernels.h"
 
@@ -20,13 +21,12 @@ constexpr int kMaxPending = 1024;
 // Kernel ids for per-kernel timing (blk_timing_read).
 enum KernelId {
   kKRmsNorm = 0, kKGemmQKV, kKRopeAppend, kKAttnPrefill, kKGemmO, kKGemmGateUp,
-  kKGemmDown, kKGemvQKV, kKAttnDecode, kKGemvO, kKGemvGateUp, kKGemvDown,
-  kKCount
+  kKGemmDown, kKDecodeStep, kKCount
 };
 const char* const kKernelNames[BLK_N_KERNELS] = {
-    "rmsnorm_rows", "gemm_qkv", "rope_append", "attn_prefill", "gemm_o",
-    "gemm_gateup", "gemm_down", "gemv_qkv_rope_append", "attn_decode_splitk",
-    "gemv_o", "gemv_gateup", "gemv_down", "", "", "", ""};
+    "rmsnorm_rows", "gemm_qkv", "(unused)", "attn_prefill", "gemm_o",
+    "gemm_gateup", "gemm_down", "decode_persistent", "", "", "", "",
+    "", "", "", ""};
 }  // namespace
 
 struct blk_handle_s {
@@ -36,7 +36,10 @@ struct blk_handle_s {
   float2* rope;   // [max_ctx][head_dim / 2] (cos, sin)
   int* status;    // device status word
   uint32_t flags;
-  int max_splits; // decode attention splits at max_ctx
+  bool decode_ok;  // shape fits the persistent decode kernel
+  blk::DecodeParams* dec;  // parameter block of the decode launch
+  uint64_t* trace;         // optional decode timeline buffer
+  size_t trace_len;
   // per-kernel timing
   bool timing;
   bool overflow;
@@ -82,9 +85,6 @@ int shape_ok(const blk_config* c) {
 struct PrefillWs {
   size_t xn16, q16, attn16, h32, hn16, act16, total;
 };
-struct DecodeWs {
-  size_t q32, attn16, h32, act16, part_ml, part_acc, counters, total;
-};
 
 PrefillWs prefill_ws(const blk_config& c, int64_t T) {
   const size_t H = c.hidden, D = c.head_dim, Hq = c.n_heads, Hkv = c.n_kv_heads,
@@ -102,21 +102,6 @@ PrefillWs prefill_ws(const blk_config& c, int64_t T) {
   return w;
 }
 
-DecodeWs decode_ws(const blk_config& c, int max_splits) {
-  const size_t H = c.hidden, D = c.head_dim, Hq = c.n_heads, Hkv = c.n_kv_heads,
-               I = c.intermediate, S = max_splits;
-  DecodeWs w;
-  size_t o = 0;
-  w.q32 = o; o = align_up(o + Hq * D * 4);
-  w.attn16 = o; o = align_up(o + Hq * D * 2);
-  w.h32 = o; o = align_up(o + H * 4);
-  w.act16 = o; o = align_up(o + I * 2);
-  w.part_ml = o; o = align_up(o + Hq * S * 8);
-  w.part_acc = o; o = align_up(o + Hq * S * D * 4);
-  w.counters = o; o = align_up(o + Hkv * 4);
-  w.total = o;
-  return w;
-}
 
 int check_weights(const blk_config& c, const blk_weights* w) {
   if (!w) return BLK_ERR_NULL;
@@ -311,7 +296,23 @@ int blk_create(const blk_config* cfg, blk_handle* out) {
   h->cfg = *cfg;
   h->device = dev;
   h->num_sms = sms;
-  h->max_splits = decode_attn_max_splits(cfg->max_ctx, cfg->n_kv_heads, sms);
+  {
+    // the decode kernel stages at most kDecMaxVec inputs and 150 weight rows
+    // per CTA and phase (one CTA per SM)
+    const int64_t rows_qkv = 2 * (((int64_t)(cfg->n_heads + 2 * cfg->n_kv_heads) *
+                                   (cfg->head_dim / 2) + sms - 1) / sms);
+    const int64_t rows_gu = 2 * ((cfg->intermediate + sms - 1) / sms);
+    const int64_t rows_h = (cfg->hidden + sms - 1) / sms;
+    h->decode_ok = cfg->hidden <= kDecMaxVec && cfg->intermediate <= kDecMaxVec &&
+                   cfg->n_heads * cfg->head_dim <= kDecMaxVec && cfg->n_kv_heads <= sms &&
+                   cfg->n_heads / cfg->n_kv_heads <= 16 && rows_qkv <= 150 &&
+                   rows_gu <= 150 && rows_h <= 150 && cfg->intermediate % 16 == 0;
+  }
+  h->dec = new (std::nothrow) blk::DecodeParams();
+  if (!h->dec) {
+    delete h;
+    return BLK_ERR_CUDA;
+  }
 
   const int half = cfg->head_dim / 2;
   std::vector<float2> table((size_t)cfg->max_ctx * half);
@@ -342,6 +343,7 @@ void blk_destroy(blk_handle h) {
     for (int i = 0; i < 2 * kMaxPending; ++i) cudaEventDestroy(h->ev[i]);
     delete[] h->ev;
   }
+  delete h->dec;
   delete h;
 }
 
@@ -353,8 +355,10 @@ int blk_set_flags(blk_handle h, uint32_t flags) {
 
 size_t blk_workspace_bytes(blk_handle h, int64_t max_T) {
   if (!h || max_T < 1) return 0;
-  const size_t a = prefill_ws(h->cfg, max_T).total;
-  const size_t b = decode_ws(h->cfg, h->max_splits).total;
+  const blk_config& c = h->cfg;
+  const size_t a = prefill_ws(c, max_T).total;
+  const size_t b = decode_ws_bytes(c.hidden, c.n_heads, c.n_kv_heads, c.head_dim,
+                                   c.intermediate, h->num_sms);
   return a > b ? a : b;
 }
 
@@ -378,108 +382,79 @@ int blk_decode(blk_handle h, const blk_weights* w, const void* x,
                const int64_t* pos, int64_t cache_len, void* k_cache,
                void* v_cache, void* out, void* k_new, void* v_new, void* ws,
                size_t ws_bytes, void* stream) {
-  int rc = check_call(h, w, x, pos, 1, cache_len, k_cache, v_cache, out, k_new,
-                      v_new, ws);
-  if (rc) return rc;
-  const blk_config& c = h->cfg;
-  const DecodeWs lay = decode_ws(c, h->max_splits);
-  if (ws_bytes < lay.total) return BLK_ERR_WORKSPACE;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  unsigned char* base = static_cast<unsigned char*>(ws);
-  float* q32 = reinterpret_cast<float*>(base + lay.q32);
-  __half* attn16 = reinterpret_cast<__half*>(base + lay.attn16);
-  float* h32 = reinterpret_cast<float*>(base + lay.h32);
-  __half* act16 = reinterpret_cast<__half*>(base + lay.act16);
-  float2* part_ml = reinterpret_cast<float2*>(base + lay.part_ml);
-  float* part_acc = reinterpret_cast<float*>(base + lay.part_acc);
-  unsigned* counters = reinterpret_cast<unsigned*>(base + lay.counters);
-  const int H = c.hidden, D = c.head_dim, Hq = c.n_heads, Hkv = c.n_kv_heads,
-            I = c.intermediate;
-  const bool first_pdl = (h->flags & BLK_FLAG_CHAIN) != 0;
-  Timer tm{h, s};
+  void* kcs[1] = {k_cache};
+  void* vcs[1] = {v_cache};
+  void* kns[1] = {k_new};
+  void* vns[1] = {v_new};
+  return blk_decode_stack(h, w, 1, kcs, vcs, x, pos, cache_len, out, kns, vns, ws, ws_bytes,
+                          stream);
+}
 
-  GemvParams g = {};
-  g.W[0] = static_cast<const __half*>(w->wq);
-  g.W[1] = static_cast<const __half*>(w->wk);
-  g.W[2] = static_cast<const __half*>(w->wv);
-  if (c.has_qkv_bias) {
-    g.bias[0] = static_cast<const __half*>(w->bq);
-    g.bias[1] = static_cast<const __half*>(w->bk);
-    g.bias[2] = static_cast<const __half*>(w->bv);
+int blk_decode_stack(blk_handle h, const blk_weights* w, int n_layers,
+                     void* const* k_caches, void* const* v_caches, const void* x,
+                     const int64_t* pos, int64_t cache_len, void* out,
+                     void* const* k_new, void* const* v_new, void* ws, size_t ws_bytes,
+                     void* stream) {
+  if (!h || !w || !k_caches || !v_caches) return BLK_ERR_NULL;
+  if (n_layers < 1) return BLK_ERR_SHAPE;
+  if (!h->decode_ok) return BLK_ERR_SHAPE;
+  for (int l = 0; l < n_layers; ++l) {
+    const int rc = check_call(h, &w[l], x, pos, 1, cache_len, k_caches[l], v_caches[l], out,
+                              k_new ? k_new[l] : nullptr, v_new ? v_new[l] : nullptr, ws);
+    if (rc) return rc;
   }
-  g.K = H;
-  g.x16 = static_cast<const __half*>(x);
-  g.gain = static_cast<const __half*>(w->ln1_g);
-  g.eps = c.rms_eps;
-  g.Hq = Hq; g.Hkv = Hkv; g.D = D;
-  const int heads = Hq + 2 * Hkv;
-  int parts = h->num_sms / heads;
-  if (parts < 1) parts = 1;
-  if (parts > D / 2) parts = D / 2;
-  g.parts = parts;
-  g.pos = pos;
-  g.rope = h->rope;
-  g.rope_len = c.max_ctx;
-  g.kc = static_cast<__half*>(k_cache);
-  g.vc = static_cast<__half*>(v_cache);
-  g.max_ctx = c.max_ctx;
-  g.slot = cache_len;
-  g.k_new = static_cast<__half*>(k_new);
-  g.v_new = static_cast<__half*>(v_new);
-  g.q32 = q32;
-  g.counters = counters;
-  g.n_counters = Hkv;
-  g.err = h->status;
-  BLK_LAUNCH(tm, kKGemvQKV,
-             launch_gemv(g, kGemvQKV, gemv_grid(g, kGemvQKV, h->num_sms), s, first_pdl));
-
-  DecodeAttnParams da = {};
-  da.q32 = q32;
-  da.kc = static_cast<const __half*>(k_cache);
-  da.vc = static_cast<const __half*>(v_cache);
-  da.max_ctx = c.max_ctx;
-  da.n_keys = cache_len + 1;
-  da.Hq = Hq; da.Hkv = Hkv; da.D = D;
-  decode_attn_splits(da.n_keys, Hkv, h->num_sms, &da.splits, &da.slots_per_split);
-  if (da.splits > h->max_splits) return BLK_ERR_WORKSPACE;
-  da.part_ml = part_ml;
-  da.part_acc = part_acc;
-  da.counters = counters;
-  da.attn16 = attn16;
-  da.scale_log2 = (float)(1.4426950408889634 / sqrt((double)D));
-  da.err = h->status;
-  BLK_LAUNCH(tm, kKAttnDecode, launch_decode_attn(da, s, true));
-
-  GemvParams go = {};
-  go.W[0] = static_cast<const __half*>(w->wo);
-  go.K = Hq * D; go.N = H;
-  go.x16 = attn16;
-  go.res16 = static_cast<const __half*>(x);
-  go.out32 = h32;
-  go.err = h->status;
-  BLK_LAUNCH(tm, kKGemvO, launch_gemv(go, kGemvO, gemv_grid(go, kGemvO, h->num_sms), s, true));
-
-  GemvParams gu = {};
-  gu.W[0] = static_cast<const __half*>(w->w_gate);
-  gu.W[1] = static_cast<const __half*>(w->w_up);
-  gu.K = H; gu.N = I;
-  gu.x32 = h32;
-  gu.gain = static_cast<const __half*>(w->ln2_g);
-  gu.eps = c.rms_eps;
-  gu.out16 = act16;
-  gu.err = h->status;
-  BLK_LAUNCH(tm, kKGemvGateUp,
-             launch_gemv(gu, kGemvGateUp, gemv_grid(gu, kGemvGateUp, h->num_sms), s, true));
-
-  GemvParams gd = {};
-  gd.W[0] = static_cast<const __half*>(w->w_down);
-  gd.K = I; gd.N = H;
-  gd.x16 = act16;
-  gd.res32 = h32;
-  gd.out16 = static_cast<__half*>(out);
-  gd.err = h->status;
-  BLK_LAUNCH(tm, kKGemvDown,
-             launch_gemv(gd, kGemvDown, gemv_grid(gd, kGemvDown, h->num_sms), s, true));
+  const blk_config& c = h->cfg;
+  if (ws_bytes < decode_ws_bytes(c.hidden, c.n_heads, c.n_kv_heads, c.head_dim,
+                                 c.intermediate, h->num_sms))
+    return BLK_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Timer tm{h, s};
+  // DecodeParams holds the tensor maps and pointers of up to kDecMaxLayers
+  // layers; it lives in the handle to keep it off the host stack.
+  DecodeParams& p = *h->dec;
+  for (int l0 = 0; l0 < n_layers; l0 += kDecMaxLayers) {
+    const int nl = n_layers - l0 < kDecMaxLayers ? n_layers - l0 : kDecMaxLayers;
+    memset(&p, 0, sizeof p);
+    p.n_layers = nl;
+    p.H = c.hidden; p.Hq = c.n_heads; p.Hkv = c.n_kv_heads; p.D = c.head_dim;
+    p.I = c.intermediate; p.eps = c.rms_eps;
+    p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)c.head_dim));
+    p.max_ctx = c.max_ctx; p.cache_len = cache_len; p.pos = pos;
+    p.rope = h->rope; p.rope_len = c.max_ctx;
+    p.x_in = static_cast<const __half*>(l0 == 0 ? x : out);
+    p.out = static_cast<__half*>(out);
+    p.err = h->status;
+    p.trace = h->trace;
+    p.trace_len = h->trace_len;
+    decode_ws_carve(p, ws, h->num_sms);
+    for (int k = 0; k < nl; ++k) {
+      const blk_weights& wl = w[l0 + k];
+      DecLayer& d = p.layer[k];
+      d.wq = static_cast<const __half*>(wl.wq);
+      d.wk = static_cast<const __half*>(wl.wk);
+      d.wv = static_cast<const __half*>(wl.wv);
+      if (c.has_qkv_bias) {
+        d.bq = static_cast<const __half*>(wl.bq);
+        d.bk = static_cast<const __half*>(wl.bk);
+        d.bv = static_cast<const __half*>(wl.bv);
+      }
+      d.wo = static_cast<const __half*>(wl.wo);
+      d.ln1 = static_cast<const __half*>(wl.ln1_g);
+      d.ln2 = static_cast<const __half*>(wl.ln2_g);
+      d.wg = static_cast<const __half*>(wl.w_gate);
+      d.wu = static_cast<const __half*>(wl.w_up);
+      d.wd = static_cast<const __half*>(wl.w_down);
+      d.kc = static_cast<__half*>(k_caches[l0 + k]);
+      d.vc = static_cast<__half*>(v_caches[l0 + k]);
+      d.k_new = static_cast<__half*>(k_new ? k_new[l0 + k] : nullptr);
+      d.v_new = static_cast<__half*>(v_new ? v_new[l0 + k] : nullptr);
+      const int64_t rows = (int64_t)c.n_kv_heads * c.max_ctx;
+      if (make_tmap_2d(&p.tm_k[k], d.kc, rows, c.head_dim, 64) ||
+          make_tmap_2d(&p.tm_v[k], d.vc, rows, c.head_dim, 64))
+        return BLK_ERR_CUDA;
+    }
+    BLK_LAUNCH(tm, kKDecodeStep, launch_decode_persistent(p, h->num_sms, s));
+  }
   return BLK_OK;
 }
 
@@ -499,12 +474,21 @@ int blk_check(blk_handle h, void* stream) {
 }  // extern "C"
 
 size_t blk_internal_decode_ws_bytes(blk_handle h) {
-  return decode_ws(h->cfg, h->max_splits).total;
+  const blk_config& c = h->cfg;
+  return decode_ws_bytes(c.hidden, c.n_heads, c.n_kv_heads, c.head_dim, c.intermediate,
+                         h->num_sms);
 }
 
 int blk_internal_device(blk_handle h) { return h->device; }
 
 extern "C" {
+
+int blk_set_trace(blk_handle h, void* device_buffer, size_t bytes) {
+  if (!h) return BLK_ERR_NULL;
+  h->trace = static_cast<uint64_t*>(device_buffer);
+  h->trace_len = device_buffer ? bytes / sizeof(uint64_t) : 0;
+  return BLK_OK;
+}
 
 int blk_timing(blk_handle h, int on) {
   if (!h) return BLK_ERR_NULL;
@@ -566,9 +550,8 @@ const char* blk_status_str(int status) {
 }  // extern "C"
 
 namespace blk {
-cudaError_t configure_gemv_kernels();
 cudaError_t configure_kernels() {
-  const cudaError_t e = configure_gemv_kernels();
+  const cudaError_t e = configure_decode_persistent();
   return e != cudaSuccess ? e : configure_tc_gemm_kernels();
 }
 }  // namespace blk

@@ -9,9 +9,11 @@ device memory, streams and graphs.
 """
 from __future__ import annotations
 
+import ctypes
+
 import torch
 
-from . import Block
+from . import BLK_OK, BlkError, Block, BlkWeights, blk_decode_stack
 
 
 class LayerStack:
@@ -36,12 +38,31 @@ class LayerStack:
         # ping-pong activations between layers
         self.bufs = [torch.empty((max_T, H), dtype=torch.float16, device=device) for _ in range(2)]
         self.graphs = {}
+        n = self.n_layers
+        self._w_arr = (BlkWeights * n)(*self.w)
+        self._kc_arr = (ctypes.c_void_p * n)(*[kc.data_ptr() for kc, _ in caches])
+        self._vc_arr = (ctypes.c_void_p * n)(*[vc.data_ptr() for _, vc in caches])
+
+    def decode_step(self, x, pos, cache_len: int, out=None, stream=None):
+        """One token through every layer in one library call (blk_decode_stack).
+        Returns the last layer's output."""
+        out = self.bufs[0][:1] if out is None else out
+        s = torch.cuda.current_stream() if stream is None else stream
+        rc = blk_decode_stack(self.block.handle, self._w_arr, self.n_layers, self._kc_arr,
+                              self._vc_arr, x.data_ptr(), pos.data_ptr(), cache_len,
+                              out.data_ptr(), None, None, self.ws.data_ptr(),
+                              self.ws.numel(), s.cuda_stream)
+        if rc != BLK_OK:
+            raise BlkError(rc, "blk_decode_stack")
+        return out
 
     def run(self, phase: str, x, pos, cache_len: int, layer_outputs=None, stream=None):
         """Runs `phase` over all layers; returns the last layer's output (a
         view of an internal buffer).  layer_outputs, if given, is a list that
         receives a copy of each layer's input (for layer-local checks)."""
         T = x.shape[0]
+        if phase == "decode" and layer_outputs is None:
+            return self.decode_step(x, pos, cache_len, stream=stream)
         cur = x
         for l in range(self.n_layers):
             out = self.bufs[l % 2][:T]

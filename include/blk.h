@@ -139,11 +139,31 @@ int blk_prefill_kv(blk_handle h, const blk_weights* w, const void* x,
 
 /* decode (§4.1): one token after cache_len slots; attends [0, cache_len].
  *   x [1, hidden], pos [1], out [1, hidden], k_new/v_new [1, n_kv_heads, D].
- * Uses the weight-streaming kernels (HBM-bound path). */
+ * One launch of the persistent decode kernel (weight streaming, HBM-bound).
+ * Supported when hidden, intermediate and n_heads*head_dim are at most 12288
+ * and the group size is at most 16 (BLK_ERR_SHAPE otherwise). */
 int blk_decode(blk_handle h, const blk_weights* w, const void* x,
                const int64_t* pos, int64_t cache_len, void* k_cache,
                void* v_cache, void* out, void* k_new, void* v_new, void* ws,
                size_t ws_bytes, void* stream);
+
+/* decode through a stack of n_layers blocks of this shape, in order: layer
+ * l's output is layer l+1's input, all at the same cache_len and position.
+ * This is the decode call of the buddy-mlir runtime's forward_decode (one
+ * token through every layer, each with its own cache; §6.4.6 of that page),
+ * done as one launch per 32 layers.
+ *   w          host array [n_layers] of weight structs
+ *   k_caches, v_caches  host arrays [n_layers] of device cache pointers
+ *   k_new, v_new        host arrays [n_layers] of device [1, n_kv_heads, D]
+ *                       pointers (entries may be NULL), or NULL
+ *   x, out     device fp16 [1, hidden]; out may alias x
+ *   ws         blk_workspace_bytes(h, 1) bytes
+ * Same return codes as blk_decode. */
+int blk_decode_stack(blk_handle h, const blk_weights* w, int n_layers,
+                     void* const* k_caches, void* const* v_caches,
+                     const void* x, const int64_t* pos, int64_t cache_len,
+                     void* out, void* const* k_new, void* const* v_new,
+                     void* ws, size_t ws_bytes, void* stream);
 
 /* blk_decode_static — decode without a workspace argument, for callers that
  * cannot allocate device memory.  (The paper has no counterpart: this entry
@@ -199,6 +219,16 @@ int blk_timing(blk_handle h, int on);
 int blk_timing_collect(blk_handle h, void* stream);
 int blk_timing_read(blk_handle h, int kernel, double* total_ms,
                     int64_t* launches, const char** name);
+
+/* Decode timeline, for performance work.  With a device buffer set, every
+ * decode launch (blk_decode, blk_decode_stack) has thread 0 of each CTA write
+ * %globaltimer nanoseconds when each phase of each layer starts (after its
+ * grid barrier) and when its work ends: uint64 entries at
+ * [(cta * n_layers + layer) * 6 + phase] * 2 + {0 = start, 1 = end}, phases
+ * QKV, attention, split combine, o_proj, gate/up, down; n_layers counts the
+ * layers of one launch (at most 32).  Entries past `bytes` are not written.
+ * NULL turns tracing off (the default).  Returns BLK_OK or BLK_ERR_NULL. */
+int blk_set_trace(blk_handle h, void* device_buffer, size_t bytes);
 
 /* Static description of a status code. */
 const char* blk_status_str(int status);

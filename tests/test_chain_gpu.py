@@ -90,6 +90,28 @@ def test_chain_flag_and_graph_match_plain_launches_bitwise():
         assert np.array_equal(r[1], results[0][1])
 
 
+def test_decode_stack_one_launch_equals_per_layer_calls():
+    """blk_decode_stack (all layers in one launch) gives the same bits as one
+    blk_decode call per layer; 40 tiny layers also cover the split into
+    launches of at most 32 layers."""
+    for s, n, C, L in ((synth.QWEN2_1P5B, 3, 600, 513), (synth.TINY, 40, 64, 37)):
+        wl, hc = _stack(s, n, C, L)
+        x = to_dev(synth.hidden_input(s, 1, seed=3))
+        pos = to_dev(synth.positions(L, 1))
+        c1 = [(to_dev(k), to_dev(v)) for k, v in hc]
+        c2 = [(to_dev(k), to_dev(v)) for k, v in hc]
+        st1 = LayerStack(s, wl, C, 1, caches=c1)
+        st2 = LayerStack(s, wl, C, 1, caches=c2)
+        one = st1.decode_step(x, pos, L).clone()
+        ins = []
+        per = st2.run("decode", x, pos, L, layer_outputs=ins).clone()
+        torch.cuda.synchronize()
+        st1.block.check()
+        assert torch.equal(one, per)
+        for (k1, v1), (k2, v2) in zip(c1, c2):
+            assert torch.equal(k1[:, L], k2[:, L]) and torch.equal(v1[:, L], v2[:, L])
+
+
 def _layer_local(s, wl_np_fn, caches_before, layer_inputs, pos, L, rows, outs_next, layers):
     for l in layers:
         w = wl_np_fn(l)
