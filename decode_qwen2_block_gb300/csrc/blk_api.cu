@@ -225,9 +225,11 @@ int run_prefill(blk_handle h, const blk_weights* w, const void* x,
 
   // causal GQA attention over [history; new rows]
   PrefillAttnParams pa = {};
+  if (make_tmap_2d(&pa.tm_k, k_cache, (int64_t)Hkv * c.max_ctx, D, 64) ||
+      make_tmap_2d(&pa.tm_v, v_cache, (int64_t)Hkv * c.max_ctx, D, 64))
+    return BLK_ERR_CUDA;
   pa.q16 = q16;
-  pa.kc = static_cast<const __half*>(k_cache);
-  pa.vc = static_cast<const __half*>(v_cache);
+  pa.err = h->status;
   pa.max_ctx = c.max_ctx; pa.cache_len = L;
   pa.T = M; pa.Hq = Hq; pa.Hkv = Hkv; pa.D = D;
   pa.scale_log2 = (float)(1.4426950408889634 / sqrt((double)D));
@@ -551,7 +553,9 @@ const char* blk_status_str(int status) {
 
 namespace blk {
 cudaError_t configure_kernels() {
-  const cudaError_t e = configure_decode_persistent();
-  return e != cudaSuccess ? e : configure_tc_gemm_kernels();
+  cudaError_t e = configure_decode_persistent();
+  if (e == cudaSuccess) e = configure_tc_gemm_kernels();
+  if (e == cudaSuccess) e = configure_prefill_attn();
+  return e;
 }
 }  // namespace blk

@@ -2,6 +2,7 @@
 // blk_api.cu validates arguments, carves the workspace and calls these.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -14,16 +15,18 @@ cudaError_t launch_rmsnorm_rows(const void* x, bool x_is_f32, const __half* g,
                                 cudaStream_t s, bool pdl);
 
 struct PrefillAttnParams {
+  CUtensorMap tm_k;   // K cache viewed as [Hkv * max_ctx, D], box 64 x 64, SW128
+  CUtensorMap tm_v;
   const __half* q16;  // [T, Hq, D]
-  const __half* kc;
-  const __half* vc;
   int64_t max_ctx, cache_len;
   int T, Hq, Hkv, D;
   float scale_log2;
   __half* attn16;  // [T, Hq * D]
+  int* err;
 };
 cudaError_t launch_prefill_attn(const PrefillAttnParams& p, cudaStream_t s,
                                 bool pdl);
+cudaError_t configure_prefill_attn();
 
 // Sets the per-kernel shared-memory limits (called once per device).
 cudaError_t configure_kernels();
