@@ -51,6 +51,8 @@ def parse():
     ap.add_argument("--no-decode", action="store_true", help="skip the decode table")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--decode-ctx", type=str, default=",".join(map(str, DECODE_CTX)))
+    ap.add_argument("--only", choices=("prefill", "decode"), default=None,
+                    help="run one part (for profiling); the headline needs both")
     return ap.parse_args()
 
 
@@ -222,6 +224,11 @@ def bench_ours(args, ws, rank, local):
     stream = torch.cuda.current_stream()
     s = synth.QWEN2_1P5B
     K, W = args.steps, args.warmup
+    if args.only == "decode":
+        clocks = ClockSampler(local)
+        clocks.start()
+        dec = bench_decode(args, s, dev, stream, peaks, ws)
+        return {"metric": "decode us/step (28 layers)", "decode": dec, "clocks": clocks.stop()}
 
     # ---------------- prefill, one layer, [1, 1024] ----------------
     T = PREFILL_T
@@ -347,7 +354,7 @@ def bench_ours(args, ws, rank, local):
     }
 
     # ---------------- decode, 28 layers ----------------
-    if not args.no_decode:
+    if not args.no_decode and args.only != "prefill":
         result["decode"] = bench_decode(args, s, dev, stream, peaks, ws)
     result["clocks"] = clocks.stop()
     return result
@@ -445,7 +452,7 @@ def main():
         print(json.dumps(line))
         return
     result = bench_ours(args, ws, rank, local)
-    if rank == 0 and not args.no_cpu:
+    if rank == 0 and not args.no_cpu and args.only is None:
         tok_s, secs, desc = oracle_prefill_sample(128)
         result["cpu_baseline"] = {"value": tok_s, "unit": UNIT, "cores": 1, "kind": "oracle",
                                   "sample": desc, "host_cores": os.cpu_count(),

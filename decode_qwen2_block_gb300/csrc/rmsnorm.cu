@@ -1,35 +1,98 @@
-// Prefill-phase row RMSNorm: y = fp16(x * rsqrt(mean(x^2) + eps) * g), one CTA
-// per row; x is the block input (fp16) or the fp32 residual stream h.
+// Prefill-phase row RMSNorm: y = fp16(x * rsqrt(mean(x^2) + eps) * g); x is
+// the block input (fp16) or the fp32 residual stream h.
 #include "common.cuh"
 #include "kernels.h"
 
 namespace blk {
 
 // ------------------------------------------------------------------ RMSNorm
-// One CTA per row: y = fp16(x * rsqrt(mean(x^2) + eps) * g).
+// One warp per row.  Each lane loads its share of the row in batches of up to
+// kMaxVec 16-byte vectors with every load of a batch in flight (a 1.5K-wide
+// row is one batch, i.e. one memory round trip); the first batch stays in
+// registers for the output pass, later batches are re-read.
+constexpr int kNormWarps = 8;
+constexpr int kMaxVec = 12;
+
 template <typename T>
-__global__ void __launch_bounds__(256)
-    rmsnorm_rows_kernel(const T* __restrict__ x, const __half* __restrict__ g,
-                        int H, float eps, __half* __restrict__ y) {
-  __shared__ float red[8];
+__device__ __forceinline__ float sumsq16(const uint4& v) {
+  if constexpr (sizeof(T) == 2) {
+    float f[8];
+    h8_to_f32(v, f);
+    float s = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) s += f[e] * f[e];
+    return s;
+  } else {
+    const float4 f = *reinterpret_cast<const float4*>(&v);
+    return f.x * f.x + f.y * f.y + f.z * f.z + f.w * f.w;
+  }
+}
+
+// Writes the normalised elements of vector i (8 fp16 or 4 fp32 inputs).
+template <typename T>
+__device__ __forceinline__ void put16(const uint4& v, int i, float r, const __half* g,
+                                      __half* yr) {
+  if constexpr (sizeof(T) == 2) {
+    float f[8], gf[8];
+    h8_to_f32(v, f);
+    h8_to_f32(__ldg(reinterpret_cast<const uint4*>(g) + i), gf);
+    uint4 o;
+    __half2* oh = reinterpret_cast<__half2*>(&o);
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      oh[e] = __floats2half2_rn(f[2 * e] * r * gf[2 * e], f[2 * e + 1] * r * gf[2 * e + 1]);
+    reinterpret_cast<uint4*>(yr)[i] = o;
+  } else {
+    const float4 f = *reinterpret_cast<const float4*>(&v);
+    const uint2 graw = __ldg(reinterpret_cast<const uint2*>(g) + i);
+    const float2 ga = __half22float2(*reinterpret_cast<const __half2*>(&graw.x));
+    const float2 gb = __half22float2(*reinterpret_cast<const __half2*>(&graw.y));
+    uint2 o;
+    *reinterpret_cast<__half2*>(&o.x) = __floats2half2_rn(f.x * r * ga.x, f.y * r * ga.y);
+    *reinterpret_cast<__half2*>(&o.y) = __floats2half2_rn(f.z * r * gb.x, f.w * r * gb.y);
+    reinterpret_cast<uint2*>(yr)[i] = o;
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kNormWarps * 32)
+    rmsnorm_rows_kernel(const T* __restrict__ x, const __half* __restrict__ g, int rows, int H,
+                        float eps, __half* __restrict__ y) {
   griddep_wait();
   griddep_launch();
-  const int row = blockIdx.x, tid = threadIdx.x;
-  const T* xr = x + (size_t)row * H;
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * kNormWarps + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const int nv = H / (16 / (int)sizeof(T));
+  const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)row * H);
+  uint4 v[kMaxVec];
   float ss = 0.f;
-  for (int i = tid; i < H; i += 256) {
-    const float v = (float)xr[i];
-    ss += v * v;
+#pragma unroll
+  for (int k = 0; k < kMaxVec; ++k) {
+    const int i = lane + 32 * k;
+    v[k] = i < nv ? __ldg(xr + i) : make_uint4(0, 0, 0, 0);
+  }
+#pragma unroll
+  for (int k = 0; k < kMaxVec; ++k) ss += sumsq16<T>(v[k]);
+  for (int base = 32 * kMaxVec; base < nv; base += 32 * kMaxVec) {   // long rows
+    uint4 w[kMaxVec];
+#pragma unroll
+    for (int k = 0; k < kMaxVec; ++k) {
+      const int i = base + lane + 32 * k;
+      w[k] = i < nv ? __ldg(xr + i) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int k = 0; k < kMaxVec; ++k) ss += sumsq16<T>(w[k]);
   }
   ss = warp_sum(ss);
-  if ((tid & 31) == 0) red[tid >> 5] = ss;
-  __syncthreads();
-  float tot = 0.f;
+  const float r = rsqrtf(ss / (float)H + eps);
+  __half* yr = y + (size_t)row * H;
 #pragma unroll
-  for (int w = 0; w < 8; ++w) tot += red[w];
-  const float r = rsqrtf(tot / (float)H + eps);
-  for (int i = tid; i < H; i += 256)
-    y[(size_t)row * H + i] = __float2half_rn((float)xr[i] * r * __half2float(g[i]));
+  for (int k = 0; k < kMaxVec; ++k) {
+    const int i = lane + 32 * k;
+    if (i < nv) put16<T>(v[k], i, r, g, yr);
+  }
+  for (int i = 32 * kMaxVec + lane; i < nv; i += 32) put16<T>(__ldg(xr + i), i, r, g, yr);
 }
 
 static cudaLaunchConfig_t make_cfg(dim3 grid, dim3 block, size_t smem,
@@ -51,12 +114,13 @@ cudaError_t launch_rmsnorm_rows(const void* x, bool x_is_f32, const __half* g,
                                 int rows, int H, float eps, __half* y,
                                 cudaStream_t s, bool pdl) {
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = make_cfg(dim3(rows), dim3(256), 0, s, pdl, attr);
+  cudaLaunchConfig_t cfg = make_cfg(dim3((rows + kNormWarps - 1) / kNormWarps),
+                                    dim3(kNormWarps * 32), 0, s, pdl, attr);
   if (x_is_f32)
     return cudaLaunchKernelEx(&cfg, rmsnorm_rows_kernel<float>,
-                              static_cast<const float*>(x), g, H, eps, y);
+                              static_cast<const float*>(x), g, rows, H, eps, y);
   return cudaLaunchKernelEx(&cfg, rmsnorm_rows_kernel<__half>,
-                            static_cast<const __half*>(x), g, H, eps, y);
+                            static_cast<const __half*>(x), g, rows, H, eps, y);
 }
 
 }  // namespace blk
