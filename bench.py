@@ -41,6 +41,19 @@ UNIT = "tok/s"
 DECODE_CTX = (1024, 4096, 16384, 32768)
 PREFILL_T = 1024
 
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from
+# the ncu captures summarised in profiles/ (prefill_kernels_1p5b_T1024.md,
+# decode_persistent_1p5b_28layers_ctx4096.md).  Must be set back to None
+# whenever the kernel changes.
+NCU_TRAFFIC = {
+    "gemm_gateup": 58.261248e6 + 1.469952e6,
+    "gemm_down": 52.183296e6 + 0.454144e6,
+    "gemm_qkv": 10.012416e6,
+    "gemm_o": 11.026688e6,
+    "attn_prefill": 4.226304e6,
+    ("decode_persistent", 4096): 2.742902e9 + 0.039405568e9,
+}
+
 
 def parse():
     ap = argparse.ArgumentParser()
@@ -327,7 +340,8 @@ def bench_ours(args, ws, rank, local):
         achieved = work / (per_launch * 1e-3) / 1e12
         roof = {"kernel": dom, "bound": "tensor", "achieved": achieved,
                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": achieved / peaks["bf16_tflops"], "traffic": None,
+                "frac": achieved / peaks["bf16_tflops"], "traffic": NCU_TRAFFIC.get(dom),
+                "traffic_unit": "bytes per launch (ncu, cold L2)",
                 "peak_source": peaks["source"] + " bf16 dense burst (fp16 runs at the bf16 rate)"}
     else:
         roof = {"kernel": dom, "bound": "hbm", "achieved": None, "peak": peaks["hbm_gbs"],
@@ -405,7 +419,8 @@ def bench_decode(args, s, dev, stream, peaks, ws):
         out[str(L)] = {"us_per_step": ms * 1e3, "tok_s": ws * 1e3 / ms,
                        "bytes_per_step": nbytes, "achieved_gbs": achieved,
                        "frac_of_hbm_peak": achieved / peaks["hbm_gbs"],
-                       "roofline_us": nbytes / (peaks["hbm_gbs"] * 1e9) * 1e6}
+                       "roofline_us": nbytes / (peaks["hbm_gbs"] * 1e9) * 1e6,
+                       "traffic": NCU_TRAFFIC.get(("decode_persistent", L))}
         del graphs
         st.graphs.clear()
     # per-kernel durations at the largest context (eager, events per kernel)
