@@ -1,0 +1,88 @@
+"""The pins catch plausible mistakes in the oracle.
+
+Each case plants one mistake in a copy of oracle/blk_oracle.cpp (a flipped
+sign, a wrong index, a dropped term, swapped operands), builds it on the CPU,
+points the oracle wrapper at the mutant and checks that at least one pin of
+tests/test_oracle_pins.py fails.  The real oracle is never modified.
+"""
+import ctypes
+import os
+import subprocess
+
+import pytest
+
+import oracle
+import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "blk_oracle.cpp")
+
+# (name, text in blk_oracle.cpp, replacement)
+MUTATIONS = [
+    ("rope sign", "v[i] = a * c - b * s;", "v[i] = a * c + b * s;"),
+    ("rope partner index", "const double a = v[i], b = v[i + half];",
+     "const double a = v[i], b = v[(i + 1) % D];"),
+    ("rope frequency", "std::pow(theta, -2.0 * static_cast<double>(i) / static_cast<double>(D))",
+     "std::pow(theta, -1.0 * static_cast<double>(i) / static_cast<double>(D))"),
+    ("gqa mapping", "const int64_t g = hq / group;", "const int64_t g = hq % Hkv;"),
+    ("attention scale", "const double scale = 1.0 / std::sqrt(static_cast<double>(D));",
+     "const double scale = 1.0 / static_cast<double>(D);"),
+    ("causal mask edge", "L + t + 1,\n                 D, D, scale", "L + t,\n                 D, D, scale"),
+    ("dropped k bias", "orc_linear(w->wk, bias ? w->bk : nullptr", "orc_linear(w->wk, nullptr"),
+    ("dropped rmsnorm eps", "std::sqrt(sum_sq / static_cast<double>(n) + eps)",
+     "std::sqrt(sum_sq / static_cast<double>(n))"),
+    ("dropped attention residual", "for (int64_t i = 0; i < H; ++i) h[i] += h2d(x[t * H + i]);",
+     "for (int64_t i = 0; i < H; ++i) h[i] += 0.0;"),
+    ("swapped swiglu operands", "act[j] = orc_silu(gate[j]) * up[j];",
+     "act[j] = orc_silu(up[j]) * gate[j];"),
+    ("transposed linear", "const uint16_t* row = W + o * n_in;\n    double acc = 0.0;\n    for (int64_t i = 0; i < n_in; ++i) acc += h2d(row[i]) * x[i];",
+     "double acc = 0.0;\n    for (int64_t i = 0; i < n_in; ++i) acc += h2d(W[i * n_out + o]) * x[i];"),
+    ("softmax max not subtracted consistently", "s[j] = std::exp(s[j] - m);", "s[j] = std::exp(s[j] - 0.5 * m);"),
+    ("v stored rotated", "const uint16_t vh = encode_half(v[g * D + d]);",
+     "const uint16_t vh = encode_half(k[g * D + d]);"),
+]
+
+PIN_TESTS = [getattr(pins, n) for n in dir(pins) if n.startswith("test_")]
+
+
+def _run_pins():
+    """Returns the names of pin tests that fail under the current oracle lib."""
+    failed = []
+    for fn in PIN_TESTS:
+        params = getattr(fn, "pytestmark", [])
+        cases = [()]
+        for mark in params:
+            if mark.name == "parametrize":
+                cases = [c if isinstance(c, tuple) else (c,) for c in mark.args[1]]
+        for case in cases:
+            try:
+                fn(*case)
+            except Exception:  # noqa: BLE001 - any failure counts as caught
+                failed.append(fn.__name__)
+                break
+    return failed
+
+
+@pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_planted_mistake_is_caught(name, old, new, tmp_path):
+    src = open(SRC).read()
+    assert old in src, f"mutation anchor for '{name}' not found"
+    mutant_src = tmp_path / "blk_oracle.cpp"
+    mutant_src.write_text(src.replace(old, new, 1))
+    (tmp_path / "blk_oracle.h").write_text(open(SRC.replace(".cpp", ".h")).read())
+    lib = tmp_path / "liboracle_mutant.so"
+    subprocess.check_call(["g++", "-O2", "-std=c++17", "-ffp-contract=off", "-fPIC", "-shared",
+                           str(mutant_src), "-o", str(lib)])
+    saved = oracle._lib
+    oracle._lib = None
+    real_build = oracle.build
+    try:
+        oracle.build = lambda force=False: str(lib)
+        failed = _run_pins()
+    finally:
+        oracle.build = real_build
+        oracle._lib = saved
+    assert failed, f"no pin caught the planted mistake '{name}'"
+
+
+def test_unmutated_oracle_passes_every_pin():
+    assert _run_pins() == []
