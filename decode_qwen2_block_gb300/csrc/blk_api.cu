@@ -299,16 +299,13 @@ int blk_create(const blk_config* cfg, blk_handle* out) {
   h->device = dev;
   h->num_sms = sms;
   {
-    // the decode kernel stages at most kDecMaxVec inputs and 150 weight rows
-    // per CTA and phase (one CTA per SM)
-    const int64_t rows_qkv = 2 * (((int64_t)(cfg->n_heads + 2 * cfg->n_kv_heads) *
-                                   (cfg->head_dim / 2) + sms - 1) / sms);
-    const int64_t rows_gu = 2 * ((cfg->intermediate + sms - 1) / sms);
-    const int64_t rows_h = (cfg->hidden + sms - 1) / sms;
+    // the decode kernel stages at most kDecMaxVec inputs and keeps the
+    // residual of at most 152 o_proj rows (8-row units) per CTA (one per SM)
+    const int64_t rows_o = 8 * ((cfg->hidden / 8 + sms - 1) / sms);
     h->decode_ok = cfg->hidden <= kDecMaxVec && cfg->intermediate <= kDecMaxVec &&
                    cfg->n_heads * cfg->head_dim <= kDecMaxVec && cfg->n_kv_heads <= sms &&
-                   cfg->n_heads / cfg->n_kv_heads <= 16 && rows_qkv <= 150 &&
-                   rows_gu <= 150 && rows_h <= 150 && cfg->intermediate % 16 == 0;
+                   cfg->n_heads / cfg->n_kv_heads <= 16 && rows_o <= 152 &&
+                   cfg->intermediate % 16 == 0;
   }
   h->dec = new (std::nothrow) blk::DecodeParams();
   if (!h->dec) {
@@ -454,6 +451,22 @@ int blk_decode_stack(blk_handle h, const blk_weights* w, int n_layers,
       if (make_tmap_2d(&p.tm_k[k], d.kc, rows, c.head_dim, 64) ||
           make_tmap_2d(&p.tm_v[k], d.vc, rows, c.head_dim, 64))
         return BLK_ERR_CUDA;
+      // weights as 8-row boxes: {base, rows, K} per role
+      const int64_t H = c.hidden, QD = (int64_t)c.n_heads * c.head_dim,
+                    KD = (int64_t)c.n_kv_heads * c.head_dim, I = c.intermediate;
+      const struct { const void* b; int64_t rows, K; } wr[kDecRoles] = {
+          {d.wq, QD, H}, {d.wk, KD, H}, {d.wv, KD, H}, {d.wo, H, QD},
+          {d.wg, I, H},  {d.wu, I, H},  {d.wd, H, I}};
+      for (int r = 0; r < kDecRoles; ++r) {
+        const int64_t nz = (wr[r].K + 63) / 64;
+        const int cbs = (int)(nz < 24 ? nz : 24);
+        int is3d = 0;
+        if (make_tmap_rows8(&p.tm_w[k][r], wr[r].b, wr[r].rows, wr[r].K, cbs, &is3d))
+          return BLK_ERR_CUDA;
+        p.w3d[r] = is3d;
+        p.wbox_z[r] = cbs;
+        p.wnz[r] = (int)nz;
+      }
     }
     BLK_LAUNCH(tm, kKDecodeStep, launch_decode_persistent(p, h->num_sms, s));
   }

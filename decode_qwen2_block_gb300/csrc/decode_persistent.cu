@@ -5,29 +5,34 @@
 // bound by the bytes of the weights (93.6 MB per 1.5B-shaped layer) and of
 // the KV history.  Those bytes never depend on the token being decoded, so
 // each CTA (one per SM) has a producer lane that streams, in consumption
-// order, every weight row block and every KV-history tile the CTA will use —
-// across phase and layer boundaries — into a 4 x 48 KB shared-memory ring
-// (untiled bulk copies for weight rows; 128B-swizzled tensor copies for K/V
-// tiles).  Twelve consumer warps run the phases of each layer and meet at a
-// grid-wide barrier between phases; while they wait, the producer keeps
+// order, every weight box and every KV-history tile the CTA will use —
+// across phase and layer boundaries — into a 4 x 48 KB shared-memory ring.
+// Every copy is a TMA tensor copy with 128-byte swizzle: a weight box is 8
+// rows x 1536 columns (one 3-D copy of 24 column blocks of 64), a KV tile
+// 64 slots x D.  Twelve consumer warps run the phases of each layer and meet
+// at a grid-wide barrier between phases; while they wait, the producer keeps
 // filling the ring, so HBM stays busy through the barriers.
 //
 // Phases of one layer (the block of the TopOp paper, Listing 2, at T = 1):
-//   QKV   RMSNorm(x) staged in shared memory; rows of wq|wk|wv in RoPE pairs
-//         (i, i + D/2); epilogue: bias, RoPE, q (fp32) to the workspace, K/V
-//         to cache slot cache_len and to k_new / v_new.
+//   QKV   x = previous layer's output (or the input), RMSNorm(x) staged in
+//         shared memory; a work unit is rows i0..i0+7 and their RoPE partners
+//         i0+D/2.. of one head of wq|wk|wv; epilogue: bias, RoPE, q (fp32) to
+//         the workspace, K/V to cache slot cache_len and to k_new / v_new.
 //   ATTN  CTA (kv head g, split s) covers slots [j0, j1) of [0, cache_len];
 //         4 warps run mma.sync m16n8k16 (rows = the G query heads of the
 //         group, padded to 16) over 64-slot tiles: S = Q K^T, online softmax
 //         in base 2, O += P V; the warps' states are merged and one partial
 //         (acc, max, sum) per query head is written.
 //   COMB  every CTA merges all splits for a slice of (head, d) pairs -> attn.
-//   O     rows of wo; epilogue h = acc + x (fp32).
-//   GU    RMSNorm(h) staged; matching rows of w_gate and w_up; epilogue
-//         silu(gate) * up (fp16).
-//   DOWN  rows of w_down; epilogue out = acc + h (fp16) = next layer's input.
-// Dot products are split over warps and lanes with 16-byte vectors and fp32
-// accumulation; per-(row, slice) partials are added in a fixed order, so the
+//   O     two 8-row units of wo; epilogue h = acc + x (fp32).
+//   GU    RMSNorm(h) staged; unit = 8 rows of w_gate and the same 8 rows of
+//         w_up; epilogue silu(gate) * up (fp16).
+//   DOWN  split over (16 rows, 1536 columns) items for balance; each item's
+//         fp32 partial goes to the workspace and the next reader adds the
+//         partials of a row in a fixed order to h: that sum, rounded to fp16,
+//         is the layer's output.
+// A final phase writes the last layer's output.  Dot products are split over
+// warps with fp32 accumulation; partials are added in a fixed order, so the
 // result does not depend on timing.
 //
 // Every wait (ring mbarriers, grid barrier) is bounded; on a timeout the
@@ -47,24 +52,29 @@ constexpr int kStageBytes = 48 * 1024;
 constexpr int kStages = 4;
 constexpr int kAttnWarps = 4;           // 4 x 16 slots = one 64-slot tile
 constexpr int kSlots = 64;
-constexpr int kGroupRows = 15;          // weight rows per mma tile (of 16)
-constexpr int kKc = 1536;               // weight columns per ring stage
-constexpr int kRowStride = (kKc + 8) * 2;  // bytes per staged row: 16-byte pad
-                                           // keeps ldmatrix free of conflicts
-constexpr int kPartFloats = 2048;       // [row group][warp][16] partial sums
+constexpr int kBoxRows = 8;             // weight rows per TMA box
+constexpr int kCB = 24;                 // 64-column blocks per box
+constexpr int kKc = kCB * 64;           // weight columns per ring stage
+constexpr int kBoxBytes = kBoxRows * kKc * 2;  // 24 KB; two boxes per stage
+constexpr int kBatch = 10;              // groups whose partials shared memory holds
+constexpr int kPfAhead = 0;             // chunks the producer may prefetch into L2
+constexpr int kPartFloats = 2048;       // [group][warp][16] partial sums
 constexpr int kQStride = 136;           // Q tile row stride in halves (padded)
-static_assert(kGroupRows * kRowStride <= kStageBytes, "stage too small");
+static_assert(2 * kBoxBytes <= kStageBytes, "stage too small");
+static_assert(kBatch * kCW * 16 <= kPartFloats, "partials too small");
 
 constexpr int kXsOff = kStages * kStageBytes;
 constexpr int kPartOff = kXsOff + kDecMaxVec * 2;
 constexpr int kQOff = kPartOff;         // the Q tile reuses the partials area
 constexpr int kBarOff = kPartOff + kPartFloats * 4;
-constexpr int kResRows = 150;           // hidden rows per CTA (o_proj / down)
-constexpr int kResOff = kBarOff + 256;  // x and h slices of this CTA's rows
-constexpr int kSmemUsed = kResOff + 2 * kResRows * 4;
+constexpr int kResRows = 152;           // hidden rows per CTA (o_proj)
+constexpr int kResOff = kBarOff + 256;  // x slice of this CTA's o_proj rows
+constexpr int kSmemUsed = kResOff + kResRows * 4;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // + alignment slack
 
 enum Phase { kPhQKV = 0, kPhAttn = 1, kPhComb = 2, kPhO = 3, kPhGU = 4, kPhDown = 5 };
+// weight roles, the order of DecodeParams::tm_w
+enum Role { kWq = 0, kWk = 1, kWv = 2, kWo = 3, kWg = 4, kWu = 5, kWd = 6 };
 constexpr int kPhases = 6;
 
 // ------------------------------------------------------------ small PTX
@@ -83,6 +93,38 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_2d_u32(uint32_t dst, const CUtensorMap* map, int x,
+                                                int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
 __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -93,13 +135,6 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
       : "r"(smem_u32(bar)), "r"(parity)
       : "memory");
   return ok != 0;
-}
-
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(x), "r"(y)
-               : "memory");
 }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t* r) {
@@ -136,56 +171,83 @@ __device__ __forceinline__ uint32_t tile_addr(uint32_t base, int r, int ch) {
 }
 
 // ------------------------------------------------------------ schedule
-__device__ __forceinline__ const __half* layer_input(const DecodeParams& p, int l) {
-  return l == 0 ? p.x_in : ((l - 1) & 1 ? p.xbuf1 : p.xbuf0);
-}
-__device__ __forceinline__ __half* layer_output(const DecodeParams& p, int l) {
-  return l == p.n_layers - 1 ? p.out : (l & 1 ? p.xbuf1 : p.xbuf0);
-}
-
-// The weight rows one CTA owns in a projection phase, as a list indexed by
-// q in [0, nrows):
-//   QKV  q <  units: row i of head hd (pair unit u = u0 + q, i = u % (D/2))
-//        q >= units: its partner row i + D/2
-//   GU   q <  units: W_gate row j0 + q;  q >= units: W_up row j0 + q - units
-//   O, DOWN  row r0 + q
-struct PhaseRows {
-  int nrows, units, K, first, ncol;
+// The work of a projection phase is a list of units of 8 weight rows; a CTA
+// owns a contiguous range of them, and a "group" is what one ring chunk (two
+// 8-row boxes = the 16 rows of an mma tile) holds for one or more column
+// chunks of 1536:
+//   QKV   group = unit u: head hd, rows i0..i0+7 (tile rows 0-7) and their
+//         RoPE partners i0+D/2.. (tile rows 8-15); all column chunks of H
+//   O     group = two consecutive units (the second may be absent)
+//   GU    group = unit u: rows 8u.. of w_gate (tile rows 0-7) and of w_up
+//   DOWN  group = item (row pair p = rows 16p..16p+15, column chunk kc):
+//         one column chunk each, so the 6+ chunks of a row pair spread over
+//         CTAs and every CTA streams about the same number of bytes.
+struct PhaseWork {
+  int first, count;   // this CTA's units (DOWN: items)
+  int ngroups;
+  int ncol;           // column chunks of the phase's K
+  int K;
 };
 
-__device__ __forceinline__ PhaseRows phase_rows(const DecodeParams& p, int ph) {
+__device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+template <int D>
+__device__ __forceinline__ PhaseWork phase_work(const DecodeParams& p, int ph) {
   const int b = blockIdx.x, G = gridDim.x;
-  PhaseRows r;
+  PhaseWork w;
   int total;
-  if (ph == kPhQKV) { total = (p.Hq + 2 * p.Hkv) * (p.D / 2); r.K = p.H; }
-  else if (ph == kPhGU) { total = p.I; r.K = p.H; }
-  else { total = p.H; r.K = ph == kPhO ? p.Hq * p.D : p.I; }
-  r.first = (int)((int64_t)b * total / G);
-  r.units = (int)((int64_t)(b + 1) * total / G) - r.first;
-  r.nrows = (ph == kPhQKV || ph == kPhGU) ? 2 * r.units : r.units;
-  r.ncol = (r.K + kKc - 1) / kKc;
-  return r;
+  if (ph == kPhQKV) { total = (p.Hq + 2 * p.Hkv) * (D / 16); w.K = p.H; }
+  else if (ph == kPhO) { total = p.H / kBoxRows; w.K = p.Hq * D; }
+  else if (ph == kPhGU) { total = p.I / kBoxRows; w.K = p.H; }
+  else { total = ceil_div(p.H, 2 * kBoxRows) * ceil_div(p.I, kKc); w.K = p.I; }
+  w.ncol = ceil_div(w.K, kKc);
+  w.first = (int)((int64_t)b * total / G);
+  w.count = (int)((int64_t)(b + 1) * total / G) - w.first;
+  w.ngroups = ph == kPhO ? ceil_div(w.count, 2) : w.count;
+  return w;
 }
 
-__device__ __forceinline__ const __half* row_ptr(const DecodeParams& p, const DecLayer& Ly,
-                                                 int ph, const PhaseRows& r, int q) {
+// What one group loads: box A (tile rows 0-7) and, unless yb < 0, box B
+// (tile rows 8-15), over column chunks [ka, kb).
+struct GroupDesc {
+  int ra, ya, rb, yb;   // role and first row of each box
+  int ka, kb;
+};
+
+template <int D>
+__device__ __forceinline__ GroupDesc group_desc(const DecodeParams& p, int ph,
+                                                const PhaseWork& w, int gi) {
+  GroupDesc g;
+  g.ka = 0;
+  g.kb = w.ncol;
   if (ph == kPhQKV) {
-    const int half = p.D / 2;
-    const bool hi = q >= r.units;
-    const int u = r.first + (hi ? q - r.units : q);
-    const int hd = u / half, i = u % half + (hi ? half : 0);
-    const __half* W;
+    constexpr int upd = D / 16;  // units per head
+    const int u = w.first + gi, hd = u / upd, i0 = (u % upd) * kBoxRows;
     int local;
-    if (hd < p.Hq) { W = Ly.wq; local = hd; }
-    else if (hd < p.Hq + p.Hkv) { W = Ly.wk; local = hd - p.Hq; }
-    else { W = Ly.wv; local = hd - p.Hq - p.Hkv; }
-    return W + (size_t)(local * p.D + i) * r.K;
+    if (hd < p.Hq) { g.ra = kWq; local = hd; }
+    else if (hd < p.Hq + p.Hkv) { g.ra = kWk; local = hd - p.Hq; }
+    else { g.ra = kWv; local = hd - p.Hq - p.Hkv; }
+    g.rb = g.ra;
+    g.ya = local * D + i0;
+    g.yb = g.ya + D / 2;
+  } else if (ph == kPhO) {
+    const int u = w.first + 2 * gi;
+    g.ra = g.rb = kWo;
+    g.ya = u * kBoxRows;
+    g.yb = u + 1 < w.first + w.count ? g.ya + kBoxRows : -1;
+  } else if (ph == kPhGU) {
+    const int u = w.first + gi;
+    g.ra = kWg; g.rb = kWu;
+    g.ya = g.yb = u * kBoxRows;
+  } else {
+    const int it = w.first + gi, pr = it / w.ncol;
+    g.ka = it % w.ncol;
+    g.kb = g.ka + 1;
+    g.ra = g.rb = kWd;
+    g.ya = pr * 2 * kBoxRows;
+    g.yb = g.ya + kBoxRows < p.H ? g.ya + kBoxRows : -1;
   }
-  if (ph == kPhGU) {
-    return q < r.units ? Ly.wg + (size_t)(r.first + q) * r.K
-                       : Ly.wu + (size_t)(r.first + q - r.units) * r.K;
-  }
-  return (ph == kPhO ? Ly.wo : Ly.wd) + (size_t)(r.first + q) * r.K;
+  return g;
 }
 
 struct AttnRange {
@@ -219,10 +281,10 @@ struct Sync {
 // phase; wait(k) returns once all CTAs arrived at barrier k (0-based).
 __device__ __forceinline__ void grid_arrive(const Sync& s) {
   named_sync(1, kCT);
-  if (threadIdx.x == 0) {
-    __threadfence();
-    atomicAdd(s.counter, 1u);
-  }
+  // release: the CTA's writes (ordered before this by the named barrier)
+  // are visible to whoever acquires the counter value that includes it
+  if (threadIdx.x == 0)
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(s.counter) : "memory");
 }
 
 __device__ __forceinline__ bool grid_wait(const Sync& s, int k) {
@@ -251,29 +313,58 @@ __device__ __forceinline__ bool grid_wait(const Sync& s, int k) {
 constexpr int kMaxV16 = (kDecMaxVec / 8 + kCT - 1) / kCT;  // uint4 per thread (fp16)
 constexpr int kMaxV32 = (kDecMaxVec / 4 + kCT - 1) / kCT;  // float4 per thread (fp32)
 
-// xs[i] = fp16(x[i] * rsqrt(mean(x^2) + eps) * g[i]) for fp16 x.
-// Also copies x[cap_lo, cap_hi) (raw) to cap[] for a later residual.
-__device__ void stage_rmsnorm16(const __half* x, const __half* g, int K, float eps, __half* xs,
-                                float* red, int cap_lo, int cap_hi, float* cap) {
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nv = K / 8;
-  const uint4* x4 = reinterpret_cast<const uint4*>(x);
-  uint4 v[kMaxV16];
-#pragma unroll
-  for (int k = 0; k < kMaxV16; ++k) {
-    const int i = tid + k * kCT;
-    v[k] = i < nv ? __ldcg(x4 + i) : make_uint4(0, 0, 0, 0);
+constexpr int kMaxNC = (kDecMaxVec + kKc - 1) / kKc;        // column chunks of DOWN
+
+// The layer input x, four elements at float4 index i: x_in (fp16) for the
+// first layer of a launch, else fp16(h + the DOWN partials of the previous
+// layer, added in column-chunk order) - that layer's output.
+__device__ __forceinline__ float4 layer_x4(const __half* x16, const float* h, const float* pdown,
+                                           int nc, int K, int i) {
+  if (x16) {
+    const uint2 raw = __ldcg(reinterpret_cast<const uint2*>(x16) + i);
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+    return make_float4(a.x, a.y, b.x, b.y);
   }
+  float4 d[kMaxNC];
+#pragma unroll
+  for (int c = 0; c < kMaxNC; ++c)
+    d[c] = c < nc ? __ldcg(reinterpret_cast<const float4*>(pdown + (size_t)c * K) + i)
+                  : make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 a = __ldcg(reinterpret_cast<const float4*>(h) + i);
+#pragma unroll
+  for (int c = 0; c < kMaxNC; ++c) {
+    if (c < nc) { a.x += d[c].x; a.y += d[c].y; a.z += d[c].z; a.w += d[c].w; }
+  }
+  a.x = __half2float(__float2half_rn(a.x));
+  a.y = __half2float(__float2half_rn(a.y));
+  a.z = __half2float(__float2half_rn(a.z));
+  a.w = __half2float(__float2half_rn(a.w));
+  return a;
+}
+
+// QKV staging: xs = fp16(x * rsqrt(mean(x^2) + eps) * g) for the layer input
+// x (see layer_x4); x[cap_lo, cap_hi) is also kept in cap[] for the o_proj
+// residual.  x itself (fp16-exact) is parked in xs between the two passes.
+__device__ void stage_qkv(const __half* x16, const float* h, const float* pdown, int nc, int K,
+                          const __half* g, float eps, __half* xs, float* red, int cap_lo,
+                          int cap_hi, float* cap) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nv = K / 4;
+  const uint2* g2 = reinterpret_cast<const uint2*>(g);
+  const uint2 g_first = tid < nv ? __ldg(g2 + tid) : make_uint2(0u, 0u);  // early
   float ss = 0.f;
+#pragma unroll 1
+  for (int i = tid; i < nv; i += kCT) {
+    const float4 v = layer_x4(x16, h, pdown, nc, K, i);
+    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+    const float f[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-  for (int k = 0; k < kMaxV16; ++k) {
-    float f[8];
-    h8_to_f32(v[k], f);
-    const int i0 = 8 * (tid + k * kCT);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      ss += f[e] * f[e];
-      if (i0 + e >= cap_lo && i0 + e < cap_hi) cap[i0 + e - cap_lo] = f[e];
-    }
+    for (int e = 0; e < 4; ++e)
+      if (4 * i + e >= cap_lo && 4 * i + e < cap_hi) cap[4 * i + e - cap_lo] = f[e];
+    uint2 o;
+    *reinterpret_cast<__half2*>(&o.x) = __floats2half2_rn(v.x, v.y);
+    *reinterpret_cast<__half2*>(&o.y) = __floats2half2_rn(v.z, v.w);
+    reinterpret_cast<uint2*>(xs)[i] = o;
   }
   ss = warp_sum(ss);
   if (lane == 0) red[warp] = ss;
@@ -282,21 +373,17 @@ __device__ void stage_rmsnorm16(const __half* x, const __half* g, int K, float e
 #pragma unroll
   for (int w = 0; w < kCW; ++w) tot += red[w];
   const float r = rsqrtf(tot / (float)K + eps);
-  const uint4* g4 = reinterpret_cast<const uint4*>(g);
-#pragma unroll
-  for (int k = 0; k < kMaxV16; ++k) {
-    const int i = tid + k * kCT;
-    if (i < nv) {
-      float f[8], gf[8];
-      h8_to_f32(v[k], f);
-      h8_to_f32(__ldg(g4 + i), gf);
-      uint4 o;
-      __half2* oh = reinterpret_cast<__half2*>(&o);
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        oh[e] = __floats2half2_rn(f[2 * e] * r * gf[2 * e], f[2 * e + 1] * r * gf[2 * e + 1]);
-      reinterpret_cast<uint4*>(xs)[i] = o;
-    }
+  for (int i = tid; i < nv; i += kCT) {
+    const uint2 graw = i == tid ? g_first : __ldg(g2 + i);
+    const uint2 xraw = reinterpret_cast<const uint2*>(xs)[i];
+    const float2 ga = __half22float2(*reinterpret_cast<const __half2*>(&graw.x));
+    const float2 gb = __half22float2(*reinterpret_cast<const __half2*>(&graw.y));
+    const float2 xa = __half22float2(*reinterpret_cast<const __half2*>(&xraw.x));
+    const float2 xb = __half22float2(*reinterpret_cast<const __half2*>(&xraw.y));
+    uint2 o;
+    *reinterpret_cast<__half2*>(&o.x) = __floats2half2_rn(xa.x * r * ga.x, xa.y * r * ga.y);
+    *reinterpret_cast<__half2*>(&o.y) = __floats2half2_rn(xb.x * r * gb.x, xb.y * r * gb.y);
+    reinterpret_cast<uint2*>(xs)[i] = o;
   }
   named_sync(1, kCT);
 }
@@ -306,11 +393,14 @@ __device__ void stage_rmsnorm32(const float* x, const __half* g, int K, float ep
                                 float* red) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nv = K / 4;
   const float4* x4 = reinterpret_cast<const float4*>(x);
+  const uint2* g2 = reinterpret_cast<const uint2*>(g);
   float4 v[kMaxV32];
+  uint2 gr[kMaxV32];   // the gains travel with x: one round trip for both
 #pragma unroll
   for (int k = 0; k < kMaxV32; ++k) {
     const int i = tid + k * kCT;
     v[k] = i < nv ? __ldcg(x4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    gr[k] = i < nv ? __ldg(g2 + i) : make_uint2(0u, 0u);
   }
   float ss = 0.f;
 #pragma unroll
@@ -322,12 +412,11 @@ __device__ void stage_rmsnorm32(const float* x, const __half* g, int K, float ep
 #pragma unroll
   for (int w = 0; w < kCW; ++w) tot += red[w];
   const float r = rsqrtf(tot / (float)K + eps);
-  const uint2* g2 = reinterpret_cast<const uint2*>(g);
 #pragma unroll
   for (int k = 0; k < kMaxV32; ++k) {
     const int i = tid + k * kCT;
     if (i < nv) {
-      const uint2 graw = __ldg(g2 + i);
+      const uint2 graw = gr[k];
       const float2 ga = __half22float2(*reinterpret_cast<const __half2*>(&graw.x));
       const float2 gb = __half22float2(*reinterpret_cast<const __half2*>(&graw.y));
       uint2 o;
@@ -358,58 +447,75 @@ __device__ void stage_copy(const __half* src, int K, __half* xs) {
 }
 
 // o_proj input when the attention used few splits: xs[h*D + d] = attention
-// output of query head h, merged here from the S split partials (acc, max,
-// sum) instead of in a separate phase.  One thread per 4 consecutive d.
+// output of query head h, merged here from the S <= 32 split partials
+// (acc, max, sum) instead of in a separate phase.  One warp per head: lane s
+// loads the (max, sum) of split s, every lane the D/32 accumulator values it
+// owns for up to 16 splits at a time, all in one round trip.
 template <int D>
 __device__ void stage_combine(const DecodeParams& p, __half* xs) {
-  constexpr int kMaxS = 32;
-  const int n4 = p.Hq * D / 4;
-  for (int c = threadIdx.x; c < n4; c += kCT) {
-    const int hq = (4 * c) / D, d = (4 * c) % D;
-    const float* base = p.part + (size_t)hq * p.S * (D + 4);
-    float2 ml[kMaxS];   // (max, sum) of every split, loaded first
+  constexpr int kDL = D / 32;   // d values per lane
+  constexpr int kB = 16;        // splits per load batch
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int S = p.S;
+  for (int hq = warp; hq < p.Hq; hq += kCW) {
+    const float* base = p.part + (size_t)hq * S * (D + 4);
+    const float2 ml = lane < S ? __ldcg(reinterpret_cast<const float2*>(base + (size_t)lane * (D + 4) + D))
+                               : make_float2(-INFINITY, 0.f);
+    float o[kDL];
 #pragma unroll
-    for (int s = 0; s < kMaxS; ++s)
-      ml[s] = s < p.S ? __ldcg(reinterpret_cast<const float2*>(base + (size_t)s * (D + 4) + D))
-                      : make_float2(-INFINITY, 0.f);
-    float M = -INFINITY;
+    for (int e = 0; e < kDL; ++e) o[e] = 0.f;
+    float wl = 0.f, Ls = 0.f;
+    for (int s0 = 0; s0 < S; s0 += kB) {
+      float a[kB][kDL];
 #pragma unroll
-    for (int s = 0; s < kMaxS; ++s) M = fmaxf(M, ml[s].x);
-    float Ls = 0.f;
-    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int j = 0; j < kB; ++j) {
+        const float* src = base + (size_t)(s0 + j) * (D + 4) + lane * kDL;
+        if (s0 + j < S) {
+          if constexpr (kDL == 4) {
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(src));
+            a[j][0] = v.x; a[j][1] = v.y; a[j][2] = v.z; a[j][3] = v.w;
+          } else {
+            const float2 v = __ldcg(reinterpret_cast<const float2*>(src));
+            a[j][0] = v.x; a[j][1] = v.y;
+          }
+        } else {
 #pragma unroll
-    for (int s0 = 0; s0 < kMaxS; s0 += 8) {   // accumulators in batches of 8 loads
-      if (s0 >= p.S) break;
-      float4 a[8];
+          for (int e = 0; e < kDL; ++e) a[j][e] = 0.f;
+        }
+      }
+      if (s0 == 0) {
+        const float M = warp_max(ml.x);
+        wl = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
+        Ls = warp_sum(ml.y * wl);
+      }
 #pragma unroll
-      for (int k = 0; k < 8; ++k)
-        a[k] = s0 + k < p.S
-                   ? __ldcg(reinterpret_cast<const float4*>(base + (size_t)(s0 + k) * (D + 4) + d))
-                   : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int j = 0; j < kB; ++j) {
+        const float w = __shfl_sync(0xffffffffu, wl, (s0 + j) & 31);
+        if (s0 + j < S) {
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const float w = ml[s0 + k].x == -INFINITY ? 0.f : exp2f(ml[s0 + k].x - M);
-        Ls += ml[s0 + k].y * w;
-        O.x += a[k].x * w; O.y += a[k].y * w; O.z += a[k].z * w; O.w += a[k].w * w;
+          for (int e = 0; e < kDL; ++e) o[e] += a[j][e] * w;
+        }
       }
     }
     const float inv = 1.f / Ls;
-    __half2* dst = reinterpret_cast<__half2*>(xs + hq * D + d);
-    dst[0] = __floats2half2_rn(O.x * inv, O.y * inv);
-    dst[1] = __floats2half2_rn(O.z * inv, O.w * inv);
+#pragma unroll
+    for (int e = 0; e < kDL; e += 2)
+      *reinterpret_cast<__half2*>(xs + hq * D + lane * kDL + e) =
+          __floats2half2_rn(o[e] * inv, o[e + 1] * inv);
   }
   named_sync(1, kCT);
 }
 
 // Position in this CTA's stream of ring chunks: layer l, phase ph, and
-// within the phase either the K/V tile c or the (row group g0, column chunk
-// kc) of the phase's weight rows.
+// within the phase either the K/V tile c or (group gi, column chunk kc).
 struct Cursor {
-  int l, ph, c, g0, kc;
-  PhaseRows R;
+  int l, ph, c, gi, kc;
+  PhaseWork W;
+  GroupDesc g;
 };
 
 // Settles on the first chunk at or after (l, ph); false past the last layer.
+template <int D>
 __device__ bool cursor_begin(Cursor& cu, const DecodeParams& p, const AttnRange& ar) {
   for (; cu.l < p.n_layers; ++cu.l, cu.ph = 0) {
     for (; cu.ph < kPhases; ++cu.ph) {
@@ -418,24 +524,32 @@ __device__ bool cursor_begin(Cursor& cu, const DecodeParams& p, const AttnRange&
         if (ar.chunks > 0) { cu.c = 0; return true; }
         continue;
       }
-      cu.R = phase_rows(p, cu.ph);
-      if (cu.R.nrows > 0) { cu.g0 = 0; cu.kc = 0; return true; }
+      cu.W = phase_work<D>(p, cu.ph);
+      if (cu.W.ngroups > 0) {
+        cu.gi = 0;
+        cu.g = group_desc<D>(p, cu.ph, cu.W, 0);
+        cu.kc = cu.g.ka;
+        return true;
+      }
     }
   }
   return false;
 }
 
+template <int D>
 __device__ bool cursor_next(Cursor& cu, const DecodeParams& p, const AttnRange& ar) {
   if (cu.ph == kPhAttn) {
     if (++cu.c < ar.chunks) return true;
   } else {
-    if (++cu.kc < cu.R.ncol) return true;
-    cu.kc = 0;
-    cu.g0 += kGroupRows;
-    if (cu.g0 < cu.R.nrows) return true;
+    if (++cu.kc < cu.g.kb) return true;
+    if (++cu.gi < cu.W.ngroups) {
+      cu.g = group_desc<D>(p, cu.ph, cu.W, cu.gi);
+      cu.kc = cu.g.ka;
+      return true;
+    }
   }
   ++cu.ph;
-  return cursor_begin(cu, p, ar);
+  return cursor_begin<D>(cu, p, ar);
 }
 
 // Optional timeline: thread 0 of every CTA records %globaltimer when a phase
@@ -462,8 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* empty = full + kStages;
   float* red = reinterpret_cast<float*>(empty + kStages);        // [16]
   volatile int* abort_flag = reinterpret_cast<volatile int*>(red + 16);
-  float* xres = reinterpret_cast<float*>(smem + kResOff);       // x[r0 + k]
-  float* hres = xres + kResRows;                                // h[r0 + k]
+  float* xres = reinterpret_cast<float*>(smem + kResOff);       // x of the o_proj rows
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
@@ -485,13 +598,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   // free ring stage.
   if (warp == kCW) {
     if (lane != 0) return;
+    // column blocks one box copy covers in chunk kc of role r
+    auto box_cbs = [&](int r, int kc) -> int {
+      return p.w3d[r] ? p.wbox_z[r] : min(kCB, p.wnz[r] - kc * kCB);
+    };
     auto chunk_bytes = [&](const Cursor& cu) -> uint32_t {
       if (cu.ph == kPhAttn) return 2u * kv_tile_bytes;
-      const int nr = min(kGroupRows, cu.R.nrows - cu.g0);
-      return (uint32_t)nr * (uint32_t)min(kKc, cu.R.K - cu.kc * kKc) * 2u;
+      const uint32_t nb = cu.g.yb >= 0 ? 2u : 1u;
+      return nb * (uint32_t)(kBoxRows * 128) * (uint32_t)box_cbs(cu.g.ra, cu.kc);
     };
     auto kv_row = [&](const Cursor& cu) {
       return (int)(ar.g * p.max_ctx + ar.j0 + (int64_t)cu.c * kSlots);
+    };
+    // one 8-row box of role r at row y, column chunk kc: a single 3-D copy,
+    // or (K not a multiple of 64) one 2-D copy per 64-column block
+    auto copy_box = [&](int l, int r, int y, int kc, uint32_t dst, uint32_t bar) {
+      const CUtensorMap* m = &p.tm_w[l][r];
+      if (p.w3d[r]) {
+        tma_load_3d(dst, m, 0, y, kc * kCB, bar);
+      } else {
+        const int n = min(kCB, p.wnz[r] - kc * kCB);
+        for (int cb = 0; cb < n; ++cb)
+          tma_load_2d_u32(dst + cb * (kBoxRows * 128), m, (kc * kCB + cb) * 64, y, bar);
+      }
     };
     auto load = [&](const Cursor& cu, uint8_t* st, uint64_t* bar) {
       if (cu.ph == kPhAttn) {
@@ -503,14 +632,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         return;
       }
-      const int nr = min(kGroupRows, cu.R.nrows - cu.g0);
-      const uint32_t rb = (uint32_t)min(kKc, cu.R.K - cu.kc * kKc) * 2u;
-      for (int r = 0; r < nr; ++r)
-        bulk_g2s(st + r * kRowStride,
-                 row_ptr(p, p.layer[cu.l], cu.ph, cu.R, cu.g0 + r) + cu.kc * kKc, rb, bar);
+      const uint32_t dst = smem_u32(st), mb = smem_u32(bar);
+      copy_box(cu.l, cu.g.ra, cu.g.ya, cu.kc, dst, mb);
+      if (cu.g.yb >= 0) copy_box(cu.l, cu.g.rb, cu.g.yb, cu.kc, dst + kBoxBytes, mb);
     };
-    Cursor rc = {0, 0, 0, 0, 0, {}};
-    bool more = cursor_begin(rc, p, ar);
+    // While the ring is full the lane asks L2 for the chunks that come next
+    // (up to kPfAhead of them): the TMA unit and HBM would otherwise idle
+    // while the consumers wait at a grid barrier, and those chunks then load
+    // from L2.
+    auto prefetch = [&](const Cursor& cu) {
+      if (cu.ph == kPhAttn) {
+        const int y = kv_row(cu);
+#pragma unroll
+        for (int h = 0; h < D / 64; ++h) {
+          tma_prefetch_2d(&p.tm_k[cu.l], h * 64, y);
+          tma_prefetch_2d(&p.tm_v[cu.l], h * 64, y);
+        }
+        return;
+      }
+      const int ys[2] = {cu.g.ya, cu.g.yb}, rs[2] = {cu.g.ra, cu.g.rb};
+      for (int b = 0; b < 2; ++b) {
+        if (ys[b] < 0) continue;
+        const CUtensorMap* m = &p.tm_w[cu.l][rs[b]];
+        if (p.w3d[rs[b]]) {
+          tma_prefetch_3d(m, 0, ys[b], cu.kc * kCB);
+        } else {
+          const int n = min(kCB, p.wnz[rs[b]] - cu.kc * kCB);
+          for (int cb = 0; cb < n; ++cb) tma_prefetch_2d(m, (cu.kc * kCB + cb) * 64, ys[b]);
+        }
+      }
+    };
+    Cursor rc = {0, 0, 0, 0, 0, {}, {}};
+    bool more = cursor_begin<D>(rc, p, ar);
+    Cursor pc = rc;     // next chunk to prefetch, index pit
+    bool pmore = more;
+    int pit = 0;
     int it = 0;   // chunks issued to the ring
     bool ok = true;
     while (more && ok) {
@@ -518,7 +674,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (it >= kStages) {
         const uint32_t par = ((it / kStages) - 1) & 1;
         uint64_t t0 = 0;
+        if (pit < it) { pc = rc; pit = it; pmore = more; }
         while (!mbar_test(&empty[s], par)) {
+          if (pmore && pit < it + kPfAhead) {
+            prefetch(pc);
+            ++pit;
+            pmore = cursor_next<D>(pc, p, ar);
+            continue;
+          }
           if (*abort_flag) { ok = false; break; }
           if (t0 == 0) t0 = global_ns();
           else if (global_ns() - t0 > kWaitLimitNs) {
@@ -533,7 +696,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive_expect_tx(&full[s], chunk_bytes(rc));
       load(rc, ring + (size_t)s * kStageBytes, &full[s]);
       ++it;
-      more = cursor_next(rc, p, ar);
+      more = cursor_next<D>(rc, p, ar);
     }
     // Copies still in flight must land before the CTA's shared memory goes away.
     for (int k = max(0, it - kStages); k < it; ++k)
@@ -565,7 +728,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   for (int l = 0; l < p.n_layers; ++l) {
     const DecLayer& Ly = p.layer[l];
-    const __half* x_l = layer_input(p, l);
     for (int ph = 0; ph < kPhases; ++ph) {
       if (ph == kPhComb && p.fold) continue;   // merged into the o_proj staging
       // wait for the producers of this phase's input
@@ -725,46 +887,51 @@ __global__ void __launch_bounds__(kThreads, 1)
             l_r[h2] += __shfl_xor_sync(0xffffffffu, l_r[h2], 1);
             l_r[h2] += __shfl_xor_sync(0xffffffffu, l_r[h2], 2);
           }
-          float* sm_m = reinterpret_cast<float*>(xs);   // [16]
-          float* sm_l = sm_m + 16;                      // [16]
-          float* sm_o = sm_l + 16;                      // [16][D]
-          for (int w = 0; w < kAttnWarps; ++w) {
-            if (warp == w) {
+          // pairwise merge through two buffers {m[16], l[16], o[16][D + 8]} in
+          // the staging area: warps 1, 3 -> 0, 2, then 2 -> 0.  Rows of o are
+          // padded so that the float2 accesses of a warp hit distinct banks.
+          constexpr int kOS = D + 8, kBuf = 32 + 16 * kOS;
+          float* bufs = reinterpret_cast<float*>(xs);
+          auto put = [&](float* bf) {
 #pragma unroll
-              for (int h2 = 0; h2 < 2; ++h2) {
-                const int row = grp + 8 * h2;
-                float a = 0.f, bsc = 1.f, Mx = m_r[h2];
-                if (w > 0) {
-                  const float mo = sm_m[row];
-                  Mx = fmaxf(mo, m_r[h2]);
-                  a = (Mx == -INFINITY) ? 0.f : exp2f(mo - Mx);
-                  bsc = (Mx == -INFINITY) ? 0.f : exp2f(m_r[h2] - Mx);
-                }
+            for (int h2 = 0; h2 < 2; ++h2) {
+              const int row = grp + 8 * h2;
+              if (tig == 0) { bf[row] = m_r[h2]; bf[16 + row] = l_r[h2]; }
 #pragma unroll
-                for (int dn = 0; dn < D / 8; ++dn) {
-                  const int col = dn * 8 + 2 * tig;
-                  float o0 = O[dn][2 * h2] * bsc, o1 = O[dn][2 * h2 + 1] * bsc;
-                  if (w > 0) {
-                    o0 += sm_o[row * D + col] * a;
-                    o1 += sm_o[row * D + col + 1] * a;
-                  }
-                  sm_o[row * D + col] = o0;
-                  sm_o[row * D + col + 1] = o1;
-                }
-                __syncwarp();
-                if (tig == 0) {
-                  const float lo = w > 0 ? sm_l[row] * a : 0.f;
-                  sm_l[row] = lo + l_r[h2] * bsc;
-                  sm_m[row] = Mx;
-                }
-              }
+              for (int dn = 0; dn < D / 8; ++dn)
+                *reinterpret_cast<float2*>(bf + 32 + row * kOS + dn * 8 + 2 * tig) =
+                    make_float2(O[dn][2 * h2], O[dn][2 * h2 + 1]);
             }
-            named_sync(2, kAttnWarps * 32);
-          }
+          };
+          auto merge_from = [&](const float* bf) {
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              const int row = grp + 8 * h2;
+              const float mo = bf[row], lo = bf[16 + row];
+              const float Mx = fmaxf(mo, m_r[h2]);
+              const float a = (Mx == -INFINITY) ? 0.f : exp2f(mo - Mx);
+              const float bsc = (Mx == -INFINITY) ? 0.f : exp2f(m_r[h2] - Mx);
+#pragma unroll
+              for (int dn = 0; dn < D / 8; ++dn) {
+                const float2 o = *reinterpret_cast<const float2*>(bf + 32 + row * kOS + dn * 8 + 2 * tig);
+                O[dn][2 * h2] = O[dn][2 * h2] * bsc + o.x * a;
+                O[dn][2 * h2 + 1] = O[dn][2 * h2 + 1] * bsc + o.y * a;
+              }
+              l_r[h2] = l_r[h2] * bsc + lo * a;
+              m_r[h2] = Mx;
+            }
+          };
+          if (warp & 1) put(bufs + (warp >> 1) * kBuf);
+          named_sync(2, kAttnWarps * 32);
+          if (!(warp & 1)) merge_from(bufs + (warp >> 1) * kBuf);
+          if (warp == 2) { __syncwarp(); put(bufs + kBuf); }
+          named_sync(2, kAttnWarps * 32);
+          if (warp == 0) { merge_from(bufs + kBuf); put(bufs); }
+          named_sync(2, kAttnWarps * 32);
           if (ar.active) {
             for (int i = tid; i < G * (D + 2); i += kAttnWarps * 32) {
               const int row = i / (D + 2), k = i % (D + 2);
-              const float v = k < D ? sm_o[row * D + k] : (k == D ? sm_m[row] : sm_l[row]);
+              const float v = k < D ? bufs[32 + row * kOS + k] : (k == D ? bufs[row] : bufs[16 + row]);
               p.part[((size_t)(ar.g * G + row) * p.S + ar.s) * (D + 4) + k] = v;
             }
           }
@@ -805,124 +972,153 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
         // ---------------------------------------------------- projections
-        const PhaseRows R = phase_rows(p, ph);
+        const PhaseWork W = phase_work<D>(p, ph);
+        // bias and RoPE factors of a QKV epilogue item (group gi, tile row m < 8)
+        struct QkvConst { float blo, bhi; float2 cs; };
+        auto qkv_const = [&](int gi, int m) {
+          constexpr int upd = D / 16;
+          const int u = W.first + gi, hd = u / upd, i = (u % upd) * kBoxRows + m;
+          QkvConst c{0.f, 0.f, make_float2(1.f, 0.f)};
+          const __half* bias;
+          int row;
+          if (hd < p.Hq) { bias = Ly.bq; row = hd * D; }
+          else if (hd < p.Hq + p.Hkv) { bias = Ly.bk; row = (hd - p.Hq) * D; }
+          else { bias = Ly.bv; row = (hd - p.Hq - p.Hkv) * D; }
+          if (bias) {
+            c.blo = __half2float(bias[row + i]);
+            c.bhi = __half2float(bias[row + half + i]);
+          }
+          if (hd < p.Hq + p.Hkv) c.cs = rope_cs(p.rope, p.rope_len, half, pos, i, p.err);
+          return c;
+        };
+        // those of this thread's item in the first batch, fetched before the
+        // staging so that their latency overlaps it
+        QkvConst qc0{0.f, 0.f, make_float2(1.f, 0.f)};
+        if (ph == kPhQKV && tid < min(W.ngroups, kBatch) * 16 && (tid & 15) < kBoxRows)
+          qc0 = qkv_const(tid >> 4, tid & 15);
         if (ph == kPhQKV) {
-          const PhaseRows RO = phase_rows(p, kPhO);   // rows whose residual we keep
-          stage_rmsnorm16(x_l, Ly.ln1, p.H, p.eps, xs, red, RO.first, RO.first + RO.units, xres);
+          const PhaseWork WO = phase_work<D>(p, kPhO);   // rows whose residual we keep
+          stage_qkv(l == 0 ? p.x_in : nullptr, p.h32, p.pdown, p.nc_down, p.H, Ly.ln1, p.eps,
+                    xs, red, WO.first * kBoxRows, (WO.first + WO.count) * kBoxRows, xres);
         } else if (ph == kPhGU) {
           stage_rmsnorm32(p.h32, Ly.ln2, p.H, p.eps, xs, red);
         } else if (ph == kPhO && p.fold) {
           stage_combine<D>(p, xs);
         } else {
-          stage_copy(ph == kPhO ? p.attn16 : p.act16, R.K, xs);
+          stage_copy(ph == kPhO ? p.attn16 : p.act16, W.K, xs);
         }
-        // y[q] = W[q] . x on the tensor cores: A = 16 staged rows x 16
-        // columns (ldmatrix), B = x as the only non-zero column, fp32
-        // accumulators; the warps split each stage's 16-column steps.
-        const int tg = lane & 3;
-        for (int g0 = 0, gi = 0; g0 < R.nrows; g0 += kGroupRows, ++gi) {
-          float d[4] = {0.f, 0.f, 0.f, 0.f};
-          for (int kc = 0; kc < R.ncol; ++kc) {
-            int s;
-            if (!take(s)) break;
-            const int nks = min(kKc, R.K - kc * kKc) / 16;
-            const int ks0 = warp * nks / kCW, ks1 = (warp + 1) * nks / kCW;
-            const uint32_t st = smem_u32(ring + (size_t)s * kStageBytes);
-            const int m = lane >> 3;
-            const uint32_t arow = st + ((lane & 7) + (m & 1) * 8) * kRowStride + (m >> 1) * 16;
-            const __half* xk = xs + kc * kKc + 2 * tg;
-            for (int ks = ks0; ks < ks1; ++ks) {
-              uint32_t a[4];
-              ldsm_x4(arow + ks * 32, a);
-              uint32_t b0 = 0u, b1 = 0u;
-              if (lane < 4) {
-                b0 = *reinterpret_cast<const uint32_t*>(xk + ks * 16);
-                b1 = *reinterpret_cast<const uint32_t*>(xk + ks * 16 + 8);
+        // y = W x on the tensor cores: A = a chunk's 16 rows x 16 columns
+        // (ldmatrix from the two swizzled boxes), B = x as the only non-zero
+        // column, fp32 accumulators; the warps split each chunk's 16-column
+        // steps.  Partials of up to kBatch groups stay in shared memory and
+        // the epilogue adds them in warp order.
+        const int tg = lane & 3, m8 = lane >> 3, r8 = lane & 7;
+        const uint32_t abox = (uint32_t)((m8 & 1) * kBoxBytes + r8 * 128);
+        const int khalf = m8 >> 1;
+        for (int b0 = 0; b0 < W.ngroups; b0 += kBatch) {
+          const int b1 = min(W.ngroups, b0 + kBatch);
+          for (int gi = b0; gi < b1; ++gi) {
+            const GroupDesc g = group_desc<D>(p, ph, W, gi);
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int kc = g.ka; kc < g.kb; ++kc) {
+              int s;
+              if (!take(s)) break;
+              const int nks = min(kKc, W.K - kc * kKc) / 16;
+              const int ks0 = warp * nks / kCW, ks1 = (warp + 1) * nks / kCW;
+              const uint32_t st = smem_u32(ring + (size_t)s * kStageBytes) + abox;
+              const __half* xk = xs + kc * kKc + 2 * tg;
+              for (int ks = ks0; ks < ks1; ++ks) {
+                uint32_t a[4];
+                ldsm_x4(st + (ks >> 2) * 1024 + (((((ks & 3) << 1) | khalf) ^ r8) << 4), a);
+                uint32_t x0 = 0u, x1 = 0u;
+                if (lane < 4) {
+                  x0 = *reinterpret_cast<const uint32_t*>(xk + ks * 16);
+                  x1 = *reinterpret_cast<const uint32_t*>(xk + ks * 16 + 8);
+                }
+                mma16816(d, a, x0, x1);
               }
-              mma16816(d, a, b0, b1);
+              give(s);
             }
-            give(s);
+            if (tg == 0) {  // column 0 of the 16 x 8 accumulator: rows lane/4 and lane/4 + 8
+              float* pr = part + ((gi - b0) * kCW + warp) * 16;
+              pr[lane >> 2] = d[0];
+              pr[(lane >> 2) + 8] = d[2];
+            }
           }
-          if (tg == 0) {  // column 0 of the 16 x 8 accumulator: rows lane/4 and lane/4 + 8
-            float* pr = part + (gi * kCW + warp) * 16;
-            pr[lane >> 2] = d[0];
-            pr[(lane >> 2) + 8] = d[2];
-          }
-        }
-        named_sync(1, kCT);
-        if (*abort_flag) return;
-        auto val = [&](int q) {  // fixed-order sum over the warps' partials
-          const float* pr = part + (q / kGroupRows) * kCW * 16 + q % kGroupRows;
-          float a = 0.f;
+          named_sync(1, kCT);
+          if (*abort_flag) return;
+          auto val = [&](int gl, int m) {  // fixed-order sum over the warps' partials
+            const float* pr = part + gl * kCW * 16 + m;
+            float a = 0.f;
 #pragma unroll
-          for (int w = 0; w < kCW; ++w) a += pr[w * 16];
-          return a;
-        };
-        if (ph == kPhQKV) {
-          for (int k = tid; k < R.units; k += kCT) {
-            const int u = R.first + k, hd = u / half, i = u % half;
-            float lo = val(k), hi = val(R.units + k);
-            if (hd < p.Hq) {
-              if (Ly.bq) {
-                lo += __half2float(Ly.bq[hd * D + i]);
-                hi += __half2float(Ly.bq[hd * D + half + i]);
+            for (int w = 0; w < kCW; ++w) a += pr[w * 16];
+            return a;
+          };
+          for (int e = tid; e < (b1 - b0) * 16; e += kCT) {
+            const int gl = e >> 4, m = e & 15, gi = b0 + gl;
+            if (ph == kPhQKV) {
+              if (m >= kBoxRows) continue;
+              constexpr int upd = D / 16;
+              const int u = W.first + gi, hd = u / upd, i = (u % upd) * kBoxRows + m;
+              const QkvConst c = b0 == 0 ? qc0 : qkv_const(gi, m);
+              const float lo = val(gl, m) + c.blo, hi = val(gl, m + kBoxRows) + c.bhi;
+              const float2 cs = c.cs;
+              if (hd < p.Hq) {
+                p.q32[hd * D + i] = lo * cs.x - hi * cs.y;
+                p.q32[hd * D + half + i] = hi * cs.x + lo * cs.y;
+              } else if (hd < p.Hq + p.Hkv) {
+                const int gk = hd - p.Hq;
+                const __half a = __float2half_rn(lo * cs.x - hi * cs.y);
+                const __half bb = __float2half_rn(hi * cs.x + lo * cs.y);
+                __half* dst = Ly.kc + ((size_t)gk * p.max_ctx + L) * D;
+                dst[i] = a;
+                dst[half + i] = bb;
+                if (Ly.k_new) {
+                  Ly.k_new[gk * D + i] = a;
+                  Ly.k_new[gk * D + half + i] = bb;
+                }
+              } else {
+                const int gv = hd - p.Hq - p.Hkv;
+                const __half a = __float2half_rn(lo), bb = __float2half_rn(hi);
+                __half* dst = Ly.vc + ((size_t)gv * p.max_ctx + L) * D;
+                dst[i] = a;
+                dst[half + i] = bb;
+                if (Ly.v_new) {
+                  Ly.v_new[gv * D + i] = a;
+                  Ly.v_new[gv * D + half + i] = bb;
+                }
               }
-              const float2 cs = rope_cs(p.rope, p.rope_len, half, pos, i, p.err);
-              p.q32[hd * D + i] = lo * cs.x - hi * cs.y;
-              p.q32[hd * D + half + i] = hi * cs.x + lo * cs.y;
-            } else if (hd < p.Hq + p.Hkv) {
-              const int g = hd - p.Hq;
-              if (Ly.bk) {
-                lo += __half2float(Ly.bk[g * D + i]);
-                hi += __half2float(Ly.bk[g * D + half + i]);
-              }
-              const float2 cs = rope_cs(p.rope, p.rope_len, half, pos, i, p.err);
-              const __half a = __float2half_rn(lo * cs.x - hi * cs.y);
-              const __half bb = __float2half_rn(hi * cs.x + lo * cs.y);
-              __half* dst = Ly.kc + ((size_t)g * p.max_ctx + L) * D;
-              dst[i] = a;
-              dst[half + i] = bb;
-              if (Ly.k_new) {
-                Ly.k_new[g * D + i] = a;
-                Ly.k_new[g * D + half + i] = bb;
-              }
+            } else if (ph == kPhO) {
+              const int row = (W.first + 2 * gi) * kBoxRows + m;
+              if (row < (W.first + W.count) * kBoxRows)
+                p.h32[row] = val(gl, m) + xres[row - W.first * kBoxRows];
+            } else if (ph == kPhGU) {
+              if (m >= kBoxRows) continue;
+              const int j = (W.first + gi) * kBoxRows + m;
+              p.act16[j] = __float2half_rn(silu(val(gl, m)) * val(gl, m + kBoxRows));
             } else {
-              const int g = hd - p.Hq - p.Hkv;
-              if (Ly.bv) {
-                lo += __half2float(Ly.bv[g * D + i]);
-                hi += __half2float(Ly.bv[g * D + half + i]);
-              }
-              const __half a = __float2half_rn(lo), bb = __float2half_rn(hi);
-              __half* dst = Ly.vc + ((size_t)g * p.max_ctx + L) * D;
-              dst[i] = a;
-              dst[half + i] = bb;
-              if (Ly.v_new) {
-                Ly.v_new[g * D + i] = a;
-                Ly.v_new[g * D + half + i] = bb;
-              }
+              const int it = W.first + gi, row = (it / W.ncol) * 2 * kBoxRows + m;
+              if (row < p.H) p.pdown[(size_t)(it % W.ncol) * p.H + row] = val(gl, m);
             }
           }
-        } else if (ph == kPhO) {
-          const int r0 = R.first;
-          for (int k = tid; k < R.units; k += kCT) {
-            const float hv = val(k) + xres[k];
-            p.h32[r0 + k] = hv;
-            hres[k] = hv;   // the down phase owns the same rows
-          }
-        } else if (ph == kPhGU) {
-          const int j0 = R.first;
-          for (int k = tid; k < R.units; k += kCT)
-            p.act16[j0 + k] = __float2half_rn(silu(val(k)) * val(R.units + k));
-        } else {
-          const int r0 = R.first;
-          __half* y = layer_output(p, l);
-          for (int k = tid; k < R.units; k += kCT)
-            y[r0 + k] = __float2half_rn(val(k) + hres[k]);
+          named_sync(1, kCT);   // the partials are reused by the next batch
         }
       }
       trace_point(p, l, ph, 1);
-      if (l == p.n_layers - 1 && ph == kPhDown) break;  // last phase of the step
       grid_arrive(sync);
+    }
+  }
+  // final phase: the last layer's output, fp16(h + its DOWN partials)
+  if (!grid_wait(sync, bar++)) return;
+  {
+    const int nv = p.H / 4, G = gridDim.x;
+    const int i0 = (int)((int64_t)blockIdx.x * nv / G), i1 = (int)((int64_t)(blockIdx.x + 1) * nv / G);
+    for (int i = i0 + tid; i < i1; i += kCT) {
+      const float4 v = layer_x4(nullptr, p.h32, p.pdown, p.nc_down, p.H, i);
+      uint2 o;
+      *reinterpret_cast<__half2*>(&o.x) = __floats2half2_rn(v.x, v.y);
+      *reinterpret_cast<__half2*>(&o.y) = __floats2half2_rn(v.z, v.w);
+      reinterpret_cast<uint2*>(p.out)[i] = o;
     }
   }
 }
@@ -935,7 +1131,7 @@ size_t decode_ws_bytes(int H, int Hq, int Hkv, int D, int I, int num_sms) {
   const size_t S = (size_t)(num_sms / Hkv);
   auto al = [](size_t v) { return (v + 255) & ~(size_t)255; };
   size_t o = 0;
-  o += al((size_t)H * 2) * 2;               // xbuf0, xbuf1
+  o += al((size_t)H * 4 * ((I + kKc - 1) / kKc));   // pdown
   o += al((size_t)Hq * D * 4);              // q32
   o += al((size_t)Hq * S * (D + 4) * 4);    // part
   o += al((size_t)Hq * D * 2);              // attn16
@@ -950,8 +1146,8 @@ void decode_ws_carve(DecodeParams& p, void* ws, int num_sms) {
   auto al = [](size_t v) { return (v + 255) & ~(size_t)255; };
   uint8_t* b = static_cast<uint8_t*>(ws);
   size_t o = 0;
-  p.xbuf0 = reinterpret_cast<__half*>(b + o); o += al((size_t)p.H * 2);
-  p.xbuf1 = reinterpret_cast<__half*>(b + o); o += al((size_t)p.H * 2);
+  p.nc_down = (p.I + kKc - 1) / kKc;
+  p.pdown = reinterpret_cast<float*>(b + o); o += al((size_t)p.H * 4 * p.nc_down);
   p.q32 = reinterpret_cast<float*>(b + o); o += al((size_t)p.Hq * p.D * 4);
   p.part = reinterpret_cast<float*>(b + o); o += al((size_t)p.Hq * S * (p.D + 4) * 4);
   p.attn16 = reinterpret_cast<__half*>(b + o); o += al((size_t)p.Hq * p.D * 2);

@@ -9,7 +9,7 @@
 
 namespace blk {
 
-constexpr int kDecMaxLayers = 32;  // layers per launch (the host loops beyond)
+constexpr int kDecMaxLayers = 16;  // layers per launch (the host loops beyond)
 constexpr int kDecMaxVec = 12288;  // longest input vector a phase stages (elements)
 
 struct DecLayer {
@@ -20,9 +20,17 @@ struct DecLayer {
   __half* v_new;
 };
 
+constexpr int kDecRoles = 7;       // wq wk wv wo w_gate w_up w_down
+
 struct DecodeParams {
   CUtensorMap tm_k[kDecMaxLayers];  // cache viewed as [Hkv * max_ctx, D], box 64 x 64, SW128
   CUtensorMap tm_v[kDecMaxLayers];
+  // weights [rows, K]: 3-D view (64, rows, K / 64) with box (64, 8, min(24, K / 64)) when
+  // K % 64 == 0, else 2-D (K, rows) with box (64, 8); 128-byte swizzle either way
+  CUtensorMap tm_w[kDecMaxLayers][kDecRoles];
+  int w3d[kDecRoles];     // 1: tm_w of this role is the 3-D view
+  int wbox_z[kDecRoles];  // 3-D box depth (column blocks)
+  int wnz[kDecRoles];     // column blocks of 64 in K, rounded up
   DecLayer layer[kDecMaxLayers];
   int n_layers;
   int H, Hq, Hkv, D, I;
@@ -36,8 +44,8 @@ struct DecodeParams {
   const __half* x_in;   // [H]
   __half* out;          // [H]
   // workspace
-  __half* xbuf0;        // [H] ping-pong layer outputs
-  __half* xbuf1;
+  float* pdown;         // [nc_down][H] DOWN partials per 1536-column chunk
+  int nc_down;
   float* q32;           // [Hq * D]
   float* part;          // [Hq][S][D + 4]  (acc[D], m, l, pad): rows 16-byte aligned
   __half* attn16;       // [Hq * D]
@@ -55,6 +63,8 @@ struct DecodeParams {
 size_t decode_ws_bytes(int H, int Hq, int Hkv, int D, int I, int num_sms);
 // Carves the workspace and fills the workspace pointers of `p`.
 void decode_ws_carve(DecodeParams& p, void* ws, int num_sms);
+
+static_assert(sizeof(DecodeParams) <= 32764, "kernel parameter space");
 
 cudaError_t launch_decode_persistent(DecodeParams& p, int num_sms, cudaStream_t s);
 cudaError_t configure_decode_persistent();

@@ -46,6 +46,11 @@ struct TcGemmParams {
 // 128-byte swizzle, zero fill out of bounds.  Returns 0 on success.
 int make_tmap_2d(CUtensorMap* map, const void* base, int64_t rows, int64_t K,
                  int box_rows);
+// Tensor map of 8-row weight boxes with 128-byte swizzle for the decode
+// kernel: the 3-D view (64, rows, K / 64) with box (64, 8, cbs) when
+// K % 64 == 0 (*is3d = 1), else the 2-D view (K, rows) with box (64, 8).
+int make_tmap_rows8(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int cbs,
+                    int* is3d);
 
 cudaError_t launch_tc_gemm(TcGemmParams& p, int epi, int num_sms, cudaStream_t s,
                            bool pdl);
