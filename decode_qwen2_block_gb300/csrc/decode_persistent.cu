@@ -37,6 +37,8 @@
 //
 // Every wait (ring mbarriers, grid barrier) is bounded; on a timeout the
 // kernel records an error, stops, lets its issued copies land and returns.
+#include <type_traits>
+
 #include "common.cuh"
 #include "decode_persistent.h"
 
@@ -446,54 +448,50 @@ __device__ void stage_copy(const __half* src, int K, __half* xs) {
   named_sync(1, kCT);
 }
 
+// Bytes of one attention partial: acc / sum as D fp16 values, then the
+// split's (max, sum) as float2, padded to 16 bytes.
+__host__ __device__ constexpr int part_row_bytes(int D) { return 2 * D + 16; }
+
 // o_proj input when the attention used few splits: xs[h*D + d] = attention
 // output of query head h, merged here from the S <= 32 split partials
-// (acc, max, sum) instead of in a separate phase.  One warp per head: lane s
-// loads the (max, sum) of split s, every lane the D/32 accumulator values it
-// owns for up to 16 splits at a time, all in one round trip.
+// instead of in a separate phase.  One warp per head: lane s loads the
+// (max, sum) of split s, every lane the D/32 values it owns for every split,
+// all in one round trip.
 template <int D>
 __device__ void stage_combine(const DecodeParams& p, __half* xs) {
   constexpr int kDL = D / 32;   // d values per lane
-  constexpr int kB = 16;        // splits per load batch
+  constexpr int kRB = part_row_bytes(D);
+  constexpr int kMaxS = 32;
+  using Raw = typename std::conditional<kDL == 4, uint2, uint32_t>::type;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = p.S;
   for (int hq = warp; hq < p.Hq; hq += kCW) {
-    const float* base = p.part + (size_t)hq * S * (D + 4);
-    const float2 ml = lane < S ? __ldcg(reinterpret_cast<const float2*>(base + (size_t)lane * (D + 4) + D))
+    const uint8_t* base = p.part + (size_t)hq * S * kRB;
+    const float2 ml = lane < S ? __ldcg(reinterpret_cast<const float2*>(base + (size_t)lane * kRB + 2 * D))
                                : make_float2(-INFINITY, 0.f);
+    Raw a[kMaxS];
+#pragma unroll
+    for (int j = 0; j < kMaxS; ++j) {
+      if (j < S) a[j] = __ldcg(reinterpret_cast<const Raw*>(base + (size_t)j * kRB) + lane);
+      else a[j] = Raw{};
+    }
+    // weight of split s: exp2(m_s - M) * l_s (its values are already / l_s)
+    const float M = warp_max(ml.x);
+    const float wl = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M) * ml.y;
+    const float Ls = warp_sum(wl);
     float o[kDL];
 #pragma unroll
     for (int e = 0; e < kDL; ++e) o[e] = 0.f;
-    float wl = 0.f, Ls = 0.f;
-    for (int s0 = 0; s0 < S; s0 += kB) {
-      float a[kB][kDL];
 #pragma unroll
-      for (int j = 0; j < kB; ++j) {
-        const float* src = base + (size_t)(s0 + j) * (D + 4) + lane * kDL;
-        if (s0 + j < S) {
-          if constexpr (kDL == 4) {
-            const float4 v = __ldcg(reinterpret_cast<const float4*>(src));
-            a[j][0] = v.x; a[j][1] = v.y; a[j][2] = v.z; a[j][3] = v.w;
-          } else {
-            const float2 v = __ldcg(reinterpret_cast<const float2*>(src));
-            a[j][0] = v.x; a[j][1] = v.y;
-          }
-        } else {
+    for (int j = 0; j < kMaxS; ++j) {
+      const float w = __shfl_sync(0xffffffffu, wl, j);
+      if (j < S) {
+        const __half2* h = reinterpret_cast<const __half2*>(&a[j]);
 #pragma unroll
-          for (int e = 0; e < kDL; ++e) a[j][e] = 0.f;
-        }
-      }
-      if (s0 == 0) {
-        const float M = warp_max(ml.x);
-        wl = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
-        Ls = warp_sum(ml.y * wl);
-      }
-#pragma unroll
-      for (int j = 0; j < kB; ++j) {
-        const float w = __shfl_sync(0xffffffffu, wl, (s0 + j) & 31);
-        if (s0 + j < S) {
-#pragma unroll
-          for (int e = 0; e < kDL; ++e) o[e] += a[j][e] * w;
+        for (int e = 0; e < kDL / 2; ++e) {
+          const float2 f = __half22float2(h[e]);
+          o[2 * e] += f.x * w;
+          o[2 * e + 1] += f.y * w;
         }
       }
     }
@@ -929,10 +927,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (warp == 0) { merge_from(bufs + kBuf); put(bufs); }
           named_sync(2, kAttnWarps * 32);
           if (ar.active) {
-            for (int i = tid; i < G * (D + 2); i += kAttnWarps * 32) {
-              const int row = i / (D + 2), k = i % (D + 2);
-              const float v = k < D ? bufs[32 + row * kOS + k] : (k == D ? bufs[row] : bufs[16 + row]);
-              p.part[((size_t)(ar.g * G + row) * p.S + ar.s) * (D + 4) + k] = v;
+            constexpr int kRB = part_row_bytes(D), kPairs = D / 2 + 1;
+            for (int i = tid; i < G * kPairs; i += kAttnWarps * 32) {
+              const int row = i / kPairs, k = i % kPairs;
+              uint8_t* dst = p.part + ((size_t)(ar.g * G + row) * p.S + ar.s) * kRB;
+              const float l = bufs[16 + row];
+              if (k < D / 2) {
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+                const float* o = bufs + 32 + row * kOS + 2 * k;
+                *reinterpret_cast<__half2*>(dst + 4 * k) = __floats2half2_rn(o[0] * inv, o[1] * inv);
+              } else {
+                *reinterpret_cast<float2*>(dst + 2 * D) = make_float2(bufs[row], l);
+              }
             }
           }
         }
@@ -944,16 +950,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr int kMaxSL = 8;  // splits per lane (S <= 256)
         for (int pi = p0 + warp; pi < p1; pi += kCW) {
           const int hq = pi / D, d = pi % D;
-          const float* base = p.part + (size_t)hq * p.S * (D + 4);
+          constexpr int kRB = part_row_bytes(D);
+          const uint8_t* base = p.part + (size_t)hq * p.S * kRB;
           float ms[kMaxSL], ls[kMaxSL], os[kMaxSL];
 #pragma unroll
           for (int k = 0; k < kMaxSL; ++k) {
             const int sp = lane + 32 * k;
-            const float* ps = base + (size_t)sp * (D + 4);
+            const uint8_t* ps = base + (size_t)sp * kRB;
             const bool in = sp < p.S;
-            ms[k] = in ? __ldcg(ps + D) : -INFINITY;
-            ls[k] = in ? __ldcg(ps + D + 1) : 0.f;
-            os[k] = in ? __ldcg(ps + d) : 0.f;
+            const float2 ml = in ? __ldcg(reinterpret_cast<const float2*>(ps + 2 * D))
+                                 : make_float2(-INFINITY, 0.f);
+            ms[k] = ml.x;
+            ls[k] = ml.y;
+            os[k] = in ? __half2float(__ldcg(reinterpret_cast<const __half*>(ps) + d)) : 0.f;
           }
           float M = -INFINITY;
 #pragma unroll
@@ -962,8 +971,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           float Ls = 0.f, Os = 0.f;
 #pragma unroll
           for (int k = 0; k < kMaxSL; ++k) {
-            const float w = (ms[k] == -INFINITY) ? 0.f : exp2f(ms[k] - M);
-            Ls += ls[k] * w;
+            const float w = (ms[k] == -INFINITY) ? 0.f : exp2f(ms[k] - M) * ls[k];
+            Ls += w;
             Os += os[k] * w;
           }
           Ls = warp_sum(Ls);
@@ -1133,7 +1142,7 @@ size_t decode_ws_bytes(int H, int Hq, int Hkv, int D, int I, int num_sms) {
   size_t o = 0;
   o += al((size_t)H * 4 * ((I + kKc - 1) / kKc));   // pdown
   o += al((size_t)Hq * D * 4);              // q32
-  o += al((size_t)Hq * S * (D + 4) * 4);    // part
+  o += al((size_t)Hq * S * part_row_bytes(D));   // part
   o += al((size_t)Hq * D * 2);              // attn16
   o += al((size_t)H * 4);                   // h32
   o += al((size_t)I * 2);                   // act16
@@ -1149,7 +1158,7 @@ void decode_ws_carve(DecodeParams& p, void* ws, int num_sms) {
   p.nc_down = (p.I + kKc - 1) / kKc;
   p.pdown = reinterpret_cast<float*>(b + o); o += al((size_t)p.H * 4 * p.nc_down);
   p.q32 = reinterpret_cast<float*>(b + o); o += al((size_t)p.Hq * p.D * 4);
-  p.part = reinterpret_cast<float*>(b + o); o += al((size_t)p.Hq * S * (p.D + 4) * 4);
+  p.part = b + o; o += al((size_t)p.Hq * S * part_row_bytes(p.D));
   p.attn16 = reinterpret_cast<__half*>(b + o); o += al((size_t)p.Hq * p.D * 2);
   p.h32 = reinterpret_cast<float*>(b + o); o += al((size_t)p.H * 4);
   p.act16 = reinterpret_cast<__half*>(b + o); o += al((size_t)p.I * 2);

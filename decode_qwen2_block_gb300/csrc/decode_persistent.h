@@ -47,7 +47,7 @@ struct DecodeParams {
   float* pdown;         // [nc_down][H] DOWN partials per 1536-column chunk
   int nc_down;
   float* q32;           // [Hq * D]
-  float* part;          // [Hq][S][D + 4]  (acc[D], m, l, pad): rows 16-byte aligned
+  uint8_t* part;        // [Hq][S] rows of 2D + 16 bytes: acc / sum (D fp16), (max, sum) float2
   __half* attn16;       // [Hq * D]
   float* h32;           // [H]
   __half* act16;        // [I]

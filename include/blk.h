@@ -182,7 +182,8 @@ int blk_decode_stack(blk_handle h, const blk_weights* w, int n_layers,
  * Limit: a shape whose decode scratch (the same bytes blk_decode would need
  * from its workspace) exceeds BLK_STATIC_SCRATCH_BYTES is rejected with
  * BLK_ERR_SCRATCH_LIMIT before anything is enqueued.  The 1.5B shape needs
- * about 0.5 MiB; the hidden-4096 / 32-head shape needs about 1.3 MiB and is
+ * about 0.3 MiB and the hidden-4096 / 32-head shape about 0.8 MiB; a
+ * hidden-12288 / 96-head / 6-kv-head shape needs about 1.1 MiB and is
  * rejected.
  *
  * Set-up: the first call on each device looks up the array's device address

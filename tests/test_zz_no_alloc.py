@@ -32,7 +32,7 @@ def _decode_static(db, x, pos, L, kc, vc):
     return out, kn, vn
 
 
-@pytest.mark.parametrize("shape_name,L", [("TINY", 30), ("QWEN2_1P5B", 4096)])
+@pytest.mark.parametrize("shape_name,L", [("TINY", 30), ("QWEN2_1P5B", 4096), ("GQA_4096", 300)])
 def test_static_scratch_decode_matches_workspace_decode(shape_name, L):
     s = getattr(synth, shape_name)
     C = L + 16
@@ -55,18 +55,26 @@ def test_static_scratch_decode_matches_workspace_decode(shape_name, L):
 
 
 def test_static_scratch_rejects_shapes_over_its_limit():
-    s = synth.GQA_4096                       # 32 query heads: about 1.3 MiB of scratch
-    C = 4096
-    db = DevBlock(s, synth.block_weights(s, seed=0), C, 1)
-    x = to_dev(synth.hidden_input(s, 1, seed=0))
+    # hidden 12288, 96 query heads over 6 kv heads: about 1.1 MiB of scratch.
+    # The call must be refused before anything is enqueued, so the weights are
+    # never read: one zero buffer large enough for every matrix stands in.
+    s = synth.BlockShape(12288, 96, 6, 128, 12288, False)
+    C = 64
+    blkh = blk.Block(s, C)
+    big = torch.zeros(s.hidden * s.hidden, dtype=torch.float16, device="cuda")
+    gains = torch.ones(s.hidden, dtype=torch.float16, device="cuda")
+    w_dev = {k: (gains if k.startswith("ln") else big) for k in synth.weight_shapes(s)}
+    w = blk.Block.weights(w_dev)
+    x = torch.zeros((1, s.hidden), dtype=torch.float16, device="cuda")
     pos = to_dev(synth.positions(10, 1))
     kc = torch.zeros((s.n_kv_heads, C, s.head_dim), dtype=torch.float16, device="cuda")
     vc = torch.zeros_like(kc)
-    out = torch.empty((1, s.hidden), dtype=torch.float16, device="cuda")
+    out = torch.full((1, s.hidden), 7.0, dtype=torch.float16, device="cuda")
     before = kc.clone()
-    rc = blk.blk_decode_static(db.block.handle, db.w, x.data_ptr(), pos.data_ptr(), 10,
+    rc = blk.blk_decode_static(blkh.handle, w, x.data_ptr(), pos.data_ptr(), 10,
                                kc.data_ptr(), vc.data_ptr(), out.data_ptr(), None, None,
                                torch.cuda.current_stream().cuda_stream)
     assert rc == blk.BLK_ERR_SCRATCH_LIMIT
     torch.cuda.synchronize()
     assert torch.equal(kc, before)           # nothing was enqueued
+    assert torch.all(out == 7.0)
