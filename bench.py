@@ -346,7 +346,8 @@ def bench_ours(args, ws, rank, local):
     else:
         roof = {"kernel": dom, "bound": "hbm", "achieved": None, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": None, "traffic": None}
-    gemm_ms = sum(table[k][0] for k in gemm_flops if k in table) / K
+    # the split-K reduction belongs to the down projection's time
+    gemm_ms = sum(table[k][0] for k in list(gemm_flops) + ["splitk_reduce"] if k in table) / K
     gemm_frac = sum(gemm_flops.values()) / (gemm_ms * 1e-3) / 1e12 / peaks["bf16_tflops"]
 
     result = {

@@ -20,11 +20,11 @@ namespace {
 constexpr int kMaxPending = 1024;
 // Kernel ids for per-kernel timing (blk_timing_read).
 enum KernelId {
-  kKRmsNorm = 0, kKGemmQKV, kKRopeAppend, kKAttnPrefill, kKGemmO, kKGemmGateUp,
+  kKRmsNorm = 0, kKGemmQKV, kKSplitReduce, kKAttnPrefill, kKGemmO, kKGemmGateUp,
   kKGemmDown, kKDecodeStep, kKCount
 };
 const char* const kKernelNames[BLK_N_KERNELS] = {
-    "rmsnorm_rows", "gemm_qkv", "(unused)", "attn_prefill", "gemm_o",
+    "rmsnorm_rows", "gemm_qkv", "splitk_reduce", "attn_prefill", "gemm_o",
     "gemm_gateup", "gemm_down", "decode_persistent", "", "", "", "",
     "", "", "", ""};
 }  // namespace
@@ -82,8 +82,10 @@ int shape_ok(const blk_config* c) {
 
 // Workspace layout.  Prefill and decode buffers start at offset 0 (a call
 // uses one of the two layouts).
+constexpr int kMaxSplits = 4;        // split-K partial buffers of the down projection
+
 struct PrefillWs {
-  size_t xn16, q16, attn16, h32, hn16, act16, total;
+  size_t xn16, q16, attn16, h32, hn16, act16, part32, total;
 };
 
 PrefillWs prefill_ws(const blk_config& c, int64_t T) {
@@ -98,6 +100,7 @@ PrefillWs prefill_ws(const blk_config& c, int64_t T) {
   w.h32 = o; o = align_up(o + T * H * 4);
   w.hn16 = o; o = align_up(o + T * H * 2);
   w.act16 = o; o = align_up(o + T * I * 2);
+  w.part32 = o; o = align_up(o + (size_t)kMaxSplits * T * H * 4);
   w.total = o;
   return w;
 }
@@ -201,9 +204,9 @@ int run_prefill(blk_handle h, const blk_weights* w, const void* x,
   // QKV projection + bias + RoPE + KV append
   TcGemmParams g = {};
   if (make_tmap_2d(&g.tmA, xn16, M, H, 128) ||
-      make_tmap_2d(&g.tmB[0], w->wq, (int64_t)Hq * D, H, 128) ||
-      make_tmap_2d(&g.tmB[1], w->wk, (int64_t)Hkv * D, H, 128) ||
-      make_tmap_2d(&g.tmB[2], w->wv, (int64_t)Hkv * D, H, 128))
+      make_tmap_2d(&g.tmB[0], w->wq, (int64_t)Hq * D, H, 64) ||
+      make_tmap_2d(&g.tmB[1], w->wk, (int64_t)Hkv * D, H, 64) ||
+      make_tmap_2d(&g.tmB[2], w->wv, (int64_t)Hkv * D, H, 64))
     return BLK_ERR_CUDA;
   g.M = M; g.N = (Hq + 2 * Hkv) * D; g.K = H;
   g.seg_rows[0] = Hq * D; g.seg_rows[1] = Hkv * D; g.seg_rows[2] = Hkv * D;
@@ -239,7 +242,7 @@ int run_prefill(blk_handle h, const blk_weights* w, const void* x,
   // o_proj + residual -> h (fp32)
   TcGemmParams go = {};
   if (make_tmap_2d(&go.tmA, attn16, M, (int64_t)Hq * D, 128) ||
-      make_tmap_2d(&go.tmB[0], w->wo, H, (int64_t)Hq * D, 128))
+      make_tmap_2d(&go.tmB[0], w->wo, H, (int64_t)Hq * D, 64))
     return BLK_ERR_CUDA;
   go.M = M; go.N = H; go.K = Hq * D;
   go.res16 = static_cast<const __half*>(x); go.out32 = h32; go.ldo = H;
@@ -254,8 +257,8 @@ int run_prefill(blk_handle h, const blk_weights* w, const void* x,
   // gate | up + SwiGLU
   TcGemmParams gu = {};
   if (make_tmap_2d(&gu.tmA, hn16, M, H, 128) ||
-      make_tmap_2d(&gu.tmB[0], w->w_gate, I, H, 128) ||
-      make_tmap_2d(&gu.tmB[1], w->w_up, I, H, 128))
+      make_tmap_2d(&gu.tmB[0], w->w_gate, I, H, 64) ||
+      make_tmap_2d(&gu.tmB[1], w->w_up, I, H, 64))
     return BLK_ERR_CUDA;
   gu.M = M; gu.N = I; gu.K = H;
   gu.out16 = act16; gu.ldo = I;
@@ -265,12 +268,16 @@ int run_prefill(blk_handle h, const blk_weights* w, const void* x,
   // down + residual -> out
   TcGemmParams gd = {};
   if (make_tmap_2d(&gd.tmA, act16, M, I, 128) ||
-      make_tmap_2d(&gd.tmB[0], w->w_down, H, I, 128))
+      make_tmap_2d(&gd.tmB[0], w->w_down, H, I, 64))
     return BLK_ERR_CUDA;
   gd.M = M; gd.N = H; gd.K = I;
   gd.res32 = h32; gd.out16 = static_cast<__half*>(out); gd.ldo = H;
+  gd.part = reinterpret_cast<float*>(base + lay.part32);
+  gd.max_splits = kMaxSplits;
   gd.err = h->status;
   BLK_LAUNCH(tm, kKGemmDown, launch_tc_gemm(gd, kTcResidOutF16, h->num_sms, s, true));
+  if (gd.splits > 1)
+    BLK_LAUNCH(tm, kKSplitReduce, launch_splitk_reduce(gd, h->num_sms, s));
   return BLK_OK;
 }
 

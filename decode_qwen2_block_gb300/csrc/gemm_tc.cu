@@ -3,11 +3,18 @@
 // D[m, n] = sum_k A[m, k] * B[n, k]: A = activations [M, K] fp16, B = weights
 // [N, K] fp16 (nn.Linear layout), both K-major; fp32 accumulation in TMEM.
 //
-// One persistent CTA per SM, 6 warps:
+// One persistent CTA per SM, 10 warps.  When there are at least two 128-row
+// tiles of A, CTAs run as clusters of NC = 2 or 4: the CTAs of a cluster
+// compute the same BN columns for consecutive 128-row tiles, and each loads
+// 1/NC of the shared weight tile with a TMA multicast into every CTA of the
+// cluster, so an SM reads 128 + BN/NC operand rows per K step instead of
+// 128 + BN (L2-to-SM traffic, not HBM, is what limits these GEMMs).
 //   warp 0   TMA producer: 128x64 A tiles and BNx64 B tiles, 128-byte
 //            swizzle, into a ring of shared-memory stages (mbarrier full /
-//            empty pairs).  Weight tiles of the first stages are issued before
-//            griddepcontrol.wait (they never depend on the previous kernel).
+//            empty pairs; with a pair, a stage is refilled only after both
+//            CTAs' MMAs released it).  Weight tiles of the first stages are
+//            issued before griddepcontrol.wait (they never depend on the
+//            previous kernel).
 //   warp 1   allocates TMEM (two accumulators of BN fp32 columns) and its lane
 //            0 issues tcgen05.mma.cta_group::1.kind::f16 (M=128, N=BN, K=16)
 //            four times per stage; tcgen05.commit frees the stage and, after
@@ -35,7 +42,8 @@ namespace blk {
 namespace {
 
 constexpr int BM = 128, BK = 64;
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;   // two per TMEM lane quarter, splitting the columns
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map,
                                             int x, int y, uint64_t* bar) {
@@ -44,6 +52,27 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map,
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
+}
+
+// Same tile into the shared memory of every CTA in `mask` (same offset), each
+// CTA's mbarrier at the offset of `bar` receiving the bytes it got.
+__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, int x, int y,
+                                               uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(mask)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -84,6 +113,15 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
           smem_u32(bar))
+      : "memory");
+}
+
+// Arrives (when this CTA's prior MMAs complete) on the mbarrier at the offset
+// of `bar` in every CTA of `mask`.
+__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_u32(bar)), "h"(mask)
       : "memory");
 }
 
@@ -129,10 +167,15 @@ struct Cfg {
   static constexpr size_t kSmem = (size_t)kStages * kStageBytes + 1024 + 256;
 };
 
-template <int EPI, int BN>
+// A work unit is (N tile nt, M tile group mg): the CTA of rank r in a cluster
+// of NC (1 or 2) takes M tile mg * NC + r.
+template <int EPI, int BN, int NC>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ TcGemmParams p) {
   using C = Cfg<BN>;
+  constexpr int kBBox = 64;                 // rows per B tensor-map box
+  constexpr int kBBoxes = BN / kBBox;
+  static_assert(kBBoxes % NC == 0, "B boxes split over the cluster");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -147,14 +190,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int KB = (p.K + BK - 1) / BK;
 
+  const int rank = NC > 1 ? (int)cluster_rank() : 0;
+  const int cl = blockIdx.x / NC, ncl = gridDim.x / NC;   // cluster index and count
+  const int mgroups = (p.tiles_m + NC - 1) / NC;
+  // K is split S ways for the down projection (partials added by the last split)
+  const int S = EPI == kTcResidOutF16 ? p.splits : 1;
+  const int KBs = (KB + S - 1) / S;   // K blocks per split
+  const int units = mgroups * p.tiles_n * S;
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], NC);   // both CTAs' MMAs release a shared stage
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 4);
+      mbar_init(&tempty[a], kEpiWarps);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -170,6 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (NC > 1) cluster_sync();   // the peer's mbarriers exist before any multicast
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -178,14 +229,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int it = 0;
       bool waited = false;
-      for (int tile = blockIdx.x; tile < p.num_tiles && !*abort_flag; tile += gridDim.x) {
-        const int mt = tile % p.tiles_m, nt = tile / p.tiles_m;
+      for (int u = cl; u < units && !*abort_flag; u += ncl) {
+        const int t = u / S, ks = u % S;
+        const int mt = (t % mgroups) * NC + rank, nt = t / mgroups;
         const int m0 = mt * BM, n0 = nt * (EPI == kTcGateUp ? BN / 2 : BN);
-        int seg = 0, row0 = n0;
-        if (EPI == kTcQKV) {
-          while (seg < 2 && row0 >= p.seg_rows[seg]) row0 -= p.seg_rows[seg++];
-        }
-        for (int kb = 0; kb < KB; ++kb, ++it) {
+        const int kb1 = min(KB, (ks + 1) * KBs);
+        for (int kb = ks * KBs; kb < kb1; ++kb, ++it) {
           const int s = it % C::kStages;
           if (!mbar_wait(&empty[s], ((it / C::kStages) & 1) ^ 1, p.err)) {
             *abort_flag = 1;
@@ -194,11 +243,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* sa = smem + (size_t)s * C::kStageBytes;
           uint8_t* sb = sa + C::kABytes;
           mbar_arrive_expect_tx(&full[s], C::kStageBytes);
-          if (EPI == kTcGateUp) {
-            tma_load_2d(sb, &p.tmB[0], kb * BK, row0, &full[s]);
-            tma_load_2d(sb + C::kBBytes / 2, &p.tmB[1], kb * BK, row0, &full[s]);
-          } else {
-            tma_load_2d(sb, &p.tmB[seg], kb * BK, row0, &full[s]);
+          // B boxes of kBBox rows; with a pair, rank r loads boxes r, r + 2, ...
+          // and multicasts each to both CTAs
+#pragma unroll
+          for (int bx = rank; bx < kBBoxes; bx += NC) {
+            const CUtensorMap* mb;
+            int row;
+            if (EPI == kTcGateUp) {   // boxes of W_gate rows, then of W_up rows
+              constexpr int kHalf = kBBoxes / 2;
+              mb = &p.tmB[bx / kHalf];
+              row = n0 + (bx % kHalf) * kBBox;
+            } else {
+              int seg = 0;
+              row = n0 + bx * kBBox;
+              if (EPI == kTcQKV) {
+                while (seg < 2 && row >= p.seg_rows[seg]) row -= p.seg_rows[seg++];
+              }
+              mb = &p.tmB[seg];
+            }
+            uint8_t* dst = sb + bx * (kBBox * BK * 2);
+            if (NC > 1) tma_load_2d_mc(dst, mb, kb * BK, row, &full[s], (uint16_t)((1u << NC) - 1));
+            else tma_load_2d(dst, mb, kb * BK, row, &full[s]);
           }
           if (!waited) {  // activations come from the previous kernel
             griddep_wait();
@@ -223,8 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc = idesc_f16(BM, BN);
       int it = 0, tcount = 0;
       bool issued = false;
-      for (int tile = blockIdx.x; tile < p.num_tiles && !*abort_flag;
-           tile += gridDim.x, ++tcount) {
+      for (int u = cl; u < units && !*abort_flag; u += ncl, ++tcount) {
         const int acc = tcount & 1;
         if (!mbar_wait(&tempty[acc], ((tcount >> 1) & 1) ^ 1, p.err)) {
           *abort_flag = 1;
@@ -232,7 +296,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int kb = 0; kb < KB; ++kb, ++it) {
+        const int ks = u % S, kb0 = ks * KBs, kb1 = min(KB, kb0 + KBs);
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const int s = it % C::kStages;
           if (!mbar_wait(&full[s], (it / C::kStages) & 1, p.err)) {
             *abort_flag = 1;
@@ -244,9 +309,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t db = smem_desc_sw128(sa + C::kABytes);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)  // +32 bytes per K step inside the swizzle atom
-            mma_f16(d_tmem, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0);
+            mma_f16(d_tmem, da + 2 * k, db + 2 * k, idesc, (kb != kb0) || (k != 0));
           issued = true;
-          mma_commit(&empty[s]);
+          if (NC > 1) mma_commit_mc(&empty[s], (uint16_t)((1u << NC) - 1));
+          else mma_commit(&empty[s]);
         }
         if (*abort_flag) break;
         mma_commit(&tfull[acc]);
@@ -260,75 +326,111 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     griddep_wait();
     griddep_launch();
+    // Thread = tile row.  Warps 2..9 read TMEM lane quarter warp % 4; the two
+    // warps of a quarter take alternate 32-column chunks.  Each warp issues
+    // the global loads its chunks need (residual, RoPE factors) before it
+    // reads the accumulator, so their latency overlaps.
     const int q = warp & 3;              // TMEM lane quarter this warp may access
+    const int e = (warp - 2) >> 2;       // which half of the chunks
     const int row_in_tile = q * 32 + lane;
     int tcount = 0;
-    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++tcount) {
+    for (int u = cl; u < units; u += ncl, ++tcount) {
       const int acc = tcount & 1;
-      if (!mbar_wait(&tfull[acc], (tcount >> 1) & 1, p.err)) {
-        *abort_flag = 1;
-        break;
-      }
-      tc_fence_after();
-      const int mt = tile % p.tiles_m, nt = tile / p.tiles_m;
+      const int t = u / S, ks = u % S;
+      const int mt = (t % mgroups) * NC + rank, nt = t / mgroups;
       const int m = mt * BM + row_in_tile;
-      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
       const bool row_ok = m < p.M;
+      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
       float v0[32], v1[32];
 
       if constexpr (EPI == kTcQKV) {
         const int D = p.D, half = D / 2;
         const int n0 = nt * BN;
         const int64_t pos = row_ok ? p.pos[m] : 0;
-        for (int hh = 0; hh < BN / D; ++hh) {
+        // (head, chunk) items of this tile, alternating between the two warps
+        const int chunks = half / 32, items = (BN / D) * chunks;
+        bool waited = false;
+        for (int it2 = e; it2 < items; it2 += 2) {
+          const int hh = it2 / chunks, c0 = (it2 % chunks) * 32;
           const int hd = n0 / D + hh;  // head index over q | k | v
-          for (int c0 = 0; c0 < half; c0 += 32) {
-            tmem_ld32(tbase + hh * D + c0, v0);
-            tmem_ld32(tbase + hh * D + half + c0, v1);
-            if (!row_ok) continue;
-            const __half* bias;
-            int local;
-            if (hd < p.Hq) { bias = p.bias[0]; local = hd; }
-            else if (hd < p.Hq + p.Hkv) { bias = p.bias[1]; local = hd - p.Hq; }
-            else { bias = p.bias[2]; local = hd - p.Hq - p.Hkv; }
-            if (bias) {
+          const __half* bias;
+          int local;
+          if (hd < p.Hq) { bias = p.bias[0]; local = hd; }
+          else if (hd < p.Hq + p.Hkv) { bias = p.bias[1]; local = hd - p.Hq; }
+          else { bias = p.bias[2]; local = hd - p.Hq - p.Hkv; }
+          const bool rope = hd < p.Hq + p.Hkv;
+          // this row's 32 rotation factors, loaded before the accumulator
+          float4 cs4[16];
+          if (rope && row_ok && pos >= 0 && pos < p.rope_len) {
+            const float4* src = reinterpret_cast<const float4*>(p.rope + (size_t)pos * half + c0);
 #pragma unroll
-              for (int i = 0; i < 32; ++i) {
-                v0[i] += __half2float(bias[local * D + c0 + i]);
-                v1[i] += __half2float(bias[local * D + half + c0 + i]);
-              }
-            }
-            if (hd < p.Hq + p.Hkv) {
+            for (int k = 0; k < 16; ++k) cs4[k] = __ldg(src + k);
+          } else {
+            if (rope && row_ok) set_error(p.err, kDevPosition);
 #pragma unroll
-              for (int i = 0; i < 32; ++i) {
-                const float2 cs = rope_cs(p.rope, p.rope_len, half, pos, c0 + i, p.err);
-                const float a = v0[i], b = v1[i];
-                v0[i] = a * cs.x - b * cs.y;
-                v1[i] = b * cs.x + a * cs.y;
-              }
+            for (int k = 0; k < 16; ++k) cs4[k] = make_float4(1.f, 0.f, 1.f, 0.f);
+          }
+          if (!waited) {
+            if (!mbar_wait(&tfull[acc], (tcount >> 1) & 1, p.err)) {
+              *abort_flag = 1;
+              break;
             }
-            if (hd < p.Hq) {
-              __half* dst = p.q16 + ((size_t)m * p.Hq + hd) * D;
-              store_h32(dst + c0, v0);
-              store_h32(dst + half + c0, v1);
-            } else {
-              const bool is_k = hd < p.Hq + p.Hkv;
-              __half* cache = is_k ? p.kc : p.vc;
-              __half* nw = is_k ? p.k_new : p.v_new;
-              __half* dst = cache + ((size_t)local * p.max_ctx + p.cache_len + m) * D;
-              store_h32(dst + c0, v0);
-              store_h32(dst + half + c0, v1);
-              if (nw) {
-                __half* d2 = nw + ((size_t)m * p.Hkv + local) * D;
-                store_h32(d2 + c0, v0);
-                store_h32(d2 + half + c0, v1);
-              }
+            tc_fence_after();
+            waited = true;
+          }
+          tmem_ld32(tbase + hh * D + c0, v0);
+          tmem_ld32(tbase + hh * D + half + c0, v1);
+          if (!row_ok) continue;
+          if (bias) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              v0[i] += __half2float(bias[local * D + c0 + i]);
+              v1[i] += __half2float(bias[local * D + half + c0 + i]);
+            }
+          }
+          if (rope) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float4 c = cs4[i >> 1];
+              const float cx = (i & 1) ? c.z : c.x, sy = (i & 1) ? c.w : c.y;
+              const float a = v0[i], b = v1[i];
+              v0[i] = a * cx - b * sy;
+              v1[i] = b * cx + a * sy;
+            }
+          }
+          if (hd < p.Hq) {
+            __half* dst = p.q16 + ((size_t)m * p.Hq + hd) * D;
+            store_h32(dst + c0, v0);
+            store_h32(dst + half + c0, v1);
+          } else {
+            const bool is_k = hd < p.Hq + p.Hkv;
+            __half* cache = is_k ? p.kc : p.vc;
+            __half* nw = is_k ? p.k_new : p.v_new;
+            __half* dst = cache + ((size_t)local * p.max_ctx + p.cache_len + m) * D;
+            store_h32(dst + c0, v0);
+            store_h32(dst + half + c0, v1);
+            if (nw) {
+              __half* d2 = nw + ((size_t)m * p.Hkv + local) * D;
+              store_h32(d2 + c0, v0);
+              store_h32(d2 + half + c0, v1);
             }
           }
         }
+        if (!waited) {   // no item for this warp: still wait so the release is ordered
+          if (!mbar_wait(&tfull[acc], (tcount >> 1) & 1, p.err)) {
+            *abort_flag = 1;
+            break;
+          }
+          tc_fence_after();
+        }
       } else if constexpr (EPI == kTcGateUp) {
+        if (!mbar_wait(&tfull[acc], (tcount >> 1) & 1, p.err)) {
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
         const int j0 = nt * (BN / 2);
-        for (int c0 = 0; c0 < BN / 2; c0 += 32) {
+        for (int c0 = 32 * e; c0 < BN / 2; c0 += 64) {
           tmem_ld32(tbase + c0, v0);
           tmem_ld32(tbase + BN / 2 + c0, v1);
           if (!row_ok) continue;
@@ -343,33 +445,88 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
         const int n0 = nt * BN;
-        for (int c0 = 0; c0 < BN; c0 += 32) {
-          tmem_ld32(tbase + c0, v0);
-          if (!row_ok || n0 + c0 >= p.N) continue;
+        constexpr int kCh = BN / 64;   // chunks per warp: c0 = 32 e + 64 c
+        // loads row m's residual for chunk c0 (zeros outside the output)
+        auto load_res = [&](int c0, float* rv) {
+          const bool ok = row_ok && n0 + c0 < p.N;
           const size_t o = (size_t)m * p.ldo + n0 + c0;
           if constexpr (EPI == kTcResidF32) {
-            const uint4* r = reinterpret_cast<const uint4*>(p.res16 + o);
-            float4* dst = reinterpret_cast<float4*>(p.out32 + o);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               float f[8];
-              h8_to_f32(r[j], f);
-              dst[2 * j] = make_float4(v0[8 * j] + f[0], v0[8 * j + 1] + f[1],
-                                       v0[8 * j + 2] + f[2], v0[8 * j + 3] + f[3]);
-              dst[2 * j + 1] = make_float4(v0[8 * j + 4] + f[4], v0[8 * j + 5] + f[5],
-                                           v0[8 * j + 6] + f[6], v0[8 * j + 7] + f[7]);
+              h8_to_f32(ok ? __ldg(reinterpret_cast<const uint4*>(p.res16 + o) + j)
+                           : make_uint4(0u, 0u, 0u, 0u), f);
+#pragma unroll
+              for (int t2 = 0; t2 < 8; ++t2) rv[8 * j + t2] = f[t2];
             }
           } else {
-            const float4* r = reinterpret_cast<const float4*>(p.res32 + o);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-              const float4 f = r[j];
-              v0[4 * j] += f.x;
-              v0[4 * j + 1] += f.y;
-              v0[4 * j + 2] += f.z;
-              v0[4 * j + 3] += f.w;
+              const float4 f = ok ? __ldg(reinterpret_cast<const float4*>(p.res32 + o) + j)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+              rv[4 * j] = f.x; rv[4 * j + 1] = f.y; rv[4 * j + 2] = f.z; rv[4 * j + 3] = f.w;
             }
-            store_h32(p.out16 + o, v0);
+          }
+        };
+        auto store_out = [&](int c0, const float* v) {
+          const size_t o = (size_t)m * p.ldo + n0 + c0;
+          if constexpr (EPI == kTcResidF32) {
+            float4* dst = reinterpret_cast<float4*>(p.out32 + o);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          } else {
+            store_h32(p.out16 + o, v);
+          }
+        };
+        if (S == 1) {
+          // two chunks at a time: their residuals are loaded before the
+          // accumulator is read
+          bool waited = false;
+#pragma unroll
+          for (int c2 = 0; c2 < kCh; c2 += 2) {
+            float rv[2][32];
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+              if (c2 + c < kCh) load_res(32 * e + 64 * (c2 + c), rv[c]);
+            if (!waited) {
+              if (!mbar_wait(&tfull[acc], (tcount >> 1) & 1, p.err)) {
+                *abort_flag = 1;
+                break;
+              }
+              tc_fence_after();
+              waited = true;
+            }
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              if (c2 + c >= kCh) break;
+              const int c0 = 32 * e + 64 * (c2 + c);
+              tmem_ld32(tbase + c0, v0);
+              if (!row_ok || n0 + c0 >= p.N) continue;
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v0[i] += rv[c][i];
+              store_out(c0, v0);
+            }
+          }
+          if (!waited) break;
+        } else {
+          // split K: this split's fp32 partial; splitk_reduce_kernel adds the
+          // partials in split order, plus the residual
+          if (!mbar_wait(&tfull[acc], (tcount >> 1) & 1, p.err)) {
+            *abort_flag = 1;
+            break;
+          }
+          tc_fence_after();
+          float* part = p.part + (size_t)ks * p.M * p.N;
+#pragma unroll
+          for (int c = 0; c < kCh; ++c) {
+            const int c0 = 32 * e + 64 * c;
+            tmem_ld32(tbase + c0, v0);
+            if (!row_ok || n0 + c0 >= p.N) continue;
+            float4* dst = reinterpret_cast<float4*>(part + (size_t)m * p.N + n0 + c0);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              dst[j] = make_float4(v0[4 * j], v0[4 * j + 1], v0[4 * j + 2], v0[4 * j + 3]);
           }
         }
       }
@@ -381,6 +538,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  // neither CTA of a pair leaves while the other may still multicast into its
+  // shared memory or arrive on its barriers
+  if (NC > 1) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
@@ -389,9 +549,56 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// out16[m, n] = fp16(sum_j part[j][m, n] + res32[m, n]), splits added in
+// order; four columns per thread.
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restrict__ part,
+                                                            int S, int64_t MN,
+                                                            const float* __restrict__ res32,
+                                                            __half* __restrict__ out16) {
+  griddep_wait();
+  griddep_launch();
+  const int64_t n4 = MN / 4;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    float4 q[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      q[j] = j < S ? __ldcg(reinterpret_cast<const float4*>(part + (size_t)j * MN) + i)
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 r = __ldg(reinterpret_cast<const float4*>(res32) + i);
+    float4 a = q[0];
+#pragma unroll
+    for (int j = 1; j < 4; ++j) {
+      if (j < S) { a.x += q[j].x; a.y += q[j].y; a.z += q[j].z; a.w += q[j].w; }
+    }
+    uint2 o;
+    *reinterpret_cast<__half2*>(&o.x) = __floats2half2_rn(a.x + r.x, a.y + r.y);
+    *reinterpret_cast<__half2*>(&o.y) = __floats2half2_rn(a.z + r.z, a.w + r.w);
+    reinterpret_cast<uint2*>(out16)[i] = o;
+  }
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------- host side
+
+cudaError_t launch_splitk_reduce(const TcGemmParams& p, int num_sms, cudaStream_t s) {
+  const int64_t MN = (int64_t)p.M * p.N;
+  const int64_t n4 = MN / 4;
+  int grid = (int)((n4 + 255) / 256);
+  if (grid > 8 * num_sms) grid = 8 * num_sms;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid < 1 ? 1 : grid);
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, (const float*)p.part, p.splits, MN,
+                            p.res32, p.out16);
+}
 
 // cuTensorMapEncodeTiled, resolved through the runtime so that the library
 // does not link libcuda (it must load on machines without a driver).
@@ -457,54 +664,110 @@ int make_tmap_rows8(CUtensorMap* map, const void* base, int64_t rows, int64_t K,
   return r == CUDA_SUCCESS ? 0 : -1;
 }
 
-template <int EPI, int BN>
+template <int EPI, int BN, int NC>
 static cudaError_t launch_tc(TcGemmParams& p, int num_sms, cudaStream_t s, bool pdl) {
   using C = Cfg<BN>;
+  const int mgroups = (p.tiles_m + NC - 1) / NC;
+  int units = mgroups * p.tiles_n;
+  // co-resident clusters: one CTA per SM, whole clusters only
+  static int max_clusters = 0;
+  if (max_clusters == 0) {
+    cudaLaunchConfig_t q = {};
+    q.gridDim = dim3(NC * 64);
+    q.blockDim = dim3(kThreads);
+    q.dynamicSmemBytes = C::kSmem;
+    cudaLaunchAttribute qa[1];
+    qa[0].id = cudaLaunchAttributeClusterDimension;
+    qa[0].val.clusterDim.x = NC;
+    qa[0].val.clusterDim.y = 1;
+    qa[0].val.clusterDim.z = 1;
+    q.attrs = qa;
+    q.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel<EPI, BN, NC>, &q) != cudaSuccess ||
+        n < 1)
+      n = num_sms / NC;
+    max_clusters = n < num_sms / NC ? n : num_sms / NC;
+  }
+  p.splits = 1;
+  if (EPI == kTcResidOutF16 && p.part) {
+    // split K so that the units fill the co-resident clusters (8+ K blocks each)
+    int S = max_clusters / units;
+    S = S < 1 ? 1 : (S > p.max_splits ? p.max_splits : S);
+    const int KB = (p.K + BK - 1) / BK;
+    while (S > 1 && KB / S < 8) --S;
+    p.splits = S;
+    units *= S;
+  }
+  const int clusters = units < max_clusters ? units : max_clusters;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(clusters * NC);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  attr[na].id = cudaLaunchAttributeClusterDimension;
+  attr[na].val.clusterDim.x = NC;
+  attr[na].val.clusterDim.y = 1;
+  attr[na].val.clusterDim.z = 1;
+  ++na;
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<EPI, BN, NC>, p);
+}
+
+template <int EPI, int BN>
+static cudaError_t launch_tc_any(TcGemmParams& p, int num_sms, cudaStream_t s, bool pdl) {
   p.tiles_m = (p.M + BM - 1) / BM;
   const int bn_out = EPI == kTcGateUp ? BN / 2 : BN;
   p.tiles_n = (p.N + bn_out - 1) / bn_out;
   p.num_tiles = p.tiles_m * p.tiles_n;
-  const int grid = p.num_tiles < num_sms ? p.num_tiles : num_sms;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = C::kSmem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<EPI, BN>, p);
+  // clusters share the weight tile when there are M tiles to group
+  if constexpr (BN / 64 % 4 == 0) {
+    if (p.tiles_m >= 4) return launch_tc<EPI, BN, 4>(p, num_sms, s, pdl);
+  }
+  if (p.tiles_m >= 2) return launch_tc<EPI, BN, 2>(p, num_sms, s, pdl);
+  return launch_tc<EPI, BN, 1>(p, num_sms, s, pdl);
 }
 
 cudaError_t launch_tc_gemm(TcGemmParams& p, int epi, int num_sms, cudaStream_t s,
                            bool pdl) {
   switch (epi) {
-    case kTcQKV: return launch_tc<kTcQKV, 128>(p, num_sms, s, pdl);
-    case kTcResidF32: return launch_tc<kTcResidF32, 128>(p, num_sms, s, pdl);
-    case kTcGateUp: return launch_tc<kTcGateUp, 256>(p, num_sms, s, pdl);
-    default: return launch_tc<kTcResidOutF16, 128>(p, num_sms, s, pdl);
+    case kTcQKV: return launch_tc_any<kTcQKV, 128>(p, num_sms, s, pdl);
+    case kTcResidF32: return launch_tc_any<kTcResidF32, 128>(p, num_sms, s, pdl);
+    case kTcGateUp: return launch_tc_any<kTcGateUp, 256>(p, num_sms, s, pdl);
+    default: return launch_tc_any<kTcResidOutF16, 256>(p, num_sms, s, pdl);
   }
+}
+
+template <int EPI, int BN>
+static cudaError_t configure_one() {
+  cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<EPI, BN, 1>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)Cfg<BN>::kSmem);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(tc_gemm_kernel<EPI, BN, 2>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg<BN>::kSmem);
+  if constexpr (BN / 64 % 4 == 0) {
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(tc_gemm_kernel<EPI, BN, 4>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg<BN>::kSmem);
+  }
+  return e;
 }
 
 cudaError_t configure_tc_gemm_kernels() {
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(tc_gemm_kernel<kTcQKV, 128>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)Cfg<128>::kSmem)))
-    return e;
-  if ((e = cudaFuncSetAttribute(tc_gemm_kernel<kTcResidF32, 128>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)Cfg<128>::kSmem)))
-    return e;
-  if ((e = cudaFuncSetAttribute(tc_gemm_kernel<kTcGateUp, 256>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)Cfg<256>::kSmem)))
-    return e;
-  return cudaFuncSetAttribute(tc_gemm_kernel<kTcResidOutF16, 128>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)Cfg<128>::kSmem);
+  if ((e = configure_one<kTcQKV, 128>())) return e;
+  if ((e = configure_one<kTcResidF32, 128>())) return e;
+  if ((e = configure_one<kTcGateUp, 256>())) return e;
+  return configure_one<kTcResidOutF16, 256>();
 }
 
 }  // namespace blk

@@ -39,6 +39,11 @@ struct TcGemmParams {
   float* out32;
   __half* out16;
   int ldo;
+  // split K (down projection): partials [splits][M][N] fp32, added by
+  // launch_splitk_reduce; splits (<= max_splits) is chosen by the launcher
+  int splits;
+  int max_splits;       // the partial buffer holds this many (at most 4)
+  float* part;
   int* err;
 };
 
@@ -54,6 +59,9 @@ int make_tmap_rows8(CUtensorMap* map, const void* base, int64_t rows, int64_t K,
 
 cudaError_t launch_tc_gemm(TcGemmParams& p, int epi, int num_sms, cudaStream_t s,
                            bool pdl);
+// After a down-projection launch with p.splits > 1: out16 = fp16(sum of the
+// split partials + res32) (N a multiple of 4).
+cudaError_t launch_splitk_reduce(const TcGemmParams& p, int num_sms, cudaStream_t s);
 cudaError_t configure_tc_gemm_kernels();
 
 }  // namespace blk
