@@ -3,23 +3,30 @@
 // D[m, n] = sum_k A[m, k] * B[n, k]: A = activations [M, K] fp16, B = weights
 // [N, K] fp16 (nn.Linear layout), both K-major; fp32 accumulation in TMEM.
 //
-// One persistent CTA per SM, 10 warps.  When there are at least two 128-row
-// tiles of A, CTAs run as clusters of NC = 2 or 4: the CTAs of a cluster
-// compute the same BN columns for consecutive 128-row tiles, and each loads
-// 1/NC of the shared weight tile with a TMA multicast into every CTA of the
-// cluster, so an SM reads 128 + BN/NC operand rows per K step instead of
-// 128 + BN (L2-to-SM traffic, not HBM, is what limits these GEMMs).
-//   warp 0   TMA producer: 128x64 A tiles and BNx64 B tiles, 128-byte
-//            swizzle, into a ring of shared-memory stages (mbarrier full /
-//            empty pairs; with a pair, a stage is refilled only after both
-//            CTAs' MMAs released it).  Weight tiles of the first stages are
+// CTAs run as pairs (clusters of 2) on 256-row tiles with the 2-SM form of
+// the MMA (tcgen05.mma.cta_group::2, M = 256): each CTA of the pair holds 128
+// rows of A and half of the BN weight rows, the leader CTA issues the MMAs for
+// both, and each SM's TMEM receives its own 128 rows of the result.  Per SM
+// and K step this moves half of the weight tile through shared memory instead
+// of all of it; with one-SM M = 128 MMAs the TMA writes plus the tensor core's
+// reads of a 128 x 256 x 64 step (96 KB) already fill the 128 B/clock
+// shared-memory port for longer than the MMA takes.
+// One persistent CTA per SM, 10 warps:
+//   warp 0   TMA producer (both CTAs): this CTA's 128x64 A tile and its
+//            (BN/2)x64 part of the weight tile, 128-byte swizzle, into a ring
+//            of shared-memory stages; the copies complete on the leader's
+//            stage barrier, and a stage is refilled after the leader's MMAs
+//            released it in both CTAs.  Weight tiles of the first stages are
 //            issued before griddepcontrol.wait (they never depend on the
 //            previous kernel).
-//   warp 1   allocates TMEM (two accumulators of BN fp32 columns) and its lane
-//            0 issues tcgen05.mma.cta_group::1.kind::f16 (M=128, N=BN, K=16)
-//            four times per stage; tcgen05.commit frees the stage and, after
-//            the last stage of a tile, hands the accumulator to the epilogue.
-//   warps 2-5 epilogue: tcgen05.ld 32 columns at a time (thread = tile row),
+//   warp 1   allocates TMEM (two accumulators of BN fp32 columns, in both SMs
+//            of the pair); in the leader its lane 0 issues
+//            tcgen05.mma.cta_group::2.kind::f16 (M=256, N=BN, K=16) four
+//            times per stage; tcgen05.commit (multicast to the pair) frees the
+//            stage and, after a tile's last stage, hands both accumulators to
+//            the epilogues.
+//   warps 2-9 epilogue (both CTAs): tcgen05.ld 32 columns at a time (thread =
+//            tile row, two warps per TMEM lane quarter),
 //            fused per projection:
 //              QKV    + bias, RoPE on q/k pairs (i, i+D/2), q -> fp16 buffer,
 //                     k/v -> cache slots cache_len + m and k_new / v_new
@@ -45,24 +52,27 @@ constexpr int BM = 128, BK = 64;
 constexpr int kEpiWarps = 8;   // two per TMEM lane quarter, splitting the columns
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map,
-                                            int x, int y, uint64_t* bar) {
+// 2-D tile into this CTA's shared memory, completing on an mbarrier that may
+// be in the other CTA of the pair (shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, int x, int y,
+                                                 uint32_t bar_cluster) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      ".cta_group::2 [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster)
       : "memory");
 }
 
-// Same tile into the shared memory of every CTA in `mask` (same offset), each
-// CTA's mbarrier at the offset of `bar` receiving the bytes it got.
-__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, int x, int y,
-                                               uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(mask)
-      : "memory");
+// Address of this CTA's shared variable `p` in the CTA of cluster rank `rank`.
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
+               : "memory");
 }
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -99,29 +109,32 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
   return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b,
-                                        uint32_t idesc, uint32_t accumulate) {
+// D (TMEM, both SMs) [+]= A (256 rows: 128 in each CTA's shared memory at the
+// offset of `a`) x B (N rows: N/2 in each CTA at the offset of `b`).
+__device__ __forceinline__ void mma_f16_pair(uint32_t d_tmem, uint64_t a, uint64_t b,
+                                             uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+// Arrives, once the MMAs issued so far complete, on the mbarrier at the offset
+// of `bar` in both CTAs of the pair.
+__device__ __forceinline__ void mma_commit_pair(uint64_t* bar) {
   asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_u32(bar))
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_u32(bar)), "h"((uint16_t)3)
       : "memory");
 }
 
-// Arrives (when this CTA's prior MMAs complete) on the mbarrier at the offset
-// of `bar` in every CTA of `mask`.
-__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t mask) {
+// Same, on this CTA's mbarrier only.
+__device__ __forceinline__ void mma_commit_local(uint64_t* bar) {
   asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(bar)), "h"(mask)
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
       : "memory");
 }
 
@@ -159,30 +172,30 @@ __device__ __forceinline__ void store_h32(__half* dst, const float* v) {
 
 template <int BN>
 struct Cfg {
-  static constexpr int kStages = BN == 256 ? 4 : 6;
+  static constexpr int kBHalf = BN / 2;                  // weight rows per CTA of the pair
   static constexpr int kABytes = BM * BK * 2;
-  static constexpr int kBBytes = BN * BK * 2;
+  static constexpr int kBBytes = kBHalf * BK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = (192 * 1024) / kStageBytes;
   static constexpr int kTmemCols = 2 * BN;  // two accumulators
   static constexpr size_t kSmem = (size_t)kStages * kStageBytes + 1024 + 256;
 };
 
-// A work unit is (N tile nt, M tile group mg): the CTA of rank r in a cluster
-// of NC (1 or 2) takes M tile mg * NC + r.
-template <int EPI, int BN, int NC>
+// A work unit is (N tile nt, M tile pair mp, K split ks): the CTA of rank r
+// in the pair takes M tile 2 mp + r.
+template <int EPI, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ TcGemmParams p) {
   using C = Cfg<BN>;
-  constexpr int kBBox = 64;                 // rows per B tensor-map box
-  constexpr int kBBoxes = BN / kBBox;
-  static_assert(kBBoxes % NC == 0, "B boxes split over the cluster");
+  constexpr int kBBox = 64;                      // rows per weight tensor-map box
+  constexpr int kBBoxes = C::kBHalf / kBBox;     // boxes per CTA and stage
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
   uint64_t* empty = full + C::kStages;
   uint64_t* tfull = empty + C::kStages;   // [2]
-  uint64_t* tempty = tfull + 2;           // [2]
+  uint64_t* tempty = tfull + 2;           // [2], counted in the leader
   uint64_t* drain = tempty + 2;           // [1], used only on the abort path
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -190,37 +203,37 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int KB = (p.K + BK - 1) / BK;
 
-  const int rank = NC > 1 ? (int)cluster_rank() : 0;
-  const int cl = blockIdx.x / NC, ncl = gridDim.x / NC;   // cluster index and count
-  const int mgroups = (p.tiles_m + NC - 1) / NC;
-  // K is split S ways for the down projection (partials added by the last split)
+  const uint32_t rank = cluster_rank();          // 0: the leader, which issues the MMAs
+  const int cl = blockIdx.x >> 1, ncl = gridDim.x >> 1;   // pair index and count
+  const int mpairs = (p.tiles_m + 1) / 2;
+  // K is split S ways for the down projection (partials added by a second kernel)
   const int S = EPI == kTcResidOutF16 ? p.splits : 1;
   const int KBs = (KB + S - 1) / S;   // K blocks per split
-  const int units = mgroups * p.tiles_n * S;
+  const int units = mpairs * p.tiles_n * S;
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], NC);   // both CTAs' MMAs release a shared stage
+      mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], kEpiWarps);
+      mbar_init(&tempty[a], 2 * kEpiWarps);   // the epilogue warps of both CTAs
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == 1) {   // the same columns in both SMs of the pair
     asm volatile(
-        "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+        "tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
             smem_u32(tmem_slot)),
         "r"((uint32_t)C::kTmemCols)
         : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
   }
   tc_fence_before();
   __syncthreads();
-  if (NC > 1) cluster_sync();   // the peer's mbarriers exist before any multicast
+  cluster_sync();   // the leader's barriers exist before the peer's copies complete on them
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -231,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool waited = false;
       for (int u = cl; u < units && !*abort_flag; u += ncl) {
         const int t = u / S, ks = u % S;
-        const int mt = (t % mgroups) * NC + rank, nt = t / mgroups;
+        const int mt = (t % mpairs) * 2 + (int)rank, nt = t / mpairs;
         const int m0 = mt * BM, n0 = nt * (EPI == kTcGateUp ? BN / 2 : BN);
         const int kb1 = min(KB, (ks + 1) * KBs);
         for (int kb = ks * KBs; kb < kb1; ++kb, ++it) {
@@ -242,50 +255,44 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           uint8_t* sa = smem + (size_t)s * C::kStageBytes;
           uint8_t* sb = sa + C::kABytes;
-          mbar_arrive_expect_tx(&full[s], C::kStageBytes);
-          // B boxes of kBBox rows; with a pair, rank r loads boxes r, r + 2, ...
-          // and multicasts each to both CTAs
+          if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * C::kStageBytes);
+          const uint32_t fb = cluster_addr(&full[s], 0);
+          // this CTA's weight rows: GATEUP leader W_gate, peer W_up (same rows);
+          // otherwise rows n0 + rank * BN/2 ...
 #pragma unroll
-          for (int bx = rank; bx < kBBoxes; bx += NC) {
+          for (int bx = 0; bx < kBBoxes; ++bx) {
             const CUtensorMap* mb;
             int row;
-            if (EPI == kTcGateUp) {   // boxes of W_gate rows, then of W_up rows
-              constexpr int kHalf = kBBoxes / 2;
-              mb = &p.tmB[bx / kHalf];
-              row = n0 + (bx % kHalf) * kBBox;
+            if (EPI == kTcGateUp) {
+              mb = &p.tmB[rank];
+              row = n0 + bx * kBBox;
             } else {
               int seg = 0;
-              row = n0 + bx * kBBox;
+              row = n0 + (int)rank * C::kBHalf + bx * kBBox;
               if (EPI == kTcQKV) {
                 while (seg < 2 && row >= p.seg_rows[seg]) row -= p.seg_rows[seg++];
               }
               mb = &p.tmB[seg];
             }
-            uint8_t* dst = sb + bx * (kBBox * BK * 2);
-            if (NC > 1) tma_load_2d_mc(dst, mb, kb * BK, row, &full[s], (uint16_t)((1u << NC) - 1));
-            else tma_load_2d(dst, mb, kb * BK, row, &full[s]);
+            tma_load_2d_pair(sb + bx * (kBBox * BK * 2), mb, kb * BK, row, fb);
           }
           if (!waited) {  // activations come from the previous kernel
             griddep_wait();
             griddep_launch();
             waited = true;
           }
-          tma_load_2d(sa, &p.tmA, kb * BK, m0, &full[s]);
+          tma_load_2d_pair(sa, &p.tmA, kb * BK, m0, fb);
         }
       }
       if (!waited) {
         griddep_wait();
         griddep_launch();
       }
-      if (*abort_flag) {
-        for (int k = max(0, it - C::kStages); k < it; ++k)
-          mbar_wait(&full[k % C::kStages], (k / C::kStages) & 1, nullptr);
-      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_f16(BM, BN);
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc = idesc_f16(2 * BM, BN);
       int it = 0, tcount = 0;
       bool issued = false;
       for (int u = cl; u < units && !*abort_flag; u += ncl, ++tcount) {
@@ -309,16 +316,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t db = smem_desc_sw128(sa + C::kABytes);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)  // +32 bytes per K step inside the swizzle atom
-            mma_f16(d_tmem, da + 2 * k, db + 2 * k, idesc, (kb != kb0) || (k != 0));
+            mma_f16_pair(d_tmem, da + 2 * k, db + 2 * k, idesc, (kb != kb0) || (k != 0));
           issued = true;
-          if (NC > 1) mma_commit_mc(&empty[s], (uint16_t)((1u << NC) - 1));
-          else mma_commit(&empty[s]);
+          mma_commit_pair(&empty[s]);
         }
         if (*abort_flag) break;
-        mma_commit(&tfull[acc]);
+        mma_commit_pair(&tfull[acc]);
       }
       if (*abort_flag && issued) {  // let issued MMAs finish before TMEM is freed
-        mma_commit(drain);
+        mma_commit_local(drain);
         mbar_wait(drain, 0, nullptr);
       }
     }
@@ -337,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int u = cl; u < units; u += ncl, ++tcount) {
       const int acc = tcount & 1;
       const int t = u / S, ks = u % S;
-      const int mt = (t % mgroups) * NC + rank, nt = t / mgroups;
+      const int mt = (t % mpairs) * 2 + (int)rank, nt = t / mpairs;
       const int m = mt * BM + row_in_tile;
       const bool row_ok = m < p.M;
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
@@ -532,18 +538,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[acc]);
+      if (lane == 0) mbar_arrive_cluster(cluster_addr(&tempty[acc], 0));   // leader's count
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  // neither CTA of a pair leaves while the other may still multicast into its
-  // shared memory or arrive on its barriers
-  if (NC > 1) cluster_sync();
+  // neither CTA of the pair leaves while the other may still use its shared
+  // memory, its barriers or its TMEM
+  cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
                  "r"((uint32_t)C::kTmemCols)
                  : "memory");
   }
@@ -664,51 +670,54 @@ int make_tmap_rows8(CUtensorMap* map, const void* base, int64_t rows, int64_t K,
   return r == CUDA_SUCCESS ? 0 : -1;
 }
 
-template <int EPI, int BN, int NC>
+template <int EPI, int BN>
 static cudaError_t launch_tc(TcGemmParams& p, int num_sms, cudaStream_t s, bool pdl) {
   using C = Cfg<BN>;
-  const int mgroups = (p.tiles_m + NC - 1) / NC;
-  int units = mgroups * p.tiles_n;
-  // co-resident clusters: one CTA per SM, whole clusters only
-  static int max_clusters = 0;
-  if (max_clusters == 0) {
+  p.tiles_m = (p.M + BM - 1) / BM;
+  const int bn_out = EPI == kTcGateUp ? BN / 2 : BN;
+  p.tiles_n = (p.N + bn_out - 1) / bn_out;
+  p.num_tiles = p.tiles_m * p.tiles_n;
+  const int mpairs = (p.tiles_m + 1) / 2;
+  int units = mpairs * p.tiles_n;
+  // co-resident pairs: one CTA per SM
+  static int max_pairs = 0;
+  if (max_pairs == 0) {
     cudaLaunchConfig_t q = {};
-    q.gridDim = dim3(NC * 64);
+    q.gridDim = dim3(2 * 64);
     q.blockDim = dim3(kThreads);
     q.dynamicSmemBytes = C::kSmem;
     cudaLaunchAttribute qa[1];
     qa[0].id = cudaLaunchAttributeClusterDimension;
-    qa[0].val.clusterDim.x = NC;
+    qa[0].val.clusterDim.x = 2;
     qa[0].val.clusterDim.y = 1;
     qa[0].val.clusterDim.z = 1;
     q.attrs = qa;
     q.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel<EPI, BN, NC>, &q) != cudaSuccess ||
-        n < 1)
-      n = num_sms / NC;
-    max_clusters = n < num_sms / NC ? n : num_sms / NC;
+    if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel<EPI, BN>, &q) != cudaSuccess || n < 1)
+      n = num_sms / 2;
+    max_pairs = n < num_sms / 2 ? n : num_sms / 2;
   }
   p.splits = 1;
   if (EPI == kTcResidOutF16 && p.part) {
-    // split K so that the units fill the co-resident clusters (8+ K blocks each)
-    int S = max_clusters / units;
+    // split K so that the units fill the co-resident pairs (8+ K blocks each)
+    int S = max_pairs / units;
     S = S < 1 ? 1 : (S > p.max_splits ? p.max_splits : S);
     const int KB = (p.K + BK - 1) / BK;
     while (S > 1 && KB / S < 8) --S;
     p.splits = S;
     units *= S;
   }
-  const int clusters = units < max_clusters ? units : max_clusters;
+  const int pairs = units < max_pairs ? units : max_pairs;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(clusters * NC);
+  cfg.gridDim = dim3(2 * pairs);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = C::kSmem;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   int na = 0;
   attr[na].id = cudaLaunchAttributeClusterDimension;
-  attr[na].val.clusterDim.x = NC;
+  attr[na].val.clusterDim.x = 2;
   attr[na].val.clusterDim.y = 1;
   attr[na].val.clusterDim.z = 1;
   ++na;
@@ -719,47 +728,23 @@ static cudaError_t launch_tc(TcGemmParams& p, int num_sms, cudaStream_t s, bool 
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<EPI, BN, NC>, p);
-}
-
-template <int EPI, int BN>
-static cudaError_t launch_tc_any(TcGemmParams& p, int num_sms, cudaStream_t s, bool pdl) {
-  p.tiles_m = (p.M + BM - 1) / BM;
-  const int bn_out = EPI == kTcGateUp ? BN / 2 : BN;
-  p.tiles_n = (p.N + bn_out - 1) / bn_out;
-  p.num_tiles = p.tiles_m * p.tiles_n;
-  // clusters share the weight tile when there are M tiles to group
-  if constexpr (BN / 64 % 4 == 0) {
-    if (p.tiles_m >= 4) return launch_tc<EPI, BN, 4>(p, num_sms, s, pdl);
-  }
-  if (p.tiles_m >= 2) return launch_tc<EPI, BN, 2>(p, num_sms, s, pdl);
-  return launch_tc<EPI, BN, 1>(p, num_sms, s, pdl);
+  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<EPI, BN>, p);
 }
 
 cudaError_t launch_tc_gemm(TcGemmParams& p, int epi, int num_sms, cudaStream_t s,
                            bool pdl) {
   switch (epi) {
-    case kTcQKV: return launch_tc_any<kTcQKV, 128>(p, num_sms, s, pdl);
-    case kTcResidF32: return launch_tc_any<kTcResidF32, 128>(p, num_sms, s, pdl);
-    case kTcGateUp: return launch_tc_any<kTcGateUp, 256>(p, num_sms, s, pdl);
-    default: return launch_tc_any<kTcResidOutF16, 256>(p, num_sms, s, pdl);
+    case kTcQKV: return launch_tc<kTcQKV, 128>(p, num_sms, s, pdl);
+    case kTcResidF32: return launch_tc<kTcResidF32, 128>(p, num_sms, s, pdl);
+    case kTcGateUp: return launch_tc<kTcGateUp, 256>(p, num_sms, s, pdl);
+    default: return launch_tc<kTcResidOutF16, 256>(p, num_sms, s, pdl);
   }
 }
 
 template <int EPI, int BN>
 static cudaError_t configure_one() {
-  cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<EPI, BN, 1>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)Cfg<BN>::kSmem);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(tc_gemm_kernel<EPI, BN, 2>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg<BN>::kSmem);
-  if constexpr (BN / 64 % 4 == 0) {
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(tc_gemm_kernel<EPI, BN, 4>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg<BN>::kSmem);
-  }
-  return e;
+  return cudaFuncSetAttribute(tc_gemm_kernel<EPI, BN>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg<BN>::kSmem);
 }
 
 cudaError_t configure_tc_gemm_kernels() {
