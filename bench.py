@@ -46,12 +46,11 @@ PREFILL_T = 1024
 # decode_persistent_1p5b_28layers_ctx4096.md).  Must be set back to None
 # whenever the kernel changes.
 NCU_TRAFFIC = {
-    "gemm_gateup": 58.261248e6 + 1.469952e6,
-    "gemm_down": 52.183296e6 + 0.454144e6,
-    "gemm_qkv": 10.012416e6,
-    "gemm_o": 11.026688e6,
+    "gemm_gateup": 58.231808e6 + 3.192832e6,
+    "gemm_down": 45.937152e6 + 1.509376e6,
+    "gemm_qkv": 10.00576e6 + 0.000768e6,
+    "gemm_o": 11.030016e6 + 0.000256e6,
     "attn_prefill": 4.226304e6,
-    ("decode_persistent", 4096): 2.742902e9 + 0.039405568e9,
 }
 
 
