@@ -228,9 +228,15 @@ int run_prefill(blk_handle h, const blk_weights* w, const void* x,
 
   // causal GQA attention over [history; new rows]
   PrefillAttnParams pa = {};
-  if (make_tmap_2d(&pa.tm_k, k_cache, (int64_t)Hkv * c.max_ctx, D, 64) ||
-      make_tmap_2d(&pa.tm_v, v_cache, (int64_t)Hkv * c.max_ctx, D, 64))
-    return BLK_ERR_CUDA;
+  {
+    const int64_t qd[3] = {D, Hq, M}, qs[2] = {(int64_t)D * 2, (int64_t)Hq * D * 2};
+    const int qb[3] = {64, 1, 128};
+    const int64_t kd[3] = {D, L + M, Hkv}, ks[2] = {(int64_t)D * 2, c.max_ctx * D * 2};
+    const int kb[3] = {64, 128, 1};
+    if (make_tmap_3d(&pa.tm_q, q16, qd, qs, qb) || make_tmap_3d(&pa.tm_k, k_cache, kd, ks, kb) ||
+        make_tmap_3d(&pa.tm_v, v_cache, kd, ks, kb))
+      return BLK_ERR_CUDA;
+  }
   pa.q16 = q16;
   pa.err = h->status;
   pa.max_ctx = c.max_ctx; pa.cache_len = L;

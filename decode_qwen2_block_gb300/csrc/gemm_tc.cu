@@ -377,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int k = 0; k < 16; ++k) cs4[k] = make_float4(1.f, 0.f, 1.f, 0.f);
           }
           if (!waited) {
-            if (!mbar_wait(&tfull[acc], (tcount >> 1) & 1, p.err)) {
+            if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], (tcount >> 1) & 1, p.err))) {
               *abort_flag = 1;
               break;
             }
@@ -423,14 +423,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (!waited) {   // no item for this warp: still wait so the release is ordered
-          if (!mbar_wait(&tfull[acc], (tcount >> 1) & 1, p.err)) {
+          if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], (tcount >> 1) & 1, p.err))) {
             *abort_flag = 1;
             break;
           }
           tc_fence_after();
         }
       } else if constexpr (EPI == kTcGateUp) {
-        if (!mbar_wait(&tfull[acc], (tcount >> 1) & 1, p.err)) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], (tcount >> 1) & 1, p.err))) {
           *abort_flag = 1;
           break;
         }
@@ -496,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < 2; ++c)
               if (c2 + c < kCh) load_res(32 * e + 64 * (c2 + c), rv[c]);
             if (!waited) {
-              if (!mbar_wait(&tfull[acc], (tcount >> 1) & 1, p.err)) {
+              if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], (tcount >> 1) & 1, p.err))) {
                 *abort_flag = 1;
                 break;
               }
@@ -518,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           // split K: this split's fp32 partial; splitk_reduce_kernel adds the
           // partials in split order, plus the residual
-          if (!mbar_wait(&tfull[acc], (tcount >> 1) & 1, p.err)) {
+          if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], (tcount >> 1) & 1, p.err))) {
             *abort_flag = 1;
             break;
           }
@@ -639,6 +639,20 @@ int make_tmap_2d(CUtensorMap* map, const void* base, int64_t rows, int64_t K,
       map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box,
       estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : -1;
+}
+
+int make_tmap_3d(CUtensorMap* map, const void* base, const int64_t* dims,
+                 const int64_t* strides, const int* box) {
+  const EncodeTiledFn encode = encode_tiled();
+  if (!encode) return -1;
+  cuuint64_t d[3] = {(cuuint64_t)dims[0], (cuuint64_t)dims[1], (cuuint64_t)dims[2]};
+  cuuint64_t st[2] = {(cuuint64_t)strides[0], (cuuint64_t)strides[1]};
+  cuuint32_t bx[3] = {(cuuint32_t)box[0], (cuuint32_t)box[1], (cuuint32_t)box[2]};
+  cuuint32_t es[3] = {1, 1, 1};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), d, st,
+                            bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? 0 : -1;
 }
 

@@ -51,6 +51,10 @@ struct TcGemmParams {
 // 128-byte swizzle, zero fill out of bounds.  Returns 0 on success.
 int make_tmap_2d(CUtensorMap* map, const void* base, int64_t rows, int64_t K,
                  int box_rows);
+// 3-D fp16 tensor map with 128-byte swizzle and zero fill: dims innermost
+// first, strides (bytes) of dims 1 and 2, box sizes.  Returns 0 on success.
+int make_tmap_3d(CUtensorMap* map, const void* base, const int64_t* dims,
+                 const int64_t* strides, const int* box);
 // Tensor map of 8-row weight boxes with 128-byte swizzle for the decode
 // kernel: the 3-D view (64, rows, K / 64) with box (64, 8, cbs) when
 // K % 64 == 0 (*is3d = 1), else the 2-D view (K, rows) with box (64, 8).

@@ -15,12 +15,13 @@ cudaError_t launch_rmsnorm_rows(const void* x, bool x_is_f32, const __half* g,
                                 cudaStream_t s, bool pdl);
 
 struct PrefillAttnParams {
-  CUtensorMap tm_k;   // K cache viewed as [Hkv * max_ctx, D], box 64 x 64, SW128
-  CUtensorMap tm_v;
+  CUtensorMap tm_q;   // q [T, Hq, D] viewed as (D, Hq, T), box 64 x 1 x 128, SW128
+  CUtensorMap tm_k;   // K cache viewed as (D, L + T, Hkv), box 64 x 128 x 1, SW128:
+  CUtensorMap tm_v;   //   slots past L + T read as zeros
   const __half* q16;  // [T, Hq, D]
   int64_t max_ctx, cache_len;
   int T, Hq, Hkv, D;
-  float scale_log2;
+  float scale_log2;   // log2(e) / sqrt(D)
   __half* attn16;  // [T, Hq * D]
   int* err;
 };
