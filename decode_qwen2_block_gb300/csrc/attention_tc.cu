@@ -2,20 +2,25 @@
 // cores (the FAttention step of the TopOp decoder block: softmax(q k^T /
 // sqrt(D)) v over slots [0, L + t] for new row t).
 //
-// CTA = (query head h, block of 128 new rows), 6 warps:
+// CTA = (query head h, block of 128 new rows, chunk of that block's 128-slot
+// tiles), 6 warps:
 //   warp 0   TMA producer: the Q block once (3-D view of q [T, Hq, D]), then
-//            128-slot K and V tiles of kv head h / (Hq/Hkv) into two stages.
-//            The K/V tensor maps end at slot L + T, so slots past the last
-//            valid one arrive as zeros (stale cache contents never reach PV).
+//            the chunk's K and V tiles of kv head h / (Hq/Hkv) into two
+//            stages.  The K/V tensor maps end at slot L + T, so slots past the
+//            last valid one arrive as zeros (stale cache contents never reach PV).
 //   warp 1   allocates TMEM (S: 128 columns, O: D columns) and its lane 0
 //            issues the MMAs (tcgen05.mma.cta_group::1.kind::f16, M = 128):
 //            S_j = Q K_j^T (N = 128, K = D), then O += P_j V_j (N = D,
 //            K = 128; V is the MN-major B operand).  S_{j+1} is issued as
 //            soon as the softmax has read S_j, so it overlaps that softmax.
-//   warps 2-5 softmax (thread = query row): read S_j from TMEM, scale by
-//            log2(e)/sqrt(D), causal mask, online softmax in base 2 (rescale
-//            O in TMEM when the row maximum grows), write P_j (fp16) to shared
-//            memory in the MMA's K-major layout; at the end O / l -> attn (fp16).
+//   warps 2-5 softmax (thread = query row): read S_j from TMEM, causal mask on
+//            tiles that cross the diagonal, online softmax in base 2 with lazy
+//            rescaling of O in TMEM, P_j (fp16) into one of two shared-memory
+//            buffers in the MMA's K-major layout; at the end O / l -> attn.
+// A block whose tiles are split over several CTAs (chunks, so that the long
+// blocks of the causal triangle do not set the kernel's duration) publishes
+// per-chunk partials (O, m, l in fp32) that attn_merge_kernel, launched next,
+// combines.
 // Every wait is bounded; on a timeout the CTA records an error, stops, lets
 // issued MMAs finish and frees its TMEM before returning.
 #include <math.h>
@@ -137,24 +142,64 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+__device__ __forceinline__ float ex2(float x) {   // 2^x; ex2(-inf) = +0
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 template <int D>
 struct Smem {
   static constexpr int kQBytes = kRows * D * 2;            // [D/64][128 rows][128 B]
   static constexpr int kKVTile = kSlots * D * 2;            // K or V: [D/64][128 slots][128 B]
   static constexpr int kStage = 2 * kKVTile;
-  static constexpr int kPBytes = kRows * kSlots * 2;        // [2][128 rows][128 B]
+  static constexpr int kPBuf = kRows * kSlots * 2;          // [2][128 rows][128 B]
   static constexpr int kQOff = 0;
   static constexpr int kKVOff = kQBytes;
-  static constexpr int kPOff = kKVOff + kStages * kStage;
-  static constexpr int kBarOff = kPOff + kPBytes;
+  static constexpr int kPOff = kKVOff + kStages * kStage;   // two P buffers
+  static constexpr int kBarOff = kPOff + 2 * kPBuf;
   static constexpr size_t kBytes = (size_t)kBarOff + 256 + 1024;
   static constexpr uint32_t kTmemCols = 256;                 // S (128) + O (D), power of two
 };
+
+// Partial result of one chunk of a query block (fp32): per 32-row quarter q
+// its O (not normalised) as [D/4][32 rows] float4 at q * D * 32 floats (one
+// contiguous block of D * 128 bytes), then at 128 * D floats, per quarter, the
+// rows' reference maxima m (log2 units) and sums l: [4][m 32 | l 32].
+template <int D>
+__device__ __forceinline__ float* part_ptr(const PrefillAttnParams& p, int h, int qb, int ch) {
+  return p.part + ((size_t)(h * p.nqb + qb) * p.max_chunks + ch) * (size_t)(kRows * (D + 2));
+}
+
+__device__ __forceinline__ void store_row32(__half* d, const float* v, float inv) {
+  uint4* d4 = reinterpret_cast<uint4*>(d);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    uint4 u;
+    __half2* hp = reinterpret_cast<__half2*>(&u);
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      hp[e] = __floats2half2_rn(v[8 * k + 2 * e] * inv, v[8 * k + 2 * e + 1] * inv);
+    d4[k] = u;
+  }
+}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_attn_tc_kernel(const __grid_constant__ PrefillAttnParams p) {
   using Sm = Smem<D>;
+  const int h = blockIdx.x;
+  const int qb = p.nqb - 1 - (int)blockIdx.y;  // longest rows first
+  const int ch = blockIdx.z;                     // chunk of the block's tiles
+  const int t0 = qb * kRows;
+  const int64_t L = p.cache_len;
+  const int64_t n_keys = L + min(p.T, t0 + kRows);  // slots this block can see
+  const int ntot = (int)((n_keys + kSlots - 1) / kSlots);
+  const int nch = (ntot + p.chunk_tiles - 1) / p.chunk_tiles;
+  if (ch >= nch) return;                         // (uniform over the CTA)
+  const int j0 = ch * p.chunk_tiles;             // first tile of this CTA
+  const int nt = min(ntot, j0 + p.chunk_tiles) - j0;
+
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -163,36 +208,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sP = smem + Sm::kPOff;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Sm::kBarOff);
   uint64_t* q_full = bars;
-  uint64_t* kv_full = bars + 1;           // [2]
-  uint64_t* kv_empty = bars + 3;          // [2]
-  uint64_t* s_full = bars + 5;            // S_j in TMEM
-  uint64_t* s_free = bars + 6;            // the softmax has read S_j
-  uint64_t* p_full = bars + 7;            // P_j in shared memory, O rescaled
-  uint64_t* o_done = bars + 8;            // O += P_j V_j complete
-  uint64_t* drain = bars + 9;             // abort path
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 10);
+  uint64_t* k_full = bars + 1;            // [2] K_j in stage j % 2
+  uint64_t* k_empty = bars + 3;           // [2] S_j complete: K stage free
+  uint64_t* v_full = bars + 5;            // [2]
+  uint64_t* v_empty = bars + 7;           // [2] PV_j complete: V stage free
+  uint64_t* s_full = bars + 9;            // S_j in TMEM
+  uint64_t* s_free = bars + 10;           // the softmax has read S_j
+  uint64_t* p_full = bars + 11;           // [2] P_j in buffer j % 2 (O rescaled)
+  uint64_t* o_done = bars + 13;           // [2] O += P_j V_j complete (j % 2)
+  uint64_t* drain = bars + 15;            // abort path
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = blockIdx.x;
-  const int nqb = (p.T + kRows - 1) / kRows;
-  const int qb = nqb - 1 - (int)blockIdx.y;  // longest rows first
-  const int t0 = qb * kRows;
   const int G = p.Hq / p.Hkv, g = h / G;
-  const int64_t L = p.cache_len;
-  const int64_t n_keys = L + min(p.T, t0 + kRows);  // slots this block can see
-  const int ntiles = (int)((n_keys + kSlots - 1) / kSlots);
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
+      mbar_init(&p_full[s], 4);
+      mbar_init(&o_done[s], 1);
     }
     mbar_init(s_full, 1);
     mbar_init(s_free, 4);
-    mbar_init(p_full, 4);
-    mbar_init(o_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -220,27 +262,41 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int hh = 0; hh < D / 64; ++hh)
         tma_load_3d(sQ + hh * (kRows * 128), &p.tm_q, hh * 64, h, t0, q_full);
-      int issued = 0;
-      for (int j = 0; j < ntiles; ++j, ++issued) {
+      // K_j's stage frees when S_j is complete, V_j's when PV_j is: K runs
+      // up to two tiles ahead of the softmax.
+      int issued_k = 0, issued_v = 0;
+      for (int j = 0; j < nt; ++j) {
         const int s = j % kStages;
+        const uint32_t par = ((j / kStages) - 1) & 1;
+        uint8_t* st = sKV + (size_t)s * Sm::kStage;
+        const int y = (j0 + j) * kSlots;
         if (*abort_flag) break;
-        if (j >= kStages && !mbar_wait(&kv_empty[s], ((j / kStages) - 1) & 1, p.err)) {
+        if (j >= kStages && !mbar_wait(&k_empty[s], par, p.err)) {
           *abort_flag = 1;
           break;
         }
-        mbar_arrive_expect_tx(&kv_full[s], Sm::kStage);
-        uint8_t* st = sKV + (size_t)s * Sm::kStage;
+        mbar_arrive_expect_tx(&k_full[s], Sm::kKVTile);
 #pragma unroll
-        for (int hh = 0; hh < D / 64; ++hh) {
-          tma_load_3d(st + hh * (kSlots * 128), &p.tm_k, hh * 64, j * kSlots, g, &kv_full[s]);
-          tma_load_3d(st + Sm::kKVTile + hh * (kSlots * 128), &p.tm_v, hh * 64, j * kSlots, g,
-                      &kv_full[s]);
+        for (int hh = 0; hh < D / 64; ++hh)
+          tma_load_3d(st + hh * (kSlots * 128), &p.tm_k, hh * 64, y, g, &k_full[s]);
+        ++issued_k;
+        if (j >= kStages && !mbar_wait(&v_empty[s], par, p.err)) {
+          *abort_flag = 1;
+          break;
         }
+        mbar_arrive_expect_tx(&v_full[s], Sm::kKVTile);
+#pragma unroll
+        for (int hh = 0; hh < D / 64; ++hh)
+          tma_load_3d(st + Sm::kKVTile + hh * (kSlots * 128), &p.tm_v, hh * 64, y, g,
+                      &v_full[s]);
+        ++issued_v;
       }
       // copies still in flight land before shared memory goes away
       mbar_wait(q_full, 0, nullptr);
-      for (int k = max(0, issued - kStages); k < issued; ++k)
-        mbar_wait(&kv_full[k % kStages], (k / kStages) & 1, nullptr);
+      for (int k = max(0, issued_k - kStages); k < issued_k; ++k)
+        mbar_wait(&k_full[k % kStages], (k / kStages) & 1, nullptr);
+      for (int k = max(0, issued_v - kStages); k < issued_v; ++k)
+        mbar_wait(&v_full[k % kStages], (k / kStages) & 1, nullptr);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -251,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool issued = false;
       auto issue_s = [&](int j) -> bool {   // S_j = Q K_j^T
         const int s = j % kStages;
-        if (!mbar_wait(&kv_full[s], (j / kStages) & 1, p.err)) return false;
+        if (!mbar_wait(&k_full[s], (j / kStages) & 1, p.err)) return false;
         if (j > 0 && !mbar_wait(s_free, (j - 1) & 1, p.err)) return false;
         tc_fence_after();
         const uint32_t kb = smem_u32(sKV + (size_t)s * Sm::kStage);
@@ -265,23 +321,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         issued = true;
         commit(s_full);
+        commit(&k_empty[s]);
         return true;
       };
       if (ok) ok = issue_s(0);
-      for (int j = 0; j < ntiles && ok; ++j) {
-        if (j + 1 < ntiles && !issue_s(j + 1)) { ok = false; break; }
-        if (!mbar_wait(p_full, j & 1, p.err)) { ok = false; break; }
+      for (int j = 0; j < nt && ok; ++j) {
+        if (j + 1 < nt && !issue_s(j + 1)) { ok = false; break; }
+        const int b = j & 1;
+        if (!mbar_wait(&p_full[b], (j >> 1) & 1, p.err)) { ok = false; break; }
+        if (!mbar_wait(&v_full[j % kStages], (j / kStages) & 1, p.err)) { ok = false; break; }
         tc_fence_after();
         const uint32_t vb = smem_u32(sKV + (size_t)(j % kStages) * Sm::kStage + Sm::kKVTile);
-        const uint32_t pb = smem_u32(sP);
+        const uint32_t pb = smem_u32(sP + b * Sm::kPBuf);
 #pragma unroll
         for (int kk = 0; kk < kSlots / 16; ++kk) {   // O += P_j V_j over 16 slots at a time
           const uint64_t a = desc_kmajor(pb + (kk >> 2) * (kRows * 128)) + ((kk & 3) * 32 >> 4);
-          const uint64_t b = desc_mnmajor(vb + kk * 16 * 128);
-          mma(tO, a, b, id_o, (j | kk) != 0);
+          const uint64_t bd = desc_mnmajor(vb + kk * 16 * 128);
+          mma(tO, a, bd, id_o, (j | kk) != 0);
         }
-        commit(o_done);
-        commit(&kv_empty[j % kStages]);
+        commit(&o_done[b]);
+        commit(&v_empty[j % kStages]);
       }
       if (!ok) {
         *abort_flag = 1;
@@ -299,6 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool row_ok = t < p.T;
     const int64_t last = L + t;             // last slot row t may see
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    const float sl2 = p.scale_log2;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     // The tcgen05.ld/st below are warp-collective (.sync.aligned): every
@@ -306,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto wait_all = [&](uint64_t* bar, uint32_t parity) {
       return __all_sync(0xffffffffu, mbar_wait(bar, parity, p.err));
     };
-    for (int j = 0; j < ntiles; ++j) {
+    for (int j = 0; j < nt; ++j) {
       if (!wait_all(s_full, j & 1)) { ok = false; break; }
       tc_fence_after();
       float sv[kSlots];
@@ -316,15 +376,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(s_free);   // S may be overwritten by S_{j+1}
-      const int64_t js = (int64_t)j * kSlots;
-      float mx = -INFINITY;
+      const int64_t js = (int64_t)(j0 + j) * kSlots;
+      if (js + kSlots - 1 > L + t0) {         // the tile crosses the causal diagonal
+        const int64_t d = last - js;
+        const int lim = d < -1 ? -1 : (d > kSlots - 1 ? kSlots - 1 : (int)d);
 #pragma unroll
-      for (int c = 0; c < kSlots; ++c) {
-        float v = sv[c] * p.scale_log2;
-        if (!row_ok || js + c > last) v = -INFINITY;
-        sv[c] = v;
-        mx = fmaxf(mx, v);
+        for (int c = 0; c < kSlots; ++c)
+          if (c > lim) sv[c] = -INFINITY;
       }
+      float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kSlots; c += 4) {
+        a0 = fmaxf(a0, sv[c]);
+        a1 = fmaxf(a1, sv[c + 1]);
+        a2 = fmaxf(a2, sv[c + 2]);
+        a3 = fmaxf(a3, sv[c + 3]);
+      }
+      const float mx = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * sl2;   // log2 units
       // The reference maximum of a row moves (and O, l are rescaled) only
       // when the row maximum grew by more than 2^8 since it last moved: P stays
       // <= 256 and the final 1 / l normalisation makes the choice exact.  The
@@ -333,69 +401,78 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool need = (m == -INFINITY) ? (mx != -INFINITY) : (mx - m > kRescaleLog2);
       const bool move = __any_sync(0xffffffffu, need);
       const float mn = move ? fmaxf(m, mx) : m;
-      const float alpha = (m == -INFINITY || mn == m) ? 1.f : exp2f(m - mn);
-      float sum = 0.f;
-#pragma unroll
-      for (int c = 0; c < kSlots; ++c) {
-        const float e = (sv[c] == -INFINITY) ? 0.f : exp2f(sv[c] - mn);
-        sv[c] = e;
-        sum += e;
-      }
-      l = l * alpha + sum;
-      m = mn;
-      if (j > 0) {
-        // PV_{j-1} must be complete before O is rescaled and P overwritten
-        if (!wait_all(o_done, (j - 1) & 1)) { ok = false; break; }
-        tc_fence_after();
-        if (move) {
-#pragma unroll
-          for (int c = 0; c < D; c += 32) {
-            float ov[32];
-            tmem_ld32(tO + lane_off + c, ov);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) ov[i] *= alpha;
-            tmem_st32(tO + lane_off + c, ov);
-          }
-          tmem_wait_st();
-        }
-      }
+      const float alpha = (m == -INFINITY || mn == m) ? 1.f : ex2(m - mn);
+      const float nref = (mn == -INFINITY) ? 0.f : -mn;
+      // P buffer j % 2 is free once PV_{j-2} is complete
+      if (j >= 2 && !wait_all(&o_done[j & 1], ((j - 2) >> 1) & 1)) { ok = false; break; }
       // P_j (fp16) into the K-major 128-byte-swizzled layout: [slot half][row][128 B]
+      uint8_t* prow = sP + (j & 1) * Sm::kPBuf + r * 128;
+      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
       for (int c = 0; c < kSlots / 8; ++c) {
+        float e[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) e[k] = ex2(fmaf(sv[8 * c + k], sl2, nref));
+        s0 += e[0] + e[4];
+        s1 += e[1] + e[5];
+        s2 += e[2] + e[6];
+        s3 += e[3] + e[7];
         uint4 u;
         __half2* hp = reinterpret_cast<__half2*>(&u);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) hp[e] = __floats2half2_rn(sv[8 * c + 2 * e], sv[8 * c + 2 * e + 1]);
-        const int half = c >> 3, cc = c & 7;
-        *reinterpret_cast<uint4*>(sP + half * (kRows * 128) + r * 128 + ((cc ^ (r & 7)) << 4)) = u;
+        for (int k = 0; k < 4; ++k) hp[k] = __floats2half2_rn(e[2 * k], e[2 * k + 1]);
+        *reinterpret_cast<uint4*>(prow + (c >> 3) * (kRows * 128) + (((c & 7) ^ (r & 7)) << 4)) = u;
+      }
+      l = l * alpha + ((s0 + s1) + (s2 + s3));
+      m = mn;
+      if (move && j > 0) {
+        // PV_{j-1} must be complete before O is rescaled
+        if (!wait_all(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < D; c += 32) {
+          float ov[32];
+          tmem_ld32(tO + lane_off + c, ov);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ov[i] *= alpha;
+          tmem_st32(tO + lane_off + c, ov);
+        }
+        tmem_wait_st();
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // for the tensor core
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
+      if (lane == 0) mbar_arrive(&p_full[j & 1]);
     }
-    if (ok && wait_all(o_done, (ntiles - 1) & 1)) {
+    if (ok && wait_all(&o_done[(nt - 1) & 1], ((nt - 1) >> 1) & 1)) {
       tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
       __half* dst = p.attn16 + ((size_t)t * p.Hq + h) * D;
+      if (nch == 1) {
+        const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
-      for (int c = 0; c < D; c += 32) {
-        float ov[32];
-        tmem_ld32(tO + lane_off + c, ov);
-        tmem_wait_ld();
-        if (row_ok) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + c);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            uint4 u;
-            __half2* hp = reinterpret_cast<__half2*>(&u);
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              hp[e] = __floats2half2_rn(ov[8 * k + 2 * e] * inv, ov[8 * k + 2 * e + 1] * inv);
-            d4[k] = u;
-          }
+        for (int c = 0; c < D; c += 32) {
+          float ov[32];
+          tmem_ld32(tO + lane_off + c, ov);
+          tmem_wait_ld();
+          if (row_ok) store_row32(dst + c, ov, inv);
         }
+      } else {
+        // Several chunks: publish this chunk's partial for attn_merge_kernel.
+        float* P = part_ptr<D>(p, h, qb, ch);
+        float4* Oq = reinterpret_cast<float4*>(P + q * D * 32);
+#pragma unroll
+        for (int c = 0; c < D; c += 32) {
+          float ov[32];
+          tmem_ld32(tO + lane_off + c, ov);
+          tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            Oq[(c / 4 + k) * 32 + lane] =
+                make_float4(ov[4 * k], ov[4 * k + 1], ov[4 * k + 2], ov[4 * k + 3]);
+        }
+        P[kRows * D + q * 64 + lane] = m;
+        P[kRows * D + q * 64 + 32 + lane] = l;
       }
     } else {
       *abort_flag = 1;
@@ -412,10 +489,68 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Merges the partials of every block whose tiles were split over several
+// CTAs: O = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c, M = max_c m_c, as
+// an online merge in chunk order with explicit roundings (the same bits on
+// every run).  CTA = block (h, qb), thread = (row, 32 output columns).
+template <int D>
+__global__ void __launch_bounds__(kRows * D / 32)
+    attn_merge_kernel(const __grid_constant__ PrefillAttnParams p) {
+  const int h = blockIdx.x, qb = blockIdx.y;
+  const int t0 = qb * kRows;
+  const int64_t n_keys = p.cache_len + min(p.T, t0 + kRows);
+  const int ntot = (int)((n_keys + kSlots - 1) / kSlots);
+  const int nch = (ntot + p.chunk_tiles - 1) / p.chunk_tiles;
+  if (nch <= 1) return;                      // written by the attention kernel
+  griddep_wait();
+  griddep_launch();
+  const int r = threadIdx.x & (kRows - 1), grp = threadIdx.x / kRows;
+  const int q = r >> 5, lane = r & 31;
+  float M = -INFINITY, lt = 0.f, acc[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+  auto add = [&](const float4* v, float mc, float lc) {
+    if (mc == -INFINITY) return;             // no slot of this chunk is visible
+    const float mn = fmaxf(M, mc);
+    const float so = (M == -INFINITY) ? 0.f : ex2(M - mn);
+    const float w = ex2(mc - mn);
+    lt = __fmaf_rn(w, lc, __fmul_rn(lt, so));
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      acc[4 * k] = __fmaf_rn(w, v[k].x, __fmul_rn(acc[4 * k], so));
+      acc[4 * k + 1] = __fmaf_rn(w, v[k].y, __fmul_rn(acc[4 * k + 1], so));
+      acc[4 * k + 2] = __fmaf_rn(w, v[k].z, __fmul_rn(acc[4 * k + 2], so));
+      acc[4 * k + 3] = __fmaf_rn(w, v[k].w, __fmul_rn(acc[4 * k + 3], so));
+    }
+    M = mn;
+  };
+  auto load = [&](int c2, float4* v, float& mc, float& lc) {
+    const float* P = part_ptr<D>(p, h, qb, c2);
+    const float4* o4 = reinterpret_cast<const float4*>(P + q * D * 32);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) v[k] = __ldcg(o4 + (grp * 8 + k) * 32 + lane);
+    mc = __ldcg(P + kRows * D + q * 64 + lane);
+    lc = __ldcg(P + kRows * D + q * 64 + 32 + lane);
+  };
+  for (int c2 = 0; c2 < nch; c2 += 2) {      // two chunks' loads in flight
+    float4 va[8], vb[8];
+    float ma, la, mb = -INFINITY, lb = 0.f;
+    load(c2, va, ma, la);
+    if (c2 + 1 < nch) load(c2 + 1, vb, mb, lb);
+    add(va, ma, la);
+    if (c2 + 1 < nch) add(vb, mb, lb);
+  }
+  const int t = t0 + r;
+  if (t < p.T) {
+    const float inv = lt > 0.f ? 1.f / lt : 0.f;
+    store_row32(p.attn16 + ((size_t)t * p.Hq + h) * D + grp * 32, acc, inv);
+  }
+}
+
 template <int D>
 cudaError_t launch_tc(const PrefillAttnParams& p, cudaStream_t s, bool pdl) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.Hq, (p.T + kRows - 1) / kRows);
+  cfg.gridDim = dim3(p.Hq, p.nqb, p.grid_chunks);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = Smem<D>::kBytes;
   cfg.stream = s;
@@ -429,9 +564,69 @@ cudaError_t launch_tc(const PrefillAttnParams& p, cudaStream_t s, bool pdl) {
 
 }  // namespace
 
+int prefill_attn_max_chunks(int64_t T, int Hq, int num_sms) {
+  const int64_t nqb = (T + kRows - 1) / kRows;
+  const int64_t need = (2 * (int64_t)num_sms + Hq * nqb - 1) / (Hq * nqb);
+  return (int)(need > 4 ? need : 4);
+}
+
+size_t prefill_attn_part_bytes(int64_t T, int Hq, int D, int num_sms) {
+  const int64_t nqb = (T + kRows - 1) / kRows;
+  return (size_t)(Hq * nqb) * prefill_attn_max_chunks(T, Hq, num_sms) * kRows * (D + 2) * 4;
+}
+
+// Chooses the chunk length C (tiles per CTA): the estimated time is the
+// number of CTA waves times C, plus one and a half tiles for publishing and
+// merging partials when blocks are split; ties go to the longer chunk.
+void plan_prefill_attn(PrefillAttnParams& p, int num_sms) {
+  const int64_t L = p.cache_len;
+  p.nqb = (p.T + kRows - 1) / kRows;
+  auto tiles = [&](int qb) {
+    return (int)((L + min(p.T, (qb + 1) * kRows) + kSlots - 1) / kSlots);
+  };
+  const int nmax = tiles(p.nqb - 1);
+  double best = 1e300;
+  int best_c = nmax, prev = -1;
+  for (int k = 1; k <= p.max_chunks; ++k) {
+    const int C = (nmax + k - 1) / k;
+    if (C == prev) continue;
+    prev = C;
+    int64_t items = 0;
+    for (int qb = 0; qb < p.nqb; ++qb) items += (tiles(qb) + C - 1) / C;
+    items *= p.Hq;
+    const int64_t waves = (items + num_sms - 1) / num_sms;
+    const double cost = (double)waves * C + (C < nmax ? 1.5 : 0.0);
+    if (cost < best) {
+      best = cost;
+      best_c = C;
+    }
+  }
+  p.chunk_tiles = best_c;
+  p.grid_chunks = (nmax + best_c - 1) / best_c;
+}
+
 cudaError_t launch_prefill_attn(const PrefillAttnParams& p, cudaStream_t s, bool pdl) {
+  if (p.grid_chunks < 1 || p.grid_chunks > p.max_chunks || p.chunk_tiles < 1)
+    return cudaErrorInvalidValue;
+  if (p.grid_chunks > 1 && !p.part) return cudaErrorInvalidValue;
   if (p.D == 128) return launch_tc<128>(p, s, pdl);
   if (p.D == 64) return launch_tc<64>(p, s, pdl);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_attn_merge(const PrefillAttnParams& p, cudaStream_t s, bool pdl) {
+  if (p.grid_chunks <= 1) return cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.Hq, p.nqb);
+  cfg.blockDim = dim3(kRows * p.D / 32);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  if (p.D == 128) return cudaLaunchKernelEx(&cfg, attn_merge_kernel<128>, p);
+  if (p.D == 64) return cudaLaunchKernelEx(&cfg, attn_merge_kernel<64>, p);
   return cudaErrorInvalidValue;
 }
 

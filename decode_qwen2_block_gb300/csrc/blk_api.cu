@@ -21,11 +21,11 @@ constexpr int kMaxPending = 1024;
 // Kernel ids for per-kernel timing (blk_timing_read).
 enum KernelId {
   kKRmsNorm = 0, kKGemmQKV, kKSplitReduce, kKAttnPrefill, kKGemmO, kKGemmGateUp,
-  kKGemmDown, kKDecodeStep, kKCount
+  kKGemmDown, kKDecodeStep, kKAttnMerge, kKCount
 };
 const char* const kKernelNames[BLK_N_KERNELS] = {
     "rmsnorm_rows", "gemm_qkv", "splitk_reduce", "attn_prefill", "gemm_o",
-    "gemm_gateup", "gemm_down", "decode_persistent", "", "", "", "",
+    "gemm_gateup", "gemm_down", "decode_persistent", "attn_merge", "", "", "",
     "", "", "", ""};
 }  // namespace
 
@@ -88,7 +88,9 @@ struct PrefillWs {
   size_t xn16, q16, attn16, h32, hn16, act16, part32, total;
 };
 
-PrefillWs prefill_ws(const blk_config& c, int64_t T) {
+// part32 holds the attention's chunk partials first and the down
+// projection's split-K partials later (never live at the same time).
+PrefillWs prefill_ws(const blk_config& c, int64_t T, int num_sms) {
   const size_t H = c.hidden, D = c.head_dim, Hq = c.n_heads, Hkv = c.n_kv_heads,
                I = c.intermediate;
   (void)Hkv;
@@ -100,7 +102,9 @@ PrefillWs prefill_ws(const blk_config& c, int64_t T) {
   w.h32 = o; o = align_up(o + T * H * 4);
   w.hn16 = o; o = align_up(o + T * H * 2);
   w.act16 = o; o = align_up(o + T * I * 2);
-  w.part32 = o; o = align_up(o + (size_t)kMaxSplits * T * H * 4);
+  const size_t split_k = (size_t)kMaxSplits * T * H * 4;
+  const size_t attn = prefill_attn_part_bytes(T, (int)Hq, (int)D, num_sms);
+  w.part32 = o; o = align_up(o + (split_k > attn ? split_k : attn));
   w.total = o;
   return w;
 }
@@ -181,7 +185,7 @@ int run_prefill(blk_handle h, const blk_weights* w, const void* x,
   int rc = check_call(h, w, x, pos, T, L, k_cache, v_cache, out, k_new, v_new, ws);
   if (rc) return rc;
   const blk_config& c = h->cfg;
-  const PrefillWs lay = prefill_ws(c, T);
+  const PrefillWs lay = prefill_ws(c, T, h->num_sms);
   if (ws_bytes < lay.total) return BLK_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   unsigned char* base = static_cast<unsigned char*>(ws);
@@ -243,7 +247,11 @@ int run_prefill(blk_handle h, const blk_weights* w, const void* x,
   pa.T = M; pa.Hq = Hq; pa.Hkv = Hkv; pa.D = D;
   pa.scale_log2 = (float)(1.4426950408889634 / sqrt((double)D));
   pa.attn16 = attn16;
+  pa.max_chunks = prefill_attn_max_chunks(T, Hq, h->num_sms);
+  pa.part = reinterpret_cast<float*>(base + lay.part32);
+  plan_prefill_attn(pa, h->num_sms);
   BLK_LAUNCH(tm, kKAttnPrefill, launch_prefill_attn(pa, s, true));
+  if (pa.grid_chunks > 1) BLK_LAUNCH(tm, kKAttnMerge, launch_attn_merge(pa, s, true));
 
   // o_proj + residual -> h (fp32)
   TcGemmParams go = {};
@@ -368,7 +376,7 @@ int blk_set_flags(blk_handle h, uint32_t flags) {
 size_t blk_workspace_bytes(blk_handle h, int64_t max_T) {
   if (!h || max_T < 1) return 0;
   const blk_config& c = h->cfg;
-  const size_t a = prefill_ws(c, max_T).total;
+  const size_t a = prefill_ws(c, max_T, h->num_sms).total;
   const size_t b = decode_ws_bytes(c.hidden, c.n_heads, c.n_kv_heads, c.head_dim,
                                    c.intermediate, h->num_sms);
   return a > b ? a : b;

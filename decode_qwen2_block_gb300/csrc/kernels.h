@@ -23,10 +23,22 @@ struct PrefillAttnParams {
   int T, Hq, Hkv, D;
   float scale_log2;   // log2(e) / sqrt(D)
   __half* attn16;  // [T, Hq * D]
+  // Split of each 128-row block's tiles into chunks of chunk_tiles (one CTA
+  // each; grid (Hq, nqb, grid_chunks)), set by plan_prefill_attn.  Blocks with
+  // more than one chunk leave partials in `part` ([Hq][nqb][max_chunks] slots,
+  // prefill_attn_part_bytes) for launch_attn_merge.
+  int nqb, chunk_tiles, grid_chunks, max_chunks;
+  float* part;
   int* err;
 };
+int prefill_attn_max_chunks(int64_t T, int Hq, int num_sms);
+size_t prefill_attn_part_bytes(int64_t T, int Hq, int D, int num_sms);
+void plan_prefill_attn(PrefillAttnParams& p, int num_sms);
 cudaError_t launch_prefill_attn(const PrefillAttnParams& p, cudaStream_t s,
                                 bool pdl);
+// Combines the partials of split blocks into attn16 (no launch when
+// grid_chunks == 1).
+cudaError_t launch_attn_merge(const PrefillAttnParams& p, cudaStream_t s, bool pdl);
 cudaError_t configure_prefill_attn();
 
 // Sets the per-kernel shared-memory limits (called once per device).

@@ -146,3 +146,20 @@ def test_gqa4096_layer_prefill_then_decode():
     _step(db, s, w, "prefill", x[:100], 0, kc_o, vc_o, kc, vc, rows=[0, 37, 99])
     for t in range(100, 103):
         _step(db, s, w, "decode", x[t:t + 1], t, kc_o, vc_o, kc, vc)
+
+
+def test_prefill_kv_long_history_split_over_ctas_repeatable():
+    """1.5B-shaped layer, 128 new rows on 8064 history slots: the 64 K/V tiles
+    of the row block are split over 11 CTAs whose partials are merged; a
+    second identical call returns the same bits (the merge counters are left
+    at zero)."""
+    s, L, T = synth.QWEN2_1P5B, 8064, 128
+    w = synth.block_weights(s, seed=3)
+    x = synth.hidden_input(s, T, seed=3)
+    kc_o, vc_o = synth.kv_history(s, L + T, L, seed=3)
+    kc, vc = to_dev(kc_o), to_dev(vc_o)
+    db = DevBlock(s, w, L + T, T)
+    rows = [0, 1, 64, 126, 127]
+    _, out1 = _step(db, s, w, "prefill_kv", x, L, kc_o, vc_o, kc, vc, rows=rows)
+    _, out2 = _step(db, s, w, "prefill_kv", x, L, kc_o, vc_o, kc, vc, rows=rows)
+    assert torch.equal(out1, out2)
