@@ -576,8 +576,9 @@ size_t prefill_attn_part_bytes(int64_t T, int Hq, int D, int num_sms) {
 }
 
 // Chooses the chunk length C (tiles per CTA): the estimated time is the
-// number of CTA waves times C, plus one and a half tiles for publishing and
-// merging partials when blocks are split; ties go to the longer chunk.
+// number of CTA waves times C, plus four tiles for publishing the partials
+// and the merge kernel when blocks are split (measured: at T = 1024 splitting
+// the 8-tile blocks in two gains nothing); ties go to the longer chunk.
 void plan_prefill_attn(PrefillAttnParams& p, int num_sms) {
   const int64_t L = p.cache_len;
   p.nqb = (p.T + kRows - 1) / kRows;
@@ -595,7 +596,7 @@ void plan_prefill_attn(PrefillAttnParams& p, int num_sms) {
     for (int qb = 0; qb < p.nqb; ++qb) items += (tiles(qb) + C - 1) / C;
     items *= p.Hq;
     const int64_t waves = (items + num_sms - 1) / num_sms;
-    const double cost = (double)waves * C + (C < nmax ? 1.5 : 0.0);
+    const double cost = (double)waves * C + (C < nmax ? 4.0 : 0.0);
     if (cost < best) {
       best = cost;
       best_c = C;

@@ -170,6 +170,46 @@ __device__ __forceinline__ void store_h32(__half* dst, const float* v) {
   }
 }
 
+// Writes this warp's 32 rows x 32 columns (lane = row, v = its 32 values)
+// as full-row pieces: the values go through `st` (this warp's staging area in
+// shared memory, 32 * (row bytes + 16) bytes) and each store instruction then
+// covers whole 64- or 128-byte row pieces instead of one 16-byte piece of 32
+// different rows.  gdst: row 0's destination (16-byte aligned), ld: row
+// pitch in bytes; rows >= nrows are not written.
+template <bool F16>
+__device__ __forceinline__ void store_rows_staged(uint8_t* st, const float* v, int lane,
+                                                  uint8_t* gdst, size_t ld, int nrows) {
+  constexpr int kRowB = F16 ? 64 : 128;
+  constexpr int kStride = kRowB + 16;
+  uint4* s4 = reinterpret_cast<uint4*>(st + lane * kStride);
+  if constexpr (F16) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint4 u;
+      __half2* h = reinterpret_cast<__half2*>(&u);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) h[i] = __floats2half2_rn(v[8 * k + 2 * i], v[8 * k + 2 * i + 1]);
+      s4[k] = u;
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      s4[k] = make_uint4(__float_as_uint(v[4 * k]), __float_as_uint(v[4 * k + 1]),
+                         __float_as_uint(v[4 * k + 2]), __float_as_uint(v[4 * k + 3]));
+  }
+  __syncwarp();
+  constexpr int kLpr = kRowB / 16;   // lanes per row piece
+  constexpr int kRpi = 32 / kLpr;    // rows per store instruction
+  const int rr = lane / kLpr, cc = lane % kLpr;
+#pragma unroll
+  for (int i = 0; i < 32 / kRpi; ++i) {
+    const int row = i * kRpi + rr;
+    const uint4 val = *reinterpret_cast<const uint4*>(st + row * kStride + cc * 16);
+    if (row < nrows) *reinterpret_cast<uint4*>(gdst + row * ld + cc * 16) = val;
+  }
+  __syncwarp();   // the staging area is reused by the warp's next call
+}
+
 template <int BN>
 struct Cfg {
   static constexpr int kBHalf = BN / 2;                  // weight rows per CTA of the pair
@@ -348,6 +388,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool row_ok = m < p.M;
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
       float v0[32], v1[32];
+      // On the CTA's last tile every stage has been consumed once the
+      // accumulator is full, so the stages serve as store staging areas.
+      const bool staged = u + ncl >= units;
+      uint8_t* stg = smem + (warp - 2) * (32 * 144);
+      const int row0 = mt * BM + q * 32;              // this warp's first row
+      const int nrows = min(32, p.M - row0);
 
       if constexpr (EPI == kTcQKV) {
         const int D = p.D, half = D / 2;
@@ -365,6 +411,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           else if (hd < p.Hq + p.Hkv) { bias = p.bias[1]; local = hd - p.Hq; }
           else { bias = p.bias[2]; local = hd - p.Hq - p.Hkv; }
           const bool rope = hd < p.Hq + p.Hkv;
+          // bias of columns c0 + lane and half + c0 + lane (shared by all rows;
+          // broadcast with shuffles), loaded before the accumulator
+          const float b0 = bias ? __half2float(bias[local * D + c0 + lane]) : 0.f;
+          const float b1 = bias ? __half2float(bias[local * D + half + c0 + lane]) : 0.f;
           // this row's 32 rotation factors, loaded before the accumulator
           float4 cs4[16];
           if (rope && row_ok && pos >= 0 && pos < p.rope_len) {
@@ -386,14 +436,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tmem_ld32(tbase + hh * D + c0, v0);
           tmem_ld32(tbase + hh * D + half + c0, v1);
-          if (!row_ok) continue;
-          if (bias) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              v0[i] += __half2float(bias[local * D + c0 + i]);
-              v1[i] += __half2float(bias[local * D + half + c0 + i]);
-            }
+          for (int i = 0; i < 32; ++i) {
+            v0[i] += __shfl_sync(0xffffffffu, b0, i);
+            v1[i] += __shfl_sync(0xffffffffu, b1, i);
           }
+          if (!row_ok && !staged) continue;
           if (rope) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
@@ -404,7 +452,29 @@ __global__ void __launch_bounds__(kThreads, 1)
               v1[i] = b * cx + a * sy;
             }
           }
-          if (hd < p.Hq) {
+          if (staged) {
+            uint8_t* g;
+            size_t ld;
+            __half* nw = nullptr;
+            if (hd < p.Hq) {
+              g = reinterpret_cast<uint8_t*>(p.q16 + ((size_t)row0 * p.Hq + hd) * D);
+              ld = (size_t)p.Hq * D * 2;
+            } else {
+              const bool is_k = hd < p.Hq + p.Hkv;
+              nw = is_k ? p.k_new : p.v_new;
+              g = reinterpret_cast<uint8_t*>((is_k ? p.kc : p.vc) +
+                                             ((size_t)local * p.max_ctx + p.cache_len + row0) * D);
+              ld = (size_t)D * 2;
+            }
+            store_rows_staged<true>(stg, v0, lane, g + c0 * 2, ld, nrows);
+            store_rows_staged<true>(stg, v1, lane, g + (half + c0) * 2, ld, nrows);
+            if (nw) {
+              uint8_t* g2 = reinterpret_cast<uint8_t*>(nw + ((size_t)row0 * p.Hkv + local) * D);
+              const size_t ld2 = (size_t)p.Hkv * D * 2;
+              store_rows_staged<true>(stg, v0, lane, g2 + c0 * 2, ld2, nrows);
+              store_rows_staged<true>(stg, v1, lane, g2 + (half + c0) * 2, ld2, nrows);
+            }
+          } else if (hd < p.Hq) {
             __half* dst = p.q16 + ((size_t)m * p.Hq + hd) * D;
             store_h32(dst + c0, v0);
             store_h32(dst + half + c0, v1);
@@ -439,9 +509,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c0 = 32 * e; c0 < BN / 2; c0 += 64) {
           tmem_ld32(tbase + c0, v0);
           tmem_ld32(tbase + BN / 2 + c0, v1);
-          if (!row_ok) continue;
 #pragma unroll
           for (int i = 0; i < 32; ++i) v0[i] = silu(v0[i]) * v1[i];
+          if (staged && j0 + c0 + 32 <= p.N) {
+            store_rows_staged<true>(
+                stg, v0, lane, reinterpret_cast<uint8_t*>(p.out16 + (size_t)row0 * p.ldo + j0 + c0),
+                (size_t)p.ldo * 2, nrows);
+            continue;
+          }
+          if (!row_ok) continue;
           __half* dst = p.out16 + (size_t)m * p.ldo + j0 + c0;
           if (j0 + c0 + 32 <= p.N) {
             store_h32(dst, v0);
@@ -508,10 +584,23 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (c2 + c >= kCh) break;
               const int c0 = 32 * e + 64 * (c2 + c);
               tmem_ld32(tbase + c0, v0);
-              if (!row_ok || n0 + c0 >= p.N) continue;
+              if (n0 + c0 >= p.N) continue;
 #pragma unroll
               for (int i = 0; i < 32; ++i) v0[i] += rv[c][i];
-              store_out(c0, v0);
+              if (staged) {
+                if constexpr (EPI == kTcResidF32)
+                  store_rows_staged<false>(
+                      stg, v0, lane,
+                      reinterpret_cast<uint8_t*>(p.out32 + (size_t)row0 * p.ldo + n0 + c0),
+                      (size_t)p.ldo * 4, nrows);
+                else
+                  store_rows_staged<true>(
+                      stg, v0, lane,
+                      reinterpret_cast<uint8_t*>(p.out16 + (size_t)row0 * p.ldo + n0 + c0),
+                      (size_t)p.ldo * 2, nrows);
+              } else if (row_ok) {
+                store_out(c0, v0);
+              }
             }
           }
           if (!waited) break;
@@ -528,7 +617,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < kCh; ++c) {
             const int c0 = 32 * e + 64 * c;
             tmem_ld32(tbase + c0, v0);
-            if (!row_ok || n0 + c0 >= p.N) continue;
+            if (n0 + c0 >= p.N) continue;
+            if (staged) {
+              store_rows_staged<false>(
+                  stg, v0, lane, reinterpret_cast<uint8_t*>(part + (size_t)row0 * p.N + n0 + c0),
+                  (size_t)p.N * 4, nrows);
+              continue;
+            }
+            if (!row_ok) continue;
             float4* dst = reinterpret_cast<float4*>(part + (size_t)m * p.N + n0 + c0);
 #pragma unroll
             for (int j = 0; j < 8; ++j)

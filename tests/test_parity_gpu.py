@@ -76,6 +76,18 @@ def test_tiny_shape_edges(phase, L, T):
     _step(db, s, w, phase, x, L, kc_o, vc_o, kc, vc)
 
 
+def test_tiny_prefill_kv_long_history_split_over_ctas():
+    """head_dim 64: 8 new rows on 1000 history slots; the block's 8 K/V tiles
+    are split over several CTAs and merged (the D = 64 merge path)."""
+    s, C, L, T = synth.TINY, 1024, 1000, 8
+    w = synth.block_weights(s, seed=4)
+    x = synth.hidden_input(s, T, seed=4, stream_offset=L + 1)
+    kc_o, vc_o = synth.kv_history(s, C, L, seed=4, sentinel=SENTINEL)
+    kc, vc = to_dev(kc_o), to_dev(vc_o)
+    db = DevBlock(s, w, C, T)
+    _step(db, s, w, "prefill_kv", x, L, kc_o, vc_o, kc, vc)
+
+
 def test_decode_first_token_returns_v_through_wo():
     """At cache_len 0 the decode attention sees only its own key, so the
     attention output is v itself (self-only first token)."""
