@@ -5,18 +5,20 @@
 // CTA = (query head h, block of 128 new rows, chunk of that block's 128-slot
 // tiles), 6 warps:
 //   warp 0   TMA producer: the Q block once (3-D view of q [T, Hq, D]), then
-//            the chunk's K and V tiles of kv head h / (Hq/Hkv) into two
-//            stages.  The K/V tensor maps end at slot L + T, so slots past the
+//            the chunk's K and V tiles of kv head h / (Hq/Hkv) into three
+//            stages; a K stage frees when S_j is computed, a V stage when
+//            PV_j is.  The K/V tensor maps end at slot L + T, so slots past the
 //            last valid one arrive as zeros (stale cache contents never reach PV).
-//   warp 1   allocates TMEM (S: 128 columns, O: D columns) and its lane 0
-//            issues the MMAs (tcgen05.mma.cta_group::1.kind::f16, M = 128):
-//            S_j = Q K_j^T (N = 128, K = D), then O += P_j V_j (N = D,
-//            K = 128; V is the MN-major B operand).  S_{j+1} is issued as
+//   warp 1   allocates TMEM (S: 128 columns, O: D columns, two P buffers of 64)
+//            and its lane 0 issues the MMAs (tcgen05.mma.cta_group::1.kind::f16,
+//            M = 128): S_j = Q K_j^T (N = 128, K = D, both from shared
+//            memory), then O += P_j V_j (N = D, K = 128; P is the A operand
+//            read from TMEM, V the MN-major B operand).  S_{j+1} is issued as
 //            soon as the softmax has read S_j, so it overlaps that softmax.
 //   warps 2-5 softmax (thread = query row): read S_j from TMEM, causal mask on
 //            tiles that cross the diagonal, online softmax in base 2 with lazy
-//            rescaling of O in TMEM, P_j (fp16) into one of two shared-memory
-//            buffers in the MMA's K-major layout; at the end O / l -> attn.
+//            rescaling of O in TMEM, P_j (fp16 pairs) into TMEM buffer j % 2;
+//            at the end O / l -> attn.
 // A block whose tiles are split over several CTAs (chunks, so that the long
 // blocks of the causal triangle do not set the kernel's duration) publishes
 // per-chunk partials (O, m, l in fp32) that attn_merge_kernel, launched next,
@@ -33,7 +35,7 @@ namespace {
 
 constexpr int kRows = 128;        // query rows per CTA (MMA M)
 constexpr int kSlots = 128;       // cache slots per K/V tile (MMA N of S, K of PV)
-constexpr int kStages = 2;
+constexpr int kStages = 3;       // K/V stages
 constexpr int kThreads = 192;
 constexpr float kRescaleLog2 = 8.f;   // see the softmax: lazy rescaling threshold
 
@@ -89,6 +91,18 @@ __device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a, uint64_t b, uin
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(id), "r"(accumulate)
+      : "memory");
+}
+
+// Same with the A operand (M x 16, K-major: row i = TMEM lane i, element
+// pairs packed in 32-bit columns) read from TMEM at a_tmem.
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t id,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(id), "r"(accumulate)
       : "memory");
 }
 
@@ -153,13 +167,14 @@ struct Smem {
   static constexpr int kQBytes = kRows * D * 2;            // [D/64][128 rows][128 B]
   static constexpr int kKVTile = kSlots * D * 2;            // K or V: [D/64][128 slots][128 B]
   static constexpr int kStage = 2 * kKVTile;
-  static constexpr int kPBuf = kRows * kSlots * 2;          // [2][128 rows][128 B]
   static constexpr int kQOff = 0;
   static constexpr int kKVOff = kQBytes;
-  static constexpr int kPOff = kKVOff + kStages * kStage;   // two P buffers
-  static constexpr int kBarOff = kPOff + 2 * kPBuf;
+  static constexpr int kBarOff = kKVOff + kStages * kStage;
   static constexpr size_t kBytes = (size_t)kBarOff + 256 + 1024;
-  static constexpr uint32_t kTmemCols = 256;                 // S (128) + O (D), power of two
+  // TMEM columns: S (128 fp32), O (D fp32), two P buffers (128 fp16 packed in
+  // 64 columns each); allocated as a power of two.
+  static constexpr uint32_t kSCol = 0, kOCol = kSlots, kPCol = kSlots + 128;
+  static constexpr uint32_t kTmemCols = 512;
 };
 
 // Partial result of one chunk of a query block (fp32): per 32-row quarter q
@@ -205,19 +220,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem + Sm::kQOff;
   uint8_t* sKV = smem + Sm::kKVOff;
-  uint8_t* sP = smem + Sm::kPOff;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Sm::kBarOff);
   uint64_t* q_full = bars;
-  uint64_t* k_full = bars + 1;            // [2] K_j in stage j % 2
-  uint64_t* k_empty = bars + 3;           // [2] S_j complete: K stage free
-  uint64_t* v_full = bars + 5;            // [2]
-  uint64_t* v_empty = bars + 7;           // [2] PV_j complete: V stage free
-  uint64_t* s_full = bars + 9;            // S_j in TMEM
-  uint64_t* s_free = bars + 10;           // the softmax has read S_j
-  uint64_t* p_full = bars + 11;           // [2] P_j in buffer j % 2 (O rescaled)
-  uint64_t* o_done = bars + 13;           // [2] O += P_j V_j complete (j % 2)
-  uint64_t* drain = bars + 15;            // abort path
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  uint64_t* k_full = bars + 1;                  // [kStages] K_j in stage j % kStages
+  uint64_t* k_empty = k_full + kStages;         // [kStages] S_j complete: K stage free
+  uint64_t* v_full = k_empty + kStages;         // [kStages]
+  uint64_t* v_empty = v_full + kStages;         // [kStages] PV_j complete: V stage free
+  uint64_t* s_full = v_empty + kStages;         // S_j in TMEM
+  uint64_t* s_free = s_full + 1;                // the softmax has read S_j
+  uint64_t* p_full = s_free + 1;                // [2] P_j in TMEM buffer j % 2 (O rescaled)
+  uint64_t* o_done = p_full + 2;                // [2] O += P_j V_j complete (j % 2)
+  uint64_t* drain = o_done + 2;                 // abort path
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -230,8 +244,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&k_empty[s], 1);
       mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
-      mbar_init(&p_full[s], 4);
-      mbar_init(&o_done[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&p_full[b], 4);
+      mbar_init(&o_done[b], 1);
     }
     mbar_init(s_full, 1);
     mbar_init(s_free, 4);
@@ -251,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem, tO = tmem + kSlots;
+  const uint32_t tS = tmem + Sm::kSCol, tO = tmem + Sm::kOCol, tP = tmem + Sm::kPCol;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -332,12 +348,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&v_full[j % kStages], (j / kStages) & 1, p.err)) { ok = false; break; }
         tc_fence_after();
         const uint32_t vb = smem_u32(sKV + (size_t)(j % kStages) * Sm::kStage + Sm::kKVTile);
-        const uint32_t pb = smem_u32(sP + b * Sm::kPBuf);
 #pragma unroll
         for (int kk = 0; kk < kSlots / 16; ++kk) {   // O += P_j V_j over 16 slots at a time
-          const uint64_t a = desc_kmajor(pb + (kk >> 2) * (kRows * 128)) + ((kk & 3) * 32 >> 4);
           const uint64_t bd = desc_mnmajor(vb + kk * 16 * 128);
-          mma(tO, a, bd, id_o, (j | kk) != 0);
+          mma_ts(tO, tP + b * (kSlots / 2) + kk * 8, bd, id_o, (j | kk) != 0);
         }
         commit(&o_done[b]);
         commit(&v_empty[j % kStages]);
@@ -405,9 +419,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float nref = (mn == -INFINITY) ? 0.f : -mn;
       // P buffer j % 2 is free once PV_{j-2} is complete
       if (j >= 2 && !wait_all(&o_done[j & 1], ((j - 2) >> 1) & 1)) { ok = false; break; }
-      // P_j (fp16) into the K-major 128-byte-swizzled layout: [slot half][row][128 B]
-      uint8_t* prow = sP + (j & 1) * Sm::kPBuf + r * 128;
+      // P_j (fp16, slot pairs packed in 32-bit columns: row r = TMEM lane r, the
+      // MMA's A operand layout) into TMEM buffer j % 2
       float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+      uint32_t pk[kSlots / 2];
 #pragma unroll
       for (int c = 0; c < kSlots / 8; ++c) {
         float e[8];
@@ -417,12 +432,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         s1 += e[1] + e[5];
         s2 += e[2] + e[6];
         s3 += e[3] + e[7];
-        uint4 u;
-        __half2* hp = reinterpret_cast<__half2*>(&u);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) hp[k] = __floats2half2_rn(e[2 * k], e[2 * k + 1]);
-        *reinterpret_cast<uint4*>(prow + (c >> 3) * (kRows * 128) + (((c & 7) ^ (r & 7)) << 4)) = u;
+        for (int k = 0; k < 4; ++k) {
+          const __half2 h2 = __floats2half2_rn(e[2 * k], e[2 * k + 1]);
+          pk[4 * c + k] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
       }
+      const uint32_t tPj = tP + (j & 1) * (kSlots / 2) + lane_off;
+      tmem_st32(tPj, reinterpret_cast<const float*>(pk));
+      tmem_st32(tPj + 32, reinterpret_cast<const float*>(pk + 32));
       l = l * alpha + ((s0 + s1) + (s2 + s3));
       m = mn;
       if (move && j > 0) {
@@ -440,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_wait_st();
       }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // for the tensor core
+      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[j & 1]);
