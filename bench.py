@@ -50,7 +50,7 @@ NCU_TRAFFIC = {
     "gemm_down": 45.937152e6 + 1.509376e6,
     "gemm_qkv": 10.00576e6 + 0.000768e6,
     "gemm_o": 11.030016e6 + 0.000256e6,
-    "attn_prefill": 4.244224e6,
+    "attn_prefill": 4.242944e6,
     # both launches of one 28-layer step (16 + 12 layers)
     ("decode_persistent", 4096): (1.577014e9 + 1.183408e9) + (24.87936e6 + 19.178752e6),
 }
