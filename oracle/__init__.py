@@ -71,6 +71,10 @@ def _load():
             lib.orc_block_forward.argtypes = [ctypes.POINTER(OrcConfig), ctypes.POINTER(OrcWeights),
                                               vp, vp, i64, i64, vp, vp, vp, vp, vp, i64, vp]
             lib.orc_block_forward.restype = ctypes.c_int
+            lib.orc_embed.argtypes = [vp, i64, i64, vp, i64, vp]
+            lib.orc_embed.restype = ctypes.c_int
+            lib.orc_lm_head.argtypes = [vp, i64, i64, vp, dbl, vp, i64, vp, vp]
+            lib.orc_lm_head.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -182,3 +186,31 @@ def block_forward(shape, weights: dict, x, pos, L: int, k_cache, v_cache, max_ct
     if rc != 0:
         raise ValueError(f"oracle rejected the arguments (rc={rc})")
     return out.view(np.float16), k_new.view(np.float16), v_new.view(np.float16)
+
+
+# ---- around the block stack ---------------------------------------------------
+
+def embed(E, ids) -> np.ndarray:
+    """x[t] = E[ids[t]] (fp16 rows)."""
+    E = _u16(E)
+    ids = np.ascontiguousarray(ids, dtype=np.int64)
+    V, H = E.shape
+    x = np.empty((ids.size, H), dtype=np.uint16)
+    if _load().orc_embed(E.ctypes.data, V, H, ids.ctypes.data, ids.size, x.ctypes.data) != 0:
+        raise ValueError("token id outside the vocabulary")
+    return x.view(np.float16)
+
+
+def lm_head(x, g, W, eps: float = 1e-6, want_logits: bool = True):
+    """Final RMSNorm, LM head and greedy token of each row of x (fp16 [T, H]).
+    Returns (logits f64 [T, vocab] or None, token int64 [T])."""
+    x, g, W = _u16(x), _u16(g), _u16(W)
+    T, H = x.shape
+    V = W.shape[0]
+    logits = np.empty((T, V), dtype=np.float64) if want_logits else None
+    token = np.empty(T, dtype=np.int64)
+    rc = _load().orc_lm_head(x.ctypes.data, T, H, g.ctypes.data, float(eps), W.ctypes.data, V,
+                             None if logits is None else logits.ctypes.data, token.ctypes.data)
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return logits, token

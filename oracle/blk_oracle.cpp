@@ -200,4 +200,34 @@ int orc_block_forward(const orc_config* cfg, const orc_weights* w,
   return 0;
 }
 
+int orc_embed(const uint16_t* E, int64_t vocab, int64_t H, const int64_t* ids,
+              int64_t T, uint16_t* x) {
+  if (T < 0 || H <= 0 || vocab <= 0) return -1;
+  for (int64_t t = 0; t < T; ++t)
+    if (ids[t] < 0 || ids[t] >= vocab) return -1;
+  for (int64_t t = 0; t < T; ++t)
+    for (int64_t i = 0; i < H; ++i) x[t * H + i] = E[ids[t] * H + i];
+  return 0;
+}
+
+int orc_lm_head(const uint16_t* x, int64_t T, int64_t H, const uint16_t* g,
+                double eps, const uint16_t* W, int64_t vocab, double* logits,
+                int64_t* token) {
+  if (T <= 0 || H <= 0 || vocab <= 0) return -1;
+  std::vector<double> row(H), gain(H), y(H), z(vocab);
+  for (int64_t i = 0; i < H; ++i) gain[i] = h2d(g[i]);
+  for (int64_t t = 0; t < T; ++t) {
+    for (int64_t i = 0; i < H; ++i) row[i] = h2d(x[t * H + i]);
+    orc_rmsnorm(row.data(), gain.data(), H, eps, y.data());
+    orc_linear(W, nullptr, y.data(), vocab, H, z.data());
+    int64_t best = 0;
+    for (int64_t v = 1; v < vocab; ++v)
+      if (z[v] > z[best]) best = v;   // strictly larger: ties keep the lower index
+    token[t] = best;
+    if (logits)
+      for (int64_t v = 0; v < vocab; ++v) logits[t * vocab + v] = z[v];
+  }
+  return 0;
+}
+
 }  // extern "C"

@@ -100,6 +100,31 @@ int orc_block_forward(const orc_config* cfg, const orc_weights* w,
                       uint16_t* k_new, uint16_t* v_new, const int64_t* rows,
                       int64_t n_rows, uint16_t* out);
 
+/* ---- around the block stack (embedding in, logits and token out) ----------
+ * Inference flow of the MLIR-compilation page (§2.3 "LLM inference
+ * overview"): input tokens -> word embedding -> the stack of blocks -> LM
+ * head -> logits -> a sampling step picks the next token.  The buddy-mlir
+ * DeepSeek-R1 page (§6.4.4 and §6.4.6) samples greedily: the index of the
+ * largest logit of the last valid position, vocabulary 151936.
+ * Readings: the LM head is preceded by a final RMSNorm with gain g (the
+ * Qwen2 convention; the pages do not print it), no bias; logits in f64 here;
+ * ties go to the lowest index.  */
+
+/* x[t, :] = E[ids[t], :] for t < T, fp16 bits copied.  E fp16 [vocab, H].
+ * Returns -1 (and writes nothing) if an id is outside [0, vocab).
+ * Pinned against array indexing of the same table. */
+int orc_embed(const uint16_t* E, int64_t vocab, int64_t H, const int64_t* ids,
+              int64_t T, uint16_t* x);
+
+/* For each row t < T of x (fp16 [T, H]): y = RMSNorm(x[t]) * g (eps),
+ * logits[t][v] = sum_i W[v][i] * y[i] for v < vocab (W fp16 [vocab, H]),
+ * token[t] = the lowest v with the largest logit.  logits may be NULL.
+ * Pinned: rows of W that are multiples of one vector (closed form), row
+ * permutations, RMSNorm scale invariance, equal rows (lowest index). */
+int orc_lm_head(const uint16_t* x, int64_t T, int64_t H, const uint16_t* g,
+                double eps, const uint16_t* W, int64_t vocab, double* logits,
+                int64_t* token);
+
 #ifdef __cplusplus
 }
 #endif

@@ -39,6 +39,12 @@ MUTATIONS = [
     ("softmax max not subtracted consistently", "s[j] = std::exp(s[j] - m);", "s[j] = std::exp(s[j] - 0.5 * m);"),
     ("v stored rotated", "const uint16_t vh = encode_half(v[g * D + d]);",
      "const uint16_t vh = encode_half(k[g * D + d]);"),
+    ("argmax ties to the higher index", "if (z[v] > z[best]) best = v;",
+     "if (z[v] >= z[best]) best = v;"),
+    ("dropped final norm gain", "orc_rmsnorm(row.data(), gain.data(), H, eps, y.data());",
+     "orc_rmsnorm(row.data(), nullptr, H, eps, y.data());"),
+    ("embedding row from the position", "x[t * H + i] = E[ids[t] * H + i];",
+     "x[t * H + i] = E[t * H + i];"),
 ]
 
 PIN_TESTS = [getattr(pins, n) for n in dir(pins) if n.startswith("test_")]

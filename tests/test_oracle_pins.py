@@ -378,3 +378,71 @@ def test_page_gqa_example_shape():
     s = synth.GQA_4096
     assert (s.n_layers, s.hidden, s.n_kv_heads, s.head_dim) == (
         c["num_layers"], c["hidden_size"], c["kv_head"], c["head_dim"])
+
+
+# ------------------------------------------------ embedding, LM head, argmax
+
+def test_embed_matches_array_indexing_and_rejects_bad_ids():
+    rng = np.random.default_rng(11)
+    E = rng.standard_normal((97, 24)).astype(np.float16)
+    ids = np.array([0, 96, 5, 5, 40], dtype=np.int64)
+    x = oracle.embed(E, ids)
+    assert np.array_equal(x.view(np.uint16), E[ids].view(np.uint16))
+    for bad in ([-1], [97], [3, 1 << 40]):
+        with pytest.raises(ValueError):
+            oracle.embed(E, bad)
+
+
+def test_lm_head_closed_form_for_rank_one_weights_and_constant_input():
+    # x = a (constant row): RMSNorm gives a / sqrt(a^2 + eps) * g; rows of W
+    # that are c_v * u give logits c_v * (a / sqrt(a^2 + eps)) * sum(u * g).
+    H, V, a, eps = 64, 33, 0.75, 1e-6
+    rng = np.random.default_rng(12)
+    u = rng.integers(-3, 4, size=H).astype(np.float16)
+    g = (1 + rng.integers(-2, 3, size=H) / 8).astype(np.float16)
+    c = rng.integers(-5, 6, size=V).astype(np.float64)
+    W = (c[:, None] * u[None, :].astype(np.float64)).astype(np.float16)
+    x = np.full((1, H), a, dtype=np.float16)
+    logits, token = oracle.lm_head(x, g, W, eps=eps)
+    dot = float(np.sum(u.astype(np.float64) * g.astype(np.float64)))
+    want = c * (a / math.sqrt(a * a + eps)) * dot
+    assert np.allclose(logits[0], want, rtol=1e-12, atol=1e-12)
+    assert token[0] == int(np.flatnonzero(want == want.max())[0])
+
+
+def test_lm_head_row_permutation_permutes_logits():
+    rng = np.random.default_rng(13)
+    H, V = 48, 71
+    W = (rng.standard_normal((V, H)) * 0.1).astype(np.float16)
+    g = np.ones(H, np.float16)
+    x = rng.standard_normal((3, H)).astype(np.float16)
+    perm = rng.permutation(V)
+    l1, t1 = oracle.lm_head(x, g, W)
+    l2, t2 = oracle.lm_head(x, g, W[perm])
+    assert np.array_equal(l2, l1[:, perm])
+    assert np.array_equal(perm[t2], t1)
+
+
+def test_lm_head_rmsnorm_scale_invariance_with_zero_eps():
+    rng = np.random.default_rng(14)
+    H, V = 40, 29
+    W = (rng.standard_normal((V, H)) * 0.1).astype(np.float16)
+    g = (1 + rng.standard_normal(H) * 0.1).astype(np.float16)
+    x = rng.standard_normal((2, H)).astype(np.float16)
+    l1, _ = oracle.lm_head(x, g, W, eps=0.0)
+    l2, _ = oracle.lm_head((x.astype(np.float64) * 4).astype(np.float16), g, W, eps=0.0)
+    assert np.allclose(l1, l2, rtol=1e-13, atol=1e-13)
+
+
+def test_lm_head_ties_go_to_the_lowest_index():
+    rng = np.random.default_rng(15)
+    H, V = 32, 50
+    x = rng.standard_normal((1, H)).astype(np.float16)
+    g = np.ones(H, np.float16)
+    W = np.zeros((V, H), np.float16)
+    best = np.sign(x[0]).astype(np.float16)          # the row with the largest dot product
+    for v in (17, 3, 41):                            # three equal maxima
+        W[v] = best
+    W[8] = (best.astype(np.float64) * 0.5).astype(np.float16)
+    _, token = oracle.lm_head(x, g, W)
+    assert token[0] == 3
