@@ -28,13 +28,14 @@ BLK_ERR_DEVICE_TIMEOUT = -7
 BLK_ERR_POSITION = -8
 BLK_ERR_DEVICE = -9
 BLK_ERR_SCRATCH_LIMIT = -10
+BLK_ERR_TOKEN = -11
 BLK_STATIC_SCRATCH_BYTES = 1 << 20
 BLK_FLAG_CHAIN = 1
 
 EXPORTED = ("blk_create", "blk_destroy", "blk_set_flags", "blk_workspace_bytes", "blk_prefill",
             "blk_prefill_kv", "blk_decode", "blk_check", "blk_status_str", "blk_timing",
             "blk_timing_collect", "blk_timing_read", "blk_decode_static", "blk_decode_stack",
-            "blk_set_trace")
+            "blk_set_trace", "blk_embed", "blk_lm_head_workspace_bytes", "blk_lm_head")
 BLK_N_KERNELS = 16
 
 WEIGHT_FIELDS = ("ln1_g", "wq", "wk", "wv", "bq", "bk", "bv", "wo", "ln2_g", "w_gate", "w_up",
@@ -111,6 +112,12 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.blk_timing_read.argtypes = [vp, i32, ctypes.POINTER(ctypes.c_double),
                                     ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_char_p)]
     lib.blk_timing_read.restype = i32
+    lib.blk_embed.argtypes = [vp, vp, i64, vp, i64, vp, vp]
+    lib.blk_embed.restype = i32
+    lib.blk_lm_head_workspace_bytes.argtypes = [vp]
+    lib.blk_lm_head_workspace_bytes.restype = ctypes.c_size_t
+    lib.blk_lm_head.argtypes = [vp, vp, i64, vp, vp, i64, vp, vp, vp, ctypes.c_size_t, vp]
+    lib.blk_lm_head.restype = i32
     _lib = lib
     return lib
 
@@ -176,6 +183,19 @@ def blk_decode_static(handle, w: BlkWeights, x, pos, cache_len, k_cache, v_cache
     (for callers that cannot allocate device memory; see include/blk.h)."""
     return load().blk_decode_static(handle, ctypes.byref(w), x, pos, cache_len, k_cache, v_cache,
                                     out, k_new, v_new, stream)
+
+
+def blk_embed(handle, table, vocab, ids, T, x, stream) -> int:
+    return load().blk_embed(handle, table, vocab, ids, T, x, stream)
+
+
+def blk_lm_head_workspace_bytes(handle) -> int:
+    return load().blk_lm_head_workspace_bytes(handle)
+
+
+def blk_lm_head(handle, x, T, norm_g, w_lm, vocab, logits, tokens, ws, ws_bytes, stream) -> int:
+    return load().blk_lm_head(handle, x, T, norm_g, w_lm, vocab, logits, tokens, ws, ws_bytes,
+                              stream)
 
 
 def blk_check(handle, stream) -> int:
@@ -274,6 +294,24 @@ class Block:
                         ws.numel() * ws.element_size(), self._stream(stream))
         if rc != BLK_OK:
             raise BlkError(rc, "blk_decode")
+
+    def embed(self, table, ids, x, stream=None):
+        """x[t] = table[ids[t]] (fp16 [vocab, hidden] table, int64 ids)."""
+        rc = blk_embed(self.handle, _ptr(table), table.shape[0], _ptr(ids), ids.numel(), _ptr(x),
+                       self._stream(stream))
+        if rc != BLK_OK:
+            raise BlkError(rc, "blk_embed")
+
+    def lm_head_workspace_bytes(self) -> int:
+        return blk_lm_head_workspace_bytes(self.handle)
+
+    def lm_head(self, x, norm_g, w_lm, tokens, ws, logits=None, stream=None):
+        """Final RMSNorm + LM head + greedy argmax of the rows of x (fp16 [T, hidden])."""
+        rc = blk_lm_head(self.handle, _ptr(x), x.shape[0], _ptr(norm_g), _ptr(w_lm),
+                         w_lm.shape[0], _ptr(logits), _ptr(tokens), _ptr(ws),
+                         ws.numel() * ws.element_size(), self._stream(stream))
+        if rc != BLK_OK:
+            raise BlkError(rc, "blk_lm_head")
 
     def timing(self, on: bool):
         rc = blk_timing(self.handle, on)

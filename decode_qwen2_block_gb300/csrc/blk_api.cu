@@ -21,11 +21,12 @@ constexpr int kMaxPending = 1024;
 // Kernel ids for per-kernel timing (blk_timing_read).
 enum KernelId {
   kKRmsNorm = 0, kKGemmQKV, kKSplitReduce, kKAttnPrefill, kKGemmO, kKGemmGateUp,
-  kKGemmDown, kKDecodeStep, kKAttnMerge, kKCount
+  kKGemmDown, kKDecodeStep, kKAttnMerge, kKLmHead, kKArgmax, kKEmbed, kKCount
 };
 const char* const kKernelNames[BLK_N_KERNELS] = {
     "rmsnorm_rows", "gemm_qkv", "splitk_reduce", "attn_prefill", "gemm_o",
-    "gemm_gateup", "gemm_down", "decode_persistent", "attn_merge", "", "", "",
+    "gemm_gateup", "gemm_down", "decode_persistent", "attn_merge", "lm_head", "argmax_reduce",
+    "embed",
     "", "", "", ""};
 }  // namespace
 
@@ -504,6 +505,65 @@ int blk_check(blk_handle h, void* stream) {
   if (v != 0 && cudaMemset(h->status, 0, sizeof v) != cudaSuccess) return BLK_ERR_CUDA;
   if (v == kDevTimeout) return BLK_ERR_DEVICE_TIMEOUT;
   if (v == kDevPosition) return BLK_ERR_POSITION;
+  if (v == kDevToken) return BLK_ERR_TOKEN;
+  return BLK_OK;
+}
+
+int blk_embed(blk_handle h, const void* table, int64_t vocab, const int64_t* ids, int64_t T,
+              void* x, void* stream) {
+  if (!h) return BLK_ERR_NULL;
+  if (!table || !ids || !x) return BLK_ERR_NULL;
+  if (!aligned(table, 16) || !aligned(x, 16) || !aligned(ids, 8)) return BLK_ERR_ALIGN;
+  if (T <= 0 || T > (1 << 20) || vocab <= 0) return BLK_ERR_SHAPE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Timer tm{h, s};
+  BLK_LAUNCH(tm, kKEmbed,
+             launch_embed(static_cast<const __half*>(table), vocab, ids, (int)T, h->cfg.hidden,
+                          static_cast<__half*>(x), h->status, s,
+                          (h->flags & BLK_FLAG_CHAIN) != 0));
+  return BLK_OK;
+}
+
+size_t blk_lm_head_workspace_bytes(blk_handle h) {
+  if (!h) return 0;
+  return lm_head_workspace_bytes(h->num_sms);
+}
+
+int blk_lm_head(blk_handle h, const void* x, int64_t T, const void* norm_g, const void* w_lm,
+                int64_t vocab, float* logits, int64_t* tokens, void* ws, size_t ws_bytes,
+                void* stream) {
+  if (!h) return BLK_ERR_NULL;
+  if (!x || !norm_g || !w_lm || !tokens || !ws) return BLK_ERR_NULL;
+  if (!aligned(x, 16) || !aligned(w_lm, 16) || !aligned(norm_g, 2) || !aligned(tokens, 8) ||
+      !aligned(ws, 16) || (logits && !aligned(logits, 4)))
+    return BLK_ERR_ALIGN;
+  const int H = h->cfg.hidden;
+  if (T < 1 || T > 8 || vocab < 1 || vocab > ((int64_t)1 << 31) - 16 || H > 4096)
+    return BLK_ERR_SHAPE;
+  if (ws_bytes < lm_head_workspace_bytes(h->num_sms)) return BLK_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  LmHeadParams p = {};
+  {
+    const int64_t dims[3] = {64, vocab, H / 64}, strides[2] = {(int64_t)H * 2, 128};
+    // always 24 column blocks (48 KB per copy; blocks past H arrive as zeros)
+    const int box[3] = {64, 16, 24};
+    if (make_tmap_3d(&p.tm_w, w_lm, dims, strides, box)) return BLK_ERR_CUDA;
+  }
+  p.x = static_cast<const __half*>(x);
+  p.g = static_cast<const __half*>(norm_g);
+  p.eps = h->cfg.rms_eps;
+  p.T = (int)T;
+  p.H = H;
+  p.vocab = vocab;
+  p.logits = logits;
+  p.part_v = static_cast<float*>(ws);
+  p.part_i = reinterpret_cast<int*>(static_cast<unsigned char*>(ws) +
+                                    (size_t)h->num_sms * 8 * sizeof(float));
+  p.token = tokens;
+  p.err = h->status;
+  Timer tm{h, s};
+  BLK_LAUNCH(tm, kKLmHead, launch_lm_head(p, h->num_sms, s, (h->flags & BLK_FLAG_CHAIN) != 0));
+  BLK_LAUNCH(tm, kKArgmax, launch_argmax_reduce(p, s));
   return BLK_OK;
 }
 
@@ -576,6 +636,7 @@ const char* blk_status_str(int status) {
     case BLK_ERR_CUDA: return "a CUDA runtime call or kernel launch failed";
     case BLK_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait timed out";
     case BLK_ERR_POSITION: return "a position id was outside [0, max_ctx) and was clamped";
+    case BLK_ERR_TOKEN: return "a token id was outside [0, vocab) (embedding row zeroed)";
     case BLK_ERR_DEVICE: return "the current GPU is not sm_103 (GB300)";
     case BLK_ERR_SCRATCH_LIMIT:
       return "the shape needs more decode scratch than blk_decode_static's fixed 1 MiB array";
@@ -590,6 +651,7 @@ cudaError_t configure_kernels() {
   cudaError_t e = configure_decode_persistent();
   if (e == cudaSuccess) e = configure_tc_gemm_kernels();
   if (e == cudaSuccess) e = configure_prefill_attn();
+  if (e == cudaSuccess) e = configure_lm_head();
   return e;
 }
 }  // namespace blk

@@ -11,6 +11,7 @@ namespace blk {
 // Device status codes written to the handle's status word (first one wins).
 constexpr int kDevTimeout = 1;
 constexpr int kDevPosition = 2;
+constexpr int kDevToken = 3;     // a token id outside [0, vocab)
 
 // A bounded wait gives up after this many nanoseconds of %globaltimer.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;

@@ -41,6 +41,28 @@ cudaError_t launch_prefill_attn(const PrefillAttnParams& p, cudaStream_t s,
 cudaError_t launch_attn_merge(const PrefillAttnParams& p, cudaStream_t s, bool pdl);
 cudaError_t configure_prefill_attn();
 
+// Final RMSNorm + LM head + greedy argmax (lm_head.cu).
+struct LmHeadParams {
+  CUtensorMap tm_w;     // W [vocab, H] viewed as (64, vocab, H / 64), box (64, 16, 24), SW128
+  const __half* x;      // [T, H] last hidden rows (16-byte aligned)
+  const __half* g;      // [H] final RMSNorm gain
+  float eps;
+  int T, H;             // 1 <= T <= 8, H % 64 == 0, H <= 4096
+  int64_t vocab;
+  float* logits;        // [T, vocab] fp32, may be null
+  float* part_v;        // [num_sms][8] per-CTA best logit (workspace)
+  int* part_i;          // [num_sms][8] its index
+  int nparts;           // set by launch_lm_head
+  int64_t* token;       // [T]
+  int* err;
+};
+size_t lm_head_workspace_bytes(int num_sms);
+cudaError_t launch_lm_head(LmHeadParams& p, int num_sms, cudaStream_t s, bool pdl);
+cudaError_t launch_argmax_reduce(const LmHeadParams& p, cudaStream_t s);
+cudaError_t launch_embed(const __half* table, int64_t vocab, const int64_t* ids, int T, int H,
+                         __half* x, int* err, cudaStream_t s, bool pdl);
+cudaError_t configure_lm_head();
+
 // Sets the per-kernel shared-memory limits (called once per device).
 cudaError_t configure_kernels();
 

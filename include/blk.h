@@ -62,6 +62,7 @@ extern "C" {
 #define BLK_ERR_DEVICE (-9)          /* the current GPU is not sm_103 (GB300)   */
 #define BLK_ERR_SCRATCH_LIMIT (-10)  /* shape needs more scratch than
                                         blk_decode_static's fixed array holds   */
+#define BLK_ERR_TOKEN (-11)          /* a token id outside [0, vocab)           */
 
 /* Block shape.  Supported: head_dim 64 or 128; n_heads % n_kv_heads == 0 with
  * group size n_heads / n_kv_heads in {1, 2, 4, 6, 8, 16}; hidden a multiple
@@ -202,8 +203,9 @@ int blk_decode_static(blk_handle h, const blk_weights* w, const void* x,
                       void* stream);
 
 /* Synchronizes `stream`, then reports and clears the handle's device status
- * word: BLK_OK, BLK_ERR_DEVICE_TIMEOUT or BLK_ERR_POSITION (a kernel clamped
- * an out-of-range position id), or BLK_ERR_CUDA if the stream failed. */
+ * word: BLK_OK, BLK_ERR_DEVICE_TIMEOUT, BLK_ERR_POSITION (a kernel clamped
+ * an out-of-range position id), BLK_ERR_TOKEN (blk_embed met an id outside
+ * the vocabulary), or BLK_ERR_CUDA if the stream failed. */
 int blk_check(blk_handle h, void* stream);
 
 /* Per-kernel timing, for benchmarks.  While on, every kernel a call enqueues
@@ -230,6 +232,40 @@ int blk_timing_read(blk_handle h, int kernel, double* total_ms,
  * layers of one launch (at most 32).  Entries past `bytes` are not written.
  * NULL turns tracing off (the default).  Returns BLK_OK or BLK_ERR_NULL. */
 int blk_set_trace(blk_handle h, void* device_buffer, size_t bytes);
+
+/* ---- around the block stack: embedding in, next token out ----------------
+ * The inference flow of the MLIR-compilation page (§2.3 "LLM inference
+ * overview"): input tokens -> word embedding -> the blocks -> LM head ->
+ * logits -> sampling; the buddy-mlir DeepSeek-R1 page (§6.4.4, §6.4.6) picks
+ * the next token greedily, the index of the largest logit of the last valid
+ * position (vocabulary 151936).
+ *
+ * blk_embed: x[t, :] = table[ids[t], :] for t < T (fp16 rows copied bit for
+ * bit).  table: device fp16 [vocab, hidden], 16-byte aligned; ids: device
+ * int64 [T]; x: device fp16 [T, hidden], 16-byte aligned.  An id outside
+ * [0, vocab) gives a zero row and BLK_ERR_TOKEN from the next blk_check.
+ * Returns BLK_OK, BLK_ERR_NULL, BLK_ERR_ALIGN, BLK_ERR_SHAPE (T <= 0,
+ * vocab <= 0) or BLK_ERR_CUDA.  Asynchronous on `stream`. */
+int blk_embed(blk_handle h, const void* table, int64_t vocab, const int64_t* ids, int64_t T,
+              void* x, void* stream);
+
+/* Bytes of workspace blk_lm_head needs (a few KB: per-SM argmax candidates). */
+size_t blk_lm_head_workspace_bytes(blk_handle h);
+
+/* Final RMSNorm, LM head and greedy argmax for T (1..8) hidden rows:
+ *   y[t] = RMSNorm(x[t]) * norm_g (eps of the handle's config, y rounded to
+ *          fp16), logits[t][v] = sum_i w_lm[v][i] * y[t][i] (fp32 accumulation),
+ *   tokens[t] = the lowest v with the largest logits[t][v].
+ * x: device fp16 [T, hidden] (16-byte aligned); norm_g: device fp16
+ * [hidden]; w_lm: device fp16 [vocab, hidden] row-major (16-byte aligned;
+ * hidden <= 4096); logits: device fp32 [T, vocab] or NULL; tokens: device
+ * int64 [T]; ws: device workspace of blk_lm_head_workspace_bytes() bytes.
+ * Returns BLK_OK, BLK_ERR_NULL, BLK_ERR_ALIGN, BLK_ERR_SHAPE (T outside
+ * [1, 8], vocab < 1 or >= 2^31 - 16, hidden > 4096), BLK_ERR_WORKSPACE or
+ * BLK_ERR_CUDA.  Asynchronous on `stream`; two kernel launches. */
+int blk_lm_head(blk_handle h, const void* x, int64_t T, const void* norm_g, const void* w_lm,
+                int64_t vocab, float* logits, int64_t* tokens, void* ws, size_t ws_bytes,
+                void* stream);
 
 /* Static description of a status code. */
 const char* blk_status_str(int status);

@@ -34,6 +34,7 @@ TENSOR_IDS = {
     "wq": 1, "wk": 2, "wv": 3, "bq": 4, "bk": 5, "bv": 6, "wo": 7,
     "w_gate": 8, "w_up": 9, "w_down": 10,
     "x": 20, "k_hist": 21, "v_hist": 22,
+    "embed": 30, "lm_head": 31, "norm_g": 32,
 }
 INPUT_LAYER = 4095
 
@@ -175,3 +176,25 @@ def kv_history(s: BlockShape, max_ctx: int, L: int, layer: int = 0, seed: int = 
 
 def positions(L: int, T: int) -> np.ndarray:
     return np.arange(L, L + T, dtype=np.int64)
+
+
+QWEN2_VOCAB = 151936   # vocabulary of the 1.5B model (buddy-mlir page, prefill/decode table)
+
+
+def head_weights(vocab: int, hidden: int, seed: int = 0, std: float = 0.02,
+                 gain_std: float = 0.0) -> dict:
+    """Embedding table and LM head ~ N(0, std) [vocab, hidden]; final RMSNorm
+    gain 1 (or ~ N(1, gain_std) when gain_std > 0)."""
+    w = {"embed": normal_f16(seed, stream_id(INPUT_LAYER - 1, "embed"), (vocab, hidden), std=std),
+         "lm_head": normal_f16(seed, stream_id(INPUT_LAYER - 1, "lm_head"), (vocab, hidden), std=std)}
+    if gain_std > 0:
+        w["norm_g"] = normal_f16(seed, stream_id(INPUT_LAYER - 1, "norm_g"), (hidden,), std=gain_std,
+                                 mean=1.0)
+    else:
+        w["norm_g"] = np.ones(hidden, dtype=np.float16)
+    return w
+
+
+def token_ids(vocab: int, T: int, seed: int = 0) -> np.ndarray:
+    """T token ids uniform in [0, vocab) (numpy's seeded generator)."""
+    return np.random.default_rng(seed).integers(0, vocab, size=T, dtype=np.int64)
