@@ -51,6 +51,7 @@ NCU_TRAFFIC = {
     "gemm_qkv": 10.00576e6 + 0.000768e6,
     "gemm_o": 11.030016e6 + 0.000256e6,
     "attn_prefill": 4.242944e6,
+    "lm_head": 466853632 + 206080,
     # both launches of one 28-layer step (16 + 12 layers)
     ("decode_persistent", 4096): (1.577014e9 + 1.183408e9) + (24.87936e6 + 19.178752e6),
 }
@@ -242,7 +243,9 @@ def bench_ours(args, ws, rank, local):
         clocks = ClockSampler(local)
         clocks.start()
         dec = bench_decode(args, s, dev, stream, peaks, ws)
-        return {"metric": "decode us/step (28 layers)", "decode": dec, "clocks": clocks.stop()}
+        head = bench_lm_head(args, s, dev, stream, peaks, ws)
+        return {"metric": "decode us/step (28 layers)", "decode": dec, "lm_head": head,
+                "clocks": clocks.stop()}
 
     # ---------------- prefill, one layer, [1, 1024] ----------------
     T = PREFILL_T
@@ -372,8 +375,64 @@ def bench_ours(args, ws, rank, local):
     # ---------------- decode, 28 layers ----------------
     if not args.no_decode and args.only != "prefill":
         result["decode"] = bench_decode(args, s, dev, stream, peaks, ws)
+        result["lm_head"] = bench_lm_head(args, s, dev, stream, peaks, ws)
     result["clocks"] = clocks.stop()
     return result
+
+
+def bench_lm_head(args, s, dev, stream, peaks, ws):
+    """Final RMSNorm + LM head + greedy argmax of one decode step (151936 x
+    1536 fp16 head, 467 MB: larger than L2, so no flush is needed), and the
+    embedding gather of the step's token."""
+    import torch
+    import synth
+    import decode_qwen2_block_gb300 as blk
+    K, W = max(args.steps, 10), args.warmup
+    V = synth.QWEN2_VOCAB
+    hw = synth.head_weights(V, s.hidden, seed=0)
+    head = torch.from_numpy(hw["lm_head"]).to(dev)
+    table = torch.from_numpy(hw["embed"]).to(dev)
+    g = torch.from_numpy(hw["norm_g"]).to(dev)
+    block = blk.Block(s, 64)
+    wsb = torch.empty(block.lm_head_workspace_bytes(), dtype=torch.uint8, device=dev)
+    x = torch.from_numpy(synth.hidden_input(s, 1, seed=0, stream_offset=99)).to(dev)
+    tok = torch.empty(1, dtype=torch.int64, device=dev)
+    xe = torch.empty((1, s.hidden), dtype=torch.float16, device=dev)
+    ids = torch.from_numpy(synth.token_ids(V, 1, seed=0)).to(dev)
+
+    def step():
+        block.embed(table, ids, xe, stream=stream)
+        block.lm_head(x, g, head, tok, wsb, stream=stream)
+
+    for _ in range(W):
+        step()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    barrier(ws)
+    for i in range(K):
+        evs[i][0].record(stream)
+        block.lm_head(x, g, head, tok, wsb, stream=stream)
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    block.check()
+    ms = reduce_max(sum(a.elapsed_time(b) for a, b in evs), ws) / K
+    nbytes = V * s.hidden * 2 + s.hidden * 2 * 2 + 8
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    block.timing(True)
+    for _ in range(3):
+        step()
+        block.timing_collect(stream)
+    block.timing(False)
+    table_t = block.timing_table()
+    return {"workload": f"final RMSNorm + LM head {V}x{s.hidden} fp16 + greedy argmax, 1 row "
+                        "(one decode step); embedding gather of the step's token",
+            "us_per_call": ms * 1e3, "achieved_gbs": achieved,
+            "frac_of_hbm_peak": achieved / peaks["hbm_gbs"],
+            "roofline_us": nbytes / (peaks["hbm_gbs"] * 1e9) * 1e6,
+            "traffic": NCU_TRAFFIC.get("lm_head"),
+            "kernels": {k: {"avg_us": 1e3 * v[0] / v[1]} for k, v in table_t.items()}}
 
 
 def bench_decode(args, s, dev, stream, peaks, ws):
