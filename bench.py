@@ -380,6 +380,44 @@ def bench_ours(args, ws, rank, local):
     return result
 
 
+def bench_model_step(args, s, dev, stream, peaks, ws, st, L):
+    import torch
+    import synth
+    from decode_qwen2_block_gb300.model import Model
+    K, W = args.steps, args.warmup
+    V = synth.QWEN2_VOCAB
+    hw = {k: torch.from_numpy(v).to(dev) for k, v in synth.head_weights(V, s.hidden, seed=0).items()}
+    model = Model(s, None, hw, 0, stack=st)
+    toks = torch.from_numpy(synth.token_ids(V, W + K + 1, seed=1)).to(dev)
+    graphs = []
+    for i in range(W + K):
+        pos = torch.tensor([L + i], dtype=torch.int64, device=dev)
+        graphs.append((model.capture_step(toks[i:i + 1], pos, L + i, toks[i + 1:i + 2],
+                                          key=("model", L + i)), pos))
+    for i in range(W):
+        graphs[i][0].replay()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    barrier(ws)
+    for i in range(K):
+        evs[i][0].record(stream)
+        graphs[W + i][0].replay()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    st.block.check()
+    ms = reduce_max(sum(a.elapsed_time(b) for a, b in evs), ws) / K
+    nbytes, _ = decode_bytes(s, L + W + K // 2, s.n_layers)
+    nbytes += V * s.hidden * 2 + s.hidden * 2   # the LM head + one embedding row
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    del graphs
+    return {"ctx": L, "us_per_token": ms * 1e3, "tok_s": ws * 1e3 / ms, "bytes_per_token": nbytes,
+            "achieved_gbs": achieved, "frac_of_hbm_peak": achieved / peaks["hbm_gbs"],
+            "workload": "token embedding + 28 blocks + final RMSNorm + 151936x1536 LM head + "
+                        "greedy argmax; the token feeds the next step on the device"}
+
+
 def bench_lm_head(args, s, dev, stream, peaks, ws):
     """Final RMSNorm + LM head + greedy argmax of one decode step (151936 x
     1536 fp16 head, 467 MB: larger than L2, so no flush is needed), and the
@@ -484,6 +522,9 @@ def bench_decode(args, s, dev, stream, peaks, ws):
                        "traffic": NCU_TRAFFIC.get(("decode_persistent", L))}
         del graphs
         st.graphs.clear()
+    # the whole model per generated token at the first context: embedding +
+    # the 28 blocks + final RMSNorm + LM head + greedy argmax, one graph per step
+    out["model_per_token"] = bench_model_step(args, s, dev, stream, peaks, ws, st, ctxs[0])
     # per-kernel durations at the largest context (eager, events per kernel)
     L = ctxs[-1]
     st.block.timing(True)
