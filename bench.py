@@ -46,10 +46,10 @@ PREFILL_T = 1024
 # decode_persistent_1p5b_28layers_ctx4096.md).  Must be set back to None
 # whenever the kernel changes.
 NCU_TRAFFIC = {
-    "gemm_gateup": 58.231808e6 + 3.192832e6,
-    "gemm_down": 45.937152e6 + 1.509376e6,
-    "gemm_qkv": 10.00576e6 + 0.000768e6,
-    "gemm_o": 11.030016e6 + 0.000256e6,
+    "gemm_gateup": 58.231808e6 + 0.156160e6,
+    "gemm_down": 45.917440e6 + 0.011520e6,
+    "gemm_qkv": 10.016768e6 + 0.0,
+    "gemm_o": 11.034624e6 + 0.0,
     "attn_prefill": 4.242944e6,
     "lm_head": 466853632 + 206080,
     # both launches of one 28-layer step (16 + 12 layers)
