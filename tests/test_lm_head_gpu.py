@@ -137,3 +137,17 @@ def test_lm_head_argument_errors():
     rc = blk.blk_lm_head(b.handle, x.data_ptr(), 1, g.data_ptr(), W.data_ptr() + 2, 100, None,
                          tokens.data_ptr(), ws.data_ptr(), ws.numel(), 0)
     assert rc == blk.BLK_ERR_ALIGN
+
+
+def test_lm_head_hidden_4096_three_stage_ring():
+    """hidden 4096 (the larger GQA shape) takes the three-stage ring; each
+    16-row group arrives in three column chunks (24, 24, 16 blocks)."""
+    s = synth.GQA_4096
+    hw = synth.head_weights(5003, s.hidden, seed=21, gain_std=0.1)
+    b = _block(s)
+    x = synth.hidden_input(s, 4, seed=21, stream_offset=3)
+    got, tok = _run_head(b, x, hw)
+    ref, _ = oracle.lm_head(x, hw["norm_g"], hw["lm_head"], eps=s.rms_eps)
+    for t in range(4):
+        assert_close(got[t], ref[t], f"H=4096 logits t={t}")
+    _check_tokens(tok, ref, "H=4096")
