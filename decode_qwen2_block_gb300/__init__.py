@@ -35,7 +35,8 @@ BLK_FLAG_CHAIN = 1
 EXPORTED = ("blk_create", "blk_destroy", "blk_set_flags", "blk_workspace_bytes", "blk_prefill",
             "blk_prefill_kv", "blk_decode", "blk_check", "blk_status_str", "blk_timing",
             "blk_timing_collect", "blk_timing_read", "blk_decode_static", "blk_decode_stack",
-            "blk_set_trace", "blk_embed", "blk_lm_head_workspace_bytes", "blk_lm_head")
+            "blk_set_trace", "blk_embed", "blk_lm_head_workspace_bytes", "blk_lm_head",
+            "blk_decode_batch_workspace_bytes", "blk_decode_batch")
 BLK_N_KERNELS = 16
 
 WEIGHT_FIELDS = ("ln1_g", "wq", "wk", "wv", "bq", "bk", "bv", "wo", "ln2_g", "w_gate", "w_up",
@@ -112,6 +113,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.blk_timing_read.argtypes = [vp, i32, ctypes.POINTER(ctypes.c_double),
                                     ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_char_p)]
     lib.blk_timing_read.restype = i32
+    lib.blk_decode_batch_workspace_bytes.argtypes = [vp, i64]
+    lib.blk_decode_batch_workspace_bytes.restype = ctypes.c_size_t
+    lib.blk_decode_batch.argtypes = [vp, ctypes.POINTER(BlkWeights), vp, vp, vp, i64, i64, vp, vp,
+                                     vp, vp, vp, vp, ctypes.c_size_t, vp]
+    lib.blk_decode_batch.restype = i32
     lib.blk_embed.argtypes = [vp, vp, i64, vp, i64, vp, vp]
     lib.blk_embed.restype = i32
     lib.blk_lm_head_workspace_bytes.argtypes = [vp]
@@ -183,6 +189,16 @@ def blk_decode_static(handle, w: BlkWeights, x, pos, cache_len, k_cache, v_cache
     (for callers that cannot allocate device memory; see include/blk.h)."""
     return load().blk_decode_static(handle, ctypes.byref(w), x, pos, cache_len, k_cache, v_cache,
                                     out, k_new, v_new, stream)
+
+
+def blk_decode_batch_workspace_bytes(handle, max_B: int) -> int:
+    return load().blk_decode_batch_workspace_bytes(handle, max_B)
+
+
+def blk_decode_batch(handle, w: BlkWeights, x, pos, cache_lens, B, max_cache_len, k_cache,
+                     v_cache, out, k_new, v_new, ws, ws_bytes, stream) -> int:
+    return load().blk_decode_batch(handle, ctypes.byref(w), x, pos, cache_lens, B, max_cache_len,
+                                   k_cache, v_cache, out, k_new, v_new, ws, ws_bytes, stream)
 
 
 def blk_embed(handle, table, vocab, ids, T, x, stream) -> int:
@@ -294,6 +310,19 @@ class Block:
                         ws.numel() * ws.element_size(), self._stream(stream))
         if rc != BLK_OK:
             raise BlkError(rc, "blk_decode")
+
+    def decode_batch_workspace_bytes(self, max_B: int) -> int:
+        return blk_decode_batch_workspace_bytes(self.handle, max_B)
+
+    def decode_batch(self, w: BlkWeights, x, pos, cache_lens, max_cache_len: int, k_cache,
+                     v_cache, out, ws, k_new=None, v_new=None, stream=None):
+        """One decode step of B = x.shape[0] sequences (caches [B, Hkv, max_ctx, D])."""
+        rc = blk_decode_batch(self.handle, w, _ptr(x), _ptr(pos), _ptr(cache_lens), x.shape[0],
+                              max_cache_len, _ptr(k_cache), _ptr(v_cache), _ptr(out),
+                              _ptr(k_new), _ptr(v_new), _ptr(ws), ws.numel() * ws.element_size(),
+                              self._stream(stream))
+        if rc != BLK_OK:
+            raise BlkError(rc, "blk_decode_batch")
 
     def embed(self, table, ids, x, stream=None):
         """x[t] = table[ids[t]] (fp16 [vocab, hidden] table, int64 ids)."""

@@ -21,13 +21,13 @@ constexpr int kMaxPending = 1024;
 // Kernel ids for per-kernel timing (blk_timing_read).
 enum KernelId {
   kKRmsNorm = 0, kKGemmQKV, kKSplitReduce, kKAttnPrefill, kKGemmO, kKGemmGateUp,
-  kKGemmDown, kKDecodeStep, kKAttnMerge, kKLmHead, kKArgmax, kKEmbed, kKCount
+  kKGemmDown, kKDecodeStep, kKAttnMerge, kKLmHead, kKArgmax, kKEmbed, kKDecodeAttnBatch,
+  kKCount
 };
 const char* const kKernelNames[BLK_N_KERNELS] = {
     "rmsnorm_rows", "gemm_qkv", "splitk_reduce", "attn_prefill", "gemm_o",
     "gemm_gateup", "gemm_down", "decode_persistent", "attn_merge", "lm_head", "argmax_reduce",
-    "embed",
-    "", "", "", ""};
+    "embed", "decode_attn_batch", "", "", ""};
 }  // namespace
 
 struct blk_handle_s {
@@ -178,6 +178,55 @@ struct Timer {
     if (e_ != cudaSuccess) return BLK_ERR_CUDA; \
   } while (0)
 
+// o_proj + residual, RMSNorm 2, gate|up + SwiGLU, down + residual for M rows
+// (shared by prefill, prefill_kv and batched decode).
+int run_block_tail(blk_handle h, const blk_weights* w, const void* x, __half* attn16,
+                   float* h32, __half* hn16, __half* act16, float* part32, void* out, int M,
+                   cudaStream_t s, Timer& tm) {
+  const blk_config& c = h->cfg;
+  const int H = c.hidden, D = c.head_dim, Hq = c.n_heads, I = c.intermediate;
+  // o_proj + residual -> h (fp32)
+  TcGemmParams go = {};
+  if (make_tmap_2d(&go.tmA, attn16, M, (int64_t)Hq * D, 128) ||
+      make_tmap_2d(&go.tmB[0], w->wo, H, (int64_t)Hq * D, 64))
+    return BLK_ERR_CUDA;
+  go.M = M; go.N = H; go.K = Hq * D;
+  go.res16 = static_cast<const __half*>(x); go.out32 = h32; go.ldo = H;
+  go.err = h->status;
+  BLK_LAUNCH(tm, kKGemmO, launch_tc_gemm(go, kTcResidF32, h->num_sms, s, true));
+
+  // RMSNorm 2
+  BLK_LAUNCH(tm, kKRmsNorm,
+             launch_rmsnorm_rows(h32, true, static_cast<const __half*>(w->ln2_g), M, H,
+                                 c.rms_eps, hn16, s, true));
+
+  // gate | up + SwiGLU
+  TcGemmParams gu = {};
+  if (make_tmap_2d(&gu.tmA, hn16, M, H, 128) ||
+      make_tmap_2d(&gu.tmB[0], w->w_gate, I, H, 64) ||
+      make_tmap_2d(&gu.tmB[1], w->w_up, I, H, 64))
+    return BLK_ERR_CUDA;
+  gu.M = M; gu.N = I; gu.K = H;
+  gu.out16 = act16; gu.ldo = I;
+  gu.err = h->status;
+  BLK_LAUNCH(tm, kKGemmGateUp, launch_tc_gemm(gu, kTcGateUp, h->num_sms, s, true));
+
+  // down + residual -> out
+  TcGemmParams gd = {};
+  if (make_tmap_2d(&gd.tmA, act16, M, I, 128) ||
+      make_tmap_2d(&gd.tmB[0], w->w_down, H, I, 64))
+    return BLK_ERR_CUDA;
+  gd.M = M; gd.N = H; gd.K = I;
+  gd.res32 = h32; gd.out16 = static_cast<__half*>(out); gd.ldo = H;
+  gd.part = part32;
+  gd.max_splits = kMaxSplits;
+  gd.err = h->status;
+  BLK_LAUNCH(tm, kKGemmDown, launch_tc_gemm(gd, kTcResidOutF16, h->num_sms, s, true));
+  if (gd.splits > 1)
+    BLK_LAUNCH(tm, kKSplitReduce, launch_splitk_reduce(gd, h->num_sms, s));
+  return BLK_OK;
+}
+
 // prefill and prefill_kv: T new rows after L history slots.
 int run_prefill(blk_handle h, const blk_weights* w, const void* x,
                 const int64_t* pos, int64_t T, int64_t L, void* k_cache,
@@ -196,8 +245,7 @@ int run_prefill(blk_handle h, const blk_weights* w, const void* x,
   float* h32 = reinterpret_cast<float*>(base + lay.h32);
   __half* hn16 = reinterpret_cast<__half*>(base + lay.hn16);
   __half* act16 = reinterpret_cast<__half*>(base + lay.act16);
-  const int H = c.hidden, D = c.head_dim, Hq = c.n_heads, Hkv = c.n_kv_heads,
-            I = c.intermediate, M = (int)T;
+  const int H = c.hidden, D = c.head_dim, Hq = c.n_heads, Hkv = c.n_kv_heads, M = (int)T;
   const bool first_pdl = (h->flags & BLK_FLAG_CHAIN) != 0;
   Timer tm{h, s};
 
@@ -254,46 +302,110 @@ int run_prefill(blk_handle h, const blk_weights* w, const void* x,
   BLK_LAUNCH(tm, kKAttnPrefill, launch_prefill_attn(pa, s, true));
   if (pa.grid_chunks > 1) BLK_LAUNCH(tm, kKAttnMerge, launch_attn_merge(pa, s, true));
 
-  // o_proj + residual -> h (fp32)
-  TcGemmParams go = {};
-  if (make_tmap_2d(&go.tmA, attn16, M, (int64_t)Hq * D, 128) ||
-      make_tmap_2d(&go.tmB[0], w->wo, H, (int64_t)Hq * D, 64))
-    return BLK_ERR_CUDA;
-  go.M = M; go.N = H; go.K = Hq * D;
-  go.res16 = static_cast<const __half*>(x); go.out32 = h32; go.ldo = H;
-  go.err = h->status;
-  BLK_LAUNCH(tm, kKGemmO, launch_tc_gemm(go, kTcResidF32, h->num_sms, s, true));
+  return run_block_tail(h, w, x, attn16, h32, hn16, act16,
+                        reinterpret_cast<float*>(base + lay.part32), out, M, s, tm);
+}
 
-  // RMSNorm 2
+// Batched decode: B sequences, one new token each, caches [B][Hkv][max_ctx][D].
+struct DecodeBatchWs {
+  size_t xn16, q16, attn16, h32, hn16, act16, part32, apart, total;
+};
+
+DecodeBatchWs decode_batch_ws(const blk_config& c, int64_t B, int num_sms) {
+  const size_t H = c.hidden, D = c.head_dim, Hq = c.n_heads, I = c.intermediate;
+  DecodeBatchWs w;
+  size_t o = 0;
+  w.xn16 = o; o = align_up(o + B * H * 2);
+  w.q16 = o; o = align_up(o + B * Hq * D * 2);
+  w.attn16 = o; o = align_up(o + B * Hq * D * 2);
+  w.h32 = o; o = align_up(o + B * H * 4);
+  w.hn16 = o; o = align_up(o + B * H * 2);
+  w.act16 = o; o = align_up(o + B * I * 2);
+  w.part32 = o; o = align_up(o + (size_t)kMaxSplits * B * H * 4);
+  const int smax = decode_batch_splits((int)B, c.n_kv_heads, c.max_ctx - 1, num_sms);
+  w.apart = o; o = align_up(o + decode_batch_part_bytes((int)B, (int)Hq, (int)D, smax));
+  w.total = o;
+  return w;
+}
+
+int run_decode_batch(blk_handle h, const blk_weights* w, const void* x, const int64_t* pos,
+                     const int64_t* cache_lens, int64_t B, int64_t max_cache_len, void* k_cache,
+                     void* v_cache, void* out, void* k_new, void* v_new, void* ws,
+                     size_t ws_bytes, void* stream) {
+  if (!h) return BLK_ERR_NULL;
+  const blk_config& c = h->cfg;
+  int rc = check_weights(c, w);
+  if (rc) return rc;
+  if (!x || !pos || !cache_lens || !k_cache || !v_cache || !out || !ws) return BLK_ERR_NULL;
+  for (const void* ptr : {x, (const void*)k_cache, (const void*)v_cache, (const void*)out,
+                          (const void*)ws})
+    if (!aligned(ptr, 16)) return BLK_ERR_ALIGN;
+  if (!aligned(pos, 8) || !aligned(cache_lens, 8)) return BLK_ERR_ALIGN;
+  if ((k_new && !aligned(k_new, 16)) || (v_new && !aligned(v_new, 16))) return BLK_ERR_ALIGN;
+  if (B < 1 || B > 4096) return BLK_ERR_SHAPE;
+  if (max_cache_len < 0 || max_cache_len + 1 > c.max_ctx) return BLK_ERR_CACHE_OVERFLOW;
+  if (c.n_heads / c.n_kv_heads > 16) return BLK_ERR_SHAPE;
+  const DecodeBatchWs lay = decode_batch_ws(c, B, h->num_sms);
+  if (ws_bytes < lay.total) return BLK_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned char* base = static_cast<unsigned char*>(ws);
+  __half* xn16 = reinterpret_cast<__half*>(base + lay.xn16);
+  __half* q16 = reinterpret_cast<__half*>(base + lay.q16);
+  __half* attn16 = reinterpret_cast<__half*>(base + lay.attn16);
+  const int H = c.hidden, D = c.head_dim, Hq = c.n_heads, Hkv = c.n_kv_heads, M = (int)B;
+  const bool first_pdl = (h->flags & BLK_FLAG_CHAIN) != 0;
+  Timer tm{h, s};
+
   BLK_LAUNCH(tm, kKRmsNorm,
-             launch_rmsnorm_rows(h32, true, static_cast<const __half*>(w->ln2_g), M, H,
-                                 c.rms_eps, hn16, s, true));
+             launch_rmsnorm_rows(x, false, static_cast<const __half*>(w->ln1_g), M, H,
+                                 c.rms_eps, xn16, s, first_pdl));
 
-  // gate | up + SwiGLU
-  TcGemmParams gu = {};
-  if (make_tmap_2d(&gu.tmA, hn16, M, H, 128) ||
-      make_tmap_2d(&gu.tmB[0], w->w_gate, I, H, 64) ||
-      make_tmap_2d(&gu.tmB[1], w->w_up, I, H, 64))
+  // QKV + bias + RoPE at pos[b]; K/V to slot cache_lens[b] of sequence b's cache
+  TcGemmParams g = {};
+  if (make_tmap_2d(&g.tmA, xn16, M, H, 128) ||
+      make_tmap_2d(&g.tmB[0], w->wq, (int64_t)Hq * D, H, 64) ||
+      make_tmap_2d(&g.tmB[1], w->wk, (int64_t)Hkv * D, H, 64) ||
+      make_tmap_2d(&g.tmB[2], w->wv, (int64_t)Hkv * D, H, 64))
     return BLK_ERR_CUDA;
-  gu.M = M; gu.N = I; gu.K = H;
-  gu.out16 = act16; gu.ldo = I;
-  gu.err = h->status;
-  BLK_LAUNCH(tm, kKGemmGateUp, launch_tc_gemm(gu, kTcGateUp, h->num_sms, s, true));
+  g.M = M; g.N = (Hq + 2 * Hkv) * D; g.K = H;
+  g.seg_rows[0] = Hq * D; g.seg_rows[1] = Hkv * D; g.seg_rows[2] = Hkv * D;
+  if (c.has_qkv_bias) {
+    g.bias[0] = static_cast<const __half*>(w->bq);
+    g.bias[1] = static_cast<const __half*>(w->bk);
+    g.bias[2] = static_cast<const __half*>(w->bv);
+  }
+  g.pos = pos; g.rope = h->rope; g.rope_len = c.max_ctx;
+  g.Hq = Hq; g.Hkv = Hkv; g.D = D;
+  g.q16 = q16;
+  g.kc = static_cast<__half*>(k_cache);
+  g.vc = static_cast<__half*>(v_cache);
+  g.k_new = static_cast<__half*>(k_new);
+  g.v_new = static_cast<__half*>(v_new);
+  g.max_ctx = c.max_ctx; g.cache_len = 0;
+  g.cache_lens = cache_lens;
+  g.seq_stride = (int64_t)Hkv * c.max_ctx * D;
+  g.err = h->status;
+  BLK_LAUNCH(tm, kKGemmQKV, launch_tc_gemm(g, kTcQKV, h->num_sms, s, true));
 
-  // down + residual -> out
-  TcGemmParams gd = {};
-  if (make_tmap_2d(&gd.tmA, act16, M, I, 128) ||
-      make_tmap_2d(&gd.tmB[0], w->w_down, H, I, 64))
-    return BLK_ERR_CUDA;
-  gd.M = M; gd.N = H; gd.K = I;
-  gd.res32 = h32; gd.out16 = static_cast<__half*>(out); gd.ldo = H;
-  gd.part = reinterpret_cast<float*>(base + lay.part32);
-  gd.max_splits = kMaxSplits;
-  gd.err = h->status;
-  BLK_LAUNCH(tm, kKGemmDown, launch_tc_gemm(gd, kTcResidOutF16, h->num_sms, s, true));
-  if (gd.splits > 1)
-    BLK_LAUNCH(tm, kKSplitReduce, launch_splitk_reduce(gd, h->num_sms, s));
-  return BLK_OK;
+  // attention of every sequence over its own slots [0, cache_lens[b]]
+  DecodeAttnBatchParams pa = {};
+  pa.q16 = q16;
+  pa.kc = static_cast<const __half*>(k_cache);
+  pa.vc = static_cast<const __half*>(v_cache);
+  pa.cache_lens = cache_lens;
+  pa.B = M; pa.Hq = Hq; pa.Hkv = Hkv; pa.D = D;
+  pa.max_ctx = c.max_ctx;
+  pa.scale_log2 = (float)(1.4426950408889634 / sqrt((double)D));
+  pa.nsplit = decode_batch_splits(M, Hkv, max_cache_len, h->num_sms);
+  pa.part = reinterpret_cast<float*>(base + lay.apart);
+  pa.attn16 = attn16;
+  pa.err = h->status;
+  BLK_LAUNCH(tm, kKDecodeAttnBatch, launch_decode_attn_batch(pa, s));
+
+  return run_block_tail(h, w, x, attn16, reinterpret_cast<float*>(base + lay.h32),
+                        reinterpret_cast<__half*>(base + lay.hn16),
+                        reinterpret_cast<__half*>(base + lay.act16),
+                        reinterpret_cast<float*>(base + lay.part32), out, M, s, tm);
 }
 
 }  // namespace
@@ -567,6 +679,19 @@ int blk_lm_head(blk_handle h, const void* x, int64_t T, const void* norm_g, cons
   return BLK_OK;
 }
 
+size_t blk_decode_batch_workspace_bytes(blk_handle h, int64_t max_B) {
+  if (!h || max_B < 1) return 0;
+  return decode_batch_ws(h->cfg, max_B, h->num_sms).total;
+}
+
+int blk_decode_batch(blk_handle h, const blk_weights* w, const void* x, const int64_t* pos,
+                     const int64_t* cache_lens, int64_t B, int64_t max_cache_len, void* k_cache,
+                     void* v_cache, void* out, void* k_new, void* v_new, void* ws,
+                     size_t ws_bytes, void* stream) {
+  return run_decode_batch(h, w, x, pos, cache_lens, B, max_cache_len, k_cache, v_cache, out,
+                          k_new, v_new, ws, ws_bytes, stream);
+}
+
 }  // extern "C"
 
 size_t blk_internal_decode_ws_bytes(blk_handle h) {
@@ -652,6 +777,7 @@ cudaError_t configure_kernels() {
   if (e == cudaSuccess) e = configure_tc_gemm_kernels();
   if (e == cudaSuccess) e = configure_prefill_attn();
   if (e == cudaSuccess) e = configure_lm_head();
+  if (e == cudaSuccess) e = configure_decode_attn_batch();
   return e;
 }
 }  // namespace blk

@@ -452,7 +452,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               v1[i] = b * cx + a * sy;
             }
           }
-          if (staged) {
+          // batched decode: row m is sequence m, its K/V go to its own cache
+          const bool kv_rows = hd >= p.Hq && p.cache_lens != nullptr;
+          if (staged && !kv_rows) {
             uint8_t* g;
             size_t ld;
             __half* nw = nullptr;
@@ -474,6 +476,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               store_rows_staged<true>(stg, v0, lane, g2 + c0 * 2, ld2, nrows);
               store_rows_staged<true>(stg, v1, lane, g2 + (half + c0) * 2, ld2, nrows);
             }
+          } else if (!row_ok) {
+            // rows past M hold nothing to store
           } else if (hd < p.Hq) {
             __half* dst = p.q16 + ((size_t)m * p.Hq + hd) * D;
             store_h32(dst + c0, v0);
@@ -482,9 +486,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool is_k = hd < p.Hq + p.Hkv;
             __half* cache = is_k ? p.kc : p.vc;
             __half* nw = is_k ? p.k_new : p.v_new;
-            __half* dst = cache + ((size_t)local * p.max_ctx + p.cache_len + m) * D;
-            store_h32(dst + c0, v0);
-            store_h32(dst + half + c0, v1);
+            int64_t slot = p.cache_len + m;
+            if (p.cache_lens) {
+              slot = p.cache_lens[m];
+              cache += (size_t)m * p.seq_stride;
+            }
+            if (slot >= 0 && slot < p.max_ctx) {
+              __half* dst = cache + ((size_t)local * p.max_ctx + slot) * D;
+              store_h32(dst + c0, v0);
+              store_h32(dst + half + c0, v1);
+            } else if (c0 == 0) {
+              set_error(p.err, kDevPosition);
+            }
             if (nw) {
               __half* d2 = nw + ((size_t)m * p.Hkv + local) * D;
               store_h32(d2 + c0, v0);

@@ -33,6 +33,10 @@ struct TcGemmParams {
   __half* k_new;
   __half* v_new;
   int64_t max_ctx, cache_len;
+  // batched decode (cache_lens != null): row m is sequence m, whose K/V go to
+  // slot cache_lens[m] of the caches at kc/vc + m * seq_stride
+  const int64_t* cache_lens;
+  int64_t seq_stride;
   // other epilogues
   const __half* res16;
   const float* res32;

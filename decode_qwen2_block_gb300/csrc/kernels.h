@@ -41,6 +41,27 @@ cudaError_t launch_prefill_attn(const PrefillAttnParams& p, cudaStream_t s,
 cudaError_t launch_attn_merge(const PrefillAttnParams& p, cudaStream_t s, bool pdl);
 cudaError_t configure_prefill_attn();
 
+// Attention of a batched decode step (decode_batch.cu): B sequences, one new
+// row each, caches [B][Hkv][max_ctx][D], slots [0, cache_lens[b]] (the last
+// one already holding the new K/V).
+struct DecodeAttnBatchParams {
+  const __half* q16;          // [B, Hq, D] (RoPE applied)
+  const __half* kc;
+  const __half* vc;
+  const int64_t* cache_lens;  // [B], device
+  int B, Hq, Hkv, D;
+  int64_t max_ctx;
+  float scale_log2;
+  int nsplit;                 // splits of each sequence's slots (decode_batch_splits)
+  float* part;                // [B][Hq][nsplit][D + 2] when nsplit > 1
+  __half* attn16;             // [B, Hq * D]
+  int* err;
+};
+int decode_batch_splits(int B, int Hkv, int64_t max_len, int num_sms);
+size_t decode_batch_part_bytes(int B, int Hq, int D, int nsplit);
+cudaError_t launch_decode_attn_batch(const DecodeAttnBatchParams& p, cudaStream_t s);
+cudaError_t configure_decode_attn_batch();
+
 // Final RMSNorm + LM head + greedy argmax (lm_head.cu).
 struct LmHeadParams {
   CUtensorMap tm_w;     // W [vocab, H] viewed as (64, vocab, H / 64), box (64, 16, 24), SW128

@@ -233,6 +233,32 @@ int blk_timing_read(blk_handle h, int kernel, double* total_ms,
  * NULL turns tracing off (the default).  Returns BLK_OK or BLK_ERR_NULL. */
 int blk_set_trace(blk_handle h, void* device_buffer, size_t bytes);
 
+/* ---- batched decode --------------------------------------------------------
+ * One decode step of the block for B independent sequences (one new token
+ * each): the decode phase of the TopOp decoder block (§4 "three-phase
+ * split") applied per sequence, with the weights read once for all B rows.
+ *   x        device fp16 [B, hidden]; pos: device int64 [B] position_ids
+ *   cache_lens device int64 [B]: sequence b's history length L_b; its new K/V
+ *            go to slot L_b and it attends to slots [0, L_b] of its own cache
+ *   max_cache_len  an upper bound of the cache_lens (host value, sizes the
+ *            attention's split of the slots); max_cache_len + 1 <= max_ctx
+ *   k_cache, v_cache  device fp16 [B, n_kv_heads, max_ctx, head_dim]
+ *   out      device fp16 [B, hidden]; k_new, v_new  [B, n_kv_heads, head_dim]
+ *            or NULL
+ * Equals blk_decode on each sequence within the tolerance (same kernels for
+ * the projections, a split-K flash-decode attention).  A cache length outside
+ * [0, max_ctx) skips that sequence's K/V write and attention, and reports
+ * BLK_ERR_POSITION from the next blk_check.  Returns BLK_OK, BLK_ERR_NULL,
+ * BLK_ERR_ALIGN, BLK_ERR_SHAPE (B outside [1, 4096], more than 16 query heads
+ * per kv head), BLK_ERR_CACHE_OVERFLOW (max_cache_len), BLK_ERR_WORKSPACE or
+ * BLK_ERR_CUDA.  Asynchronous on `stream`.  The cache lengths are read on the
+ * device, so one captured CUDA graph serves consecutive steps. */
+size_t blk_decode_batch_workspace_bytes(blk_handle h, int64_t max_B);
+int blk_decode_batch(blk_handle h, const blk_weights* w, const void* x, const int64_t* pos,
+                     const int64_t* cache_lens, int64_t B, int64_t max_cache_len, void* k_cache,
+                     void* v_cache, void* out, void* k_new, void* v_new, void* ws,
+                     size_t ws_bytes, void* stream);
+
 /* ---- around the block stack: embedding in, next token out ----------------
  * The inference flow of the MLIR-compilation page (§2.3 "LLM inference
  * overview"): input tokens -> word embedding -> the blocks -> LM head ->

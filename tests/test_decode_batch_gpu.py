@@ -1,0 +1,125 @@
+"""GPU parity of batched decode: B sequences with their own caches and cache
+lengths in one call, each checked against the oracle's decode of that
+sequence alone (the benchmark spec tolerance), the new K/V slot bit-exact and every
+other cache slot untouched."""
+import numpy as np
+import pytest
+import torch
+
+import decode_qwen2_block_gb300 as blk
+import oracle
+import synth
+from gpu_harness import assert_close, to_dev
+
+pytestmark = pytest.mark.gpu
+SENTINEL = np.float16(-3.5)
+
+
+def _run_batch(s, w, lens, C, seed, max_len=None):
+    B = len(lens)
+    hist = [synth.kv_history(s, C, L, layer=b, seed=seed, sentinel=SENTINEL)
+            for b, L in enumerate(lens)]
+    kc_np = np.stack([k for k, _ in hist])
+    vc_np = np.stack([v for _, v in hist])
+    x = synth.hidden_input(s, B, seed=seed, stream_offset=5)
+    pos = np.array(lens, dtype=np.int64)          # position = cache length
+    block = blk.Block(s, C)
+    wd = {k: to_dev(v) for k, v in w.items()}
+    wts = blk.Block.weights(wd)
+    kc, vc = to_dev(kc_np), to_dev(vc_np)
+    out = torch.empty((B, s.hidden), dtype=torch.float16, device="cuda")
+    kn = torch.empty((B, s.n_kv_heads, s.head_dim), dtype=torch.float16, device="cuda")
+    vn = torch.empty_like(kn)
+    ws = torch.empty(block.decode_batch_workspace_bytes(B), dtype=torch.uint8, device="cuda")
+    block.decode_batch(wts, to_dev(x), to_dev(pos), to_dev(pos), max(lens) if max_len is None else max_len,
+                       kc, vc, out, ws, k_new=kn, v_new=vn)
+    torch.cuda.synchronize()
+    block.check()
+    return x, kc_np, vc_np, out.cpu().numpy(), kn.cpu().numpy(), vn.cpu().numpy(), \
+        kc.cpu().numpy(), vc.cpu().numpy()
+
+
+def _check(s, w, lens, C, seed, **kw):
+    x, kc0, vc0, out, kn, vn, kc1, vc1 = _run_batch(s, w, lens, C, seed, **kw)
+    for b, L in enumerate(lens):
+        kc_o, vc_o = kc0[b].copy(), vc0[b].copy()
+        o_ref, k_ref, v_ref = oracle.block_forward(s, w, x[b:b + 1], [L], L, kc_o, vc_o)
+        assert_close(out[b:b + 1], o_ref, f"seq {b} L={L} out")
+        assert_close(kn[b:b + 1], k_ref, f"seq {b} k_new")
+        assert_close(vn[b:b + 1], v_ref, f"seq {b} v_new")
+        # slot L holds the returned K/V bit for bit; every other slot is unchanged
+        assert np.array_equal(kc1[b][:, L].view(np.uint16), kn[b].view(np.uint16))
+        assert np.array_equal(vc1[b][:, L].view(np.uint16), vn[b].view(np.uint16))
+        for got, before in ((kc1[b], kc0[b]), (vc1[b], vc0[b])):
+            mask = np.ones(got.shape[1], bool)
+            mask[L] = False
+            assert np.array_equal(got[:, mask].view(np.uint16), before[:, mask].view(np.uint16))
+
+
+def test_tiny_batch_of_three_lengths():
+    s = synth.TINY
+    w = synth.block_weights(s, seed=7)
+    _check(s, w, [0, 37, 100], 128, seed=7)
+
+
+def test_1p5b_batch_mixed_lengths():
+    s = synth.QWEN2_1P5B
+    w = synth.block_weights(s, seed=8)
+    _check(s, w, [1000, 4095, 17, 2048], 4096 + 64, seed=8)
+
+
+def test_gqa4096_batch_and_a_generous_length_bound():
+    """16 query heads per kv head (a full MMA tile of rows); max_cache_len far
+    above the actual lengths only changes the split count."""
+    s = synth.GQA_4096
+    w = synth.block_weights(s, seed=9)
+    _check(s, w, [300, 5], 512, seed=9, max_len=511)
+
+
+def test_batch_equals_single_sequence_decode():
+    """The same sequence through blk_decode and through a batch of 5."""
+    s = synth.QWEN2_1P5B
+    w = synth.block_weights(s, seed=10)
+    C, L = 1024, 700
+    k0, v0 = synth.kv_history(s, C, L, seed=10)
+    x = synth.hidden_input(s, 5, seed=10)
+    block = blk.Block(s, C)
+    wd = {k: to_dev(v) for k, v in w.items()}   # kept alive: the handle holds raw pointers
+    wts = blk.Block.weights(wd)
+    out1 = torch.empty((1, s.hidden), dtype=torch.float16, device="cuda")
+    ws1 = torch.empty(block.workspace_bytes(1), dtype=torch.uint8, device="cuda")
+    kc1, vc1 = to_dev(k0), to_dev(v0)
+    block.decode(wts, to_dev(x[2:3]), to_dev(np.array([L])), L, kc1, vc1, out1, ws1)
+    kcb = to_dev(np.stack([k0] * 5))
+    vcb = to_dev(np.stack([v0] * 5))
+    lens = to_dev(np.array([L] * 5, dtype=np.int64))
+    outb = torch.empty((5, s.hidden), dtype=torch.float16, device="cuda")
+    wsb = torch.empty(block.decode_batch_workspace_bytes(5), dtype=torch.uint8, device="cuda")
+    block.decode_batch(wts, to_dev(x), lens, lens, L, kcb, vcb, outb, wsb)
+    torch.cuda.synchronize()
+    block.check()
+    assert_close(outb[2:3].cpu().numpy(), out1.cpu().numpy().astype(np.float64), "batch vs single")
+
+
+def test_batch_argument_errors_and_bad_length():
+    s = synth.TINY
+    w = synth.block_weights(s, seed=11)
+    C, B = 64, 2
+    block = blk.Block(s, C)
+    wd = {k: to_dev(v) for k, v in w.items()}   # kept alive: the handle holds raw pointers
+    wts = blk.Block.weights(wd)
+    kc = torch.zeros((B, s.n_kv_heads, C, s.head_dim), dtype=torch.float16, device="cuda")
+    vc = torch.zeros_like(kc)
+    x = torch.zeros((B, s.hidden), dtype=torch.float16, device="cuda")
+    out = torch.empty_like(x)
+    ws = torch.empty(block.decode_batch_workspace_bytes(B), dtype=torch.uint8, device="cuda")
+    lens = torch.tensor([3, 70], dtype=torch.int64, device="cuda")   # 70 >= max_ctx
+    with pytest.raises(blk.BlkError) as e:
+        block.decode_batch(wts, x, lens, lens, C, kc, vc, out, ws)
+    assert e.value.status == blk.BLK_ERR_CACHE_OVERFLOW
+    block.decode_batch(wts, x, lens, lens, C - 1, kc, vc, out, ws)
+    torch.cuda.synchronize()
+    with pytest.raises(blk.BlkError) as e:
+        block.check()
+    assert e.value.status == blk.BLK_ERR_POSITION
+    assert not kc[1].any() and not vc[1].any()           # nothing written for the bad sequence
