@@ -66,7 +66,10 @@ def parse():
     ap.add_argument("--no-decode", action="store_true", help="skip the decode table")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--decode-ctx", type=str, default=",".join(map(str, DECODE_CTX)))
-    ap.add_argument("--only", choices=("prefill", "decode"), default=None,
+    ap.add_argument("--decode-batch", type=str, default="8,32,64",
+                    help="batch sizes of the batched decode table (ctx --decode-batch-ctx)")
+    ap.add_argument("--decode-batch-ctx", type=int, default=1024)
+    ap.add_argument("--only", choices=("prefill", "decode", "decode_batch"), default=None,
                     help="run one part (for profiling); the headline needs both")
     return ap.parse_args()
 
@@ -246,6 +249,12 @@ def bench_ours(args, ws, rank, local):
         head = bench_lm_head(args, s, dev, stream, peaks, ws)
         return {"metric": "decode us/step (28 layers)", "decode": dec, "lm_head": head,
                 "clocks": clocks.stop()}
+    if args.only == "decode_batch":
+        clocks = ClockSampler(local)
+        clocks.start()
+        db = bench_decode_batch(args, s, dev, stream, peaks, ws)
+        return {"metric": "batched decode tok/s (28 layers)", "decode_batch": db,
+                "clocks": clocks.stop()}
 
     # ---------------- prefill, one layer, [1, 1024] ----------------
     T = PREFILL_T
@@ -376,6 +385,7 @@ def bench_ours(args, ws, rank, local):
     if not args.no_decode and args.only != "prefill":
         result["decode"] = bench_decode(args, s, dev, stream, peaks, ws)
         result["lm_head"] = bench_lm_head(args, s, dev, stream, peaks, ws)
+        result["decode_batch"] = bench_decode_batch(args, s, dev, stream, peaks, ws)
     result["clocks"] = clocks.stop()
     return result
 
@@ -471,6 +481,110 @@ def bench_lm_head(args, s, dev, stream, peaks, ws):
             "roofline_us": nbytes / (peaks["hbm_gbs"] * 1e9) * 1e6,
             "traffic": NCU_TRAFFIC.get("lm_head"),
             "kernels": {k: {"avg_us": 1e3 * v[0] / v[1]} for k, v in table_t.items()}}
+
+
+def bench_decode_batch(args, s, dev, stream, peaks, ws):
+    """Batched decode: B sequences, one new token each, through the 28-layer
+    stack (blk_decode_batch per layer), one CUDA graph per step.  Every
+    sequence holds ctx history slots (each layer's seeded history, the same
+    for every sequence of the layer); the step appends slot ctx + i.  Bytes
+    per step: every layer's weights once + each sequence's K/V slots read;
+    the weights (2.6 GB) exceed L2, so no flush is needed."""
+    import torch
+    import synth
+    import decode_qwen2_block_gb300 as blk
+    K, W = args.steps, args.warmup
+    Bs = [int(b) for b in args.decode_batch.split(",") if b]
+    L0 = args.decode_batch_ctx
+    n = s.n_layers
+    C = L0 + W + K + 8
+    Bmax = max(Bs)
+    H = s.hidden
+    wd = []
+    for l in range(n):
+        wnp = synth.block_weights(s, layer=l, seed=0)
+        wd.append({k: torch.from_numpy(v).to(dev) for k, v in wnp.items()})
+    block = blk.Block(s, C, chain=True)
+    wts = [blk.Block.weights(w) for w in wd]
+    caches = []
+    for l in range(n):
+        k, v = synth.kv_history(s, C, L0, layer=l, seed=0)
+        kc = torch.from_numpy(k).to(dev).unsqueeze(0).repeat(Bmax, 1, 1, 1).contiguous()
+        vc = torch.from_numpy(v).to(dev).unsqueeze(0).repeat(Bmax, 1, 1, 1).contiguous()
+        caches.append((kc, vc))
+    wsb = torch.empty(block.decode_batch_workspace_bytes(Bmax), dtype=torch.uint8, device=dev)
+    x = torch.from_numpy(synth.hidden_input(s, Bmax, seed=0, stream_offset=5)).to(dev)
+    bufs = [torch.empty((Bmax, H), dtype=torch.float16, device=dev) for _ in range(2)]
+    maxlen = L0 + W + K
+
+    def step(B, lens):
+        cur = x[:B]
+        for l in range(n):
+            out = bufs[l % 2][:B]
+            block.decode_batch(wts[l], cur, lens, lens, maxlen, caches[l][0][:B],
+                               caches[l][1][:B], out, wsb, stream=stream)
+            cur = out
+
+    out = {}
+    for B in Bs:
+        lens = [torch.full((B,), L0 + i, dtype=torch.int64, device=dev) for i in range(W + K)]
+        graphs = []
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        for i in range(W + K):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(side):
+                with torch.cuda.graph(g, stream=side):
+                    cur = x[:B]
+                    for l in range(n):
+                        o = bufs[l % 2][:B]
+                        block.decode_batch(wts[l], cur, lens[i], lens[i], maxlen,
+                                           caches[l][0][:B], caches[l][1][:B], o, wsb,
+                                           stream=side)
+                        cur = o
+            graphs.append(g)
+        torch.cuda.current_stream().wait_stream(side)
+        for i in range(W):
+            graphs[i].replay()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)]
+        barrier(ws)
+        for i in range(K):
+            evs[i][0].record(stream)
+            graphs[W + i].replay()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        barrier(ws)
+        block.check()
+        ms = reduce_max(sum(a.elapsed_time(b) for a, b in evs), ws) / K
+        _, wbytes = decode_bytes(s, 0, n)
+        kv = n * 2 * s.n_kv_heads * s.head_dim * 2 * (L0 + W + K // 2 + 1)
+        nbytes = wbytes + B * kv + n * B * H * 2 * 2
+        achieved = nbytes / (ms * 1e-3) / 1e9
+        row = {"us_per_step": ms * 1e3, "tok_s": ws * B * 1e3 / ms, "bytes_per_step": nbytes,
+               "achieved_gbs": achieved, "frac_of_hbm_peak": achieved / peaks["hbm_gbs"],
+               "roofline_us": nbytes / (peaks["hbm_gbs"] * 1e9) * 1e6}
+        # per-kernel durations (eager, events per kernel), two steps
+        before = block.timing_table()
+        block.timing(True)
+        for _ in range(2):
+            step(B, lens[W])
+            block.timing_collect(stream)
+        block.timing(False)
+        table = {k: (t - before.get(k, (0.0, 0))[0], c - before.get(k, (0.0, 0))[1])
+                 for k, (t, c) in block.timing_table().items()}
+        table = {k: v for k, v in table.items() if v[1] > 0}
+        tot = sum(v[0] for v in table.values())
+        row["kernels"] = {k: {"avg_us": 1e3 * t / c, "share": t / tot}
+                          for k, (t, c) in table.items()}
+        row["launches_per_step"] = sum(c for _, c in table.values()) // 2
+        out[str(B)] = row
+        del graphs
+    out["ctx"] = L0
+    out["workload"] = (f"qwen2-1.5B-shaped 28-layer stack, B sequences x 1 new token, "
+                       f"{L0} history slots each, one CUDA graph per step")
+    return out
 
 
 def bench_decode(args, s, dev, stream, peaks, ws):

@@ -84,6 +84,9 @@ int shape_ok(const blk_config* c) {
 // Workspace layout.  Prefill and decode buffers start at offset 0 (a call
 // uses one of the two layouts).
 constexpr int kMaxSplits = 4;        // split-K partial buffers of the down projection
+// Batched decode (at most a few hundred rows): the down projection's few
+// N tiles need more K splits to occupy every SM pair.
+constexpr int kMaxSplitsBatch = 16;
 
 struct PrefillWs {
   size_t xn16, q16, attn16, h32, hn16, act16, part32, total;
@@ -181,16 +184,16 @@ struct Timer {
 // o_proj + residual, RMSNorm 2, gate|up + SwiGLU, down + residual for M rows
 // (shared by prefill, prefill_kv and batched decode).
 int run_block_tail(blk_handle h, const blk_weights* w, const void* x, __half* attn16,
-                   float* h32, __half* hn16, __half* act16, float* part32, void* out, int M,
-                   cudaStream_t s, Timer& tm) {
+                   float* h32, __half* hn16, __half* act16, float* part32, int max_splits,
+                   void* out, int M, cudaStream_t s, Timer& tm) {
   const blk_config& c = h->cfg;
   const int H = c.hidden, D = c.head_dim, Hq = c.n_heads, I = c.intermediate;
   // o_proj + residual -> h (fp32)
   TcGemmParams go = {};
-  if (make_tmap_2d(&go.tmA, attn16, M, (int64_t)Hq * D, 128) ||
+  if (make_tmap_2d(&go.tmA, attn16, M, (int64_t)Hq * D, tc_a_box_rows(M)) ||
       make_tmap_2d(&go.tmB[0], w->wo, H, (int64_t)Hq * D, 64))
     return BLK_ERR_CUDA;
-  go.M = M; go.N = H; go.K = Hq * D;
+  go.M = M; go.N = H; go.K = Hq * D; go.a_rows = tc_a_box_rows(M);
   go.res16 = static_cast<const __half*>(x); go.out32 = h32; go.ldo = H;
   go.err = h->status;
   BLK_LAUNCH(tm, kKGemmO, launch_tc_gemm(go, kTcResidF32, h->num_sms, s, true));
@@ -202,24 +205,24 @@ int run_block_tail(blk_handle h, const blk_weights* w, const void* x, __half* at
 
   // gate | up + SwiGLU
   TcGemmParams gu = {};
-  if (make_tmap_2d(&gu.tmA, hn16, M, H, 128) ||
+  if (make_tmap_2d(&gu.tmA, hn16, M, H, tc_a_box_rows(M)) ||
       make_tmap_2d(&gu.tmB[0], w->w_gate, I, H, 64) ||
       make_tmap_2d(&gu.tmB[1], w->w_up, I, H, 64))
     return BLK_ERR_CUDA;
-  gu.M = M; gu.N = I; gu.K = H;
+  gu.M = M; gu.N = I; gu.K = H; gu.a_rows = tc_a_box_rows(M);
   gu.out16 = act16; gu.ldo = I;
   gu.err = h->status;
   BLK_LAUNCH(tm, kKGemmGateUp, launch_tc_gemm(gu, kTcGateUp, h->num_sms, s, true));
 
   // down + residual -> out
   TcGemmParams gd = {};
-  if (make_tmap_2d(&gd.tmA, act16, M, I, 128) ||
+  if (make_tmap_2d(&gd.tmA, act16, M, I, tc_a_box_rows(M)) ||
       make_tmap_2d(&gd.tmB[0], w->w_down, H, I, 64))
     return BLK_ERR_CUDA;
-  gd.M = M; gd.N = H; gd.K = I;
+  gd.M = M; gd.N = H; gd.K = I; gd.a_rows = tc_a_box_rows(M);
   gd.res32 = h32; gd.out16 = static_cast<__half*>(out); gd.ldo = H;
   gd.part = part32;
-  gd.max_splits = kMaxSplits;
+  gd.max_splits = max_splits;
   gd.err = h->status;
   BLK_LAUNCH(tm, kKGemmDown, launch_tc_gemm(gd, kTcResidOutF16, h->num_sms, s, true));
   if (gd.splits > 1)
@@ -256,12 +259,12 @@ int run_prefill(blk_handle h, const blk_weights* w, const void* x,
 
   // QKV projection + bias + RoPE + KV append
   TcGemmParams g = {};
-  if (make_tmap_2d(&g.tmA, xn16, M, H, 128) ||
+  if (make_tmap_2d(&g.tmA, xn16, M, H, tc_a_box_rows(M)) ||
       make_tmap_2d(&g.tmB[0], w->wq, (int64_t)Hq * D, H, 64) ||
       make_tmap_2d(&g.tmB[1], w->wk, (int64_t)Hkv * D, H, 64) ||
       make_tmap_2d(&g.tmB[2], w->wv, (int64_t)Hkv * D, H, 64))
     return BLK_ERR_CUDA;
-  g.M = M; g.N = (Hq + 2 * Hkv) * D; g.K = H;
+  g.M = M; g.N = (Hq + 2 * Hkv) * D; g.K = H; g.a_rows = tc_a_box_rows(M);
   g.seg_rows[0] = Hq * D; g.seg_rows[1] = Hkv * D; g.seg_rows[2] = Hkv * D;
   if (c.has_qkv_bias) {
     g.bias[0] = static_cast<const __half*>(w->bq);
@@ -303,7 +306,8 @@ int run_prefill(blk_handle h, const blk_weights* w, const void* x,
   if (pa.grid_chunks > 1) BLK_LAUNCH(tm, kKAttnMerge, launch_attn_merge(pa, s, true));
 
   return run_block_tail(h, w, x, attn16, h32, hn16, act16,
-                        reinterpret_cast<float*>(base + lay.part32), out, M, s, tm);
+                        reinterpret_cast<float*>(base + lay.part32), kMaxSplits, out, M, s,
+                        tm);
 }
 
 // Batched decode: B sequences, one new token each, caches [B][Hkv][max_ctx][D].
@@ -321,7 +325,7 @@ DecodeBatchWs decode_batch_ws(const blk_config& c, int64_t B, int num_sms) {
   w.h32 = o; o = align_up(o + B * H * 4);
   w.hn16 = o; o = align_up(o + B * H * 2);
   w.act16 = o; o = align_up(o + B * I * 2);
-  w.part32 = o; o = align_up(o + (size_t)kMaxSplits * B * H * 4);
+  w.part32 = o; o = align_up(o + (size_t)kMaxSplitsBatch * B * H * 4);
   const int smax = decode_batch_splits((int)B, c.n_kv_heads, c.max_ctx - 1, num_sms);
   w.apart = o; o = align_up(o + decode_batch_part_bytes((int)B, (int)Hq, (int)D, smax));
   w.total = o;
@@ -362,12 +366,12 @@ int run_decode_batch(blk_handle h, const blk_weights* w, const void* x, const in
 
   // QKV + bias + RoPE at pos[b]; K/V to slot cache_lens[b] of sequence b's cache
   TcGemmParams g = {};
-  if (make_tmap_2d(&g.tmA, xn16, M, H, 128) ||
+  if (make_tmap_2d(&g.tmA, xn16, M, H, tc_a_box_rows(M)) ||
       make_tmap_2d(&g.tmB[0], w->wq, (int64_t)Hq * D, H, 64) ||
       make_tmap_2d(&g.tmB[1], w->wk, (int64_t)Hkv * D, H, 64) ||
       make_tmap_2d(&g.tmB[2], w->wv, (int64_t)Hkv * D, H, 64))
     return BLK_ERR_CUDA;
-  g.M = M; g.N = (Hq + 2 * Hkv) * D; g.K = H;
+  g.M = M; g.N = (Hq + 2 * Hkv) * D; g.K = H; g.a_rows = tc_a_box_rows(M);
   g.seg_rows[0] = Hq * D; g.seg_rows[1] = Hkv * D; g.seg_rows[2] = Hkv * D;
   if (c.has_qkv_bias) {
     g.bias[0] = static_cast<const __half*>(w->bq);
@@ -405,7 +409,8 @@ int run_decode_batch(blk_handle h, const blk_weights* w, const void* x, const in
   return run_block_tail(h, w, x, attn16, reinterpret_cast<float*>(base + lay.h32),
                         reinterpret_cast<__half*>(base + lay.hn16),
                         reinterpret_cast<__half*>(base + lay.act16),
-                        reinterpret_cast<float*>(base + lay.part32), out, M, s, tm);
+                        reinterpret_cast<float*>(base + lay.part32), kMaxSplitsBatch, out, M,
+                        s, tm);
 }
 
 }  // namespace

@@ -135,7 +135,10 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
-__device__ __forceinline__ float silu(float z) { return z / (1.0f + __expf(-z)); }
+// silu(z) = z / (1 + e^-z) with the single-path fast divide: an IEEE divide
+// takes a long special-case path for huge or non-finite operands, which rows
+// past the end of a tile can hold.
+__device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 // 8 fp16 values (one 16-byte vector) to fp32.
 __device__ __forceinline__ void h8_to_f32(const uint4& v, float* f) {

@@ -282,11 +282,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int it = 0;
       bool waited = false;
+      const uint32_t a_bytes = (uint32_t)(p.a_rows > 0 ? p.a_rows : BM) * BK * 2;
       for (int u = cl; u < units && !*abort_flag; u += ncl) {
         const int t = u / S, ks = u % S;
         const int mt = (t % mpairs) * 2 + (int)rank, nt = t / mpairs;
         const int m0 = mt * BM, n0 = nt * (EPI == kTcGateUp ? BN / 2 : BN);
         const int kb1 = min(KB, (ks + 1) * KBs);
+        // A tiles that start past M are not loaded: their accumulator rows
+        // are never stored.  Both CTAs' copies complete on the leader's barrier.
+        const bool a_mine = m0 < p.M;
+        const uint32_t tx = 2 * C::kBBytes +
+                            ((t % mpairs) * 2 * BM < p.M ? a_bytes : 0) +
+                            (((t % mpairs) * 2 + 1) * BM < p.M ? a_bytes : 0);
         for (int kb = ks * KBs; kb < kb1; ++kb, ++it) {
           const int s = it % C::kStages;
           if (!mbar_wait(&empty[s], ((it / C::kStages) & 1) ^ 1, p.err)) {
@@ -295,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           uint8_t* sa = smem + (size_t)s * C::kStageBytes;
           uint8_t* sb = sa + C::kABytes;
-          if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * C::kStageBytes);
+          if (rank == 0) mbar_arrive_expect_tx(&full[s], tx);
           const uint32_t fb = cluster_addr(&full[s], 0);
           // this CTA's weight rows: GATEUP leader W_gate, peer W_up (same rows);
           // otherwise rows n0 + rank * BN/2 ...
@@ -321,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             griddep_launch();
             waited = true;
           }
-          tma_load_2d_pair(sa, &p.tmA, kb * BK, m0, fb);
+          if (a_mine) tma_load_2d_pair(sa, &p.tmA, kb * BK, m0, fb);
         }
       }
       if (!waited) {
@@ -519,7 +526,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const int j0 = nt * (BN / 2);
-        for (int c0 = 32 * e; c0 < BN / 2; c0 += 64) {
+        // a warp whose 32 rows all lie past M has nothing to store (its
+        // accumulator rows come from unloaded, arbitrary A rows)
+        for (int c0 = 32 * e; c0 < BN / 2 && row0 < p.M; c0 += 64) {
           tmem_ld32(tbase + c0, v0);
           tmem_ld32(tbase + BN / 2 + c0, v1);
 #pragma unroll
@@ -534,8 +543,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           __half* dst = p.out16 + (size_t)m * p.ldo + j0 + c0;
           if (j0 + c0 + 32 <= p.N) {
             store_h32(dst, v0);
-          } else {
-            for (int i = 0; i < 32 && j0 + c0 + i < p.N; ++i) dst[i] = __float2half_rn(v0[i]);
+          } else {   // ragged last columns (unrolled: v0 stays in registers)
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (j0 + c0 + i < p.N) dst[i] = __float2half_rn(v0[i]);
           }
         }
       } else {
@@ -675,16 +686,21 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restr
   const int64_t n4 = MN / 4;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
        i += (int64_t)gridDim.x * blockDim.x) {
-    float4 q[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      q[j] = j < S ? __ldcg(reinterpret_cast<const float4*>(part + (size_t)j * MN) + i)
-                   : make_float4(0.f, 0.f, 0.f, 0.f);
     const float4 r = __ldg(reinterpret_cast<const float4*>(res32) + i);
-    float4 a = q[0];
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    // splits in ascending order, four loads in flight at a time
+    for (int j0 = 0; j0 < S; j0 += 4) {
+      float4 q[4];
 #pragma unroll
-    for (int j = 1; j < 4; ++j) {
-      if (j < S) { a.x += q[j].x; a.y += q[j].y; a.z += q[j].z; a.w += q[j].w; }
+      for (int j = 0; j < 4; ++j)
+        q[j] = j0 + j < S
+                   ? __ldcg(reinterpret_cast<const float4*>(part + (size_t)(j0 + j) * MN) + i)
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (j0 + j == 0) a = q[0];
+        else if (j0 + j < S) { a.x += q[j].x; a.y += q[j].y; a.z += q[j].z; a.w += q[j].w; }
+      }
     }
     uint2 o;
     *reinterpret_cast<__half2*>(&o.x) = __floats2half2_rn(a.x + r.x, a.y + r.y);

@@ -16,7 +16,9 @@ enum TcEpi {
 };
 
 struct TcGemmParams {
-  CUtensorMap tmA;      // activations [M, K]
+  CUtensorMap tmA;      // activations [M, K], box 64 x a_rows
+  int a_rows;           // rows of tmA's box: 128, or M rounded up to 8 when M < 128
+                        // (0 means 128); an M tile past M is not loaded at all
   CUtensorMap tmB[3];   // weights: QKV q/k/v; GATEUP gate/up; else [0]
   int M, N, K;          // N: output columns (QKV: (Hq+2Hkv)*D; GATEUP: I)
   int seg_rows[3];      // QKV: rows of wq, wk, wv
@@ -46,10 +48,15 @@ struct TcGemmParams {
   // split K (down projection): partials [splits][M][N] fp32, added by
   // launch_splitk_reduce; splits (<= max_splits) is chosen by the launcher
   int splits;
-  int max_splits;       // the partial buffer holds this many (at most 4)
+  int max_splits;       // the partial buffer holds this many
   float* part;
   int* err;
 };
+
+// Rows of the activation box for an M-row operand: all 128 of a tile, or M
+// rounded up to 8 when the operand is one partial tile (the tile rows past it
+// are never stored, so they need not be loaded).
+inline int tc_a_box_rows(int64_t M) { return M >= 128 ? 128 : (int)((M + 7) & ~int64_t(7)); }
 
 // 2-D tensor map over a row-major [rows, K] fp16 matrix, box 64 x box_rows,
 // 128-byte swizzle, zero fill out of bounds.  Returns 0 on success.
