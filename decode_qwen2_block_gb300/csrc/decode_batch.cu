@@ -4,8 +4,10 @@
 // [0, cache_len] of its own cache, slot cache_len holding its new K/V).
 //
 // Split-K flash decode: CTA = (split, kv head g, sequence b), 4 warps.  The
-// split's slots stream through two 64-slot K/V tiles in shared memory
-// (128-bit cp.async copies, 128-byte XOR swizzle, zero fill past the range).
+// split's slots stream through a ring of three 64-slot K/V tiles in shared
+// memory, two copies in flight ahead of the tile being used (128-bit
+// cp.async copies, 128-byte XOR swizzle, zero fill past the range); two CTAs
+// fit on an SM, and the splits are chosen so that every CTA runs in one wave.
 // Each warp owns 16 slots of a tile and runs mma.sync m16n8k16 with the G
 // query heads of kv head g as the rows (padded to 16): S = Q K^T, an online
 // base-2 softmax per head, O += P V; the warps' states are merged pairwise in
@@ -20,6 +22,8 @@ namespace blk {
 namespace {
 
 constexpr int kTileSlots = 64;
+constexpr int kStages = 3;                 // K/V tiles in the ring
+constexpr int kCtasPerSm = 2;              // resident CTAs the shared memory allows
 constexpr int kAWarps = 4;                 // 16 slots of a tile each
 constexpr int kAThreads = kAWarps * 32;
 
@@ -78,8 +82,11 @@ struct BSmem {
   static constexpr int kKVBase = (kKVOff + 1023) / 1024 * 1024;
   static constexpr int kOS = D + 8;                           // merge buffer row stride (floats)
   static constexpr int kBuf = 32 + 16 * kOS;                  // floats: m[16], l[16], o[16][kOS]
-  static constexpr int kMergeOff = kKVBase + 4 * kTile;       // K0 V0 K1 V1
-  static constexpr size_t kBytes = (size_t)kMergeOff + 2 * kBuf * 4 + 1024;
+  static constexpr int kRing = kStages * 2 * kTile;           // (K, V) per stage
+  // the warps' merge buffers reuse the ring once every tile has been used
+  static constexpr int kMergeOff = kKVBase;
+  static constexpr int kBody = kRing > 2 * kBuf * 4 ? kRing : 2 * kBuf * 4;
+  static constexpr size_t kBytes = (size_t)kKVBase + kBody + 1024;
 };
 
 template <int D>
@@ -114,8 +121,8 @@ __global__ void __launch_bounds__(kAThreads)
     if (r < G) v = *reinterpret_cast<const uint4*>(p.q16 + ((size_t)b * p.Hq + g * G + r) * D + ch * 8);
     *reinterpret_cast<uint4*>(qtile + r * Sm::kQStride + ch * 8) = v;
   }
-  auto load_tile = [&](int t) {   // tile t into buffer t & 1
-    const uint32_t kb = kv0 + (t & 1) * 2 * Sm::kTile, vb = kb + Sm::kTile;
+  auto load_tile = [&](int t) {   // tile t into stage t % kStages (one copy group)
+    const uint32_t kb = kv0 + (t % kStages) * 2 * Sm::kTile, vb = kb + Sm::kTile;
     const int64_t cs = j0 + (int64_t)t * kTileSlots;
     for (int i = tid; i < kTileSlots * kCPR; i += kAThreads) {
       const int r = i / kCPR, ch = i % kCPR;
@@ -127,7 +134,14 @@ __global__ void __launch_bounds__(kAThreads)
     }
     cp_async_commit();
   };
-  if (ntiles > 0) load_tile(0);
+  // tiles 0 .. kStages-2 in flight; an empty group stands for a missing tile
+  // so that "tile t has landed" is always "all but the newest kStages-2
+  // groups have completed"
+#pragma unroll
+  for (int s = 0; s < kStages - 1; ++s) {
+    if (s < ntiles) load_tile(s);
+    else cp_async_commit();
+  }
 
   const int grp = lane >> 2, tig = lane & 3;
   float m_r[2] = {-INFINITY, -INFINITY}, l_r[2] = {0.f, 0.f};
@@ -138,14 +152,11 @@ __global__ void __launch_bounds__(kAThreads)
   const float sl2 = p.scale_log2;
 
   for (int t = 0; t < ntiles; ++t) {
-    if (t + 1 < ntiles) {
-      load_tile(t + 1);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
-    __syncthreads();
-    const uint32_t kb = kv0 + (t & 1) * 2 * Sm::kTile, vb = kb + Sm::kTile;
+    cp_async_wait<kStages - 2>();   // tile t has landed (this thread's copies)
+    __syncthreads();                // everyone's copies; stage (t-1) % kStages is free
+    if (t + kStages - 1 < ntiles) load_tile(t + kStages - 1);
+    else cp_async_commit();
+    const uint32_t kb = kv0 + (t % kStages) * 2 * Sm::kTile, vb = kb + Sm::kTile;
     const int64_t cs = j0 + (int64_t)t * kTileSlots;
     const int nval = (int)min((int64_t)kTileSlots, j1 - cs);
     const int r0 = warp * 16;
@@ -218,8 +229,9 @@ __global__ void __launch_bounds__(kAThreads)
         mma16816(O[2 * dp + 1], pa, bv[2], bv[3]);
       }
     }
-    __syncthreads();   // the buffer is refilled by the next iteration's copy
   }
+  cp_async_wait<0>();   // only empty groups can remain
+  __syncthreads();      // every warp is done with the ring: the merge buffers reuse it
 
   // merge the warps' states: 1 -> 0, 3 -> 2, then 2 -> 0
 #pragma unroll
@@ -313,9 +325,11 @@ __global__ void __launch_bounds__(D) decode_attn_merge_kernel(const float* part,
 
 }  // namespace
 
+// As many splits as keep every CTA in one wave of kCtasPerSm CTAs per SM
+// (at least one, at most one per 64-slot tile of the longest sequence).
 int decode_batch_splits(int B, int Hkv, int64_t max_len, int num_sms) {
   const int64_t tiles = (max_len + 1 + kTileSlots - 1) / kTileSlots;
-  int64_t s = (2 * (int64_t)num_sms + (int64_t)B * Hkv - 1) / ((int64_t)B * Hkv);
+  int64_t s = (int64_t)kCtasPerSm * num_sms / ((int64_t)B * Hkv);
   if (s > tiles) s = tiles;
   if (s > 256) s = 256;
   return (int)(s < 1 ? 1 : s);
