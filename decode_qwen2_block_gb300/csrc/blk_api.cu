@@ -22,12 +22,13 @@ constexpr int kMaxPending = 1024;
 enum KernelId {
   kKRmsNorm = 0, kKGemmQKV, kKSplitReduce, kKAttnPrefill, kKGemmO, kKGemmGateUp,
   kKGemmDown, kKDecodeStep, kKAttnMerge, kKLmHead, kKArgmax, kKEmbed, kKDecodeAttnBatch,
-  kKCount
+  kKQkvFinish, kKCount
 };
+static_assert(kKCount <= BLK_N_KERNELS, "kernel id table");
 const char* const kKernelNames[BLK_N_KERNELS] = {
     "rmsnorm_rows", "gemm_qkv", "splitk_reduce", "attn_prefill", "gemm_o",
     "gemm_gateup", "gemm_down", "decode_persistent", "attn_merge", "lm_head", "argmax_reduce",
-    "embed", "decode_attn_batch", "", "", ""};
+    "embed", "decode_attn_batch", "qkv_finish", "", ""};
 }  // namespace
 
 struct blk_handle_s {
@@ -87,6 +88,7 @@ constexpr int kMaxSplits = 4;        // split-K partial buffers of the down proj
 // Batched decode (at most a few hundred rows): the down projection's few
 // N tiles need more K splits to occupy every SM pair.
 constexpr int kMaxSplitsBatch = 16;
+constexpr int kMaxSplitsNorm = 8;    // partials the split-K RMSNorm adds
 
 struct PrefillWs {
   size_t xn16, q16, attn16, h32, hn16, act16, part32, total;
@@ -185,7 +187,7 @@ struct Timer {
 // (shared by prefill, prefill_kv and batched decode).
 int run_block_tail(blk_handle h, const blk_weights* w, const void* x, __half* attn16,
                    float* h32, __half* hn16, __half* act16, float* part32, int max_splits,
-                   void* out, int M, cudaStream_t s, Timer& tm) {
+                   bool split_o, void* out, int M, cudaStream_t s, Timer& tm) {
   const blk_config& c = h->cfg;
   const int H = c.hidden, D = c.head_dim, Hq = c.n_heads, I = c.intermediate;
   // o_proj + residual -> h (fp32)
@@ -195,13 +197,23 @@ int run_block_tail(blk_handle h, const blk_weights* w, const void* x, __half* at
     return BLK_ERR_CUDA;
   go.M = M; go.N = H; go.K = Hq * D; go.a_rows = tc_a_box_rows(M);
   go.res16 = static_cast<const __half*>(x); go.out32 = h32; go.ldo = H;
+  if (split_o) {   // few rows: K splits fill the SM pairs; the partials are
+    go.part = part32;   // summed (with the residual) by the RMSNorm below,
+    go.max_splits = max_splits < kMaxSplitsNorm ? max_splits : kMaxSplitsNorm;   // <= 8 of them
+  }
   go.err = h->status;
   BLK_LAUNCH(tm, kKGemmO, launch_tc_gemm(go, kTcResidF32, h->num_sms, s, true));
 
-  // RMSNorm 2
-  BLK_LAUNCH(tm, kKRmsNorm,
-             launch_rmsnorm_rows(h32, true, static_cast<const __half*>(w->ln2_g), M, H,
-                                 c.rms_eps, hn16, s, true));
+  // RMSNorm 2 (h = the o_proj partials + x when o_proj was split)
+  if (go.splits > 1)
+    BLK_LAUNCH(tm, kKRmsNorm,
+               launch_rmsnorm_splitk(part32, go.splits, static_cast<const __half*>(x), h32,
+                                     static_cast<const __half*>(w->ln2_g), M, H, c.rms_eps,
+                                     hn16, s, true));
+  else
+    BLK_LAUNCH(tm, kKRmsNorm,
+               launch_rmsnorm_rows(h32, true, static_cast<const __half*>(w->ln2_g), M, H,
+                                   c.rms_eps, hn16, s, true));
 
   // gate | up + SwiGLU
   TcGemmParams gu = {};
@@ -306,8 +318,8 @@ int run_prefill(blk_handle h, const blk_weights* w, const void* x,
   if (pa.grid_chunks > 1) BLK_LAUNCH(tm, kKAttnMerge, launch_attn_merge(pa, s, true));
 
   return run_block_tail(h, w, x, attn16, h32, hn16, act16,
-                        reinterpret_cast<float*>(base + lay.part32), kMaxSplits, out, M, s,
-                        tm);
+                        reinterpret_cast<float*>(base + lay.part32), kMaxSplits, false, out, M,
+                        s, tm);
 }
 
 // Batched decode: B sequences, one new token each, caches [B][Hkv][max_ctx][D].
@@ -325,7 +337,9 @@ DecodeBatchWs decode_batch_ws(const blk_config& c, int64_t B, int num_sms) {
   w.h32 = o; o = align_up(o + B * H * 4);
   w.hn16 = o; o = align_up(o + B * H * 2);
   w.act16 = o; o = align_up(o + B * I * 2);
-  w.part32 = o; o = align_up(o + (size_t)kMaxSplitsBatch * B * H * 4);
+  // split-K partials of QKV, o_proj and down (never live at the same time)
+  const size_t nmax = (size_t)(Hq + 2 * c.n_kv_heads) * D > H ? (Hq + 2 * c.n_kv_heads) * D : H;
+  w.part32 = o; o = align_up(o + (size_t)kMaxSplitsBatch * B * nmax * 4);
   const int smax = decode_batch_splits((int)B, c.n_kv_heads, c.max_ctx - 1, num_sms);
   w.apart = o; o = align_up(o + decode_batch_part_bytes((int)B, (int)Hq, (int)D, smax));
   w.total = o;
@@ -388,8 +402,11 @@ int run_decode_batch(blk_handle h, const blk_weights* w, const void* x, const in
   g.max_ctx = c.max_ctx; g.cache_len = 0;
   g.cache_lens = cache_lens;
   g.seq_stride = (int64_t)Hkv * c.max_ctx * D;
+  g.part = reinterpret_cast<float*>(base + lay.part32);   // K splits fill the SM pairs;
+  g.max_splits = kMaxSplitsBatch;                         // qkv_finish applies the epilogue
   g.err = h->status;
   BLK_LAUNCH(tm, kKGemmQKV, launch_tc_gemm(g, kTcQKV, h->num_sms, s, true));
+  if (g.splits > 1) BLK_LAUNCH(tm, kKQkvFinish, launch_qkv_finish(g, s));
 
   // attention of every sequence over its own slots [0, cache_lens[b]]
   DecodeAttnBatchParams pa = {};
@@ -409,8 +426,8 @@ int run_decode_batch(blk_handle h, const blk_weights* w, const void* x, const in
   return run_block_tail(h, w, x, attn16, reinterpret_cast<float*>(base + lay.h32),
                         reinterpret_cast<__half*>(base + lay.hn16),
                         reinterpret_cast<__half*>(base + lay.act16),
-                        reinterpret_cast<float*>(base + lay.part32), kMaxSplitsBatch, out, M,
-                        s, tm);
+                        reinterpret_cast<float*>(base + lay.part32), kMaxSplitsBatch, true, out,
+                        M, s, tm);
 }
 
 }  // namespace

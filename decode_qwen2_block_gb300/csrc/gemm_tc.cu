@@ -246,8 +246,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t rank = cluster_rank();          // 0: the leader, which issues the MMAs
   const int cl = blockIdx.x >> 1, ncl = gridDim.x >> 1;   // pair index and count
   const int mpairs = (p.tiles_m + 1) / 2;
-  // K is split S ways for the down projection (partials added by a second kernel)
-  const int S = EPI == kTcResidOutF16 ? p.splits : 1;
+  // K is split S ways when the launcher chose to (every epilogue but gate/up):
+  // each split writes an fp32 partial that a later kernel adds up
+  const int S = EPI == kTcGateUp ? 1 : p.splits;
   const int KBs = (KB + S - 1) / S;   // K blocks per split
   const int units = mpairs * p.tiles_n * S;
   if (threadIdx.x == 0) {
@@ -402,7 +403,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row0 = mt * BM + q * 32;              // this warp's first row
       const int nrows = min(32, p.M - row0);
 
-      if constexpr (EPI == kTcQKV) {
+      if (S > 1) {
+        // split K: this split's fp32 partial [ks][M][N]; the finishing kernel
+        // (split-K reduction, QKV finish, or RMSNorm of the summed rows) adds
+        // the partials in split order and applies the epilogue
+        if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], (tcount >> 1) & 1, p.err))) {
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        const int n0 = nt * BN;
+        float* part = p.part + (size_t)ks * p.M * p.N;
+#pragma unroll
+        for (int c = 0; c < BN / 64; ++c) {
+          const int c0 = 32 * e + 64 * c;
+          if (row0 >= p.M) break;   // warp-uniform: no row of this warp exists
+          tmem_ld32(tbase + c0, v0);
+          if (n0 + c0 >= p.N) continue;
+          if (staged) {
+            store_rows_staged<false>(
+                stg, v0, lane, reinterpret_cast<uint8_t*>(part + (size_t)row0 * p.N + n0 + c0),
+                (size_t)p.N * 4, nrows);
+            continue;
+          }
+          if (!row_ok) continue;
+          float4* dst = reinterpret_cast<float4*>(part + (size_t)m * p.N + n0 + c0);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            dst[j] = make_float4(v0[4 * j], v0[4 * j + 1], v0[4 * j + 2], v0[4 * j + 3]);
+        }
+      } else if constexpr (EPI == kTcQKV) {
         const int D = p.D, half = D / 2;
         const int n0 = nt * BN;
         const int64_t pos = row_ok ? p.pos[m] : 0;
@@ -585,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             store_h32(p.out16 + o, v);
           }
         };
-        if (S == 1) {
+        {
           // two chunks at a time: their residuals are loaded before the
           // accumulator is read
           bool waited = false;
@@ -628,32 +658,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           if (!waited) break;
-        } else {
-          // split K: this split's fp32 partial; splitk_reduce_kernel adds the
-          // partials in split order, plus the residual
-          if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], (tcount >> 1) & 1, p.err))) {
-            *abort_flag = 1;
-            break;
-          }
-          tc_fence_after();
-          float* part = p.part + (size_t)ks * p.M * p.N;
-#pragma unroll
-          for (int c = 0; c < kCh; ++c) {
-            const int c0 = 32 * e + 64 * c;
-            tmem_ld32(tbase + c0, v0);
-            if (n0 + c0 >= p.N) continue;
-            if (staged) {
-              store_rows_staged<false>(
-                  stg, v0, lane, reinterpret_cast<uint8_t*>(part + (size_t)row0 * p.N + n0 + c0),
-                  (size_t)p.N * 4, nrows);
-              continue;
-            }
-            if (!row_ok) continue;
-            float4* dst = reinterpret_cast<float4*>(part + (size_t)m * p.N + n0 + c0);
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              dst[j] = make_float4(v0[4 * j], v0[4 * j + 1], v0[4 * j + 2], v0[4 * j + 3]);
-          }
         }
       }
       tc_fence_before();
@@ -709,6 +713,83 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restr
   }
 }
 
+// Finishes a K-split QKV projection: element (row m, head hd, pair i) of the
+// fused q | k | v output is the sum of the split partials (split order) plus
+// the bias, rotated by RoPE for q and k heads, then stored exactly as the
+// GEMM's own QKV epilogue does (q16; K/V into the cache slot and k_new/v_new).
+__global__ void __launch_bounds__(64) qkv_finish_kernel(const __grid_constant__ TcGemmParams p) {
+  griddep_wait();
+  griddep_launch();
+  const int hd = blockIdx.x, m = blockIdx.y;
+  const int D = p.D, half = D / 2;
+  const size_t MN = (size_t)p.M * p.N;
+  int local;
+  const __half* bias;
+  if (hd < p.Hq) { bias = p.bias[0]; local = hd; }
+  else if (hd < p.Hq + p.Hkv) { bias = p.bias[1]; local = hd - p.Hq; }
+  else { bias = p.bias[2]; local = hd - p.Hq - p.Hkv; }
+  const bool rope = hd < p.Hq + p.Hkv;
+  const int64_t pos = p.pos[m];
+  const bool pos_ok = pos >= 0 && pos < p.rope_len;
+  if (rope && !pos_ok && threadIdx.x == 0) set_error(p.err, kDevPosition);
+  for (int i = threadIdx.x; i < half; i += blockDim.x) {
+    const size_t c0 = (size_t)m * p.N + (size_t)hd * D + i, c1 = c0 + half;
+    // every split's pair is loaded before any is added (one round trip)
+    constexpr int kMaxS = 16;
+    float qa[kMaxS], qb[kMaxS];
+#pragma unroll
+    for (int s = 0; s < kMaxS; ++s)
+      if (s < p.splits) {
+        qa[s] = __ldcg(p.part + s * MN + c0);
+        qb[s] = __ldcg(p.part + s * MN + c1);
+      }
+    float a = 0.f, b = 0.f;
+#pragma unroll
+    for (int s = 0; s < kMaxS; ++s)
+      if (s < p.splits) {
+        a += qa[s];
+        b += qb[s];
+      }
+    if (bias) {
+      a += __half2float(bias[local * D + i]);
+      b += __half2float(bias[local * D + half + i]);
+    }
+    if (rope && pos_ok) {
+      const float2 cs = p.rope[(size_t)pos * half + i];
+      const float a2 = a * cs.x - b * cs.y, b2 = b * cs.x + a * cs.y;
+      a = a2;
+      b = b2;
+    }
+    const __half ha = __float2half_rn(a), hb = __float2half_rn(b);
+    if (hd < p.Hq) {
+      __half* dst = p.q16 + ((size_t)m * p.Hq + hd) * D;
+      dst[i] = ha;
+      dst[half + i] = hb;
+      continue;
+    }
+    const bool is_k = hd < p.Hq + p.Hkv;
+    __half* cache = is_k ? p.kc : p.vc;
+    __half* nw = is_k ? p.k_new : p.v_new;
+    int64_t slot = p.cache_len + m;
+    if (p.cache_lens) {
+      slot = p.cache_lens[m];
+      cache += (size_t)m * p.seq_stride;
+    }
+    if (slot >= 0 && slot < p.max_ctx) {
+      __half* dst = cache + ((size_t)local * p.max_ctx + slot) * D;
+      dst[i] = ha;
+      dst[half + i] = hb;
+    } else if (i == 0) {
+      set_error(p.err, kDevPosition);
+    }
+    if (nw) {
+      __half* d2 = nw + ((size_t)m * p.Hkv + local) * D;
+      d2[i] = ha;
+      d2[half + i] = hb;
+    }
+  }
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------- host side
@@ -729,6 +810,20 @@ cudaError_t launch_splitk_reduce(const TcGemmParams& p, int num_sms, cudaStream_
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, (const float*)p.part, p.splits, MN,
                             p.res32, p.out16);
+}
+
+cudaError_t launch_qkv_finish(const TcGemmParams& p, cudaStream_t s) {
+  if (p.splits < 2 || p.splits > 16 || !p.part || p.D / 2 > 64) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.Hq + 2 * p.Hkv, p.M);
+  cfg.blockDim = dim3(p.D / 2);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, qkv_finish_kernel, p);
 }
 
 // cuTensorMapEncodeTiled, resolved through the runtime so that the library
@@ -838,7 +933,7 @@ static cudaError_t launch_tc(TcGemmParams& p, int num_sms, cudaStream_t s, bool 
     max_pairs = n < num_sms / 2 ? n : num_sms / 2;
   }
   p.splits = 1;
-  if (EPI == kTcResidOutF16 && p.part) {
+  if (EPI != kTcGateUp && p.part && p.max_splits > 1) {
     // split K so that the units fill the co-resident pairs (8+ K blocks each)
     int S = max_pairs / units;
     S = S < 1 ? 1 : (S > p.max_splits ? p.max_splits : S);

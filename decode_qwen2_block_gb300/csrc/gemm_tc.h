@@ -45,8 +45,10 @@ struct TcGemmParams {
   float* out32;
   __half* out16;
   int ldo;
-  // split K (down projection): partials [splits][M][N] fp32, added by
-  // launch_splitk_reduce; splits (<= max_splits) is chosen by the launcher
+  // split K (any epilogue but gate/up, when part is set and max_splits > 1):
+  // partials [splits][M][N] fp32; splits (<= max_splits) is chosen by the
+  // launcher and the partials are finished by launch_splitk_reduce (down),
+  // launch_qkv_finish (QKV) or launch_rmsnorm_splitk (o_proj)
   int splits;
   int max_splits;       // the partial buffer holds this many
   float* part;
@@ -77,6 +79,9 @@ cudaError_t launch_tc_gemm(TcGemmParams& p, int epi, int num_sms, cudaStream_t s
 // After a down-projection launch with p.splits > 1: out16 = fp16(sum of the
 // split partials + res32) (N a multiple of 4).
 cudaError_t launch_splitk_reduce(const TcGemmParams& p, int num_sms, cudaStream_t s);
+// After a QKV launch with p.splits > 1: sums the partials in split order and
+// applies the QKV epilogue (bias, RoPE, q16 / cache slot / k_new, v_new).
+cudaError_t launch_qkv_finish(const TcGemmParams& p, cudaStream_t s);
 cudaError_t configure_tc_gemm_kernels();
 
 }  // namespace blk

@@ -13,6 +13,11 @@ namespace blk {
 cudaError_t launch_rmsnorm_rows(const void* x, bool x_is_f32, const __half* g,
                                 int rows, int H, float eps, __half* y,
                                 cudaStream_t s, bool pdl);
+// h32 = sum_s part[s] (s ascending) + res16, y = RMSNorm(h32) * g (rows of
+// width H, part = S <= 8 partials [rows][H] fp32).
+cudaError_t launch_rmsnorm_splitk(const float* part, int S, const __half* res16, float* h32,
+                                  const __half* g, int rows, int H, float eps, __half* y,
+                                  cudaStream_t s, bool pdl);
 
 struct PrefillAttnParams {
   CUtensorMap tm_q;   // q [T, Hq, D] viewed as (D, Hq, T), box 64 x 1 x 128, SW128

@@ -95,6 +95,56 @@ __global__ void __launch_bounds__(kNormWarps * 32)
   for (int i = 32 * kMaxVec + lane; i < nv; i += 32) put16<T>(__ldg(xr + i), i, r, g, yr);
 }
 
+// After a K-split o_proj: h = (sum of the split partials, split order) + res16
+// is written to h32 (the residual of the down projection) and y = RMSNorm(h)
+// * g.  One CTA per row, four columns per thread and step; every partial of a
+// step is loaded before any is added, so a row costs one memory round trip
+// per step rather than one per split.
+constexpr int kSplitNormMaxS = 8;
+
+__global__ void __launch_bounds__(1024)
+    rmsnorm_splitk_kernel(const float* __restrict__ part, int S, const __half* __restrict__ res16,
+                          float* __restrict__ h32, const __half* __restrict__ g, int rows, int H,
+                          float eps, __half* __restrict__ y) {
+  __shared__ float red[32];
+  griddep_wait();
+  griddep_launch();
+  const int row = blockIdx.x;
+  const size_t MN = (size_t)rows * H, r0 = (size_t)row * H;
+  float ss = 0.f;
+  for (int i = 4 * threadIdx.x; i < H; i += 4 * blockDim.x) {
+    float4 q[kSplitNormMaxS];
+#pragma unroll
+    for (int s = 0; s < kSplitNormMaxS; ++s)
+      if (s < S) q[s] = __ldcg(reinterpret_cast<const float4*>(part + s * MN + r0 + i));
+    const uint2 rr = __ldg(reinterpret_cast<const uint2*>(res16 + r0 + i));
+    float4 a = q[0];
+#pragma unroll
+    for (int s = 1; s < kSplitNormMaxS; ++s)
+      if (s < S) { a.x += q[s].x; a.y += q[s].y; a.z += q[s].z; a.w += q[s].w; }
+    const float2 ra = __half22float2(*reinterpret_cast<const __half2*>(&rr.x));
+    const float2 rb = __half22float2(*reinterpret_cast<const __half2*>(&rr.y));
+    a.x += ra.x; a.y += ra.y; a.z += rb.x; a.w += rb.y;
+    *reinterpret_cast<float4*>(h32 + r0 + i) = a;
+    ss += a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w;
+  }
+  ss = warp_sum(ss);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  if (lane == 0) red[warp] = ss;
+  __syncthreads();
+  if (warp == 0) {
+    float v = lane < nw ? red[lane] : 0.f;
+    v = warp_sum(v);
+    if (lane == 0) red[0] = v;
+  }
+  __syncthreads();
+  const float r = rsqrtf(red[0] / (float)H + eps);
+  for (int i = 4 * threadIdx.x; i < H; i += 4 * blockDim.x) {   // this thread's own h32 values
+    const float4 a = *reinterpret_cast<const float4*>(h32 + r0 + i);
+    put16<float>(*reinterpret_cast<const uint4*>(&a), i / 4, r, g, y + r0);
+  }
+}
+
 static cudaLaunchConfig_t make_cfg(dim3 grid, dim3 block, size_t smem,
                                    cudaStream_t s, bool pdl,
                                    cudaLaunchAttribute* attr) {
@@ -121,6 +171,18 @@ cudaError_t launch_rmsnorm_rows(const void* x, bool x_is_f32, const __half* g,
                               static_cast<const float*>(x), g, rows, H, eps, y);
   return cudaLaunchKernelEx(&cfg, rmsnorm_rows_kernel<__half>,
                             static_cast<const __half*>(x), g, rows, H, eps, y);
+}
+
+cudaError_t launch_rmsnorm_splitk(const float* part, int S, const __half* res16, float* h32,
+                                  const __half* g, int rows, int H, float eps, __half* y,
+                                  cudaStream_t s, bool pdl) {
+  if (S < 1 || S > kSplitNormMaxS || H % 4) return cudaErrorInvalidValue;
+  int threads = (H / 4 + 31) / 32 * 32;
+  if (threads > 1024) threads = 1024;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = make_cfg(dim3(rows), dim3(threads), 0, s, pdl, attr);
+  return cudaLaunchKernelEx(&cfg, rmsnorm_splitk_kernel, part, S, res16, h32, g, rows, H, eps,
+                            y);
 }
 
 }  // namespace blk
