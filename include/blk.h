@@ -245,8 +245,9 @@ int blk_set_trace(blk_handle h, void* device_buffer, size_t bytes);
  *   k_cache, v_cache  device fp16 [B, n_kv_heads, max_ctx, head_dim]
  *   out      device fp16 [B, hidden]; k_new, v_new  [B, n_kv_heads, head_dim]
  *            or NULL
- * Equals blk_decode on each sequence within the tolerance (same kernels for
- * the projections, a split-K flash-decode attention).  A cache length outside
+ * Equals blk_decode on each sequence within the tolerance (the projections
+ * run on the tcgen05 GEMMs with B rows and K split across the SM pairs; the
+ * attention is a split-K flash decode per sequence).  A cache length outside
  * [0, max_ctx) skips that sequence's K/V write and attention, and reports
  * BLK_ERR_POSITION from the next blk_check.  Returns BLK_OK, BLK_ERR_NULL,
  * BLK_ERR_ALIGN, BLK_ERR_SHAPE (B outside [1, 4096], more than 16 query heads
