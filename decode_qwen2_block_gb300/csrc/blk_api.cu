@@ -123,11 +123,12 @@ int check_weights(const blk_config& c, const blk_weights* w) {
     if (!m) return BLK_ERR_NULL;
     if (!aligned(m, 16)) return BLK_ERR_ALIGN;
   }
+  // gains and biases are read as 16-byte vectors, like every other operand
   if (!w->ln1_g || !w->ln2_g) return BLK_ERR_NULL;
-  if (!aligned(w->ln1_g, 2) || !aligned(w->ln2_g, 2)) return BLK_ERR_ALIGN;
+  if (!aligned(w->ln1_g, 16) || !aligned(w->ln2_g, 16)) return BLK_ERR_ALIGN;
   if (c.has_qkv_bias) {
     if (!w->bq || !w->bk || !w->bv) return BLK_ERR_NULL;
-    if (!aligned(w->bq, 2) || !aligned(w->bk, 2) || !aligned(w->bv, 2))
+    if (!aligned(w->bq, 16) || !aligned(w->bk, 16) || !aligned(w->bv, 16))
       return BLK_ERR_ALIGN;
   }
   return BLK_OK;
@@ -668,7 +669,7 @@ int blk_lm_head(blk_handle h, const void* x, int64_t T, const void* norm_g, cons
                 void* stream) {
   if (!h) return BLK_ERR_NULL;
   if (!x || !norm_g || !w_lm || !tokens || !ws) return BLK_ERR_NULL;
-  if (!aligned(x, 16) || !aligned(w_lm, 16) || !aligned(norm_g, 2) || !aligned(tokens, 8) ||
+  if (!aligned(x, 16) || !aligned(w_lm, 16) || !aligned(norm_g, 16) || !aligned(tokens, 8) ||
       !aligned(ws, 16) || (logits && !aligned(logits, 4)))
     return BLK_ERR_ALIGN;
   const int H = h->cfg.hidden;

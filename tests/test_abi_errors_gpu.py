@@ -47,6 +47,11 @@ def test_argument_errors(setup):
     w = blk.Block.weights(db.w_dev)
     w.wq = None
     assert _prefill(db, P(x), P(pos), 8, P(kc), P(vc), P(out), w=w) == blk.BLK_ERR_NULL
+    # gains (and biases) are read as 16-byte vectors: a 2-byte-aligned gain is refused
+    for name in ("ln1_g", "ln2_g"):
+        w = blk.Block.weights(db.w_dev)
+        setattr(w, name, db.w_dev[name].data_ptr() + 2)
+        assert _prefill(db, P(x), P(pos), 8, P(kc), P(vc), P(out), w=w) == blk.BLK_ERR_ALIGN
     h = db.block.handle
     stream = torch.cuda.current_stream().cuda_stream
     ws, nb = db.ws.data_ptr(), db.ws.numel()

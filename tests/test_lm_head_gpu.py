@@ -137,6 +137,10 @@ def test_lm_head_argument_errors():
     rc = blk.blk_lm_head(b.handle, x.data_ptr(), 1, g.data_ptr(), W.data_ptr() + 2, 100, None,
                          tokens.data_ptr(), ws.data_ptr(), ws.numel(), 0)
     assert rc == blk.BLK_ERR_ALIGN
+    gp = torch.zeros(s.hidden + 8, dtype=torch.float16, device="cuda")
+    rc = blk.blk_lm_head(b.handle, x.data_ptr(), 1, gp.data_ptr() + 2, W.data_ptr(), 100, None,
+                         tokens.data_ptr(), ws.data_ptr(), ws.numel(), 0)
+    assert rc == blk.BLK_ERR_ALIGN
 
 
 def test_lm_head_hidden_4096_three_stage_ring():
