@@ -419,6 +419,7 @@ int run_decode_batch(blk_handle h, const blk_weights* w, const void* x, const in
   pa.max_ctx = c.max_ctx;
   pa.scale_log2 = (float)(1.4426950408889634 / sqrt((double)D));
   pa.nsplit = decode_batch_splits(M, Hkv, max_cache_len, h->num_sms);
+  pa.deep = decode_batch_deep(M, Hkv, h->num_sms) ? 1 : 0;
   pa.part = reinterpret_cast<float*>(base + lay.apart);
   pa.attn16 = attn16;
   pa.err = h->status;

@@ -4,10 +4,12 @@
 // [0, cache_len] of its own cache, slot cache_len holding its new K/V).
 //
 // Split-K flash decode: CTA = (split, kv head g, sequence b), 4 warps.  The
-// split's slots stream through a ring of three 64-slot K/V tiles in shared
-// memory, two copies in flight ahead of the tile being used (128-bit
-// cp.async copies, 128-byte XOR swizzle, zero fill past the range); two CTAs
-// fit on an SM, and the splits are chosen so that every CTA runs in one wave.
+// split's slots stream through a ring of 64-slot K/V tiles in shared memory
+// (128-bit cp.async copies, 128-byte XOR swizzle, zero fill past the range).
+// Two forms: when the (sequence, kv head) pairs are at most one per SM, one
+// CTA per SM with a five-stage ring (four tiles in flight); otherwise two
+// CTAs per SM with three stages.  The splits are chosen so that every CTA
+// runs in one wave.
 // Each warp owns 16 slots of a tile and runs mma.sync m16n8k16 with the G
 // query heads of kv head g as the rows (padded to 16): S = Q K^T, an online
 // base-2 softmax per head, O += P V; the warps' states are merged pairwise in
@@ -22,8 +24,8 @@ namespace blk {
 namespace {
 
 constexpr int kTileSlots = 64;
-constexpr int kStages = 3;                 // K/V tiles in the ring
-constexpr int kCtasPerSm = 2;              // resident CTAs the shared memory allows
+constexpr int kStagesDeep = 5;             // one CTA per SM
+constexpr int kStagesPair = 3;             // two CTAs per SM (at D = 128)
 constexpr int kAWarps = 4;                 // 16 slots of a tile each
 constexpr int kAThreads = kAWarps * 32;
 
@@ -73,7 +75,7 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-template <int D>
+template <int D, int kStages>
 struct BSmem {
   static constexpr int kQStride = D + 8;                      // halves (conflict-free ldmatrix)
   static constexpr int kTile = kTileSlots * D * 2;            // K or V tile bytes
@@ -89,10 +91,10 @@ struct BSmem {
   static constexpr size_t kBytes = (size_t)kKVBase + kBody + 1024;
 };
 
-template <int D>
+template <int D, int kStages>
 __global__ void __launch_bounds__(kAThreads)
     decode_attn_batch_kernel(const __grid_constant__ DecodeAttnBatchParams p) {
-  using Sm = BSmem<D>;
+  using Sm = BSmem<D, kStages>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -325,11 +327,15 @@ __global__ void __launch_bounds__(D) decode_attn_merge_kernel(const float* part,
 
 }  // namespace
 
-// As many splits as keep every CTA in one wave of kCtasPerSm CTAs per SM
-// (at least one, at most one per 64-slot tile of the longest sequence).
+bool decode_batch_deep(int B, int Hkv, int num_sms) { return (int64_t)B * Hkv <= num_sms; }
+
+// As many splits as keep every CTA in one wave (one CTA per SM in the deep
+// form, two otherwise); at least one, at most one per 64-slot tile of the
+// longest sequence.
 int decode_batch_splits(int B, int Hkv, int64_t max_len, int num_sms) {
   const int64_t tiles = (max_len + 1 + kTileSlots - 1) / kTileSlots;
-  int64_t s = (int64_t)kCtasPerSm * num_sms / ((int64_t)B * Hkv);
+  const int per_sm = decode_batch_deep(B, Hkv, num_sms) ? 1 : 2;
+  int64_t s = (int64_t)per_sm * num_sms / ((int64_t)B * Hkv);
   if (s > tiles) s = tiles;
   if (s > 256) s = 256;
   return (int)(s < 1 ? 1 : s);
@@ -339,19 +345,19 @@ size_t decode_batch_part_bytes(int B, int Hq, int D, int nsplit) {
   return nsplit > 1 ? (size_t)B * Hq * nsplit * (D + 2) * 4 : 0;
 }
 
-template <int D>
+template <int D, int kStages>
 static cudaError_t launch_attn_batch_d(const DecodeAttnBatchParams& p, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.nsplit, p.Hkv, p.B);
   cfg.blockDim = dim3(kAThreads);
-  cfg.dynamicSmemBytes = BSmem<D>::kBytes;
+  cfg.dynamicSmemBytes = BSmem<D, kStages>::kBytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_attn_batch_kernel<D>, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_attn_batch_kernel<D, kStages>, p);
   if (e != cudaSuccess || p.nsplit == 1) return e;
   cudaLaunchConfig_t mc = {};
   mc.gridDim = dim3(p.B * p.Hq);
@@ -366,18 +372,28 @@ static cudaError_t launch_attn_batch_d(const DecodeAttnBatchParams& p, cudaStrea
 cudaError_t launch_decode_attn_batch(const DecodeAttnBatchParams& p, cudaStream_t s) {
   if (p.nsplit > 1 && !p.part) return cudaErrorInvalidValue;
   if (p.Hq / p.Hkv > 16) return cudaErrorInvalidValue;   // the rows of one MMA tile
-  if (p.D == 128) return launch_attn_batch_d<128>(p, s);
-  if (p.D == 64) return launch_attn_batch_d<64>(p, s);
+  if (p.D == 128)
+    return p.deep ? launch_attn_batch_d<128, kStagesDeep>(p, s)
+                  : launch_attn_batch_d<128, kStagesPair>(p, s);
+  if (p.D == 64)
+    return p.deep ? launch_attn_batch_d<64, kStagesDeep>(p, s)
+                  : launch_attn_batch_d<64, kStagesPair>(p, s);
   return cudaErrorInvalidValue;
 }
 
+template <int D, int kStages>
+static cudaError_t configure_one() {
+  return cudaFuncSetAttribute(decode_attn_batch_kernel<D, kStages>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)BSmem<D, kStages>::kBytes);
+}
+
 cudaError_t configure_decode_attn_batch() {
-  cudaError_t e = cudaFuncSetAttribute(decode_attn_batch_kernel<128>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)BSmem<128>::kBytes);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(decode_attn_batch_kernel<64>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)BSmem<64>::kBytes);
+  cudaError_t e = configure_one<128, kStagesDeep>();
+  if (e == cudaSuccess) e = configure_one<128, kStagesPair>();
+  if (e == cudaSuccess) e = configure_one<64, kStagesDeep>();
+  if (e == cudaSuccess) e = configure_one<64, kStagesPair>();
+  return e;
 }
 
 }  // namespace blk

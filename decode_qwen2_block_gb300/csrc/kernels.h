@@ -58,10 +58,12 @@ struct DecodeAttnBatchParams {
   int64_t max_ctx;
   float scale_log2;
   int nsplit;                 // splits of each sequence's slots (decode_batch_splits)
+  int deep;                   // decode_batch_deep: one CTA per SM, five-stage ring
   float* part;                // [B][Hq][nsplit][D + 2] when nsplit > 1
   __half* attn16;             // [B, Hq * D]
   int* err;
 };
+bool decode_batch_deep(int B, int Hkv, int num_sms);
 int decode_batch_splits(int B, int Hkv, int64_t max_len, int num_sms);
 size_t decode_batch_part_bytes(int B, int Hq, int D, int nsplit);
 cudaError_t launch_decode_attn_batch(const DecodeAttnBatchParams& p, cudaStream_t s);
