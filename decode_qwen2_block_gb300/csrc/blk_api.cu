@@ -411,9 +411,14 @@ int run_decode_batch(blk_handle h, const blk_weights* w, const void* x, const in
 
   // attention of every sequence over its own slots [0, cache_lens[b]]
   DecodeAttnBatchParams pa = {};
+  {
+    const int64_t kd[3] = {D, c.max_ctx, (int64_t)M * Hkv};
+    const int64_t ks[2] = {(int64_t)D * 2, c.max_ctx * D * 2};
+    const int kb[3] = {64, 64, 1};
+    if (make_tmap_3d(&pa.tm_k, k_cache, kd, ks, kb) || make_tmap_3d(&pa.tm_v, v_cache, kd, ks, kb))
+      return BLK_ERR_CUDA;
+  }
   pa.q16 = q16;
-  pa.kc = static_cast<const __half*>(k_cache);
-  pa.vc = static_cast<const __half*>(v_cache);
   pa.cache_lens = cache_lens;
   pa.B = M; pa.Hq = Hq; pa.Hkv = Hkv; pa.D = D;
   pa.max_ctx = c.max_ctx;

@@ -7,9 +7,9 @@
 // split's slots stream through a ring of 64-slot K/V tiles in shared memory
 // (128-bit cp.async copies, 128-byte XOR swizzle, zero fill past the range).
 // Two forms: when the (sequence, kv head) pairs are at most one per SM, one
-// CTA per SM with a five-stage ring (four tiles in flight); otherwise two
-// CTAs per SM with three stages.  The splits are chosen so that every CTA
-// runs in one wave.
+// CTA per SM of 8 warps that use two tiles at a time, with three such pairs
+// in the ring (four tiles in flight); otherwise two CTAs per SM of 4 warps
+// with three tiles.  The splits are chosen so that every CTA runs in one wave.
 // Each warp owns 16 slots of a tile and runs mma.sync m16n8k16 with the G
 // query heads of kv head g as the rows (padded to 16): S = Q K^T, an online
 // base-2 softmax per head, O += P V; the warps' states are merged pairwise in
@@ -24,10 +24,10 @@ namespace blk {
 namespace {
 
 constexpr int kTileSlots = 64;
-constexpr int kStagesDeep = 5;             // one CTA per SM
-constexpr int kStagesPair = 3;             // two CTAs per SM (at D = 128)
-constexpr int kAWarps = 4;                 // 16 slots of a tile each
-constexpr int kAThreads = kAWarps * 32;
+// The ring holds kGroups copy groups of kTPG tiles; 4 * kTPG warps use one
+// group at a time, four warps (16 slots each) per tile.
+constexpr int kGroupsDeep = 3, kTpgDeep = 2;   // one CTA per SM, 8 warps
+constexpr int kGroupsPair = 3, kTpgPair = 1;   // two CTAs per SM (at D = 128), 4 warps
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t* r) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
@@ -61,40 +61,52 @@ __device__ __forceinline__ uint32_t tile_addr(uint32_t base, int r, int ch) {
   return base + (ch >> 3) * (kTileSlots * 128) + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
 }
 
-// 16 bytes global -> shared; zeros instead when !valid (nothing is read).
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-               "r"(valid ? 16 : 0)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+// One box (x, y, z) of a 3-D tensor map into shared memory; completion is
+// counted on `bar` as transaction bytes.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            int z, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
 }
 
-template <int D, int kStages>
+__device__ __forceinline__ void st_shared_zero16(uint32_t addr) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
+}
+
+// Orders this thread's generic-proxy shared-memory accesses before later
+// tensor (async-proxy) copies into the same memory.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+template <int D, int kGroups, int kTPG>
 struct BSmem {
   static constexpr int kQStride = D + 8;                      // halves (conflict-free ldmatrix)
   static constexpr int kTile = kTileSlots * D * 2;            // K or V tile bytes
   static constexpr int kQOff = 0;
   static constexpr int kKVOff = 16 * kQStride * 2;            // multiple of 16... rounded below
   static constexpr int kKVBase = (kKVOff + 1023) / 1024 * 1024;
+  static constexpr int kBarOff = kKVBase - 64;                // kGroups mbarriers
+  static_assert(kKVOff <= kBarOff && kGroups <= 8, "barrier area");
   static constexpr int kOS = D + 8;                           // merge buffer row stride (floats)
   static constexpr int kBuf = 32 + 16 * kOS;                  // floats: m[16], l[16], o[16][kOS]
-  static constexpr int kRing = kStages * 2 * kTile;           // (K, V) per stage
-  // the warps' merge buffers reuse the ring once every tile has been used
+  static constexpr int kRing = kGroups * kTPG * 2 * kTile;   // (K, V) per tile
+  // the warps' merge buffers (half the warps' states at once) reuse the
+  // ring once every tile has been used
   static constexpr int kMergeOff = kKVBase;
-  static constexpr int kBody = kRing > 2 * kBuf * 4 ? kRing : 2 * kBuf * 4;
+  static constexpr int kMergeBytes = 2 * kTPG * kBuf * 4;
+  static constexpr int kBody = kRing > kMergeBytes ? kRing : kMergeBytes;
   static constexpr size_t kBytes = (size_t)kKVBase + kBody + 1024;
 };
 
-template <int D, int kStages>
-__global__ void __launch_bounds__(kAThreads)
+template <int D, int kGroups, int kTPG>
+__global__ void __launch_bounds__(128 * kTPG)
     decode_attn_batch_kernel(const __grid_constant__ DecodeAttnBatchParams p) {
-  using Sm = BSmem<D, kStages>;
+  using Sm = BSmem<D, kGroups, kTPG>;
+  constexpr int kWarps = 4 * kTPG, kThreads = 32 * kWarps;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -102,8 +114,10 @@ __global__ void __launch_bounds__(kAThreads)
   float* bufs = reinterpret_cast<float*>(smem + Sm::kMergeOff);
   const uint32_t kv0 = smem_u32(smem + Sm::kKVBase);
 
-  griddep_wait();    // q, the caches' new slots and cache_lens come from earlier kernels
-  griddep_launch();
+  // Before griddepcontrol.wait only what the previous kernel of the chain
+  // (qkv_finish) does not write may be read: everything older is complete
+  // when this kernel starts, so the cache lengths and the history slots
+  // below L are final; q and slot L are not.
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int sp = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int G = p.Hq / p.Hkv;
@@ -111,39 +125,54 @@ __global__ void __launch_bounds__(kAThreads)
   const int64_t n = (L >= 0 && L < p.max_ctx) ? L + 1 : 0;   // slots [0, L]
   const int64_t j0 = (int64_t)sp * n / p.nsplit, j1 = (int64_t)(sp + 1) * n / p.nsplit;
   const int ntiles = (int)((j1 - j0 + kTileSlots - 1) / kTileSlots);
-  const size_t head = ((size_t)b * p.Hkv + g) * (size_t)p.max_ctx;
-  const __half* kc = p.kc + head * D;
-  const __half* vc = p.vc + head * D;
-  constexpr int kCPR = D / 8;   // 16-byte chunks per row
+  const int ngroups = (ntiles + kTPG - 1) / kTPG;
+  const int zh = b * p.Hkv + g;   // this (sequence, kv head) in the tensor maps
+  constexpr int kCPR = D / 8;     // 16-byte chunks per row
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Sm::kBarOff);   // [kGroups]
+  // Tile slot u of the ring: K at kv0 + u * 2 * kTile, V right after it, each
+  // [D/64][64 slots][128 B] with the 128-byte swizzle (the tensor copies' own
+  // layout).  Thread 0 loads group gi (tiles gi*kTPG..) into ring group
+  // gi % kGroups, completing on full[gi % kGroups].  Slots past the split's
+  // end inside a tile are real cache rows (or zeros past max_ctx); they are
+  // masked out below.
+  auto group_nt = [&](int gi) { return min(kTPG, ntiles - gi * kTPG); };
+  auto load_group = [&](int gi) {
+    const int nt = group_nt(gi);
+    uint64_t* bar = &full[gi % kGroups];
+    fence_proxy_async_smem();   // the previous use of this group came first
+    mbar_arrive_expect_tx(bar, (uint32_t)(nt * 2 * Sm::kTile));
+    for (int jt = 0; jt < nt; ++jt) {
+      const uint32_t kb = kv0 + ((gi % kGroups) * kTPG + jt) * 2 * Sm::kTile, vb = kb + Sm::kTile;
+      const int y = (int)(j0 + (int64_t)(gi * kTPG + jt) * kTileSlots);
+#pragma unroll
+      for (int h = 0; h < D / 64; ++h) {
+        tma_load_3d(kb + h * (kTileSlots * 128), &p.tm_k, h * 64, y, zh, bar);
+        tma_load_3d(vb + h * (kTileSlots * 128), &p.tm_v, h * 64, y, zh, bar);
+      }
+    }
+  };
+  int issued = 0;   // thread 0: groups loaded so far
+  if (tid == 0) {
+    for (int s = 0; s < kGroups; ++s) mbar_init(&full[s], 1);
+    fence_mbar_init();
+    // groups whose boxes end before slot L, ahead of the wait
+    while (issued < kGroups - 1 && issued < ngroups &&
+           j0 + (int64_t)(issued * kTPG + group_nt(issued)) * kTileSlots <= L)
+      load_group(issued++);
+  }
+  griddep_wait();    // q and the new slot L come from the previous kernel
+  griddep_launch();
 
   // Q tile: rows 0..G-1 = query heads g*G.., rows G..15 zero
-  for (int i = tid; i < 16 * kCPR; i += kAThreads) {
+  for (int i = tid; i < 16 * kCPR; i += kThreads) {
     const int r = i / kCPR, ch = i % kCPR;
     uint4 v = make_uint4(0, 0, 0, 0);
     if (r < G) v = *reinterpret_cast<const uint4*>(p.q16 + ((size_t)b * p.Hq + g * G + r) * D + ch * 8);
     *reinterpret_cast<uint4*>(qtile + r * Sm::kQStride + ch * 8) = v;
   }
-  auto load_tile = [&](int t) {   // tile t into stage t % kStages (one copy group)
-    const uint32_t kb = kv0 + (t % kStages) * 2 * Sm::kTile, vb = kb + Sm::kTile;
-    const int64_t cs = j0 + (int64_t)t * kTileSlots;
-    for (int i = tid; i < kTileSlots * kCPR; i += kAThreads) {
-      const int r = i / kCPR, ch = i % kCPR;
-      const int64_t j = cs + r;
-      const bool valid = j < j1;
-      const size_t off = (size_t)(valid ? j : j0) * D + ch * 8;
-      cp_async16(tile_addr(kb, r, ch), kc + off, valid);
-      cp_async16(tile_addr(vb, r, ch), vc + off, valid);
-    }
-    cp_async_commit();
-  };
-  // tiles 0 .. kStages-2 in flight; an empty group stands for a missing tile
-  // so that "tile t has landed" is always "all but the newest kStages-2
-  // groups have completed"
-#pragma unroll
-  for (int s = 0; s < kStages - 1; ++s) {
-    if (s < ntiles) load_tile(s);
-    else cp_async_commit();
-  }
+  if (tid == 0)
+    for (; issued < kGroups - 1 && issued < ngroups; ++issued) load_group(issued);
+  __syncthreads();   // the barriers are initialised before anyone waits on them
 
   const int grp = lane >> 2, tig = lane & 3;
   float m_r[2] = {-INFINITY, -INFINITY}, l_r[2] = {0.f, 0.f};
@@ -153,15 +182,23 @@ __global__ void __launch_bounds__(kAThreads)
   const uint32_t qbase = smem_u32(qtile);
   const float sl2 = p.scale_log2;
 
-  for (int t = 0; t < ntiles; ++t) {
-    cp_async_wait<kStages - 2>();   // tile t has landed (this thread's copies)
-    __syncthreads();                // everyone's copies; stage (t-1) % kStages is free
-    if (t + kStages - 1 < ntiles) load_tile(t + kStages - 1);
-    else cp_async_commit();
-    const uint32_t kb = kv0 + (t % kStages) * 2 * Sm::kTile, vb = kb + Sm::kTile;
-    const int64_t cs = j0 + (int64_t)t * kTileSlots;
-    const int nval = (int)min((int64_t)kTileSlots, j1 - cs);
-    const int r0 = warp * 16;
+  bool aborted = false;
+  int gi = 0;
+  for (; gi < ngroups; ++gi) {
+    // group gi has landed (bounded wait); the block agrees on giving up, and
+    // the barrier also frees group (gi-1) % kGroups for the next copy
+    const bool ok = mbar_wait(&full[gi % kGroups], (uint32_t)(gi / kGroups) & 1u, p.err);
+    if (__syncthreads_or(!ok)) {
+      aborted = true;
+      break;
+    }
+    if (tid == 0 && gi + kGroups - 1 < ngroups) load_group(gi + kGroups - 1);
+    // this warp: tile gi*kTPG + warp/4 of the group, its slots 16*(warp%4)..
+    const int jt = warp >> 2;
+    const uint32_t kb = kv0 + ((gi % kGroups) * kTPG + jt) * 2 * Sm::kTile, vb = kb + Sm::kTile;
+    const int64_t cs = j0 + (int64_t)(gi * kTPG + jt) * kTileSlots;
+    const int nval = (int)max((int64_t)0, min((int64_t)kTileSlots, j1 - cs));
+    const int r0 = (warp & 3) * 16;
     if (r0 < nval) {
       // S = Q K^T for this warp's 16 slots (two n-tiles of 8)
       float S[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -221,6 +258,16 @@ __global__ void __launch_bounds__(kAThreads)
         O[dn][2] *= corr[1];
         O[dn][3] *= corr[1];
       }
+      if (r0 + 16 > nval) {
+        // slots past the split's end: their P is 0, but their V rows (other
+        // slots' data) could hold non-finite values, so this warp zeroes its own
+        for (int i = lane; i < 16 * kCPR; i += 32) {
+          const int r = r0 + i / kCPR;
+          if (r >= nval) st_shared_zero16(tile_addr(vb, r, i % kCPR));
+        }
+        fence_proxy_async_smem();   // before a later tensor copy into this tile
+        __syncwarp();
+      }
 #pragma unroll
       for (int dp = 0; dp < D / 16; ++dp) {   // O += P V
         uint32_t bv[4];
@@ -232,10 +279,17 @@ __global__ void __launch_bounds__(kAThreads)
       }
     }
   }
-  cp_async_wait<0>();   // only empty groups can remain
+  if (aborted) {
+    // the copies already issued (groups gi .. gi + kGroups - 2) land before
+    // the CTA exits; the status word already holds the timeout
+    if (tid == 0)
+      for (int g2 = gi; g2 < ngroups && g2 < gi + kGroups - 1; ++g2)
+        mbar_wait(&full[g2 % kGroups], (uint32_t)(g2 / kGroups) & 1u, nullptr);
+    return;
+  }
   __syncthreads();      // every warp is done with the ring: the merge buffers reuse it
 
-  // merge the warps' states: 1 -> 0, 3 -> 2, then 2 -> 0
+  // merge the warps' states in a fixed tree (1 -> 0, 3 -> 2, ..., then 2 -> 0, ...)
 #pragma unroll
   for (int h2 = 0; h2 < 2; ++h2) {
     l_r[h2] += __shfl_xor_sync(0xffffffffu, l_r[h2], 1);
@@ -274,20 +328,19 @@ __global__ void __launch_bounds__(kAThreads)
       m_r[h2] = Mx;
     }
   };
-  if (warp & 1) put(bufs + (warp >> 1) * kBuf);
-  __syncthreads();
-  if (!(warp & 1)) merge_from(bufs + (warp >> 1) * kBuf);
-  __syncthreads();
-  if (warp == 2) put(bufs + kBuf);
-  __syncthreads();
-  if (warp == 0) {
-    merge_from(bufs + kBuf);
-    put(bufs);
+#pragma unroll
+  for (int d = 1; d < kWarps; d *= 2) {   // warp w with w % 2d == d hands over to w - d
+    float* bf = bufs + (warp / (2 * d)) * kBuf;
+    if (warp % (2 * d) == d) put(bf);
+    __syncthreads();
+    if (warp % (2 * d) == 0) merge_from(bf);
+    __syncthreads();
   }
+  if (warp == 0) put(bufs);
   __syncthreads();
 
   // rows < G: attn (one split) or this split's fp32 partial
-  for (int i = tid; i < G * D; i += kAThreads) {
+  for (int i = tid; i < G * D; i += kThreads) {
     const int row = i / D, d = i % D;
     const float m = bufs[row], l = bufs[16 + row], o = bufs[32 + row * kOS + d];
     const size_t bh = (size_t)b * p.Hq + g * G + row;
@@ -345,19 +398,19 @@ size_t decode_batch_part_bytes(int B, int Hq, int D, int nsplit) {
   return nsplit > 1 ? (size_t)B * Hq * nsplit * (D + 2) * 4 : 0;
 }
 
-template <int D, int kStages>
+template <int D, int kGroups, int kTPG>
 static cudaError_t launch_attn_batch_d(const DecodeAttnBatchParams& p, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.nsplit, p.Hkv, p.B);
-  cfg.blockDim = dim3(kAThreads);
-  cfg.dynamicSmemBytes = BSmem<D, kStages>::kBytes;
+  cfg.blockDim = dim3(128 * kTPG);
+  cfg.dynamicSmemBytes = BSmem<D, kGroups, kTPG>::kBytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_attn_batch_kernel<D, kStages>, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_attn_batch_kernel<D, kGroups, kTPG>, p);
   if (e != cudaSuccess || p.nsplit == 1) return e;
   cudaLaunchConfig_t mc = {};
   mc.gridDim = dim3(p.B * p.Hq);
@@ -373,26 +426,26 @@ cudaError_t launch_decode_attn_batch(const DecodeAttnBatchParams& p, cudaStream_
   if (p.nsplit > 1 && !p.part) return cudaErrorInvalidValue;
   if (p.Hq / p.Hkv > 16) return cudaErrorInvalidValue;   // the rows of one MMA tile
   if (p.D == 128)
-    return p.deep ? launch_attn_batch_d<128, kStagesDeep>(p, s)
-                  : launch_attn_batch_d<128, kStagesPair>(p, s);
+    return p.deep ? launch_attn_batch_d<128, kGroupsDeep, kTpgDeep>(p, s)
+                  : launch_attn_batch_d<128, kGroupsPair, kTpgPair>(p, s);
   if (p.D == 64)
-    return p.deep ? launch_attn_batch_d<64, kStagesDeep>(p, s)
-                  : launch_attn_batch_d<64, kStagesPair>(p, s);
+    return p.deep ? launch_attn_batch_d<64, kGroupsDeep, kTpgDeep>(p, s)
+                  : launch_attn_batch_d<64, kGroupsPair, kTpgPair>(p, s);
   return cudaErrorInvalidValue;
 }
 
-template <int D, int kStages>
+template <int D, int kGroups, int kTPG>
 static cudaError_t configure_one() {
-  return cudaFuncSetAttribute(decode_attn_batch_kernel<D, kStages>,
+  return cudaFuncSetAttribute(decode_attn_batch_kernel<D, kGroups, kTPG>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)BSmem<D, kStages>::kBytes);
+                              (int)BSmem<D, kGroups, kTPG>::kBytes);
 }
 
 cudaError_t configure_decode_attn_batch() {
-  cudaError_t e = configure_one<128, kStagesDeep>();
-  if (e == cudaSuccess) e = configure_one<128, kStagesPair>();
-  if (e == cudaSuccess) e = configure_one<64, kStagesDeep>();
-  if (e == cudaSuccess) e = configure_one<64, kStagesPair>();
+  cudaError_t e = configure_one<128, kGroupsDeep, kTpgDeep>();
+  if (e == cudaSuccess) e = configure_one<128, kGroupsPair, kTpgPair>();
+  if (e == cudaSuccess) e = configure_one<64, kGroupsDeep, kTpgDeep>();
+  if (e == cudaSuccess) e = configure_one<64, kGroupsPair, kTpgPair>();
   return e;
 }
 

@@ -50,15 +50,15 @@ cudaError_t configure_prefill_attn();
 // row each, caches [B][Hkv][max_ctx][D], slots [0, cache_lens[b]] (the last
 // one already holding the new K/V).
 struct DecodeAttnBatchParams {
+  CUtensorMap tm_k;           // K cache viewed as (D, max_ctx, B * Hkv), box 64 x 64 x 1,
+  CUtensorMap tm_v;           //   SW128; the same for V (slots past max_ctx read as zeros)
   const __half* q16;          // [B, Hq, D] (RoPE applied)
-  const __half* kc;
-  const __half* vc;
   const int64_t* cache_lens;  // [B], device
   int B, Hq, Hkv, D;
   int64_t max_ctx;
   float scale_log2;
   int nsplit;                 // splits of each sequence's slots (decode_batch_splits)
-  int deep;                   // decode_batch_deep: one CTA per SM, five-stage ring
+  int deep;                   // decode_batch_deep: one CTA per SM of 8 warps
   float* part;                // [B][Hq][nsplit][D + 2] when nsplit > 1
   __half* attn16;             // [B, Hq * D]
   int* err;

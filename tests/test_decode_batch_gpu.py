@@ -15,9 +15,9 @@ pytestmark = pytest.mark.gpu
 SENTINEL = np.float16(-3.5)
 
 
-def _run_batch(s, w, lens, C, seed, max_len=None):
+def _run_batch(s, w, lens, C, seed, max_len=None, sentinel=SENTINEL):
     B = len(lens)
-    hist = [synth.kv_history(s, C, L, layer=b, seed=seed, sentinel=SENTINEL)
+    hist = [synth.kv_history(s, C, L, layer=b, seed=seed, sentinel=sentinel)
             for b, L in enumerate(lens)]
     kc_np = np.stack([k for k, _ in hist])
     vc_np = np.stack([v for _, v in hist])
@@ -79,6 +79,18 @@ def test_tiny_batch_past_one_row_tile():
     rng = np.random.default_rng(12)
     lens = [int(v) for v in rng.integers(0, 62, size=130)]
     _check(s, w, lens, 64, seed=12)
+
+
+@pytest.mark.parametrize("B", [3, 80])
+def test_nan_in_unused_slots_is_never_read(B):
+    """Every slot past a sequence's length holds NaN: slots past the end of a
+    split share a tile with real ones, and none of them may reach the output
+    (3 sequences: one CTA per SM; 80 x 2 kv heads: two CTAs per SM)."""
+    s = synth.TINY
+    w = synth.block_weights(s, seed=14)
+    rng = np.random.default_rng(14)
+    lens = [int(v) for v in rng.integers(0, 190, size=B)]
+    _check(s, w, lens, 192, seed=14, sentinel=np.float16(np.nan))
 
 
 def test_1p5b_bench_launch_configuration():
