@@ -85,8 +85,8 @@ int shape_ok(const blk_config* c) {
 // Workspace layout.  Prefill and decode buffers start at offset 0 (a call
 // uses one of the two layouts).
 constexpr int kMaxSplits = 4;        // split-K partial buffers of the down projection
-// Batched decode (at most a few hundred rows): the down projection's few
-// N tiles need more K splits to occupy every SM pair.
+// Batched decode (at most a few hundred rows): QKV, o_proj and down have few
+// N tiles and need K splits to occupy every SM pair.
 constexpr int kMaxSplitsBatch = 16;
 constexpr int kMaxSplitsNorm = 8;    // partials the split-K RMSNorm adds
 

@@ -34,8 +34,13 @@
 //              GATEUP B tile = 128 rows of W_gate over 128 rows of W_up,
 //                     silu(gate) * up -> activation (fp16)
 //              DOWN   + residual h (fp32) -> block output (fp16)
-//            and then release the accumulator, so the MMA of the next tile
-//            overlaps this epilogue.
+//            or, when the launcher splits K (every projection but GATEUP,
+//            given a partial buffer), an fp32 partial per split that a
+//            finishing kernel adds up in split order; then release the
+//            accumulator, so the MMA of the next tile overlaps this epilogue.
+// Few rows (batched decode): the A box covers M rounded up to 8 rows, an M
+// tile that starts past M is not loaded, and epilogue warps whose rows all
+// lie past M skip their math (those accumulator rows hold arbitrary values).
 // Every mbarrier wait is bounded; on a timeout the CTA records an error,
 // stops issuing work, waits (bounded) for what it already issued and frees
 // its TMEM before returning.

@@ -1,5 +1,7 @@
-// Prefill-phase row RMSNorm: y = fp16(x * rsqrt(mean(x^2) + eps) * g); x is
-// the block input (fp16) or the fp32 residual stream h.
+// Row RMSNorm of the prefill and batched-decode chains: y = fp16(x *
+// rsqrt(mean(x^2) + eps) * g); x is the block input (fp16), the fp32 residual
+// stream h, or (after a K-split o_proj) the sum of its partials and the block
+// input, which is also written out as h.
 #include "common.cuh"
 #include "kernels.h"
 
