@@ -696,21 +696,17 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restr
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
        i += (int64_t)gridDim.x * blockDim.x) {
     const float4 r = __ldg(reinterpret_cast<const float4*>(res32) + i);
-    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-    // splits in ascending order, four loads in flight at a time
-    for (int j0 = 0; j0 < S; j0 += 4) {
-      float4 q[4];
+    // every split loaded before any is added (one round trip), then added
+    // in ascending order
+    constexpr int kMaxS = 16;
+    float4 q[kMaxS];
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        q[j] = j0 + j < S
-                   ? __ldcg(reinterpret_cast<const float4*>(part + (size_t)(j0 + j) * MN) + i)
-                   : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < kMaxS; ++j)
+      if (j < S) q[j] = __ldcg(reinterpret_cast<const float4*>(part + (size_t)j * MN) + i);
+    float4 a = q[0];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        if (j0 + j == 0) a = q[0];
-        else if (j0 + j < S) { a.x += q[j].x; a.y += q[j].y; a.z += q[j].z; a.w += q[j].w; }
-      }
-    }
+    for (int j = 1; j < kMaxS; ++j)
+      if (j < S) { a.x += q[j].x; a.y += q[j].y; a.z += q[j].z; a.w += q[j].w; }
     uint2 o;
     *reinterpret_cast<__half2*>(&o.x) = __floats2half2_rn(a.x + r.x, a.y + r.y);
     *reinterpret_cast<__half2*>(&o.y) = __floats2half2_rn(a.z + r.z, a.w + r.w);
@@ -800,6 +796,7 @@ __global__ void __launch_bounds__(64) qkv_finish_kernel(const __grid_constant__ 
 // ---------------------------------------------------------------- host side
 
 cudaError_t launch_splitk_reduce(const TcGemmParams& p, int num_sms, cudaStream_t s) {
+  if (p.splits < 1 || p.splits > 16) return cudaErrorInvalidValue;
   const int64_t MN = (int64_t)p.M * p.N;
   const int64_t n4 = MN / 4;
   int grid = (int)((n4 + 255) / 256);
