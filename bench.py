@@ -485,14 +485,14 @@ def bench_lm_head(args, s, dev, stream, peaks, ws):
 
 def bench_decode_batch(args, s, dev, stream, peaks, ws):
     """Batched decode: B sequences, one new token each, through the 28-layer
-    stack (blk_decode_batch per layer), one CUDA graph per step.  Every
+    stack (one blk_decode_batch_stack call), one CUDA graph per step.  Every
     sequence holds ctx history slots (each layer's seeded history, the same
     for every sequence of the layer); the step appends slot ctx + i.  Bytes
     per step: every layer's weights once + each sequence's K/V slots read;
     the weights (2.6 GB) exceed L2, so no flush is needed."""
     import torch
     import synth
-    import decode_qwen2_block_gb300 as blk
+    from decode_qwen2_block_gb300.stack import BatchStack
     K, W = args.steps, args.warmup
     Bs = [int(b) for b in args.decode_batch.split(",") if b]
     L0 = args.decode_batch_ctx
@@ -504,26 +504,20 @@ def bench_decode_batch(args, s, dev, stream, peaks, ws):
     for l in range(n):
         wnp = synth.block_weights(s, layer=l, seed=0)
         wd.append({k: torch.from_numpy(v).to(dev) for k, v in wnp.items()})
-    block = blk.Block(s, C, chain=True)
-    wts = [blk.Block.weights(w) for w in wd]
     caches = []
     for l in range(n):
         k, v = synth.kv_history(s, C, L0, layer=l, seed=0)
         kc = torch.from_numpy(k).to(dev).unsqueeze(0).repeat(Bmax, 1, 1, 1).contiguous()
         vc = torch.from_numpy(v).to(dev).unsqueeze(0).repeat(Bmax, 1, 1, 1).contiguous()
         caches.append((kc, vc))
-    wsb = torch.empty(block.decode_batch_workspace_bytes(Bmax), dtype=torch.uint8, device=dev)
+    st = BatchStack(s, wd, C, Bmax, caches=caches, device=dev)
+    block = st.block
     x = torch.from_numpy(synth.hidden_input(s, Bmax, seed=0, stream_offset=5)).to(dev)
-    bufs = [torch.empty((Bmax, H), dtype=torch.float16, device=dev) for _ in range(2)]
+    y = torch.empty((Bmax, H), dtype=torch.float16, device=dev)
     maxlen = L0 + W + K
 
     def step(B, lens):
-        cur = x[:B]
-        for l in range(n):
-            out = bufs[l % 2][:B]
-            block.decode_batch(wts[l], cur, lens, lens, maxlen, caches[l][0][:B],
-                               caches[l][1][:B], out, wsb, stream=stream)
-            cur = out
+        st.step(x[:B], lens, lens, maxlen, y[:B], stream=stream)
 
     out = {}
     for B in Bs:
@@ -535,13 +529,7 @@ def bench_decode_batch(args, s, dev, stream, peaks, ws):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.stream(side):
                 with torch.cuda.graph(g, stream=side):
-                    cur = x[:B]
-                    for l in range(n):
-                        o = bufs[l % 2][:B]
-                        block.decode_batch(wts[l], cur, lens[i], lens[i], maxlen,
-                                           caches[l][0][:B], caches[l][1][:B], o, wsb,
-                                           stream=side)
-                        cur = o
+                    st.step(x[:B], lens[i], lens[i], maxlen, y[:B], stream=side)
             graphs.append(g)
         torch.cuda.current_stream().wait_stream(side)
         for i in range(W):

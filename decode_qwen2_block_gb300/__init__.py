@@ -36,7 +36,8 @@ EXPORTED = ("blk_create", "blk_destroy", "blk_set_flags", "blk_workspace_bytes",
             "blk_prefill_kv", "blk_decode", "blk_check", "blk_status_str", "blk_timing",
             "blk_timing_collect", "blk_timing_read", "blk_decode_static", "blk_decode_stack",
             "blk_set_trace", "blk_embed", "blk_lm_head_workspace_bytes", "blk_lm_head",
-            "blk_decode_batch_workspace_bytes", "blk_decode_batch")
+            "blk_decode_batch_workspace_bytes", "blk_decode_batch",
+            "blk_decode_batch_stack_workspace_bytes", "blk_decode_batch_stack")
 BLK_N_KERNELS = 16
 
 WEIGHT_FIELDS = ("ln1_g", "wq", "wk", "wv", "bq", "bk", "bv", "wo", "ln2_g", "w_gate", "w_up",
@@ -118,6 +119,12 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.blk_decode_batch.argtypes = [vp, ctypes.POINTER(BlkWeights), vp, vp, vp, i64, i64, vp, vp,
                                      vp, vp, vp, vp, ctypes.c_size_t, vp]
     lib.blk_decode_batch.restype = i32
+    lib.blk_decode_batch_stack_workspace_bytes.argtypes = [vp, i64]
+    lib.blk_decode_batch_stack_workspace_bytes.restype = ctypes.c_size_t
+    lib.blk_decode_batch_stack.argtypes = [vp, ctypes.POINTER(BlkWeights), i32, ctypes.POINTER(vp),
+                                           ctypes.POINTER(vp), vp, vp, vp, i64, i64, vp, vp,
+                                           ctypes.c_size_t, vp]
+    lib.blk_decode_batch_stack.restype = i32
     lib.blk_embed.argtypes = [vp, vp, i64, vp, i64, vp, vp]
     lib.blk_embed.restype = i32
     lib.blk_lm_head_workspace_bytes.argtypes = [vp]
@@ -199,6 +206,17 @@ def blk_decode_batch(handle, w: BlkWeights, x, pos, cache_lens, B, max_cache_len
                      v_cache, out, k_new, v_new, ws, ws_bytes, stream) -> int:
     return load().blk_decode_batch(handle, ctypes.byref(w), x, pos, cache_lens, B, max_cache_len,
                                    k_cache, v_cache, out, k_new, v_new, ws, ws_bytes, stream)
+
+
+def blk_decode_batch_stack_workspace_bytes(handle, max_B: int) -> int:
+    return load().blk_decode_batch_stack_workspace_bytes(handle, max_B)
+
+
+def blk_decode_batch_stack(handle, w_array, n_layers, k_caches, v_caches, x, pos, cache_lens, B,
+                           max_cache_len, out, ws, ws_bytes, stream) -> int:
+    """w_array: (BlkWeights * n); k_caches/v_caches: (c_void_p * n)."""
+    return load().blk_decode_batch_stack(handle, w_array, n_layers, k_caches, v_caches, x, pos,
+                                         cache_lens, B, max_cache_len, out, ws, ws_bytes, stream)
 
 
 def blk_embed(handle, table, vocab, ids, T, x, stream) -> int:

@@ -347,25 +347,36 @@ DecodeBatchWs decode_batch_ws(const blk_config& c, int64_t B, int num_sms) {
   return w;
 }
 
-int run_decode_batch(blk_handle h, const blk_weights* w, const void* x, const int64_t* pos,
-                     const int64_t* cache_lens, int64_t B, int64_t max_cache_len, void* k_cache,
-                     void* v_cache, void* out, void* k_new, void* v_new, void* ws,
-                     size_t ws_bytes, void* stream) {
+// Every host-side check of a batched decode call (nothing is enqueued).
+int check_decode_batch(blk_handle h, const blk_weights* w, const void* x, const int64_t* pos,
+                       const int64_t* cache_lens, int64_t B, int64_t max_cache_len,
+                       const void* k_cache, const void* v_cache, const void* out,
+                       const void* k_new, const void* v_new, const void* ws, size_t ws_bytes) {
   if (!h) return BLK_ERR_NULL;
   const blk_config& c = h->cfg;
   int rc = check_weights(c, w);
   if (rc) return rc;
   if (!x || !pos || !cache_lens || !k_cache || !v_cache || !out || !ws) return BLK_ERR_NULL;
-  for (const void* ptr : {x, (const void*)k_cache, (const void*)v_cache, (const void*)out,
-                          (const void*)ws})
+  for (const void* ptr : {x, k_cache, v_cache, out, ws})
     if (!aligned(ptr, 16)) return BLK_ERR_ALIGN;
   if (!aligned(pos, 8) || !aligned(cache_lens, 8)) return BLK_ERR_ALIGN;
   if ((k_new && !aligned(k_new, 16)) || (v_new && !aligned(v_new, 16))) return BLK_ERR_ALIGN;
   if (B < 1 || B > 4096) return BLK_ERR_SHAPE;
   if (max_cache_len < 0 || max_cache_len + 1 > c.max_ctx) return BLK_ERR_CACHE_OVERFLOW;
   if (c.n_heads / c.n_kv_heads > 16) return BLK_ERR_SHAPE;
+  if (ws_bytes < decode_batch_ws(c, B, h->num_sms).total) return BLK_ERR_WORKSPACE;
+  return BLK_OK;
+}
+
+int run_decode_batch(blk_handle h, const blk_weights* w, const void* x, const int64_t* pos,
+                     const int64_t* cache_lens, int64_t B, int64_t max_cache_len, void* k_cache,
+                     void* v_cache, void* out, void* k_new, void* v_new, void* ws,
+                     size_t ws_bytes, void* stream) {
+  int rc = check_decode_batch(h, w, x, pos, cache_lens, B, max_cache_len, k_cache, v_cache, out,
+                              k_new, v_new, ws, ws_bytes);
+  if (rc) return rc;
+  const blk_config& c = h->cfg;
   const DecodeBatchWs lay = decode_batch_ws(c, B, h->num_sms);
-  if (ws_bytes < lay.total) return BLK_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   unsigned char* base = static_cast<unsigned char*>(ws);
   __half* xn16 = reinterpret_cast<__half*>(base + lay.xn16);
@@ -719,6 +730,43 @@ int blk_decode_batch(blk_handle h, const blk_weights* w, const void* x, const in
                      size_t ws_bytes, void* stream) {
   return run_decode_batch(h, w, x, pos, cache_lens, B, max_cache_len, k_cache, v_cache, out,
                           k_new, v_new, ws, ws_bytes, stream);
+}
+
+size_t blk_decode_batch_stack_workspace_bytes(blk_handle h, int64_t max_B) {
+  if (!h || max_B < 1 || max_B > 4096) return 0;
+  const size_t act = align_up((size_t)max_B * h->cfg.hidden * 2);
+  return decode_batch_ws(h->cfg, max_B, h->num_sms).total + 2 * act;
+}
+
+int blk_decode_batch_stack(blk_handle h, const blk_weights* w, int n_layers,
+                           void* const* k_caches, void* const* v_caches, const void* x,
+                           const int64_t* pos, const int64_t* cache_lens, int64_t B,
+                           int64_t max_cache_len, void* out, void* ws, size_t ws_bytes,
+                           void* stream) {
+  if (!h || !w || !k_caches || !v_caches || !ws) return BLK_ERR_NULL;
+  if (n_layers < 1 || B < 1 || B > 4096) return BLK_ERR_SHAPE;
+  // the two activation buffers between layers follow the one-layer workspace
+  const size_t act = align_up((size_t)B * h->cfg.hidden * 2);
+  const size_t layer_ws = decode_batch_ws(h->cfg, B, h->num_sms).total;
+  if (ws_bytes < layer_ws + 2 * act) return BLK_ERR_WORKSPACE;
+  unsigned char* base = static_cast<unsigned char*>(ws);
+  void* bufs[2] = {base + layer_ws, base + layer_ws + act};
+  auto layer_in = [&](int l) -> const void* { return l == 0 ? x : bufs[(l - 1) % 2]; };
+  auto layer_out = [&](int l) -> void* { return l == n_layers - 1 ? out : bufs[l % 2]; };
+  // every layer's arguments are checked before anything is enqueued
+  for (int l = 0; l < n_layers; ++l) {
+    const int rc = check_decode_batch(h, &w[l], layer_in(l), pos, cache_lens, B, max_cache_len,
+                                      k_caches[l], v_caches[l], layer_out(l), nullptr, nullptr,
+                                      ws, layer_ws);
+    if (rc) return rc;
+  }
+  for (int l = 0; l < n_layers; ++l) {
+    const int rc = run_decode_batch(h, &w[l], layer_in(l), pos, cache_lens, B, max_cache_len,
+                                    k_caches[l], v_caches[l], layer_out(l), nullptr, nullptr, ws,
+                                    layer_ws, stream);
+    if (rc) return rc;
+  }
+  return BLK_OK;
 }
 
 }  // extern "C"

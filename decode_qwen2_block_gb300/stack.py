@@ -13,7 +13,8 @@ import ctypes
 
 import torch
 
-from . import BLK_OK, BlkError, Block, BlkWeights, blk_decode_stack
+from . import (BLK_ERR_SHAPE, BLK_OK, BlkError, Block, BlkWeights, blk_decode_batch_stack,
+               blk_decode_batch_stack_workspace_bytes, blk_decode_stack)
 
 
 class LayerStack:
@@ -92,3 +93,48 @@ class LayerStack:
         torch.cuda.current_stream().wait_stream(s)
         self.graphs[key if key is not None else (phase, cache_len)] = (g, out)
         return g, out
+
+
+class BatchStack:
+    """B sequences, one new token each, through a stack of decoder blocks in
+    one library call per step (blk_decode_batch_stack)."""
+
+    def __init__(self, shape, layer_weights, max_ctx: int, max_B: int, caches=None,
+                 device="cuda"):
+        """layer_weights: list of dicts of fp16 CUDA tensors (one per layer).
+        caches: optional list of (k_cache, v_cache) per layer, each
+        [max_B, Hkv, max_ctx, D]; allocated (zero-filled) when None.  A step
+        with B <= max_B sequences uses the first B of every cache."""
+        self.shape = shape
+        self.n_layers = len(layer_weights)
+        self.block = Block(shape, max_ctx, chain=True)
+        self.wdev = layer_weights
+        self.w = [Block.weights(wd) for wd in layer_weights]
+        Hkv, D = shape.n_kv_heads, shape.head_dim
+        if caches is None:
+            caches = [(torch.zeros((max_B, Hkv, max_ctx, D), dtype=torch.float16, device=device),
+                       torch.zeros((max_B, Hkv, max_ctx, D), dtype=torch.float16, device=device))
+                      for _ in range(self.n_layers)]
+        self.caches = caches
+        self.max_B = max_B
+        nbytes = blk_decode_batch_stack_workspace_bytes(self.block.handle, max_B)
+        self.ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        n = self.n_layers
+        self._w_arr = (BlkWeights * n)(*self.w)
+        self._kc_arr = (ctypes.c_void_p * n)(*[kc.data_ptr() for kc, _ in caches])
+        self._vc_arr = (ctypes.c_void_p * n)(*[vc.data_ptr() for _, vc in caches])
+
+    def step(self, x, pos, cache_lens, max_cache_len: int, out, stream=None):
+        """x, out: fp16 [B, hidden]; pos, cache_lens: int64 [B] on the device;
+        max_cache_len bounds the cache lengths.  Returns out."""
+        B = x.shape[0]
+        if B > self.max_B:
+            raise BlkError(BLK_ERR_SHAPE, "BatchStack.step: B > max_B")
+        s = torch.cuda.current_stream() if stream is None else stream
+        rc = blk_decode_batch_stack(self.block.handle, self._w_arr, self.n_layers, self._kc_arr,
+                                    self._vc_arr, x.data_ptr(), pos.data_ptr(),
+                                    cache_lens.data_ptr(), B, max_cache_len, out.data_ptr(),
+                                    self.ws.data_ptr(), self.ws.numel(), s.cuda_stream)
+        if rc != BLK_OK:
+            raise BlkError(rc, "blk_decode_batch_stack")
+        return out

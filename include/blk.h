@@ -260,6 +260,27 @@ int blk_decode_batch(blk_handle h, const blk_weights* w, const void* x, const in
                      void* v_cache, void* out, void* k_new, void* v_new, void* ws,
                      size_t ws_bytes, void* stream);
 
+/* Batched decode through a stack of n_layers blocks of this shape, in order:
+ * layer l's output rows are layer l+1's input rows, every layer at the same
+ * positions and cache lengths (the batched counterpart of blk_decode_stack).
+ *   w                    host array [n_layers] of weight structs
+ *   k_caches, v_caches   host arrays [n_layers] of device caches, each
+ *                        [B, n_kv_heads, max_ctx, head_dim] as for blk_decode_batch
+ *   x, out               device fp16 [B, hidden]; out must not alias x
+ *   ws                   blk_decode_batch_stack_workspace_bytes(h, B) bytes or
+ *                        more (the one-layer workspace plus two [B, hidden]
+ *                        fp16 buffers between layers)
+ * No k_new / v_new: the new K/V are in each layer's cache slot.  Every
+ * layer's arguments are checked before anything is enqueued.  Returns the
+ * codes of blk_decode_batch, BLK_ERR_NULL for a NULL array and BLK_ERR_SHAPE
+ * for n_layers < 1. */
+size_t blk_decode_batch_stack_workspace_bytes(blk_handle h, int64_t max_B);
+int blk_decode_batch_stack(blk_handle h, const blk_weights* w, int n_layers,
+                           void* const* k_caches, void* const* v_caches, const void* x,
+                           const int64_t* pos, const int64_t* cache_lens, int64_t B,
+                           int64_t max_cache_len, void* out, void* ws, size_t ws_bytes,
+                           void* stream);
+
 /* ---- around the block stack: embedding in, next token out ----------------
  * The inference flow of the MLIR-compilation page (§2.3 "LLM inference
  * overview"): input tokens -> word embedding -> the blocks -> LM head ->

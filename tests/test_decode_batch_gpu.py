@@ -158,3 +158,63 @@ def test_batch_argument_errors_and_bad_length():
         block.check()
     assert e.value.status == blk.BLK_ERR_POSITION
     assert not kc[1].any() and not vc[1].any()           # nothing written for the bad sequence
+
+
+def _stack_inputs(s, n_layers, B, C, seed):
+    wl = [synth.block_weights(s, layer=l, seed=seed) for l in range(n_layers)]
+    lens = [3 + 11 * b for b in range(B)]
+    caches = []
+    for l in range(n_layers):
+        hist = [synth.kv_history(s, C, L, layer=100 * l + b, seed=seed, sentinel=SENTINEL)
+                for b, L in enumerate(lens)]
+        caches.append((np.stack([k for k, _ in hist]), np.stack([v for _, v in hist])))
+    x = synth.hidden_input(s, B, seed=seed, stream_offset=9)
+    return wl, lens, caches, x
+
+
+def test_batch_stack_equals_one_call_per_layer():
+    """blk_decode_batch_stack over 3 layers = blk_decode_batch per layer, bit
+    for bit (outputs and every cache)."""
+    from decode_qwen2_block_gb300.stack import BatchStack
+    s, n, B, C = synth.TINY, 3, 5, 64
+    wl, lens, caches, x = _stack_inputs(s, n, B, C, seed=15)
+    wd = [{k: to_dev(v) for k, v in w.items()} for w in wl]
+    lens_d = to_dev(np.array(lens, dtype=np.int64))
+    st = BatchStack(s, wd, C, B, caches=[(to_dev(k), to_dev(v)) for k, v in caches])
+    out = torch.empty((B, s.hidden), dtype=torch.float16, device="cuda")
+    st.step(to_dev(x), lens_d, lens_d, max(lens), out)
+    torch.cuda.synchronize()
+    st.block.check()
+    block = blk.Block(s, C)
+    ws = torch.empty(block.decode_batch_workspace_bytes(B), dtype=torch.uint8, device="cuda")
+    cur = to_dev(x)
+    ref_caches = [(to_dev(k), to_dev(v)) for k, v in caches]
+    for l in range(n):
+        nxt = torch.empty_like(cur)
+        block.decode_batch(blk.Block.weights(wd[l]), cur, lens_d, lens_d, max(lens),
+                           ref_caches[l][0], ref_caches[l][1], nxt, ws)
+        cur = nxt
+    torch.cuda.synchronize()
+    block.check()
+    assert torch.equal(out.view(torch.int16), cur.view(torch.int16))
+    for (k1, v1), (k2, v2) in zip(st.caches, ref_caches):
+        assert torch.equal(k1.view(torch.int16), k2.view(torch.int16))
+        assert torch.equal(v1.view(torch.int16), v2.view(torch.int16))
+
+
+def test_batch_stack_checks_every_layer_before_enqueueing():
+    from decode_qwen2_block_gb300.stack import BatchStack
+    s, n, B, C = synth.TINY, 3, 2, 64
+    wl, lens, caches, x = _stack_inputs(s, n, B, C, seed=16)
+    wd = [{k: to_dev(v) for k, v in w.items()} for w in wl]
+    st = BatchStack(s, wd, C, B, caches=[(to_dev(k), to_dev(v)) for k, v in caches])
+    st._w_arr[2].wq = None                       # the last layer is bad
+    lens_d = to_dev(np.array(lens, dtype=np.int64))
+    out = torch.empty((B, s.hidden), dtype=torch.float16, device="cuda")
+    with pytest.raises(blk.BlkError) as e:
+        st.step(to_dev(x), lens_d, lens_d, max(lens), out)
+    assert e.value.status == blk.BLK_ERR_NULL
+    torch.cuda.synchronize()
+    for (kc, vc), (k0, v0) in zip(st.caches, caches):   # nothing ran: caches unchanged
+        assert np.array_equal(kc.cpu().numpy().view(np.uint16), k0.view(np.uint16))
+        assert np.array_equal(vc.cpu().numpy().view(np.uint16), v0.view(np.uint16))
