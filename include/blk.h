@@ -1,8 +1,10 @@
 /*
  * blk.h — C ABI of the GB300 decoder-block library (libblk.so).
  *
- * One call runs one Qwen2-style decoder block forward for one sequence
- * (batch 1) on one GPU.  The block is the one printed as TopOp pseudo-code in
+ * One call runs one Qwen2-style decoder block forward (or a stack of them)
+ * on one GPU, for one sequence (batch 1) or, with blk_decode_batch and
+ * blk_decode_batch_stack, for B sequences of one new token each.  The block
+ * is the one printed as TopOp pseudo-code in
  * "An MLIR-based LLM compilation method" (TopOp/TpuOp paper translation),
  * §3.1 Listing 1 (no history) and Listing 2 (with history K/V):
  *
@@ -37,7 +39,8 @@
  * (the buddy-mlir runtime's per-layer [1, kv_heads, max_len, head_dim] cache of
  * its §6.4.3).  A call reads slots [0, cache_len), writes slots
  * [cache_len, cache_len + T) in place, and leaves every other slot untouched.
- * Slots are the cache's order; position_ids drive RoPE only.
+ * Slots are the cache's order; position_ids drive RoPE only.  Batched decode
+ * takes B such caches back to back per layer, [B][n_kv_heads][max_ctx][head_dim].
  */
 #ifndef BLK_H
 #define BLK_H
@@ -152,7 +155,7 @@ int blk_decode(blk_handle h, const blk_weights* w, const void* x,
  * l's output is layer l+1's input, all at the same cache_len and position.
  * This is the decode call of the buddy-mlir runtime's forward_decode (one
  * token through every layer, each with its own cache; §6.4.6 of that page),
- * done as one launch per 32 layers.
+ * done as one launch per 16 layers.
  *   w          host array [n_layers] of weight structs
  *   k_caches, v_caches  host arrays [n_layers] of device cache pointers
  *   k_new, v_new        host arrays [n_layers] of device [1, n_kv_heads, D]
@@ -229,7 +232,7 @@ int blk_timing_read(blk_handle h, int kernel, double* total_ms,
  * grid barrier) and when its work ends: uint64 entries at
  * [(cta * n_layers + layer) * 6 + phase] * 2 + {0 = start, 1 = end}, phases
  * QKV, attention, split combine, o_proj, gate/up, down; n_layers counts the
- * layers of one launch (at most 32).  Entries past `bytes` are not written.
+ * layers of one launch (at most 16).  Entries past `bytes` are not written.
  * NULL turns tracing off (the default).  Returns BLK_OK or BLK_ERR_NULL. */
 int blk_set_trace(blk_handle h, void* device_buffer, size_t bytes);
 
