@@ -45,15 +45,18 @@ PREFILL_T = 1024
 # the ncu captures summarised in profiles/ (prefill_kernels_1p5b_T1024.md,
 # decode_persistent_1p5b_28layers_ctx4096.md).  Must be set back to None
 # whenever the kernel changes.
+# The GEMMs (epilogues, A boxes, split-K paths), the split-K reduction and
+# the decode kernel (its SiLU) changed after their last capture, so their
+# entries are None until they are captured again; the last figures are kept
+# in the profiles as history.
 NCU_TRAFFIC = {
-    "gemm_gateup": 58.231808e6 + 0.156160e6,
-    "gemm_down": 45.917440e6 + 0.011520e6,
-    "gemm_qkv": 10.016768e6 + 0.0,
-    "gemm_o": 11.034624e6 + 0.0,
+    "gemm_gateup": None,
+    "gemm_down": None,
+    "gemm_qkv": None,
+    "gemm_o": None,
     "attn_prefill": 4.242944e6,
     "lm_head": 466853632 + 206080,
-    # both launches of one 28-layer step (16 + 12 layers)
-    ("decode_persistent", 4096): (1.577014e9 + 1.183408e9) + (24.87936e6 + 19.178752e6),
+    ("decode_persistent", 4096): None,
 }
 
 
