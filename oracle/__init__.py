@@ -36,6 +36,13 @@ class OrcWeights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in WEIGHT_FIELDS]
 
 
+MATRIX_FIELDS = ("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down")
+
+
+class OrcWeightsF64(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in MATRIX_FIELDS]
+
+
 def build(force: bool = False) -> str:
     """Compile liboracle.so with g++: -O2, no FP contraction, no fast-math."""
     newest = max(os.path.getmtime(s) for s in _SRC)
@@ -71,6 +78,15 @@ def _load():
             lib.orc_block_forward.argtypes = [ctypes.POINTER(OrcConfig), ctypes.POINTER(OrcWeights),
                                               vp, vp, i64, i64, vp, vp, vp, vp, vp, i64, vp]
             lib.orc_block_forward.restype = ctypes.c_int
+            lib.orc_block_forward_f64w.argtypes = [ctypes.POINTER(OrcConfig),
+                                                   ctypes.POINTER(OrcWeights),
+                                                   ctypes.POINTER(OrcWeightsF64), vp, vp, i64,
+                                                   i64, vp, vp, vp, vp, vp, i64, vp]
+            lib.orc_block_forward_f64w.restype = ctypes.c_int
+            lib.orc_dequant_i8.argtypes = [vp, vp, i64, i64, vp]
+            lib.orc_dequant_i8.restype = None
+            lib.orc_dequant_u4.argtypes = [vp, vp, vp, i64, i64, i64, vp]
+            lib.orc_dequant_u4.restype = ctypes.c_int
             lib.orc_embed.argtypes = [vp, i64, i64, vp, i64, vp]
             lib.orc_embed.restype = ctypes.c_int
             lib.orc_lm_head.argtypes = [vp, i64, i64, vp, dbl, vp, i64, vp, vp]
@@ -144,12 +160,15 @@ def attend(q, K, V, scale: float) -> np.ndarray:
 # ---- the whole block --------------------------------------------------------
 
 def block_forward(shape, weights: dict, x, pos, L: int, k_cache, v_cache, max_ctx: int | None = None,
-                  rows=None):
+                  rows=None, mats64: dict | None = None):
     """Run the block for T = len(x) new tokens on top of L history slots.
 
     ``shape`` is a ``synth.BlockShape``.  ``k_cache``/``v_cache`` (fp16
     [Hkv, max_ctx, D]) are updated in place.  Returns (out, k_new, v_new);
-    ``out`` covers ``rows`` (all rows when None)."""
+    ``out`` covers ``rows`` (all rows when None).  ``mats64``, if given, holds
+    the seven matrices as f64 values (e.g. dequantized weights, see
+    ``dequant_i8`` / ``dequant_u4``); ``weights`` then supplies only the gains
+    and biases."""
     lib = _load()
     x = _u16(x)
     T = x.shape[0]
@@ -164,6 +183,8 @@ def block_forward(shape, weights: dict, x, pos, L: int, k_cache, v_cache, max_ct
     wts = OrcWeights()
     for name in WEIGHT_FIELDS:
         arr = weights.get(name)
+        if mats64 is not None and name in MATRIX_FIELDS:
+            arr = None
         if arr is None:
             setattr(wts, name, None)
             continue
@@ -179,13 +200,54 @@ def block_forward(shape, weights: dict, x, pos, L: int, k_cache, v_cache, max_ct
         rows_arr = np.ascontiguousarray(rows, dtype=np.int64)
         n_rows = rows_arr.size
     out = np.empty((n_rows, H), dtype=np.uint16)
-    rc = lib.orc_block_forward(ctypes.byref(cfg), ctypes.byref(wts), x.ctypes.data, pos.ctypes.data,
-                               T, L, kc.ctypes.data, vc.ctypes.data, k_new.ctypes.data,
-                               v_new.ctypes.data, None if rows_arr is None else rows_arr.ctypes.data,
-                               n_rows, out.ctypes.data)
+    args = (x.ctypes.data, pos.ctypes.data, T, L, kc.ctypes.data, vc.ctypes.data,
+            k_new.ctypes.data, v_new.ctypes.data,
+            None if rows_arr is None else rows_arr.ctypes.data, n_rows, out.ctypes.data)
+    if mats64 is None:
+        rc = lib.orc_block_forward(ctypes.byref(cfg), ctypes.byref(wts), *args)
+    else:
+        m64 = OrcWeightsF64()
+        for name in MATRIX_FIELDS:
+            arr = _f64(mats64[name])
+            keep["m64_" + name] = arr
+            setattr(m64, name, arr.ctypes.data)
+        rc = lib.orc_block_forward_f64w(ctypes.byref(cfg), ctypes.byref(wts), ctypes.byref(m64),
+                                        *args)
     if rc != 0:
         raise ValueError(f"oracle rejected the arguments (rc={rc})")
     return out.view(np.float16), k_new.view(np.float16), v_new.view(np.float16)
+
+
+# ---- weight-only quantized projections -----------------------------------------
+
+def dequant_i8(q, scale) -> np.ndarray:
+    """f64 w[o][i] = scale[o] * q[o][i] (q int8 [N, K], scale fp16 [N])."""
+    q = np.ascontiguousarray(q, dtype=np.int8)
+    s = _u16(scale)
+    N, K = q.shape
+    if s.shape != (N,):
+        raise ValueError("one scale per output row")
+    w = np.empty((N, K), dtype=np.float64)
+    _load().orc_dequant_i8(q.ctypes.data, s.ctypes.data, N, K, w.ctypes.data)
+    return w
+
+
+def dequant_u4(packed, scale, zero, group: int) -> np.ndarray:
+    """f64 w[o][i] = scale[o][i//group] * (code(o, i) - zero[o][i//group]);
+    packed uint8 [N, K/2] holds two 4-bit codes per byte, the even i in the
+    low nibble; scale fp16 and zero uint8 are [N, K/group]."""
+    packed = np.ascontiguousarray(packed, dtype=np.uint8)
+    s = _u16(scale)
+    z = np.ascontiguousarray(zero, dtype=np.uint8)
+    N, K2 = packed.shape
+    K = 2 * K2
+    if K % group or s.shape != (N, K // group) or z.shape != (N, K // group):
+        raise ValueError("scale / zero must be [N, K/group] with K a multiple of group")
+    w = np.empty((N, K), dtype=np.float64)
+    if _load().orc_dequant_u4(packed.ctypes.data, s.ctypes.data, z.ctypes.data, N, K, group,
+                              w.ctypes.data) != 0:
+        raise ValueError("oracle rejected the arguments")
+    return w
 
 
 # ---- around the block stack ---------------------------------------------------

@@ -38,6 +38,32 @@ const double* half_table() {
 
 inline double h2d(uint16_t h) { return half_table()[h]; }
 
+// A weight matrix [n_out][n_in] row-major, read element by element: fp16 bit
+// patterns (the block's own weights) or f64 values (e.g. dequantized weights).
+struct MatF16 {
+  const uint16_t* p;
+  double at(int64_t o, int64_t i, int64_t n_out, int64_t n_in) const {
+    (void)n_out; return h2d(p[o * n_in + i]);
+  }
+};
+struct MatF64 {
+  const double* p;
+  double at(int64_t o, int64_t i, int64_t n_out, int64_t n_in) const {
+    (void)n_out; return p[o * n_in + i];
+  }
+};
+
+// y[o] = sum_i W[o][i] * x[i] (+ b[o]), i ascending.
+template <class M>
+void linear(const M& W, const uint16_t* b, const double* x, int64_t n_out, int64_t n_in,
+            double* y) {
+  for (int64_t o = 0; o < n_out; ++o) {
+    double acc = 0.0;
+    for (int64_t i = 0; i < n_in; ++i) acc += W.at(o, i, n_out, n_in) * x[i];
+    y[o] = b ? acc + h2d(b[o]) : acc;
+  }
+}
+
 // f64 -> binary16, round to nearest, ties to even, on the bit pattern.
 uint16_t encode_half(double v) {
   uint64_t b;
@@ -100,12 +126,7 @@ void orc_rope(double* v, int64_t D, double pos, double theta) {
 
 void orc_linear(const uint16_t* W, const uint16_t* b, const double* x,
                 int64_t n_out, int64_t n_in, double* y) {
-  for (int64_t o = 0; o < n_out; ++o) {
-    const uint16_t* row = W + o * n_in;
-    double acc = 0.0;
-    for (int64_t i = 0; i < n_in; ++i) acc += h2d(row[i]) * x[i];
-    y[o] = b ? acc + h2d(b[o]) : acc;
-  }
+  linear(MatF16{W}, b, x, n_out, n_in, y);
 }
 
 double orc_silu(double z) { return z / (1.0 + std::exp(-z)); }
@@ -132,11 +153,18 @@ void orc_attend(const double* q, const uint16_t* K, const uint16_t* V,
   for (int64_t d = 0; d < D; ++d) o[d] /= denom;
 }
 
-int orc_block_forward(const orc_config* cfg, const orc_weights* w,
-                      const uint16_t* x, const int64_t* pos, int64_t T,
-                      int64_t L, uint16_t* k_cache, uint16_t* v_cache,
-                      uint16_t* k_new, uint16_t* v_new, const int64_t* rows,
-                      int64_t n_rows, uint16_t* out) {
+}  // extern "C"
+
+namespace {
+
+// The block with its seven matrices given as views (gains and biases are
+// always fp16 from `w`).
+template <class M>
+int block_forward(const orc_config* cfg, const orc_weights* w, const M& wq, const M& wk,
+                  const M& wv, const M& wo, const M& w_gate, const M& w_up, const M& w_down,
+                  const uint16_t* x, const int64_t* pos, int64_t T, int64_t L,
+                  uint16_t* k_cache, uint16_t* v_cache, uint16_t* k_new, uint16_t* v_new,
+                  const int64_t* rows, int64_t n_rows, uint16_t* out) {
   const int64_t H = cfg->hidden, Hq = cfg->n_heads, Hkv = cfg->n_kv_heads;
   const int64_t D = cfg->head_dim, I = cfg->intermediate, C = cfg->max_ctx;
   if (T <= 0 || L < 0 || L + T > C || Hkv <= 0 || Hq % Hkv != 0 || D % 2 != 0)
@@ -158,8 +186,8 @@ int orc_block_forward(const orc_config* cfg, const orc_weights* w,
   for (int64_t t = 0; t < T; ++t) {
     for (int64_t i = 0; i < H; ++i) xrow[i] = h2d(x[t * H + i]);
     orc_rmsnorm(xrow.data(), ln1.data(), H, cfg->rms_eps, &xn[t * H]);
-    orc_linear(w->wk, bias ? w->bk : nullptr, &xn[t * H], Hkv * D, H, k.data());
-    orc_linear(w->wv, bias ? w->bv : nullptr, &xn[t * H], Hkv * D, H, v.data());
+    linear(wk, bias ? w->bk : nullptr, &xn[t * H], Hkv * D, H, k.data());
+    linear(wv, bias ? w->bv : nullptr, &xn[t * H], Hkv * D, H, v.data());
     for (int64_t g = 0; g < Hkv; ++g) {
       orc_rope(&k[g * D], D, static_cast<double>(pos[t]), cfg->rope_theta);
       for (int64_t d = 0; d < D; ++d) {
@@ -181,22 +209,72 @@ int orc_block_forward(const orc_config* cfg, const orc_weights* w,
   for (int64_t r = 0; r < count; ++r) {
     const int64_t t = rows ? rows[r] : r;
     if (t < 0 || t >= T) return -1;
-    orc_linear(w->wq, bias ? w->bq : nullptr, &xn[t * H], Hq * D, H, q.data());
+    linear(wq, bias ? w->bq : nullptr, &xn[t * H], Hq * D, H, q.data());
     for (int64_t hq = 0; hq < Hq; ++hq) {
       orc_rope(&q[hq * D], D, static_cast<double>(pos[t]), cfg->rope_theta);
       const int64_t g = hq / group;
       orc_attend(&q[hq * D], &k_cache[g * C * D], &v_cache[g * C * D], L + t + 1,
                  D, D, scale, &attn[hq * D]);
     }
-    orc_linear(w->wo, nullptr, attn.data(), H, Hq * D, h.data());
+    linear(wo, nullptr, attn.data(), H, Hq * D, h.data());
     for (int64_t i = 0; i < H; ++i) h[i] += h2d(x[t * H + i]);
     orc_rmsnorm(h.data(), ln2.data(), H, cfg->rms_eps, hn.data());
-    orc_linear(w->w_gate, nullptr, hn.data(), I, H, gate.data());
-    orc_linear(w->w_up, nullptr, hn.data(), I, H, up.data());
+    linear(w_gate, nullptr, hn.data(), I, H, gate.data());
+    linear(w_up, nullptr, hn.data(), I, H, up.data());
     for (int64_t j = 0; j < I; ++j) act[j] = orc_silu(gate[j]) * up[j];
-    orc_linear(w->w_down, nullptr, act.data(), H, I, mlp.data());
+    linear(w_down, nullptr, act.data(), H, I, mlp.data());
     for (int64_t i = 0; i < H; ++i) out[r * H + i] = encode_half(h[i] + mlp[i]);
   }
+  return 0;
+}
+
+}  // namespace
+
+extern "C" {
+
+int orc_block_forward(const orc_config* cfg, const orc_weights* w,
+                      const uint16_t* x, const int64_t* pos, int64_t T,
+                      int64_t L, uint16_t* k_cache, uint16_t* v_cache,
+                      uint16_t* k_new, uint16_t* v_new, const int64_t* rows,
+                      int64_t n_rows, uint16_t* out) {
+  return block_forward(cfg, w, MatF16{w->wq}, MatF16{w->wk}, MatF16{w->wv}, MatF16{w->wo},
+                       MatF16{w->w_gate}, MatF16{w->w_up}, MatF16{w->w_down}, x, pos, T, L,
+                       k_cache, v_cache, k_new, v_new, rows, n_rows, out);
+}
+
+int orc_block_forward_f64w(const orc_config* cfg, const orc_weights* w,
+                           const orc_weights_f64* m, const uint16_t* x, const int64_t* pos,
+                           int64_t T, int64_t L, uint16_t* k_cache, uint16_t* v_cache,
+                           uint16_t* k_new, uint16_t* v_new, const int64_t* rows,
+                           int64_t n_rows, uint16_t* out) {
+  if (!m || !m->wq || !m->wk || !m->wv || !m->wo || !m->w_gate || !m->w_up || !m->w_down)
+    return -1;
+  return block_forward(cfg, w, MatF64{m->wq}, MatF64{m->wk}, MatF64{m->wv}, MatF64{m->wo},
+                       MatF64{m->w_gate}, MatF64{m->w_up}, MatF64{m->w_down}, x, pos, T, L,
+                       k_cache, v_cache, k_new, v_new, rows, n_rows, out);
+}
+
+void orc_dequant_i8(const int8_t* q, const uint16_t* scale, int64_t n_out, int64_t n_in,
+                    double* w) {
+  for (int64_t o = 0; o < n_out; ++o) {
+    const double s = h2d(scale[o]);
+    for (int64_t i = 0; i < n_in; ++i)
+      w[o * n_in + i] = s * static_cast<double>(q[o * n_in + i]);
+  }
+}
+
+int orc_dequant_u4(const uint8_t* packed, const uint16_t* scale, const uint8_t* zero,
+                   int64_t n_out, int64_t n_in, int64_t group, double* w) {
+  if (n_in <= 0 || n_in % 2 != 0 || group <= 0 || n_in % group != 0) return -1;
+  const int64_t ng = n_in / group;
+  for (int64_t o = 0; o < n_out; ++o)
+    for (int64_t i = 0; i < n_in; ++i) {
+      const uint8_t byte = packed[o * (n_in / 2) + i / 2];
+      const int code = (i % 2 == 0) ? (byte & 0x0F) : (byte >> 4);
+      const int64_t g = o * ng + i / group;
+      w[o * n_in + i] =
+          h2d(scale[g]) * (static_cast<double>(code) - static_cast<double>(zero[g]));
+    }
   return 0;
 }
 

@@ -100,6 +100,49 @@ int orc_block_forward(const orc_config* cfg, const orc_weights* w,
                       uint16_t* k_new, uint16_t* v_new, const int64_t* rows,
                       int64_t n_rows, uint16_t* out);
 
+/* ---- weight-only quantized projections --------------------------------------
+ * The MLIR-compilation page names W4A16 and INT8 (symmetric / asymmetric)
+ * weight quantization, with scales and zero points, and GPTQ / AWQ formats
+ * (§2.2 on the TpuOp dialect, §3.2 on lowering TopOp to TpuOp).  It fixes no
+ * layout; the readings followed here (also in the design notes):
+ *   INT8  symmetric, one fp16 scale per output row:  w[o][i] = s[o] * q[o][i],
+ *         q int8 in [-127, 127]
+ *   int4  asymmetric, groups of `group` consecutive inputs per output row:
+ *         w[o][i] = s[o][g] * (q[o][i] - z[o][g]), g = i / group, q and z in
+ *         [0, 15]; two codes per byte along i, the even i in the low nibble;
+ *         z one per byte
+ * Activations stay fp16 (A16); the block is then the same with these f64
+ * weights (orc_block_forward_f64w). */
+
+/* w = dequantized INT8 weights, f64 [n_out, n_in].
+ * Pinned: hand-computed rows (sign, row scale). */
+void orc_dequant_i8(const int8_t* q, const uint16_t* scale, int64_t n_out, int64_t n_in,
+                    double* w);
+
+/* w = dequantized int4 weights, f64 [n_out, n_in]; packed uint8
+ * [n_out, n_in/2], scale fp16 and zero uint8 [n_out, n_in/group].  Returns -1
+ * (nothing written) unless n_in is even and a multiple of group > 0.
+ * Pinned: nibble order, group boundaries and zero points by hand-computed
+ * rows. */
+int orc_dequant_u4(const uint8_t* packed, const uint16_t* scale, const uint8_t* zero,
+                   int64_t n_out, int64_t n_in, int64_t group, double* w);
+
+/* f64 values of the seven matrices, [out, in] row-major like orc_weights. */
+typedef struct {
+  const double *wq, *wk, *wv, *wo, *w_gate, *w_up, *w_down;
+} orc_weights_f64;
+
+/* orc_block_forward with the matrices taken from `m` (f64 values) and the
+ * gains and biases from `w` (its matrix pointers are ignored).  Returns -1 if
+ * a matrix of `m` is NULL, else as orc_block_forward.
+ * Pinned: with matrices that fp16 holds exactly it equals orc_block_forward
+ * on their fp16 bits, bit for bit (the same arithmetic in the same order). */
+int orc_block_forward_f64w(const orc_config* cfg, const orc_weights* w,
+                           const orc_weights_f64* m, const uint16_t* x, const int64_t* pos,
+                           int64_t T, int64_t L, uint16_t* k_cache, uint16_t* v_cache,
+                           uint16_t* k_new, uint16_t* v_new, const int64_t* rows,
+                           int64_t n_rows, uint16_t* out);
+
 /* ---- around the block stack (embedding in, logits and token out) ----------
  * Inference flow of the MLIR-compilation page (§2.3 "LLM inference
  * overview"): input tokens -> word embedding -> the stack of blocks -> LM

@@ -37,6 +37,12 @@ TENSOR_IDS = {
     "embed": 30, "lm_head": 31, "norm_g": 32,
 }
 INPUT_LAYER = 4095
+# Weight-only quantized matrices: codes come from the matrix's own stream,
+# scales and zero points from two more streams per matrix.
+QUANT_MATRICES = ("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down")
+for _i, _n in enumerate(QUANT_MATRICES):
+    TENSOR_IDS[_n + "_scale"] = 33 + _i
+    TENSOR_IDS[_n + "_zero"] = 40 + _i
 
 
 def build(force: bool = False) -> str:
@@ -152,6 +158,44 @@ def block_weights(s: BlockShape, layer: int = 0, seed: int = 0, std: float = 0.0
         else:
             w[name] = normal_f16(seed, stream_id(layer, name), shp, std=std)
     return w
+
+
+def quant_weights(s: BlockShape, fmt: str, layer: int = 0, seed: int = 0,
+                  group: int = 128) -> dict:
+    """Seeded weight-only quantized matrices of one layer: {name: {"q", "scale"
+    [, "zero"]}} for the seven matrices.  Codes, scales and zero points are
+    drawn directly (nothing is quantized here), sized so that the weights
+    they stand for have a spread near N(0, 0.02):
+      "i8": q int8 [N, K] = rint(42 z) clipped to [-127, 127]; scale fp16 [N]
+            = fp16(0.02/42 * (1 + 0.1 z'))
+      "u4": codes rint(7.5 + 3.5 z) clipped to [0, 15], packed two per byte
+            along K (even k in the low nibble), uint8 [N, K/2]; scale fp16
+            [N, K/group] = fp16(0.02/3.5 * (1 + 0.1 z')); zero uint8
+            [N, K/group] = rint(7.5 + 0.5 z'') clipped to [0, 15]
+    with z, z', z'' standard normal draws."""
+    out = {}
+    shapes = weight_shapes(s)
+    for name in QUANT_MATRICES:
+        N, K = shapes[name]
+        z = normal_f64(seed, stream_id(layer, name), 0, N * K).reshape(N, K)
+        if fmt == "i8":
+            q = np.clip(np.rint(42.0 * z), -127, 127).astype(np.int8)
+            zs = normal_f64(seed, stream_id(layer, name + "_scale"), 0, N)
+            out[name] = {"q": q, "scale": round_f16(0.02 / 42.0 * (1.0 + 0.1 * zs))}
+        elif fmt == "u4":
+            if K % group or group % 2:
+                raise ValueError(f"{name}: K={K} is not a multiple of the group {group}")
+            codes = np.clip(np.rint(7.5 + 3.5 * z), 0, 15).astype(np.uint8)
+            packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+            ng = K // group
+            zs = normal_f64(seed, stream_id(layer, name + "_scale"), 0, N * ng).reshape(N, ng)
+            zz = normal_f64(seed, stream_id(layer, name + "_zero"), 0, N * ng).reshape(N, ng)
+            out[name] = {"q": packed,
+                         "scale": round_f16(0.02 / 3.5 * (1.0 + 0.1 * zs)),
+                         "zero": np.clip(np.rint(7.5 + 0.5 * zz), 0, 15).astype(np.uint8)}
+        else:
+            raise ValueError(f"unknown format {fmt!r}")
+    return out
 
 
 def hidden_input(s: BlockShape, T: int, seed: int = 0, stream_offset: int = 0) -> np.ndarray:

@@ -27,15 +27,15 @@ MUTATIONS = [
     ("attention scale", "const double scale = 1.0 / std::sqrt(static_cast<double>(D));",
      "const double scale = 1.0 / static_cast<double>(D);"),
     ("causal mask edge", "L + t + 1,\n                 D, D, scale", "L + t,\n                 D, D, scale"),
-    ("dropped k bias", "orc_linear(w->wk, bias ? w->bk : nullptr", "orc_linear(w->wk, nullptr"),
+    ("dropped k bias", "linear(wk, bias ? w->bk : nullptr", "linear(wk, nullptr"),
     ("dropped rmsnorm eps", "std::sqrt(sum_sq / static_cast<double>(n) + eps)",
      "std::sqrt(sum_sq / static_cast<double>(n))"),
     ("dropped attention residual", "for (int64_t i = 0; i < H; ++i) h[i] += h2d(x[t * H + i]);",
      "for (int64_t i = 0; i < H; ++i) h[i] += 0.0;"),
     ("swapped swiglu operands", "act[j] = orc_silu(gate[j]) * up[j];",
      "act[j] = orc_silu(up[j]) * gate[j];"),
-    ("transposed linear", "const uint16_t* row = W + o * n_in;\n    double acc = 0.0;\n    for (int64_t i = 0; i < n_in; ++i) acc += h2d(row[i]) * x[i];",
-     "double acc = 0.0;\n    for (int64_t i = 0; i < n_in; ++i) acc += h2d(W[i * n_out + o]) * x[i];"),
+    ("transposed linear", "(void)n_out; return h2d(p[o * n_in + i]);",
+     "(void)n_in; return h2d(p[i * n_out + o]);"),
     ("softmax max not subtracted consistently", "s[j] = std::exp(s[j] - m);", "s[j] = std::exp(s[j] - 0.5 * m);"),
     ("v stored rotated", "const uint16_t vh = encode_half(v[g * D + d]);",
      "const uint16_t vh = encode_half(k[g * D + d]);"),
@@ -45,6 +45,15 @@ MUTATIONS = [
      "orc_rmsnorm(row.data(), nullptr, H, eps, y.data());"),
     ("embedding row from the position", "x[t * H + i] = E[ids[t] * H + i];",
      "x[t * H + i] = E[t * H + i];"),
+    ("i8: the first row's scale everywhere", "const double s = h2d(scale[o]);",
+     "const double s = h2d(scale[0]);"),
+    ("u4: nibble order swapped", "const int code = (i % 2 == 0) ? (byte & 0x0F) : (byte >> 4);",
+     "const int code = (i % 2 == 0) ? (byte >> 4) : (byte & 0x0F);"),
+    ("u4: zero point dropped", "(static_cast<double>(code) - static_cast<double>(zero[g]))",
+     "(static_cast<double>(code) - 0.0)"),
+    ("u4: the next group's scale and zero", "const int64_t g = o * ng + i / group;",
+     "const int64_t g = o * ng + (i / group + 1) % ng;"),
+    ("f64 weights: v projected with wk", "MatF64{m->wv}", "MatF64{m->wk}"),
 ]
 
 PIN_TESTS = [getattr(pins, n) for n in dir(pins) if n.startswith("test_")]

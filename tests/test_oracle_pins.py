@@ -446,3 +446,78 @@ def test_lm_head_ties_go_to_the_lowest_index():
     W[8] = (best.astype(np.float64) * 0.5).astype(np.float16)
     _, token = oracle.lm_head(x, g, W)
     assert token[0] == 3
+
+
+# ------------------------------------------- weight-only quantized projections
+
+def test_dequant_i8_hand_computed_rows():
+    """w = s[o] * q: signs, the clip values and a different scale per row."""
+    q = np.array([[1, -2, 127], [0, 5, -127]], dtype=np.int8)
+    s = np.array([0.5, 0.25], dtype=np.float16)
+    want = np.array([[0.5, -1.0, 63.5], [0.0, 1.25, -31.75]])
+    assert np.array_equal(oracle.dequant_i8(q, s), want)
+
+
+def test_dequant_u4_nibble_order_groups_and_zero_points():
+    """Two codes per byte, the even input in the low nibble; each group of
+    inputs has its own scale and zero point."""
+    packed = np.array([[0x21, 0xF0, 0x3C],
+                       [0x00, 0xFF, 0x87]], dtype=np.uint8)
+    # group = 2: groups are inputs (0,1), (2,3), (4,5)
+    scale = np.array([[1.0, 0.5, 2.0],
+                      [0.25, 1.0, -1.0]], dtype=np.float16)
+    zero = np.array([[1, 8, 3],
+                     [0, 15, 7]], dtype=np.uint8)
+    # row 0 codes: 1, 2 | 0, 15 | 12, 3 ; row 1 codes: 0, 0 | 15, 15 | 7, 8
+    want = np.array([[0.0, 1.0, -4.0, 3.5, 18.0, 0.0],
+                     [0.0, 0.0, 0.0, 0.0, -0.0, -1.0]])
+    got = oracle.dequant_u4(packed, scale, zero, group=2)
+    assert np.array_equal(got, want)
+    with pytest.raises(ValueError):     # K = 6 is not a multiple of 4
+        oracle.dequant_u4(packed, scale[:, :1], zero[:, :1], group=4)
+
+
+def _exact_quant_case(s, fmt, seed):
+    """Quantized matrices whose weights fp16 holds exactly (power-of-two
+    scales, codes within +-15), with the fp16 copy of those weights."""
+    rng = np.random.default_rng(seed)
+    mats, f16 = {}, {}
+    for name in oracle.MATRIX_FIELDS:
+        N, K = synth.weight_shapes(s)[name]
+        if fmt == "i8":
+            q = rng.integers(-15, 16, size=(N, K)).astype(np.int8)
+            sc = np.full(N, 2.0 ** -8, dtype=np.float16)
+            w = oracle.dequant_i8(q, sc)
+        else:
+            group = 16
+            codes = rng.integers(0, 16, size=(N, K)).astype(np.uint8)
+            packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+            sc = np.full((N, K // group), 2.0 ** -7, dtype=np.float16)
+            z = rng.integers(0, 16, size=(N, K // group)).astype(np.uint8)
+            w = oracle.dequant_u4(packed, sc, z, group)
+        assert np.array_equal(w.astype(np.float16).astype(np.float64), w)   # exact in fp16
+        mats[name] = w
+        f16[name] = w.astype(np.float16)
+    return mats, f16
+
+
+@pytest.mark.parametrize("fmt", ["i8", "u4"])
+def test_block_with_f64_weights_equals_the_fp16_block_when_exact(fmt):
+    """Dequantized weights that fp16 holds exactly give, through the f64-weight
+    entry, the same bits as the pinned fp16 block: prefill and a decode on
+    history (out, k_new, v_new and every cache slot)."""
+    s = synth.TINY
+    base = synth.block_weights(s, seed=3)
+    mats, f16 = _exact_quant_case(s, fmt, seed=3)
+    w16 = dict(base, **f16)
+    for T, L in ((6, 0), (1, 9)):
+        x = synth.hidden_input(s, T, seed=3, stream_offset=T)
+        pos = synth.positions(L, T)
+        ka, va = synth.kv_history(s, 32, L, seed=3)
+        kb, vb = ka.copy(), va.copy()
+        ra = oracle.block_forward(s, w16, x, pos, L, ka, va)
+        rb = oracle.block_forward(s, base, x, pos, L, kb, vb, mats64=mats)
+        for a, b in zip(ra, rb):
+            assert np.array_equal(a.view(np.uint16), b.view(np.uint16))
+        assert np.array_equal(ka.view(np.uint16), kb.view(np.uint16))
+        assert np.array_equal(va.view(np.uint16), vb.view(np.uint16))
