@@ -38,19 +38,16 @@ const double* half_table() {
 
 inline double h2d(uint16_t h) { return half_table()[h]; }
 
-// A weight matrix [n_out][n_in] row-major, read element by element: fp16 bit
-// patterns (the block's own weights) or f64 values (e.g. dequantized weights).
+// A weight matrix [n_out][n_in] row-major: fp16 bit patterns (the block's own
+// weights) or f64 values (e.g. dequantized weights); val(p, k) reads element
+// k of the flat array as f64.
 struct MatF16 {
   const uint16_t* p;
-  double at(int64_t o, int64_t i, int64_t n_out, int64_t n_in) const {
-    (void)n_out; return h2d(p[o * n_in + i]);
-  }
+  static double val(const uint16_t* a, int64_t k) { return h2d(a[k]); }
 };
 struct MatF64 {
   const double* p;
-  double at(int64_t o, int64_t i, int64_t n_out, int64_t n_in) const {
-    (void)n_out; return p[o * n_in + i];
-  }
+  static double val(const double* a, int64_t k) { return a[k]; }
 };
 
 // y[o] = sum_i W[o][i] * x[i] (+ b[o]), i ascending.
@@ -58,8 +55,9 @@ template <class M>
 void linear(const M& W, const uint16_t* b, const double* x, int64_t n_out, int64_t n_in,
             double* y) {
   for (int64_t o = 0; o < n_out; ++o) {
+    const auto* row = W.p + o * n_in;
     double acc = 0.0;
-    for (int64_t i = 0; i < n_in; ++i) acc += W.at(o, i, n_out, n_in) * x[i];
+    for (int64_t i = 0; i < n_in; ++i) acc += M::val(row, i) * x[i];
     y[o] = b ? acc + h2d(b[o]) : acc;
   }
 }

@@ -34,8 +34,8 @@ MUTATIONS = [
      "for (int64_t i = 0; i < H; ++i) h[i] += 0.0;"),
     ("swapped swiglu operands", "act[j] = orc_silu(gate[j]) * up[j];",
      "act[j] = orc_silu(up[j]) * gate[j];"),
-    ("transposed linear", "(void)n_out; return h2d(p[o * n_in + i]);",
-     "(void)n_in; return h2d(p[i * n_out + o]);"),
+    ("transposed linear", "acc += M::val(row, i) * x[i];",
+     "acc += M::val(W.p, i * n_out + o) * x[i];"),
     ("softmax max not subtracted consistently", "s[j] = std::exp(s[j] - m);", "s[j] = std::exp(s[j] - 0.5 * m);"),
     ("v stored rotated", "const uint16_t vh = encode_half(v[g * D + d]);",
      "const uint16_t vh = encode_half(k[g * D + d]);"),
