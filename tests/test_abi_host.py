@@ -80,3 +80,13 @@ def test_missing_library_fails_loudly(tmp_path):
             blk.load(str(tmp_path / "libblk.so"))
     finally:
         blk._lib = saved
+
+
+def test_batched_entry_points_reject_a_null_handle(lib):
+    w = blk.BlkWeights()
+    assert lib.blk_decode_batch(None, ctypes.byref(w), 16, 16, 16, 1, 0, 16, 16, 16, None, None,
+                                16, 1 << 20, None) == blk.BLK_ERR_NULL
+    assert lib.blk_decode_batch_stack(None, ctypes.byref(w), 1, None, None, 16, 16, 16, 1, 0, 16,
+                                      16, 1 << 20, None) == blk.BLK_ERR_NULL
+    assert lib.blk_decode_batch_workspace_bytes(None, 4) == 0
+    assert lib.blk_decode_batch_stack_workspace_bytes(None, 4) == 0

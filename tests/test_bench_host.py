@@ -53,3 +53,26 @@ def test_reference_arm_under_torchrun_world_size_2():
     assert d["impl"] == "reference" and d["n_gpus"] == 2
     assert d["value"] > 0 and d["cpu_baseline"]["kind"] == "oracle"
     assert d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_decode_bytes_follow_the_shape():
+    """Per layer of the 1.5B shape: 93,595,648 weight bytes (q/k/v with bias,
+    o, gate, up, down, two gains) plus 2 * Hkv * D * 2 = 1,024 K/V bytes per
+    attended slot."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import synth
+    total, weights = bench.decode_bytes(synth.QWEN2_1P5B, 1024, 28)
+    assert weights == 28 * 93_595_648
+    assert total == 28 * (93_595_648 + 1024 * 1025)
+
+
+def test_prefill_flops_follow_the_shape():
+    """[1, 1024] through one 1.5B layer: 95.83 GFLOP of projections and
+    4 * D * Hq * (1024 * 1025 / 2) of causal attention."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import synth
+    gemm, attn = bench.prefill_flops(synth.QWEN2_1P5B, 1024)
+    assert abs(sum(gemm.values()) - 95.83e9) < 0.01e9
+    assert attn == 4 * 128 * 12 * (1024 * 1025 // 2)

@@ -54,3 +54,26 @@ def test_fp16_rounding_matches_numpy():
     ours = synth.round_f16(vals).view(np.uint16)
     ref = vals.astype(np.float16).view(np.uint16)
     assert np.array_equal(ours, ref)
+
+
+def test_quant_weights_are_seeded_and_in_range():
+    a = synth.quant_weights(synth.TINY, "i8", seed=1)
+    b = synth.quant_weights(synth.TINY, "i8", seed=1)
+    c = synth.quant_weights(synth.TINY, "i8", seed=2)
+    shapes = synth.weight_shapes(synth.TINY)
+    for n in synth.QUANT_MATRICES:
+        N, K = shapes[n]
+        assert a[n]["q"].shape == (N, K) and a[n]["q"].dtype == np.int8
+        assert np.array_equal(a[n]["q"], b[n]["q"]) and not np.array_equal(a[n]["q"], c[n]["q"])
+        assert a[n]["q"].min() >= -127 and a[n]["scale"].shape == (N,)
+        assert a[n]["scale"].dtype == np.float16 and (a[n]["scale"] > 0).all()
+    u = synth.quant_weights(synth.TINY, "u4", group=16)
+    for n in synth.QUANT_MATRICES:
+        N, K = shapes[n]
+        assert u[n]["q"].shape == (N, K // 2) and u[n]["q"].dtype == np.uint8
+        assert u[n]["scale"].shape == (N, K // 16) and u[n]["zero"].shape == (N, K // 16)
+        assert u[n]["zero"].max() <= 15
+    # distinct matrices draw from distinct streams
+    assert not np.array_equal(u["wk"]["q"], u["wv"]["q"])
+    with pytest.raises(ValueError):            # intermediate 688 is not a multiple of 128
+        synth.quant_weights(synth.TINY, "u4", group=128)
