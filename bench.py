@@ -13,7 +13,11 @@ Also reported: decode of the 28-layer 1.5B stack at cache lengths 1024,
 4096, 16384 and 32768 (one CUDA graph per step, KV appended in place;
 2.6 GB of weights per step, so no flush is needed), µs/step and the
 fraction of the HBM roofline (weight + KV bytes over measured copy
-bandwidth).
+bandwidth); the whole model per generated token (embedding, the stack,
+final RMSNorm + LM head, greedy argmax); the LM head alone; and batched
+decode of B sequences through the stack (decode_batch).  The CPU oracle is
+timed on a bounded prefill sample (cpu_baseline) and on one decode layer
+extrapolated to the stack (cpu_baseline_decode).
 
 --impl reference times the CPU oracle (single-threaded f64) on a bounded
 sample of the same prefill workload.  Under torchrun (N > 1) each rank runs
@@ -43,12 +47,10 @@ PREFILL_T = 1024
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from
 # the ncu captures summarised in profiles/ (prefill_kernels_1p5b_T1024.md,
-# decode_persistent_1p5b_28layers_ctx4096.md).  Must be set back to None
-# whenever the kernel changes.
-# The GEMMs (epilogues, A boxes, split-K paths), the split-K reduction and
-# the decode kernel (its SiLU) changed after their last capture, so their
-# entries are None until they are captured again; the last figures are kept
-# in the profiles as history.
+# decode_persistent_1p5b_28layers_ctx4096.md, lm_head_1p5b_vocab151936.md);
+# None whenever the kernel changed after its last capture.  The GEMMs
+# (epilogues, A boxes, split-K paths) and the decode kernel (its SiLU) did;
+# their last figures stay in the profiles as history.
 NCU_TRAFFIC = {
     "gemm_gateup": None,
     "gemm_down": None,
@@ -228,6 +230,32 @@ def oracle_prefill_sample(n_rows: int, rotate: int = 0):
     desc = (f"oracle on the 1.5B-shaped layer, prefill [1,1024]: K/V for all 1024 rows + full "
             f"output of {n_rows} evenly spaced rows, scaled to 1024 rows; single-threaded")
     return PREFILL_T / t_full, spent, desc
+
+
+def synth_layers() -> int:
+    import synth
+    return synth.QWEN2_1P5B.n_layers
+
+
+def oracle_decode_sample(L: int = 1024, n_layers: int = 28):
+    """Times the oracle's decode of one token through one 1.5B-shaped layer
+    at L history slots, and extrapolates to an n_layers step.  Returns
+    (us per step extrapolated, seconds spent, sample description)."""
+    import oracle
+    import synth
+    s = synth.QWEN2_1P5B
+    oracle.build()
+    if "w" not in _ORACLE_INPUTS:
+        _ORACLE_INPUTS["w"] = synth.block_weights(s, seed=0)
+    w = _ORACLE_INPUTS["w"]
+    kc, vc = synth.kv_history(s, L + 1, L, seed=0)
+    x = synth.hidden_input(s, 1, seed=0, stream_offset=1)
+    t0 = time.perf_counter()
+    oracle.block_forward(s, w, x, synth.positions(L, 1), L, kc, vc)
+    spent = time.perf_counter() - t0
+    desc = (f"oracle decode of one token through one 1.5B-shaped layer at ctx {L}, "
+            f"extrapolated x{n_layers} layers; single-threaded")
+    return spent * n_layers * 1e6, spent, desc
 
 
 # ------------------------------------------------------------------ ours
@@ -679,6 +707,11 @@ def main():
         result["cpu_baseline"] = {"value": tok_s, "unit": UNIT, "cores": 1, "kind": "oracle",
                                   "sample": desc, "host_cores": os.cpu_count(),
                                   "seconds": secs}
+        if "decode" in result:
+            us, secs_d, desc_d = oracle_decode_sample(1024, synth_layers())
+            result["cpu_baseline_decode"] = {"value": us, "unit": "us/step", "cores": 1,
+                                             "kind": "oracle", "sample": desc_d,
+                                             "seconds": secs_d}
     if rank == 0:
         print(json.dumps(result))
     if ws > 1:

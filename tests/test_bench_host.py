@@ -76,3 +76,11 @@ def test_prefill_flops_follow_the_shape():
     gemm, attn = bench.prefill_flops(synth.QWEN2_1P5B, 1024)
     assert abs(sum(gemm.values()) - 95.83e9) < 0.01e9
     assert attn == 4 * 128 * 12 * (1024 * 1025 // 2)
+
+
+def test_oracle_decode_sample_extrapolates_over_layers():
+    sys.path.insert(0, ROOT)
+    import bench
+    us, secs, desc = bench.oracle_decode_sample(L=16, n_layers=3)
+    assert secs > 0 and abs(us - 3 * secs * 1e6) < 1e-6 * us
+    assert "extrapolated x3 layers" in desc
