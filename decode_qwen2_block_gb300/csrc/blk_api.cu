@@ -529,7 +529,14 @@ int blk_set_flags(blk_handle h, uint32_t flags) {
 size_t blk_workspace_bytes(blk_handle h, int64_t max_T) {
   if (!h || max_T < 1) return 0;
   const blk_config& c = h->cfg;
-  const size_t a = prefill_ws(c, max_T, h->num_sms).total;
+  // Enough for every T <= max_T: the attention's chunk partials shrink at
+  // some row-block counts, so take the largest layout over the T that end a
+  // 128-row block (within one block the other buffers only grow with T).
+  size_t a = prefill_ws(c, max_T, h->num_sms).total;
+  for (int64_t t = 128; t < max_T; t += 128) {
+    const size_t at = prefill_ws(c, t, h->num_sms).total;
+    if (at > a) a = at;
+  }
   const size_t b = decode_ws_bytes(c.hidden, c.n_heads, c.n_kv_heads, c.head_dim,
                                    c.intermediate, h->num_sms);
   return a > b ? a : b;
@@ -719,9 +726,20 @@ int blk_lm_head(blk_handle h, const void* x, int64_t T, const void* norm_g, cons
   return BLK_OK;
 }
 
+// Largest batched-decode layout over B' <= max_B (the attention's split
+// partials, B' x splits(B'), do not grow monotonically with B').
+static size_t decode_batch_ws_upto(const blk_config& c, int64_t max_B, int num_sms) {
+  size_t best = 0;
+  for (int64_t b = 1; b <= max_B; ++b) {
+    const size_t t = decode_batch_ws(c, b, num_sms).total;
+    if (t > best) best = t;
+  }
+  return best;
+}
+
 size_t blk_decode_batch_workspace_bytes(blk_handle h, int64_t max_B) {
-  if (!h || max_B < 1) return 0;
-  return decode_batch_ws(h->cfg, max_B, h->num_sms).total;
+  if (!h || max_B < 1 || max_B > 4096) return 0;
+  return decode_batch_ws_upto(h->cfg, max_B, h->num_sms);
 }
 
 int blk_decode_batch(blk_handle h, const blk_weights* w, const void* x, const int64_t* pos,
@@ -735,7 +753,7 @@ int blk_decode_batch(blk_handle h, const blk_weights* w, const void* x, const in
 size_t blk_decode_batch_stack_workspace_bytes(blk_handle h, int64_t max_B) {
   if (!h || max_B < 1 || max_B > 4096) return 0;
   const size_t act = align_up((size_t)max_B * h->cfg.hidden * 2);
-  return decode_batch_ws(h->cfg, max_B, h->num_sms).total + 2 * act;
+  return decode_batch_ws_upto(h->cfg, max_B, h->num_sms) + 2 * act;
 }
 
 int blk_decode_batch_stack(blk_handle h, const blk_weights* w, int n_layers,

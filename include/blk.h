@@ -115,8 +115,8 @@ void blk_destroy(blk_handle h);
 
 int blk_set_flags(blk_handle h, uint32_t flags);
 
-/* Workspace bytes needed by a call with up to max_T new tokens (decode needs
- * max_T = 1).  0 on a bad handle or max_T < 1. */
+/* Workspace bytes enough for every call with T <= max_T new tokens (decode
+ * needs max_T = 1).  0 on a bad handle or max_T < 1. */
 size_t blk_workspace_bytes(blk_handle h, int64_t max_T);
 
 /* prefill (Listing 1): T new tokens, no history (cache_len = 0).
@@ -256,7 +256,9 @@ int blk_set_trace(blk_handle h, void* device_buffer, size_t bytes);
  * BLK_ERR_ALIGN, BLK_ERR_SHAPE (B outside [1, 4096], more than 16 query heads
  * per kv head), BLK_ERR_CACHE_OVERFLOW (max_cache_len), BLK_ERR_WORKSPACE or
  * BLK_ERR_CUDA.  Asynchronous on `stream`.  The cache lengths are read on the
- * device, so one captured CUDA graph serves consecutive steps. */
+ * device, so one captured CUDA graph serves consecutive steps.
+ * blk_decode_batch_workspace_bytes: enough for every call with B <= max_B
+ * sequences; 0 on a bad handle or max_B outside [1, 4096]. */
 size_t blk_decode_batch_workspace_bytes(blk_handle h, int64_t max_B);
 int blk_decode_batch(blk_handle h, const blk_weights* w, const void* x, const int64_t* pos,
                      const int64_t* cache_lens, int64_t B, int64_t max_cache_len, void* k_cache,
@@ -270,9 +272,9 @@ int blk_decode_batch(blk_handle h, const blk_weights* w, const void* x, const in
  *   k_caches, v_caches   host arrays [n_layers] of device caches, each
  *                        [B, n_kv_heads, max_ctx, head_dim] as for blk_decode_batch
  *   x, out               device fp16 [B, hidden]; out must not alias x
- *   ws                   blk_decode_batch_stack_workspace_bytes(h, B) bytes or
- *                        more (the one-layer workspace plus two [B, hidden]
- *                        fp16 buffers between layers)
+ *   ws                   blk_decode_batch_stack_workspace_bytes(h, max_B) bytes
+ *                        or more, for any max_B >= B (the one-layer workspace
+ *                        plus two [B, hidden] fp16 buffers between layers)
  * No k_new / v_new: the new K/V are in each layer's cache slot.  Every
  * layer's arguments are checked before anything is enqueued.  Returns the
  * codes of blk_decode_batch, BLK_ERR_NULL for a NULL array and BLK_ERR_SHAPE

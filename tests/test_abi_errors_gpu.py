@@ -81,3 +81,16 @@ def test_workspace_size_is_monotone(setup):
     sizes = [db.block.workspace_bytes(t) for t in (1, 2, 8, 100)]
     assert all(a <= b for a, b in zip(sizes, sizes[1:]))
     assert db.block.workspace_bytes(0) == 0
+
+
+def test_workspace_queries_cover_every_smaller_call():
+    """blk_workspace_bytes(max_T) and blk_decode_batch_workspace_bytes(max_B)
+    never shrink as the bound grows: a workspace sized for a bound serves
+    every smaller call (the attention's partial buffers alone do shrink at
+    some sizes)."""
+    for s in (synth.TINY, synth.QWEN2_1P5B):
+        b = blk.Block(s, 4096)
+        t_sizes = [b.workspace_bytes(T) for T in range(1, 3000, 5)]
+        assert all(x <= y for x, y in zip(t_sizes, t_sizes[1:]))
+        b_sizes = [b.decode_batch_workspace_bytes(B) for B in range(1, 400)]
+        assert all(x <= y for x, y in zip(b_sizes, b_sizes[1:]))
