@@ -37,7 +37,8 @@ EXPORTED = ("blk_create", "blk_destroy", "blk_set_flags", "blk_workspace_bytes",
             "blk_timing_collect", "blk_timing_read", "blk_decode_static", "blk_decode_stack",
             "blk_set_trace", "blk_embed", "blk_lm_head_workspace_bytes", "blk_lm_head",
             "blk_decode_batch_workspace_bytes", "blk_decode_batch",
-            "blk_decode_batch_stack_workspace_bytes", "blk_decode_batch_stack")
+            "blk_decode_batch_stack_workspace_bytes", "blk_decode_batch_stack",
+            "blk_wait_probe")
 BLK_N_KERNELS = 16
 
 WEIGHT_FIELDS = ("ln1_g", "wq", "wk", "wv", "bq", "bk", "bv", "wo", "ln2_g", "w_gate", "w_up",
@@ -103,6 +104,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.blk_decode_static.argtypes = [vp, ctypes.POINTER(BlkWeights), vp, vp, i64, vp, vp, vp, vp,
                                       vp, vp]
     lib.blk_decode_static.restype = i32
+    lib.blk_wait_probe.argtypes = [vp, vp, ctypes.c_uint64, vp]
+    lib.blk_wait_probe.restype = i32
     lib.blk_check.argtypes = [vp, vp]
     lib.blk_check.restype = i32
     lib.blk_status_str.argtypes = [i32]
@@ -206,6 +209,11 @@ def blk_decode_batch(handle, w: BlkWeights, x, pos, cache_lens, B, max_cache_len
                      v_cache, out, k_new, v_new, ws, ws_bytes, stream) -> int:
     return load().blk_decode_batch(handle, ctypes.byref(w), x, pos, cache_lens, B, max_cache_len,
                                    k_cache, v_cache, out, k_new, v_new, ws, ws_bytes, stream)
+
+
+def blk_wait_probe(handle, flag_ptr, limit_ns: int, stream) -> int:
+    """One kernel waiting (bounded) for the device int at flag_ptr; see include/blk.h."""
+    return load().blk_wait_probe(handle, flag_ptr, limit_ns, stream)
 
 
 def blk_decode_batch_stack_workspace_bytes(handle, max_B: int) -> int:

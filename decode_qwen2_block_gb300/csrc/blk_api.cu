@@ -654,6 +654,34 @@ int blk_decode_stack(blk_handle h, const blk_weights* w, int n_layers,
   return BLK_OK;
 }
 
+}  // extern "C"
+
+namespace {
+// Polls *flag until it is non-zero or limit_ns of %globaltimer have passed;
+// a timeout records kDevTimeout in the status word, as every kernel's own
+// bounded waits do.
+__global__ void wait_probe_kernel(const volatile int* flag, uint64_t limit_ns, int* err) {
+  const uint64_t t0 = global_ns();
+  while (*flag == 0) {
+    if (global_ns() - t0 > limit_ns) {
+      set_error(err, kDevTimeout);
+      return;
+    }
+  }
+}
+}  // namespace
+
+extern "C" {
+
+int blk_wait_probe(blk_handle h, const void* flag, uint64_t limit_ns, void* stream) {
+  if (!h || !flag) return BLK_ERR_NULL;
+  if (!aligned(flag, 4)) return BLK_ERR_ALIGN;
+  if (limit_ns < 1000 || limit_ns > 2000000000ull) return BLK_ERR_SHAPE;
+  wait_probe_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const volatile int*>(flag), limit_ns, h->status);
+  return cudaGetLastError() == cudaSuccess ? BLK_OK : BLK_ERR_CUDA;
+}
+
 int blk_check(blk_handle h, void* stream) {
   if (!h) return BLK_ERR_NULL;
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)

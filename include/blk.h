@@ -211,6 +211,15 @@ int blk_decode_static(blk_handle h, const blk_weights* w, const void* x,
  * the vocabulary), or BLK_ERR_CUDA if the stream failed. */
 int blk_check(blk_handle h, void* stream);
 
+/* Diagnostics of the failure path: launches one kernel that waits for the
+ * device int at `flag` (4-byte aligned) to become non-zero, bounded by
+ * limit_ns (1 us .. 2 s) of %globaltimer, exactly like the kernels' own
+ * waits.  If the limit passes first, the next blk_check reports
+ * BLK_ERR_DEVICE_TIMEOUT and the context stays usable.  Returns BLK_OK,
+ * BLK_ERR_NULL, BLK_ERR_ALIGN, BLK_ERR_SHAPE (limit out of range) or
+ * BLK_ERR_CUDA. */
+int blk_wait_probe(blk_handle h, const void* flag, uint64_t limit_ns, void* stream);
+
 /* Per-kernel timing, for benchmarks.  While on, every kernel a call enqueues
  * is bracketed by CUDA events recorded on the call's stream (this keeps
  * consecutive kernels from overlapping, so time the whole step with timing

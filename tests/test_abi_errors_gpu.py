@@ -94,3 +94,25 @@ def test_workspace_queries_cover_every_smaller_call():
         assert all(x <= y for x, y in zip(t_sizes, t_sizes[1:]))
         b_sizes = [b.decode_batch_workspace_bytes(B) for B in range(1, 400)]
         assert all(x <= y for x, y in zip(b_sizes, b_sizes[1:]))
+
+
+def test_bounded_wait_times_out_and_the_context_stays_usable(setup):
+    """A device wait on a flag that nothing sets gives up after its limit,
+    blk_check reports the timeout, and the same context then runs the block."""
+    import time
+    s, db, x, pos, kc, vc, out = setup
+    P = lambda t: t.data_ptr()
+    h = db.block.handle
+    stream = torch.cuda.current_stream().cuda_stream
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t0 = time.perf_counter()
+    assert blk.blk_wait_probe(h, P(flag), 50_000_000, stream) == blk.BLK_OK
+    assert blk.blk_check(h, stream) == blk.BLK_ERR_DEVICE_TIMEOUT
+    assert time.perf_counter() - t0 < 10
+    flag.fill_(1)
+    assert blk.blk_wait_probe(h, P(flag), 50_000_000, stream) == blk.BLK_OK
+    assert blk.blk_check(h, stream) == blk.BLK_OK
+    assert _prefill(db, P(x), P(pos), 8, P(kc), P(vc), P(out)) == blk.BLK_OK
+    assert blk.blk_check(h, stream) == blk.BLK_OK
+    assert blk.blk_wait_probe(h, P(flag), 10, stream) == blk.BLK_ERR_SHAPE
+    assert blk.blk_wait_probe(h, P(flag) + 2, 50_000_000, stream) == blk.BLK_ERR_ALIGN
