@@ -521,3 +521,27 @@ def test_block_with_f64_weights_equals_the_fp16_block_when_exact(fmt):
             assert np.array_equal(a.view(np.uint16), b.view(np.uint16))
         assert np.array_equal(ka.view(np.uint16), kb.view(np.uint16))
         assert np.array_equal(va.view(np.uint16), vb.view(np.uint16))
+
+
+@pytest.mark.parametrize("fmt", ["i8", "u4"])
+def test_block_with_dequantized_weights_matches_bruteforce(fmt):
+    """Seeded quantized weights (not exact in fp16) through the f64-weight
+    entry against the independent numpy restatement fed the same f64 matrices,
+    at the one-ulp tolerance of the fp16 block's brute-force pin."""
+    s = synth.TINY
+    T, L = 4, 16
+    base = synth.block_weights(s, seed=5)
+    qw = synth.quant_weights(s, fmt, seed=5, group=16)
+    mats = {}
+    for name, d in qw.items():
+        mats[name] = (oracle.dequant_i8(d["q"], d["scale"]) if fmt == "i8"
+                      else oracle.dequant_u4(d["q"], d["scale"], d["zero"], 16))
+    x = synth.hidden_input(s, T, seed=5)
+    pos = synth.positions(L, T)
+    kc, vc = synth.kv_history(s, 64, L, seed=5, sentinel=-7.0)
+    bo, bk, bv = brute_block(s, dict(base, **mats), x, pos, L, kc.copy(), vc.copy())
+    out, kn, vn = oracle.block_forward(s, base, x, pos, L, kc, vc, mats64=mats)
+    assert np.max(np.abs(kn.astype(np.float64) - bk.astype(np.float64))) <= 2.0 ** -10
+    assert np.max(np.abs(vn.astype(np.float64) - bv.astype(np.float64))) <= 2.0 ** -10
+    assert np.abs(out.astype(np.float64) - bo.astype(np.float64)).max() <= 2.0 ** -8
+    assert np.mean(out.view(np.uint16) == bo.view(np.uint16)) > 0.99
