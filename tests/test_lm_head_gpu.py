@@ -1,11 +1,11 @@
-"""GPU parity of the model head around the block stack: token embedding (bit
-for bit), final RMSNorm + LM head logits (relative L2 <= 1e-2, max abs <=
-5e-2) and the greedy token.  Where several tokens are correct (logits closer than the tolerance)
-the test checks that the returned one is valid: its oracle logit is within the
-tolerance of the largest; when the oracle's two best logits are further apart
-than twice the tolerance the token must equal the oracle's.  Equal weight rows
-give equal fp32 logits on the GPU, so the lowest-index rule is checked exactly.
-"""
+"""GPU parity of the model head around the block stack: token embedding (bit for
+bit), final RMSNorm + LM head logits (relative L2 <= 1e-2, max abs <= 5e-2)
+and the greedy token. Where several tokens are correct (logits closer than the
+tolerance) the test checks that the returned one is valid: its oracle logit is
+within the tolerance of the largest; when the oracle's two best logits are
+further apart than twice the tolerance the token must equal the oracle's.
+Equal weight rows give equal fp32 logits on the GPU, so the lowest-index rule
+is checked exactly."""
 import numpy as np
 import pytest
 import torch
