@@ -90,3 +90,4 @@ def test_batched_entry_points_reject_a_null_handle(lib):
                                       16, 1 << 20, None) == blk.BLK_ERR_NULL
     assert lib.blk_decode_batch_workspace_bytes(None, 4) == 0
     assert lib.blk_decode_batch_stack_workspace_bytes(None, 4) == 0
+    assert lib.blk_wait_probe(None, 16, 1_000_000, None) == blk.BLK_ERR_NULL
