@@ -9,19 +9,28 @@ causal GQA attention, o_proj + residual, RMSNorm, SwiGLU MLP + residual).
 The L2 is flushed (a 256 MB write) before every timed step, because one
 layer's weights (94 MB) fit in the 129 MB L2.
 
-Also reported: decode of the 28-layer 1.5B stack at cache lengths 1024,
-4096, 16384 and 32768 (one CUDA graph per step, KV appended in place;
-2.6 GB of weights per step, so no flush is needed), µs/step and the
-fraction of the HBM roofline (weight + KV bytes over measured copy
-bandwidth); the whole model per generated token (embedding, the stack,
-final RMSNorm + LM head, greedy argmax); the LM head alone; and batched
-decode of B sequences through the stack (decode_batch).  The CPU oracle is
-timed on a bounded prefill sample (cpu_baseline) and on one decode layer
-extrapolated to the stack (cpu_baseline_decode).
+Also reported, each as an absolute number and a fraction of its roofline:
+  decode         the 28-layer 1.5B stack at cache lengths 1024, 4096, 16384
+                 and 32768 (one CUDA graph per step, KV appended in place),
+                 us/step vs the HBM roofline (weight + KV bytes over the
+                 measured copy bandwidth), plus an end-to-end figure (host
+                 hidden row in, host output row out, through the public API)
+  prefill_kv_28  the 28-layer 1.5B stack, 512 new tokens at positions
+                 3584..4095 on 3584 history slots: tok/s, GEMM time vs the
+                 tensor peak, attention time and share reported separately
+  gqa4096        32 layers of hidden 4096 / 32 q heads / 2 kv heads: a
+                 prefill of 100 tokens, then 256 decode steps at positions
+                 100..355 (both bound by HBM bytes)
+  lm_head, model_per_token, decode_batch  the model head, a whole generated
+                 token, batched decode of B sequences
+The weights of every leg exceed the L2 except the headline's (flushed).
+The CPU oracle is timed on a bounded prefill sample (cpu_baseline) and on one
+decode layer extrapolated to the stack (cpu_baseline_decode).  The last key
+of the line, "summary", repeats the main figures in a few hundred bytes.
 
---impl reference times the CPU oracle (single-threaded f64) on a bounded
-sample of the same prefill workload.  Under torchrun (N > 1) each rank runs
-an independent replica (no collective on the data path); rank 0 prints the
+--impl reference times the CPU oracle (single-threaded f64) on the same
+bounded prefill sample per step.  Under torchrun (N > 1) each rank runs an
+independent replica (no collective on the data path); rank 0 prints the
 whole-job numbers.
 """
 from __future__ import annotations
@@ -44,19 +53,19 @@ METRIC = "prefill tok/s (1.5B-shaped layer, [1,1024]) + decode us/step vs ctx (2
 UNIT = "tok/s"
 DECODE_CTX = (1024, 4096, 16384, 32768)
 PREFILL_T = 1024
+ORACLE_SAMPLE_ROWS = 32     # full-output rows of the oracle's prefill sample
+PKV_HIST, PKV_T = 3584, 512        # prefill_kv leg: history slots, new tokens
+G4_PREFILL, G4_DECODES = 100, 256  # hidden-4096 leg: prefill tokens, decode steps
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from
-# the ncu captures summarised in profiles/ (prefill_kernels_1p5b_T1024.md,
-# decode_persistent_1p5b_28layers_ctx4096.md, lm_head_1p5b_vocab151936.md);
-# None whenever the kernel changed after its last capture.  The GEMMs
-# (epilogues, A boxes, split-K paths) and the decode kernel (its SiLU) did;
-# their last figures stay in the profiles as history.
+# one ncu capture of the kernel as it is built now; None when the kernel
+# changed after its last capture.
 NCU_TRAFFIC = {
     "gemm_gateup": None,
     "gemm_down": None,
     "gemm_qkv": None,
     "gemm_o": None,
-    "attn_prefill": 4.242944e6,
+    "attn_prefill": None,
     "lm_head": 466853632 + 206080,
     ("decode_persistent", 4096): None,
 }
@@ -74,8 +83,11 @@ def parse():
     ap.add_argument("--decode-batch", type=str, default="8,32,64",
                     help="batch sizes of the batched decode table (ctx --decode-batch-ctx)")
     ap.add_argument("--decode-batch-ctx", type=int, default=1024)
-    ap.add_argument("--only", choices=("prefill", "decode", "decode_batch"), default=None,
-                    help="run one part (for profiling); the headline needs both")
+    ap.add_argument("--only", choices=("prefill", "decode", "decode_batch", "prefill_kv",
+                                       "gqa4096", "decode_layer"), default=None,
+                    help="run one part (for profiling); the headline needs the prefill.  "
+                         "decode_layer runs one 1.5B-shaped layer of decode at ctx "
+                         "--decode-ctx[0] (small enough for an ncu capture)")
     return ap.parse_args()
 
 
@@ -200,10 +212,13 @@ def decode_bytes(s, L, n_layers):
 _ORACLE_INPUTS = {}
 
 
-def oracle_prefill_sample(n_rows: int, rotate: int = 0):
-    """Times the oracle on the prefill workload: K/V of all 1024 rows plus the
-    full block output of n_rows evenly spaced rows; returns (tok/s
-    extrapolated to all rows, seconds spent, sample description)."""
+def oracle_prefill_sample(n_rows: int, rotate: int = 0, t_kv: float | None = None):
+    """Times the oracle on a bounded sample of the prefill workload: K/V of
+    all 1024 rows plus the full block output of n_rows evenly spaced rows.
+    The whole-layer figure is extrapolated from it: t_kv (the K/V of every
+    row plus one output row, timed once when not given) + the sampled rows'
+    cost scaled to 1024 rows.  Returns (tok/s extrapolated, seconds the
+    sample took, t_kv, description)."""
     import oracle
     import synth
     s = synth.QWEN2_1P5B
@@ -213,23 +228,23 @@ def oracle_prefill_sample(n_rows: int, rotate: int = 0):
                               x=synth.hidden_input(s, PREFILL_T, seed=0),
                               pos=synth.positions(0, PREFILL_T))
     w, x, pos = _ORACLE_INPUTS["w"], _ORACLE_INPUTS["x"], _ORACLE_INPUTS["pos"]
-    kc, vc = synth.kv_history(s, PREFILL_T, 0)
-    t0 = time.perf_counter()
-    oracle.block_forward(s, w, x, pos, 0, kc, vc, rows=[0])
-    t_kv = time.perf_counter() - t0               # all K/V rows + one output row
-    spent = t_kv
+    if t_kv is None:
+        kc, vc = synth.kv_history(s, PREFILL_T, 0)
+        t0 = time.perf_counter()
+        oracle.block_forward(s, w, x, pos, 0, kc, vc, rows=[0])
+        t_kv = time.perf_counter() - t0           # all K/V rows + one output row
     step = PREFILL_T // n_rows
     rows = [(i * step + rotate) % PREFILL_T for i in range(n_rows)]
     kc2, vc2 = synth.kv_history(s, PREFILL_T, 0)
     t0 = time.perf_counter()
     oracle.block_forward(s, w, x, pos, 0, kc2, vc2, rows=rows)
-    t2 = time.perf_counter() - t0
-    spent += t2
-    t_rows = max(t2 - t_kv, 1e-9)                 # cost of the sampled output rows
+    spent = time.perf_counter() - t0
+    t_rows = max(spent - t_kv, 1e-9)              # cost of the sampled output rows
     t_full = t_kv + t_rows * PREFILL_T / n_rows
     desc = (f"oracle on the 1.5B-shaped layer, prefill [1,1024]: K/V for all 1024 rows + full "
-            f"output of {n_rows} evenly spaced rows, scaled to 1024 rows; single-threaded")
-    return PREFILL_T / t_full, spent, desc
+            f"output of {n_rows} evenly spaced rows per step; tok/s extrapolated to 1024 rows; "
+            f"single-threaded")
+    return PREFILL_T / t_full, spent, t_kv, desc
 
 
 def synth_layers() -> int:
@@ -273,19 +288,20 @@ def bench_ours(args, ws, rank, local):
     stream = torch.cuda.current_stream()
     s = synth.QWEN2_1P5B
     K, W = args.steps, args.warmup
-    if args.only == "decode":
+    parts = {"decode": ("decode us/step (28 layers)", bench_decode),
+             "decode_batch": ("batched decode tok/s (28 layers)", bench_decode_batch),
+             "prefill_kv": ("prefill_kv tok/s (28 layers, 512 on 3584)", bench_prefill_kv_stack),
+             "gqa4096": ("hidden-4096 32-layer prefill + decode", bench_gqa4096),
+             "decode_layer": ("decode us/launch (1 layer)", bench_decode_layer)}
+    if args.only in parts:
         clocks = ClockSampler(local)
         clocks.start()
-        dec = bench_decode(args, s, dev, stream, peaks, ws)
-        head = bench_lm_head(args, s, dev, stream, peaks, ws)
-        return {"metric": "decode us/step (28 layers)", "decode": dec, "lm_head": head,
-                "clocks": clocks.stop()}
-    if args.only == "decode_batch":
-        clocks = ClockSampler(local)
-        clocks.start()
-        db = bench_decode_batch(args, s, dev, stream, peaks, ws)
-        return {"metric": "batched decode tok/s (28 layers)", "decode_batch": db,
-                "clocks": clocks.stop()}
+        metric, fn = parts[args.only]
+        res = {"metric": metric, args.only: fn(args, s, dev, stream, peaks, ws)}
+        if args.only == "decode":
+            res["lm_head"] = bench_lm_head(args, s, dev, stream, peaks, ws)
+        res["clocks"] = clocks.stop()
+        return res
 
     # ---------------- prefill, one layer, [1, 1024] ----------------
     T = PREFILL_T
@@ -412,11 +428,15 @@ def bench_ours(args, ws, rank, local):
         "kernels": kernels,
     }
 
-    # ---------------- decode, 28 layers ----------------
+    # ---------------- decode, prefill_kv, hidden 4096 ----------------
     if not args.no_decode and args.only != "prefill":
         result["decode"] = bench_decode(args, s, dev, stream, peaks, ws)
         result["lm_head"] = bench_lm_head(args, s, dev, stream, peaks, ws)
         result["decode_batch"] = bench_decode_batch(args, s, dev, stream, peaks, ws)
+        result["prefill_kv_28"] = bench_prefill_kv_stack(args, s, dev, stream, peaks, ws)
+        _STACK_W.clear()
+        torch.cuda.empty_cache()
+        result["gqa4096"] = bench_gqa4096(args, s, dev, stream, peaks, ws)
     result["clocks"] = clocks.stop()
     return result
 
@@ -531,10 +551,7 @@ def bench_decode_batch(args, s, dev, stream, peaks, ws):
     C = L0 + W + K + 8
     Bmax = max(Bs)
     H = s.hidden
-    wd = []
-    for l in range(n):
-        wnp = synth.block_weights(s, layer=l, seed=0)
-        wd.append({k: torch.from_numpy(v).to(dev) for k, v in wnp.items()})
+    wd = stack_weights(s, dev)
     caches = []
     for l in range(n):
         k, v = synth.kv_history(s, C, L0, layer=l, seed=0)
@@ -585,24 +602,87 @@ def bench_decode_batch(args, s, dev, stream, peaks, ws):
                "achieved_gbs": achieved, "frac_of_hbm_peak": achieved / peaks["hbm_gbs"],
                "roofline_us": nbytes / (peaks["hbm_gbs"] * 1e9) * 1e6}
         # per-kernel durations (eager, events per kernel), two steps
-        before = block.timing_table()
-        block.timing(True)
-        for _ in range(2):
-            step(B, lens[W])
-            block.timing_collect(stream)
-        block.timing(False)
-        table = {k: (t - before.get(k, (0.0, 0))[0], c - before.get(k, (0.0, 0))[1])
-                 for k, (t, c) in block.timing_table().items()}
-        table = {k: v for k, v in table.items() if v[1] > 0}
+        table = kernel_table(block, lambda: step(B, lens[W]), stream)
         tot = sum(v[0] for v in table.values())
-        row["kernels"] = {k: {"avg_us": 1e3 * t / c, "share": t / tot}
-                          for k, (t, c) in table.items()}
-        row["launches_per_step"] = sum(c for _, c in table.values()) // 2
+        row["kernel_share"] = {k: t / tot for k, (t, c) in table.items()}
+        row["launches_per_step"] = sum(c for _, c in table.values())
         out[str(B)] = row
         del graphs
     out["ctx"] = L0
     out["workload"] = (f"qwen2-1.5B-shaped 28-layer stack, B sequences x 1 new token, "
                        f"{L0} history slots each, one CUDA graph per step")
+    return out
+
+
+_STACK_W = {}
+
+
+def stack_weights(s, dev):
+    """Device copies of every layer's seeded weights of shape s (from synth,
+    the generator the tests use), made once and shared by the legs."""
+    import torch
+    import synth
+    if s not in _STACK_W:
+        _STACK_W[s] = [{k: torch.from_numpy(v).to(dev)
+                        for k, v in synth.block_weights(s, layer=l, seed=0).items()}
+                       for l in range(s.n_layers)]
+    return _STACK_W[s]
+
+
+def device_weights(s, layer: int, seed: int, dev):
+    """One layer's random-init weights drawn on the device by torch's seeded
+    generator: W ~ N(0, 0.02) rounded to fp16, gains 1, biases ~ N(0, 0.02).
+    The same distribution as synth.block_weights (not the same bits); used
+    where the host generator would take minutes (32 layers of hidden 4096)."""
+    import torch
+    import synth
+    g = torch.Generator(device=dev)
+    g.manual_seed(1000003 * seed + layer)
+    w = {}
+    for name, shp in synth.weight_shapes(s).items():
+        if name in ("ln1_g", "ln2_g"):
+            w[name] = torch.ones(shp, dtype=torch.float16, device=dev)
+        else:
+            w[name] = (torch.randn(shp, generator=g, device=dev) * 0.02).half()
+    return w
+
+
+def timed(fn, K, W, ws, stream):
+    """W untimed calls of fn(i), then K calls fn(W + i) each bracketed by CUDA
+    events on `stream`, with a barrier and a synchronize on both sides.
+    Returns (max over ranks of the summed ms, per-call ms on this rank)."""
+    import torch
+    for i in range(W):
+        fn(i)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    barrier(ws)
+    torch.cuda.synchronize()
+    for i in range(K):
+        evs[i][0].record(stream)
+        fn(W + i)
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    per = [a.elapsed_time(b) for a, b in evs]
+    return reduce_max(sum(per), ws), per
+
+
+def kernel_table(block, run, stream, reps=2):
+    """Per-kernel CUDA-event durations of `reps` eager calls of run(): {name:
+    (ms per call, launches per call)}, the handle's earlier totals removed."""
+    before = block.timing_table()
+    block.timing(True)
+    for _ in range(reps):
+        run()
+        block.timing_collect(stream)
+    block.timing(False)
+    out = {}
+    for k, (t, c) in block.timing_table().items():
+        t0, c0 = before.get(k, (0.0, 0))
+        if c > c0:
+            out[k] = ((t - t0) / reps, (c - c0) // reps)
     return out
 
 
@@ -615,37 +695,22 @@ def bench_decode(args, s, dev, stream, peaks, ws):
     n = s.n_layers
     C = max(ctxs) + W + K + 8
     Lmax = max(ctxs)
-    wl = []
-    for l in range(n):
-        wnp = synth.block_weights(s, layer=l, seed=0)
-        wl.append({k: torch.from_numpy(v).to(dev) for k, v in wnp.items()})
+    wl = stack_weights(s, dev)
     caches = []
     for l in range(n):
         k, v = synth.kv_history(s, C, Lmax, layer=l, seed=0)
         caches.append((torch.from_numpy(k).to(dev), torch.from_numpy(v).to(dev)))
     st = LayerStack(s, wl, C, 1, caches=caches, chain=True)
-    xs = [torch.from_numpy(synth.hidden_input(s, 1, seed=0, stream_offset=i + 1)).to(dev)
-          for i in range(W + K)]
+    xs_np = [synth.hidden_input(s, 1, seed=0, stream_offset=i + 1) for i in range(W + K)]
+    xs = [torch.from_numpy(a).to(dev) for a in xs_np]
     out = {}
     for L in ctxs:
         poss = [torch.tensor([L + i], dtype=torch.int64, device=dev) for i in range(W + K)]
         graphs = [st.capture("decode", xs[i], poss[i], L + i, key=("decode", L, i))[0]
                   for i in range(W + K)]
-        for i in range(W):
-            graphs[i].replay()
-        torch.cuda.synchronize()
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(K)]
-        barrier(ws)
-        torch.cuda.synchronize()
-        for i in range(K):
-            evs[i][0].record(stream)
-            graphs[W + i].replay()
-            evs[i][1].record(stream)
-        torch.cuda.synchronize()
-        barrier(ws)
+        total, _ = timed(lambda i: graphs[i].replay(), K, W, ws, stream)
         st.block.check()
-        ms = reduce_max(sum(a.elapsed_time(b) for a, b in evs), ws) / K
+        ms = total / K
         nbytes, wbytes = decode_bytes(s, L + W + K // 2, n)
         achieved = nbytes / (ms * 1e-3) / 1e9
         out[str(L)] = {"us_per_step": ms * 1e3, "tok_s": ws * 1e3 / ms,
@@ -655,65 +720,291 @@ def bench_decode(args, s, dev, stream, peaks, ws):
                        "traffic": NCU_TRAFFIC.get(("decode_persistent", L))}
         del graphs
         st.graphs.clear()
+    # end to end at the first context through the public API, eager: the
+    # step's hidden row and position go host (pinned) -> device, the 28-layer
+    # step runs (blk_decode_stack), the output row comes back to the host
+    L = ctxs[0]
+    x_h = [torch.from_numpy(a).pin_memory() for a in xs_np]
+    pos_h = [torch.tensor([L + i], dtype=torch.int64).pin_memory() for i in range(W + K)]
+    x_d = torch.empty((1, s.hidden), dtype=torch.float16, device=dev)
+    pos_d = torch.empty(1, dtype=torch.int64, device=dev)
+    out_d = torch.empty((1, s.hidden), dtype=torch.float16, device=dev)
+    out_h = torch.empty((1, s.hidden), dtype=torch.float16).pin_memory()
+
+    def e2e(i):
+        x_d.copy_(x_h[i], non_blocking=True)
+        pos_d.copy_(pos_h[i], non_blocking=True)
+        st.decode_step(x_d, pos_d, L + i, out=out_d, stream=stream)
+        out_h.copy_(out_d, non_blocking=True)
+
+    total, _ = timed(e2e, K, W, ws, stream)
+    st.block.check()
+    ms = total / K
+    out["e2e"] = {"ctx": L, "value": ws * 1e3 / ms, "unit": "tok/s", "us_per_step": ms * 1e3,
+                  "h2d_bytes_per_step": x_h[0].numel() * 2 + 8,
+                  "d2h_bytes_per_step": out_h.numel() * 2,
+                  "path": "blk_decode_stack through LayerStack.decode_step, eager (no graph)"}
     # the whole model per generated token at the first context: embedding +
     # the 28 blocks + final RMSNorm + LM head + greedy argmax, one graph per step
     out["model_per_token"] = bench_model_step(args, s, dev, stream, peaks, ws, st, ctxs[0])
     # per-kernel durations at the largest context (eager, events per kernel)
     L = ctxs[-1]
-    st.block.timing(True)
     pos = torch.tensor([L], dtype=torch.int64, device=dev)
-    for i in range(2):
-        st.run("decode", xs[0], pos, L)
-        st.block.timing_collect(stream)
-    st.block.timing(False)
-    table = st.block.timing_table()
+    table = kernel_table(st.block, lambda: st.run("decode", xs[0], pos, L), stream)
     tot = sum(v[0] for v in table.values())
     out["kernels_at_ctx"] = L
-    out["kernels"] = {k: {"avg_us": 1e3 * ms / cnt, "share": ms / tot} for k, (ms, cnt) in table.items()}
-    out["launches_per_step"] = sum(c for _, c in table.values()) // 2
+    out["kernels"] = {k: {"avg_us": 1e3 * ms / cnt, "share": ms / tot}
+                      for k, (ms, cnt) in table.items()}
+    out["launches_per_step"] = sum(c for _, c in table.values())
     out["workload"] = "qwen2-1.5B-shaped 28-layer stack, batch-1 decode, one CUDA graph per step"
     return out
 
 
+def bench_decode_layer(args, s, dev, stream, peaks, ws):
+    """One 1.5B-shaped layer of decode (blk_decode) at ctx --decode-ctx[0]:
+    a small case for ncu captures of the decode kernel (one launch = one
+    layer: 93.6 MB of weights + the K/V slots)."""
+    import torch
+    import synth
+    from decode_qwen2_block_gb300.stack import LayerStack
+    K, W = args.steps, args.warmup
+    L = int(args.decode_ctx.split(",")[0])
+    w = synth.block_weights(s, layer=0, seed=0)
+    wl = [{k: torch.from_numpy(v).to(dev) for k, v in w.items()}]
+    k, v = synth.kv_history(s, L + W + K + 8, L, layer=0, seed=0)
+    st = LayerStack(s, wl, L + W + K + 8, 1, caches=[(torch.from_numpy(k).to(dev),
+                                                      torch.from_numpy(v).to(dev))])
+    x = torch.from_numpy(synth.hidden_input(s, 1, seed=0, stream_offset=1)).to(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    poss = [torch.tensor([L + i], dtype=torch.int64, device=dev) for i in range(W + K)]
+
+    def step(i):
+        flush.zero_()
+        st.decode_step(x, poss[i], L + i, stream=stream)
+
+    total, per = timed(step, K, W, ws, stream)
+    st.block.check()
+    nbytes, _ = decode_bytes(s, L + W + K // 2, 1)
+    return {"ctx": L, "us_per_launch_incl_flush": total / K * 1e3, "bytes_per_launch": nbytes,
+            "workload": f"one 1.5B-shaped layer, decode at ctx {L}, L2 flushed before each call"}
+
+
+def bench_prefill_kv_stack(args, s, dev, stream, peaks, ws):
+    """prefill_kv through the 28-layer 1.5B stack: 512 new tokens at
+    positions 3584..4095 on 3584 seeded history slots per layer (the
+    TopOp paper's Listing 2 block with history K/V, per layer).  One call =
+    28 blk_prefill_kv launches chains.  GEMM flops are 1,341.6 GFLOP per
+    call and attention 338.3 GFLOP; their kernel times (events around each
+    kernel, separate pass) are reported apart."""
+    import torch
+    import synth
+    from decode_qwen2_block_gb300.stack import LayerStack
+    K, W = args.steps, args.warmup
+    n, L0, T = s.n_layers, PKV_HIST, PKV_T
+    C = L0 + T
+    wl = stack_weights(s, dev)
+    caches = []
+    for l in range(n):
+        k, v = synth.kv_history(s, C, L0, layer=l, seed=0)
+        caches.append((torch.from_numpy(k).to(dev), torch.from_numpy(v).to(dev)))
+    st = LayerStack(s, wl, C, T, caches=caches, chain=True)
+    x = torch.from_numpy(synth.hidden_input(s, T, seed=0, stream_offset=7)).to(dev)
+    pos = torch.from_numpy(synth.positions(L0, T)).to(dev)
+
+    def step(i=0):
+        st.run("prefill_kv", x, pos, L0, stream=stream)
+
+    total, _ = timed(step, K, W, ws, stream)
+    st.block.check()
+    ms = total / K
+    gemm, attn = prefill_flops(s, T, L0)
+    gemm_flops, attn_flops = n * sum(gemm.values()), n * attn
+    table = kernel_table(st.block, step, stream)
+    tot = sum(v[0] for v in table.values())
+    gemm_ms = sum(table[k][0] for k in list(gemm) + ["splitk_reduce"] if k in table)
+    attn_ms = sum(table[k][0] for k in ("attn_prefill", "attn_merge") if k in table)
+    peak = peaks["bf16_tflops"]
+    del st, caches
+    return {"workload": "qwen2-1.5B-shaped 28-layer stack, prefill_kv of 512 tokens at positions "
+                        "3584..4095 on 3584 history slots per layer",
+            "ms_per_call": ms, "tok_s": ws * T / (ms * 1e-3),
+            "gemm_gflop": gemm_flops / 1e9, "attn_gflop": attn_flops / 1e9,
+            "gemm_us": gemm_ms * 1e3, "gemm_tflops": gemm_flops / (gemm_ms * 1e-3) / 1e12,
+            "gemm_frac_of_tensor_peak": gemm_flops / (gemm_ms * 1e-3) / 1e12 / peak,
+            "gemm_target_us": gemm_flops / (0.6 * peak * 1e12) * 1e6,
+            "attn_us": attn_ms * 1e3, "attn_tflops": attn_flops / (attn_ms * 1e-3) / 1e12,
+            "attn_frac_of_tensor_peak": attn_flops / (attn_ms * 1e-3) / 1e12 / peak,
+            "attn_share_of_kernel_time": attn_ms / tot,
+            "whole_call_frac_of_tensor_peak": (gemm_flops + attn_flops) / (ms * 1e-3) / 1e12 / peak,
+            "kernels": {k: {"us_per_call": 1e3 * t, "launches": c, "share": t / tot}
+                        for k, (t, c) in table.items()}}
+
+
+def bench_gqa4096(args, s15, dev, stream, peaks, ws):
+    """The TopOp paper's Figure 2 example shape (32 layers, hidden 4096, 32 q
+    heads, 2 kv heads, head_dim 128, intermediate 11008, no bias): one
+    32-layer prefill of 100 tokens (positions 0..99), then 256 decode steps
+    at positions 100..355 appending to the same caches.  Both are bound by
+    the weight bytes (10.94 GB per pass).  Weights are drawn on the device
+    (device_weights); inputs from synth."""
+    import torch
+    import synth
+    from decode_qwen2_block_gb300.stack import LayerStack
+    s = synth.GQA_4096
+    K, W = args.steps, args.warmup
+    n, T, ND = s.n_layers, G4_PREFILL, G4_DECODES
+    C = T + ND + 8
+    wl = [device_weights(s, l, 0, dev) for l in range(n)]
+    st = LayerStack(s, wl, C, T, chain=True)
+    x = torch.from_numpy(synth.hidden_input(s, T, seed=0)).to(dev)
+    pos = torch.from_numpy(synth.positions(0, T)).to(dev)
+
+    def prefill(i=0):
+        st.run("prefill", x, pos, 0, stream=stream)
+
+    total, _ = timed(prefill, K, W, ws, stream)
+    st.block.check()
+    pre_ms = total / K
+    _, wbytes = decode_bytes(s, 0, n)
+    pre_bytes = wbytes + n * 2 * s.n_kv_heads * s.head_dim * 2 * T
+    pre_gbs = pre_bytes / (pre_ms * 1e-3) / 1e9
+    table = kernel_table(st.block, prefill, stream)
+    tot = sum(v[0] for v in table.values())
+    # the decode steps continue from the prefill's caches (slots 0..99)
+    xd = torch.from_numpy(synth.hidden_input(s, ND, seed=0, stream_offset=3)).to(dev)
+    poss = torch.arange(T, T + ND, dtype=torch.int64, device=dev)
+    outs = torch.empty((2, s.hidden), dtype=torch.float16, device=dev)
+
+    def dec(i):
+        st.decode_step(xd[i:i + 1], poss[i:i + 1], T + i, out=outs[i % 2:i % 2 + 1], stream=stream)
+
+    # warm-up: the first decode steps, then every one of the 256 steps timed
+    total, per = timed(lambda i: dec(i - W if i >= W else i), ND, W, ws, stream)
+    st.block.check()
+    dec_ms = total / ND
+    kv_avg = n * 2 * s.n_kv_heads * s.head_dim * 2 * (T + ND / 2 + 0.5)
+    dec_bytes = wbytes + kv_avg
+    dec_gbs = dec_bytes / (dec_ms * 1e-3) / 1e9
+    del st, wl
+    torch.cuda.empty_cache()
+    hbm = peaks["hbm_gbs"]
+    return {"workload": "hidden 4096, 32 q / 2 kv heads, head_dim 128, intermediate 11008, 32 "
+                        "layers: prefill of 100 tokens, then 256 decode steps (positions 100..355)",
+            "prefill_us": pre_ms * 1e3, "prefill_tok_s": ws * T / (pre_ms * 1e-3),
+            "prefill_bytes": pre_bytes, "prefill_gbs": pre_gbs,
+            "prefill_frac_of_hbm_peak": pre_gbs / hbm,
+            "prefill_roofline_us": pre_bytes / (hbm * 1e9) * 1e6,
+            "prefill_kernels": {k: {"us_per_call": 1e3 * t, "share": t / tot}
+                                for k, (t, c) in table.items()},
+            "decode_us_per_step": dec_ms * 1e3, "decode_tok_s": ws * 1e3 / dec_ms,
+            "decode_us_first_last": [per[0] * 1e3, per[-1] * 1e3],
+            "decode_bytes_per_step": dec_bytes, "decode_gbs": dec_gbs,
+            "decode_frac_of_hbm_peak": dec_gbs / hbm,
+            "decode_roofline_us": dec_bytes / (hbm * 1e9) * 1e6,
+            "weights": "drawn on the device by a seeded generator (same distribution as the "
+                       "host generator); inputs from the host generator"}
+
+
 # ------------------------------------------------------------------ main
+
+def compact(v, digits=4):
+    """Rounds every float to `digits` significant digits (keeps the line short)."""
+    if isinstance(v, float):
+        return float(f"{v:.{digits}g}")
+    if isinstance(v, dict):
+        return {k: compact(x, digits) for k, x in v.items()}
+    if isinstance(v, (list, tuple)):
+        return [compact(x, digits) for x in v]
+    return v
+
+
+def summary(r):
+    """The main figures in a few hundred bytes, placed last in the line."""
+    out = {"prefill_tok_s": r.get("value"), "prefill_ms": r.get("ms_per_step"),
+           "prefill_gemm_frac": r.get("prefill_gemm_frac_of_tensor_peak"),
+           "roofline_frac": (r.get("roofline") or {}).get("frac")}
+    dec = r.get("decode")
+    if dec:
+        out["decode_us_frac"] = {c: [dec[c]["us_per_step"], dec[c]["frac_of_hbm_peak"]]
+                                 for c in dec if c.isdigit()}
+        if "e2e" in dec:
+            out["decode_e2e_tok_s"] = dec["e2e"]["value"]
+        if "model_per_token" in dec:
+            out["model_us_per_token"] = dec["model_per_token"]["us_per_token"]
+    pkv = r.get("prefill_kv_28")
+    if pkv:
+        out["cfg4_prefill_kv"] = {"ms": pkv["ms_per_call"], "tok_s": pkv["tok_s"],
+                                  "gemm_us": pkv["gemm_us"],
+                                  "gemm_frac": pkv["gemm_frac_of_tensor_peak"],
+                                  "attn_us": pkv["attn_us"],
+                                  "attn_frac": pkv["attn_frac_of_tensor_peak"],
+                                  "attn_share": pkv["attn_share_of_kernel_time"]}
+    g4 = r.get("gqa4096")
+    if g4:
+        out["cfg5_gqa4096"] = {"prefill_us": g4["prefill_us"],
+                               "prefill_frac": g4["prefill_frac_of_hbm_peak"],
+                               "decode_us": g4["decode_us_per_step"],
+                               "decode_frac": g4["decode_frac_of_hbm_peak"]}
+    db = r.get("decode_batch")
+    if db:
+        out["decode_batch_us_frac"] = {b: [db[b]["us_per_step"], db[b]["frac_of_hbm_peak"]]
+                                       for b in db if b.isdigit()}
+    if "cpu_baseline" in r:
+        out["cpu_oracle_tok_s"] = r["cpu_baseline"]["value"]
+    return out
+
+
+def reference_arm(args, ws, rank):
+    """The oracle, as it stands, on the host cores: each step is the bounded
+    prefill sample that cpu_baseline also times; value is its tok/s
+    extrapolated to the whole [1,1024] layer, ms_per_step the sample's own
+    wall time."""
+    if rank != 0:
+        return
+    per_step, times = [], []
+    t_kv = None
+    for i in range(args.warmup + args.steps):
+        tok_s, secs, t_kv, desc = oracle_prefill_sample(ORACLE_SAMPLE_ROWS, rotate=i, t_kv=t_kv)
+        if i >= args.warmup:
+            per_step.append(tok_s)
+            times.append(secs)
+    v = statistics.mean(per_step)
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * statistics.mean(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded)",
+            "config": {"workload": "qwen2-1.5B-shaped decoder layer, prefill [1,1024], pos 0..1023",
+                       "sample": f"{ORACLE_SAMPLE_ROWS} of 1024 output rows per step, "
+                                 "value extrapolated to 1024 rows"},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": desc, "extrapolated": True,
+                             "host_cores": os.cpu_count()},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(compact(line)))
+
 
 def main():
     args = parse()
     ws, rank, local = dist_init(args)
     if args.impl == "reference":
-        if rank != 0:
-            return
-        per_step, times = [], []
-        sample_rows = 8
-        for i in range(args.warmup + args.steps):
-            tok_s, secs, desc = oracle_prefill_sample(sample_rows, rotate=i)
-            if i >= args.warmup:
-                per_step.append(tok_s)
-                times.append(secs)
-        v = statistics.mean(per_step)
-        line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": ws,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * PREFILL_T / v,
-                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-                "data": "synthetic (seeded)",
-                "config": {"workload": "qwen2-1.5B-shaped decoder layer, prefill [1,1024], pos 0..1023"},
-                "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
-                                 "sample": desc, "host_cores": os.cpu_count()},
-                "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-        print(json.dumps(line))
+        reference_arm(args, ws, rank)
         return
     result = bench_ours(args, ws, rank, local)
     if rank == 0 and not args.no_cpu and args.only is None:
-        tok_s, secs, desc = oracle_prefill_sample(128)
+        tok_s, secs, _, desc = oracle_prefill_sample(ORACLE_SAMPLE_ROWS)
         result["cpu_baseline"] = {"value": tok_s, "unit": UNIT, "cores": 1, "kind": "oracle",
-                                  "sample": desc, "host_cores": os.cpu_count(),
-                                  "seconds": secs}
+                                  "sample": desc, "extrapolated": True,
+                                  "host_cores": os.cpu_count(), "seconds": secs}
         if "decode" in result:
             us, secs_d, desc_d = oracle_decode_sample(1024, synth_layers())
             result["cpu_baseline_decode"] = {"value": us, "unit": "us/step", "cores": 1,
                                              "kind": "oracle", "sample": desc_d,
-                                             "seconds": secs_d}
+                                             "extrapolated": True, "seconds": secs_d}
     if rank == 0:
-        print(json.dumps(result))
+        if args.only is None:
+            result["summary"] = summary(result)
+        print(json.dumps(compact(result), separators=(",", ":")))
     if ws > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

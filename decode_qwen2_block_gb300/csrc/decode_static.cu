@@ -49,15 +49,18 @@ extern "C" int blk_decode_static(blk_handle h, const blk_weights* w, const void*
                                  const int64_t* pos, int64_t cache_len, void* k_cache,
                                  void* v_cache, void* out, void* k_new, void* v_new,
                                  void* stream) {
-  if (!h) return BLK_ERR_NULL;
+  // A missing pointer is reported before the size limit, the size limit
+  // before blk_decode's own checks (shape, alignment, cache bounds).
+  if (!h || !w || !x || !pos || !k_cache || !v_cache || !out) return BLK_ERR_NULL;
   if (blk_internal_decode_ws_bytes(h) > BLK_STATIC_SCRATCH_BYTES)
     return BLK_ERR_SCRATCH_LIMIT;
   void* scratch = nullptr;
   const int rc = scratch_address(blk_internal_device(h), &scratch);
   if (rc != BLK_OK) return rc;
-  // The decode kernels zero what must start at zero (the split-K counters are
-  // cleared by the first kernel of every call), so the array's leftover
-  // contents from an earlier call do not matter.
+  // Leftovers of an earlier call in the array do not matter: the only words
+  // that must start at zero (the decode kernel's synchronisation counters)
+  // are zeroed by a cudaMemsetAsync on the call's stream before each launch,
+  // and every other region is written in full before it is read.
   return blk_decode(h, w, x, pos, cache_len, k_cache, v_cache, out, k_new, v_new, scratch,
                     BLK_STATIC_SCRATCH_BYTES, stream);
 }

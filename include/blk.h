@@ -198,7 +198,9 @@ int blk_decode_stack(blk_handle h, const blk_weights* w, int n_layers,
  * call's contents (the kernels clear what must start at zero).  Calls whose
  * work overlaps on the GPU — on different streams, or from different
  * handles — race on the array; serialize them (one stream, or events).
- * Return codes are those of blk_decode plus BLK_ERR_SCRATCH_LIMIT. */
+ * Return codes are those of blk_decode plus BLK_ERR_SCRATCH_LIMIT.  When
+ * several apply, BLK_ERR_NULL (a NULL handle, w, x, pos, cache or out) comes
+ * first, then BLK_ERR_SCRATCH_LIMIT, then blk_decode's other checks. */
 #define BLK_STATIC_SCRATCH_BYTES ((size_t)1 << 20)
 int blk_decode_static(blk_handle h, const blk_weights* w, const void* x,
                       const int64_t* pos, int64_t cache_len, void* k_cache,

@@ -84,3 +84,33 @@ def test_oracle_decode_sample_extrapolates_over_layers():
     us, secs, desc = bench.oracle_decode_sample(L=16, n_layers=3)
     assert secs > 0 and abs(us - 3 * secs * 1e6) < 1e-6 * us
     assert "extrapolated x3 layers" in desc
+
+
+def test_prefill_kv_and_gqa4096_work_follow_the_shapes():
+    """prefill_kv of 512 tokens on 3584 history slots through 28 1.5B layers:
+    1,341.6 GFLOP of projections and 338.3 GFLOP of attention (1,966,336
+    query-key pairs per head per layer); hidden-4096 32-layer weights:
+    10,939 MB."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import synth
+    gemm, attn = bench.prefill_flops(synth.QWEN2_1P5B, 512, 3584)
+    assert abs(28 * sum(gemm.values()) - 1341.6e9) < 0.1e9
+    assert sum(3584 + t + 1 for t in range(512)) == 1_966_336
+    assert abs(28 * attn - 338.3e9) < 0.1e9
+    _, wbytes = bench.decode_bytes(synth.GQA_4096, 0, 32)
+    assert abs(wbytes - 10_939e6) < 1e6
+
+
+def test_summary_is_last_and_compact():
+    """The summary repeats the main figures and compact() keeps 4 digits."""
+    sys.path.insert(0, ROOT)
+    import bench
+    r = {"value": 1234567.891, "ms_per_step": 0.1234567, "roofline": {"frac": 0.6791457},
+         "prefill_gemm_frac_of_tensor_peak": 0.4412,
+         "decode": {"1024": {"us_per_step": 1129.123, "frac_of_hbm_peak": 0.3461},
+                    "e2e": {"value": 800.5}, "workload": "x"}}
+    s = bench.summary(r)
+    assert s["decode_us_frac"] == {"1024": [1129.123, 0.3461]}
+    assert s["decode_e2e_tok_s"] == 800.5
+    assert bench.compact(s)["prefill_tok_s"] == 1235000.0

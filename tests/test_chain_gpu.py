@@ -124,12 +124,14 @@ def _layer_local(s, wl_np_fn, caches_before, layer_inputs, pos, L, rows, outs_ne
         assert_close(got, o_ref, f"layer {l}")
 
 
-def test_decode_28_layer_stack_graph_layer_local():
-    """28 layers of the 1.5B shape, decode at cache length 4096, captured in a
-    CUDA graph with the overlapped launch (the benchmark's configuration).
-    Each checked layer is compared with the oracle run on the GPU's own input
-    to that layer."""
-    s, L = synth.QWEN2_1P5B, 4096
+@pytest.mark.parametrize("L", [4096, 32768])
+def test_decode_28_layer_stack_graph_layer_local(L):
+    """28 layers of the 1.5B shape, decode at cache length 4096 and at the
+    longest context the benchmark times (32768), captured in a CUDA graph
+    with the overlapped launch (the benchmark's configuration).  Each checked
+    layer is compared with the oracle run on the GPU's own input to that
+    layer."""
+    s = synth.QWEN2_1P5B
     C = L + 128
     n = s.n_layers
     wl, hc = _stack(s, n, C, L)
@@ -169,3 +171,63 @@ def test_prefill_kv_28_layer_stack_layer_local():
     outs_next = ins[1:] + [final]
     _layer_local(s, lambda l: synth.block_weights(s, layer=l, seed=0), hc, ins,
                  synth.positions(L, T), L, [0, 255, 511], outs_next, layers=[0, 27])
+
+
+def test_gqa4096_prefill_then_64_decodes_layer_local():
+    """The hidden-4096 shape (32 q / 2 kv heads, head_dim 128, intermediate
+    11008, the TopOp paper's Figure 2 example) through a 4-layer stack: a
+    prefill of 100 tokens, then 64 decode steps at positions 100..163, each
+    step appending to the caches the earlier steps wrote.  Layer- and
+    step-local against the oracle: every step's K/V slot of every layer
+    (the oracle given that layer's input and the GPU's cache before the
+    step), and the full output of every layer at the prefill (sampled rows)
+    and at four of the decode steps, within the benchmark spec tolerance."""
+    s, n, T, ND = synth.GQA_4096, 4, 100, 64
+    C = T + ND + 8
+    w_np = [synth.block_weights(s, layer=l, seed=2) for l in range(n)]
+    wl = [weights_to_dev(w) for w in w_np]
+    st = LayerStack(s, wl, C, T, chain=True)
+    x = synth.hidden_input(s, T, seed=2)
+    ins_p = []
+    final_p = st.run("prefill", to_dev(x), to_dev(synth.positions(0, T)), 0,
+                     layer_outputs=ins_p).clone()
+    torch.cuda.synchronize()
+    st.block.check()
+    after_prefill = [(k.cpu().numpy().copy(), v.cpu().numpy().copy()) for k, v in st.caches]
+    rows = [0, 57, 99]
+    for l in range(n):
+        k0 = np.zeros_like(after_prefill[l][0])
+        v0 = np.zeros_like(after_prefill[l][1])
+        o_ref, k_ref, v_ref = oracle.block_forward(s, w_np[l], ins_p[l].cpu().numpy(),
+                                                   synth.positions(0, T), 0, k0, v0, rows=rows)
+        got = (ins_p[l + 1] if l + 1 < n else final_p).cpu().numpy()[rows]
+        assert_close(got, o_ref, f"prefill layer {l}")
+        assert_close(after_prefill[l][0][:, :T].transpose(1, 0, 2), k_ref, f"prefill K layer {l}")
+        assert_close(after_prefill[l][1][:, :T].transpose(1, 0, 2), v_ref, f"prefill V layer {l}")
+    xd = synth.hidden_input(s, ND, seed=2, stream_offset=1)
+    step_ins, step_outs = [], []
+    for i in range(ND):
+        ins = []
+        o = st.run("decode", to_dev(xd[i:i + 1]), to_dev(synth.positions(T + i, 1)), T + i,
+                   layer_outputs=ins).clone()
+        step_ins.append([a.cpu().numpy() for a in ins])
+        step_outs.append(o.cpu().numpy())
+    torch.cuda.synchronize()
+    st.block.check()
+    final = [(k.cpu().numpy(), v.cpu().numpy()) for k, v in st.caches]
+    full_steps = (0, 21, 42, 63)
+    for i in range(ND):
+        L = T + i
+        for l in range(n):
+            kc_o = final[l][0].copy()
+            vc_o = final[l][1].copy()
+            kc_o[:, L:] = 0
+            vc_o[:, L:] = 0
+            o_ref, k_ref, v_ref = oracle.block_forward(
+                s, w_np[l], step_ins[i][l], synth.positions(L, 1), L, kc_o, vc_o,
+                rows=None if i in full_steps else [])
+            assert_close(final[l][0][:, L], k_ref[0], f"step {i} K layer {l}")
+            assert_close(final[l][1][:, L], v_ref[0], f"step {i} V layer {l}")
+            if i in full_steps:
+                got = step_ins[i][l + 1] if l + 1 < n else step_outs[i]
+                assert_close(got, o_ref, f"step {i} out layer {l}")
