@@ -10,8 +10,10 @@
 // Every copy is a TMA tensor copy with 128-byte swizzle: a weight box is 8
 // rows x 1536 columns (one 3-D copy of 24 column blocks of 64), a KV tile
 // 64 slots x D.  Twelve consumer warps run the phases of each layer and meet
-// at a grid-wide barrier between phases; while they wait, the producer keeps
-// filling the ring, so HBM stays busy through the barriers.
+// at a grid-wide barrier between phases.  The producer fills the ring ahead
+// across phases, but issues nothing from a phase's last chunk until the next
+// phase's inputs are staged: the barrier's polls and the staging loads of an
+// SM wait behind every byte that SM has in flight.
 //
 // Phases of one layer (the block of the TopOp paper, Listing 2, at T = 1):
 //   QKV   x = previous layer's output (or the input), RMSNorm(x) staged in
@@ -574,6 +576,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* empty = full + kStages;
   float* red = reinterpret_cast<float*>(empty + kStages);        // [16]
   volatile int* abort_flag = reinterpret_cast<volatile int*>(red + 16);
+  // quiet: set from the moment the consumers take the last ring chunk of a
+  // phase until they have staged the next phase's inputs.  The producer
+  // issues no new copy meanwhile: the grid barrier's polls and the staging
+  // loads of an SM queue behind the bytes that SM has requested, so copies
+  // issued then would delay them (measured: a grid barrier took ~2.5 us with
+  // copies in flight, ~1.4 us without).
+  volatile int* quiet = abort_flag + 1;
   float* xres = reinterpret_cast<float*>(smem + kResOff);       // x of the o_proj rows
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -583,6 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&empty[s], kCW);
     }
     *abort_flag = 0;
+    *quiet = 0;
     fence_mbar_init();
   }
   __syncthreads();
@@ -691,6 +701,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
       }
+      if (*quiet) {
+        const uint64_t t0 = global_ns();
+        while (*quiet && !*abort_flag) {
+          if (global_ns() - t0 > kWaitLimitNs) {
+            set_error(p.err, kDevTimeout);
+            *abort_flag = 1;
+            break;
+          }
+        }
+        if (*abort_flag) break;
+      }
       mbar_arrive_expect_tx(&full[s], chunk_bytes(rc));
       load(rc, ring + (size_t)s * kStageBytes, &full[s]);
       ++it;
@@ -760,6 +781,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           named_sync(2, kAttnWarps * 32);
+          if (tid == 0) *quiet = 0;
         }
         const int grp = lane >> 2, tig = lane & 3;
         float m_r[2] = {-INFINITY, -INFINITY}, l_r[2] = {0.f, 0.f};
@@ -772,6 +794,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < ar.chunks; ++c) {
           int s;
           if (!take(s)) break;
+          if (c == ar.chunks - 1 && tid == 0) *quiet = 1;
           if (warp < kAttnWarps) {
             uint8_t* st = ring + (size_t)s * kStageBytes;
             const uint32_t kb = smem_u32(st), vb = kb + kv_tile_bytes;
@@ -944,6 +967,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else if (ph == kPhComb) {
         // ---------------------------------------------------- combine splits
+        if (tid == 0) *quiet = 0;
         const int P = p.Hq * D;
         const int p0 = (int)((int64_t)blockIdx.x * P / gridDim.x);
         const int p1 = (int)((int64_t)(blockIdx.x + 1) * P / gridDim.x);
@@ -1016,6 +1040,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           stage_copy(ph == kPhO ? p.attn16 : p.act16, W.K, xs);
         }
+        if (tid == 0) *quiet = 0;
         // y = W x on the tensor cores: A = a chunk's 16 rows x 16 columns
         // (ldmatrix from the two swizzled boxes), B = x as the only non-zero
         // column, fp32 accumulators; the warps split each chunk's 16-column
@@ -1032,6 +1057,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kc = g.ka; kc < g.kb; ++kc) {
               int s;
               if (!take(s)) break;
+              if (gi == W.ngroups - 1 && kc == g.kb - 1 && tid == 0) *quiet = 1;
               const int nks = min(kKc, W.K - kc * kKc) / 16;
               const int ks0 = warp * nks / kCW, ks1 = (warp + 1) * nks / kCW;
               const uint32_t st = smem_u32(ring + (size_t)s * kStageBytes) + abox;
@@ -1114,6 +1140,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       trace_point(p, l, ph, 1);
+      if (tid == 0) *quiet = 1;
       grid_arrive(sync);
     }
   }
