@@ -84,7 +84,7 @@ def parse():
                     help="batch sizes of the batched decode table (ctx --decode-batch-ctx)")
     ap.add_argument("--decode-batch-ctx", type=int, default=1024)
     ap.add_argument("--only", choices=("prefill", "decode", "decode_batch", "prefill_kv",
-                                       "gqa4096", "decode_layer"), default=None,
+                                       "gqa4096", "decode_layer", "decode_quant"), default=None,
                     help="run one part (for profiling); the headline needs the prefill.  "
                          "decode_layer runs one 1.5B-shaped layer of decode at ctx "
                          "--decode-ctx[0] (small enough for an ncu capture)")
@@ -292,7 +292,8 @@ def bench_ours(args, ws, rank, local):
              "decode_batch": ("batched decode tok/s (28 layers)", bench_decode_batch),
              "prefill_kv": ("prefill_kv tok/s (28 layers, 512 on 3584)", bench_prefill_kv_stack),
              "gqa4096": ("hidden-4096 32-layer prefill + decode", bench_gqa4096),
-             "decode_layer": ("decode us/launch (1 layer)", bench_decode_layer)}
+             "decode_layer": ("decode us/launch (1 layer)", bench_decode_layer),
+             "decode_quant": ("quantized decode us/step (28 layers)", bench_decode_quant)}
     if args.only in parts:
         clocks = ClockSampler(local)
         clocks.start()
@@ -433,6 +434,7 @@ def bench_ours(args, ws, rank, local):
         result["decode"] = bench_decode(args, s, dev, stream, peaks, ws)
         result["lm_head"] = bench_lm_head(args, s, dev, stream, peaks, ws)
         result["decode_batch"] = bench_decode_batch(args, s, dev, stream, peaks, ws)
+        result["decode_quant"] = bench_decode_quant(args, s, dev, stream, peaks, ws)
         result["prefill_kv_28"] = bench_prefill_kv_stack(args, s, dev, stream, peaks, ws)
         _STACK_W.clear()
         torch.cuda.empty_cache()
@@ -760,6 +762,96 @@ def bench_decode(args, s, dev, stream, peaks, ws):
     return out
 
 
+def quant_bytes(s, fmt: str, group: int, L: int, n_layers: int):
+    """HBM bytes of one decode step with quantized projections: codes (1
+    byte per weight for INT8, half a byte for int4), fp16 scales (one per
+    row, or per row and group), int4 zero points (one byte per row and
+    group), the fp16 gains and biases, and the K/V slots read."""
+    H, Hq, Hkv, D, I = s.hidden, s.n_heads, s.n_kv_heads, s.head_dim, s.intermediate
+    mats = [((Hq + 2 * Hkv) * D, H), (H, Hq * D), (2 * I, H), (H, I)]   # (rows, K)
+    w = 0
+    for rows, K in mats:
+        if fmt == "i8":
+            w += rows * K + 2 * rows
+        else:
+            w += rows * K // 2 + 3 * rows * (K // group)
+    w += 2 * 2 * H + (2 * (Hq + 2 * Hkv) * D if s.has_qkv_bias else 0)
+    kv = 2 * Hkv * D * 2 * (L + 1)
+    return n_layers * (w + kv)
+
+
+def device_qweights(s, fmt: str, group: int, layer: int, seed: int, dev):
+    """One layer's quantized matrices drawn on the device by torch's seeded
+    generator, in the layouts of include/blk.h (codes, scales near
+    0.02 / spread of the codes, int4 zero points near 7.5): the same recipe
+    as synth.quant_weights, not the same bits."""
+    import torch
+    import synth
+    g = torch.Generator(device=dev)
+    g.manual_seed(7919 * seed + layer)
+    out = {}
+    for name, (N, K) in synth.weight_shapes(s).items():
+        if name not in synth.QUANT_MATRICES:
+            continue
+        if fmt == "i8":
+            q = torch.randint(-127, 128, (N, K), generator=g, device=dev, dtype=torch.int8)
+            sc = (0.02 / 42 * (1 + 0.1 * torch.randn(N, generator=g, device=dev))).half()
+            out[name] = {"q": q, "scale": sc}
+        else:
+            q = torch.randint(0, 256, (N, K // 2), generator=g, device=dev, dtype=torch.uint8)
+            sc = (0.02 / 3.5 * (1 + 0.1 * torch.randn(N, K // group, generator=g,
+                                                      device=dev))).half()
+            z = torch.randint(6, 10, (N, K // group), generator=g, device=dev, dtype=torch.uint8)
+            out[name] = {"q": q, "scale": sc, "zero": z}
+    return out
+
+
+def bench_decode_quant(args, s, dev, stream, peaks, ws):
+    """Batch-1 decode through the 28-layer 1.5B stack with weight-only
+    quantized projections (INT8 per row; int4 in groups of 128), one CUDA
+    graph per step, at the first decode context; bytes per step are the
+    codes, scales, zero points, gains, biases and K/V read."""
+    import torch
+    import synth
+    import decode_qwen2_block_gb300 as blk
+    from decode_qwen2_block_gb300.stack import QuantDecodeStack
+    K, W = args.steps, args.warmup
+    L = int(args.decode_ctx.split(",")[0])
+    n = s.n_layers
+    C = L + W + K + 8
+    caches = []
+    for l in range(n):
+        k, v = synth.kv_history(s, C, L, layer=l, seed=0)
+        caches.append((torch.from_numpy(k).to(dev), torch.from_numpy(v).to(dev)))
+    wl = stack_weights(s, dev)
+    xs = [torch.from_numpy(synth.hidden_input(s, 1, seed=0, stream_offset=i + 1)).to(dev)
+          for i in range(W + K)]
+    out = {}
+    for fmt, group in (("i8", 0), ("u4", 128)):
+        qd = [device_qweights(s, fmt, group, l, 0, dev) for l in range(n)]
+        code = blk.BLK_WFMT_I8 if fmt == "i8" else blk.BLK_WFMT_U4
+        qws = [blk.Block.qweights(code, group, wl[l], qd[l]) for l in range(n)]
+        st = QuantDecodeStack(s, qws, C, caches=caches)
+        poss = [torch.tensor([L + i], dtype=torch.int64, device=dev) for i in range(W + K)]
+        graphs = [st.capture(xs[i], poss[i], L + i)[0] for i in range(W + K)]
+        total, _ = timed(lambda i: graphs[i].replay(), K, W, ws, stream)
+        st.block.check()
+        ms = total / K
+        nbytes = quant_bytes(s, fmt, group, L + W + K // 2, n)
+        achieved = nbytes / (ms * 1e-3) / 1e9
+        out[fmt] = {"us_per_step": ms * 1e3, "tok_s": ws * 1e3 / ms, "bytes_per_step": nbytes,
+                    "achieved_gbs": achieved, "frac_of_hbm_peak": achieved / peaks["hbm_gbs"],
+                    "roofline_us": nbytes / (peaks["hbm_gbs"] * 1e9) * 1e6,
+                    "group": group if fmt == "u4" else None}
+        del graphs, st, qd, qws
+        torch.cuda.empty_cache()
+    out["ctx"] = L
+    out["workload"] = ("qwen2-1.5B-shaped 28-layer stack, batch-1 decode, weight-only INT8 "
+                       "(per-row scale) and int4 (groups of 128, scale + zero point), "
+                       "weights drawn on the device")
+    return out
+
+
 def bench_decode_layer(args, s, dev, stream, peaks, ws):
     """One 1.5B-shaped layer of decode (blk_decode) at ctx --decode-ctx[0]:
     a small case for ncu captures of the decode kernel (one launch = one
@@ -945,6 +1037,10 @@ def summary(r):
                                "prefill_frac": g4["prefill_frac_of_hbm_peak"],
                                "decode_us": g4["decode_us_per_step"],
                                "decode_frac": g4["decode_frac_of_hbm_peak"]}
+    dq = r.get("decode_quant")
+    if dq:
+        out["decode_quant_us_frac"] = {f: [dq[f]["us_per_step"], dq[f]["frac_of_hbm_peak"]]
+                                       for f in ("i8", "u4") if f in dq}
     db = r.get("decode_batch")
     if db:
         out["decode_batch_us_frac"] = {b: [db[b]["us_per_step"], db[b]["frac_of_hbm_peak"]]

@@ -31,6 +31,7 @@ BLK_ERR_SCRATCH_LIMIT = -10
 BLK_ERR_TOKEN = -11
 BLK_STATIC_SCRATCH_BYTES = 1 << 20
 BLK_FLAG_CHAIN = 1
+BLK_WFMT_F16, BLK_WFMT_I8, BLK_WFMT_U4 = 0, 1, 2
 
 EXPORTED = ("blk_create", "blk_destroy", "blk_set_flags", "blk_workspace_bytes", "blk_prefill",
             "blk_prefill_kv", "blk_decode", "blk_check", "blk_status_str", "blk_timing",
@@ -38,7 +39,8 @@ EXPORTED = ("blk_create", "blk_destroy", "blk_set_flags", "blk_workspace_bytes",
             "blk_set_trace", "blk_embed", "blk_lm_head_workspace_bytes", "blk_lm_head",
             "blk_decode_batch_workspace_bytes", "blk_decode_batch",
             "blk_decode_batch_stack_workspace_bytes", "blk_decode_batch_stack",
-            "blk_wait_probe")
+            "blk_wait_probe", "blk_qworkspace_bytes", "blk_prefill_q", "blk_prefill_kv_q",
+            "blk_decode_q", "blk_decode_stack_q")
 BLK_N_KERNELS = 16
 
 WEIGHT_FIELDS = ("ln1_g", "wq", "wk", "wv", "bq", "bk", "bv", "wo", "ln2_g", "w_gate", "w_up",
@@ -55,6 +57,19 @@ class BlkConfig(ctypes.Structure):
 
 class BlkWeights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in WEIGHT_FIELDS]
+
+
+class BlkQMatrix(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("scale", ctypes.c_void_p), ("zero", ctypes.c_void_p)]
+
+
+QMATRIX_FIELDS = ("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down")
+
+
+class BlkQWeights(ctypes.Structure):
+    _fields_ = ([("format", ctypes.c_int32), ("group", ctypes.c_int32)] +
+                [(n, ctypes.c_void_p) for n in ("ln1_g", "bq", "bk", "bv", "ln2_g")] +
+                [(n, BlkQMatrix) for n in QMATRIX_FIELDS])
 
 
 class BlkError(RuntimeError):
@@ -134,6 +149,20 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.blk_lm_head_workspace_bytes.restype = ctypes.c_size_t
     lib.blk_lm_head.argtypes = [vp, vp, i64, vp, vp, i64, vp, vp, vp, ctypes.c_size_t, vp]
     lib.blk_lm_head.restype = i32
+    qw = ctypes.POINTER(BlkQWeights)
+    lib.blk_qworkspace_bytes.argtypes = [vp, i64]
+    lib.blk_qworkspace_bytes.restype = ctypes.c_size_t
+    lib.blk_prefill_q.argtypes = [vp, qw, vp, vp, i64, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+    lib.blk_prefill_q.restype = i32
+    lib.blk_prefill_kv_q.argtypes = [vp, qw, vp, vp, i64, i64, vp, vp, vp, vp, vp, vp,
+                                     ctypes.c_size_t, vp]
+    lib.blk_prefill_kv_q.restype = i32
+    lib.blk_decode_q.argtypes = [vp, qw, vp, vp, i64, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+    lib.blk_decode_q.restype = i32
+    lib.blk_decode_stack_q.argtypes = [vp, qw, i32, ctypes.POINTER(vp), ctypes.POINTER(vp), vp, vp,
+                                       i64, vp, ctypes.POINTER(vp), ctypes.POINTER(vp), vp,
+                                       ctypes.c_size_t, vp]
+    lib.blk_decode_stack_q.restype = i32
     _lib = lib
     return lib
 
@@ -199,6 +228,34 @@ def blk_decode_static(handle, w: BlkWeights, x, pos, cache_len, k_cache, v_cache
     (for callers that cannot allocate device memory; see include/blk.h)."""
     return load().blk_decode_static(handle, ctypes.byref(w), x, pos, cache_len, k_cache, v_cache,
                                     out, k_new, v_new, stream)
+
+
+def blk_qworkspace_bytes(handle, max_T: int) -> int:
+    return load().blk_qworkspace_bytes(handle, max_T)
+
+
+def blk_prefill_q(handle, w: BlkQWeights, x, pos, T, k_cache, v_cache, out, k_new, v_new, ws,
+                  ws_bytes, stream) -> int:
+    return load().blk_prefill_q(handle, ctypes.byref(w), x, pos, T, k_cache, v_cache, out, k_new,
+                                v_new, ws, ws_bytes, stream)
+
+
+def blk_prefill_kv_q(handle, w: BlkQWeights, x, pos, T, cache_len, k_cache, v_cache, out, k_new,
+                     v_new, ws, ws_bytes, stream) -> int:
+    return load().blk_prefill_kv_q(handle, ctypes.byref(w), x, pos, T, cache_len, k_cache, v_cache,
+                                   out, k_new, v_new, ws, ws_bytes, stream)
+
+
+def blk_decode_q(handle, w: BlkQWeights, x, pos, cache_len, k_cache, v_cache, out, k_new, v_new,
+                 ws, ws_bytes, stream) -> int:
+    return load().blk_decode_q(handle, ctypes.byref(w), x, pos, cache_len, k_cache, v_cache, out,
+                               k_new, v_new, ws, ws_bytes, stream)
+
+
+def blk_decode_stack_q(handle, w_array, n_layers, k_caches, v_caches, x, pos, cache_len, out,
+                       k_new, v_new, ws, ws_bytes, stream) -> int:
+    return load().blk_decode_stack_q(handle, w_array, n_layers, k_caches, v_caches, x, pos,
+                                     cache_len, out, k_new, v_new, ws, ws_bytes, stream)
 
 
 def blk_decode_batch_workspace_bytes(handle, max_B: int) -> int:
@@ -306,6 +363,44 @@ class Block:
         for n in WEIGHT_FIELDS:
             setattr(w, n, _ptr(wdict.get(n)))
         return w
+
+    @staticmethod
+    def qweights(fmt: int, group: int, wdict, qdict) -> BlkQWeights:
+        """Quantized weights: gains and biases from ``wdict`` (fp16 tensors),
+        the seven matrices from ``qdict[name] = {"q", "scale"[, "zero"]}``
+        (device tensors in the layouts of include/blk.h)."""
+        w = BlkQWeights()
+        w.format, w.group = fmt, group
+        for n in ("ln1_g", "bq", "bk", "bv", "ln2_g"):
+            setattr(w, n, _ptr(wdict.get(n)))
+        for n in QMATRIX_FIELDS:
+            m = getattr(w, n)
+            m.q, m.scale, m.zero = (_ptr(qdict[n]["q"]), _ptr(qdict[n]["scale"]),
+                                    _ptr(qdict[n].get("zero")))
+        return w
+
+    def qworkspace_bytes(self, max_T: int) -> int:
+        return blk_qworkspace_bytes(self.handle, max_T)
+
+    def run_q(self, phase: str, w: BlkQWeights, x, pos, cache_len: int, k_cache, v_cache, out,
+              ws, k_new=None, v_new=None, stream=None):
+        """One call of the quantized prefill / prefill_kv / decode."""
+        nb = ws.numel() * ws.element_size()
+        st = self._stream(stream)
+        if phase == "prefill":
+            rc = blk_prefill_q(self.handle, w, _ptr(x), _ptr(pos), x.shape[0], _ptr(k_cache),
+                               _ptr(v_cache), _ptr(out), _ptr(k_new), _ptr(v_new), _ptr(ws), nb, st)
+        elif phase == "prefill_kv":
+            rc = blk_prefill_kv_q(self.handle, w, _ptr(x), _ptr(pos), x.shape[0], cache_len,
+                                  _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(k_new),
+                                  _ptr(v_new), _ptr(ws), nb, st)
+        elif phase == "decode":
+            rc = blk_decode_q(self.handle, w, _ptr(x), _ptr(pos), cache_len, _ptr(k_cache),
+                              _ptr(v_cache), _ptr(out), _ptr(k_new), _ptr(v_new), _ptr(ws), nb, st)
+        else:
+            raise ValueError(phase)
+        if rc != BLK_OK:
+            raise BlkError(rc, f"blk_{phase}_q")
 
     @staticmethod
     def _stream(stream):

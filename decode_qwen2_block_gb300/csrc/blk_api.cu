@@ -22,13 +22,13 @@ constexpr int kMaxPending = 1024;
 enum KernelId {
   kKRmsNorm = 0, kKGemmQKV, kKSplitReduce, kKAttnPrefill, kKGemmO, kKGemmGateUp,
   kKGemmDown, kKDecodeStep, kKAttnMerge, kKLmHead, kKArgmax, kKEmbed, kKDecodeAttnBatch,
-  kKQkvFinish, kKCount
+  kKQkvFinish, kKDequant, kKCount
 };
 static_assert(kKCount <= BLK_N_KERNELS, "kernel id table");
 const char* const kKernelNames[BLK_N_KERNELS] = {
     "rmsnorm_rows", "gemm_qkv", "splitk_reduce", "attn_prefill", "gemm_o",
     "gemm_gateup", "gemm_down", "decode_persistent", "attn_merge", "lm_head", "argmax_reduce",
-    "embed", "decode_attn_batch", "qkv_finish", "", ""};
+    "embed", "decode_attn_batch", "qkv_finish", "dequant_weights", ""};
 }  // namespace
 
 struct blk_handle_s {
@@ -134,13 +134,36 @@ int check_weights(const blk_config& c, const blk_weights* w) {
   return BLK_OK;
 }
 
-int check_call(blk_handle h, const blk_weights* w, const void* x,
-               const int64_t* pos, int64_t T, int64_t L, const void* kc,
-               const void* vc, const void* out, const void* kn, const void* vn,
-               const void* ws) {
+// Quantized weights: pointers, alignment and the shape rules of blk.h.
+int check_qweights(const blk_config& c, const blk_qweights* w) {
+  if (!w) return BLK_ERR_NULL;
+  if (w->format != BLK_WFMT_I8 && w->format != BLK_WFMT_U4) return BLK_ERR_SHAPE;
+  const int64_t Ks[3] = {c.hidden, (int64_t)c.n_heads * c.head_dim, c.intermediate};
+  for (int64_t K : Ks) {
+    if (K % (w->format == BLK_WFMT_I8 ? 16 : 32)) return BLK_ERR_SHAPE;
+    if (w->format == BLK_WFMT_U4 && (w->group < 16 || w->group % 16 || K % w->group))
+      return BLK_ERR_SHAPE;
+  }
+  const blk_qmatrix* m[] = {&w->wq, &w->wk, &w->wv, &w->wo, &w->w_gate, &w->w_up, &w->w_down};
+  for (const blk_qmatrix* q : m) {
+    if (!q->q || !q->scale || (w->format == BLK_WFMT_U4 && !q->zero)) return BLK_ERR_NULL;
+    if (!aligned(q->q, 16) || !aligned(q->scale, 2)) return BLK_ERR_ALIGN;
+  }
+  if (!w->ln1_g || !w->ln2_g) return BLK_ERR_NULL;
+  if (!aligned(w->ln1_g, 16) || !aligned(w->ln2_g, 16)) return BLK_ERR_ALIGN;
+  if (c.has_qkv_bias) {
+    if (!w->bq || !w->bk || !w->bv) return BLK_ERR_NULL;
+    if (!aligned(w->bq, 16) || !aligned(w->bk, 16) || !aligned(w->bv, 16))
+      return BLK_ERR_ALIGN;
+  }
+  return BLK_OK;
+}
+
+// The arguments of a call other than its weights.
+int check_args(blk_handle h, const void* x, const int64_t* pos, int64_t T, int64_t L,
+               const void* kc, const void* vc, const void* out, const void* kn,
+               const void* vn, const void* ws) {
   if (!h) return BLK_ERR_NULL;
-  int rc = check_weights(h->cfg, w);
-  if (rc) return rc;
   if (!x || !pos || !kc || !vc || !out || !ws) return BLK_ERR_NULL;
   const void* a16[] = {x, kc, vc, out, ws};
   for (const void* p : a16)
@@ -150,6 +173,16 @@ int check_call(blk_handle h, const blk_weights* w, const void* x,
   if (T < 1 || T > ((int64_t)1 << 31)) return BLK_ERR_SHAPE;
   if (L < 0 || L + T > h->cfg.max_ctx) return BLK_ERR_CACHE_OVERFLOW;
   return BLK_OK;
+}
+
+int check_call(blk_handle h, const blk_weights* w, const void* x,
+               const int64_t* pos, int64_t T, int64_t L, const void* kc,
+               const void* vc, const void* out, const void* kn, const void* vn,
+               const void* ws) {
+  if (!h) return BLK_ERR_NULL;
+  const int rc = check_weights(h->cfg, w);
+  if (rc) return rc;
+  return check_args(h, x, pos, T, L, kc, vc, out, kn, vn, ws);
 }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? BLK_OK : BLK_ERR_CUDA; }
@@ -450,6 +483,210 @@ int run_decode_batch(blk_handle h, const blk_weights* w, const void* x, const in
 
 }  // namespace
 
+namespace {
+
+// ---------------------------------------------------------------- decode
+// One layer's weights as the decode launch consumes them: fp16 matrices, or
+// quantized codes with their scales (and int4 zero points).
+struct LayerSrc {
+  const void* mat[kDecRoles];   // wq wk wv wo w_gate w_up w_down
+  const uint16_t* scale[kDecRoles];
+  const uint8_t* zero[kDecRoles];
+  const void *ln1, *ln2, *bq, *bk, *bv;
+};
+
+LayerSrc layer_src(const blk_weights& w) {
+  LayerSrc s = {};
+  const void* m[kDecRoles] = {w.wq, w.wk, w.wv, w.wo, w.w_gate, w.w_up, w.w_down};
+  for (int r = 0; r < kDecRoles; ++r) s.mat[r] = m[r];
+  s.ln1 = w.ln1_g; s.ln2 = w.ln2_g; s.bq = w.bq; s.bk = w.bk; s.bv = w.bv;
+  return s;
+}
+
+LayerSrc layer_src(const blk_qweights& w) {
+  LayerSrc s = {};
+  const blk_qmatrix* m[kDecRoles] = {&w.wq, &w.wk, &w.wv, &w.wo, &w.w_gate, &w.w_up, &w.w_down};
+  for (int r = 0; r < kDecRoles; ++r) {
+    s.mat[r] = m[r]->q;
+    s.scale[r] = static_cast<const uint16_t*>(m[r]->scale);
+    s.zero[r] = static_cast<const uint8_t*>(m[r]->zero);
+  }
+  s.ln1 = w.ln1_g; s.ln2 = w.ln2_g; s.bq = w.bq; s.bk = w.bk; s.bv = w.bv;
+  return s;
+}
+
+int weight_fmt(const blk_weights*) { return BLK_WFMT_F16; }
+int weight_fmt(const blk_qweights* w) { return w->format; }
+int weight_group(const blk_weights*) { return 0; }
+int weight_group(const blk_qweights* w) { return w->group; }
+int check_layer_weights(blk_handle h, const blk_weights* w) { return check_weights(h->cfg, w); }
+int check_layer_weights(blk_handle h, const blk_qweights* w) { return check_qweights(h->cfg, w); }
+
+template <typename WT>
+int decode_stack_impl(blk_handle h, const WT* w, int n_layers, void* const* k_caches,
+                      void* const* v_caches, const void* x, const int64_t* pos,
+                      int64_t cache_len, void* out, void* const* k_new, void* const* v_new,
+                      void* ws, size_t ws_bytes, void* stream) {
+  if (!h || !w || !k_caches || !v_caches) return BLK_ERR_NULL;
+  if (n_layers < 1) return BLK_ERR_SHAPE;
+  if (!h->decode_ok) return BLK_ERR_SHAPE;
+  for (int l = 0; l < n_layers; ++l) {
+    int rc = check_layer_weights(h, &w[l]);
+    if (rc) return rc;
+    rc = check_args(h, x, pos, 1, cache_len, k_caches[l], v_caches[l], out,
+                    k_new ? k_new[l] : nullptr, v_new ? v_new[l] : nullptr, ws);
+    if (rc) return rc;
+    if (weight_fmt(&w[l]) != weight_fmt(w) || weight_group(&w[l]) != weight_group(w))
+      return BLK_ERR_SHAPE;
+  }
+  const blk_config& c = h->cfg;
+  const int fmt = weight_fmt(w), group = weight_group(w);
+  if (decode_q_max_entries(c.hidden, c.n_heads, c.n_kv_heads, c.head_dim, c.intermediate, fmt,
+                           group, h->num_sms) > decode_q_entry_limit())
+    return BLK_ERR_SHAPE;
+  if (ws_bytes < decode_ws_bytes(c.hidden, c.n_heads, c.n_kv_heads, c.head_dim,
+                                 c.intermediate, h->num_sms))
+    return BLK_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Timer tm{h, s};
+  // DecodeParams holds the tensor maps and pointers of up to kDecMaxLayers
+  // layers; it lives in the handle to keep it off the host stack.
+  DecodeParams& p = *h->dec;
+  for (int l0 = 0; l0 < n_layers; l0 += kDecMaxLayers) {
+    const int nl = n_layers - l0 < kDecMaxLayers ? n_layers - l0 : kDecMaxLayers;
+    memset(&p, 0, sizeof p);
+    p.n_layers = nl;
+    p.H = c.hidden; p.Hq = c.n_heads; p.Hkv = c.n_kv_heads; p.D = c.head_dim;
+    p.I = c.intermediate; p.eps = c.rms_eps;
+    p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)c.head_dim));
+    p.max_ctx = c.max_ctx; p.cache_len = cache_len; p.pos = pos;
+    p.rope = h->rope; p.rope_len = c.max_ctx;
+    p.x_in = static_cast<const __half*>(l0 == 0 ? x : out);
+    p.out = static_cast<__half*>(out);
+    p.err = h->status;
+    p.trace = h->trace;
+    p.trace_len = h->trace_len;
+    p.fmt = fmt;
+    p.qgroup = group;
+    decode_ws_carve(p, ws, h->num_sms);
+    for (int k = 0; k < nl; ++k) {
+      const LayerSrc src = layer_src(w[l0 + k]);
+      DecLayer& d = p.layer[k];
+      d.wq = static_cast<const __half*>(src.mat[0]);
+      d.wk = static_cast<const __half*>(src.mat[1]);
+      d.wv = static_cast<const __half*>(src.mat[2]);
+      if (c.has_qkv_bias) {
+        d.bq = static_cast<const __half*>(src.bq);
+        d.bk = static_cast<const __half*>(src.bk);
+        d.bv = static_cast<const __half*>(src.bv);
+      }
+      d.wo = static_cast<const __half*>(src.mat[3]);
+      d.ln1 = static_cast<const __half*>(src.ln1);
+      d.ln2 = static_cast<const __half*>(src.ln2);
+      d.wg = static_cast<const __half*>(src.mat[4]);
+      d.wu = static_cast<const __half*>(src.mat[5]);
+      d.wd = static_cast<const __half*>(src.mat[6]);
+      d.kc = static_cast<__half*>(k_caches[l0 + k]);
+      d.vc = static_cast<__half*>(v_caches[l0 + k]);
+      d.k_new = static_cast<__half*>(k_new ? k_new[l0 + k] : nullptr);
+      d.v_new = static_cast<__half*>(v_new ? v_new[l0 + k] : nullptr);
+      const int64_t rows = (int64_t)c.n_kv_heads * c.max_ctx;
+      if (make_tmap_2d(&p.tm_k[k], d.kc, rows, c.head_dim, 64) ||
+          make_tmap_2d(&p.tm_v[k], d.vc, rows, c.head_dim, 64))
+        return BLK_ERR_CUDA;
+      // weights as 8-row boxes: {rows, K} per role
+      const int64_t H = c.hidden, QD = (int64_t)c.n_heads * c.head_dim,
+                    KD = (int64_t)c.n_kv_heads * c.head_dim, I = c.intermediate;
+      const int64_t rk[kDecRoles][2] = {{QD, H}, {KD, H}, {KD, H}, {H, QD},
+                                        {I, H},  {I, H},  {H, I}};
+      for (int r = 0; r < kDecRoles; ++r) {
+        int is3d = 0;
+        if (fmt == BLK_WFMT_F16) {
+          const int64_t nz = (rk[r][1] + 63) / 64;
+          const int cbs = (int)(nz < 24 ? nz : 24);
+          if (make_tmap_rows8(&p.tm_w[k][r], src.mat[r], rk[r][0], rk[r][1], cbs, &is3d))
+            return BLK_ERR_CUDA;
+          p.wbox_z[r] = cbs;
+          p.wnz[r] = (int)nz;
+        } else {
+          // code bytes per row; a box row covers 12 blocks of 128 INT8 codes
+          // or 6 blocks of 256 int4 codes: 1536 columns either way
+          const int64_t row_bytes = fmt == BLK_WFMT_I8 ? rk[r][1] : rk[r][1] / 2;
+          const int64_t nz = (row_bytes + 127) / 128;
+          const int per = fmt == BLK_WFMT_I8 ? 12 : 6;
+          const int cbs = (int)(nz < per ? nz : per);
+          if (make_tmap_codes(&p.tm_w[k][r], src.mat[r], rk[r][0], row_bytes, cbs, &is3d))
+            return BLK_ERR_CUDA;
+          p.wbox_z[r] = cbs;
+          p.wnz[r] = (int)nz;
+          p.qscale[k][r] = src.scale[r];
+          p.qzero[k][r] = src.zero[r];
+        }
+        p.w3d[r] = is3d;
+      }
+    }
+    BLK_LAUNCH(tm, kKDecodeStep, launch_decode_persistent(p, h->num_sms, s));
+  }
+  return BLK_OK;
+}
+
+// ------------------------------------------------------ quantized prefill
+size_t layer_f16_bytes(const blk_config& c) {
+  const size_t H = c.hidden, QD = (size_t)c.n_heads * c.head_dim,
+               KD = (size_t)c.n_kv_heads * c.head_dim, I = c.intermediate;
+  return 2 * (QD * H + 2 * KD * H + H * QD + 3 * I * H) + 7 * kAlign;
+}
+
+// Forms the layer's weights as fp16 at the start of the workspace, then runs
+// the fp16 prefill on them with the rest of the workspace.
+int run_prefill_q(blk_handle h, const blk_qweights* w, const void* x, const int64_t* pos,
+                  int64_t T, int64_t L, void* k_cache, void* v_cache, void* out, void* k_new,
+                  void* v_new, void* ws, size_t ws_bytes, void* stream) {
+  if (!h) return BLK_ERR_NULL;
+  int rc = check_qweights(h->cfg, w);
+  if (rc) return rc;
+  rc = check_args(h, x, pos, T, L, k_cache, v_cache, out, k_new, v_new, ws);
+  if (rc) return rc;
+  const blk_config& c = h->cfg;
+  const size_t wbytes = align_up(layer_f16_bytes(c));
+  if (ws_bytes < wbytes) return BLK_ERR_WORKSPACE;
+  if (ws_bytes - wbytes < prefill_ws(c, T, h->num_sms).total) return BLK_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int64_t H = c.hidden, QD = (int64_t)c.n_heads * c.head_dim,
+                KD = (int64_t)c.n_kv_heads * c.head_dim, I = c.intermediate;
+  const blk_qmatrix* m[kDecRoles] = {&w->wq, &w->wk, &w->wv, &w->wo, &w->w_gate, &w->w_up,
+                                     &w->w_down};
+  const int64_t rk[kDecRoles][2] = {{QD, H}, {KD, H}, {KD, H}, {H, QD}, {I, H}, {I, H}, {H, I}};
+  unsigned char* base = static_cast<unsigned char*>(ws);
+  __half* f16[kDecRoles];
+  size_t o = 0;
+  for (int r = 0; r < kDecRoles; ++r) {
+    f16[r] = reinterpret_cast<__half*>(base + o);
+    o = align_up(o + (size_t)rk[r][0] * rk[r][1] * 2);
+  }
+  {
+    Timer tm{h, s};
+    for (int r = 0; r < kDecRoles; ++r)
+      BLK_LAUNCH(tm, kKDequant, launch_dequant(w->format, m[r]->q, m[r]->scale, m[r]->zero,
+                                               rk[r][0], rk[r][1], w->group, f16[r],
+                                               h->num_sms, s));
+  }
+  blk_weights fw = {};
+  fw.ln1_g = w->ln1_g; fw.ln2_g = w->ln2_g; fw.bq = w->bq; fw.bk = w->bk; fw.bv = w->bv;
+  fw.wq = f16[0]; fw.wk = f16[1]; fw.wv = f16[2]; fw.wo = f16[3];
+  fw.w_gate = f16[4]; fw.w_up = f16[5]; fw.w_down = f16[6];
+  // the dequantized weights were written by the kernels just enqueued: the
+  // first prefill kernel must not start early (no chained launch here)
+  const uint32_t flags = h->flags;
+  h->flags &= ~BLK_FLAG_CHAIN;
+  rc = run_prefill(h, &fw, x, pos, T, L, k_cache, v_cache, out, k_new, v_new, base + wbytes,
+                   ws_bytes - wbytes, stream);
+  h->flags = flags;
+  return rc;
+}
+
+}  // namespace
+
 extern "C" {
 
 int blk_create(const blk_config* cfg, blk_handle* out) {
@@ -575,83 +812,46 @@ int blk_decode_stack(blk_handle h, const blk_weights* w, int n_layers,
                      const int64_t* pos, int64_t cache_len, void* out,
                      void* const* k_new, void* const* v_new, void* ws, size_t ws_bytes,
                      void* stream) {
-  if (!h || !w || !k_caches || !v_caches) return BLK_ERR_NULL;
-  if (n_layers < 1) return BLK_ERR_SHAPE;
-  if (!h->decode_ok) return BLK_ERR_SHAPE;
-  for (int l = 0; l < n_layers; ++l) {
-    const int rc = check_call(h, &w[l], x, pos, 1, cache_len, k_caches[l], v_caches[l], out,
-                              k_new ? k_new[l] : nullptr, v_new ? v_new[l] : nullptr, ws);
-    if (rc) return rc;
-  }
-  const blk_config& c = h->cfg;
-  if (ws_bytes < decode_ws_bytes(c.hidden, c.n_heads, c.n_kv_heads, c.head_dim,
-                                 c.intermediate, h->num_sms))
-    return BLK_ERR_WORKSPACE;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  Timer tm{h, s};
-  // DecodeParams holds the tensor maps and pointers of up to kDecMaxLayers
-  // layers; it lives in the handle to keep it off the host stack.
-  DecodeParams& p = *h->dec;
-  for (int l0 = 0; l0 < n_layers; l0 += kDecMaxLayers) {
-    const int nl = n_layers - l0 < kDecMaxLayers ? n_layers - l0 : kDecMaxLayers;
-    memset(&p, 0, sizeof p);
-    p.n_layers = nl;
-    p.H = c.hidden; p.Hq = c.n_heads; p.Hkv = c.n_kv_heads; p.D = c.head_dim;
-    p.I = c.intermediate; p.eps = c.rms_eps;
-    p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)c.head_dim));
-    p.max_ctx = c.max_ctx; p.cache_len = cache_len; p.pos = pos;
-    p.rope = h->rope; p.rope_len = c.max_ctx;
-    p.x_in = static_cast<const __half*>(l0 == 0 ? x : out);
-    p.out = static_cast<__half*>(out);
-    p.err = h->status;
-    p.trace = h->trace;
-    p.trace_len = h->trace_len;
-    decode_ws_carve(p, ws, h->num_sms);
-    for (int k = 0; k < nl; ++k) {
-      const blk_weights& wl = w[l0 + k];
-      DecLayer& d = p.layer[k];
-      d.wq = static_cast<const __half*>(wl.wq);
-      d.wk = static_cast<const __half*>(wl.wk);
-      d.wv = static_cast<const __half*>(wl.wv);
-      if (c.has_qkv_bias) {
-        d.bq = static_cast<const __half*>(wl.bq);
-        d.bk = static_cast<const __half*>(wl.bk);
-        d.bv = static_cast<const __half*>(wl.bv);
-      }
-      d.wo = static_cast<const __half*>(wl.wo);
-      d.ln1 = static_cast<const __half*>(wl.ln1_g);
-      d.ln2 = static_cast<const __half*>(wl.ln2_g);
-      d.wg = static_cast<const __half*>(wl.w_gate);
-      d.wu = static_cast<const __half*>(wl.w_up);
-      d.wd = static_cast<const __half*>(wl.w_down);
-      d.kc = static_cast<__half*>(k_caches[l0 + k]);
-      d.vc = static_cast<__half*>(v_caches[l0 + k]);
-      d.k_new = static_cast<__half*>(k_new ? k_new[l0 + k] : nullptr);
-      d.v_new = static_cast<__half*>(v_new ? v_new[l0 + k] : nullptr);
-      const int64_t rows = (int64_t)c.n_kv_heads * c.max_ctx;
-      if (make_tmap_2d(&p.tm_k[k], d.kc, rows, c.head_dim, 64) ||
-          make_tmap_2d(&p.tm_v[k], d.vc, rows, c.head_dim, 64))
-        return BLK_ERR_CUDA;
-      // weights as 8-row boxes: {base, rows, K} per role
-      const int64_t H = c.hidden, QD = (int64_t)c.n_heads * c.head_dim,
-                    KD = (int64_t)c.n_kv_heads * c.head_dim, I = c.intermediate;
-      const struct { const void* b; int64_t rows, K; } wr[kDecRoles] = {
-          {d.wq, QD, H}, {d.wk, KD, H}, {d.wv, KD, H}, {d.wo, H, QD},
-          {d.wg, I, H},  {d.wu, I, H},  {d.wd, H, I}};
-      for (int r = 0; r < kDecRoles; ++r) {
-        const int64_t nz = (wr[r].K + 63) / 64;
-        const int cbs = (int)(nz < 24 ? nz : 24);
-        int is3d = 0;
-        if (make_tmap_rows8(&p.tm_w[k][r], wr[r].b, wr[r].rows, wr[r].K, cbs, &is3d))
-          return BLK_ERR_CUDA;
-        p.w3d[r] = is3d;
-        p.wbox_z[r] = cbs;
-        p.wnz[r] = (int)nz;
-      }
-    }
-    BLK_LAUNCH(tm, kKDecodeStep, launch_decode_persistent(p, h->num_sms, s));
-  }
-  return BLK_OK;
+  return decode_stack_impl(h, w, n_layers, k_caches, v_caches, x, pos, cache_len, out, k_new,
+                           v_new, ws, ws_bytes, stream);
+}
+
+int blk_decode_stack_q(blk_handle h, const blk_qweights* w, int n_layers,
+                       void* const* k_caches, void* const* v_caches, const void* x,
+                       const int64_t* pos, int64_t cache_len, void* out, void* const* k_new,
+                       void* const* v_new, void* ws, size_t ws_bytes, void* stream) {
+  return decode_stack_impl(h, w, n_layers, k_caches, v_caches, x, pos, cache_len, out, k_new,
+                           v_new, ws, ws_bytes, stream);
+}
+
+int blk_decode_q(blk_handle h, const blk_qweights* w, const void* x, const int64_t* pos,
+                 int64_t cache_len, void* k_cache, void* v_cache, void* out, void* k_new,
+                 void* v_new, void* ws, size_t ws_bytes, void* stream) {
+  void* kcs[1] = {k_cache};
+  void* vcs[1] = {v_cache};
+  void* kns[1] = {k_new};
+  void* vns[1] = {v_new};
+  return decode_stack_impl(h, w, 1, kcs, vcs, x, pos, cache_len, out, kns, vns, ws, ws_bytes,
+                           stream);
+}
+
+size_t blk_qworkspace_bytes(blk_handle h, int64_t max_T) {
+  if (!h || max_T < 1) return 0;
+  return align_up(layer_f16_bytes(h->cfg)) + blk_workspace_bytes(h, max_T);
+}
+
+int blk_prefill_q(blk_handle h, const blk_qweights* w, const void* x, const int64_t* pos,
+                  int64_t T, void* k_cache, void* v_cache, void* out, void* k_new, void* v_new,
+                  void* ws, size_t ws_bytes, void* stream) {
+  return run_prefill_q(h, w, x, pos, T, 0, k_cache, v_cache, out, k_new, v_new, ws, ws_bytes,
+                       stream);
+}
+
+int blk_prefill_kv_q(blk_handle h, const blk_qweights* w, const void* x, const int64_t* pos,
+                     int64_t T, int64_t cache_len, void* k_cache, void* v_cache, void* out,
+                     void* k_new, void* v_new, void* ws, size_t ws_bytes, void* stream) {
+  return run_prefill_q(h, w, x, pos, T, cache_len, k_cache, v_cache, out, k_new, v_new, ws,
+                       ws_bytes, stream);
 }
 
 }  // extern "C"

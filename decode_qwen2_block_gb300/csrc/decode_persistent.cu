@@ -39,6 +39,7 @@
 //
 // Every wait (ring mbarriers, grid barrier) is bounded; on a timeout the
 // kernel records an error, stops, lets its issued copies land and returns.
+#include <algorithm>
 #include <type_traits>
 
 #include "common.cuh"
@@ -52,29 +53,47 @@ namespace {
 constexpr int kCW = 12;                 // consumer warps
 constexpr int kCT = kCW * 32;           // consumer threads
 constexpr int kThreads = kCT + 32;      // + one producer warp
-constexpr int kStageBytes = 48 * 1024;
-constexpr int kStages = 4;
+// Weight formats of the projections (the ABI's BLK_WFMT_* values).
+enum WFmt { kF16 = 0, kI8 = 1, kU4 = 2 };
+// Ring geometry per weight format.  A chunk is always 16 weight rows x kKc
+// columns: 48 KB of fp16, 24 KB of INT8 codes, 12 KB of packed int4 codes;
+// a K/V tile (64 slots of K and V) is 32 KB at D = 128.  Quantized formats
+// use five 32 KB stages and keep 16 KB for the phase's scales.
+template <int FMT> struct Ring {
+  static constexpr int kStages = FMT == kF16 ? 4 : 5;
+  static constexpr int kStageBytes = FMT == kF16 ? 48 * 1024 : 32 * 1024;
+  static constexpr int kBoxCB = FMT == kF16 ? 24 : (FMT == kI8 ? 12 : 6);  // 128-byte blocks per box row
+  static constexpr int kBoxBytes = 8 * 128 * kBoxCB;   // one 8-row box
+  static constexpr int kQsBytes = FMT == kF16 ? 0 : 16 * 1024;
+};
+constexpr int kMaxStages = 5;
+constexpr int kQsEntries = 5120;        // staged scales (and zero points) per phase
 constexpr int kAttnWarps = 4;           // 4 x 16 slots = one 64-slot tile
 constexpr int kSlots = 64;
 constexpr int kBoxRows = 8;             // weight rows per TMA box
-constexpr int kCB = 24;                 // 64-column blocks per box
-constexpr int kKc = kCB * 64;           // weight columns per ring stage
-constexpr int kBoxBytes = kBoxRows * kKc * 2;  // 24 KB; two boxes per stage
+constexpr int kCB = 24;                 // 64-column blocks per fp16 box
+constexpr int kKc = kCB * 64;           // weight columns per chunk (every format)
 constexpr int kBatch = 10;              // groups whose partials shared memory holds
-constexpr int kPfAhead = 0;             // chunks the producer may prefetch into L2
 constexpr int kPartFloats = 2048;       // [group][warp][16] partial sums
 constexpr int kQStride = 136;           // Q tile row stride in halves (padded)
-static_assert(2 * kBoxBytes <= kStageBytes, "stage too small");
+static_assert(2 * Ring<kF16>::kBoxBytes <= Ring<kF16>::kStageBytes, "stage too small");
+static_assert(2 * Ring<kI8>::kBoxBytes <= Ring<kI8>::kStageBytes, "stage too small");
 static_assert(kBatch * kCW * 16 <= kPartFloats, "partials too small");
 
-constexpr int kXsOff = kStages * kStageBytes;
-constexpr int kPartOff = kXsOff + kDecMaxVec * 2;
-constexpr int kQOff = kPartOff;         // the Q tile reuses the partials area
-constexpr int kBarOff = kPartOff + kPartFloats * 4;
 constexpr int kResRows = 152;           // hidden rows per CTA (o_proj)
-constexpr int kResOff = kBarOff + 256;  // x slice of this CTA's o_proj rows
-constexpr int kSmemUsed = kResOff + kResRows * 4;
-constexpr int kSmemBytes = kSmemUsed + 1024;  // + alignment slack
+// shared memory layout: ring | staged input vector | partial sums (also the
+// Q tile) | mbarriers and flags | o_proj residual slice | staged scales
+template <int FMT> struct Smem {
+  static constexpr int kXsOff = Ring<FMT>::kStages * Ring<FMT>::kStageBytes;
+  static constexpr int kPartOff = kXsOff + kDecMaxVec * 2;
+  static constexpr int kQOff = kPartOff;
+  static constexpr int kBarOff = kPartOff + kPartFloats * 4;
+  static constexpr int kResOff = kBarOff + 256;
+  static constexpr int kQsOff = kResOff + kResRows * 4;
+  static constexpr int kUsed = kQsOff + Ring<FMT>::kQsBytes;
+  static constexpr int kBytes = kUsed + 1024;   // + alignment slack
+};
+static_assert(Smem<kF16>::kBytes <= 227 * 1024 && Smem<kU4>::kBytes <= 227 * 1024, "smem");
 
 enum Phase { kPhQKV = 0, kPhAttn = 1, kPhComb = 2, kPhO = 3, kPhGU = 4, kPhDown = 5 };
 // weight roles, the order of DecodeParams::tm_w
@@ -115,20 +134,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(x), "r"(y)
-               : "memory");
-}
-
-__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, int y, int z) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(x), "r"(y), "r"(z)
-               : "memory");
-}
-
 __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -165,6 +170,45 @@ __device__ __forceinline__ void mma16816(float* d, const uint32_t* a, uint32_t b
 __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
   const __half2 h = __floats2half2_rn(a, b);
   return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ __half2 u32_as_h2(uint32_t v) { return *reinterpret_cast<__half2*>(&v); }
+__device__ __forceinline__ uint32_t h2_as_u32(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+
+// Four INT8 codes (bytes of r, in k order) to two fp16 pairs scaled by s.
+// Byte b + 128 placed under the exponent field of 1024 (fp16 0x6400) is the
+// fp16 value 1024 + b + 128, exactly (the spacing of fp16 at 1024 is 1), so
+// subtracting 1152 gives the code b exactly; the product with the scale is
+// the one rounding.
+__device__ __forceinline__ void i8x4_scaled(uint32_t r, __half2 s, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = r ^ 0x80808080u;
+  const __half2 off = __float2half2_rn(1152.f);
+  lo = h2_as_u32(__hmul2(__hsub2(u32_as_h2(__byte_perm(u, 0x64646464u, 0x4140)), off), s));
+  hi = h2_as_u32(__hmul2(__hsub2(u32_as_h2(__byte_perm(u, 0x64646464u, 0x4342)), off), s));
+}
+
+// Four 4-bit codes (nibbles of v, in k order, the first in the low nibble)
+// minus the zero point z, scaled by s; 1024 + c and 1024 + z are exact fp16
+// values, so c - z is exact before the scaling.
+__device__ __forceinline__ void u4x4_scaled(uint32_t v, uint32_t z, __half2 s, uint32_t& lo,
+                                            uint32_t& hi) {
+  const uint32_t a = 0x64006400u | (v & 0xFu) | ((v & 0xF0u) << 12);
+  const uint32_t b = 0x64006400u | ((v >> 8) & 0xFu) | ((v & 0xF000u) << 4);
+  const __half2 off = u32_as_h2((0x6400u + z) * 0x10001u);
+  lo = h2_as_u32(__hmul2(__hsub2(u32_as_h2(a), off), s));
+  hi = h2_as_u32(__hmul2(__hsub2(u32_as_h2(b), off), s));
 }
 
 // Address of the 16-byte chunk `ch` (8 halves) of row `r` in a 64-row tile
@@ -506,6 +550,74 @@ __device__ void stage_combine(const DecodeParams& p, __half* xs) {
   named_sync(1, kCT);
 }
 
+// Rows and K of weight role r.
+__device__ __forceinline__ void role_shape(const DecodeParams& p, int r, int& rows, int& K) {
+  const int QD = p.Hq * p.D, KD = p.Hkv * p.D;
+  if (r == kWq) { rows = QD; K = p.H; }
+  else if (r == kWk || r == kWv) { rows = KD; K = p.H; }
+  else if (r == kWo) { rows = p.H; K = QD; }
+  else if (r == kWg || r == kWu) { rows = p.I; K = p.H; }
+  else { rows = p.H; K = p.I; }
+}
+
+// Quantized weights: scales staged per tile row of a work group.  INT8 has
+// one scale per row; int4 one scale and one zero point per `group` columns
+// of the work group's column range (all of K, or the one column chunk of a
+// down-projection item).
+template <int FMT>
+__host__ __device__ __forceinline__ int qs_groups(int ph, int K, int group) {
+  if (FMT != kU4) return 1;
+  return ph == kPhDown ? (K < kKc ? K : kKc) / group : K / group;
+}
+
+// Stages this CTA's scales (and int4 zero points) of one projection phase
+// into shared memory, entry (gi * 16 + m) * GM + j for tile row m of work
+// group gi and scale group j; rows past the matrix get scale 0.  Every load
+// is issued before any store, so the staging costs one round trip.
+template <int D, int FMT>
+__device__ void stage_qscales(const DecodeParams& p, int l, int ph, const PhaseWork& W,
+                              __half* qs_s, uint8_t* qs_z) {
+  const int GM = qs_groups<FMT>(ph, W.K, p.qgroup);
+  const int total = W.ngroups * 16 * GM;   // <= kQsEntries, checked on the host
+  constexpr int kPer = (kQsEntries + kCT - 1) / kCT;
+  uint16_t sv[kPer];
+  uint32_t zv[kPer];
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int e = threadIdx.x + k * kCT;
+    sv[k] = 0;
+    zv[k] = 0;
+    if (e < total) {
+      const int j = e % GM, m = (e / GM) & 15, gi = e / (16 * GM);
+      const GroupDesc g = group_desc<D>(p, ph, W, gi);
+      const int r = m < kBoxRows ? g.ra : g.rb;
+      const int y = m < kBoxRows ? g.ya + m : (g.yb >= 0 ? g.yb + m - kBoxRows : -1);
+      int rows, K;
+      role_shape(p, r, rows, K);
+      if (y >= 0 && y < rows) {
+        if (FMT == kI8) {
+          sv[k] = __ldg(p.qscale[l][r] + y);
+        } else {
+          const int ng = K / p.qgroup, jg = g.ka * kKc / p.qgroup + j;
+          if (jg < ng) {
+            sv[k] = __ldg(p.qscale[l][r] + (size_t)y * ng + jg);
+            zv[k] = __ldg(p.qzero[l][r] + (size_t)y * ng + jg);
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int e = threadIdx.x + k * kCT;
+    if (e < total) {
+      qs_s[e] = __ushort_as_half(sv[k]);
+      if (FMT == kU4) qs_z[e] = (uint8_t)zv[k];
+    }
+  }
+  named_sync(1, kCT);
+}
+
 // Position in this CTA's stream of ring chunks: layer l, phase ph, and
 // within the phase either the K/V tile c or (group gi, column chunk kc).
 struct Cursor {
@@ -562,19 +674,27 @@ __device__ __forceinline__ void trace_point(const DecodeParams& p, int l, int ph
 }
 
 // ------------------------------------------------------------ the kernel
-template <int D>
+template <int D, int FMT>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
+  using RG = Ring<FMT>;
+  using SM = Smem<FMT>;
+  constexpr int kStages = RG::kStages;
+  constexpr int kStageBytes = RG::kStageBytes;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
-  __half* xs = reinterpret_cast<__half*>(smem + kXsOff);
-  float* part = reinterpret_cast<float*>(smem + kPartOff);
-  __half* qtile = reinterpret_cast<__half*>(smem + kQOff);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBarOff);
-  uint64_t* empty = full + kStages;
-  float* red = reinterpret_cast<float*>(empty + kStages);        // [16]
+  __half* xs = reinterpret_cast<__half*>(smem + SM::kXsOff);
+  float* part = reinterpret_cast<float*>(smem + SM::kPartOff);
+  __half* qtile = reinterpret_cast<__half*>(smem + SM::kQOff);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + SM::kBarOff);
+  uint64_t* empty = full + kMaxStages;
+  float* red = reinterpret_cast<float*>(empty + kMaxStages);     // [16]
+  // staged scales of a quantized phase: kQsEntries fp16 scales, then as many
+  // int4 zero points
+  __half* qs_s = reinterpret_cast<__half*>(smem + SM::kQsOff);
+  uint8_t* qs_z = reinterpret_cast<uint8_t*>(qs_s + kQsEntries);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(red + 16);
   // quiet: set from the moment the consumers take the last ring chunk of a
   // phase until they have staged the next phase's inputs.  The producer
@@ -583,7 +703,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // issued then would delay them (measured: a grid barrier took ~2.5 us with
   // copies in flight, ~1.4 us without).
   volatile int* quiet = abort_flag + 1;
-  float* xres = reinterpret_cast<float*>(smem + kResOff);       // x of the o_proj rows
+  float* xres = reinterpret_cast<float*>(smem + SM::kResOff);   // x of the o_proj rows
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
@@ -608,7 +728,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane != 0) return;
     // column blocks one box copy covers in chunk kc of role r
     auto box_cbs = [&](int r, int kc) -> int {
-      return p.w3d[r] ? p.wbox_z[r] : min(kCB, p.wnz[r] - kc * kCB);
+      return p.w3d[r] ? p.wbox_z[r] : min(RG::kBoxCB, p.wnz[r] - kc * RG::kBoxCB);
     };
     auto chunk_bytes = [&](const Cursor& cu) -> uint32_t {
       if (cu.ph == kPhAttn) return 2u * kv_tile_bytes;
@@ -619,15 +739,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       return (int)(ar.g * p.max_ctx + ar.j0 + (int64_t)cu.c * kSlots);
     };
     // one 8-row box of role r at row y, column chunk kc: a single 3-D copy,
-    // or (K not a multiple of 64) one 2-D copy per 64-column block
+    // or (a row not a multiple of 128 bytes) one 2-D copy per 128-byte block
+    // (64 fp16 columns, 128 INT8 columns or 128 bytes of packed int4)
     auto copy_box = [&](int l, int r, int y, int kc, uint32_t dst, uint32_t bar) {
       const CUtensorMap* m = &p.tm_w[l][r];
       if (p.w3d[r]) {
-        tma_load_3d(dst, m, 0, y, kc * kCB, bar);
+        tma_load_3d(dst, m, 0, y, kc * RG::kBoxCB, bar);
       } else {
-        const int n = min(kCB, p.wnz[r] - kc * kCB);
+        const int n = min(RG::kBoxCB, p.wnz[r] - kc * RG::kBoxCB);
+        const int epb = FMT == kF16 ? 64 : 128;   // tensor elements per block
         for (int cb = 0; cb < n; ++cb)
-          tma_load_2d_u32(dst + cb * (kBoxRows * 128), m, (kc * kCB + cb) * 64, y, bar);
+          tma_load_2d_u32(dst + cb * (kBoxRows * 128), m, (kc * RG::kBoxCB + cb) * epb, y, bar);
       }
     };
     auto load = [&](const Cursor& cu, uint8_t* st, uint64_t* bar) {
@@ -642,39 +764,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const uint32_t dst = smem_u32(st), mb = smem_u32(bar);
       copy_box(cu.l, cu.g.ra, cu.g.ya, cu.kc, dst, mb);
-      if (cu.g.yb >= 0) copy_box(cu.l, cu.g.rb, cu.g.yb, cu.kc, dst + kBoxBytes, mb);
-    };
-    // While the ring is full the lane asks L2 for the chunks that come next
-    // (up to kPfAhead of them): the TMA unit and HBM would otherwise idle
-    // while the consumers wait at a grid barrier, and those chunks then load
-    // from L2.
-    auto prefetch = [&](const Cursor& cu) {
-      if (cu.ph == kPhAttn) {
-        const int y = kv_row(cu);
-#pragma unroll
-        for (int h = 0; h < D / 64; ++h) {
-          tma_prefetch_2d(&p.tm_k[cu.l], h * 64, y);
-          tma_prefetch_2d(&p.tm_v[cu.l], h * 64, y);
-        }
-        return;
-      }
-      const int ys[2] = {cu.g.ya, cu.g.yb}, rs[2] = {cu.g.ra, cu.g.rb};
-      for (int b = 0; b < 2; ++b) {
-        if (ys[b] < 0) continue;
-        const CUtensorMap* m = &p.tm_w[cu.l][rs[b]];
-        if (p.w3d[rs[b]]) {
-          tma_prefetch_3d(m, 0, ys[b], cu.kc * kCB);
-        } else {
-          const int n = min(kCB, p.wnz[rs[b]] - cu.kc * kCB);
-          for (int cb = 0; cb < n; ++cb) tma_prefetch_2d(m, (cu.kc * kCB + cb) * 64, ys[b]);
-        }
-      }
+      if (cu.g.yb >= 0) copy_box(cu.l, cu.g.rb, cu.g.yb, cu.kc, dst + RG::kBoxBytes, mb);
     };
     Cursor rc = {0, 0, 0, 0, 0, {}, {}};
     bool more = cursor_begin<D>(rc, p, ar);
-    Cursor pc = rc;     // next chunk to prefetch, index pit
-    bool pmore = more;
-    int pit = 0;
     int it = 0;   // chunks issued to the ring
     bool ok = true;
     while (more && ok) {
@@ -682,14 +775,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (it >= kStages) {
         const uint32_t par = ((it / kStages) - 1) & 1;
         uint64_t t0 = 0;
-        if (pit < it) { pc = rc; pit = it; pmore = more; }
         while (!mbar_test(&empty[s], par)) {
-          if (pmore && pit < it + kPfAhead) {
-            prefetch(pc);
-            ++pit;
-            pmore = cursor_next<D>(pc, p, ar);
-            continue;
-          }
           if (*abort_flag) { ok = false; break; }
           if (t0 == 0) t0 = global_ns();
           else if (global_ns() - t0 > kWaitLimitNs) {
@@ -1040,15 +1126,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           stage_copy(ph == kPhO ? p.attn16 : p.act16, W.K, xs);
         }
+        if constexpr (FMT != kF16) stage_qscales<D, FMT>(p, l, ph, W, qs_s, qs_z);
         if (tid == 0) *quiet = 0;
         // y = W x on the tensor cores: A = a chunk's 16 rows x 16 columns
         // (ldmatrix from the two swizzled boxes), B = x as the only non-zero
         // column, fp32 accumulators; the warps split each chunk's 16-column
         // steps.  Partials of up to kBatch groups stay in shared memory and
         // the epilogue adds them in warp order.
-        const int tg = lane & 3, m8 = lane >> 3, r8 = lane & 7;
-        const uint32_t abox = (uint32_t)((m8 & 1) * kBoxBytes + r8 * 128);
+        const int tg = lane & 3, m8 = lane >> 3, r8 = lane & 7, g8 = lane >> 2;
+        const uint32_t abox = (uint32_t)((m8 & 1) * RG::kBoxBytes + r8 * 128);
         const int khalf = m8 >> 1;
+        const int GM = qs_groups<FMT>(ph, W.K, p.qgroup);
         for (int b0 = 0; b0 < W.ngroups; b0 += kBatch) {
           const int b1 = min(W.ngroups, b0 + kBatch);
           for (int gi = b0; gi < b1; ++gi) {
@@ -1060,17 +1148,53 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (gi == W.ngroups - 1 && kc == g.kb - 1 && tid == 0) *quiet = 1;
               const int nks = min(kKc, W.K - kc * kKc) / 16;
               const int ks0 = warp * nks / kCW, ks1 = (warp + 1) * nks / kCW;
-              const uint32_t st = smem_u32(ring + (size_t)s * kStageBytes) + abox;
-              const __half* xk = xs + kc * kKc + 2 * tg;
-              for (int ks = ks0; ks < ks1; ++ks) {
-                uint32_t a[4];
-                ldsm_x4(st + (ks >> 2) * 1024 + (((((ks & 3) << 1) | khalf) ^ r8) << 4), a);
-                uint32_t x0 = 0u, x1 = 0u;
-                if (lane < 4) {
-                  x0 = *reinterpret_cast<const uint32_t*>(xk + ks * 16);
-                  x1 = *reinterpret_cast<const uint32_t*>(xk + ks * 16 + 8);
+              if constexpr (FMT == kF16) {
+                const uint32_t st = smem_u32(ring + (size_t)s * kStageBytes) + abox;
+                const __half* xk = xs + kc * kKc + 2 * tg;
+                for (int ks = ks0; ks < ks1; ++ks) {
+                  uint32_t a[4];
+                  ldsm_x4(st + (ks >> 2) * 1024 + (((((ks & 3) << 1) | khalf) ^ r8) << 4), a);
+                  uint32_t x0 = 0u, x1 = 0u;
+                  if (lane < 4) {
+                    x0 = *reinterpret_cast<const uint32_t*>(xk + ks * 16);
+                    x1 = *reinterpret_cast<const uint32_t*>(xk + ks * 16 + 8);
+                  }
+                  mma16816(d, a, x0, x1);
                 }
-                mma16816(d, a, x0, x1);
+              } else {
+                // Quantized codes: each lane reads the 4 consecutive codes
+                // k = 16 ks + 4 tg .. + 3 of rows g8 (box A) and g8 + 8 (box
+                // B) and makes them the A-fragment slots (2 tg, 2 tg + 1) and
+                // (2 tg + 8, 2 tg + 9); x is read in the same k order, so the
+                // product sums every k once.
+                const uint32_t sta = smem_u32(ring + (size_t)s * kStageBytes) + g8 * 128;
+                const uint32_t stb = sta + RG::kBoxBytes;
+                const __half* srow = qs_s + (gi * 16 + g8) * GM;
+                const uint8_t* zrow = qs_z + (gi * 16 + g8) * GM;
+                const int kbase = (kc - g.ka) * kKc;
+                for (int ks = ks0; ks < ks1; ++ks) {
+                  const int j = FMT == kI8 ? 0 : (kbase + 16 * ks) / p.qgroup;
+                  const __half2 sA = __half2half2(srow[j]), sB = __half2half2(srow[8 * GM + j]);
+                  uint32_t a[4];
+                  if constexpr (FMT == kI8) {
+                    const uint32_t off = (ks >> 3) * 1024 + (((ks & 7) ^ g8) << 4) + 4 * tg;
+                    i8x4_scaled(lds_u32(sta + off), sA, a[0], a[2]);
+                    i8x4_scaled(lds_u32(stb + off), sB, a[1], a[3]);
+                  } else {
+                    const uint32_t off =
+                        (ks >> 4) * 1024 + ((((ks & 15) >> 1) ^ g8) << 4) + 8 * (ks & 1) + 2 * tg;
+                    u4x4_scaled(lds_u16(sta + off), zrow[j], sA, a[0], a[2]);
+                    u4x4_scaled(lds_u16(stb + off), zrow[8 * GM + j], sB, a[1], a[3]);
+                  }
+                  uint32_t x0 = 0u, x1 = 0u;
+                  if (lane < 4) {
+                    const uint2 xv =
+                        *reinterpret_cast<const uint2*>(xs + kc * kKc + 16 * ks + 4 * lane);
+                    x0 = xv.x;
+                    x1 = xv.y;
+                  }
+                  mma16816(d, a, x0, x1);
+                }
               }
               give(s);
             }
@@ -1198,30 +1322,71 @@ void decode_ws_carve(DecodeParams& p, void* ws, int num_sms) {
   p.fold = p.S <= 32 ? 1 : 0;
 }
 
+template <int D, int FMT>
+static cudaError_t launch_one(const cudaLaunchConfig_t& base, const DecodeParams& p) {
+  cudaLaunchConfig_t cfg = base;
+  cfg.dynamicSmemBytes = Smem<FMT>::kBytes;
+  return cudaLaunchKernelEx(&cfg, decode_persistent_kernel<D, FMT>, p);
+}
+
 cudaError_t launch_decode_persistent(DecodeParams& p, int num_sms, cudaStream_t s) {
   cudaError_t e = cudaMemsetAsync(p.barrier, 0, sizeof(unsigned), s);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_sms);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (p.D == 128) return cudaLaunchKernelEx(&cfg, decode_persistent_kernel<128>, p);
-  if (p.D == 64) return cudaLaunchKernelEx(&cfg, decode_persistent_kernel<64>, p);
+  if (p.D == 128) {
+    if (p.fmt == kF16) return launch_one<128, kF16>(cfg, p);
+    if (p.fmt == kI8) return launch_one<128, kI8>(cfg, p);
+    if (p.fmt == kU4) return launch_one<128, kU4>(cfg, p);
+  } else if (p.D == 64) {
+    if (p.fmt == kF16) return launch_one<64, kF16>(cfg, p);
+    if (p.fmt == kI8) return launch_one<64, kI8>(cfg, p);
+    if (p.fmt == kU4) return launch_one<64, kU4>(cfg, p);
+  }
   return cudaErrorInvalidValue;
 }
 
-cudaError_t configure_decode_persistent() {
-  const cudaError_t e = cudaFuncSetAttribute(
-      decode_persistent_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(decode_persistent_kernel<64>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+template <int D, int FMT>
+static cudaError_t configure_one() {
+  return cudaFuncSetAttribute(decode_persistent_kernel<D, FMT>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<FMT>::kBytes);
 }
+
+cudaError_t configure_decode_persistent() {
+  const cudaError_t es[6] = {configure_one<128, kF16>(), configure_one<128, kI8>(),
+                             configure_one<128, kU4>(),  configure_one<64, kF16>(),
+                             configure_one<64, kI8>(),   configure_one<64, kU4>()};
+  for (cudaError_t e : es)
+    if (e != cudaSuccess) return e;
+  return cudaSuccess;
+}
+
+int decode_q_max_entries(int H, int Hq, int Hkv, int D, int I, int fmt, int group, int num_sms) {
+  if (fmt == kF16) return 0;
+  const int QD = Hq * D;
+  auto per_cta = [&](int units) { return (units + num_sms - 1) / num_sms; };
+  // work groups per CTA and K of each phase (see phase_work)
+  const int g_qkv = per_cta((Hq + 2 * Hkv) * (D / 16));
+  const int g_o = (per_cta(H / kBoxRows) + 1) / 2;
+  const int g_gu = per_cta(I / kBoxRows);
+  const int g_dn = per_cta(((H + 2 * kBoxRows - 1) / (2 * kBoxRows)) * ((I + kKc - 1) / kKc));
+  auto gm = [&](int ph, int K) {
+    return fmt == kI8 ? qs_groups<kI8>(ph, K, group) : qs_groups<kU4>(ph, K, group);
+  };
+  int m = g_qkv * 16 * gm(kPhQKV, H);
+  m = std::max(m, g_o * 16 * gm(kPhO, QD));
+  m = std::max(m, g_gu * 16 * gm(kPhGU, H));
+  m = std::max(m, g_dn * 16 * gm(kPhDown, I));
+  return m;
+}
+
+int decode_q_entry_limit() { return kQsEntries; }
 
 }  // namespace blk

@@ -57,6 +57,13 @@ struct DecodeParams {
   int fold;             // S <= 32: splits merged in the o_proj staging
   uint64_t* trace;      // optional per-CTA phase timeline (nullptr = off)
   size_t trace_len;     // entries of trace
+  // weight format: 0 fp16 (tm_w views the fp16 matrices), 1 INT8 codes with
+  // one fp16 scale per row, 2 packed int4 codes with an fp16 scale and a
+  // uint8 zero point per qgroup columns of a row (tm_w views the codes)
+  int fmt;
+  int qgroup;
+  const uint16_t* qscale[kDecMaxLayers][kDecRoles];  // fp16 bits
+  const uint8_t* qzero[kDecMaxLayers][kDecRoles];
 };
 
 // Workspace bytes for the decode path (grid = num_sms CTAs).
@@ -68,5 +75,9 @@ static_assert(sizeof(DecodeParams) <= 32764, "kernel parameter space");
 
 cudaError_t launch_decode_persistent(DecodeParams& p, int num_sms, cudaStream_t s);
 cudaError_t configure_decode_persistent();
+// Quantized formats stage a phase's scales in shared memory: the largest
+// number of entries any phase needs (0 for fp16), and the limit.
+int decode_q_max_entries(int H, int Hq, int Hkv, int D, int I, int fmt, int group, int num_sms);
+int decode_q_entry_limit();
 
 }  // namespace blk

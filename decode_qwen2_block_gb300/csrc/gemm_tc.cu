@@ -906,6 +906,34 @@ int make_tmap_rows8(CUtensorMap* map, const void* base, int64_t rows, int64_t K,
   return r == CUDA_SUCCESS ? 0 : -1;
 }
 
+int make_tmap_codes(CUtensorMap* map, const void* base, int64_t rows, int64_t row_bytes,
+                    int cbs, int* is3d) {
+  const EncodeTiledFn encode = encode_tiled();
+  if (!encode) return -1;
+  CUresult r;
+  if (row_bytes % 128 == 0) {
+    // (128 bytes, rows, row_bytes / 128 blocks): one copy moves 8 rows x cbs blocks
+    cuuint64_t dims[3] = {128, (cuuint64_t)rows, (cuuint64_t)(row_bytes / 128)};
+    cuuint64_t strides[2] = {(cuuint64_t)row_bytes, 128};
+    cuuint32_t box[3] = {128, 8, (cuuint32_t)cbs};
+    cuuint32_t estr[3] = {1, 1, 1};
+    r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    *is3d = 1;
+  } else {
+    cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+    cuuint32_t box[2] = {128, 8};
+    cuuint32_t estr[2] = {1, 1};
+    r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    *is3d = 0;
+  }
+  return r == CUDA_SUCCESS ? 0 : -1;
+}
+
 template <int EPI, int BN>
 static cudaError_t launch_tc(TcGemmParams& p, int num_sms, cudaStream_t s, bool pdl) {
   using C = Cfg<BN>;

@@ -73,6 +73,11 @@ int make_tmap_3d(CUtensorMap* map, const void* base, const int64_t* dims,
 // K % 64 == 0 (*is3d = 1), else the 2-D view (K, rows) with box (64, 8).
 int make_tmap_rows8(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int cbs,
                     int* is3d);
+// The same for a matrix of quantized codes viewed as bytes [rows, row_bytes]
+// (row_bytes a multiple of 16): 3-D (128, rows, row_bytes / 128) with box
+// (128, 8, cbs) when row_bytes % 128 == 0, else 2-D with box (128, 8).
+int make_tmap_codes(CUtensorMap* map, const void* base, int64_t rows, int64_t row_bytes,
+                    int cbs, int* is3d);
 
 cudaError_t launch_tc_gemm(TcGemmParams& p, int epi, int num_sms, cudaStream_t s,
                            bool pdl);

@@ -92,6 +92,13 @@ cudaError_t launch_embed(const __half* table, int64_t vocab, const int64_t* ids,
 cudaError_t configure_lm_head();
 
 // Sets the per-kernel shared-memory limits (called once per device).
+// Quantized weights formed as fp16: fmt 1 INT8 (q int8 [rows, K], scale
+// fp16 [rows]), fmt 2 int4 (packed uint8 [rows, K / 2], scale fp16 and zero
+// uint8 [rows, K / group]); w fp16 [rows, K].  K a multiple of 16.
+cudaError_t launch_dequant(int fmt, const void* q, const void* scale, const void* zero,
+                           int64_t rows, int64_t K, int group, __half* w, int num_sms,
+                           cudaStream_t s);
+
 cudaError_t configure_kernels();
 
 }  // namespace blk

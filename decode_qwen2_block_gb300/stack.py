@@ -13,8 +13,9 @@ import ctypes
 
 import torch
 
-from . import (BLK_ERR_SHAPE, BLK_OK, BlkError, Block, BlkWeights, blk_decode_batch_stack,
-               blk_decode_batch_stack_workspace_bytes, blk_decode_stack)
+from . import (BLK_ERR_SHAPE, BLK_OK, BlkError, Block, BlkQWeights, BlkWeights,
+               blk_decode_batch_stack, blk_decode_batch_stack_workspace_bytes, blk_decode_stack,
+               blk_decode_stack_q)
 
 
 class LayerStack:
@@ -138,3 +139,51 @@ class BatchStack:
         if rc != BLK_OK:
             raise BlkError(rc, "blk_decode_batch_stack")
         return out
+
+
+class QuantDecodeStack:
+    """Decode through a stack of blocks with weight-only quantized projections
+    (blk_decode_stack_q), one library call per step."""
+
+    def __init__(self, shape, qweights, max_ctx: int, caches=None, chain: bool = True,
+                 device="cuda"):
+        """qweights: list of BlkQWeights (one per layer; the tensors they
+        point to must stay alive).  caches: optional list of (k_cache,
+        v_cache) per layer, [Hkv, max_ctx, D]; zero-filled when None."""
+        self.shape = shape
+        self.n_layers = len(qweights)
+        self.block = Block(shape, max_ctx, chain=chain)
+        Hkv, D = shape.n_kv_heads, shape.head_dim
+        if caches is None:
+            caches = [(torch.zeros((Hkv, max_ctx, D), dtype=torch.float16, device=device),
+                       torch.zeros((Hkv, max_ctx, D), dtype=torch.float16, device=device))
+                      for _ in range(self.n_layers)]
+        self.caches = caches
+        self.ws = torch.empty(self.block.qworkspace_bytes(1), dtype=torch.uint8, device=device)
+        self.out = torch.empty((1, shape.hidden), dtype=torch.float16, device=device)
+        n = self.n_layers
+        self._w_arr = (BlkQWeights * n)(*qweights)
+        self._kc_arr = (ctypes.c_void_p * n)(*[kc.data_ptr() for kc, _ in caches])
+        self._vc_arr = (ctypes.c_void_p * n)(*[vc.data_ptr() for _, vc in caches])
+
+    def decode_step(self, x, pos, cache_len: int, out=None, stream=None):
+        out = self.out if out is None else out
+        s = torch.cuda.current_stream() if stream is None else stream
+        rc = blk_decode_stack_q(self.block.handle, self._w_arr, self.n_layers, self._kc_arr,
+                                self._vc_arr, x.data_ptr(), pos.data_ptr(), cache_len,
+                                out.data_ptr(), None, None, self.ws.data_ptr(), self.ws.numel(),
+                                s.cuda_stream)
+        if rc != BLK_OK:
+            raise BlkError(rc, "blk_decode_stack_q")
+        return out
+
+    def capture(self, x, pos, cache_len: int):
+        """One decode step captured into a CUDA graph (x, pos stay alive)."""
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                out = self.decode_step(x, pos, cache_len, stream=s)
+        torch.cuda.current_stream().wait_stream(s)
+        return g, out

@@ -331,6 +331,69 @@ int blk_lm_head(blk_handle h, const void* x, int64_t T, const void* norm_g, cons
                 int64_t vocab, float* logits, int64_t* tokens, void* ws, size_t ws_bytes,
                 void* stream);
 
+/* ---- weight-only quantized projections ------------------------------------
+ * The TpuOp dialect of "An MLIR-based LLM compilation method" (§2.2) carries
+ * INT8 and W4A16 weights with scales and zero points, and its lowering (§3.2)
+ * takes GPTQ / AWQ-style formats; activations stay fp16.  Here the seven
+ * matrices of a layer (wq, wk, wv, wo, w_gate, w_up, w_down; each [out, in])
+ * are quantized per output row:
+ *   BLK_WFMT_I8  w[o][i] = scale[o] * q[o][i]
+ *                q: int8 [out, in], scale: fp16 [out]
+ *   BLK_WFMT_U4  w[o][i] = scale[o][i / group] * (c(o, i) - zero[o][i / group])
+ *                c: 4-bit codes 0..15, two per byte along `in`, the even i in
+ *                the low nibble: uint8 [out, in / 2]; scale: fp16
+ *                [out, in / group]; zero: uint8 [out, in / group], 0..15
+ * Gains and q/k/v biases stay fp16, as in blk_weights.  The kernels form
+ * each weight as the fp16 product fp16(scale * (code - zero)) (exact code
+ * arithmetic, one rounding) and accumulate in fp32.
+ * Shape rules (BLK_ERR_SHAPE otherwise): INT8 needs hidden, n_heads*head_dim
+ * and intermediate multiples of 16; int4 needs them multiples of 32 and of
+ * `group`, a multiple of 16.  Decode also needs the scales of one
+ * projection phase to fit the kernel's staging area (about 5000 entries per
+ * SM: every shape here fits at group 128). */
+#define BLK_WFMT_F16 0
+#define BLK_WFMT_I8 1
+#define BLK_WFMT_U4 2
+typedef struct {
+  const void* q;      /* codes (device, 16-byte aligned)                      */
+  const void* scale;  /* fp16 scales (device, 2-byte aligned)                 */
+  const void* zero;   /* uint8 zero points (device), BLK_WFMT_U4 only         */
+} blk_qmatrix;
+typedef struct {
+  int32_t format;     /* BLK_WFMT_I8 or BLK_WFMT_U4                           */
+  int32_t group;      /* BLK_WFMT_U4: columns per scale and zero point        */
+  const void *ln1_g, *bq, *bk, *bv, *ln2_g;   /* fp16, as in blk_weights     */
+  blk_qmatrix wq, wk, wv, wo, w_gate, w_up, w_down;
+} blk_qweights;
+
+/* Workspace bytes enough for every quantized call with T <= max_T: decode
+ * needs blk_workspace_bytes(h, 1); prefill and prefill_kv also hold the
+ * layer's weights formed as fp16 (the first part of the workspace) before
+ * the fp16 tensor-core GEMMs run on them.  0 on a bad handle or max_T < 1. */
+size_t blk_qworkspace_bytes(blk_handle h, int64_t max_T);
+
+/* The three phases with quantized weights; arguments, caches, outputs and
+ * return codes as blk_prefill / blk_prefill_kv / blk_decode /
+ * blk_decode_stack, with the workspace sized by blk_qworkspace_bytes.
+ * Decode streams the codes themselves (the persistent kernel forms the
+ * weights in registers, so a step reads about half (INT8) or a quarter
+ * (int4) of the fp16 bytes); prefill and prefill_kv first write the layer's
+ * fp16 weights into the workspace (one extra kernel), then run as
+ * blk_prefill. */
+int blk_prefill_q(blk_handle h, const blk_qweights* w, const void* x, const int64_t* pos,
+                  int64_t T, void* k_cache, void* v_cache, void* out, void* k_new, void* v_new,
+                  void* ws, size_t ws_bytes, void* stream);
+int blk_prefill_kv_q(blk_handle h, const blk_qweights* w, const void* x, const int64_t* pos,
+                     int64_t T, int64_t cache_len, void* k_cache, void* v_cache, void* out,
+                     void* k_new, void* v_new, void* ws, size_t ws_bytes, void* stream);
+int blk_decode_q(blk_handle h, const blk_qweights* w, const void* x, const int64_t* pos,
+                 int64_t cache_len, void* k_cache, void* v_cache, void* out, void* k_new,
+                 void* v_new, void* ws, size_t ws_bytes, void* stream);
+int blk_decode_stack_q(blk_handle h, const blk_qweights* w, int n_layers,
+                       void* const* k_caches, void* const* v_caches, const void* x,
+                       const int64_t* pos, int64_t cache_len, void* out, void* const* k_new,
+                       void* const* v_new, void* ws, size_t ws_bytes, void* stream);
+
 /* Static description of a status code. */
 const char* blk_status_str(int status);
 

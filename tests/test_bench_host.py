@@ -114,3 +114,20 @@ def test_summary_is_last_and_compact():
     assert s["decode_us_frac"] == {"1024": [1129.123, 0.3461]}
     assert s["decode_e2e_tok_s"] == 800.5
     assert bench.compact(s)["prefill_tok_s"] == 1235000.0
+
+
+def test_quantized_decode_bytes_follow_the_formats():
+    """Per 1.5B layer: INT8 codes are half the fp16 matrix bytes plus one
+    fp16 scale per row; int4 codes a quarter plus an fp16 scale and a zero
+    byte per row and group of 128."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import synth
+    s = synth.QWEN2_1P5B
+    n_w = (2048 * 1536 + 1536 * 1536 + 2 * 8960 * 1536 + 1536 * 8960)
+    rows = 2048 + 1536 + 2 * 8960 + 1536
+    extra = 2 * 2 * 1536 + 2 * 2048           # gains, q/k/v biases
+    kv = 1024 * 1025
+    assert bench.quant_bytes(s, "i8", 0, 1024, 1) == n_w + 2 * rows + extra + kv
+    groups = (2048 + 1536 + 2 * 8960) * (1536 // 128) + 1536 * (8960 // 128)
+    assert bench.quant_bytes(s, "u4", 128, 1024, 1) == n_w // 2 + 3 * groups + extra + kv
