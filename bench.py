@@ -790,9 +790,9 @@ def device_qweights(s, fmt: str, group: int, layer: int, seed: int, dev):
     g = torch.Generator(device=dev)
     g.manual_seed(7919 * seed + layer)
     out = {}
-    for name, (N, K) in synth.weight_shapes(s).items():
-        if name not in synth.QUANT_MATRICES:
-            continue
+    shapes = synth.weight_shapes(s)
+    for name in synth.QUANT_MATRICES:
+        N, K = shapes[name]
         if fmt == "i8":
             q = torch.randint(-127, 128, (N, K), generator=g, device=dev, dtype=torch.int8)
             sc = (0.02 / 42 * (1 + 0.1 * torch.randn(N, generator=g, device=dev))).half()

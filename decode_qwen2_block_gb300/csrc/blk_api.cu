@@ -141,7 +141,8 @@ int check_qweights(const blk_config& c, const blk_qweights* w) {
   const int64_t Ks[3] = {c.hidden, (int64_t)c.n_heads * c.head_dim, c.intermediate};
   for (int64_t K : Ks) {
     if (K % (w->format == BLK_WFMT_I8 ? 16 : 32)) return BLK_ERR_SHAPE;
-    if (w->format == BLK_WFMT_U4 && (w->group < 16 || w->group % 16 || K % w->group))
+    if (w->format == BLK_WFMT_U4 &&
+        (w->group < 16 || (w->group & (w->group - 1)) || K % w->group))
       return BLK_ERR_SHAPE;
   }
   const blk_qmatrix* m[] = {&w->wq, &w->wk, &w->wv, &w->wo, &w->w_gate, &w->w_up, &w->w_down};
@@ -568,6 +569,8 @@ int decode_stack_impl(blk_handle h, const WT* w, int n_layers, void* const* k_ca
     p.trace_len = h->trace_len;
     p.fmt = fmt;
     p.qgroup = group;
+    p.qgroup_lg = 0;
+    while (group > 0 && (1 << p.qgroup_lg) < group) ++p.qgroup_lg;
     decode_ws_carve(p, ws, h->num_sms);
     for (int k = 0; k < nl; ++k) {
       const LayerSrc src = layer_src(w[l0 + k]);

@@ -56,17 +56,21 @@ constexpr int kThreads = kCT + 32;      // + one producer warp
 // Weight formats of the projections (the ABI's BLK_WFMT_* values).
 enum WFmt { kF16 = 0, kI8 = 1, kU4 = 2 };
 // Ring geometry per weight format.  A chunk is always 16 weight rows x kKc
-// columns: 48 KB of fp16, 24 KB of INT8 codes, 12 KB of packed int4 codes;
-// a K/V tile (64 slots of K and V) is 32 KB at D = 128.  Quantized formats
-// use five 32 KB stages and keep 16 KB for the phase's scales.
+// columns: 48 KB of fp16, 24 KB of INT8 codes, 12 KB of packed int4 codes.
+// With fp16 weights a K/V tile (64 slots of K and V, 32 KB at D = 128) is
+// one ring item; with quantized weights the stages are sized to the weight
+// chunk (at least the 16 KB of one half tile), a K/V tile is two items (K,
+// then V), and 16 KB stay for the phase's scales.  The ring then holds 7
+// (INT8) or 11 (int4) weight chunks instead of 4.
 template <int FMT> struct Ring {
-  static constexpr int kStages = FMT == kF16 ? 4 : 5;
-  static constexpr int kStageBytes = FMT == kF16 ? 48 * 1024 : 32 * 1024;
+  static constexpr int kStages = FMT == kF16 ? 4 : (FMT == kI8 ? 7 : 11);
+  static constexpr int kStageBytes = FMT == kF16 ? 48 * 1024 : (FMT == kI8 ? 24 : 16) * 1024;
+  static constexpr int kKvItems = FMT == kF16 ? 1 : 2;   // ring items per K/V tile
   static constexpr int kBoxCB = FMT == kF16 ? 24 : (FMT == kI8 ? 12 : 6);  // 128-byte blocks per box row
   static constexpr int kBoxBytes = 8 * 128 * kBoxCB;   // one 8-row box
   static constexpr int kQsBytes = FMT == kF16 ? 0 : 16 * 1024;
 };
-constexpr int kMaxStages = 5;
+constexpr int kMaxStages = 11;
 constexpr int kQsEntries = 5120;        // staged scales (and zero points) per phase
 constexpr int kAttnWarps = 4;           // 4 x 16 slots = one 64-slot tile
 constexpr int kSlots = 64;
@@ -78,6 +82,8 @@ constexpr int kPartFloats = 2048;       // [group][warp][16] partial sums
 constexpr int kQStride = 136;           // Q tile row stride in halves (padded)
 static_assert(2 * Ring<kF16>::kBoxBytes <= Ring<kF16>::kStageBytes, "stage too small");
 static_assert(2 * Ring<kI8>::kBoxBytes <= Ring<kI8>::kStageBytes, "stage too small");
+static_assert(2 * Ring<kU4>::kBoxBytes <= Ring<kU4>::kStageBytes, "stage too small");
+static_assert(64 * 128 * 2 <= Ring<kU4>::kStageBytes, "a K or V half tile fits a stage");
 static_assert(kBatch * kCW * 16 <= kPartFloats, "partials too small");
 
 constexpr int kResRows = 152;           // hidden rows per CTA (o_proj)
@@ -88,7 +94,7 @@ template <int FMT> struct Smem {
   static constexpr int kPartOff = kXsOff + kDecMaxVec * 2;
   static constexpr int kQOff = kPartOff;
   static constexpr int kBarOff = kPartOff + kPartFloats * 4;
-  static constexpr int kResOff = kBarOff + 256;
+  static constexpr int kResOff = kBarOff + 512;
   static constexpr int kQsOff = kResOff + kResRows * 4;
   static constexpr int kUsed = kQsOff + Ring<FMT>::kQsBytes;
   static constexpr int kBytes = kUsed + 1024;   // + alignment slack
@@ -570,23 +576,27 @@ __host__ __device__ __forceinline__ int qs_groups(int ph, int K, int group) {
   return ph == kPhDown ? (K < kKc ? K : kKc) / group : K / group;
 }
 
-// Stages this CTA's scales (and int4 zero points) of one projection phase
-// into shared memory, entry (gi * 16 + m) * GM + j for tile row m of work
-// group gi and scale group j; rows past the matrix get scale 0.  Every load
-// is issued before any store, so the staging costs one round trip.
+// Quantized weights: a CTA's scales (and int4 zero points) of one projection
+// phase, staged into shared memory as entry (gi * 16 + m) * GM + j for tile
+// row m of work group gi and scale group j; rows past the matrix get scale
+// 0.  qscale_load issues every load into registers before the phase's input
+// staging, so both cost one round trip; qscale_store writes them after it.
+constexpr int kQsPer = (kQsEntries + kCT - 1) / kCT;
+struct QsRegs {
+  uint16_t s[kQsPer];
+  uint8_t z[kQsPer];
+};
+
 template <int D, int FMT>
-__device__ void stage_qscales(const DecodeParams& p, int l, int ph, const PhaseWork& W,
-                              __half* qs_s, uint8_t* qs_z) {
+__device__ __forceinline__ void qscale_load(const DecodeParams& p, int l, int ph,
+                                            const PhaseWork& W, QsRegs& q) {
   const int GM = qs_groups<FMT>(ph, W.K, p.qgroup);
   const int total = W.ngroups * 16 * GM;   // <= kQsEntries, checked on the host
-  constexpr int kPer = (kQsEntries + kCT - 1) / kCT;
-  uint16_t sv[kPer];
-  uint32_t zv[kPer];
 #pragma unroll
-  for (int k = 0; k < kPer; ++k) {
+  for (int k = 0; k < kQsPer; ++k) {
     const int e = threadIdx.x + k * kCT;
-    sv[k] = 0;
-    zv[k] = 0;
+    q.s[k] = 0;
+    q.z[k] = 0;
     if (e < total) {
       const int j = e % GM, m = (e / GM) & 15, gi = e / (16 * GM);
       const GroupDesc g = group_desc<D>(p, ph, W, gi);
@@ -596,23 +606,29 @@ __device__ void stage_qscales(const DecodeParams& p, int l, int ph, const PhaseW
       role_shape(p, r, rows, K);
       if (y >= 0 && y < rows) {
         if (FMT == kI8) {
-          sv[k] = __ldg(p.qscale[l][r] + y);
+          q.s[k] = __ldg(p.qscale[l][r] + y);
         } else {
           const int ng = K / p.qgroup, jg = g.ka * kKc / p.qgroup + j;
           if (jg < ng) {
-            sv[k] = __ldg(p.qscale[l][r] + (size_t)y * ng + jg);
-            zv[k] = __ldg(p.qzero[l][r] + (size_t)y * ng + jg);
+            q.s[k] = __ldg(p.qscale[l][r] + (size_t)y * ng + jg);
+            q.z[k] = __ldg(p.qzero[l][r] + (size_t)y * ng + jg);
           }
         }
       }
     }
   }
+}
+
+template <int FMT>
+__device__ __forceinline__ void qscale_store(const DecodeParams& p, int ph, const PhaseWork& W,
+                                             const QsRegs& q, __half* qs_s, uint8_t* qs_z) {
+  const int total = W.ngroups * 16 * qs_groups<FMT>(ph, W.K, p.qgroup);
 #pragma unroll
-  for (int k = 0; k < kPer; ++k) {
+  for (int k = 0; k < kQsPer; ++k) {
     const int e = threadIdx.x + k * kCT;
     if (e < total) {
-      qs_s[e] = __ushort_as_half(sv[k]);
-      if (FMT == kU4) qs_z[e] = (uint8_t)zv[k];
+      qs_s[e] = __ushort_as_half(q.s[k]);
+      if (FMT == kU4) qs_z[e] = q.z[k];
     }
   }
   named_sync(1, kCT);
@@ -628,7 +644,8 @@ struct Cursor {
 
 // Settles on the first chunk at or after (l, ph); false past the last layer.
 template <int D>
-__device__ bool cursor_begin(Cursor& cu, const DecodeParams& p, const AttnRange& ar) {
+__device__ bool cursor_begin(Cursor& cu, const DecodeParams& p, const AttnRange& ar,
+                             int kv_items) {
   for (; cu.l < p.n_layers; ++cu.l, cu.ph = 0) {
     for (; cu.ph < kPhases; ++cu.ph) {
       if (cu.ph == kPhComb) continue;
@@ -649,9 +666,10 @@ __device__ bool cursor_begin(Cursor& cu, const DecodeParams& p, const AttnRange&
 }
 
 template <int D>
-__device__ bool cursor_next(Cursor& cu, const DecodeParams& p, const AttnRange& ar) {
+__device__ bool cursor_next(Cursor& cu, const DecodeParams& p, const AttnRange& ar,
+                            int kv_items) {
   if (cu.ph == kPhAttn) {
-    if (++cu.c < ar.chunks) return true;
+    if (++cu.c < ar.chunks * kv_items) return true;
   } else {
     if (++cu.kc < cu.g.kb) return true;
     if (++cu.gi < cu.W.ngroups) {
@@ -661,7 +679,7 @@ __device__ bool cursor_next(Cursor& cu, const DecodeParams& p, const AttnRange& 
     }
   }
   ++cu.ph;
-  return cursor_begin<D>(cu, p, ar);
+  return cursor_begin<D>(cu, p, ar, kv_items);
 }
 
 // Optional timeline: thread 0 of every CTA records %globaltimer when a phase
@@ -731,12 +749,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       return p.w3d[r] ? p.wbox_z[r] : min(RG::kBoxCB, p.wnz[r] - kc * RG::kBoxCB);
     };
     auto chunk_bytes = [&](const Cursor& cu) -> uint32_t {
-      if (cu.ph == kPhAttn) return 2u * kv_tile_bytes;
+      if (cu.ph == kPhAttn) return (uint32_t)(2 / RG::kKvItems) * kv_tile_bytes;
       const uint32_t nb = cu.g.yb >= 0 ? 2u : 1u;
       return nb * (uint32_t)(kBoxRows * 128) * (uint32_t)box_cbs(cu.g.ra, cu.kc);
     };
     auto kv_row = [&](const Cursor& cu) {
-      return (int)(ar.g * p.max_ctx + ar.j0 + (int64_t)cu.c * kSlots);
+      return (int)(ar.g * p.max_ctx + ar.j0 + (int64_t)(cu.c / RG::kKvItems) * kSlots);
     };
     // one 8-row box of role r at row y, column chunk kc: a single 3-D copy,
     // or (a row not a multiple of 128 bytes) one 2-D copy per 128-byte block
@@ -755,10 +773,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto load = [&](const Cursor& cu, uint8_t* st, uint64_t* bar) {
       if (cu.ph == kPhAttn) {
         const int y = kv_row(cu);
+        if (RG::kKvItems == 1) {
 #pragma unroll
-        for (int h = 0; h < D / 64; ++h) {
-          tma_load_2d(st + h * 8192, &p.tm_k[cu.l], h * 64, y, bar);
-          tma_load_2d(st + kv_tile_bytes + h * 8192, &p.tm_v[cu.l], h * 64, y, bar);
+          for (int h = 0; h < D / 64; ++h) {
+            tma_load_2d(st + h * 8192, &p.tm_k[cu.l], h * 64, y, bar);
+            tma_load_2d(st + kv_tile_bytes + h * 8192, &p.tm_v[cu.l], h * 64, y, bar);
+          }
+        } else {
+          const CUtensorMap* m = (cu.c & 1) ? &p.tm_v[cu.l] : &p.tm_k[cu.l];
+#pragma unroll
+          for (int h = 0; h < D / 64; ++h) tma_load_2d(st + h * 8192, m, h * 64, y, bar);
         }
         return;
       }
@@ -767,7 +791,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (cu.g.yb >= 0) copy_box(cu.l, cu.g.rb, cu.g.yb, cu.kc, dst + RG::kBoxBytes, mb);
     };
     Cursor rc = {0, 0, 0, 0, 0, {}, {}};
-    bool more = cursor_begin<D>(rc, p, ar);
+    bool more = cursor_begin<D>(rc, p, ar, RG::kKvItems);
     int it = 0;   // chunks issued to the ring
     bool ok = true;
     while (more && ok) {
@@ -801,7 +825,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive_expect_tx(&full[s], chunk_bytes(rc));
       load(rc, ring + (size_t)s * kStageBytes, &full[s]);
       ++it;
-      more = cursor_next<D>(rc, p, ar);
+      more = cursor_next<D>(rc, p, ar, RG::kKvItems);
     }
     // Copies still in flight must land before the CTA's shared memory goes away.
     for (int k = max(0, it - kStages); k < it; ++k)
@@ -813,10 +837,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Sync sync{p.barrier, p.err, abort_flag};
   int it = 0;          // ring position, in step with the producer
   int bar = 0;         // grid barriers passed
-  auto take = [&](int& s) -> bool {   // wait for the next ring stage
-    s = it % kStages;
+  auto take = [&](int& s, int ahead = 0) -> bool {   // wait for ring item it + ahead
+    const int k = it + ahead;
+    s = k % kStages;
     if (*abort_flag) return false;
-    if (!mbar_wait(&full[s], (it / kStages) & 1, p.err)) {
+    if (!mbar_wait(&full[s], (k / kStages) & 1, p.err)) {
       *abort_flag = 1;
       return false;
     }
@@ -878,12 +903,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const __half* kc_head = Ly.kc + (size_t)ar.g * p.max_ctx * D;
         const __half* vc_head = Ly.vc + (size_t)ar.g * p.max_ctx * D;
         for (int c = 0; c < ar.chunks; ++c) {
-          int s;
+          int s, sv = 0;   // the stages of the tile's K and V (one stage for fp16 weights)
           if (!take(s)) break;
+          if (RG::kKvItems == 2 && !take(sv, 1)) break;
           if (c == ar.chunks - 1 && tid == 0) *quiet = 1;
           if (warp < kAttnWarps) {
             uint8_t* st = ring + (size_t)s * kStageBytes;
-            const uint32_t kb = smem_u32(st), vb = kb + kv_tile_bytes;
+            uint8_t* vst = RG::kKvItems == 1 ? st + kv_tile_bytes : ring + (size_t)sv * kStageBytes;
+            const uint32_t kb = smem_u32(st), vb = smem_u32(vst);
             const int64_t cs = ar.j0 + (int64_t)c * kSlots;
             const int nval = (int)min((int64_t)kSlots, ar.j1 - cs);
             const int r0 = warp * 16;
@@ -907,7 +934,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (write) {
                   *reinterpret_cast<uint4*>(st + (tile_addr(kb, r, ch) - kb)) = kv_k;
-                  *reinterpret_cast<uint4*>(st + (tile_addr(vb, r, ch) - kb)) = kv_v;
+                  *reinterpret_cast<uint4*>(vst + (tile_addr(vb, r, ch) - vb)) = kv_v;
                 }
               }
               __syncwarp();
@@ -983,6 +1010,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           give(s);
+          if (RG::kKvItems == 2) give(sv);
         }
         // every consumer thread passes this barrier, also after an abort
         named_sync(1, kCT);
@@ -1115,6 +1143,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         QkvConst qc0{0.f, 0.f, make_float2(1.f, 0.f)};
         if (ph == kPhQKV && tid < min(W.ngroups, kBatch) * 16 && (tid & 15) < kBoxRows)
           qc0 = qkv_const(tid >> 4, tid & 15);
+        QsRegs qsr;
+        if constexpr (FMT != kF16) qscale_load<D, FMT>(p, l, ph, W, qsr);
         if (ph == kPhQKV) {
           const PhaseWork WO = phase_work<D>(p, kPhO);   // rows whose residual we keep
           stage_qkv(l == 0 ? p.x_in : nullptr, p.h32, p.pdown, p.nc_down, p.H, Ly.ln1, p.eps,
@@ -1126,7 +1156,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           stage_copy(ph == kPhO ? p.attn16 : p.act16, W.K, xs);
         }
-        if constexpr (FMT != kF16) stage_qscales<D, FMT>(p, l, ph, W, qs_s, qs_z);
+        if constexpr (FMT != kF16) qscale_store<FMT>(p, ph, W, qsr, qs_s, qs_z);
         if (tid == 0) *quiet = 0;
         // y = W x on the tensor cores: A = a chunk's 16 rows x 16 columns
         // (ldmatrix from the two swizzled boxes), B = x as the only non-zero
@@ -1172,19 +1202,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const __half* srow = qs_s + (gi * 16 + g8) * GM;
                 const uint8_t* zrow = qs_z + (gi * 16 + g8) * GM;
                 const int kbase = (kc - g.ka) * kKc;
+                // the scales (and zero points) change every `group` columns
+                int jc = -1;
+                __half2 sA = __half2half2(srow[0]), sB = __half2half2(srow[8 * GM]);
+                uint32_t zA = 0, zB = 0;
                 for (int ks = ks0; ks < ks1; ++ks) {
-                  const int j = FMT == kI8 ? 0 : (kbase + 16 * ks) / p.qgroup;
-                  const __half2 sA = __half2half2(srow[j]), sB = __half2half2(srow[8 * GM + j]);
                   uint32_t a[4];
                   if constexpr (FMT == kI8) {
                     const uint32_t off = (ks >> 3) * 1024 + (((ks & 7) ^ g8) << 4) + 4 * tg;
                     i8x4_scaled(lds_u32(sta + off), sA, a[0], a[2]);
                     i8x4_scaled(lds_u32(stb + off), sB, a[1], a[3]);
                   } else {
+                    const int j = (kbase + 16 * ks) >> p.qgroup_lg;
+                    if (j != jc) {
+                      jc = j;
+                      sA = __half2half2(srow[j]);
+                      sB = __half2half2(srow[8 * GM + j]);
+                      zA = zrow[j];
+                      zB = zrow[8 * GM + j];
+                    }
                     const uint32_t off =
                         (ks >> 4) * 1024 + ((((ks & 15) >> 1) ^ g8) << 4) + 8 * (ks & 1) + 2 * tg;
-                    u4x4_scaled(lds_u16(sta + off), zrow[j], sA, a[0], a[2]);
-                    u4x4_scaled(lds_u16(stb + off), zrow[8 * GM + j], sB, a[1], a[3]);
+                    u4x4_scaled(lds_u16(sta + off), zA, sA, a[0], a[2]);
+                    u4x4_scaled(lds_u16(stb + off), zB, sB, a[1], a[3]);
                   }
                   uint32_t x0 = 0u, x1 = 0u;
                   if (lane < 4) {

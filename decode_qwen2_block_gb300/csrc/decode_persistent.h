@@ -62,6 +62,7 @@ struct DecodeParams {
   // uint8 zero point per qgroup columns of a row (tm_w views the codes)
   int fmt;
   int qgroup;
+  int qgroup_lg;        // log2(qgroup): int4 groups are powers of two
   const uint16_t* qscale[kDecMaxLayers][kDecRoles];  // fp16 bits
   const uint8_t* qzero[kDecMaxLayers][kDecRoles];
 };

@@ -348,7 +348,7 @@ int blk_lm_head(blk_handle h, const void* x, int64_t T, const void* norm_g, cons
  * arithmetic, one rounding) and accumulate in fp32.
  * Shape rules (BLK_ERR_SHAPE otherwise): INT8 needs hidden, n_heads*head_dim
  * and intermediate multiples of 16; int4 needs them multiples of 32 and of
- * `group`, a multiple of 16.  Decode also needs the scales of one
+ * `group`, a power of two of at least 16.  Decode also needs the scales of one
  * projection phase to fit the kernel's staging area (about 5000 entries per
  * SM: every shape here fits at group 128). */
 #define BLK_WFMT_F16 0
