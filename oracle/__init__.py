@@ -29,7 +29,7 @@ class OrcConfig(ctypes.Structure):
                 ("n_kv_heads", ctypes.c_int64), ("head_dim", ctypes.c_int64),
                 ("intermediate", ctypes.c_int64), ("rms_eps", ctypes.c_double),
                 ("rope_theta", ctypes.c_double), ("max_ctx", ctypes.c_int64),
-                ("has_qkv_bias", ctypes.c_int64)]
+                ("has_qkv_bias", ctypes.c_int64), ("window", ctypes.c_int64)]
 
 
 class OrcWeights(ctypes.Structure):
@@ -160,7 +160,7 @@ def attend(q, K, V, scale: float) -> np.ndarray:
 # ---- the whole block --------------------------------------------------------
 
 def block_forward(shape, weights: dict, x, pos, L: int, k_cache, v_cache, max_ctx: int | None = None,
-                  rows=None, mats64: dict | None = None):
+                  rows=None, mats64: dict | None = None, window: int = 0):
     """Run the block for T = len(x) new tokens on top of L history slots.
 
     ``shape`` is a ``synth.BlockShape``.  ``k_cache``/``v_cache`` (fp16
@@ -168,7 +168,8 @@ def block_forward(shape, weights: dict, x, pos, L: int, k_cache, v_cache, max_ct
     ``out`` covers ``rows`` (all rows when None).  ``mats64``, if given, holds
     the seven matrices as f64 values (e.g. dequantized weights, see
     ``dequant_i8`` / ``dequant_u4``); ``weights`` then supplies only the gains
-    and biases."""
+    and biases.  ``window`` > 0: sliding-window attention over the last
+    ``window`` slots (the query's own slot included); 0 = full attention."""
     lib = _load()
     x = _u16(x)
     T = x.shape[0]
@@ -178,7 +179,7 @@ def block_forward(shape, weights: dict, x, pos, L: int, k_cache, v_cache, max_ct
         raise ValueError("caches must be C-contiguous")
     C = kc.shape[1] if max_ctx is None else max_ctx
     cfg = OrcConfig(shape.hidden, shape.n_heads, shape.n_kv_heads, shape.head_dim, shape.intermediate,
-                    shape.rms_eps, shape.rope_theta, C, 1 if shape.has_qkv_bias else 0)
+                    shape.rms_eps, shape.rope_theta, C, 1 if shape.has_qkv_bias else 0, int(window))
     keep = {}
     wts = OrcWeights()
     for name in WEIGHT_FIELDS:

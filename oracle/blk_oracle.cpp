@@ -165,7 +165,8 @@ int block_forward(const orc_config* cfg, const orc_weights* w, const M& wq, cons
                   const int64_t* rows, int64_t n_rows, uint16_t* out) {
   const int64_t H = cfg->hidden, Hq = cfg->n_heads, Hkv = cfg->n_kv_heads;
   const int64_t D = cfg->head_dim, I = cfg->intermediate, C = cfg->max_ctx;
-  if (T <= 0 || L < 0 || L + T > C || Hkv <= 0 || Hq % Hkv != 0 || D % 2 != 0)
+  if (T <= 0 || L < 0 || L + T > C || Hkv <= 0 || Hq % Hkv != 0 || D % 2 != 0 ||
+      cfg->window < 0)
     return -1;
   const int64_t group = Hq / Hkv;
   const bool bias = cfg->has_qkv_bias != 0;
@@ -200,7 +201,8 @@ int block_forward(const orc_config* cfg, const orc_weights* w, const M& wq, cons
   }
 
   // Step 2, each requested row: Q, RoPE on Q, attention over slots
-  // [0, L + t], o_proj + residual, RMSNorm, SwiGLU MLP + residual.
+  // [0, L + t] (or the window's part of them), o_proj + residual, RMSNorm,
+  // SwiGLU MLP + residual.
   const int64_t count = rows ? n_rows : T;
   std::vector<double> q(Hq * D), attn(Hq * D), h(H), hn(H), gate(I), up(I),
       act(I), mlp(H);
@@ -211,8 +213,11 @@ int block_forward(const orc_config* cfg, const orc_weights* w, const M& wq, cons
     for (int64_t hq = 0; hq < Hq; ++hq) {
       orc_rope(&q[hq * D], D, static_cast<double>(pos[t]), cfg->rope_theta);
       const int64_t g = hq / group;
-      orc_attend(&q[hq * D], &k_cache[g * C * D], &v_cache[g * C * D], L + t + 1,
-                 D, D, scale, &attn[hq * D]);
+      // slots [lo, L + t]: all of them, or the last `window` (sliding window)
+      const int64_t lo =
+          (cfg->window > 0 && L + t + 1 > cfg->window) ? L + t + 1 - cfg->window : 0;
+      orc_attend(&q[hq * D], &k_cache[(g * C + lo) * D], &v_cache[(g * C + lo) * D],
+                 L + t + 1 - lo, D, D, scale, &attn[hq * D]);
     }
     linear(wo, nullptr, attn.data(), H, Hq * D, h.data());
     for (int64_t i = 0; i < H; ++i) h[i] += h2d(x[t * H + i]);

@@ -45,6 +45,14 @@ typedef struct {
   double rms_eps, rope_theta;
   int64_t max_ctx;
   int64_t has_qkv_bias;
+  /* Sliding-window attention (the "swa" layer forward of the ds4.c study
+   * notes, Part 4, whose listing names the variant but states no window
+   * semantics): 0 = full causal attention; W > 0 = the query in slot p
+   * attends slots [max(0, p - W + 1), p], the last W slots including its
+   * own.  Pinned: W >= L + T equals full attention bit for bit; W = 1 gives
+   * each row the output of a lone token; slots outside the window are never
+   * read; a band-masked brute-force restatement agrees. */
+  int64_t window;
 } orc_config;
 
 /* Host pointers to fp16 bit patterns, weights [out, in] row-major. */

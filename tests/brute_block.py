@@ -28,8 +28,10 @@ def _rope(x, pos, theta):
     return x * cos + _rotate_half(x) * sin
 
 
-def block(shape, w, x16, pos, L, kc16, vc16):
-    """Returns (out fp16 [T,H], k_new fp16, v_new fp16); caches are not modified."""
+def block(shape, w, x16, pos, L, kc16, vc16, window=0):
+    """Returns (out fp16 [T,H], k_new fp16, v_new fp16); caches are not modified.
+    window > 0: row t sees only slots [L + t - window + 1, L + t] (a band of
+    the score matrix)."""
     H, Hq, Hkv, D = shape.hidden, shape.n_heads, shape.n_kv_heads, shape.head_dim
     f = lambda a: np.asarray(a, dtype=np.float64)
     x = f(x16)
@@ -53,7 +55,8 @@ def block(shape, w, x16, pos, L, kc16, vc16):
     S = np.einsum("thd,hjd->htj", q, K) / np.sqrt(D)                   # [Hq, T, L+T]
     mask = np.full((T, L + T), -np.inf)
     for t in range(T):
-        mask[t, : L + t + 1] = 0.0
+        lo = max(0, L + t + 1 - window) if window > 0 else 0
+        mask[t, lo: L + t + 1] = 0.0
     S = S + mask[None]
     P = np.exp(S - S.max(axis=-1, keepdims=True))
     P = P / P.sum(axis=-1, keepdims=True)

@@ -26,7 +26,9 @@ MUTATIONS = [
     ("gqa mapping", "const int64_t g = hq / group;", "const int64_t g = hq % Hkv;"),
     ("attention scale", "const double scale = 1.0 / std::sqrt(static_cast<double>(D));",
      "const double scale = 1.0 / static_cast<double>(D);"),
-    ("causal mask edge", "L + t + 1,\n                 D, D, scale", "L + t,\n                 D, D, scale"),
+    ("causal mask edge", "L + t + 1 - lo, D, D, scale", "L + t - lo, D, D, scale"),
+    ("window one slot too wide", "? L + t + 1 - cfg->window : 0;", "? L + t - cfg->window : 0;"),
+    ("window ignored", "(cfg->window > 0 && L + t + 1 > cfg->window)", "(false)"),
     ("dropped k bias", "linear(wk, bias ? w->bk : nullptr", "linear(wk, nullptr"),
     ("dropped rmsnorm eps", "std::sqrt(sum_sq / static_cast<double>(n) + eps)",
      "std::sqrt(sum_sq / static_cast<double>(n))"),

@@ -545,3 +545,61 @@ def test_block_with_dequantized_weights_matches_bruteforce(fmt):
     assert np.max(np.abs(vn.astype(np.float64) - bv.astype(np.float64))) <= 2.0 ** -10
     assert np.abs(out.astype(np.float64) - bo.astype(np.float64)).max() <= 2.0 ** -8
     assert np.mean(out.view(np.uint16) == bo.view(np.uint16)) > 0.99
+
+
+# ------------------------------------------------------------ sliding window
+# The ds4.c study notes name a sliding-window ("swa") layer forward without
+# stating its window; the reading pinned here: the query in slot p attends
+# the last W slots, [max(0, p - W + 1), p].
+
+@pytest.mark.parametrize("T,L", [(16, 0), (4, 16), (1, 30)])
+def test_window_covering_the_context_equals_full_attention(T, L):
+    s, w, x, pos, kc, vc = _tiny_case(T, L)
+    full = oracle.block_forward(s, w, x, pos, L, kc.copy(), vc.copy())
+    for W in (L + T, L + T + 5, 64):
+        win = oracle.block_forward(s, w, x, pos, L, kc.copy(), vc.copy(), window=W)
+        for a, b in zip(full, win):
+            assert np.array_equal(a.view(np.uint16), b.view(np.uint16))
+
+
+def test_window_of_one_gives_each_row_the_output_of_a_lone_token():
+    """With W = 1 a row attends only its own slot: softmax over one key is
+    1, so the attention output is the row's own V whatever q, the history or
+    the position; the block output equals a one-token prefill of that row."""
+    T, L = 6, 20
+    s, w, x, pos, kc, vc = _tiny_case(T, L)
+    out, kn, vn = oracle.block_forward(s, w, x, pos, L, kc, vc, window=1)
+    for t in range(T):
+        k1, v1 = synth.kv_history(s, 8, 0)
+        o1, _, _ = oracle.block_forward(s, w, x[t:t + 1], synth.positions(0, 1), 0, k1, v1)
+        assert np.array_equal(out[t:t + 1].view(np.uint16), o1.view(np.uint16))
+
+
+def test_slots_outside_the_window_are_never_read():
+    T, L, W = 5, 30, 12
+    s, w, x, pos, kc, vc = _tiny_case(T, L)
+    ref = oracle.block_forward(s, w, x, pos, L, kc.copy(), vc.copy(), window=W)
+    junk_k, junk_v = kc.copy(), vc.copy()
+    lo = L + 1 - W                      # the first row's first visible slot
+    rng = np.random.default_rng(5)
+    junk_k[:, :lo] = rng.normal(0, 50, junk_k[:, :lo].shape).astype(np.float16)
+    junk_v[:, :lo] = np.float16(np.nan)
+    got = oracle.block_forward(s, w, x, pos, L, junk_k, junk_v, window=W)
+    for a, b in zip(ref, got):
+        assert np.array_equal(a.view(np.uint16), b.view(np.uint16))
+    # and one slot more does change it: the window edge is where it says
+    junk_v[:, lo] = np.float16(3.0)
+    moved = oracle.block_forward(s, w, x, pos, L, kc.copy(), junk_v, window=W)
+    assert not np.array_equal(moved[0][0].view(np.uint16), ref[0][0].view(np.uint16))
+
+
+@pytest.mark.parametrize("T,L,W", [(16, 0, 5), (7, 9, 4), (4, 16, 10), (1, 25, 3)])
+def test_window_matches_band_masked_bruteforce(T, L, W):
+    s, w, x, pos, kc, vc = _tiny_case(T, L)
+    bo, bk, bv = brute_block(s, w, x, pos, L, kc.copy(), vc.copy(), window=W)
+    out, kn, vn = oracle.block_forward(s, w, x, pos, L, kc, vc, window=W)
+    d = np.abs(out.astype(np.float64) - bo.astype(np.float64))
+    assert d.max() <= 2.0 ** -8
+    assert np.mean(out.view(np.uint16) == bo.view(np.uint16)) > 0.99
+    full = oracle.block_forward(s, w, x, pos, L, kc.copy(), vc.copy())[0]
+    assert not np.array_equal(full.view(np.uint16), out.view(np.uint16))
