@@ -40,7 +40,7 @@ EXPORTED = ("blk_create", "blk_destroy", "blk_set_flags", "blk_workspace_bytes",
             "blk_decode_batch_workspace_bytes", "blk_decode_batch",
             "blk_decode_batch_stack_workspace_bytes", "blk_decode_batch_stack",
             "blk_wait_probe", "blk_qworkspace_bytes", "blk_prefill_q", "blk_prefill_kv_q",
-            "blk_decode_q", "blk_decode_stack_q")
+            "blk_decode_q", "blk_decode_stack_q", "blk_set_window")
 BLK_N_KERNELS = 16
 
 WEIGHT_FIELDS = ("ln1_g", "wq", "wk", "wv", "bq", "bk", "bv", "wo", "ln2_g", "w_gate", "w_up",
@@ -99,6 +99,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.blk_destroy.restype = None
     lib.blk_set_flags.argtypes = [vp, ctypes.c_uint32]
     lib.blk_set_flags.restype = i32
+    lib.blk_set_window.argtypes = [vp, i64]
+    lib.blk_set_window.restype = i32
     lib.blk_workspace_bytes.argtypes = [vp, i64]
     lib.blk_workspace_bytes.restype = ctypes.c_size_t
     lib.blk_prefill.argtypes = [vp, ctypes.POINTER(BlkWeights), vp, vp, i64, vp, vp, vp, vp, vp,
@@ -187,6 +189,10 @@ def blk_destroy(handle: int) -> None:
 
 def blk_set_flags(handle: int, flags: int) -> int:
     return load().blk_set_flags(handle, flags)
+
+
+def blk_set_window(handle: int, window: int) -> int:
+    return load().blk_set_window(handle, window)
 
 
 def blk_workspace_bytes(handle: int, max_T: int) -> int:
@@ -353,6 +359,12 @@ class Block:
 
     def set_chain(self, on: bool):
         blk_set_flags(self.handle, BLK_FLAG_CHAIN if on else 0)
+
+    def set_window(self, window: int):
+        """Sliding-window attention over the last `window` slots (0 = full)."""
+        rc = blk_set_window(self.handle, window)
+        if rc != BLK_OK:
+            raise BlkError(rc, "blk_set_window")
 
     def workspace_bytes(self, max_T: int) -> int:
         return blk_workspace_bytes(self.handle, max_T)

@@ -210,9 +210,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t L = p.cache_len;
   const int64_t n_keys = L + min(p.T, t0 + kRows);  // slots this block can see
   const int ntot = (int)((n_keys + kSlots - 1) / kSlots);
-  const int nch = (ntot + p.chunk_tiles - 1) / p.chunk_tiles;
+  // with a sliding window the block's first row sees slots from window_lo on
+  const int jlo = (int)(window_lo(p.window, L + t0) / kSlots);
+  const int nch = (ntot - jlo + p.chunk_tiles - 1) / p.chunk_tiles;
   if (ch >= nch) return;                         // (uniform over the CTA)
-  const int j0 = ch * p.chunk_tiles;             // first tile of this CTA
+  const int j0 = jlo + ch * p.chunk_tiles;       // first tile of this CTA
   const int nt = min(ntot, j0 + p.chunk_tiles) - j0;
 
   extern __shared__ uint8_t smem_raw[];
@@ -380,7 +382,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto wait_all = [&](uint64_t* bar, uint32_t parity) {
       return __all_sync(0xffffffffu, mbar_wait(bar, parity, p.err));
     };
-    for (int j = 0; j < nt; ++j) {
+    // With a sliding window the block's first tile can hold slots below
+    // every row's window: their P is 0, but 0 * NaN is NaN in the PV MMA, so
+    // a non-finite value left in such a slot is zeroed in shared memory
+    // before PV_0 is issued (it waits for this warp's arrive on p_full[0]).
+    if (p.window > 0 && ch == 0) {
+      const int64_t lo0 = window_lo(p.window, L + t0), js0 = (int64_t)j0 * kSlots;
+      if (lo0 > js0) {
+        if (!wait_all(&v_full[0], 0)) ok = false;
+        if (ok && js0 + r < lo0) {
+          uint8_t* vrow = sKV + Sm::kKVTile + (size_t)r * 128;
+#pragma unroll
+          for (int hh = 0; hh < D / 64; ++hh)
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              *reinterpret_cast<uint4*>(vrow + hh * (kSlots * 128) + c * 16) = make_uint4(0, 0, 0, 0);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      }
+    }
+    for (int j = 0; j < nt && ok; ++j) {
       if (!wait_all(s_full, j & 1)) { ok = false; break; }
       tc_fence_after();
       float sv[kSlots];
@@ -397,6 +418,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < kSlots; ++c)
           if (c > lim) sv[c] = -INFINITY;
+      }
+      if (p.window > 0) {                     // slots before the row's window
+        const int64_t d = window_lo(p.window, last) - js;
+        const int lim = d < 0 ? 0 : (d > kSlots ? kSlots : (int)d);
+#pragma unroll
+        for (int c = 0; c < kSlots; ++c)
+          if (c < lim) sv[c] = -INFINITY;
       }
       float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
 #pragma unroll
@@ -518,7 +546,8 @@ __global__ void __launch_bounds__(kRows * D / 32)
   const int t0 = qb * kRows;
   const int64_t n_keys = p.cache_len + min(p.T, t0 + kRows);
   const int ntot = (int)((n_keys + kSlots - 1) / kSlots);
-  const int nch = (ntot + p.chunk_tiles - 1) / p.chunk_tiles;
+  const int jlo = (int)(window_lo(p.window, p.cache_len + t0) / kSlots);
+  const int nch = (ntot - jlo + p.chunk_tiles - 1) / p.chunk_tiles;
   if (nch <= 1) return;                      // written by the attention kernel
   griddep_wait();
   griddep_launch();
@@ -601,9 +630,11 @@ void plan_prefill_attn(PrefillAttnParams& p, int num_sms) {
   const int64_t L = p.cache_len;
   p.nqb = (p.T + kRows - 1) / kRows;
   auto tiles = [&](int qb) {
-    return (int)((L + min(p.T, (qb + 1) * kRows) + kSlots - 1) / kSlots);
+    return (int)((L + min(p.T, (qb + 1) * kRows) + kSlots - 1) / kSlots) -
+           (int)(window_lo(p.window, L + qb * kRows) / kSlots);
   };
-  const int nmax = tiles(p.nqb - 1);
+  int nmax = 0;   // the most tiles any block sees (the last block without a window)
+  for (int qb = 0; qb < p.nqb; ++qb) nmax = max(nmax, tiles(qb));
   double best = 1e300;
   int best_c = nmax, prev = -1;
   for (int k = 1; k <= p.max_chunks; ++k) {

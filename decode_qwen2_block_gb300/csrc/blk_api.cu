@@ -39,6 +39,7 @@ struct blk_handle_s {
   int* status;    // device status word
   uint32_t flags;
   bool decode_ok;  // shape fits the persistent decode kernel
+  int64_t window;  // sliding-window attention in slots (0 = full), blk_set_window
   blk::DecodeParams* dec;  // parameter block of the decode launch
   uint64_t* trace;         // optional decode timeline buffer
   size_t trace_len;
@@ -344,6 +345,7 @@ int run_prefill(blk_handle h, const blk_weights* w, const void* x,
   pa.err = h->status;
   pa.max_ctx = c.max_ctx; pa.cache_len = L;
   pa.T = M; pa.Hq = Hq; pa.Hkv = Hkv; pa.D = D;
+  pa.window = h->window;
   pa.scale_log2 = (float)(1.4426950408889634 / sqrt((double)D));
   pa.attn16 = attn16;
   pa.max_chunks = prefill_attn_max_chunks(T, Hq, h->num_sms);
@@ -468,7 +470,11 @@ int run_decode_batch(blk_handle h, const blk_weights* w, const void* x, const in
   pa.B = M; pa.Hq = Hq; pa.Hkv = Hkv; pa.D = D;
   pa.max_ctx = c.max_ctx;
   pa.scale_log2 = (float)(1.4426950408889634 / sqrt((double)D));
-  pa.nsplit = decode_batch_splits(M, Hkv, max_cache_len, h->num_sms);
+  pa.window = h->window;
+  // with a window a sequence attends at most `window` slots
+  pa.nsplit = decode_batch_splits(
+      M, Hkv, h->window > 0 && h->window <= max_cache_len ? h->window - 1 : max_cache_len,
+      h->num_sms);
   pa.deep = decode_batch_deep(M, Hkv, h->num_sms) ? 1 : 0;
   pa.part = reinterpret_cast<float*>(base + lay.apart);
   pa.attn16 = attn16;
@@ -571,6 +577,7 @@ int decode_stack_impl(blk_handle h, const WT* w, int n_layers, void* const* k_ca
     p.qgroup = group;
     p.qgroup_lg = 0;
     while (group > 0 && (1 << p.qgroup_lg) < group) ++p.qgroup_lg;
+    p.window = h->window;
     decode_ws_carve(p, ws, h->num_sms);
     for (int k = 0; k < nl; ++k) {
       const LayerSrc src = layer_src(w[l0 + k]);
@@ -763,6 +770,13 @@ void blk_destroy(blk_handle h) {
 int blk_set_flags(blk_handle h, uint32_t flags) {
   if (!h) return BLK_ERR_NULL;
   h->flags = flags;
+  return BLK_OK;
+}
+
+int blk_set_window(blk_handle h, int64_t window) {
+  if (!h) return BLK_ERR_NULL;
+  if (window < 0) return BLK_ERR_SHAPE;
+  h->window = window;
   return BLK_OK;
 }
 

@@ -121,6 +121,13 @@ __device__ __forceinline__ void named_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// ---- sliding window ---------------------------------------------------------
+// First slot a query in slot `last` attends: with a sliding window of
+// `window` slots the last `window` slots (its own included), else slot 0.
+__host__ __device__ __forceinline__ int64_t window_lo(int64_t window, int64_t last) {
+  return (window > 0 && last + 1 > window) ? last + 1 - window : 0;
+}
+
 // ---- small math --------------------------------------------------------------
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll

@@ -123,7 +123,9 @@ __global__ void __launch_bounds__(128 * kTPG)
   const int G = p.Hq / p.Hkv;
   const int64_t L = p.cache_lens[b];
   const int64_t n = (L >= 0 && L < p.max_ctx) ? L + 1 : 0;   // slots [0, L]
-  const int64_t j0 = (int64_t)sp * n / p.nsplit, j1 = (int64_t)(sp + 1) * n / p.nsplit;
+  const int64_t lo = n > 0 ? window_lo(p.window, L) : 0;        // or the window's part
+  const int64_t j0 = lo + (int64_t)sp * (n - lo) / p.nsplit;
+  const int64_t j1 = lo + (int64_t)(sp + 1) * (n - lo) / p.nsplit;
   const int ntiles = (int)((j1 - j0 + kTileSlots - 1) / kTileSlots);
   const int ngroups = (ntiles + kTPG - 1) / kTPG;
   const int zh = b * p.Hkv + g;   // this (sequence, kv head) in the tensor maps

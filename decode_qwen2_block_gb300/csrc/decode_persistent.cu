@@ -318,8 +318,9 @@ __device__ __forceinline__ AttnRange attn_range(const DecodeParams& p) {
   a.g = b / p.S;
   a.s = b % p.S;
   const int64_t n = p.cache_len + 1;
-  a.j0 = a.active ? (int64_t)a.s * n / p.S : 0;
-  a.j1 = a.active ? (int64_t)(a.s + 1) * n / p.S : 0;
+  const int64_t lo = window_lo(p.window, p.cache_len);   // slots [lo, cache_len]
+  a.j0 = a.active ? lo + (int64_t)a.s * (n - lo) / p.S : 0;
+  a.j1 = a.active ? lo + (int64_t)(a.s + 1) * (n - lo) / p.S : 0;
   a.chunks = (int)((a.j1 - a.j0 + kSlots - 1) / kSlots);
   return a;
 }
@@ -1357,7 +1358,7 @@ void decode_ws_carve(DecodeParams& p, void* ws, int num_sms) {
   // One 64-slot tile per split while there are CTAs for it (more slots per
   // split beyond that); with at most 32 splits their partials are merged in
   // the o_proj staging instead of a separate phase.
-  const int64_t want = (p.cache_len + 1 + 63) / 64;
+  const int64_t want = (p.cache_len + 1 - window_lo(p.window, p.cache_len) + 63) / 64;
   p.S = (int)(want < 1 ? 1 : (want > (int64_t)S ? (int64_t)S : want));
   p.fold = p.S <= 32 ? 1 : 0;
 }

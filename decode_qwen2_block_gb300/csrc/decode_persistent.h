@@ -38,6 +38,7 @@ struct DecodeParams {
   float scale_log2;     // log2(e) / sqrt(D)
   int64_t max_ctx;
   int64_t cache_len;    // slot of the new token
+  int64_t window;       // sliding window in slots (0 = attend [0, cache_len])
   const int64_t* pos;   // [1]
   const float2* rope;
   int64_t rope_len;

@@ -27,6 +27,7 @@ struct PrefillAttnParams {
   int64_t max_ctx, cache_len;
   int T, Hq, Hkv, D;
   float scale_log2;   // log2(e) / sqrt(D)
+  int64_t window;     // sliding window in slots (0 = full causal attention)
   __half* attn16;  // [T, Hq * D]
   // Split of each 128-row block's tiles into chunks of chunk_tiles (one CTA
   // each; grid (Hq, nqb, grid_chunks)), set by plan_prefill_attn.  Blocks with
@@ -57,6 +58,7 @@ struct DecodeAttnBatchParams {
   int B, Hq, Hkv, D;
   int64_t max_ctx;
   float scale_log2;
+  int64_t window;             // sliding window in slots (0 = full)
   int nsplit;                 // splits of each sequence's slots (decode_batch_splits)
   int deep;                   // decode_batch_deep: one CTA per SM of 8 warps
   float* part;                // [B][Hq][nsplit][D + 2] when nsplit > 1

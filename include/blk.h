@@ -104,6 +104,15 @@ typedef struct blk_handle_s* blk_handle;
  * (programmatic dependent launch).  Off by default: the first kernel then
  * waits for all earlier stream work. */
 
+/* Sliding-window attention (the "swa" layer forward of the ds4.c study
+ * notes, Part 4, which names the variant without its window; the reading
+ * here is the plain one): with window W > 0 the query in cache slot p
+ * attends slots [max(0, p - W + 1), p], the last W slots including its own,
+ * in every phase and entry point of the handle; W = 0 (the default) is full
+ * causal attention.  Slots before a query's window are never read for its
+ * result.  Returns BLK_OK, BLK_ERR_NULL or BLK_ERR_SHAPE (W < 0). */
+int blk_set_window(blk_handle h, int64_t window);
+
 /* Creates a handle for `cfg` on the current CUDA device: validates the shape,
  * builds the fp32 cos/sin table [max_ctx][head_dim/2] (angles in f64) and a
  * status word.  Returns BLK_OK, BLK_ERR_NULL, BLK_ERR_SHAPE, BLK_ERR_DEVICE or
