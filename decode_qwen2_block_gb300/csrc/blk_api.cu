@@ -328,6 +328,8 @@ int run_prefill(blk_handle h, const blk_weights* w, const void* x,
   g.v_new = static_cast<__half*>(v_new);
   g.max_ctx = c.max_ctx; g.cache_len = L;
   g.err = h->status;
+  // (not split in K: a split QKV projection needs qkv_finish, which costs
+  // more than the split saves at T = 512, measured)
   BLK_LAUNCH(tm, kKGemmQKV, launch_tc_gemm(g, kTcQKV, h->num_sms, s, true));
 
   // causal GQA attention over [history; new rows]
@@ -354,8 +356,10 @@ int run_prefill(blk_handle h, const blk_weights* w, const void* x,
   BLK_LAUNCH(tm, kKAttnPrefill, launch_prefill_attn(pa, s, true));
   if (pa.grid_chunks > 1) BLK_LAUNCH(tm, kKAttnMerge, launch_attn_merge(pa, s, true));
 
+  // o_proj splits K the same way when its tiles are few; the RMSNorm that
+  // follows it adds the partials and the residual
   return run_block_tail(h, w, x, attn16, h32, hn16, act16,
-                        reinterpret_cast<float*>(base + lay.part32), kMaxSplits, false, out, M,
+                        reinterpret_cast<float*>(base + lay.part32), kMaxSplits, true, out, M,
                         s, tm);
 }
 
