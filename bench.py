@@ -67,7 +67,8 @@ NCU_TRAFFIC = {
     "gemm_o": 11042560 + 0,
     "attn_prefill": 4243712 + 0,
     "lm_head": 466853632 + 206080,
-    ("decode_persistent", 4096): None,
+    # one-layer capture scaled to the 28-layer step (traffic grows with the layers)
+    ("decode_persistent", 4096): 28 * (101665280 + 4095488),
 }
 
 
