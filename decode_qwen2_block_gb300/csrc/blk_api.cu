@@ -22,13 +22,13 @@ constexpr int kMaxPending = 1024;
 enum KernelId {
   kKRmsNorm = 0, kKGemmQKV, kKSplitReduce, kKAttnPrefill, kKGemmO, kKGemmGateUp,
   kKGemmDown, kKDecodeStep, kKAttnMerge, kKLmHead, kKArgmax, kKEmbed, kKDecodeAttnBatch,
-  kKQkvFinish, kKDequant, kKCount
+  kKQkvFinish, kKDequant, kKReduceNorm, kKCount
 };
 static_assert(kKCount <= BLK_N_KERNELS, "kernel id table");
 const char* const kKernelNames[BLK_N_KERNELS] = {
     "rmsnorm_rows", "gemm_qkv", "splitk_reduce", "attn_prefill", "gemm_o",
     "gemm_gateup", "gemm_down", "decode_persistent", "attn_merge", "lm_head", "argmax_reduce",
-    "embed", "decode_attn_batch", "qkv_finish", "dequant_weights", ""};
+    "embed", "decode_attn_batch", "qkv_finish", "dequant_weights", "splitk_reduce_norm"};
 }  // namespace
 
 struct blk_handle_s {
@@ -220,10 +220,14 @@ struct Timer {
   } while (0)
 
 // o_proj + residual, RMSNorm 2, gate|up + SwiGLU, down + residual for M rows
-// (shared by prefill, prefill_kv and batched decode).
+// (shared by prefill, prefill_kv and batched decode).  With next_g set (a
+// layer stack), the next layer's RMSNorm 1 of out (gain next_g) is also
+// written to next_xn16, fused with the down split-K reduction when there is
+// one.
 int run_block_tail(blk_handle h, const blk_weights* w, const void* x, __half* attn16,
                    float* h32, __half* hn16, __half* act16, float* part32, int max_splits,
-                   bool split_o, void* out, int M, cudaStream_t s, Timer& tm) {
+                   bool split_o, void* out, int M, cudaStream_t s, Timer& tm,
+                   const __half* next_g = nullptr, __half* next_xn16 = nullptr) {
   const blk_config& c = h->cfg;
   const int H = c.hidden, D = c.head_dim, Hq = c.n_heads, I = c.intermediate;
   // o_proj + residual -> h (fp32)
@@ -273,8 +277,15 @@ int run_block_tail(blk_handle h, const blk_weights* w, const void* x, __half* at
   gd.max_splits = max_splits;
   gd.err = h->status;
   BLK_LAUNCH(tm, kKGemmDown, launch_tc_gemm(gd, kTcResidOutF16, h->num_sms, s, true));
-  if (gd.splits > 1)
+  if (next_g && gd.splits > 1)
+    BLK_LAUNCH(tm, kKReduceNorm,
+               launch_splitk_reduce_norm(part32, gd.splits, h32, gd.out16, next_g, M, H,
+                                         c.rms_eps, next_xn16, s));
+  else if (gd.splits > 1)
     BLK_LAUNCH(tm, kKSplitReduce, launch_splitk_reduce(gd, h->num_sms, s));
+  else if (next_g)
+    BLK_LAUNCH(tm, kKRmsNorm,
+               launch_rmsnorm_rows(out, false, next_g, M, H, c.rms_eps, next_xn16, s, true));
   return BLK_OK;
 }
 
@@ -408,10 +419,15 @@ int check_decode_batch(blk_handle h, const blk_weights* w, const void* x, const 
   return BLK_OK;
 }
 
+// One batched-decode layer.  In a layer stack, x_normed says that the
+// workspace's xn16 already holds RMSNorm 1 of x (written by the previous
+// layer's tail) and next_ln1, when set, has this layer's tail write the next
+// layer's RMSNorm 1 there.
 int run_decode_batch(blk_handle h, const blk_weights* w, const void* x, const int64_t* pos,
                      const int64_t* cache_lens, int64_t B, int64_t max_cache_len, void* k_cache,
                      void* v_cache, void* out, void* k_new, void* v_new, void* ws,
-                     size_t ws_bytes, void* stream) {
+                     size_t ws_bytes, void* stream, bool x_normed = false,
+                     const __half* next_ln1 = nullptr) {
   int rc = check_decode_batch(h, w, x, pos, cache_lens, B, max_cache_len, k_cache, v_cache, out,
                               k_new, v_new, ws, ws_bytes);
   if (rc) return rc;
@@ -426,9 +442,10 @@ int run_decode_batch(blk_handle h, const blk_weights* w, const void* x, const in
   const bool first_pdl = (h->flags & BLK_FLAG_CHAIN) != 0;
   Timer tm{h, s};
 
-  BLK_LAUNCH(tm, kKRmsNorm,
-             launch_rmsnorm_rows(x, false, static_cast<const __half*>(w->ln1_g), M, H,
-                                 c.rms_eps, xn16, s, first_pdl));
+  if (!x_normed)
+    BLK_LAUNCH(tm, kKRmsNorm,
+               launch_rmsnorm_rows(x, false, static_cast<const __half*>(w->ln1_g), M, H,
+                                   c.rms_eps, xn16, s, first_pdl));
 
   // QKV + bias + RoPE at pos[b]; K/V to slot cache_lens[b] of sequence b's cache
   TcGemmParams g = {};
@@ -489,7 +506,7 @@ int run_decode_batch(blk_handle h, const blk_weights* w, const void* x, const in
                         reinterpret_cast<__half*>(base + lay.hn16),
                         reinterpret_cast<__half*>(base + lay.act16),
                         reinterpret_cast<float*>(base + lay.part32), kMaxSplitsBatch, true, out,
-                        M, s, tm);
+                        M, s, tm, next_ln1, xn16);
 }
 
 }  // namespace
@@ -1028,9 +1045,12 @@ int blk_decode_batch_stack(blk_handle h, const blk_weights* w, int n_layers,
     if (rc) return rc;
   }
   for (int l = 0; l < n_layers; ++l) {
+    // layer l's tail writes layer l + 1's RMSNorm 1 (one launch fewer a layer)
+    const __half* next_ln1 =
+        l + 1 < n_layers ? static_cast<const __half*>(w[l + 1].ln1_g) : nullptr;
     const int rc = run_decode_batch(h, &w[l], layer_in(l), pos, cache_lens, B, max_cache_len,
                                     k_caches[l], v_caches[l], layer_out(l), nullptr, nullptr, ws,
-                                    layer_ws, stream);
+                                    layer_ws, stream, l > 0, next_ln1);
     if (rc) return rc;
   }
   return BLK_OK;

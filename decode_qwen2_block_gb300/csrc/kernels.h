@@ -15,6 +15,13 @@ cudaError_t launch_rmsnorm_rows(const void* x, bool x_is_f32, const __half* g,
                                 cudaStream_t s, bool pdl);
 // h32 = sum_s part[s] (s ascending) + res16, y = RMSNorm(h32) * g (rows of
 // width H, part = S <= 8 partials [rows][H] fp32).
+// Down split-K reduction fused with the next layer's RMSNorm (layer stacks):
+// out16 = fp16(sum of S partials [S][rows][H] + res32) and y = RMSNorm(out16)
+// * g, bit-identical to launch_splitk_reduce followed by launch_rmsnorm_rows
+// on out16.  S <= 16, H a multiple of 8.
+cudaError_t launch_splitk_reduce_norm(const float* part, int S, const float* res32,
+                                      __half* out16, const __half* g, int rows, int H, float eps,
+                                      __half* y, cudaStream_t s);
 cudaError_t launch_rmsnorm_splitk(const float* part, int S, const __half* res16, float* h32,
                                   const __half* g, int rows, int H, float eps, __half* y,
                                   cudaStream_t s, bool pdl);

@@ -147,6 +147,73 @@ __global__ void __launch_bounds__(1024)
   }
 }
 
+// After a K-split down projection inside a layer stack: the layer's output
+// out16 = fp16(sum of the split partials, split order, + res32) -- the
+// values splitk_reduce_kernel writes -- and the next layer's RMSNorm of that
+// output, y = fp16(out * rsqrt(mean(out^2) + eps) * g), in one launch.  One
+// CTA per row; each thread owns 8-column vectors i = t, t + blockDim, ...
+// The squares are added exactly as rmsnorm_rows_kernel adds them for a
+// one-warp row (per vector in column order; lane l then adds the vectors l,
+// l + 32, ... in that order; then the warp's butterfly), so y has the same
+// bits as a separate reduction followed by rmsnorm_rows.
+constexpr int kReduceNormMaxS = 16;
+constexpr int kReduceNormThreads = 256;
+
+__global__ void __launch_bounds__(kReduceNormThreads)
+    splitk_reduce_norm_kernel(const float* __restrict__ part, int S,
+                              const float* __restrict__ res32, __half* __restrict__ out16,
+                              const __half* __restrict__ g, int rows, int H, float eps,
+                              __half* __restrict__ y) {
+  extern __shared__ float vec_ss[];   // [H / 8] per-vector sums of squares
+  __shared__ float r_row;
+  griddep_wait();
+  griddep_launch();
+  const int row = blockIdx.x;
+  const int nv = H / 8;
+  const size_t MN = (size_t)rows * H, r0 = (size_t)row * H;
+  uint4 first = make_uint4(0, 0, 0, 0);
+  for (int i = threadIdx.x; i < nv; i += blockDim.x) {
+    const size_t c = r0 + (size_t)i * 8;
+    float4 q[kReduceNormMaxS][2];
+#pragma unroll
+    for (int j = 0; j < kReduceNormMaxS; ++j)
+      if (j < S) {
+        q[j][0] = __ldcg(reinterpret_cast<const float4*>(part + j * MN + c));
+        q[j][1] = __ldcg(reinterpret_cast<const float4*>(part + j * MN + c) + 1);
+      }
+    const float4 ra = __ldcg(reinterpret_cast<const float4*>(res32 + c));
+    const float4 rb = __ldcg(reinterpret_cast<const float4*>(res32 + c) + 1);
+    float4 a = q[0][0], b = q[0][1];
+#pragma unroll
+    for (int j = 1; j < kReduceNormMaxS; ++j)
+      if (j < S) {
+        a.x += q[j][0].x; a.y += q[j][0].y; a.z += q[j][0].z; a.w += q[j][0].w;
+        b.x += q[j][1].x; b.y += q[j][1].y; b.z += q[j][1].z; b.w += q[j][1].w;
+      }
+    uint4 o;
+    *reinterpret_cast<__half2*>(&o.x) = __floats2half2_rn(a.x + ra.x, a.y + ra.y);
+    *reinterpret_cast<__half2*>(&o.y) = __floats2half2_rn(a.z + ra.z, a.w + ra.w);
+    *reinterpret_cast<__half2*>(&o.z) = __floats2half2_rn(b.x + rb.x, b.y + rb.y);
+    *reinterpret_cast<__half2*>(&o.w) = __floats2half2_rn(b.z + rb.z, b.w + rb.w);
+    reinterpret_cast<uint4*>(out16 + r0)[i] = o;
+    vec_ss[i] = sumsq16<__half>(o);
+    if (i == threadIdx.x) first = o;
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float ss = 0.f;
+    for (int i = threadIdx.x; i < nv; i += 32) ss += vec_ss[i];
+    ss = warp_sum(ss);
+    if (threadIdx.x == 0) r_row = rsqrtf(ss / (float)H + eps);
+  }
+  __syncthreads();
+  const float r = r_row;
+  __half* yr = y + r0;
+  for (int i = threadIdx.x; i < nv; i += blockDim.x)   // this thread's own output vectors
+    put16<__half>(i == threadIdx.x ? first : reinterpret_cast<const uint4*>(out16 + r0)[i], i,
+                  r, g, yr);
+}
+
 static cudaLaunchConfig_t make_cfg(dim3 grid, dim3 block, size_t smem,
                                    cudaStream_t s, bool pdl,
                                    cudaLaunchAttribute* attr) {
@@ -185,6 +252,19 @@ cudaError_t launch_rmsnorm_splitk(const float* part, int S, const __half* res16,
   cudaLaunchConfig_t cfg = make_cfg(dim3(rows), dim3(threads), 0, s, pdl, attr);
   return cudaLaunchKernelEx(&cfg, rmsnorm_splitk_kernel, part, S, res16, h32, g, rows, H, eps,
                             y);
+}
+
+cudaError_t launch_splitk_reduce_norm(const float* part, int S, const float* res32,
+                                      __half* out16, const __half* g, int rows, int H, float eps,
+                                      __half* y, cudaStream_t s) {
+  if (S < 1 || S > kReduceNormMaxS || H % 8) return cudaErrorInvalidValue;
+  int threads = (H / 8 + 31) / 32 * 32;
+  if (threads > kReduceNormThreads) threads = kReduceNormThreads;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = make_cfg(dim3(rows), dim3(threads), (size_t)(H / 8) * sizeof(float),
+                                    s, true, attr);
+  return cudaLaunchKernelEx(&cfg, splitk_reduce_norm_kernel, part, S, res32, out16, g, rows, H,
+                            eps, y);
 }
 
 }  // namespace blk

@@ -173,19 +173,36 @@ def _stack_inputs(s, n_layers, B, C, seed):
     return wl, lens, caches, x
 
 
-def test_batch_stack_equals_one_call_per_layer():
-    """blk_decode_batch_stack over 3 layers = blk_decode_batch per layer, bit
-    for bit (outputs and every cache)."""
+@pytest.mark.parametrize("shape_name,n,B,C,fused", [
+    ("TINY", 3, 5, 64, False),          # down K too short to split: plain RMSNorm
+    ("QWEN2_1P5B", 2, 3, 64, True),     # down split K: reduction fused with RMSNorm 1
+    ("QWEN2_1P5B", 3, 64, 704, True),   # the bench's batch size
+])
+def test_batch_stack_equals_one_call_per_layer(shape_name, n, B, C, fused):
+    """blk_decode_batch_stack = blk_decode_batch per layer, bit for bit
+    (outputs and every cache).  The stack writes layer l + 1's RMSNorm 1 from
+    layer l's tail (fused with the down split-K reduction when the down
+    projection splits K), so its launches differ from the per-layer calls'
+    while the bits must not."""
     from decode_qwen2_block_gb300.stack import BatchStack
-    s, n, B, C = synth.TINY, 3, 5, 64
+    s = getattr(synth, shape_name)
     wl, lens, caches, x = _stack_inputs(s, n, B, C, seed=15)
     wd = [{k: to_dev(v) for k, v in w.items()} for w in wl]
     lens_d = to_dev(np.array(lens, dtype=np.int64))
     st = BatchStack(s, wd, C, B, caches=[(to_dev(k), to_dev(v)) for k, v in caches])
     out = torch.empty((B, s.hidden), dtype=torch.float16, device="cuda")
+    st.block.timing(True)
     st.step(to_dev(x), lens_d, lens_d, max(lens), out)
+    st.block.timing_collect()
+    st.block.timing(False)
     torch.cuda.synchronize()
     st.block.check()
+    launched = {k: c for k, (_, c) in st.block.timing_table().items()}
+    if fused:
+        assert launched.get("splitk_reduce_norm") == n - 1
+        assert launched.get("splitk_reduce") == 1           # the last layer's
+    else:
+        assert "splitk_reduce_norm" not in launched
     block = blk.Block(s, C)
     ws = torch.empty(block.decode_batch_workspace_bytes(B), dtype=torch.uint8, device="cuda")
     cur = to_dev(x)
