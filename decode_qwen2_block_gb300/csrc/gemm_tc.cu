@@ -685,7 +685,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // out16[m, n] = fp16(sum_j part[j][m, n] + res32[m, n]), splits added in
-// order; four columns per thread.
+// order; four columns per element, two elements (a grid stride apart) per
+// thread with every load of both issued before any add.  MAXS (>= S) sizes
+// the register arrays: 4 for the usual 2-4 splits keeps a thread near 40
+// registers, so that a whole grid is resident at once.
+template <int MAXS>
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restrict__ part,
                                                             int S, int64_t MN,
                                                             const float* __restrict__ res32,
@@ -693,24 +697,31 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restr
   griddep_wait();
   griddep_launch();
   const int64_t n4 = MN / 4;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const float4 r = __ldg(reinterpret_cast<const float4*>(res32) + i);
-    // every split loaded before any is added (one round trip), then added
-    // in ascending order
-    constexpr int kMaxS = 16;
-    float4 q[kMaxS];
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i0 < n4; i0 += 2 * stride) {
+    float4 r[2], q[2][MAXS];
 #pragma unroll
-    for (int j = 0; j < kMaxS; ++j)
-      if (j < S) q[j] = __ldcg(reinterpret_cast<const float4*>(part + (size_t)j * MN) + i);
-    float4 a = q[0];
+    for (int e = 0; e < 2; ++e) {
+      const int64_t i = i0 + e * stride;
+      if (i >= n4) break;
+      r[e] = __ldg(reinterpret_cast<const float4*>(res32) + i);
 #pragma unroll
-    for (int j = 1; j < kMaxS; ++j)
-      if (j < S) { a.x += q[j].x; a.y += q[j].y; a.z += q[j].z; a.w += q[j].w; }
-    uint2 o;
-    *reinterpret_cast<__half2*>(&o.x) = __floats2half2_rn(a.x + r.x, a.y + r.y);
-    *reinterpret_cast<__half2*>(&o.y) = __floats2half2_rn(a.z + r.z, a.w + r.w);
-    reinterpret_cast<uint2*>(out16)[i] = o;
+      for (int j = 0; j < MAXS; ++j)
+        if (j < S) q[e][j] = __ldcg(reinterpret_cast<const float4*>(part + (size_t)j * MN) + i);
+    }
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int64_t i = i0 + e * stride;
+      if (i >= n4) break;
+      float4 a = q[e][0];   // splits added in ascending order, then the residual
+#pragma unroll
+      for (int j = 1; j < MAXS; ++j)
+        if (j < S) { a.x += q[e][j].x; a.y += q[e][j].y; a.z += q[e][j].z; a.w += q[e][j].w; }
+      uint2 o;
+      *reinterpret_cast<__half2*>(&o.x) = __floats2half2_rn(a.x + r[e].x, a.y + r[e].y);
+      *reinterpret_cast<__half2*>(&o.y) = __floats2half2_rn(a.z + r[e].z, a.w + r[e].w);
+      reinterpret_cast<uint2*>(out16)[i] = o;
+    }
   }
 }
 
@@ -718,6 +729,7 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restr
 // fused q | k | v output is the sum of the split partials (split order) plus
 // the bias, rotated by RoPE for q and k heads, then stored exactly as the
 // GEMM's own QKV epilogue does (q16; K/V into the cache slot and k_new/v_new).
+template <int MAXS>
 __global__ void __launch_bounds__(64) qkv_finish_kernel(const __grid_constant__ TcGemmParams p) {
   griddep_wait();
   griddep_launch();
@@ -736,17 +748,16 @@ __global__ void __launch_bounds__(64) qkv_finish_kernel(const __grid_constant__ 
   for (int i = threadIdx.x; i < half; i += blockDim.x) {
     const size_t c0 = (size_t)m * p.N + (size_t)hd * D + i, c1 = c0 + half;
     // every split's pair is loaded before any is added (one round trip)
-    constexpr int kMaxS = 16;
-    float qa[kMaxS], qb[kMaxS];
+    float qa[MAXS], qb[MAXS];
 #pragma unroll
-    for (int s = 0; s < kMaxS; ++s)
+    for (int s = 0; s < MAXS; ++s)
       if (s < p.splits) {
         qa[s] = __ldcg(p.part + s * MN + c0);
         qb[s] = __ldcg(p.part + s * MN + c1);
       }
     float a = 0.f, b = 0.f;
 #pragma unroll
-    for (int s = 0; s < kMaxS; ++s)
+    for (int s = 0; s < MAXS; ++s)
       if (s < p.splits) {
         a += qa[s];
         b += qb[s];
@@ -799,8 +810,21 @@ cudaError_t launch_splitk_reduce(const TcGemmParams& p, int num_sms, cudaStream_
   if (p.splits < 1 || p.splits > 16) return cudaErrorInvalidValue;
   const int64_t MN = (int64_t)p.M * p.N;
   const int64_t n4 = MN / 4;
-  int grid = (int)((n4 + 255) / 256);
-  if (grid > 8 * num_sms) grid = 8 * num_sms;
+  const int maxs = p.splits <= 4 ? 4 : (p.splits <= 8 ? 8 : 16);
+  // two elements per thread; no more blocks than are resident at once
+  static int resident[3] = {0, 0, 0};
+  int& res = resident[maxs == 4 ? 0 : (maxs == 8 ? 1 : 2)];
+  if (res == 0) {
+    int nb = 0;
+    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &nb,
+        maxs == 4 ? splitk_reduce_kernel<4> : (maxs == 8 ? splitk_reduce_kernel<8>
+                                                         : splitk_reduce_kernel<16>),
+        256, 0);
+    res = (e == cudaSuccess && nb > 0 ? nb : 1) * num_sms;
+  }
+  int grid = (int)((n4 + 511) / 512);
+  if (grid > res) grid = res;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid < 1 ? 1 : grid);
   cfg.blockDim = dim3(256);
@@ -810,8 +834,12 @@ cudaError_t launch_splitk_reduce(const TcGemmParams& p, int num_sms, cudaStream_
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, (const float*)p.part, p.splits, MN,
-                            p.res32, p.out16);
+  const float* part = p.part;
+  if (maxs == 4)
+    return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<4>, part, p.splits, MN, p.res32, p.out16);
+  if (maxs == 8)
+    return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<8>, part, p.splits, MN, p.res32, p.out16);
+  return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<16>, part, p.splits, MN, p.res32, p.out16);
 }
 
 cudaError_t launch_qkv_finish(const TcGemmParams& p, cudaStream_t s) {
@@ -825,7 +853,9 @@ cudaError_t launch_qkv_finish(const TcGemmParams& p, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, qkv_finish_kernel, p);
+  if (p.splits <= 4) return cudaLaunchKernelEx(&cfg, qkv_finish_kernel<4>, p);
+  if (p.splits <= 8) return cudaLaunchKernelEx(&cfg, qkv_finish_kernel<8>, p);
+  return cudaLaunchKernelEx(&cfg, qkv_finish_kernel<16>, p);
 }
 
 // cuTensorMapEncodeTiled, resolved through the runtime so that the library
