@@ -24,12 +24,22 @@ WEIGHT_FIELDS = ("ln1_g", "wq", "wk", "wv", "bq", "bk", "bv", "wo", "ln2_g",
                  "w_gate", "w_up", "w_down")
 
 
+class OrcYarn(ctypes.Structure):
+    _fields_ = [("freq_scale", ctypes.c_double), ("ext_factor", ctypes.c_double),
+                ("attn_factor", ctypes.c_double), ("beta_fast", ctypes.c_double),
+                ("beta_slow", ctypes.c_double), ("n_ctx_orig", ctypes.c_int64)]
+
+
+YARN_FIELDS = ("freq_scale", "ext_factor", "attn_factor", "beta_fast", "beta_slow", "n_ctx_orig")
+
+
 class OrcConfig(ctypes.Structure):
     _fields_ = [("hidden", ctypes.c_int64), ("n_heads", ctypes.c_int64),
                 ("n_kv_heads", ctypes.c_int64), ("head_dim", ctypes.c_int64),
                 ("intermediate", ctypes.c_int64), ("rms_eps", ctypes.c_double),
                 ("rope_theta", ctypes.c_double), ("max_ctx", ctypes.c_int64),
-                ("has_qkv_bias", ctypes.c_int64), ("window", ctypes.c_int64)]
+                ("has_qkv_bias", ctypes.c_int64), ("window", ctypes.c_int64),
+                ("use_yarn", ctypes.c_int64), ("yarn", OrcYarn)]
 
 
 class OrcWeights(ctypes.Structure):
@@ -69,6 +79,12 @@ def _load():
             lib.orc_rmsnorm.restype = None
             lib.orc_rope.argtypes = [vp, i64, dbl, dbl]
             lib.orc_rope.restype = None
+            lib.orc_yarn_ramp.argtypes = [dbl, dbl, i64]
+            lib.orc_yarn_ramp.restype = dbl
+            lib.orc_yarn_corr_dim.argtypes = [i64, i64, dbl, dbl]
+            lib.orc_yarn_corr_dim.restype = dbl
+            lib.orc_rope_yarn.argtypes = [vp, i64, dbl, dbl, ctypes.POINTER(OrcYarn)]
+            lib.orc_rope_yarn.restype = None
             lib.orc_linear.argtypes = [vp, vp, vp, i64, i64, vp]
             lib.orc_linear.restype = None
             lib.orc_silu.argtypes = [dbl]
@@ -132,6 +148,28 @@ def rope(v, pos: float, theta: float = 10000.0) -> np.ndarray:
     return v
 
 
+def _yarn(y) -> "OrcYarn":
+    """OrcYarn from a dict with the YARN_FIELDS keys."""
+    return OrcYarn(*(float(y[k]) if k != "n_ctx_orig" else int(y[k]) for k in YARN_FIELDS))
+
+
+def yarn_ramp(low: float, high: float, i0: int) -> float:
+    return _load().orc_yarn_ramp(float(low), float(high), int(i0))
+
+
+def yarn_corr_dim(n_dims: int, n_ctx_orig: int, n_rot: float, base: float) -> float:
+    return _load().orc_yarn_corr_dim(int(n_dims), int(n_ctx_orig), float(n_rot), float(base))
+
+
+def rope_yarn(v, pos: float, yarn: dict, theta: float = 10000.0) -> np.ndarray:
+    """rotate_half RoPE with YaRN frequencies and magnitude; ``yarn`` holds
+    the YARN_FIELDS keys."""
+    v = _f64(v).copy()
+    y = _yarn(yarn)
+    _load().orc_rope_yarn(v.ctypes.data, v.size, float(pos), float(theta), ctypes.byref(y))
+    return v
+
+
 def linear(W, x, b=None) -> np.ndarray:
     W = _u16(W)
     x = _f64(x)
@@ -160,7 +198,8 @@ def attend(q, K, V, scale: float) -> np.ndarray:
 # ---- the whole block --------------------------------------------------------
 
 def block_forward(shape, weights: dict, x, pos, L: int, k_cache, v_cache, max_ctx: int | None = None,
-                  rows=None, mats64: dict | None = None, window: int = 0):
+                  rows=None, mats64: dict | None = None, window: int = 0,
+                  yarn: dict | None = None):
     """Run the block for T = len(x) new tokens on top of L history slots.
 
     ``shape`` is a ``synth.BlockShape``.  ``k_cache``/``v_cache`` (fp16
@@ -169,7 +208,8 @@ def block_forward(shape, weights: dict, x, pos, L: int, k_cache, v_cache, max_ct
     the seven matrices as f64 values (e.g. dequantized weights, see
     ``dequant_i8`` / ``dequant_u4``); ``weights`` then supplies only the gains
     and biases.  ``window`` > 0: sliding-window attention over the last
-    ``window`` slots (the query's own slot included); 0 = full attention."""
+    ``window`` slots (the query's own slot included); 0 = full attention.
+    ``yarn``: YaRN RoPE parameters (the YARN_FIELDS keys), None = plain RoPE."""
     lib = _load()
     x = _u16(x)
     T = x.shape[0]
@@ -179,7 +219,8 @@ def block_forward(shape, weights: dict, x, pos, L: int, k_cache, v_cache, max_ct
         raise ValueError("caches must be C-contiguous")
     C = kc.shape[1] if max_ctx is None else max_ctx
     cfg = OrcConfig(shape.hidden, shape.n_heads, shape.n_kv_heads, shape.head_dim, shape.intermediate,
-                    shape.rms_eps, shape.rope_theta, C, 1 if shape.has_qkv_bias else 0, int(window))
+                    shape.rms_eps, shape.rope_theta, C, 1 if shape.has_qkv_bias else 0, int(window),
+                    0 if yarn is None else 1, OrcYarn() if yarn is None else _yarn(yarn))
     keep = {}
     wts = OrcWeights()
     for name in WEIGHT_FIELDS:

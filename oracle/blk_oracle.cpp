@@ -4,6 +4,7 @@
 // ascending index order; no blocking, fusion or reordering.
 #include "blk_oracle.h"
 
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <vector>
@@ -122,6 +123,38 @@ void orc_rope(double* v, int64_t D, double pos, double theta) {
   }
 }
 
+double orc_yarn_ramp(double low, double high, int64_t i0) {
+  const double y = (static_cast<double>(i0 / 2) - low) / std::max(0.001, high - low);
+  return 1.0 - std::min(1.0, std::max(0.0, y));
+}
+
+double orc_yarn_corr_dim(int64_t n_dims, int64_t n_ctx_orig, double n_rot, double base) {
+  const double pi = 3.14159265358979323846;
+  return static_cast<double>(n_dims) *
+         std::log(static_cast<double>(n_ctx_orig) / (n_rot * 2.0 * pi)) / (2.0 * std::log(base));
+}
+
+void orc_rope_yarn(double* v, int64_t D, double pos, double theta, const orc_yarn* y) {
+  const int64_t half = D / 2;
+  const double low = orc_yarn_corr_dim(D, y->n_ctx_orig, y->beta_fast, theta);
+  const double high = orc_yarn_corr_dim(D, y->n_ctx_orig, y->beta_slow, theta);
+  const double m = y->ext_factor != 0.0
+                       ? y->attn_factor * (1.0 + 0.1 * std::log(1.0 / y->freq_scale))
+                       : y->attn_factor;
+  for (int64_t i = 0; i < half; ++i) {
+    const double inv_freq =
+        std::pow(theta, -2.0 * static_cast<double>(i) / static_cast<double>(D));
+    const double a_orig = pos * inv_freq;
+    const double a_int = y->freq_scale * a_orig;
+    const double r = orc_yarn_ramp(low, high, 2 * i) * y->ext_factor;
+    const double angle = a_int * (1.0 - r) + a_orig * r;
+    const double c = std::cos(angle) * m, s = std::sin(angle) * m;
+    const double a = v[i], b = v[i + half];
+    v[i] = a * c - b * s;
+    v[i + half] = b * c + a * s;
+  }
+}
+
 void orc_linear(const uint16_t* W, const uint16_t* b, const double* x,
                 int64_t n_out, int64_t n_in, double* y) {
   linear(MatF16{W}, b, x, n_out, n_in, y);
@@ -154,6 +187,14 @@ void orc_attend(const double* q, const uint16_t* K, const uint16_t* V,
 }  // extern "C"
 
 namespace {
+
+// RoPE of one head at position pos: plain, or YaRN when the config asks.
+void rope_of(const orc_config* cfg, double* v, int64_t pos) {
+  if (cfg->use_yarn)
+    orc_rope_yarn(v, cfg->head_dim, static_cast<double>(pos), cfg->rope_theta, &cfg->yarn);
+  else
+    orc_rope(v, cfg->head_dim, static_cast<double>(pos), cfg->rope_theta);
+}
 
 // The block with its seven matrices given as views (gains and biases are
 // always fp16 from `w`).
@@ -188,7 +229,7 @@ int block_forward(const orc_config* cfg, const orc_weights* w, const M& wq, cons
     linear(wk, bias ? w->bk : nullptr, &xn[t * H], Hkv * D, H, k.data());
     linear(wv, bias ? w->bv : nullptr, &xn[t * H], Hkv * D, H, v.data());
     for (int64_t g = 0; g < Hkv; ++g) {
-      orc_rope(&k[g * D], D, static_cast<double>(pos[t]), cfg->rope_theta);
+      rope_of(cfg, &k[g * D], pos[t]);
       for (int64_t d = 0; d < D; ++d) {
         const uint16_t kh = encode_half(k[g * D + d]);
         const uint16_t vh = encode_half(v[g * D + d]);
@@ -211,7 +252,7 @@ int block_forward(const orc_config* cfg, const orc_weights* w, const M& wq, cons
     if (t < 0 || t >= T) return -1;
     linear(wq, bias ? w->bq : nullptr, &xn[t * H], Hq * D, H, q.data());
     for (int64_t hq = 0; hq < Hq; ++hq) {
-      orc_rope(&q[hq * D], D, static_cast<double>(pos[t]), cfg->rope_theta);
+      rope_of(cfg, &q[hq * D], pos[t]);
       const int64_t g = hq / group;
       // slots [lo, L + t]: all of them, or the last `window` (sliding window)
       const int64_t lo =

@@ -40,6 +40,29 @@
 extern "C" {
 #endif
 
+/* YaRN RoPE (the ds4.c study notes, Part 4, "Trace 1: YaRN frequency
+ * scaling" and "Trace 2: RoPE tail rotation").  The notes give the ramp, the
+ * correction dimension and the per-layer scale; they elide how the ramp
+ * blends the original and the scaled frequency and never define the
+ * magnitude factor.  Readings (also in the design notes), from the YaRN
+ * method the notes trace ("NTK-by-parts" interpolation plus an attention
+ * temperature):
+ *   low  = corr_dim(beta_fast), high = corr_dim(beta_slow) (no rounding)
+ *   frequency pair i (rotate_half partners i, i + D/2; the ramp's i0 = 2i):
+ *     a_orig = pos * theta^(-2i/D),  a_int = freq_scale * a_orig,
+ *     r = ramp(low, high, 2i) * ext_factor,
+ *     angle = a_int * (1 - r) + a_orig * r
+ *   magnitude m = attn_factor * (1 + 0.1 ln(1 / freq_scale)) when
+ *     ext_factor != 0, else attn_factor; both cos and sin are scaled by m. */
+typedef struct {
+  double freq_scale;    /* 1/s: the interpolated frequencies are s times lower */
+  double ext_factor;    /* weight of the ramp (the notes: 1 on scaled layers, else 0) */
+  double attn_factor;   /* extra magnitude factor (1 = none) */
+  double beta_fast;     /* rotations over the original context that start the ramp */
+  double beta_slow;     /* ... and end it */
+  int64_t n_ctx_orig;   /* the original training context */
+} orc_yarn;
+
 typedef struct {
   int64_t hidden, n_heads, n_kv_heads, head_dim, intermediate;
   double rms_eps, rope_theta;
@@ -53,6 +76,9 @@ typedef struct {
    * each row the output of a lone token; slots outside the window are never
    * read; a band-masked brute-force restatement agrees. */
   int64_t window;
+  /* use_yarn != 0: RoPE of q and k is orc_rope_yarn with `yarn`. */
+  int64_t use_yarn;
+  orc_yarn yarn;
 } orc_config;
 
 /* Host pointers to fp16 bit patterns, weights [out, in] row-major. */
@@ -74,6 +100,26 @@ void orc_rmsnorm(const double* x, const double* g, int64_t n, double eps,
  * Pinned: one-hot closed forms (pairing, sign, frequency), pos 0 identity,
  * pair-norm preservation, rot(a) then rot(b) == rot(a+b). */
 void orc_rope(double* v, int64_t D, double pos, double theta);
+
+/* The notes' ramp: 1 - clamp((i0/2 - low) / max(0.001, high - low), 0, 1)
+ * (1 below the ramp: the original frequency; 0 above it: the scaled one).
+ * Pinned: 1 at i0 = 2 low, 0 at i0 = 2 high, 1/2 half way, a step when
+ * high = low. */
+double orc_yarn_ramp(double low, double high, int64_t i0);
+
+/* The notes' correction dimension: the frequency-pair index at which a
+ * rotation of wavelength 2 pi base^(2d / n_dims) turns n_rot times over the
+ * original context, n_dims ln(n_ctx_orig / (2 pi n_rot)) / (2 ln base).
+ * Pinned by that defining property (inverse check). */
+double orc_yarn_corr_dim(int64_t n_dims, int64_t n_ctx_orig, double n_rot, double base);
+
+/* In-place rotate_half RoPE with YaRN frequencies and magnitude (readings
+ * above).  Pinned: equals orc_rope when ext_factor = 0, freq_scale = 1,
+ * attn_factor = 1; equals orc_rope at pos * freq_scale when ext_factor = 0
+ * (position interpolation); every pair below the ramp turns as orc_rope and
+ * every pair above it as the interpolated rotation, both scaled by m; a pair
+ * half way up the ramp turns by the mean of the two angles. */
+void orc_rope_yarn(double* v, int64_t D, double pos, double theta, const orc_yarn* y);
 
 /* y[o] = sum_i W[o][i] * x[i] (+ b[o] when b != NULL); W fp16 [n_out, n_in].
  * Pinned: one-hot input selects a weight column; zero weights give the bias. */

@@ -56,6 +56,18 @@ MUTATIONS = [
     ("u4: the next group's scale and zero", "const int64_t g = o * ng + i / group;",
      "const int64_t g = o * ng + (i / group + 1) % ng;"),
     ("f64 weights: v projected with wk", "MatF64{m->wv}", "MatF64{m->wk}"),
+    ("yarn ramp inverted", "return 1.0 - std::min(1.0, std::max(0.0, y));",
+     "return std::min(1.0, std::max(0.0, y));"),
+    ("yarn ramp on the element index", "static_cast<double>(i0 / 2) - low",
+     "static_cast<double>(i0) - low"),
+    ("yarn corr dim without the factor 2", "(2.0 * std::log(base))", "(std::log(base))"),
+    ("yarn betas swapped", "orc_yarn_corr_dim(D, y->n_ctx_orig, y->beta_fast, theta);",
+     "orc_yarn_corr_dim(D, y->n_ctx_orig, y->beta_slow, theta);"),
+    ("yarn blend weights swapped", "const double angle = a_int * (1.0 - r) + a_orig * r;",
+     "const double angle = a_orig * (1.0 - r) + a_int * r;"),
+    ("yarn magnitude dropped", "? y->attn_factor * (1.0 + 0.1 * std::log(1.0 / y->freq_scale))",
+     "? y->attn_factor"),
+    ("yarn ignored by the block", "if (cfg->use_yarn)", "if (false)"),
 ]
 
 PIN_TESTS = [getattr(pins, n) for n in dir(pins) if n.startswith("test_")]

@@ -603,3 +603,112 @@ def test_window_matches_band_masked_bruteforce(T, L, W):
     assert np.mean(out.view(np.uint16) == bo.view(np.uint16)) > 0.99
     full = oracle.block_forward(s, w, x, pos, L, kc.copy(), vc.copy())[0]
     assert not np.array_equal(full.view(np.uint16), out.view(np.uint16))
+
+
+# ------------------------------------------------------------ YaRN RoPE
+# The ds4.c study notes (Part 4, "Trace 1: YaRN frequency scaling") give the
+# ramp and the correction dimension; the blend of the original and scaled
+# frequencies and the magnitude factor are readings (oracle/blk_oracle.h).
+
+YARN = {"freq_scale": 0.125, "ext_factor": 1.0, "attn_factor": 1.3, "beta_fast": 32.0,
+        "beta_slow": 1.0, "n_ctx_orig": 4096}
+
+
+def test_yarn_ramp_closed_forms():
+    low, high = 7.0, 19.0
+    assert oracle.yarn_ramp(low, high, 2 * 7) == 1.0        # start of the ramp: original
+    assert oracle.yarn_ramp(low, high, 2 * 19) == 0.0       # its end: scaled
+    assert oracle.yarn_ramp(low, high, 2 * 13) == 0.5       # half way
+    assert oracle.yarn_ramp(low, high, 0) == 1.0 and oracle.yarn_ramp(low, high, 126) == 0.0
+    # the pair index is i0 / 2 (i0 counts elements): i0 = 2 * 10 sits at 1 - 3/12
+    assert oracle.yarn_ramp(low, high, 20) == 0.75
+    # high == low: a step at low (the 0.001 floor on the width)
+    assert oracle.yarn_ramp(5.0, 5.0, 10) == 1.0 and oracle.yarn_ramp(5.0, 5.0, 12) == 0.0
+
+
+@pytest.mark.parametrize("n_dims,ctx,n_rot,base", [(128, 4096, 32.0, 10000.0),
+                                                   (128, 4096, 1.0, 10000.0),
+                                                   (64, 32768, 4.0, 1e6)])
+def test_yarn_corr_dim_is_where_a_pair_turns_n_rot_times(n_dims, ctx, n_rot, base):
+    """Defining property: pair d's wavelength 2 pi base^(2d / n_dims) fits
+    n_rot times into the original context."""
+    d = oracle.yarn_corr_dim(n_dims, ctx, n_rot, base)
+    wavelength = 2.0 * math.pi * base ** (2.0 * d / n_dims)
+    assert math.isclose(ctx / wavelength, n_rot, rel_tol=1e-12)
+    # more turns = a higher frequency = a lower pair index
+    assert oracle.yarn_corr_dim(n_dims, ctx, 2 * n_rot, base) < d
+
+
+def test_yarn_off_equals_plain_rope():
+    v = synth.normal_f64(0, 120, 0, 128)
+    off = dict(YARN, freq_scale=1.0, ext_factor=0.0, attn_factor=1.0)
+    for p in (0.0, 1.0, 777.0, 40000.0):
+        assert np.array_equal(oracle.rope_yarn(v, p, off), oracle.rope(v, p))
+
+
+def test_yarn_without_the_ramp_is_position_interpolation():
+    """ext_factor = 0: every pair runs at freq_scale times its frequency, i.e.
+    plain RoPE at position pos * freq_scale (exact for a power-of-two scale)."""
+    v = synth.normal_f64(0, 121, 0, 128)
+    pi_only = dict(YARN, ext_factor=0.0, attn_factor=1.0)
+    for p in (3.0, 1000.0, 50000.0):
+        assert np.array_equal(oracle.rope_yarn(v, p, pi_only), oracle.rope(v, p * 0.125))
+
+
+def test_yarn_pairs_below_and_above_the_ramp():
+    """Pairs below corr_dim(beta_fast) keep the original angle, pairs above
+    corr_dim(beta_slow) take the interpolated one; all are scaled by the
+    magnitude m = attn_factor * (1 + 0.1 ln(1 / freq_scale))."""
+    D, p = 128, 9000.0
+    low = oracle.yarn_corr_dim(D, 4096, 32.0, 10000.0)
+    high = oracle.yarn_corr_dim(D, 4096, 1.0, 10000.0)
+    assert 10 < low < high < 60
+    m = 1.3 * (1.0 + 0.1 * math.log(8.0))
+    v = synth.normal_f64(0, 122, 0, D)
+    got = oracle.rope_yarn(v, p, YARN)
+    orig, interp = oracle.rope(v, p), oracle.rope(v, p * 0.125)
+    h = D // 2
+    for i in range(h):
+        idx = [i, i + h]
+        if i <= math.floor(low):
+            assert np.allclose(got[idx], m * orig[idx], rtol=1e-12, atol=1e-12), i
+        elif i >= math.ceil(high):
+            assert np.allclose(got[idx], m * interp[idx], rtol=1e-12, atol=1e-12), i
+
+
+def test_yarn_pair_on_the_ramp_turns_by_the_blended_angle():
+    D, p = 128, 5.0                    # small angles: read back with atan2
+    low = oracle.yarn_corr_dim(D, 4096, 32.0, 10000.0)
+    high = oracle.yarn_corr_dim(D, 4096, 1.0, 10000.0)
+    m = 1.3 * (1.0 + 0.1 * math.log(8.0))
+    for i in range(math.ceil(low), math.floor(high) + 1):
+        r = oracle.yarn_ramp(low, high, 2 * i)
+        assert 0.0 < r < 1.0
+        e = np.zeros(D)
+        e[i] = 1.0
+        out = oracle.rope_yarn(e, p, YARN)
+        a = p * 10000.0 ** (-2.0 * i / D)
+        want = 0.125 * a * (1.0 - r) + a * r
+        assert math.isclose(math.atan2(out[i + D // 2], out[i]), want, rel_tol=1e-12), i
+        assert math.isclose(math.hypot(out[i], out[i + D // 2]), m, rel_tol=1e-12), i
+
+
+def test_block_with_yarn_off_or_interpolating_equals_plain_block():
+    """The block threads YaRN through RoPE of q and k only: switched off it
+    is the plain block bit for bit, and pure interpolation by 1/2 at even
+    positions is the plain block at half those positions."""
+    T, L = 5, 9
+    s, w, x, pos, kc, vc = _tiny_case(T, L)
+    off = dict(YARN, freq_scale=1.0, ext_factor=0.0, attn_factor=1.0)
+    plain = oracle.block_forward(s, w, x, pos, L, kc.copy(), vc.copy())
+    got = oracle.block_forward(s, w, x, pos, L, kc.copy(), vc.copy(), yarn=off)
+    for a, b in zip(plain, got):
+        assert np.array_equal(a.view(np.uint16), b.view(np.uint16))
+    half = dict(off, freq_scale=0.5)
+    got = oracle.block_forward(s, w, x, 2 * pos, L, kc.copy(), vc.copy(), yarn=half)
+    for a, b in zip(plain, got):
+        assert np.array_equal(a.view(np.uint16), b.view(np.uint16))
+    # and the full YaRN rotation does change the block
+    on = oracle.block_forward(s, w, x, pos + 5000, L, kc.copy(), vc.copy(), yarn=YARN)
+    ref = oracle.block_forward(s, w, x, pos + 5000, L, kc.copy(), vc.copy())
+    assert not np.array_equal(on[0].view(np.uint16), ref[0].view(np.uint16))
