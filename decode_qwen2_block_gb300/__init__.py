@@ -40,7 +40,7 @@ EXPORTED = ("blk_create", "blk_destroy", "blk_set_flags", "blk_workspace_bytes",
             "blk_decode_batch_workspace_bytes", "blk_decode_batch",
             "blk_decode_batch_stack_workspace_bytes", "blk_decode_batch_stack",
             "blk_wait_probe", "blk_qworkspace_bytes", "blk_prefill_q", "blk_prefill_kv_q",
-            "blk_decode_q", "blk_decode_stack_q", "blk_set_window")
+            "blk_decode_q", "blk_decode_stack_q", "blk_set_window", "blk_set_rope_yarn")
 BLK_N_KERNELS = 16
 
 WEIGHT_FIELDS = ("ln1_g", "wq", "wk", "wv", "bq", "bk", "bv", "wo", "ln2_g", "w_gate", "w_up",
@@ -72,6 +72,15 @@ class BlkQWeights(ctypes.Structure):
                 [(n, BlkQMatrix) for n in QMATRIX_FIELDS])
 
 
+YARN_FIELDS = ("freq_scale", "ext_factor", "attn_factor", "beta_fast", "beta_slow", "n_ctx_orig")
+
+
+class BlkYarn(ctypes.Structure):
+    _fields_ = [("freq_scale", ctypes.c_double), ("ext_factor", ctypes.c_double),
+                ("attn_factor", ctypes.c_double), ("beta_fast", ctypes.c_double),
+                ("beta_slow", ctypes.c_double), ("n_ctx_orig", ctypes.c_int64)]
+
+
 class BlkError(RuntimeError):
     def __init__(self, status: int, what: str = ""):
         self.status = status
@@ -101,6 +110,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.blk_set_flags.restype = i32
     lib.blk_set_window.argtypes = [vp, i64]
     lib.blk_set_window.restype = i32
+    lib.blk_set_rope_yarn.argtypes = [vp, ctypes.POINTER(BlkYarn)]
+    lib.blk_set_rope_yarn.restype = i32
     lib.blk_workspace_bytes.argtypes = [vp, i64]
     lib.blk_workspace_bytes.restype = ctypes.c_size_t
     lib.blk_prefill.argtypes = [vp, ctypes.POINTER(BlkWeights), vp, vp, i64, vp, vp, vp, vp, vp,
@@ -193,6 +204,11 @@ def blk_set_flags(handle: int, flags: int) -> int:
 
 def blk_set_window(handle: int, window: int) -> int:
     return load().blk_set_window(handle, window)
+
+
+def blk_set_rope_yarn(handle: int, yarn) -> int:
+    """yarn: a BlkYarn, or None for plain RoPE."""
+    return load().blk_set_rope_yarn(handle, None if yarn is None else ctypes.byref(yarn))
 
 
 def blk_workspace_bytes(handle: int, max_T: int) -> int:
@@ -365,6 +381,13 @@ class Block:
         rc = blk_set_window(self.handle, window)
         if rc != BLK_OK:
             raise BlkError(rc, "blk_set_window")
+
+    def set_rope_yarn(self, yarn: dict | None):
+        """YaRN RoPE with the YARN_FIELDS parameters (None: plain RoPE)."""
+        y = None if yarn is None else BlkYarn(*(yarn[k] for k in YARN_FIELDS))
+        rc = blk_set_rope_yarn(self.handle, y)
+        if rc != BLK_OK:
+            raise BlkError(rc, "blk_set_rope_yarn")
 
     def workspace_bytes(self, max_T: int) -> int:
         return blk_workspace_bytes(self.handle, max_T)

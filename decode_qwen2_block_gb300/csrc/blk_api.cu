@@ -720,6 +720,45 @@ int run_prefill_q(blk_handle h, const blk_qweights* w, const void* x, const int6
 
 extern "C" {
 
+// The handle's rotation table [max_ctx][head_dim / 2] of (cos, sin) pairs,
+// computed in f64 and stored as fp32.  Plain RoPE: pair i of position p turns
+// by p * theta^(-2i / D).  YaRN (y != NULL; the ds4.c study notes, Part 4,
+// "Trace 1: YaRN frequency scaling" and the tail-rotation listing): the
+// notes' ramp 1 - clamp((i - low) / max(0.001, high - low), 0, 1) between
+// low = corr_dim(beta_fast) and high = corr_dim(beta_slow), corr_dim(n) =
+// D ln(n_ctx_orig / (2 pi n)) / (2 ln theta); the angle blends the
+// interpolated freq_scale * a and the original a with weight ramp *
+// ext_factor on the original; cos and sin are scaled by attn_factor * (1 +
+// 0.1 ln(1 / freq_scale)) when ext_factor != 0 (else attn_factor), the YaRN
+// method's temperature, so q . k carries it squared.
+static void rope_table(const blk_config& c, const blk_yarn* y, std::vector<float2>& table) {
+  const int half = c.head_dim / 2;
+  const double D = (double)c.head_dim, theta = (double)c.rope_theta;
+  table.assign((size_t)c.max_ctx * half, make_float2(0.f, 0.f));
+  const double pi = 3.14159265358979323846;
+  auto corr_dim = [&](double n_rot) {
+    return D * log((double)y->n_ctx_orig / (n_rot * 2.0 * pi)) / (2.0 * log(theta));
+  };
+  const double low = y ? corr_dim(y->beta_fast) : 0.0, high = y ? corr_dim(y->beta_slow) : 0.0;
+  const double m = !y ? 1.0
+                      : (y->ext_factor != 0.0
+                             ? y->attn_factor * (1.0 + 0.1 * log(1.0 / y->freq_scale))
+                             : y->attn_factor);
+  for (int i = 0; i < half; ++i) {
+    const double inv = pow(theta, -2.0 * i / D);
+    double r = 0.0;   // weight of the original frequency
+    if (y) {
+      const double t = ((double)i - low) / (high - low > 0.001 ? high - low : 0.001);
+      r = (1.0 - (t < 0.0 ? 0.0 : (t > 1.0 ? 1.0 : t))) * y->ext_factor;
+    }
+    for (int64_t p = 0; p < c.max_ctx; ++p) {
+      const double a_orig = (double)p * inv;
+      const double a = y ? (y->freq_scale * a_orig) * (1.0 - r) + a_orig * r : a_orig;
+      table[(size_t)p * half + i] = make_float2((float)(cos(a) * m), (float)(sin(a) * m));
+    }
+  }
+}
+
 int blk_create(const blk_config* cfg, blk_handle* out) {
   if (!cfg || !out) return BLK_ERR_NULL;
   *out = nullptr;
@@ -755,15 +794,8 @@ int blk_create(const blk_config* cfg, blk_handle* out) {
     return BLK_ERR_CUDA;
   }
 
-  const int half = cfg->head_dim / 2;
-  std::vector<float2> table((size_t)cfg->max_ctx * half);
-  for (int i = 0; i < half; ++i) {
-    const double inv = pow((double)cfg->rope_theta, -2.0 * i / (double)cfg->head_dim);
-    for (int64_t p = 0; p < cfg->max_ctx; ++p) {
-      const double a = (double)p * inv;
-      table[(size_t)p * half + i] = make_float2((float)cos(a), (float)sin(a));
-    }
-  }
+  std::vector<float2> table;
+  rope_table(*cfg, nullptr, table);
   if (cudaMalloc(&h->rope, table.size() * sizeof(float2)) != cudaSuccess ||
       cudaMalloc(&h->status, sizeof(int)) != cudaSuccess ||
       cudaMemcpy(h->rope, table.data(), table.size() * sizeof(float2),
@@ -798,6 +830,24 @@ int blk_set_window(blk_handle h, int64_t window) {
   if (!h) return BLK_ERR_NULL;
   if (window < 0) return BLK_ERR_SHAPE;
   h->window = window;
+  return BLK_OK;
+}
+
+int blk_set_rope_yarn(blk_handle h, const blk_yarn* y) {
+  if (!h) return BLK_ERR_NULL;
+  if (y && !(y->freq_scale > 0.0 && y->freq_scale <= 1.0 && y->ext_factor >= 0.0 &&
+             y->ext_factor <= 1.0 && y->attn_factor > 0.0 && y->beta_fast > 0.0 &&
+             y->beta_slow > 0.0 && y->n_ctx_orig >= 1))
+    return BLK_ERR_SHAPE;
+  std::vector<float2> table;
+  rope_table(h->cfg, y, table);
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev != h->device) return BLK_ERR_CUDA;
+  // the table is read by kernels already enqueued: let them finish first
+  if (cudaDeviceSynchronize() != cudaSuccess ||
+      cudaMemcpy(h->rope, table.data(), table.size() * sizeof(float2),
+                 cudaMemcpyHostToDevice) != cudaSuccess)
+    return BLK_ERR_CUDA;
   return BLK_OK;
 }
 

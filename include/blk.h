@@ -113,6 +113,39 @@ typedef struct blk_handle_s* blk_handle;
  * result.  Returns BLK_OK, BLK_ERR_NULL or BLK_ERR_SHAPE (W < 0). */
 int blk_set_window(blk_handle h, int64_t window);
 
+/* YaRN RoPE (the ds4.c study notes, Part 4, "Trace 1: YaRN frequency
+ * scaling" and the RoPE tail-rotation listing), for the handle's whole
+ * rotation table: every phase and entry point then rotates q and k with it.
+ * With D = head_dim, pair i (rotate_half partners i, i + D/2) at position p:
+ *   a      = p * rope_theta^(-2i/D)                       (the original angle)
+ *   low    = corr_dim(beta_fast), high = corr_dim(beta_slow),
+ *            corr_dim(n) = D ln(n_ctx_orig / (2 pi n)) / (2 ln rope_theta)
+ *   ramp_i = 1 - clamp((i - low) / max(0.001, high - low), 0, 1)  (the notes' ramp)
+ *   r_i    = ramp_i * ext_factor
+ *   angle  = freq_scale * a * (1 - r_i) + a * r_i
+ *   cos, sin are multiplied by m = attn_factor * (1 + 0.1 ln(1/freq_scale))
+ *            when ext_factor != 0, else by attn_factor
+ * The notes elide the blend and never define m; the two are the readings
+ * above, the YaRN method's interpolation by parts and its attention
+ * temperature (q . k is scaled by m^2).  freq_scale = 1, ext_factor = 0,
+ * attn_factor = 1 is plain RoPE. */
+typedef struct {
+  double freq_scale;   /* 1/s, in (0, 1]                                          */
+  double ext_factor;   /* in [0, 1]; the notes use 1 on scaled layers, 0 elsewhere */
+  double attn_factor;  /* > 0                                                      */
+  double beta_fast;    /* > 0, rotations over n_ctx_orig where the ramp starts (32) */
+  double beta_slow;    /* > 0, ... where it ends (1)                               */
+  int64_t n_ctx_orig;  /* >= 1, the original training context                      */
+} blk_yarn;
+
+/* Sets YaRN RoPE for the handle (y = NULL: back to plain RoPE).  Rebuilds the
+ * handle's cos/sin table on the host in f64 and copies it to the device; it
+ * first waits for all work on the device (the table may be in use), so it is
+ * a setup call, not one for the hot path.  Allocates nothing.  Returns
+ * BLK_OK, BLK_ERR_NULL, BLK_ERR_SHAPE (a field out of range) or BLK_ERR_CUDA
+ * (including: the current device is not the handle's). */
+int blk_set_rope_yarn(blk_handle h, const blk_yarn* y);
+
 /* Creates a handle for `cfg` on the current CUDA device: validates the shape,
  * builds the fp32 cos/sin table [max_ctx][head_dim/2] (angles in f64) and a
  * status word.  Returns BLK_OK, BLK_ERR_NULL, BLK_ERR_SHAPE, BLK_ERR_DEVICE or
