@@ -33,7 +33,9 @@
  * on the handle's GPU, 16-byte aligned.  The library allocates device memory
  * only in blk_create (a RoPE table and a status word), never on the hot path.
  * Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
- * stream) and never synchronize, trap or abort.
+ * stream) and never synchronize, trap or abort; the one exception is the
+ * setup call blk_set_rope_yarn, which waits for the device before it
+ * replaces the rotation table.
  *
  * KV cache: one K and one V buffer per layer, each [n_kv_heads][max_ctx][head_dim]
  * (the buddy-mlir runtime's per-layer [1, kv_heads, max_len, head_dim] cache of
