@@ -472,13 +472,26 @@ int run_decode_batch(blk_handle h, const blk_weights* w, const void* x, const in
   g.cache_lens = cache_lens;
   g.seq_stride = (int64_t)Hkv * c.max_ctx * D;
   g.part = reinterpret_cast<float*>(base + lay.part32);   // K splits fill the SM pairs;
-  g.max_splits = kMaxSplitsBatch;                         // qkv_finish applies the epilogue
+  g.max_splits = kMaxSplitsBatch;   // the attention kernel (or qkv_finish) applies the epilogue
   g.err = h->status;
   BLK_LAUNCH(tm, kKGemmQKV, launch_tc_gemm(g, kTcQKV, h->num_sms, s, true));
-  if (g.splits > 1) BLK_LAUNCH(tm, kKQkvFinish, launch_qkv_finish(g, s));
 
-  // attention of every sequence over its own slots [0, cache_lens[b]]
+  // attention of every sequence over its own slots [0, cache_lens[b]]; a
+  // K-split QKV projection is finished inside it (bias, RoPE, new K/V)
   DecodeAttnBatchParams pa = {};
+  if (g.splits > 4) BLK_LAUNCH(tm, kKQkvFinish, launch_qkv_finish(g, s));
+  else if (g.splits > 1) {
+    pa.qkv_part = g.part;
+    pa.qkv_splits = g.splits;
+    for (int i = 0; i < 3; ++i) pa.bias[i] = g.bias[i];
+    pa.pos = pos;
+    pa.rope = h->rope;
+    pa.rope_len = c.max_ctx;
+    pa.kc = static_cast<__half*>(k_cache);
+    pa.vc = static_cast<__half*>(v_cache);
+    pa.k_new = static_cast<__half*>(k_new);
+    pa.v_new = static_cast<__half*>(v_new);
+  }
   {
     const int64_t kd[3] = {D, c.max_ctx, (int64_t)M * Hkv};
     const int64_t ks[2] = {(int64_t)D * 2, c.max_ctx * D * 2};

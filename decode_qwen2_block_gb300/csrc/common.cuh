@@ -96,6 +96,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   return true;
 }
 
+// Brings a tensor map (a kernel parameter or global memory) into the TMA
+// unit's descriptor cache ahead of its first copy.
+__device__ __forceinline__ void prefetch_tmap(const void* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
 // ---- bulk copies (TMA, untiled) ----------------------------------------------
 // Copies `bytes` (multiple of 16, both addresses 16-byte aligned) from global
 // to shared memory; completion is signalled on `bar` as transaction bytes.

@@ -82,6 +82,47 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// The same for global memory: this thread's stores before later tensor
+// copies that read them.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// The attention kernel finishes a K-split QKV projection of at most this
+// many splits (more: qkv_finish does it first).
+constexpr int kQkvMaxSplits = 4;
+
+// Column pair (c0, c0 + D/2) of row b of the K-split QKV output: the S
+// partials (every load issued before any add), added in split order, plus
+// the bias pair.
+struct QkvPair {
+  float a[kQkvMaxSplits], c[kQkvMaxSplits];
+  float ba, bc;
+};
+__device__ __forceinline__ void qkv_pair_load(const DecodeAttnBatchParams& p, int b, int c0,
+                                              int half, const __half* bias, int bi, QkvPair& q) {
+  const size_t N = (size_t)(p.Hq + 2 * p.Hkv) * p.D, MN = (size_t)p.B * N;
+  const float* src = p.qkv_part + (size_t)b * N + c0;
+#pragma unroll
+  for (int s = 0; s < kQkvMaxSplits; ++s)
+    if (s < p.qkv_splits) {
+      q.a[s] = __ldcg(src + s * MN);
+      q.c[s] = __ldcg(src + s * MN + half);
+    }
+  q.ba = bias ? __half2float(bias[bi]) : 0.f;
+  q.bc = bias ? __half2float(bias[bi + half]) : 0.f;
+}
+__device__ __forceinline__ float2 qkv_pair_sum(const DecodeAttnBatchParams& p, const QkvPair& q) {
+  float a = 0.f, c = 0.f;
+#pragma unroll
+  for (int s = 0; s < kQkvMaxSplits; ++s)
+    if (s < p.qkv_splits) {
+      a += q.a[s];
+      c += q.c[s];
+    }
+  return make_float2(a + q.ba, c + q.bc);
+}
+
 template <int D, int kGroups, int kTPG>
 struct BSmem {
   static constexpr int kQStride = D + 8;                      // halves (conflict-free ldmatrix)
@@ -165,12 +206,83 @@ __global__ void __launch_bounds__(128 * kTPG)
   griddep_wait();    // q and the new slot L come from the previous kernel
   griddep_launch();
 
-  // Q tile: rows 0..G-1 = query heads g*G.., rows G..15 zero
-  for (int i = tid; i < 16 * kCPR; i += kThreads) {
-    const int r = i / kCPR, ch = i % kCPR;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (r < G) v = *reinterpret_cast<const uint4*>(p.q16 + ((size_t)b * p.Hq + g * G + r) * D + ch * 8);
-    *reinterpret_cast<uint4*>(qtile + r * Sm::kQStride + ch * 8) = v;
+  if (p.qkv_part) {
+    // the QKV projection's K splits: q of this CTA's G heads (rows G..15
+    // zero), and in the split that holds slot L the new K/V, stored in the
+    // cache before the copies below read that slot
+    constexpr int half = D / 2;
+    const int64_t ps = p.pos[b];
+    const bool pos_ok = ps >= 0 && ps < p.rope_len;
+    if (!pos_ok && tid == 0 && sp == 0 && g == 0) set_error(p.err, kDevPosition);
+    const float2* cs = p.rope + (size_t)(pos_ok ? ps : 0) * half;
+    // every thread's loads of every item first (one round trip), then the
+    // sums; rows G..15 of the tile are zero
+    constexpr int kItems = (16 * half + kThreads - 1) / kThreads;
+    QkvPair qp[kItems];
+    float2 rf[kItems];
+#pragma unroll
+    for (int k = 0; k < kItems; ++k) {
+      const int i = tid + k * kThreads, r = i / half, c = i % half;
+      if (i < 16 * half && r < G) {
+        const int hq = g * G + r;
+        qkv_pair_load(p, b, hq * D + c, half, p.bias[0], hq * D + c, qp[k]);
+        rf[k] = pos_ok ? cs[c] : make_float2(1.f, 0.f);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kItems; ++k) {
+      const int i = tid + k * kThreads, r = i / half, c = i % half;
+      if (i >= 16 * half) break;
+      float2 v = make_float2(0.f, 0.f);
+      if (r < G) {
+        v = qkv_pair_sum(p, qp[k]);
+        if (pos_ok) {
+          const float2 f = rf[k];
+          v = make_float2(v.x * f.x - v.y * f.y, v.y * f.x + v.x * f.y);
+        }
+      }
+      qtile[r * Sm::kQStride + c] = __float2half_rn(v.x);
+      qtile[r * Sm::kQStride + half + c] = __float2half_rn(v.y);
+    }
+    const bool slot_here = n > 0 && L >= j0 && L < j1;
+    if (n == 0 && tid == 0 && sp == 0 && g == 0) set_error(p.err, kDevPosition);
+    if (slot_here) {
+      __half* kd = p.kc + (size_t)b * p.Hkv * p.max_ctx * D + ((size_t)g * p.max_ctx + L) * D;
+      __half* vd = p.vc + (size_t)b * p.Hkv * p.max_ctx * D + ((size_t)g * p.max_ctx + L) * D;
+      const size_t nw = ((size_t)b * p.Hkv + g) * D;
+      for (int i = tid; i < 2 * half; i += kThreads) {
+        const bool is_k = i < half;
+        const int c = is_k ? i : i - half;
+        const int col = (is_k ? p.Hq + g : p.Hq + p.Hkv + g) * D + c;
+        QkvPair kp;
+        qkv_pair_load(p, b, col, half, is_k ? p.bias[1] : p.bias[2], g * D + c, kp);
+        float2 v = qkv_pair_sum(p, kp);
+        if (is_k && pos_ok) {
+          const float2 f = cs[c];
+          v = make_float2(v.x * f.x - v.y * f.y, v.y * f.x + v.x * f.y);
+        }
+        const __half h0 = __float2half_rn(v.x), h1 = __float2half_rn(v.y);
+        __half* d = is_k ? kd : vd;
+        d[c] = h0;
+        d[half + c] = h1;
+        __half* nwp = is_k ? p.k_new : p.v_new;
+        if (nwp) {
+          nwp[nw + c] = h0;
+          nwp[nw + half + c] = h1;
+        }
+      }
+      fence_proxy_async_global();   // before the tensor copy of slot L
+    }
+    __syncthreads();
+  } else {
+    // Q tile: rows 0..G-1 = query heads g*G.., rows G..15 zero
+    for (int i = tid; i < 16 * kCPR; i += kThreads) {
+      const int r = i / kCPR, ch = i % kCPR;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (r < G)
+        v = *reinterpret_cast<const uint4*>(p.q16 + ((size_t)b * p.Hq + g * G + r) * D + ch * 8);
+      *reinterpret_cast<uint4*>(qtile + r * Sm::kQStride + ch * 8) = v;
+    }
   }
   if (tid == 0)
     for (; issued < kGroups - 1 && issued < ngroups; ++issued) load_group(issued);

@@ -286,6 +286,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      prefetch_tmap(&p.tmA);
+      prefetch_tmap(&p.tmB[0]);
+      if (EPI == kTcQKV || EPI == kTcGateUp) prefetch_tmap(&p.tmB[1]);
+      if (EPI == kTcQKV) prefetch_tmap(&p.tmB[2]);
       int it = 0;
       bool waited = false;
       const uint32_t a_bytes = (uint32_t)(p.a_rows > 0 ? p.a_rows : BM) * BK * 2;

@@ -86,6 +86,7 @@ cudaError_t launch_tc_gemm(TcGemmParams& p, int epi, int num_sms, cudaStream_t s
 cudaError_t launch_splitk_reduce(const TcGemmParams& p, int num_sms, cudaStream_t s);
 // After a QKV launch with p.splits > 1: sums the partials in split order and
 // applies the QKV epilogue (bias, RoPE, q16 / cache slot / k_new, v_new).
+// (Batched decode with at most 4 splits leaves this to its attention kernel.)
 cudaError_t launch_qkv_finish(const TcGemmParams& p, cudaStream_t s);
 cudaError_t configure_tc_gemm_kernels();
 

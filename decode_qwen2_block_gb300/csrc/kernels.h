@@ -71,6 +71,22 @@ struct DecodeAttnBatchParams {
   float* part;                // [B][Hq][nsplit][D + 2] when nsplit > 1
   __half* attn16;             // [B, Hq * D]
   int* err;
+  // K-split QKV (qkv_part != null, qkv_splits <= 4): the GEMM left qkv_splits fp32 partials
+  // [S][B][(Hq + 2 Hkv) D]; this kernel adds them in split order, adds the
+  // bias, rotates q and k at pos[b] and, in the CTA whose split holds slot
+  // cache_lens[b], writes the new K/V there (and to k_new / v_new) before
+  // reading it -- the work of qkv_finish, which is then not launched.  q16
+  // is not used.
+  const float* qkv_part;
+  int qkv_splits;
+  const __half* bias[3];      // q, k, v biases (null: none)
+  const int64_t* pos;         // [B]
+  const float2* rope;         // [rope_len][D / 2]
+  int64_t rope_len;
+  __half* kc;                 // caches [B][Hkv][max_ctx][D]
+  __half* vc;
+  __half* k_new;              // [B, Hkv, D] or null
+  __half* v_new;
 };
 bool decode_batch_deep(int B, int Hkv, int num_sms);
 int decode_batch_splits(int B, int Hkv, int64_t max_len, int num_sms);

@@ -137,8 +137,12 @@ def test_batch_equals_single_sequence_decode():
     assert_close(outb[2:3].cpu().numpy(), out1.cpu().numpy().astype(np.float64), "batch vs single")
 
 
-def test_batch_argument_errors_and_bad_length():
-    s = synth.TINY
+@pytest.mark.parametrize("shape_name", ["TINY", "QWEN2_1P5B"])
+def test_batch_argument_errors_and_bad_length(shape_name):
+    """A length past max_ctx is refused on the host when max_cache_len says
+    so, else reported on the device with nothing written for that sequence
+    (1.5B: the QKV projection splits K and the attention kernel finishes it)."""
+    s = getattr(synth, shape_name)
     w = synth.block_weights(s, seed=11)
     C, B = 64, 2
     block = blk.Block(s, C)
