@@ -40,7 +40,8 @@ EXPORTED = ("blk_create", "blk_destroy", "blk_set_flags", "blk_workspace_bytes",
             "blk_decode_batch_workspace_bytes", "blk_decode_batch",
             "blk_decode_batch_stack_workspace_bytes", "blk_decode_batch_stack",
             "blk_wait_probe", "blk_qworkspace_bytes", "blk_prefill_q", "blk_prefill_kv_q",
-            "blk_decode_q", "blk_decode_stack_q", "blk_set_window", "blk_set_rope_yarn")
+            "blk_decode_q", "blk_decode_stack_q", "blk_set_window", "blk_set_rope_yarn",
+            "blk_prefill_stack_workspace_bytes", "blk_prefill_stack")
 BLK_N_KERNELS = 16
 
 WEIGHT_FIELDS = ("ln1_g", "wq", "wk", "wv", "bq", "bk", "bv", "wo", "ln2_g", "w_gate", "w_up",
@@ -150,6 +151,12 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.blk_decode_batch.argtypes = [vp, ctypes.POINTER(BlkWeights), vp, vp, vp, i64, i64, vp, vp,
                                      vp, vp, vp, vp, ctypes.c_size_t, vp]
     lib.blk_decode_batch.restype = i32
+    lib.blk_prefill_stack_workspace_bytes.argtypes = [vp, i64]
+    lib.blk_prefill_stack_workspace_bytes.restype = ctypes.c_size_t
+    lib.blk_prefill_stack.argtypes = [vp, ctypes.POINTER(BlkWeights), i32, ctypes.POINTER(vp),
+                                      ctypes.POINTER(vp), vp, vp, i64, i64, vp, vp, ctypes.c_size_t,
+                                      vp]
+    lib.blk_prefill_stack.restype = i32
     lib.blk_decode_batch_stack_workspace_bytes.argtypes = [vp, i64]
     lib.blk_decode_batch_stack_workspace_bytes.restype = ctypes.c_size_t
     lib.blk_decode_batch_stack.argtypes = [vp, ctypes.POINTER(BlkWeights), i32, ctypes.POINTER(vp),
@@ -293,6 +300,17 @@ def blk_decode_batch(handle, w: BlkWeights, x, pos, cache_lens, B, max_cache_len
 def blk_wait_probe(handle, flag_ptr, limit_ns: int, stream) -> int:
     """One kernel waiting (bounded) for the device int at flag_ptr; see include/blk.h."""
     return load().blk_wait_probe(handle, flag_ptr, limit_ns, stream)
+
+
+def blk_prefill_stack_workspace_bytes(handle, max_T: int) -> int:
+    return load().blk_prefill_stack_workspace_bytes(handle, max_T)
+
+
+def blk_prefill_stack(handle, w_array, n_layers, k_caches, v_caches, x, pos, T, cache_len, out,
+                      ws, ws_bytes, stream) -> int:
+    """w_array: (BlkWeights * n); k_caches/v_caches: (c_void_p * n)."""
+    return load().blk_prefill_stack(handle, w_array, n_layers, k_caches, v_caches, x, pos, T,
+                                    cache_len, out, ws, ws_bytes, stream)
 
 
 def blk_decode_batch_stack_workspace_bytes(handle, max_B: int) -> int:

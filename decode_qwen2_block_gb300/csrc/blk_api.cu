@@ -289,11 +289,15 @@ int run_block_tail(blk_handle h, const blk_weights* w, const void* x, __half* at
   return BLK_OK;
 }
 
-// prefill and prefill_kv: T new rows after L history slots.
+// prefill and prefill_kv: T new rows after L history slots.  In a layer
+// stack, x_normed says that the workspace's xn16 already holds RMSNorm 1 of x
+// (written by the previous layer's tail) and next_ln1, when set, has this
+// layer's tail write the next layer's RMSNorm 1 there.
 int run_prefill(blk_handle h, const blk_weights* w, const void* x,
                 const int64_t* pos, int64_t T, int64_t L, void* k_cache,
                 void* v_cache, void* out, void* k_new, void* v_new, void* ws,
-                size_t ws_bytes, void* stream) {
+                size_t ws_bytes, void* stream, bool x_normed = false,
+                const __half* next_ln1 = nullptr) {
   int rc = check_call(h, w, x, pos, T, L, k_cache, v_cache, out, k_new, v_new, ws);
   if (rc) return rc;
   const blk_config& c = h->cfg;
@@ -312,9 +316,10 @@ int run_prefill(blk_handle h, const blk_weights* w, const void* x,
   Timer tm{h, s};
 
   // RMSNorm 1
-  BLK_LAUNCH(tm, kKRmsNorm,
-             launch_rmsnorm_rows(x, false, static_cast<const __half*>(w->ln1_g), M, H,
-                                 c.rms_eps, xn16, s, first_pdl));
+  if (!x_normed)
+    BLK_LAUNCH(tm, kKRmsNorm,
+               launch_rmsnorm_rows(x, false, static_cast<const __half*>(w->ln1_g), M, H,
+                                   c.rms_eps, xn16, s, first_pdl));
 
   // QKV projection + bias + RoPE + KV append
   TcGemmParams g = {};
@@ -371,7 +376,7 @@ int run_prefill(blk_handle h, const blk_weights* w, const void* x,
   // follows it adds the partials and the residual
   return run_block_tail(h, w, x, attn16, h32, hn16, act16,
                         reinterpret_cast<float*>(base + lay.part32), kMaxSplits, true, out, M,
-                        s, tm);
+                        s, tm, next_ln1, xn16);
 }
 
 // Batched decode: B sequences, one new token each, caches [B][Hkv][max_ctx][D].
@@ -894,6 +899,43 @@ int blk_prefill_kv(blk_handle h, const blk_weights* w, const void* x,
                    void* v_new, void* ws, size_t ws_bytes, void* stream) {
   return run_prefill(h, w, x, pos, T, cache_len, k_cache, v_cache, out, k_new,
                      v_new, ws, ws_bytes, stream);
+}
+
+size_t blk_prefill_stack_workspace_bytes(blk_handle h, int64_t max_T) {
+  const size_t one = blk_workspace_bytes(h, max_T);
+  if (!one) return 0;
+  return one + 2 * align_up((size_t)max_T * h->cfg.hidden * 2);
+}
+
+int blk_prefill_stack(blk_handle h, const blk_weights* w, int n_layers, void* const* k_caches,
+                      void* const* v_caches, const void* x, const int64_t* pos, int64_t T,
+                      int64_t cache_len, void* out, void* ws, size_t ws_bytes, void* stream) {
+  if (!h || !w || !k_caches || !v_caches || !ws) return BLK_ERR_NULL;
+  if (n_layers < 1 || T < 1) return BLK_ERR_SHAPE;
+  // the two activation buffers between layers follow the one-layer workspace
+  const size_t act = align_up((size_t)T * h->cfg.hidden * 2);
+  const size_t layer_ws = prefill_ws(h->cfg, T, h->num_sms).total;
+  if (ws_bytes < layer_ws + 2 * act) return BLK_ERR_WORKSPACE;
+  unsigned char* base = static_cast<unsigned char*>(ws);
+  void* bufs[2] = {base + layer_ws, base + layer_ws + act};
+  auto layer_in = [&](int l) -> const void* { return l == 0 ? x : bufs[(l - 1) % 2]; };
+  auto layer_out = [&](int l) -> void* { return l == n_layers - 1 ? out : bufs[l % 2]; };
+  // every layer's arguments are checked before anything is enqueued
+  for (int l = 0; l < n_layers; ++l) {
+    const int rc = check_call(h, &w[l], layer_in(l), pos, T, cache_len, k_caches[l],
+                              v_caches[l], layer_out(l), nullptr, nullptr, ws);
+    if (rc) return rc;
+  }
+  for (int l = 0; l < n_layers; ++l) {
+    // layer l's tail writes layer l + 1's RMSNorm 1 (one launch fewer a layer)
+    const __half* next_ln1 =
+        l + 1 < n_layers ? static_cast<const __half*>(w[l + 1].ln1_g) : nullptr;
+    const int rc = run_prefill(h, &w[l], layer_in(l), pos, T, cache_len, k_caches[l],
+                               v_caches[l], layer_out(l), nullptr, nullptr, ws, layer_ws, stream,
+                               l > 0, next_ln1);
+    if (rc) return rc;
+  }
+  return BLK_OK;
 }
 
 int blk_decode(blk_handle h, const blk_weights* w, const void* x,

@@ -159,6 +159,9 @@ __global__ void __launch_bounds__(1024)
 constexpr int kReduceNormMaxS = 16;
 constexpr int kReduceNormThreads = 256;
 
+// MAXS (>= S) sizes the partial registers: 4 or 8 for the usual split
+// counts keeps several blocks resident per SM when there are many rows.
+template <int MAXS>
 __global__ void __launch_bounds__(kReduceNormThreads)
     splitk_reduce_norm_kernel(const float* __restrict__ part, int S,
                               const float* __restrict__ res32, __half* __restrict__ out16,
@@ -174,9 +177,9 @@ __global__ void __launch_bounds__(kReduceNormThreads)
   uint4 first = make_uint4(0, 0, 0, 0);
   for (int i = threadIdx.x; i < nv; i += blockDim.x) {
     const size_t c = r0 + (size_t)i * 8;
-    float4 q[kReduceNormMaxS][2];
+    float4 q[MAXS][2];
 #pragma unroll
-    for (int j = 0; j < kReduceNormMaxS; ++j)
+    for (int j = 0; j < MAXS; ++j)
       if (j < S) {
         q[j][0] = __ldcg(reinterpret_cast<const float4*>(part + j * MN + c));
         q[j][1] = __ldcg(reinterpret_cast<const float4*>(part + j * MN + c) + 1);
@@ -185,7 +188,7 @@ __global__ void __launch_bounds__(kReduceNormThreads)
     const float4 rb = __ldcg(reinterpret_cast<const float4*>(res32 + c) + 1);
     float4 a = q[0][0], b = q[0][1];
 #pragma unroll
-    for (int j = 1; j < kReduceNormMaxS; ++j)
+    for (int j = 1; j < MAXS; ++j)
       if (j < S) {
         a.x += q[j][0].x; a.y += q[j][0].y; a.z += q[j][0].z; a.w += q[j][0].w;
         b.x += q[j][1].x; b.y += q[j][1].y; b.z += q[j][1].z; b.w += q[j][1].w;
@@ -263,8 +266,14 @@ cudaError_t launch_splitk_reduce_norm(const float* part, int S, const float* res
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = make_cfg(dim3(rows), dim3(threads), (size_t)(H / 8) * sizeof(float),
                                     s, true, attr);
-  return cudaLaunchKernelEx(&cfg, splitk_reduce_norm_kernel, part, S, res32, out16, g, rows, H,
-                            eps, y);
+  if (S <= 4)
+    return cudaLaunchKernelEx(&cfg, splitk_reduce_norm_kernel<4>, part, S, res32, out16, g, rows,
+                              H, eps, y);
+  if (S <= 8)
+    return cudaLaunchKernelEx(&cfg, splitk_reduce_norm_kernel<8>, part, S, res32, out16, g, rows,
+                              H, eps, y);
+  return cudaLaunchKernelEx(&cfg, splitk_reduce_norm_kernel<16>, part, S, res32, out16, g, rows,
+                            H, eps, y);
 }
 
 }  // namespace blk

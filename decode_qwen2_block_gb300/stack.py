@@ -15,7 +15,7 @@ import torch
 
 from . import (BLK_ERR_SHAPE, BLK_OK, BlkError, Block, BlkQWeights, BlkWeights,
                blk_decode_batch_stack, blk_decode_batch_stack_workspace_bytes, blk_decode_stack,
-               blk_decode_stack_q)
+               blk_decode_stack_q, blk_prefill_stack, blk_prefill_stack_workspace_bytes)
 
 
 class LayerStack:
@@ -35,7 +35,11 @@ class LayerStack:
                        torch.zeros((Hkv, max_ctx, D), dtype=torch.float16, device=device))
                       for _ in range(self.n_layers)]
         self.caches = caches
-        self.ws = torch.empty(self.block.workspace_bytes(max_T), dtype=torch.uint8, device=device)
+        # one workspace for every call: the one-layer calls, decode, and the
+        # prefill stack (which also keeps its activation buffers in it)
+        nbytes = max(self.block.workspace_bytes(max_T),
+                     blk_prefill_stack_workspace_bytes(self.block.handle, max_T))
+        self.ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
         self.max_T = max_T
         # ping-pong activations between layers
         self.bufs = [torch.empty((max_T, H), dtype=torch.float16, device=device) for _ in range(2)]
@@ -58,13 +62,31 @@ class LayerStack:
             raise BlkError(rc, "blk_decode_stack")
         return out
 
+    def prefill_step(self, x, pos, cache_len: int, out=None, stream=None):
+        """T new tokens through every layer in one library call
+        (blk_prefill_stack; prefill when cache_len is 0, else prefill_kv).
+        Returns the last layer's output."""
+        T = x.shape[0]
+        out = self.bufs[0][:T] if out is None else out
+        s = torch.cuda.current_stream() if stream is None else stream
+        rc = blk_prefill_stack(self.block.handle, self._w_arr, self.n_layers, self._kc_arr,
+                               self._vc_arr, x.data_ptr(), pos.data_ptr(), T, cache_len,
+                               out.data_ptr(), self.ws.data_ptr(), self.ws.numel(), s.cuda_stream)
+        if rc != BLK_OK:
+            raise BlkError(rc, "blk_prefill_stack")
+        return out
+
     def run(self, phase: str, x, pos, cache_len: int, layer_outputs=None, stream=None):
         """Runs `phase` over all layers; returns the last layer's output (a
         view of an internal buffer).  layer_outputs, if given, is a list that
-        receives a copy of each layer's input (for layer-local checks)."""
+        receives a copy of each layer's input (for layer-local checks); the
+        layers then run as one call each."""
         T = x.shape[0]
         if phase == "decode" and layer_outputs is None:
             return self.decode_step(x, pos, cache_len, stream=stream)
+        if layer_outputs is None:
+            return self.prefill_step(x, pos, 0 if phase == "prefill" else cache_len,
+                                     stream=stream)
         cur = x
         for l in range(self.n_layers):
             out = self.bufs[l % 2][:T]

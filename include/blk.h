@@ -185,6 +185,23 @@ int blk_prefill_kv(blk_handle h, const blk_weights* w, const void* x,
                    void* k_cache, void* v_cache, void* out, void* k_new,
                    void* v_new, void* ws, size_t ws_bytes, void* stream);
 
+/* A whole layer stack for T new tokens (prefill when cache_len = 0, else
+ * prefill_kv on cache_len history slots) in one call: layer l's output is
+ * layer l+1's input, w[l], k_caches[l], v_caches[l] are layer l's weights and
+ * caches (as for blk_prefill / blk_prefill_kv), x is the first layer's
+ * input and out the last layer's output (device fp16 [T, hidden]); no k_new
+ * / v_new (the caches hold them).  Rows pass between layers through two
+ * buffers at the end of ws, and each layer's last kernel also writes the next
+ * layer's RMSNorm 1, so the result equals one call per layer bit for bit
+ * with one launch fewer per layer.  Every layer's arguments are checked
+ * before anything is enqueued.  ws_bytes >=
+ * blk_prefill_stack_workspace_bytes(h, T).  Returns what blk_prefill_kv
+ * returns. */
+size_t blk_prefill_stack_workspace_bytes(blk_handle h, int64_t max_T);
+int blk_prefill_stack(blk_handle h, const blk_weights* w, int n_layers, void* const* k_caches,
+                      void* const* v_caches, const void* x, const int64_t* pos, int64_t T,
+                      int64_t cache_len, void* out, void* ws, size_t ws_bytes, void* stream);
+
 /* decode (§4.1): one token after cache_len slots; attends [0, cache_len].
  *   x [1, hidden], pos [1], out [1, hidden], k_new/v_new [1, n_kv_heads, D].
  * One launch of the persistent decode kernel (weight streaming, HBM-bound).

@@ -168,9 +168,44 @@ def test_prefill_kv_28_layer_stack_layer_local():
     final = st.run("prefill_kv", x, pos, L, layer_outputs=ins).clone()
     torch.cuda.synchronize()
     st.block.check()
+    # the benchmark's path, one blk_prefill_stack call, gives the same bits
+    caches2 = [(to_dev(k), to_dev(v)) for k, v in hc]
+    st2 = LayerStack(s, wl, C, T, caches=caches2, chain=True)
+    one = st2.run("prefill_kv", x, pos, L).clone()
+    torch.cuda.synchronize()
+    st2.block.check()
+    assert torch.equal(one.view(torch.int16), final.view(torch.int16))
+    for (k1, v1), (k2, v2) in zip(caches, caches2):
+        assert torch.equal(k1.view(torch.int16), k2.view(torch.int16))
+        assert torch.equal(v1.view(torch.int16), v2.view(torch.int16))
     outs_next = ins[1:] + [final]
     _layer_local(s, lambda l: synth.block_weights(s, layer=l, seed=0), hc, ins,
                  synth.positions(L, T), L, [0, 255, 511], outs_next, layers=[0, 27])
+
+
+@pytest.mark.parametrize("shape_name,n,T", [("TINY", 3, 40), ("QWEN2_1P5B", 3, 1024),
+                                            ("QWEN2_1P5B", 2, 2048)])
+def test_prefill_stack_equals_one_call_per_layer(shape_name, n, T):
+    """blk_prefill_stack = blk_prefill per layer, bit for bit (output and
+    caches), with the down projection's K split fused with the next layer's
+    RMSNorm 1 (1.5B at T = 1024: 3 splits) or not split at all (T = 2048;
+    the tiny shape's K is too short to split)."""
+    s = getattr(synth, shape_name)
+    wl = [weights_to_dev(synth.block_weights(s, layer=l, seed=4)) for l in range(n)]
+    x = to_dev(synth.hidden_input(s, T, seed=4))
+    pos = to_dev(synth.positions(0, T))
+    outs = []
+    for mode in ("per_layer", "stack"):
+        st = LayerStack(s, wl, T, T, chain=True)
+        o = st.run("prefill", x, pos, 0, layer_outputs=[] if mode == "per_layer" else None)
+        torch.cuda.synchronize()
+        st.block.check()
+        outs.append((o.clone(), [(k.clone(), v.clone()) for k, v in st.caches]))
+    (o1, c1), (o2, c2) = outs
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    for (k1, v1), (k2, v2) in zip(c1, c2):
+        assert torch.equal(k1.view(torch.int16), k2.view(torch.int16))
+        assert torch.equal(v1.view(torch.int16), v2.view(torch.int16))
 
 
 def test_gqa4096_prefill_then_64_decodes_layer_local():
