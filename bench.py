@@ -59,13 +59,17 @@ G4_PREFILL, G4_DECODES = 100, 256  # hidden-4096 leg: prefill tokens, decode ste
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from
 # one ncu capture of the kernel as it is built now; None when the kernel
-# changed after its last capture.
+# changed after its last capture.  The captures and their commands:
+# profiles/prefill_kernels_1p5b_T1024.md (the prefill GEMMs, attention and
+# split-K reduction), profiles/decode_persistent_1p5b_1layer_ctx4096.md
+# (decode) and profiles/lm_head_1p5b_vocab151936.md (model head).
 NCU_TRAFFIC = {
-    "gemm_gateup": 58234880 + 326144,
-    "gemm_down": 45917952 + 12288,
-    "gemm_qkv": 10026496 + 0,
+    "gemm_gateup": 58228736 + 79104,
+    "gemm_down": 45917952 + 15872,
+    "gemm_qkv": 10027008 + 0,
     "gemm_o": 11042560 + 0,
-    "attn_prefill": 4243712 + 0,
+    "attn_prefill": 4251392 + 0,
+    "splitk_reduce": 25171456 + 0,
     "lm_head": 466853632 + 206080,
     # one-layer capture scaled to the 28-layer step (traffic grows with the layers)
     ("decode_persistent", 4096): 28 * (101665280 + 4095488),
