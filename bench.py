@@ -89,10 +89,13 @@ def parse():
                     help="batch sizes of the batched decode table (ctx --decode-batch-ctx)")
     ap.add_argument("--decode-batch-ctx", type=int, default=1024)
     ap.add_argument("--only", choices=("prefill", "decode", "decode_batch", "prefill_kv",
-                                       "gqa4096", "decode_layer", "decode_quant"), default=None,
+                                       "gqa4096", "decode_layer", "decode_quant",
+                                       "decode_batch_layer"), default=None,
                     help="run one part (for profiling); the headline needs the prefill.  "
                          "decode_layer runs one 1.5B-shaped layer of decode at ctx "
-                         "--decode-ctx[0] (small enough for an ncu capture)")
+                         "--decode-ctx[0] (small enough for an ncu capture); "
+                         "decode_batch_layer one layer of batched decode at the largest "
+                         "--decode-batch, ctx --decode-batch-ctx")
     return ap.parse_args()
 
 
@@ -298,6 +301,7 @@ def bench_ours(args, ws, rank, local):
              "prefill_kv": ("prefill_kv tok/s (28 layers, 512 on 3584)", bench_prefill_kv_stack),
              "gqa4096": ("hidden-4096 32-layer prefill + decode", bench_gqa4096),
              "decode_layer": ("decode us/launch (1 layer)", bench_decode_layer),
+             "decode_batch_layer": ("batched decode us/call (1 layer)", bench_decode_batch_layer),
              "decode_quant": ("quantized decode us/step (28 layers)", bench_decode_quant)}
     if args.only in parts:
         clocks = ClockSampler(local)
@@ -886,11 +890,48 @@ def bench_decode_layer(args, s, dev, stream, peaks, ws):
             "workload": f"one 1.5B-shaped layer, decode at ctx {L}, L2 flushed before each call"}
 
 
+def bench_decode_batch_layer(args, s, dev, stream, peaks, ws):
+    """One 1.5B-shaped layer of batched decode (blk_decode_batch) for B =
+    the largest --decode-batch sequences at ctx --decode-batch-ctx: a small
+    case for ncu captures of the batched kernels (94 MB of weights, B x the
+    K/V slots)."""
+    import torch
+    import synth
+    K, W = args.steps, args.warmup
+    B = max(int(b) for b in args.decode_batch.split(",") if b)
+    L = args.decode_batch_ctx
+    C = L + W + K + 8
+    w = synth.block_weights(s, layer=0, seed=0)
+    wd = {k: torch.from_numpy(v).to(dev) for k, v in w.items()}
+    from decode_qwen2_block_gb300 import Block
+    block = Block(s, C)
+    wts = Block.weights(wd)
+    k, v = synth.kv_history(s, C, L, layer=0, seed=0)
+    kc = torch.from_numpy(k).to(dev).unsqueeze(0).repeat(B, 1, 1, 1).contiguous()
+    vc = torch.from_numpy(v).to(dev).unsqueeze(0).repeat(B, 1, 1, 1).contiguous()
+    x = torch.from_numpy(synth.hidden_input(s, B, seed=0, stream_offset=5)).to(dev)
+    out = torch.empty_like(x)
+    wsb = torch.empty(block.decode_batch_workspace_bytes(B), dtype=torch.uint8, device=dev)
+    lens = [torch.full((B,), L + i, dtype=torch.int64, device=dev) for i in range(W + K)]
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def step(i):
+        flush.zero_()
+        block.decode_batch(wts, x, lens[i], lens[i], L + W + K, kc, vc, out, wsb, stream=stream)
+
+    total, _ = timed(step, K, W, ws, stream)
+    block.check()
+    return {"B": B, "ctx": L, "us_per_call_incl_flush": total / K * 1e3,
+            "workload": f"one 1.5B-shaped layer, batched decode of {B} sequences at ctx {L}, "
+                        f"L2 flushed before each call"}
+
+
 def bench_prefill_kv_stack(args, s, dev, stream, peaks, ws):
     """prefill_kv through the 28-layer 1.5B stack: 512 new tokens at
     positions 3584..4095 on 3584 seeded history slots per layer (the
     TopOp paper's Listing 2 block with history K/V, per layer).  One call =
-    28 blk_prefill_kv launches chains.  GEMM flops are 1,341.6 GFLOP per
+    one blk_prefill_stack (each layer's last kernel also normalises the next
+    layer's input).  GEMM flops are 1,341.6 GFLOP per
     call and attention 338.3 GFLOP; their kernel times (events around each
     kernel, separate pass) are reported apart."""
     import torch
