@@ -538,9 +538,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Merges the partials of every block whose tiles were split over several
 // CTAs: O = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c, M = max_c m_c, as
 // an online merge in chunk order with explicit roundings (the same bits on
-// every run).  CTA = block (h, qb), thread = (row, 32 output columns).
+// every run).  CTA = (block (h, qb), 32 output columns), thread = row: the
+// D/32 column groups of a block are separate CTAs so that the merge spreads
+// over four times as many SMs.
 template <int D>
-__global__ void __launch_bounds__(kRows * D / 32)
+__global__ void __launch_bounds__(kRows)
     attn_merge_kernel(const __grid_constant__ PrefillAttnParams p) {
   const int h = blockIdx.x, qb = blockIdx.y;
   const int t0 = qb * kRows;
@@ -551,7 +553,7 @@ __global__ void __launch_bounds__(kRows * D / 32)
   if (nch <= 1) return;                      // written by the attention kernel
   griddep_wait();
   griddep_launch();
-  const int r = threadIdx.x & (kRows - 1), grp = threadIdx.x / kRows;
+  const int r = threadIdx.x, grp = blockIdx.z;
   const int q = r >> 5, lane = r & 31;
   float M = -INFINITY, lt = 0.f, acc[32];
 #pragma unroll
@@ -667,8 +669,8 @@ cudaError_t launch_prefill_attn(const PrefillAttnParams& p, cudaStream_t s, bool
 cudaError_t launch_attn_merge(const PrefillAttnParams& p, cudaStream_t s, bool pdl) {
   if (p.grid_chunks <= 1) return cudaSuccess;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.Hq, p.nqb);
-  cfg.blockDim = dim3(kRows * p.D / 32);
+  cfg.gridDim = dim3(p.Hq, p.nqb, p.D / 32);
+  cfg.blockDim = dim3(kRows);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
