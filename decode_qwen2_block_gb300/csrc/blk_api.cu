@@ -498,10 +498,12 @@ int run_decode_batch(blk_handle h, const blk_weights* w, const void* x, const in
     pa.v_new = static_cast<__half*>(v_new);
   }
   {
-    const int64_t kd[3] = {D, c.max_ctx, (int64_t)M * Hkv};
-    const int64_t ks[2] = {(int64_t)D * 2, c.max_ctx * D * 2};
-    const int kb[3] = {64, 64, 1};
-    if (make_tmap_3d(&pa.tm_k, k_cache, kd, ks, kb) || make_tmap_3d(&pa.tm_v, v_cache, kd, ks, kb))
+    // (64 columns, slot, D / 64 column halves, sequence x kv head): one copy
+    // moves a whole 64-slot tile, [D/64][64 slots][128 B]
+    const int64_t kd[4] = {64, c.max_ctx, D / 64, (int64_t)M * Hkv};
+    const int64_t ks[3] = {(int64_t)D * 2, 128, c.max_ctx * D * 2};
+    const int kb[4] = {64, 64, D / 64, 1};
+    if (make_tmap_4d(&pa.tm_k, k_cache, kd, ks, kb) || make_tmap_4d(&pa.tm_v, v_cache, kd, ks, kb))
       return BLK_ERR_CUDA;
   }
   pa.q16 = q16;

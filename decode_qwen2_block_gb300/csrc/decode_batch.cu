@@ -5,7 +5,8 @@
 //
 // Split-K flash decode: CTA = (split, kv head g, sequence b), 4 warps.  The
 // split's slots stream through a ring of 64-slot K/V tiles in shared memory
-// (128-bit cp.async copies, 128-byte XOR swizzle, zero fill past the range).
+// (one TMA tensor copy per K or V tile, 128-byte swizzle, zero fill past
+// max_ctx; rows past the split's end are masked).
 // Two forms: when the (sequence, kv head) pairs are at most one per SM, one
 // CTA per SM of 8 warps that use two tiles at a time, with three such pairs
 // in the ring (four tiles in flight); otherwise two CTAs per SM of 4 warps
@@ -61,14 +62,14 @@ __device__ __forceinline__ uint32_t tile_addr(uint32_t base, int r, int ch) {
   return base + (ch >> 3) * (kTileSlots * 128) + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
 }
 
-// One box (x, y, z) of a 3-D tensor map into shared memory; completion is
+// One box (0, y, 0, z) of a 4-D tensor map into shared memory; completion is
 // counted on `bar` as transaction bytes.
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                            int z, uint64_t* bar) {
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int y, int z,
+                                            uint64_t* bar) {
   asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(y), "r"(0), "r"(z), "r"(smem_u32(bar))
       : "memory");
 }
 
@@ -187,11 +188,8 @@ __global__ void __launch_bounds__(128 * kTPG)
     for (int jt = 0; jt < nt; ++jt) {
       const uint32_t kb = kv0 + ((gi % kGroups) * kTPG + jt) * 2 * Sm::kTile, vb = kb + Sm::kTile;
       const int y = (int)(j0 + (int64_t)(gi * kTPG + jt) * kTileSlots);
-#pragma unroll
-      for (int h = 0; h < D / 64; ++h) {
-        tma_load_3d(kb + h * (kTileSlots * 128), &p.tm_k, h * 64, y, zh, bar);
-        tma_load_3d(vb + h * (kTileSlots * 128), &p.tm_v, h * 64, y, zh, bar);
-      }
+      tma_load_4d(kb, &p.tm_k, y, zh, bar);   // the tile's D/64 halves in one copy each
+      tma_load_4d(vb, &p.tm_v, y, zh, bar);
     }
   };
   int issued = 0;   // thread 0: groups loaded so far

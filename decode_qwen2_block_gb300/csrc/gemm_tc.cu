@@ -912,6 +912,22 @@ int make_tmap_3d(CUtensorMap* map, const void* base, const int64_t* dims,
   return r == CUDA_SUCCESS ? 0 : -1;
 }
 
+int make_tmap_4d(CUtensorMap* map, const void* base, const int64_t* dims,
+                 const int64_t* strides, const int* box) {
+  const EncodeTiledFn encode = encode_tiled();
+  if (!encode) return -1;
+  cuuint64_t d[4] = {(cuuint64_t)dims[0], (cuuint64_t)dims[1], (cuuint64_t)dims[2],
+                     (cuuint64_t)dims[3]};
+  cuuint64_t st[3] = {(cuuint64_t)strides[0], (cuuint64_t)strides[1], (cuuint64_t)strides[2]};
+  cuuint32_t bx[4] = {(cuuint32_t)box[0], (cuuint32_t)box[1], (cuuint32_t)box[2],
+                      (cuuint32_t)box[3]};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void*>(base), d, st,
+                            bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : -1;
+}
+
 int make_tmap_rows8(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int cbs,
                     int* is3d) {
   const EncodeTiledFn encode = encode_tiled();

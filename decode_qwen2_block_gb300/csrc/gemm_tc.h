@@ -68,6 +68,9 @@ int make_tmap_2d(CUtensorMap* map, const void* base, int64_t rows, int64_t K,
 // first, strides (bytes) of dims 1 and 2, box sizes.  Returns 0 on success.
 int make_tmap_3d(CUtensorMap* map, const void* base, const int64_t* dims,
                  const int64_t* strides, const int* box);
+// The same with four dims (strides of dims 1..3 in bytes).
+int make_tmap_4d(CUtensorMap* map, const void* base, const int64_t* dims,
+                 const int64_t* strides, const int* box);
 // Tensor map of 8-row weight boxes with 128-byte swizzle for the decode
 // kernel: the 3-D view (64, rows, K / 64) with box (64, 8, cbs) when
 // K % 64 == 0 (*is3d = 1), else the 2-D view (K, rows) with box (64, 8).

@@ -58,8 +58,9 @@ cudaError_t configure_prefill_attn();
 // row each, caches [B][Hkv][max_ctx][D], slots [0, cache_lens[b]] (the last
 // one already holding the new K/V).
 struct DecodeAttnBatchParams {
-  CUtensorMap tm_k;           // K cache viewed as (D, max_ctx, B * Hkv), box 64 x 64 x 1,
-  CUtensorMap tm_v;           //   SW128; the same for V (slots past max_ctx read as zeros)
+  CUtensorMap tm_k;           // K cache viewed as (64, max_ctx, D / 64, B * Hkv), box
+  CUtensorMap tm_v;           //   64 x 64 x D/64 x 1, SW128; the same for V (slots past
+                              //   max_ctx read as zeros)
   const __half* q16;          // [B, Hq, D] (RoPE applied)
   const int64_t* cache_lens;  // [B], device
   int B, Hq, Hkv, D;
