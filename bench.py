@@ -56,6 +56,7 @@ PREFILL_T = 1024
 ORACLE_SAMPLE_ROWS = 32     # full-output rows of the oracle's prefill sample
 PKV_HIST, PKV_T = 3584, 512        # prefill_kv leg: history slots, new tokens
 G4_PREFILL, G4_DECODES = 100, 256  # hidden-4096 leg: prefill tokens, decode steps
+DECODE_STEPS = 128                 # consecutive decode steps timed per context length
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from
 # one ncu capture of the kernel as it is built now; None when the kernel
@@ -698,10 +699,12 @@ def kernel_table(block, run, stream, reps=2):
 
 
 def bench_decode(args, s, dev, stream, peaks, ws):
+    """The 28-layer decode at each context length: DECODE_STEPS (or --steps,
+    if more) consecutive steps timed, each appending its K/V in place."""
     import torch
     import synth
     from decode_qwen2_block_gb300.stack import LayerStack
-    K, W = args.steps, args.warmup
+    K, W = max(args.steps, DECODE_STEPS), args.warmup
     ctxs = [int(c) for c in args.decode_ctx.split(",") if c]
     n = s.n_layers
     C = max(ctxs) + W + K + 8
@@ -767,7 +770,9 @@ def bench_decode(args, s, dev, stream, peaks, ws):
     out["kernels"] = {k: {"avg_us": 1e3 * ms / cnt, "share": ms / tot}
                       for k, (ms, cnt) in table.items()}
     out["launches_per_step"] = sum(c for _, c in table.values())
-    out["workload"] = "qwen2-1.5B-shaped 28-layer stack, batch-1 decode, one CUDA graph per step"
+    out["steps_per_ctx"] = K
+    out["workload"] = (f"qwen2-1.5B-shaped 28-layer stack, batch-1 decode, {K} consecutive "
+                       f"steps per context length (KV appended in place), one CUDA graph per step")
     return out
 
 
