@@ -356,21 +356,29 @@ def bench_ours(args, ws, rank, local):
     step_ms = [a.elapsed_time(b) for a, b in evs]
     total_ms = reduce_max(sum(step_ms), ws)
 
-    # e2e: host (pinned) inputs -> device -> block -> host outputs, every step
-    x_h = torch.from_numpy(x_np).pin_memory()
-    pos_h = torch.from_numpy(synth.positions(0, T)).pin_memory()
-    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    kn_h = torch.empty(kn.shape, dtype=kn.dtype).pin_memory()
-    vn_h = torch.empty(vn.shape, dtype=vn.dtype).pin_memory()
-    x_e, pos_e = torch.empty_like(x), torch.empty_like(pos)
+    # e2e: host (pinned) inputs -> device -> block -> host outputs, every
+    # step.  The step's inputs (x, then position_ids) sit back to back in one
+    # pinned buffer and one device buffer, and its results (out, k_new,
+    # v_new) likewise, so a step is one host->device copy, the call, and one
+    # device->host copy.
+    nx, npos = T * s.hidden * 2, T * 8
+    nout, nkv = T * s.hidden * 2, T * s.n_kv_heads * s.head_dim * 2
+    in_h = torch.empty(nx + npos, dtype=torch.uint8).pin_memory()
+    in_h[:nx].copy_(torch.from_numpy(x_np).view(torch.uint8).reshape(-1))
+    in_h[nx:].copy_(torch.from_numpy(synth.positions(0, T)).view(torch.uint8).reshape(-1))
+    res_h = torch.empty(nout + 2 * nkv, dtype=torch.uint8).pin_memory()
+    in_d = torch.empty(nx + npos, dtype=torch.uint8, device=dev)
+    res_d = torch.empty(nout + 2 * nkv, dtype=torch.uint8, device=dev)
+    x_e = in_d[:nx].view(torch.float16).view(T, s.hidden)
+    pos_e = in_d[nx:].view(torch.int64)
+    out_e = res_d[:nout].view(torch.float16).view(T, s.hidden)
+    kn_e = res_d[nout:nout + nkv].view(torch.float16).view(kn.shape)
+    vn_e = res_d[nout + nkv:].view(torch.float16).view(vn.shape)
 
     def e2e_step():
-        x_e.copy_(x_h, non_blocking=True)
-        pos_e.copy_(pos_h, non_blocking=True)
-        block.prefill(wts, x_e, pos_e, kc, vc, out, wsb, kn, vn, stream=stream)
-        out_h.copy_(out, non_blocking=True)
-        kn_h.copy_(kn, non_blocking=True)
-        vn_h.copy_(vn, non_blocking=True)
+        in_d.copy_(in_h, non_blocking=True)
+        block.prefill(wts, x_e, pos_e, kc, vc, out_e, wsb, kn_e, vn_e, stream=stream)
+        res_h.copy_(res_d, non_blocking=True)
 
     for _ in range(W):
         flush.zero_()
@@ -387,8 +395,8 @@ def bench_ours(args, ws, rank, local):
     torch.cuda.synchronize()
     barrier(ws)
     e2e_ms = reduce_max(sum(a.elapsed_time(b) for a, b in e2e_evs), ws)
-    h2d = x_h.numel() * 2 + pos_h.numel() * 8
-    d2h = (out_h.numel() + kn_h.numel() + vn_h.numel()) * 2
+    h2d = in_h.numel()
+    d2h = res_h.numel()
 
     # per-kernel durations (events around each kernel; separate pass)
     block.timing(True)
@@ -737,17 +745,23 @@ def bench_decode(args, s, dev, stream, peaks, ws):
     # end to end at the first context through the public API, eager: the
     # step's hidden row and position go host (pinned) -> device, the 28-layer
     # step runs (blk_decode_stack), the output row comes back to the host
+    # (the hidden row and the position in one pinned buffer: one copy in)
     L = ctxs[0]
-    x_h = [torch.from_numpy(a).pin_memory() for a in xs_np]
-    pos_h = [torch.tensor([L + i], dtype=torch.int64).pin_memory() for i in range(W + K)]
-    x_d = torch.empty((1, s.hidden), dtype=torch.float16, device=dev)
-    pos_d = torch.empty(1, dtype=torch.int64, device=dev)
+    nx = s.hidden * 2
+    in_h = []
+    for i in range(W + K):
+        b = torch.empty(nx + 8, dtype=torch.uint8).pin_memory()
+        b[:nx].copy_(torch.from_numpy(xs_np[i]).view(torch.uint8).reshape(-1))
+        b[nx:].copy_(torch.tensor([L + i], dtype=torch.int64).view(torch.uint8))
+        in_h.append(b)
+    in_d = torch.empty(nx + 8, dtype=torch.uint8, device=dev)
+    x_d = in_d[:nx].view(torch.float16).view(1, s.hidden)
+    pos_d = in_d[nx:].view(torch.int64)
     out_d = torch.empty((1, s.hidden), dtype=torch.float16, device=dev)
     out_h = torch.empty((1, s.hidden), dtype=torch.float16).pin_memory()
 
     def e2e(i):
-        x_d.copy_(x_h[i], non_blocking=True)
-        pos_d.copy_(pos_h[i], non_blocking=True)
+        in_d.copy_(in_h[i], non_blocking=True)
         st.decode_step(x_d, pos_d, L + i, out=out_d, stream=stream)
         out_h.copy_(out_d, non_blocking=True)
 
@@ -755,7 +769,7 @@ def bench_decode(args, s, dev, stream, peaks, ws):
     st.block.check()
     ms = total / K
     out["e2e"] = {"ctx": L, "value": ws * 1e3 / ms, "unit": "tok/s", "us_per_step": ms * 1e3,
-                  "h2d_bytes_per_step": x_h[0].numel() * 2 + 8,
+                  "h2d_bytes_per_step": in_h[0].numel(),
                   "d2h_bytes_per_step": out_h.numel() * 2,
                   "path": "blk_decode_stack through LayerStack.decode_step, eager (no graph)"}
     # the whole model per generated token at the first context: embedding +
