@@ -7,6 +7,7 @@ import numpy as np
 import pytest
 import torch
 
+import decode_qwen2_block_gb300 as blk
 import oracle
 import synth
 from decode_qwen2_block_gb300.stack import LayerStack
@@ -266,3 +267,33 @@ def test_gqa4096_prefill_then_64_decodes_layer_local():
             if i in full_steps:
                 got = step_ins[i][l + 1] if l + 1 < n else step_outs[i]
                 assert_close(got, o_ref, f"step {i} out layer {l}")
+
+
+def test_prefill_stack_checks_every_layer_before_enqueueing():
+    """A bad argument of the last layer is reported before any layer runs:
+    every cache stays as it was; a workspace too small is refused, and the
+    stack's workspace size covers the one-layer calls' plus two activation
+    buffers."""
+    s, n, T, C = synth.TINY, 3, 8, 32
+    wl = [weights_to_dev(synth.block_weights(s, layer=l, seed=6)) for l in range(n)]
+    st = LayerStack(s, wl, C, T, chain=True)
+    for kc, vc in st.caches:
+        kc.fill_(1.5)
+        vc.fill_(-2.0)
+    st._w_arr[2].w_down = None                   # the last layer is bad
+    x = to_dev(synth.hidden_input(s, T, seed=6))
+    pos = to_dev(synth.positions(0, T))
+    with pytest.raises(blk.BlkError) as e:
+        st.prefill_step(x, pos, 0)
+    assert e.value.status == blk.BLK_ERR_NULL
+    torch.cuda.synchronize()
+    for kc, vc in st.caches:                     # nothing ran
+        assert bool((kc == 1.5).all()) and bool((vc == -2.0).all())
+    st._w_arr[2].w_down = st._w_arr[1].w_down
+    one = blk.blk_prefill_stack_workspace_bytes(st.block.handle, T)
+    assert one > blk.blk_workspace_bytes(st.block.handle, T)
+    out = torch.empty((T, s.hidden), dtype=torch.float16, device="cuda")
+    rc = blk.blk_prefill_stack(st.block.handle, st._w_arr, n, st._kc_arr, st._vc_arr,
+                               x.data_ptr(), pos.data_ptr(), T, 0, out.data_ptr(),
+                               st.ws.data_ptr(), 1024, None)
+    assert rc == blk.BLK_ERR_WORKSPACE
