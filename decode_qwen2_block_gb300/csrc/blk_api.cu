@@ -11,6 +11,7 @@
 #include "common.cuh"
 #include "blk_internal.h"
 #include "decode_persistent.h"
+#include "gemm_fr.h"
 #include "gemm_tc.h"
 #include "kernels.h"
 
@@ -219,15 +220,62 @@ struct Timer {
     if (e_ != cudaSuccess) return BLK_ERR_CUDA; \
   } while (0)
 
+// The same tail for a decode batch of M <= kFrMaxRows rows on the few-row
+// projections (gemm_fr.cu): o_proj and down write K-split partials that the
+// RMSNorm 2 and the down reduction add up, gate|up applies SwiGLU itself.
+int run_block_tail_few(blk_handle h, const blk_weights* w, const void* x, __half* attn16,
+                       float* h32, __half* hn16, __half* act16, float* part32, int max_splits,
+                       void* out, int M, cudaStream_t s, Timer& tm, const __half* next_g,
+                       __half* next_xn16) {
+  const blk_config& c = h->cfg;
+  const int H = c.hidden, D = c.head_dim, Hq = c.n_heads, I = c.intermediate;
+  FrGemmParams fo = {};
+  fo.x = attn16; fo.w[0] = w->wo; fo.seg_rows[0] = H;
+  fo.M = M; fo.N = H; fo.K = Hq * D;
+  fo.max_splits = max_splits < kMaxSplitsNorm ? max_splits : kMaxSplitsNorm;
+  fo.part = part32; fo.err = h->status;
+  BLK_LAUNCH(tm, kKGemmO, launch_fr_gemm(fo, kFrPart, h->num_sms, s, true));
+  BLK_LAUNCH(tm, kKRmsNorm,
+             launch_rmsnorm_splitk(part32, fo.splits, static_cast<const __half*>(x), h32,
+                                   static_cast<const __half*>(w->ln2_g), M, H, c.rms_eps, hn16,
+                                   s, true));
+  FrGemmParams fg = {};
+  fg.x = hn16; fg.w[0] = w->w_gate; fg.w[1] = w->w_up;
+  fg.M = M; fg.N = I; fg.K = H;
+  fg.out16 = act16; fg.ldo = I; fg.err = h->status;
+  BLK_LAUNCH(tm, kKGemmGateUp, launch_fr_gemm(fg, kFrGateUp, h->num_sms, s, true));
+  FrGemmParams fd = {};
+  fd.x = act16; fd.w[0] = w->w_down; fd.seg_rows[0] = H;
+  fd.M = M; fd.N = H; fd.K = I;
+  fd.max_splits = max_splits;
+  fd.part = part32; fd.err = h->status;
+  BLK_LAUNCH(tm, kKGemmDown, launch_fr_gemm(fd, kFrPart, h->num_sms, s, true));
+  if (next_g) {
+    BLK_LAUNCH(tm, kKReduceNorm,
+               launch_splitk_reduce_norm(part32, fd.splits, h32, static_cast<__half*>(out),
+                                         next_g, M, H, c.rms_eps, next_xn16, s));
+  } else {
+    TcGemmParams r = {};
+    r.part = part32; r.splits = fd.splits; r.M = M; r.N = H;
+    r.res32 = h32; r.out16 = static_cast<__half*>(out);
+    BLK_LAUNCH(tm, kKSplitReduce, launch_splitk_reduce(r, h->num_sms, s));
+  }
+  return BLK_OK;
+}
+
 // o_proj + residual, RMSNorm 2, gate|up + SwiGLU, down + residual for M rows
 // (shared by prefill, prefill_kv and batched decode).  With next_g set (a
 // layer stack), the next layer's RMSNorm 1 of out (gain next_g) is also
 // written to next_xn16, fused with the down split-K reduction when there is
-// one.
+// one.  few_rows (batched decode) takes the few-row projections when M is
+// small enough for them.
 int run_block_tail(blk_handle h, const blk_weights* w, const void* x, __half* attn16,
                    float* h32, __half* hn16, __half* act16, float* part32, int max_splits,
-                   bool split_o, void* out, int M, cudaStream_t s, Timer& tm,
+                   bool split_o, bool few_rows, void* out, int M, cudaStream_t s, Timer& tm,
                    const __half* next_g = nullptr, __half* next_xn16 = nullptr) {
+  if (few_rows && M <= kFrMaxRows)
+    return run_block_tail_few(h, w, x, attn16, h32, hn16, act16, part32, max_splits, out, M, s,
+                              tm, next_g, next_xn16);
   const blk_config& c = h->cfg;
   const int H = c.hidden, D = c.head_dim, Hq = c.n_heads, I = c.intermediate;
   // o_proj + residual -> h (fp32)
@@ -375,8 +423,8 @@ int run_prefill(blk_handle h, const blk_weights* w, const void* x,
   // o_proj splits K the same way when its tiles are few; the RMSNorm that
   // follows it adds the partials and the residual
   return run_block_tail(h, w, x, attn16, h32, hn16, act16,
-                        reinterpret_cast<float*>(base + lay.part32), kMaxSplits, true, out, M,
-                        s, tm, next_ln1, xn16);
+                        reinterpret_cast<float*>(base + lay.part32), kMaxSplits, true, false,
+                        out, M, s, tm, next_ln1, xn16);
 }
 
 // Batched decode: B sequences, one new token each, caches [B][Hkv][max_ctx][D].
@@ -452,7 +500,11 @@ int run_decode_batch(blk_handle h, const blk_weights* w, const void* x, const in
                launch_rmsnorm_rows(x, false, static_cast<const __half*>(w->ln1_g), M, H,
                                    c.rms_eps, xn16, s, first_pdl));
 
-  // QKV + bias + RoPE at pos[b]; K/V to slot cache_lens[b] of sequence b's cache
+  // QKV + bias + RoPE at pos[b]; K/V to slot cache_lens[b] of sequence b's cache.
+  // Up to kFrMaxRows sequences: the few-row projection writes at most 4 K-split
+  // partials, which the attention kernel adds up and finishes.
+  const bool few = M <= kFrMaxRows;
+  FrGemmParams fq = {};
   TcGemmParams g = {};
   if (make_tmap_2d(&g.tmA, xn16, M, H, tc_a_box_rows(M)) ||
       make_tmap_2d(&g.tmB[0], w->wq, (int64_t)Hq * D, H, 64) ||
@@ -479,15 +531,25 @@ int run_decode_batch(blk_handle h, const blk_weights* w, const void* x, const in
   g.part = reinterpret_cast<float*>(base + lay.part32);   // K splits fill the SM pairs;
   g.max_splits = kMaxSplitsBatch;   // the attention kernel (or qkv_finish) applies the epilogue
   g.err = h->status;
-  BLK_LAUNCH(tm, kKGemmQKV, launch_tc_gemm(g, kTcQKV, h->num_sms, s, true));
+  if (few) {
+    fq.x = xn16; fq.w[0] = w->wq; fq.w[1] = w->wk; fq.w[2] = w->wv;
+    for (int i = 0; i < 3; ++i) fq.seg_rows[i] = g.seg_rows[i];
+    fq.M = M; fq.N = g.N; fq.K = H;
+    fq.max_splits = 4;
+    fq.part = g.part; fq.err = h->status;
+    BLK_LAUNCH(tm, kKGemmQKV, launch_fr_gemm(fq, kFrPart, h->num_sms, s, true));
+  } else {
+    BLK_LAUNCH(tm, kKGemmQKV, launch_tc_gemm(g, kTcQKV, h->num_sms, s, true));
+  }
 
   // attention of every sequence over its own slots [0, cache_lens[b]]; a
   // K-split QKV projection is finished inside it (bias, RoPE, new K/V)
   DecodeAttnBatchParams pa = {};
-  if (g.splits > 4) BLK_LAUNCH(tm, kKQkvFinish, launch_qkv_finish(g, s));
-  else if (g.splits > 1) {
+  const int qkv_splits = few ? fq.splits : g.splits;
+  if (!few && g.splits > 4) BLK_LAUNCH(tm, kKQkvFinish, launch_qkv_finish(g, s));
+  else if (few || g.splits > 1) {
     pa.qkv_part = g.part;
-    pa.qkv_splits = g.splits;
+    pa.qkv_splits = qkv_splits;
     for (int i = 0; i < 3; ++i) pa.bias[i] = g.bias[i];
     pa.pos = pos;
     pa.rope = h->rope;
@@ -525,8 +587,8 @@ int run_decode_batch(blk_handle h, const blk_weights* w, const void* x, const in
   return run_block_tail(h, w, x, attn16, reinterpret_cast<float*>(base + lay.h32),
                         reinterpret_cast<__half*>(base + lay.hn16),
                         reinterpret_cast<__half*>(base + lay.act16),
-                        reinterpret_cast<float*>(base + lay.part32), kMaxSplitsBatch, true, out,
-                        M, s, tm, next_ln1, xn16);
+                        reinterpret_cast<float*>(base + lay.part32), kMaxSplitsBatch, true, true,
+                        out, M, s, tm, next_ln1, xn16);
 }
 
 }  // namespace
@@ -1246,6 +1308,7 @@ namespace blk {
 cudaError_t configure_kernels() {
   cudaError_t e = configure_decode_persistent();
   if (e == cudaSuccess) e = configure_tc_gemm_kernels();
+  if (e == cudaSuccess) e = configure_fr_gemm_kernels();
   if (e == cudaSuccess) e = configure_prefill_attn();
   if (e == cudaSuccess) e = configure_lm_head();
   if (e == cudaSuccess) e = configure_decode_attn_batch();

@@ -178,9 +178,14 @@ def _stack_inputs(s, n_layers, B, C, seed):
 
 
 @pytest.mark.parametrize("shape_name,n,B,C,fused", [
-    ("TINY", 3, 5, 64, False),          # down K too short to split: plain RMSNorm
-    ("QWEN2_1P5B", 2, 3, 64, True),     # down split K: reduction fused with RMSNorm 1
+    # up to 128 sequences the few-row projections always split the down K:
+    # its reduction is fused with the next layer's RMSNorm 1
+    ("TINY", 3, 5, 64, True),
+    ("QWEN2_1P5B", 2, 3, 64, True),
     ("QWEN2_1P5B", 3, 64, 704, True),   # the bench's batch size
+    # 130 sequences take the 2-SM GEMMs, whose tiny down K is too short to
+    # split: the next layer's RMSNorm 1 runs as its own kernel
+    ("TINY", 2, 130, 1440, False),
 ])
 def test_batch_stack_equals_one_call_per_layer(shape_name, n, B, C, fused):
     """blk_decode_batch_stack = blk_decode_batch per layer, bit for bit
