@@ -86,7 +86,8 @@ def test_tiny_batch_past_one_row_tile():
 def test_nan_in_unused_slots_is_never_read(B):
     """Every slot past a sequence's length holds NaN: slots past the end of a
     split share a tile with real ones, and none of them may reach the output
-    (3 sequences: one CTA per SM; 80 x 2 kv heads: two CTAs per SM)."""
+    (3 sequences: one CTA per SM; 80 x 2 kv heads: two CTAs per SM, and
+    the few-row projections with their 128-row activation box)."""
     s = synth.TINY
     w = synth.block_weights(s, seed=14)
     rng = np.random.default_rng(14)
@@ -96,8 +97,8 @@ def test_nan_in_unused_slots_is_never_read(B):
 
 def test_1p5b_bench_launch_configuration():
     """The batched bench's configuration: 64 sequences near ctx 1024 (two
-    attention splits, QKV and o_proj split 3 ways, down 12 ways); the oracle
-    checks three sequences, the cache placement all 64."""
+    attention splits; the few-row projections split QKV 4 ways, o_proj 8 and
+    down 12); the oracle checks three sequences, the cache placement all 64."""
     s = synth.QWEN2_1P5B
     w = synth.block_weights(s, seed=13)
     lens = [1024 - (b % 7) for b in range(64)]
