@@ -9,7 +9,9 @@
 // range.  Y^T = W X^T sits in TMEM with one lane per weight row and one
 // column per activation row.
 //
-// One CTA per (128-row weight tile, K split), a single wave, 6 warps:
+// One CTA per (128-row weight tile, K split), 6 warps; the launcher splits K
+// only as far as the units still fit one wave (every projection of the 1.5B
+// shape runs in one; gate/up of a 11008-wide MLP has 172 tiles, two waves):
 //   warp 0   TMA producer: per 64-column K block, the tile's two 64-row
 //            weight boxes and X's box (npad rows; rows past M arrive as
 //            zeros) into a ring of 6 stages, 128-byte swizzle.  The weight
