@@ -321,8 +321,10 @@ int blk_set_trace(blk_handle h, void* device_buffer, size_t bytes);
  *   out      device fp16 [B, hidden]; k_new, v_new  [B, n_kv_heads, head_dim]
  *            or NULL
  * Equals blk_decode on each sequence within the tolerance (the projections
- * run on the tcgen05 GEMMs with B rows and K split across the SM pairs; the
- * attention is a split-K flash decode per sequence).  A cache length outside
+ * run on tcgen05 MMAs with K split: up to 128 sequences with the weight rows
+ * as the MMA's M side, one CTA per 128-row tile and split; more sequences on
+ * the 2-SM GEMMs with B rows; the attention is a split-K flash decode per
+ * sequence).  A cache length outside
  * [0, max_ctx) skips that sequence's K/V write and attention, and reports
  * BLK_ERR_POSITION from the next blk_check.  Returns BLK_OK, BLK_ERR_NULL,
  * BLK_ERR_ALIGN, BLK_ERR_SHAPE (B outside [1, 4096], more than 16 query heads
