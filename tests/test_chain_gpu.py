@@ -217,7 +217,8 @@ def test_gqa4096_prefill_then_64_decodes_layer_local():
     step-local against the oracle: every step's K/V slot of every layer
     (the oracle given that layer's input and the GPU's cache before the
     step), and the full output of every layer at the prefill (sampled rows)
-    and at four of the decode steps, within the benchmark spec tolerance."""
+    and at four of the decode steps, within the parity tolerance (relative L2
+    <= 1e-2, max abs <= 5e-2 per tensor)."""
     s, n, T, ND = synth.GQA_4096, 4, 100, 64
     C = T + ND + 8
     w_np = [synth.block_weights(s, layer=l, seed=2) for l in range(n)]

@@ -7,7 +7,7 @@ The TpuOp dialect of the MLIR-compilation paper (§2.2) carries INT8 and
 W4A16 weights with scales and zero points.  Each step is checked layer- and
 call-local: the oracle gets the GPU's cache as it was before the call, so
 the comparison does not accumulate drift.  Tolerance: relative L2 <= 1e-2
-and max abs <= 5e-2 per tensor (out, k_new, v_new), the north_star bound;
+and max abs <= 5e-2 per tensor (out, k_new, v_new), the bound of every parity test;
 the kernels round each weight once to fp16 (scale * (code - zero)), which
 that bound covers."""
 import numpy as np

@@ -4,7 +4,7 @@ attends slots [max(0, p - W + 1), p] (the reading of the "swa" layer
 forward that the ds4.c study notes name without a window).  Slots before a
 query's window hold NaN in the cache where the case allows it, so a read of
 one would reach the output.  Tolerance: relative L2 <= 1e-2 and max abs
-<= 5e-2 per tensor, the benchmark spec bound."""
+<= 5e-2 per tensor, the bound of every parity test."""
 import numpy as np
 import pytest
 import torch

@@ -4,7 +4,7 @@ parameters, in every phase and in batched decode.  The ds4.c study notes
 dimension; the blend and the magnitude are the readings in include/blk.h,
 which the oracle follows too.  Positions run past the original context, the
 case YaRN exists for.  Tolerance: relative L2 <= 1e-2 and max abs <= 5e-2
-per tensor, the benchmark spec bound."""
+per tensor, the bound of every parity test."""
 import numpy as np
 import pytest
 import torch
